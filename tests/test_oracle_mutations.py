@@ -1,0 +1,167 @@
+"""Planted mistakes: each plausible error in the oracle must make a pin fail.
+
+A mutation is one textual change to the oracle's source (a dropped term, a
+flipped sign, a wrong index, a transposed operand).  The mutated copy is built
+in a temporary place (never in the tree) and the pins are re-run on it; the test
+passes when at least one pin rejects the mutant.  This shows that the pins in
+test_oracle_pins.py would catch such a mistake in the real oracle.
+"""
+import json
+import os
+import subprocess
+import types
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from chunked_gated_delta_prepare_gb300.inputs import make_inputs
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+CHUNKED_SRC = os.path.join(ROOT, "oracle", "chunked.py")
+NAIVE_SRC = os.path.join(ROOT, "oracle", "naive_recurrence.c")
+GOLDEN = os.path.join(ROOT, "tests", "golden", "worked_examples.json")
+
+
+def _inputs(per_k, K=6, V=6, T=64, seed=21):
+    x = make_inputs(1, T, 2, K, V, per_k_gate=per_k, io_dtype=torch.float32, with_h0=True, seed=seed)
+    d = {n: t.double().numpy() for n, t in x.tensors().items()}
+    d["h0"] = d["h0"] * 20
+    return d
+
+
+def _golden_cases():
+    with open(GOLDEN) as f:
+        for ex in json.load(f)["examples"]:
+            T, K, V = ex["T"], ex["K"], ex["V"]
+            gf = np.log(np.array(ex["g_decay_factor"]))
+            yield (dict(q=np.array(ex["q"]).reshape(1, T, 1, K), k=np.array(ex["k"]).reshape(1, T, 1, K),
+                        v=np.array(ex["v"]).reshape(1, T, 1, V),
+                        g=gf.reshape(1, T, 1, K) if ex["gate"] == "per_key_dim" else gf.reshape(1, T, 1),
+                        beta=np.array(ex["beta"]).reshape(1, T, 1), h0=np.array(ex["h0"]).reshape(1, 1, K, V)),
+                   ex["scale"], np.array(ex["o"]).reshape(1, T, 1, V), np.array(ex["h_final"]).reshape(1, 1, K, V))
+
+
+# ------------------------------------------------------------ chunked (numpy) mutants
+
+CHUNKED_MUTANTS = [
+    ("k_beta without exp(G), as the prepare page's fragment writes it",
+     "k_beta_g = kc * bc * np.exp(Gc)", "k_beta_g = kc * bc"),
+    ("gate sign flipped inside A",
+     "gate = np.exp(Gc[..., i:i + 1, :] - Gc[..., :i, :])", "gate = np.exp(Gc[..., :i, :] - Gc[..., i:i + 1, :])"),
+    ("beta taken from the column instead of the row",
+     "A[..., i, :i] = bc[..., i:i + 1] *", "A[..., i, :i] = bc[..., :i] *"),
+    ("A transposed in the substitution",
+     "A[..., i, :i], X[..., :i, :]", "A[..., :i, i], X[..., :i, :]"),
+    ("identity dropped from the inverse", "row[..., i] = 1.0", "row[..., i] = 0.0"),
+    ("v' sign flipped", "vp = uc[:, c] - wc[:, c] @ h", "vp = uc[:, c] + wc[:, c] @ h"),
+    ("state not decayed across chunks",
+     "h = np.exp(G_last)[..., None] * h + ", "h = h + "),
+    ("kg gate inverted",
+     "np.exp(G_last[:, :, None, :] - Gc[:, c])", "np.exp(Gc[:, c] - G_last[:, :, None, :])"),
+    ("checkpoint taken after the update",
+     "        ckpt[:, c] = h\n        vp = uc[:, c] - wc[:, c] @ h",
+     "        vp = uc[:, c] - wc[:, c] @ h"),
+    ("gate cumsum not restarted per chunk",
+     "return np.cumsum(gc, axis=2).reshape(g.shape)", "return np.cumsum(g, axis=1)"),
+    ("output diagonal excluded",
+     "Qt[..., i, :i + 1] = np.einsum(\"...d,...jd->...j\", qc[..., i, :], kc[..., :i + 1, :] * gate)",
+     "Qt[..., i, :i] = np.einsum(\"...d,...jd->...j\", qc[..., i, :], kc[..., :i, :] * gate[..., :i, :])"),
+    ("scale on the inter-chunk term only",
+     "scale * (inter + intra)", "scale * inter + intra"),
+    ("query not gated in the inter-chunk term",
+     "inter = (qc * np.exp(Gc)) @ ckpt", "inter = qc @ ckpt"),
+    ("checkpoint transposed in the output",
+     "inter = (qc * np.exp(Gc)) @ ckpt", "inter = (qc * np.exp(Gc)) @ np.swapaxes(ckpt, -1, -2)"),
+]
+
+
+def _chunked_pins_fail(mod) -> bool:
+    """True when some pin rejects this version of the chunked oracle."""
+    for per_k in (False, True):
+        d = _inputs(per_k)
+        try:
+            ref = oracle.naive_forward(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], 16, 0.5)
+            got = mod.forward_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], 16, 0.5)
+        except Exception:
+            return True
+        for key in ("o", "h_final", "ckpt"):
+            if np.abs(got[key] - ref[key]).max() > 1e-10:
+                return True
+    for args, scale, o_ref, h_ref in _golden_cases():
+        got = mod.forward_chunked(args["q"], args["k"], args["v"], args["g"], args["beta"], args["h0"], 2, scale)
+        if np.abs(got["o"] - o_ref).max() > 1e-12 or np.abs(got["h_final"] - h_ref).max() > 1e-12:
+            return True
+    return False
+
+
+def _load_chunked(src: str):
+    mod = types.ModuleType("chunked_mutant")
+    exec(compile(src, "chunked_mutant.py", "exec"), mod.__dict__)
+    return mod
+
+
+def test_unmutated_chunked_passes_the_pins():
+    with open(CHUNKED_SRC) as f:
+        assert not _chunked_pins_fail(_load_chunked(f.read()))
+
+
+@pytest.mark.parametrize("what,old,new", CHUNKED_MUTANTS, ids=[m[0] for m in CHUNKED_MUTANTS])
+def test_chunked_mutant_is_caught(what, old, new):
+    with open(CHUNKED_SRC) as f:
+        src = f.read()
+    assert src.count(old) == 1, f"mutation site not found: {old!r}"
+    assert _chunked_pins_fail(_load_chunked(src.replace(old, new)))
+
+
+# ------------------------------------------------------------ naive (C) mutants
+
+NAIVE_MUTANTS = [
+    ("delta sign flipped", "r[jj] = bt * (vt[j0 + jj] - r[jj]);", "r[jj] = bt * (vt[j0 + jj] + r[jj]);"),
+    ("beta dropped", "r[jj] = bt * (vt[j0 + jj] - r[jj]);", "r[jj] = (vt[j0 + jj] - r[jj]);"),
+    ("scale dropped", "for (int64_t jj = 0; jj < nj; ++jj) ot[jj] *= J->scale;", ""),
+    ("per-key gate read from the first key only", "dk[i] = exp(J->g[tok * K + i]);", "dk[i] = exp(J->g[tok * K]);"),
+    ("initial state transposed", "S[i * nj + jj] = src[i * V + j0 + jj];", "S[i * nj + jj] = src[(j0 + jj) * V + i];"),
+    ("output read with k instead of q", "const double qi = qt[i];", "const double qi = kt[i];"),
+    ("no decay", "S[i * nj + jj] *= dk[i];", "(void)dk;"),
+]
+
+
+def _naive_pins_fail(lib) -> bool:
+    for args, scale, o_ref, h_ref in _golden_cases():
+        got = oracle.naive_forward(args["q"], args["k"], args["v"], args["g"], args["beta"], args["h0"],
+                                   1, scale, lib=lib)
+        if np.abs(got["o"] - o_ref).max() > 1e-12 or np.abs(got["h_final"] - h_ref).max() > 1e-12:
+            return True
+    # square problems, so that a transposed K x V operand still has the right shape
+    from test_oracle_pins import explicit_matrix_recurrence
+    for per_k in (False, True):
+        d = _inputs(per_k, T=16)
+        o_ref, h_ref = explicit_matrix_recurrence(d, 0.5)
+        got = oracle.naive_forward(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], 8, 0.5, lib=lib)
+        if np.abs(got["o"] - o_ref).max() > 1e-12 or np.abs(got["h_final"] - h_ref).max() > 1e-12:
+            return True
+    return False
+
+
+def _build_naive(src: str, tmp_path, tag: str):
+    c = tmp_path / f"mut_{tag}.c"
+    so = tmp_path / f"mut_{tag}.so"
+    c.write_text(src)
+    subprocess.check_call(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-pthread", str(c), "-o", str(so), "-lm"])
+    return oracle.load_library(str(so))
+
+
+def test_unmutated_naive_passes_the_pins(tmp_path):
+    with open(NAIVE_SRC) as f:
+        assert not _naive_pins_fail(_build_naive(f.read(), tmp_path, "none"))
+
+
+@pytest.mark.parametrize("what,old,new", NAIVE_MUTANTS, ids=[m[0] for m in NAIVE_MUTANTS])
+def test_naive_mutant_is_caught(what, old, new, tmp_path):
+    with open(NAIVE_SRC) as f:
+        src = f.read()
+    assert src.count(old) == 1, f"mutation site not found: {old!r}"
+    idx = NAIVE_MUTANTS.index((what, old, new))
+    assert _naive_pins_fail(_build_naive(src.replace(old, new), tmp_path, str(idx)))

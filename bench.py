@@ -1,0 +1,384 @@
+"""Throughput of the chunked gated-delta-rule forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+One step = one whole forward (gate cumsum, WY prepare, state scan, chunk output)
+over one batch of the 32k-token GDN workload (B=1, T=32768, H=32, K=V=128, C=64,
+bf16 io, fp32 state, h0 ~ N(0, 0.02)), inputs already resident in HBM.  Each
+timed step is bracketed by CUDA events on the launching stream; a 256 MiB
+buffer (about twice the L2) is overwritten before every timed step, outside the
+events.  Rank 0 prints one JSON line.
+
+--impl reference times the float64 CPU oracle (the only other implementation
+of this computation) on the host cores, one bounded sample of the same workload
+per step.
+
+Under torchrun (N > 1) every rank runs its own copy of the workload on its own
+GPU (the problem shards by (batch, head) with no exchange): weak scaling, and
+`value` is the tokens all ranks processed divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from chunked_gated_delta_prepare_gb300 import gdr, workloads  # noqa: E402
+from chunked_gated_delta_prepare_gb300.inputs import make_workload_inputs  # noqa: E402
+
+METRIC = "gated-delta-rule fwd tokens/s at 1 GB300; achieved HBM GB/s & % roofline"
+FLUSH_BYTES = 256 << 20
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        return float(m["hbm_gbs"]), float(m["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+# Algorithmic HBM bytes per (token, head) of each kernel, and per (batch, head)
+# for the state.  e = io bytes, GW = 4 (scalar gate) or 4K (per-key-dim gate).
+def algorithmic_bytes(wl, kernel: str) -> int:
+    e = 2 if wl.io == "bf16" else 4
+    K, V, C = wl.K, wl.V, wl.chunk
+    gw = 4 * (K if wl.per_k_gate else 1)
+    th = wl.B * wl.T * wl.H
+    bh = wl.B * wl.H
+    state = (4 * K * V if wl.with_h0 else 0) + 4 * K * V
+    if kernel == "prepare":      # read k, v, g, beta; write w, u, g_cum
+        per = 2 * K * e + 2 * V * e + 2 * gw + e
+        return th * per
+    if kernel == "scan":         # read k, w, u, g_cum; write v_new, checkpoint (K*V*e per chunk)
+        per = 2 * K * e + 2 * V * e + gw + (K * V * e) // C
+        return th * per + bh * state
+    if kernel == "output":       # read q, k, v_new, g_cum, checkpoint; write o
+        per = 2 * K * e + 2 * V * e + gw + (K * V * e) // C
+        return th * per
+    if kernel == "forward":      # the I/O floor: read q, k, v, g, beta, h0; write o, h_final
+        per = 2 * K * e + 2 * V * e + gw + e
+        return th * per + bh * state
+    raise ValueError(kernel)
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        if not self.out:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def traffic_for(kernel_name: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when the kernel
+    source changed after the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)[kernel_name]
+        src = os.path.join(ROOT, rec["source"])
+        with open(src, "rb") as f:
+            digest = hashlib.sha256(f.read()).hexdigest()
+        if digest != rec["source_sha256"]:
+            return None
+        return rec["bytes_per_launch"]
+    except Exception:
+        return None
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ CPU oracle leg
+
+def oracle_sample(wl, x, n_heads: int):
+    """Time the float64 token-recurrence oracle on the first n_heads heads (all T tokens)."""
+    import oracle
+    pairs = [(b, h) for b in range(wl.B) for h in range(wl.H)][:n_heads]
+    def tok(t):
+        return torch.stack([t[b, :, h] for b, h in pairs]).unsqueeze(2)
+    q, k, v, g, beta = (tok(t) for t in (x.q, x.k, x.v, x.g, x.beta))
+    h0 = None if x.h0 is None else torch.stack([x.h0[b, h] for b, h in pairs]).unsqueeze(1)
+    args = [oracle.chunked._f64(t) for t in (q, k, v, g, beta)] + [oracle.chunked._f64(h0)]
+    cores = oracle.host_cores()
+    t0 = time.perf_counter()
+    oracle.naive_forward(*args, wl.chunk, 1.0 / wl.K ** 0.5, with_ckpt=False, nthreads=cores)
+    dt = time.perf_counter() - t0
+    token_heads = len(pairs) * wl.T
+    return dict(seconds=dt, tokens_per_s=token_heads / wl.H / dt, cores=cores,
+                sample=f"{len(pairs)} of {wl.B * wl.H} (batch, head) pairs x all {wl.T} tokens "
+                       f"({token_heads} token-heads), float64 C token recurrence, {cores} threads")
+
+
+def run_reference(args, wl):
+    # rank 0 alone times the oracle; other ranks (under torchrun) exit without work
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    x = make_workload_inputs(wl)
+    n_heads = max(1, min(wl.B * wl.H, args.ref_heads))
+    for _ in range(args.warmup):
+        oracle_sample(wl, x, n_heads)
+    secs, last = 0.0, None
+    for _ in range(args.steps):
+        last = oracle_sample(wl, x, n_heads)
+        secs += last["seconds"]
+    tokens = n_heads * wl.T / wl.H * args.steps
+    value = tokens / secs
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded, the workload's distributions)",
+            "config": dict(wl.describe(), sample=last["sample"]),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": last["cores"], "kind": "oracle",
+                             "sample": last["sample"]},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU leg
+
+def run_ours(args, wl):
+    world, rank, local = dist_setup()
+    dev = torch.device("cuda", local)
+    x = make_workload_inputs(wl)
+    q, k, v, g, beta = (t.to(dev) for t in (x.q, x.k, x.v, x.g, x.beta))
+    h0 = x.h0.to(dev) if x.h0 is not None else None
+    B, T, H, K, V, C = wl.B, wl.T, wl.H, wl.K, wl.V, wl.chunk
+    p = gdr.problem_for(q, v, g, C, None, args.variant)
+    o = torch.empty(B, T, H, V, device=dev, dtype=q.dtype)
+    hf = torch.empty(B, H, K, V, device=dev, dtype=torch.float32)
+    nbytes = gdr.gdr_forward_workspace_bytes(p)
+    ws = torch.empty(max(nbytes, 1), device=dev, dtype=torch.uint8)
+    flush = torch.empty(FLUSH_BYTES, device=dev, dtype=torch.uint8)
+    stream = torch.cuda.current_stream()
+
+    # Probe which variant gdr_forward runs, and how its work splits into launches.
+    gdr.gdr_forward(p, q, k, v, g, beta, h0, o, hf, ws if nbytes else None, nbytes)
+    torch.cuda.synchronize()
+    variant = gdr.gdr_last_variant()
+    staged = variant != "fused"
+    if staged:
+        NT = T // C
+        e = q.element_size()
+        # the same three kernels gdr_forward runs, called one by one so each can be timed
+        g_cum = torch.empty_like(g)
+        w = torch.empty_like(k)
+        u = torch.empty_like(v)
+        v_new = torch.empty_like(v)
+        h_ckpt = torch.empty(B, NT, H, K, V, device=dev, dtype=q.dtype)
+        sp = gdr.problem_for(q, v, g, C, None, variant)
+        kernels = ["prepare", "scan", "output"]
+
+        def launches():
+            return [lambda: gdr.gdr_prepare_wy(sp, k, v, g, beta, w, u, g_cum),
+                    lambda: gdr.gdr_scan_h(sp, k, w, u, g_cum, h0, h_ckpt, v_new, hf),
+                    lambda: gdr.gdr_chunk_output(sp, q, k, v_new, h_ckpt, g_cum, o)]
+        del e
+    else:
+        kernels = ["forward"]
+
+        def launches():
+            return [lambda: gdr.gdr_forward(p, q, k, v, g, beta, h0, o, hf, ws if nbytes else None, nbytes)]
+
+    calls = launches()
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        for f in calls:
+            f()
+    torch.cuda.synchronize()
+    assert gdr.gdr_get_device_status() == 0
+
+    n = len(calls)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for s in range(args.steps):
+            flush.fill_(s & 0xFF)
+            evs[s][0].record(stream)
+            for i, f in enumerate(calls):
+                f()
+                evs[s][i + 1].record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    status = gdr.gdr_get_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed region")
+    per_kernel_ms = [0.0] * n
+    step_ms = []
+    for s in range(args.steps):
+        step_ms.append(evs[s][0].elapsed_time(evs[s][n]))
+        for i in range(n):
+            per_kernel_ms[i] += evs[s][i].elapsed_time(evs[s][i + 1])
+    total_s = max_over_ranks(sum(step_ms) / 1e3, world)
+    value = world * B * T * args.steps / total_s
+
+    # roofline of the dominant kernel
+    hbm_gbs, _, peak_kind = peaks()
+    avg_ms = [t / args.steps for t in per_kernel_ms]
+    dom = max(range(n), key=lambda i: avg_ms[i])
+    dom_name = kernels[dom]
+    dom_bytes = algorithmic_bytes(wl, dom_name)
+    achieved = dom_bytes / (avg_ms[dom] / 1e3) / 1e9
+    kname = {"prepare": "simt_prepare_kernel", "scan": "simt_scan_kernel", "output": "simt_output_kernel",
+             "forward": "fused_forward_kernel"}[dom_name]
+    traffic = traffic_for(f"{variant}:{dom_name}")
+
+    # end to end through the public API: pinned host inputs in, o and h_final back to host
+    hx = {n_: t.pin_memory() for n_, t in x.tensors().items() if t is not None}
+    h2d = sum(t.numel() * t.element_size() for t in hx.values())
+    d2h = o.numel() * o.element_size() + hf.numel() * hf.element_size()
+    for _ in range(2):
+        gdr.forward(hx["q"], hx["k"], hx["v"], hx["g"], hx["beta"], hx.get("h0"), chunk=C, workspace=ws)
+    torch.cuda.synchronize()
+    e2e_steps = max(3, min(args.steps, 10))
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        oo, hh = gdr.forward(hx["q"], hx["k"], hx["v"], hx["g"], hx["beta"], hx.get("h0"), chunk=C,
+                             workspace=ws)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    e2e_value = world * B * T * e2e_steps / e2e_s
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = oracle_sample(wl, x, max(1, min(wl.B * wl.H, args.cpu_heads)))
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.io == "bf16" else "f32",
+            "data": "synthetic (seeded; q,k unit-norm, v N(0,1), beta sigmoid, g logsigmoid/16)",
+            "config": dict(wl.describe(), variant=variant, l2="256 MiB buffer overwritten before every timed step",
+                           kernels_per_step=n),
+            "roofline": {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+                         "frac": achieved / hbm_gbs, "peak_source": f"{peak_kind} HBM copy bandwidth",
+                         "traffic": traffic, "algorithmic_bytes_per_launch": dom_bytes,
+                         "avg_launch_ms": avg_ms[dom]},
+            "kernel_ms": {kernels[i]: avg_ms[i] for i in range(n)},
+            "floor_roofline_frac": (algorithmic_bytes(wl, "forward") / (hbm_gbs * 1e9)) / (total_s / args.steps),
+            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": n * args.steps,
+            "clocks": clk.summary(),
+        }
+        if cpu is not None:
+            line["cpu_baseline"] = {"value": cpu["tokens_per_s"], "unit": "tokens/s", "cores": cpu["cores"],
+                                    "kind": "oracle", "sample": cpu["sample"]}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=workloads.THROUGHPUT.name, choices=sorted(workloads.BY_NAME))
+    ap.add_argument("--variant", default="auto", choices=sorted(gdr.VARIANTS))
+    ap.add_argument("--cpu-heads", type=int, default=32, help="heads in the CPU-oracle baseline sample")
+    ap.add_argument("--ref-heads", type=int, default=4, help="heads per step of --impl reference")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    wl = workloads.BY_NAME[args.workload]
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,187 @@
+// The C ABI of libgdr (include/gdr.h): argument validation, workspace
+// planning and kernel dispatch.  No arithmetic of the method happens here;
+// every step runs in the kernels.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <string>
+
+#include "gdr.h"
+#include "gdr_internal.h"
+
+namespace {
+
+thread_local std::string t_last_variant;
+
+constexpr int64_t kMaxGridYZ = 65535;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Checks the descriptor and fills Dims.  Does not look at pointers.
+gdr_status check_problem(const gdr_problem* p, gdr::Dims* d) {
+    if (!p) return GDR_ERR_NULL;
+    if (p->io_dtype != GDR_F32 && p->io_dtype != GDR_BF16) return GDR_ERR_DTYPE;
+    if (p->gate != GDR_GATE_SCALAR && p->gate != GDR_GATE_PER_K) return GDR_ERR_DTYPE;
+    if (p->B <= 0 || p->T <= 0 || p->H <= 0 || p->K <= 0 || p->V <= 0 || p->chunk <= 0) return GDR_ERR_SHAPE;
+    if ((p->K != 64 && p->K != 128) || (p->V != 64 && p->V != 128)) return GDR_ERR_SHAPE;
+    if (p->chunk != 32 && p->chunk != 64) return GDR_ERR_SHAPE;
+    if (p->T % p->chunk != 0) return GDR_ERR_SHAPE;
+    // grid and 32-bit dims limits: T, B*T*H fit int32; H and B*(V/32) fit a grid y/z extent
+    if (p->T > INT32_MAX || p->H > kMaxGridYZ || p->B * (p->V / 32) > kMaxGridYZ) return GDR_ERR_SHAPE;
+    if (p->B > INT32_MAX / p->T || p->B * p->T > INT32_MAX / p->H) return GDR_ERR_SHAPE;
+    if (std::isnan(p->scale) || std::isinf(p->scale)) return GDR_ERR_ARG;
+    if (p->variant < GDR_VARIANT_AUTO || p->variant > GDR_VARIANT_FUSED) return GDR_ERR_ARG;
+    d->B = (int)p->B;
+    d->T = (int)p->T;
+    d->H = (int)p->H;
+    d->K = (int)p->K;
+    d->V = (int)p->V;
+    d->C = (int)p->chunk;
+    d->NT = d->T / d->C;
+    d->per_k = p->gate == GDR_GATE_PER_K;
+    d->bf16 = p->io_dtype == GDR_BF16;
+    d->scale = p->scale > 0.f ? p->scale : 1.0f / std::sqrt((float)p->K);
+    return GDR_OK;
+}
+
+gdr_status check_ptrs(std::initializer_list<const void*> required, std::initializer_list<const void*> optional) {
+    for (const void* q : required)
+        if (!q) return GDR_ERR_NULL;
+    for (const void* q : required)
+        if (!aligned16(q)) return GDR_ERR_ALIGN;
+    for (const void* q : optional)
+        if (q && !aligned16(q)) return GDR_ERR_ALIGN;
+    return GDR_OK;
+}
+
+gdr_status from_cuda(cudaError_t e) { return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA; }
+
+// Only the fp32 CUDA-core variant exists for the staged entry points so far.
+gdr_status pick_stage_variant(const gdr_problem* p) {
+    if (p->variant == GDR_VARIANT_AUTO || p->variant == GDR_VARIANT_SIMT) return GDR_OK;
+    return GDR_ERR_UNSUPPORTED;
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Staged gdr_forward scratch: g_cum, w, u, v_new, h_ckpt, each 256-byte aligned.
+struct StagedWorkspace {
+    size_t g_cum, w, u, v_new, h_ckpt, total;
+};
+
+StagedWorkspace plan_staged(const gdr::Dims& d) {
+    const size_t e = d.bf16 ? 2 : 4;
+    const size_t rows = (size_t)d.B * d.T * d.H;
+    StagedWorkspace ws;
+    size_t off = 0;
+    ws.g_cum = off; off = round_up(off + rows * (d.per_k ? d.K : 1) * 4, 256);
+    ws.w = off;     off = round_up(off + rows * d.K * e, 256);
+    ws.u = off;     off = round_up(off + rows * d.V * e, 256);
+    ws.v_new = off; off = round_up(off + rows * d.V * e, 256);
+    ws.h_ckpt = off; off = round_up(off + (size_t)d.B * d.NT * d.H * d.K * d.V * e, 256);
+    ws.total = off;
+    return ws;
+}
+
+}  // namespace
+
+extern "C" {
+
+gdr_status gdr_prepare_wy(const gdr_problem* p, const void* k, const void* v, const float* g, const void* beta,
+                          void* w, void* u, float* g_cum, void* stream) {
+    gdr::Dims d;
+    gdr_status st = check_problem(p, &d);
+    if (st != GDR_OK) return st;
+    if ((st = check_ptrs({k, v, g, beta, w, u, g_cum}, {})) != GDR_OK) return st;
+    if ((st = pick_stage_variant(p)) != GDR_OK) return st;
+    st = from_cuda(gdr::simt_prepare(d, k, v, g, beta, w, u, g_cum, (cudaStream_t)stream));
+    if (st == GDR_OK) t_last_variant = "simt";
+    return st;
+}
+
+gdr_status gdr_scan_h(const gdr_problem* p, const void* k, const void* w, const void* u, const float* g_cum,
+                      const float* h0, void* h_ckpt, void* v_new, float* h_final, void* stream) {
+    gdr::Dims d;
+    gdr_status st = check_problem(p, &d);
+    if (st != GDR_OK) return st;
+    if ((st = check_ptrs({k, w, u, g_cum, v_new}, {h0, h_ckpt, h_final})) != GDR_OK) return st;
+    if ((st = pick_stage_variant(p)) != GDR_OK) return st;
+    st = from_cuda(gdr::simt_scan(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, (cudaStream_t)stream));
+    if (st == GDR_OK) t_last_variant = "simt";
+    return st;
+}
+
+gdr_status gdr_chunk_output(const gdr_problem* p, const void* q, const void* k, const void* v_new,
+                            const void* h_ckpt, const float* g_cum, void* o, void* stream) {
+    gdr::Dims d;
+    gdr_status st = check_problem(p, &d);
+    if (st != GDR_OK) return st;
+    if ((st = check_ptrs({q, k, v_new, h_ckpt, g_cum, o}, {})) != GDR_OK) return st;
+    if ((st = pick_stage_variant(p)) != GDR_OK) return st;
+    st = from_cuda(gdr::simt_output(d, q, k, v_new, h_ckpt, g_cum, o, (cudaStream_t)stream));
+    if (st == GDR_OK) t_last_variant = "simt";
+    return st;
+}
+
+size_t gdr_forward_workspace_bytes(const gdr_problem* p) {
+    gdr::Dims d;
+    if (check_problem(p, &d) != GDR_OK) return 0;
+    if (pick_stage_variant(p) != GDR_OK) return 0;
+    return plan_staged(d).total;
+}
+
+gdr_status gdr_forward(const gdr_problem* p, const void* q, const void* k, const void* v, const float* g,
+                       const void* beta, const float* h0, void* o, float* h_final, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+    gdr::Dims d;
+    gdr_status st = check_problem(p, &d);
+    if (st != GDR_OK) return st;
+    if ((st = check_ptrs({q, k, v, g, beta, o}, {h0, h_final})) != GDR_OK) return st;
+    if ((st = pick_stage_variant(p)) != GDR_OK) return st;
+    const StagedWorkspace ws = plan_staged(d);
+    if (!workspace || workspace_bytes < ws.total) return GDR_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GDR_ERR_ALIGN;
+    char* base = static_cast<char*>(workspace);
+    float* g_cum = reinterpret_cast<float*>(base + ws.g_cum);
+    void* w = base + ws.w;
+    void* u = base + ws.u;
+    void* v_new = base + ws.v_new;
+    void* h_ckpt = base + ws.h_ckpt;
+    cudaStream_t s = (cudaStream_t)stream;
+    if ((st = from_cuda(gdr::simt_prepare(d, k, v, g, beta, w, u, g_cum, s))) != GDR_OK) return st;
+    if ((st = from_cuda(gdr::simt_scan(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, s))) != GDR_OK) return st;
+    if ((st = from_cuda(gdr::simt_output(d, q, k, v_new, h_ckpt, g_cum, o, s))) != GDR_OK) return st;
+    t_last_variant = "simt";
+    return GDR_OK;
+}
+
+const char* gdr_status_string(gdr_status s) {
+    switch (s) {
+        case GDR_OK: return "ok";
+        case GDR_ERR_NULL: return "a required pointer is NULL";
+        case GDR_ERR_SHAPE: return "unsupported or inconsistent sizes";
+        case GDR_ERR_DTYPE: return "unknown io dtype or gate kind";
+        case GDR_ERR_ALIGN: return "a pointer is not 16-byte aligned (workspace: 256-byte)";
+        case GDR_ERR_WORKSPACE: return "workspace missing or too small";
+        case GDR_ERR_CUDA: return "a CUDA call or kernel launch failed";
+        case GDR_ERR_DEVICE_TIMEOUT: return "a bounded wait inside a kernel gave up";
+        case GDR_ERR_UNSUPPORTED: return "the requested variant cannot run this problem";
+        case GDR_ERR_ARG: return "invalid argument";
+    }
+    return "unknown status";
+}
+
+gdr_status gdr_get_device_status(void* stream) {
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return GDR_ERR_CUDA;
+    unsigned int code = 0;
+    if (gdr::read_and_clear_device_error(&code) != cudaSuccess) return GDR_ERR_CUDA;
+    return code == 0 ? GDR_OK : GDR_ERR_DEVICE_TIMEOUT;
+}
+
+const char* gdr_last_variant(void) { return t_last_variant.c_str(); }
+
+int gdr_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,35 @@
+// Internal interface between the C ABI (gdr_api.cpp) and the kernel files.
+// Not installed; the public interface is include/gdr.h.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gdr.h"
+
+namespace gdr {
+
+// Validated problem sizes, as every launcher receives them.
+struct Dims {
+    int B, T, H, K, V, C, NT;
+    int per_k;      // 1: per-key-dim gate (g is [B,T,H,K]); 0: scalar gate
+    int bf16;       // 1: io tensors are bf16; 0: fp32
+    float scale;    // resolved output scale
+};
+
+// ---- fp32 CUDA-core kernels (simt_kernels.cu): every K, V in {64,128}, C in {32,64}, both dtypes.
+cudaError_t simt_prepare(const Dims& d, const void* k, const void* v, const float* g, const void* beta,
+                         void* w, void* u, float* g_cum, cudaStream_t s);
+cudaError_t simt_scan(const Dims& d, const void* k, const void* w, const void* u, const float* g_cum,
+                      const float* h0, void* h_ckpt, void* v_new, float* h_final, cudaStream_t s);
+cudaError_t simt_output(const Dims& d, const void* q, const void* k, const void* v_new, const void* h_ckpt,
+                        const float* g_cum, void* o, cudaStream_t s);
+
+// ---- device error word (device_status.cu)
+// Bounded waits in kernels write a nonzero code here instead of trapping.
+cudaError_t read_and_clear_device_error(unsigned int* code);
+// Address of the error word on the current device (to pass to kernels).
+cudaError_t device_error_ptr(unsigned int** ptr);
+constexpr unsigned int kDeviceErrTimeout = 1u;
+
+}  // namespace gdr

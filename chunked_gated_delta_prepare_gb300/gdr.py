@@ -1,0 +1,202 @@
+"""ctypes binding of libgdr (include/gdr.h).
+
+Argument marshalling only: every step of the forward runs in libgdr's CUDA
+kernels.  PyTorch supplies device memory and the current stream.  There is no
+CPU fallback: if the library is missing or cannot load, every call raises.
+
+The functions mirror the C ABI names:
+    gdr_prepare_wy, gdr_scan_h, gdr_chunk_output, gdr_forward,
+    gdr_forward_workspace_bytes, gdr_status_string, gdr_get_device_status,
+    gdr_last_variant, gdr_version
+and `forward(...)` is the convenience call that allocates outputs and the
+workspace (and, given CPU tensors, copies them to the GPU and the results back).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libgdr.so")
+
+GDR_OK = 0
+STATUS_NAMES = {0: "GDR_OK", 1: "GDR_ERR_NULL", 2: "GDR_ERR_SHAPE", 3: "GDR_ERR_DTYPE", 4: "GDR_ERR_ALIGN",
+                5: "GDR_ERR_WORKSPACE", 6: "GDR_ERR_CUDA", 7: "GDR_ERR_DEVICE_TIMEOUT",
+                8: "GDR_ERR_UNSUPPORTED", 9: "GDR_ERR_ARG"}
+DTYPES = {torch.float32: 0, torch.bfloat16: 1}
+VARIANTS = {"auto": 0, "simt": 1, "tensor": 2, "fused": 3}
+EXPORTS = ["gdr_prepare_wy", "gdr_scan_h", "gdr_chunk_output", "gdr_forward", "gdr_forward_workspace_bytes",
+           "gdr_status_string", "gdr_get_device_status", "gdr_last_variant", "gdr_version"]
+
+
+class GdrError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)} ({_status_text(status)})")
+
+
+class gdr_problem(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("T", ctypes.c_int64), ("H", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("V", ctypes.c_int64), ("chunk", ctypes.c_int64), ("io_dtype", ctypes.c_int32),
+                ("gate", ctypes.c_int32), ("scale", ctypes.c_float), ("variant", ctypes.c_int32)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load(path: str | None = None):
+    """Load libgdr.so (built by `build.py`).  Raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"libgdr is not built ({p} missing); run __graft_entry__.build() "
+                               "or python -m chunked_gated_delta_prepare_gb300.build")
+        lib = ctypes.CDLL(p)
+        vp, P = ctypes.c_void_p, ctypes.POINTER(gdr_problem)
+        sig = {
+            "gdr_prepare_wy": [P, vp, vp, vp, vp, vp, vp, vp, vp],
+            "gdr_scan_h": [P, vp, vp, vp, vp, vp, vp, vp, vp, vp],
+            "gdr_chunk_output": [P, vp, vp, vp, vp, vp, vp, vp],
+            "gdr_forward": [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp],
+            "gdr_forward_workspace_bytes": [P],
+            "gdr_status_string": [ctypes.c_int],
+            "gdr_get_device_status": [vp],
+            "gdr_last_variant": [],
+            "gdr_version": [],
+        }
+        for name, args in sig.items():
+            f = getattr(lib, name)
+            f.argtypes = args
+            f.restype = ctypes.c_int
+        lib.gdr_forward_workspace_bytes.restype = ctypes.c_size_t
+        lib.gdr_status_string.restype = ctypes.c_char_p
+        lib.gdr_last_variant.restype = ctypes.c_char_p
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _status_text(status: int) -> str:
+    try:
+        return load().gdr_status_string(status).decode()
+    except Exception:  # the library may be the thing that is missing
+        return "?"
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, where: str):
+    if status != GDR_OK:
+        raise GdrError(status, where)
+
+
+def make_problem(B, T, H, K, V, chunk, io_dtype=torch.bfloat16, per_k_gate=False, scale=None,
+                 variant="auto") -> gdr_problem:
+    dt = DTYPES[io_dtype] if isinstance(io_dtype, torch.dtype) else int(io_dtype)
+    return gdr_problem(B=B, T=T, H=H, K=K, V=V, chunk=chunk, io_dtype=dt, gate=1 if per_k_gate else 0,
+                       scale=-1.0 if scale is None else float(scale),
+                       variant=VARIANTS[variant] if isinstance(variant, str) else int(variant))
+
+
+def problem_for(q, v, g, chunk, scale=None, variant="auto") -> gdr_problem:
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    return make_problem(B, T, H, K, V, chunk, q.dtype, g.dim() == 4, scale, variant)
+
+
+# ---------------------------------------------------------------- raw entry points
+
+def gdr_prepare_wy(p, k, v, g, beta, w, u, g_cum, stream=None):
+    _check(load().gdr_prepare_wy(ctypes.byref(p), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(w), _ptr(u),
+                                 _ptr(g_cum), _stream(stream)), "gdr_prepare_wy")
+
+
+def gdr_scan_h(p, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, stream=None):
+    _check(load().gdr_scan_h(ctypes.byref(p), _ptr(k), _ptr(w), _ptr(u), _ptr(g_cum), _ptr(h0), _ptr(h_ckpt),
+                             _ptr(v_new), _ptr(h_final), _stream(stream)), "gdr_scan_h")
+
+
+def gdr_chunk_output(p, q, k, v_new, h_ckpt, g_cum, o, stream=None):
+    _check(load().gdr_chunk_output(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v_new), _ptr(h_ckpt), _ptr(g_cum),
+                                   _ptr(o), _stream(stream)), "gdr_chunk_output")
+
+
+def gdr_forward_workspace_bytes(p) -> int:
+    return int(load().gdr_forward_workspace_bytes(ctypes.byref(p)))
+
+
+def gdr_forward(p, q, k, v, g, beta, h0, o, h_final, workspace, workspace_bytes, stream=None):
+    _check(load().gdr_forward(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(o),
+                              _ptr(h_final), _ptr(workspace), int(workspace_bytes), _stream(stream)),
+           "gdr_forward")
+
+
+def gdr_status_string(status: int) -> str:
+    return load().gdr_status_string(int(status)).decode()
+
+
+def gdr_get_device_status(stream=None) -> int:
+    return int(load().gdr_get_device_status(_stream(stream)))
+
+
+def gdr_last_variant() -> str:
+    return load().gdr_last_variant().decode()
+
+
+def gdr_version() -> int:
+    return int(load().gdr_version())
+
+
+# ---------------------------------------------------------------- convenience
+
+def forward(q, k, v, g, beta, h0=None, *, chunk=64, scale=None, variant="auto", want_h_final=True,
+            workspace=None, stream=None):
+    """o, h_final = forward(q, k, v, g, beta, h0).
+
+    Device tensors are used in place.  CPU tensors are copied to the current
+    CUDA device (non-blocking from pinned memory) and the results copied back.
+    """
+    on_host = q.device.type == "cpu"
+    if on_host:
+        dev = torch.device("cuda", torch.cuda.current_device())
+        q, k, v, g, beta = (t.to(dev, non_blocking=True) for t in (q, k, v, g, beta))
+        h0 = h0.to(dev, non_blocking=True) if h0 is not None else None
+    p = problem_for(q, v, g, chunk, scale, variant)
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    o = torch.empty(B, T, H, V, device=q.device, dtype=q.dtype)
+    hf = torch.empty(B, H, K, V, device=q.device, dtype=torch.float32) if want_h_final else None
+    nbytes = gdr_forward_workspace_bytes(p)
+    if workspace is None and nbytes:
+        workspace = torch.empty(nbytes, device=q.device, dtype=torch.uint8)
+    gdr_forward(p, q, k, v, g, beta, h0, o, hf, workspace, nbytes, stream)
+    if on_host:
+        o = o.to("cpu", non_blocking=False)
+        hf = hf.to("cpu") if hf is not None else None
+    return o, hf
+
+
+def default_scale(K: int) -> float:
+    return 1.0 / math.sqrt(K)

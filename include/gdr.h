@@ -1,0 +1,186 @@
+/*
+ * gdr.h -- C ABI of libgdr, the chunked gated-delta-rule forward on one GPU.
+ *
+ * The gated delta rule keeps, per (batch b, head h), a K x V state S and for
+ * every token t applies
+ *     S~ = D_t S_{t-1},  delta_t = beta_t (v_t - S~^T k_t),  S_t = S~ + k_t delta_t^T,
+ *     o_t = scale * S_t^T q_t,
+ * with D_t = exp(g_t) (scalar gate, GDN) or diag(exp(g_t[0..K))) (per-key-dim gate,
+ * KDA).  The library computes this in chunks of C tokens in three stages:
+ *
+ *   gdr_prepare_wy   the fused WY prepare of "Reuse P as beta tiles in gated
+ *                    deltanet fused prepare" (TileOPs-Metax PR #60): the gated
+ *                    strictly-lower A, its inverse (I + A)^{-1}, w and u;
+ *   gdr_scan_h       the serial inter-chunk state scan of
+ *                    "kernel_fun/kda/_kernels/bwd_scan.py" (module docstring:
+ *                    hck[c] = h before the update, v' = u - w h, h = decay*h + kg^T v');
+ *   gdr_chunk_output the chunk output that the same page says the forward
+ *                    assembled in its epilogue warps (module docstring, "the
+ *                    warps that assembled o in the forward");
+ *   gdr_forward      all three, (q, k, v, g, beta, h0) -> (o, h_final).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *   never allocates device memory; gdr_forward takes its scratch from a caller
+ *   workspace.  Every call is asynchronous on `stream` (a cudaStream_t passed
+ *   as void*; NULL is the legacy default stream) and returns as soon as the
+ *   launches are queued.
+ * - Layouts are contiguous, head dim last ("head-last", as the re-scan page's
+ *   host wrapper takes them): q, k, w [B,T,H,K]; v, u, v_new, o [B,T,H,V];
+ *   g, g_cum [B,T,H] (scalar gate) or [B,T,H,K] (per-key-dim gate), always fp32;
+ *   beta [B,T,H]; h0, h_final [B,H,K,V] fp32; h_ckpt [B,NT,H,K,V] with NT = T/C.
+ * - "io" tensors (q, k, v, beta, w, u, v_new, o, h_ckpt) have the problem's
+ *   io_dtype: fp32 or bf16.  g, g_cum, h0 and h_final are always fp32.
+ * - g is the natural-log per-token decay (<= 0 for a decaying state); the
+ *   library takes its chunk-local inclusive cumsum itself.
+ * - Argument errors are detected before anything is launched and returned as a
+ *   status code; nothing is written in that case.  A launch failure returns
+ *   GDR_ERR_CUDA.  Waits inside kernels are bounded: if one gives up, the kernel
+ *   records GDR_ERR_DEVICE_TIMEOUT in a device error word and exits; read it with
+ *   gdr_get_device_status().
+ * - Supported: K, V in {64, 128}; chunk C in {32, 64}; T % C == 0; B, H, T >= 1;
+ *   every pointer 16-byte aligned.
+ * - Thread safety: calls may be made from several host threads.  The only
+ *   per-call host state is the name of the kernel variant that ran, which is
+ *   kept per host thread (gdr_last_variant).
+ */
+#ifndef GDR_H
+#define GDR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GDR_API __attribute__((visibility("default")))
+#else
+#define GDR_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gdr_status {
+    GDR_OK = 0,
+    GDR_ERR_NULL = 1,            /* a required pointer is NULL */
+    GDR_ERR_SHAPE = 2,           /* a size is <= 0, T % chunk != 0, K/V/chunk unsupported */
+    GDR_ERR_DTYPE = 3,           /* io_dtype or gate kind not known */
+    GDR_ERR_ALIGN = 4,           /* a pointer is not 16-byte aligned */
+    GDR_ERR_WORKSPACE = 5,       /* workspace NULL or smaller than gdr_forward_workspace_bytes */
+    GDR_ERR_CUDA = 6,            /* a CUDA call or launch failed */
+    GDR_ERR_DEVICE_TIMEOUT = 7,  /* a bounded in-kernel wait gave up (read via gdr_get_device_status) */
+    GDR_ERR_UNSUPPORTED = 8,     /* a variant hint that cannot run this problem */
+    GDR_ERR_ARG = 9              /* another invalid argument (e.g. a NaN scale) */
+} gdr_status;
+
+typedef enum gdr_dtype { GDR_F32 = 0, GDR_BF16 = 1 } gdr_dtype;
+
+typedef enum gdr_gate {
+    GDR_GATE_SCALAR = 0,  /* GDN: g [B,T,H] */
+    GDR_GATE_PER_K = 1    /* KDA: g [B,T,H,K] */
+} gdr_gate;
+
+/* Which kernels to run.  AUTO picks the fastest variant that supports the problem. */
+typedef enum gdr_variant {
+    GDR_VARIANT_AUTO = 0,
+    GDR_VARIANT_SIMT = 1,     /* fp32 CUDA-core arithmetic throughout (exact-fp32 path) */
+    GDR_VARIANT_TENSOR = 2,   /* staged kernels on the tensor cores (bf16 io only) */
+    GDR_VARIANT_FUSED = 3     /* one fused forward kernel (gdr_forward only; bf16 io only) */
+} gdr_variant;
+
+typedef struct gdr_problem {
+    int64_t B, T, H, K, V;
+    int64_t chunk;      /* C: tokens per chunk */
+    int32_t io_dtype;   /* gdr_dtype */
+    int32_t gate;       /* gdr_gate */
+    float scale;        /* output scale; <= 0 selects 1/sqrt(K) */
+    int32_t variant;    /* gdr_variant */
+} gdr_problem;
+
+/*
+ * Stage 1: WY prepare ("Reuse P as beta tiles in gated deltanet fused prepare":
+ * A_g, the Neumann/substitution inverse, w = A_g^{-1} k_beta, u = A_g^{-1} v_beta).
+ * Per (b, h, chunk), with G the chunk-local inclusive cumsum of g:
+ *     A_ij  = beta_i sum_d k_id k_jd exp(G_id - G_jd)   for i > j, else 0
+ *     w     = (I + A)^{-1} (k * beta * exp(G))          [C,K]
+ *     u     = (I + A)^{-1} (v * beta)                   [C,V]
+ * Inputs:  k [B,T,H,K] io, v [B,T,H,V] io, g fp32, beta [B,T,H] io.
+ * Outputs: w [B,T,H,K] io, u [B,T,H,V] io, g_cum (same shape as g) fp32 = G.
+ * The prepare page builds k_beta without exp(G); the form above is the one
+ * under which v' = u - w h is the recurrence's delta, and it is the one used.
+ */
+GDR_API gdr_status gdr_prepare_wy(const gdr_problem* p, const void* k, const void* v, const float* g,
+                          const void* beta, void* w, void* u, float* g_cum, void* stream);
+
+/*
+ * Stage 2: the serial state scan ("kernel_fun/kda/_kernels/bwd_scan.py", module
+ * docstring).  Per (b, h), h = h0 (zero if h0 == NULL), then for c = 0 .. NT-1:
+ *     h_ckpt[c] = h                          (rounded to io dtype)
+ *     v'_c      = u_c - w_c h                -> v_new (io dtype)
+ *     h         = exp(G_last) * h + (k * exp(G_last - G))^T v'_c
+ * where G = g_cum of chunk c and G_last its last row (a K-vector for KDA that
+ * scales the rows of h).  h is carried in fp32; h_final = h after the last chunk.
+ * Inputs:  k, w [B,T,H,K] io; u [B,T,H,V] io; g_cum fp32; h0 [B,H,K,V] fp32 or NULL.
+ * Outputs: h_ckpt [B,NT,H,K,V] io or NULL (not written); v_new [B,T,H,V] io;
+ *          h_final [B,H,K,V] fp32 or NULL (not written).
+ */
+GDR_API gdr_status gdr_scan_h(const gdr_problem* p, const void* k, const void* w, const void* u,
+                      const float* g_cum, const float* h0, void* h_ckpt, void* v_new,
+                      float* h_final, void* stream);
+
+/*
+ * Stage 3: chunk output.  Per (b, h, chunk c), with G = g_cum of the chunk:
+ *     o_c = scale * [ (q * exp(G)) h_ckpt[c] + tril_0(Q~) v'_c ],
+ *     Q~_ij = sum_d q_id k_jd exp(G_id - G_jd)   (diagonal included)
+ * Inputs:  q, k [B,T,H,K] io; v_new [B,T,H,V] io; h_ckpt [B,NT,H,K,V] io; g_cum fp32.
+ * Output:  o [B,T,H,V] io.
+ */
+GDR_API gdr_status gdr_chunk_output(const gdr_problem* p, const void* q, const void* k, const void* v_new,
+                            const void* h_ckpt, const float* g_cum, void* o, void* stream);
+
+/*
+ * Bytes of device workspace gdr_forward needs for this problem (0 when the
+ * variant it would run keeps every intermediate on chip).  Returns 0 for a
+ * problem that gdr_forward would reject.
+ */
+GDR_API size_t gdr_forward_workspace_bytes(const gdr_problem* p);
+
+/*
+ * The whole forward: (q, k, v, g, beta, h0) -> (o, h_final).
+ * Inputs:  q, k [B,T,H,K] io; v [B,T,H,V] io; g fp32; beta [B,T,H] io;
+ *          h0 [B,H,K,V] fp32 or NULL (zero initial state).
+ * Outputs: o [B,T,H,V] io; h_final [B,H,K,V] fp32 or NULL (not written).
+ * workspace: device memory of at least gdr_forward_workspace_bytes(p) bytes,
+ *          256-byte aligned, owned by the caller, not read before written;
+ *          may be NULL when that size is 0.
+ */
+GDR_API gdr_status gdr_forward(const gdr_problem* p, const void* q, const void* k, const void* v,
+                       const float* g, const void* beta, const float* h0, void* o,
+                       float* h_final, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Static, human-readable text for a status code. */
+GDR_API const char* gdr_status_string(gdr_status s);
+
+/*
+ * Synchronises `stream`, then reads and clears the device error word of the
+ * current device.  Returns GDR_OK, GDR_ERR_DEVICE_TIMEOUT, or GDR_ERR_CUDA when
+ * the synchronisation itself failed.
+ */
+GDR_API gdr_status gdr_get_device_status(void* stream);
+
+/*
+ * Name of the kernel variant the last successful call on this host thread
+ * launched (e.g. "simt", "tensor", "fused"); "" before any call.  The pointer
+ * stays valid until the next call on the same thread.
+ */
+GDR_API const char* gdr_last_variant(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+GDR_API int gdr_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDR_H */

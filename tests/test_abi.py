@@ -1,0 +1,131 @@
+"""Host-side checks of the C ABI: the library builds and loads without a GPU,
+exports every function include/gdr.h declares, and rejects bad arguments with
+the documented status codes before it launches anything."""
+import ctypes
+import os
+import re
+import threading
+
+import pytest
+
+from chunked_gated_delta_prepare_gb300 import build as gdr_build
+from chunked_gated_delta_prepare_gb300 import gdr
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdr.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gdr_build.build()
+    return gdr.load()
+
+
+def declared_functions():
+    with open(HEADER) as f:
+        src = f.read()
+    return re.findall(r"^GDR_API\s+[\w\s\*]+?\b(gdr_\w+)\s*\(", src, flags=re.M)
+
+
+def test_header_declares_the_stage_entry_points():
+    names = declared_functions()
+    for n in ("gdr_prepare_wy", "gdr_scan_h", "gdr_chunk_output", "gdr_forward", "gdr_forward_workspace_bytes",
+              "gdr_status_string", "gdr_get_device_status", "gdr_last_variant", "gdr_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+    assert set(gdr.EXPORTS) <= set(declared_functions())
+
+
+def test_status_strings(lib):
+    for code in range(10):
+        s = gdr.gdr_status_string(code)
+        assert s and s != "unknown status"
+    assert gdr.gdr_status_string(123) == "unknown status"
+
+
+def test_last_variant_empty_on_new_thread(lib):
+    out = []
+    t = threading.Thread(target=lambda: out.append(gdr.gdr_last_variant()))
+    t.start()
+    t.join()
+    assert out == [""]
+
+
+def _fwd(lib, p, ptrs=None, ws=None, ws_bytes=0):
+    a = dict(q=16, k=16, v=16, g=16, beta=16, h0=None, o=16, hf=None)
+    a.update(ptrs or {})
+    return lib.gdr_forward(ctypes.byref(p) if p is not None else None, a["q"], a["k"], a["v"], a["g"], a["beta"],
+                           a["h0"], a["o"], a["hf"], ws, ws_bytes, None)
+
+
+def good():
+    return gdr.make_problem(1, 256, 2, 64, 64, 64)
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("T", 100, 2), ("T", 0, 2), ("B", 0, 2), ("H", -1, 2), ("K", 96, 2), ("V", 32, 2), ("chunk", 16, 2),
+    ("chunk", 0, 2), ("H", 70000, 2), ("io_dtype", 7, 3), ("gate", 2, 3), ("variant", 9, 9),
+    ("scale", float("nan"), 9), ("scale", float("inf"), 9),
+])
+def test_bad_problem_is_rejected(lib, field, value, code):
+    p = good()
+    setattr(p, field, value)
+    assert _fwd(lib, p) == code
+    assert lib.gdr_forward_workspace_bytes(ctypes.byref(p)) == 0
+
+
+def test_null_problem(lib):
+    assert _fwd(lib, None) == 1
+    assert lib.gdr_forward_workspace_bytes(None) == 0
+
+
+@pytest.mark.parametrize("name", ["q", "k", "v", "g", "beta", "o"])
+def test_null_required_pointer(lib, name):
+    assert _fwd(lib, good(), {name: None}) == 1
+
+
+@pytest.mark.parametrize("name", ["q", "k", "v", "g", "beta", "o", "h0", "hf"])
+def test_misaligned_pointer(lib, name):
+    assert _fwd(lib, good(), {name: 24}) == 4
+
+
+def test_workspace_checks(lib):
+    p = good()
+    need = lib.gdr_forward_workspace_bytes(ctypes.byref(p))
+    assert need > 0
+    assert _fwd(lib, p, ws=None, ws_bytes=need) == 5
+    assert _fwd(lib, p, ws=256, ws_bytes=need - 1) == 5
+    assert _fwd(lib, p, ws=272, ws_bytes=need) == 4          # workspace must be 256-byte aligned
+
+
+def test_workspace_size_formula(lib):
+    # g_cum fp32, then w, u, v_new, h_ckpt in the io dtype, each rounded up to 256 bytes
+    for (B, T, H, K, V, C, bf16, per_k) in [(1, 256, 2, 64, 64, 64, 0, 0), (2, 4096, 8, 64, 64, 32, 1, 0),
+                                            (2, 8192, 16, 128, 128, 64, 1, 1)]:
+        p = gdr.make_problem(B, T, H, K, V, C, 1 if bf16 else 0, bool(per_k), variant="simt")
+        e = 2 if bf16 else 4
+        r = lambda x: (x + 255) // 256 * 256
+        rows = B * T * H
+        want = r(rows * (K if per_k else 1) * 4) + r(rows * K * e) + 2 * r(rows * V * e) + r(B * (T // C) * H * K * V * e)
+        assert lib.gdr_forward_workspace_bytes(ctypes.byref(p)) == want
+
+
+def test_stage_entry_points_validate(lib):
+    p = good()
+    P = ctypes.byref(p)
+    assert lib.gdr_prepare_wy(P, 16, 16, 16, 16, 16, None, 16, None) == 1
+    assert lib.gdr_prepare_wy(P, 16, 16, 16, 16, 16, 16, 20, None) == 4
+    assert lib.gdr_scan_h(P, 16, 16, 16, 16, None, None, None, None, None) == 1      # v_new required
+    assert lib.gdr_scan_h(P, 16, 16, 16, 16, 8, None, 16, None, None) == 4           # h0 misaligned
+    assert lib.gdr_chunk_output(P, 16, 16, 16, None, 16, 16, None) == 1              # h_ckpt required
+    p.T = 96
+    assert lib.gdr_chunk_output(P, 16, 16, 16, 16, 16, 16, None) == 2
+
+
+def test_python_binding_raises_on_missing_library(tmp_path):
+    with pytest.raises(RuntimeError):
+        gdr.load(str(tmp_path / "libgdr_missing.so"))

@@ -1,0 +1,134 @@
+"""Whole-forward parity on the GPU (gdr_forward through the C ABI) against the
+float64 token-recurrence oracle, plus invariants and edge cases."""
+import itertools
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from chunked_gated_delta_prepare_gb300 import gdr, workloads
+from chunked_gated_delta_prepare_gb300.inputs import GdrInputs, make_inputs, make_workload_inputs
+from gpu_helpers import (H_TOL, O_TOL, all_pairs, check_forward, gpu_forward, io_name, max_abs, rel_frob)
+
+pytestmark = pytest.mark.gpu
+
+# every variant gdr_forward offers, with the io dtypes it takes
+FORWARD_VARIANTS = {"simt": (torch.float32, torch.bfloat16)}
+SHAPES = [(2, 256, 3, 64, 64, 64), (1, 192, 2, 128, 128, 64), (2, 128, 3, 64, 128, 32),
+          (1, 160, 1, 128, 64, 32), (1, 64, 2, 128, 128, 64), (1, 32, 1, 64, 64, 32)]
+
+
+def small_cases():
+    for shape, per_k, (variant, dts) in itertools.product(SHAPES, (False, True), FORWARD_VARIANTS.items()):
+        for dt in dts:
+            yield pytest.param(shape, per_k, variant, dt,
+                               id=f"{'x'.join(map(str, shape))}-{'kda' if per_k else 'gdn'}-{variant}-{io_name(dt)}")
+
+
+@pytest.mark.parametrize("shape,per_k,variant,dtype", list(small_cases()))
+def test_forward_small_all_heads(shape, per_k, variant, dtype):
+    B, T, H, K, V, C = shape
+    x = make_inputs(B, T, H, K, V, per_k_gate=per_k, io_dtype=dtype, with_h0=True, seed=5)
+    scale = 1.0 / np.sqrt(K)
+    o, hf, ran = gpu_forward(x, C, variant)
+    assert ran == variant
+    check_forward(x, o, hf, all_pairs(B, H), C, scale, io_name(dtype))
+
+
+# The named workloads at full size, in the launch configuration the benchmark
+# times (variant "auto").  Heads are sampled where the oracle would be slow;
+# each sampled head is checked on every token.
+WORKLOAD_SAMPLES = {
+    workloads.GDN_F32_T256.name: None,            # every head
+    workloads.GDN_BF16_T2K.name: None,
+    workloads.GDN_BF16_C32.name: None,
+    workloads.KDA_BF16_T8K.name: [(0, 0), (0, 7), (1, 3), (1, 15)],
+    workloads.GDN_BF16_T32K.name: [(0, 0), (0, 13), (0, 31)],
+}
+
+
+@pytest.mark.parametrize("wl", workloads.ALL, ids=lambda w: w.name)
+def test_forward_workload_full_size(wl):
+    x = make_workload_inputs(wl)
+    o, hf, ran = gpu_forward(x, wl.chunk, "auto")
+    pairs = WORKLOAD_SAMPLES[wl.name] or all_pairs(wl.B, wl.H)
+    eo, eh = check_forward(x, o, hf, pairs, wl.chunk, 1.0 / np.sqrt(wl.K), wl.io)
+    assert torch.isfinite(o).all() and torch.isfinite(hf).all()
+    print(f"{wl.name}: variant={ran} o max-abs {eo:.2e}  h_final rel-F {eh:.2e}")
+
+
+@pytest.mark.parametrize("variant,dtype", [(v, d) for v, ds in FORWARD_VARIANTS.items() for d in ds])
+@pytest.mark.parametrize("per_k", [False, True])
+def test_deterministic_and_exact_scaling(variant, dtype, per_k):
+    """Two runs are bitwise equal; scaling (v, h0) by 2 scales (o, h_final) by exactly 2."""
+    x = make_inputs(2, 256, 2, 128, 128, per_k_gate=per_k, io_dtype=dtype, with_h0=True, seed=6)
+    o1, h1, _ = gpu_forward(x, 64, variant)
+    o2, h2, _ = gpu_forward(x, 64, variant)
+    assert torch.equal(o1, o2) and torch.equal(h1, h2)
+    x2 = GdrInputs(q=x.q, k=x.k, v=x.v * 2, g=x.g, beta=x.beta, h0=x.h0 * 2)
+    o3, h3, _ = gpu_forward(x2, 64, variant)
+    assert torch.equal(o3, o1 * 2) and torch.equal(h3, h1 * 2)
+
+
+@pytest.mark.parametrize("variant,dtype", [(v, d) for v, ds in FORWARD_VARIANTS.items() for d in ds])
+def test_state_carry(variant, dtype):
+    x = make_inputs(1, 512, 2, 128, 128, io_dtype=dtype, with_h0=True, seed=7)
+    o, hf, _ = gpu_forward(x, 64, variant)
+    T1 = 192
+    a = GdrInputs(q=x.q[:, :T1], k=x.k[:, :T1], v=x.v[:, :T1], g=x.g[:, :T1], beta=x.beta[:, :T1], h0=x.h0)
+    oa, ha, _ = gpu_forward(a, 64, variant)
+    b = GdrInputs(q=x.q[:, T1:], k=x.k[:, T1:], v=x.v[:, T1:], g=x.g[:, T1:], beta=x.beta[:, T1:], h0=ha.cpu())
+    ob, hb, _ = gpu_forward(b, 64, variant)
+    io = io_name(dtype)
+    assert max_abs(torch.cat([oa, ob], dim=1), o.cpu().double().numpy()) <= O_TOL[io]
+    assert rel_frob(hb, hf.cpu().double().numpy()) <= H_TOL[io]
+
+
+@pytest.mark.parametrize("variant,dtype", [(v, d) for v, ds in FORWARD_VARIANTS.items() for d in ds])
+def test_null_h0_is_zero_state_and_h_final_optional(variant, dtype):
+    x = make_inputs(1, 128, 2, 64, 64, io_dtype=dtype, with_h0=False, seed=8)
+    o1, h1, _ = gpu_forward(x, 64, variant, h0=None)
+    o2, h2, _ = gpu_forward(x, 64, variant, h0=torch.zeros(1, 2, 64, 64))
+    o3, _, _ = gpu_forward(x, 64, variant, h0=None, want_h_final=False)
+    assert torch.equal(o1, o2) and torch.equal(h1, h2) and torch.equal(o1, o3)
+
+
+def _edge_inputs(kind, per_k, dtype):
+    x = make_inputs(1, 128, 2, 64, 64, per_k_gate=per_k, io_dtype=dtype, with_h0=True, seed=9)
+    g, beta = x.g.clone(), x.beta.clone()
+    if kind == "beta_zero":
+        beta.zero_()
+    elif kind == "no_decay":
+        g.zero_()
+    elif kind == "strong_decay":
+        g.fill_(-20.0)
+    elif kind == "single_chunk":
+        return GdrInputs(q=x.q[:, :32], k=x.k[:, :32], v=x.v[:, :32], g=x.g[:, :32], beta=x.beta[:, :32], h0=x.h0)
+    return GdrInputs(q=x.q, k=x.k, v=x.v, g=g, beta=beta, h0=x.h0 * 20)
+
+
+@pytest.mark.parametrize("kind", ["beta_zero", "no_decay", "strong_decay", "single_chunk"])
+@pytest.mark.parametrize("per_k", [False, True])
+@pytest.mark.parametrize("variant,dtype", [(v, d) for v, ds in FORWARD_VARIANTS.items() for d in ds])
+def test_edge_cases(kind, per_k, variant, dtype):
+    x = _edge_inputs(kind, per_k, dtype)
+    C = 32
+    o, hf, _ = gpu_forward(x, C, variant)
+    check_forward(x, o, hf, all_pairs(1, 2), C, 1.0 / 8.0, io_name(dtype))
+
+
+def test_convenience_forward_host_tensors():
+    x = make_inputs(1, 128, 2, 64, 64, io_dtype=torch.bfloat16, with_h0=True, seed=10)
+    o, hf = gdr.forward(x.q, x.k, x.v, x.g, x.beta, x.h0, chunk=64)
+    assert o.device.type == "cpu" and hf.device.type == "cpu"
+    ref = oracle.naive_forward(x.q, x.k, x.v, x.g, x.beta, x.h0, 64, 1 / 8.0, with_ckpt=False)
+    assert max_abs(o, ref["o"]) <= O_TOL["bf16"]
+    assert rel_frob(hf, ref["h_final"]) <= H_TOL["bf16"]
+
+
+def test_invalid_shape_launches_nothing():
+    x = make_inputs(1, 96, 1, 64, 64, io_dtype=torch.bfloat16, seed=11)  # T % C != 0
+    with pytest.raises(gdr.GdrError) as e:
+        gpu_forward(x, 64, "auto")
+    assert e.value.status == 2

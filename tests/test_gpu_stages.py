@@ -1,0 +1,113 @@
+"""Per-stage parity on the GPU: each C-ABI stage entry point against the
+chunked float64 oracle's stage function, fed the same rounded inputs."""
+import itertools
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import chunked
+from chunked_gated_delta_prepare_gb300 import gdr
+from chunked_gated_delta_prepare_gb300.inputs import make_inputs
+from gpu_helpers import STAGE_TOL, dev, io_name, rel_frob, scaled_err
+
+pytestmark = pytest.mark.gpu
+
+# (B, T, H, K, V, C): several chunks per head, odd head counts, K != V, both chunk sizes
+SHAPES = [(2, 256, 3, 64, 64, 64), (1, 192, 2, 128, 128, 64), (2, 128, 3, 64, 128, 32),
+          (1, 160, 1, 128, 64, 32), (1, 256, 2, 128, 128, 32), (2, 128, 1, 64, 64, 32)]
+# variants that run the staged entry points, with the io dtypes each one takes
+STAGE_VARIANTS = {"simt": (torch.float32, torch.bfloat16)}
+
+
+def cases():
+    for shape, per_k, (variant, dtypes) in itertools.product(SHAPES, (False, True), STAGE_VARIANTS.items()):
+        for dt in dtypes:
+            yield pytest.param(shape, per_k, variant, dt,
+                               id=f"{'x'.join(map(str, shape))}-{'kda' if per_k else 'gdn'}-{variant}-{io_name(dt)}")
+
+
+def rounded(a, dtype):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dtype)
+
+
+@pytest.mark.parametrize("shape,per_k,variant,dtype", list(cases()))
+def test_prepare_stage(shape, per_k, variant, dtype):
+    B, T, H, K, V, C = shape
+    x = make_inputs(B, T, H, K, V, per_k_gate=per_k, io_dtype=dtype, with_h0=False, seed=1)
+    p = gdr.problem_for(x.q, x.v, x.g, C, variant=variant)
+    k, v, g, beta = (dev(t) for t in (x.k, x.v, x.g, x.beta))
+    w = torch.full_like(k, float("nan"))
+    u = torch.full_like(v, float("nan"))
+    g_cum = torch.full_like(g, float("nan"))
+    gdr.gdr_prepare_wy(p, k, v, g, beta, w, u, g_cum)
+    torch.cuda.synchronize()
+    assert gdr.gdr_last_variant() == variant
+    ref = chunked.prepare_wy(x.k, x.v, x.g, x.beta, C)
+    io = io_name(dtype)
+    assert scaled_err(g_cum, ref["G"]) <= 1e-6
+    assert scaled_err(w, ref["w"]) <= STAGE_TOL[io]
+    assert scaled_err(u, ref["u"]) <= STAGE_TOL[io]
+
+
+@pytest.mark.parametrize("shape,per_k,variant,dtype", list(cases()))
+@pytest.mark.parametrize("with_h0", [False, True])
+def test_scan_stage(shape, per_k, variant, dtype, with_h0):
+    B, T, H, K, V, C = shape
+    x = make_inputs(B, T, H, K, V, per_k_gate=per_k, io_dtype=dtype, with_h0=with_h0, seed=2)
+    pre = chunked.prepare_wy(x.k, x.v, x.g, x.beta, C)
+    w_r, u_r = rounded(pre["w"], dtype), rounded(pre["u"], dtype)
+    G_r = rounded(pre["G"], torch.float32)
+    h0 = None if x.h0 is None else x.h0 * 20          # a state large enough to matter
+    ref = chunked.scan_h(x.k, w_r, u_r, G_r, h0, C)
+    p = gdr.problem_for(x.q, x.v, x.g, C, variant=variant)
+    NT = T // C
+    h_ckpt = torch.full((B, NT, H, K, V), float("nan"), device="cuda", dtype=dtype)
+    v_new = torch.full((B, T, H, V), float("nan"), device="cuda", dtype=dtype)
+    h_final = torch.full((B, H, K, V), float("nan"), device="cuda", dtype=torch.float32)
+    gdr.gdr_scan_h(p, dev(x.k), dev(w_r), dev(u_r), dev(G_r), dev(h0), h_ckpt, v_new, h_final)
+    torch.cuda.synchronize()
+    assert gdr.gdr_last_variant() == variant
+    io = io_name(dtype)
+    assert scaled_err(v_new, ref["v_new"]) <= STAGE_TOL[io]
+    assert scaled_err(h_ckpt, ref["ckpt"]) <= STAGE_TOL[io]
+    assert rel_frob(h_final, ref["h_final"]) <= STAGE_TOL[io]
+    if h0 is None:
+        assert float(h_ckpt[:, 0].abs().max()) == 0.0
+    else:
+        assert scaled_err(h_ckpt[:, 0], h0.numpy()) <= STAGE_TOL[io]
+
+
+@pytest.mark.parametrize("shape,per_k,variant,dtype", list(cases()))
+def test_scan_stage_optional_outputs(shape, per_k, variant, dtype):
+    """h_ckpt and h_final may be NULL; v_new must not change when they are."""
+    B, T, H, K, V, C = shape
+    x = make_inputs(B, T, H, K, V, per_k_gate=per_k, io_dtype=dtype, with_h0=True, seed=3)
+    pre = chunked.prepare_wy(x.k, x.v, x.g, x.beta, C)
+    w_r, u_r, G_r = rounded(pre["w"], dtype), rounded(pre["u"], dtype), rounded(pre["G"], torch.float32)
+    p = gdr.problem_for(x.q, x.v, x.g, C, variant=variant)
+    args = (dev(x.k), dev(w_r), dev(u_r), dev(G_r), dev(x.h0))
+    v1 = torch.empty(B, T, H, V, device="cuda", dtype=dtype)
+    v2 = torch.empty_like(v1)
+    hc = torch.empty(B, T // C, H, K, V, device="cuda", dtype=dtype)
+    hf = torch.empty(B, H, K, V, device="cuda", dtype=torch.float32)
+    gdr.gdr_scan_h(p, *args, hc, v1, hf)
+    gdr.gdr_scan_h(p, *args, None, v2, None)
+    torch.cuda.synchronize()
+    assert torch.equal(v1, v2)
+
+
+@pytest.mark.parametrize("shape,per_k,variant,dtype", list(cases()))
+def test_output_stage(shape, per_k, variant, dtype):
+    B, T, H, K, V, C = shape
+    x = make_inputs(B, T, H, K, V, per_k_gate=per_k, io_dtype=dtype, with_h0=True, seed=4)
+    full = chunked.forward_chunked(x.q, x.k, x.v, x.g, x.beta, x.h0 * 20, C, 0.125)
+    vn_r, ck_r = rounded(full["v_new"], dtype), rounded(full["ckpt"], dtype)
+    G_r = rounded(full["G"], torch.float32)
+    ref = chunked.chunk_output(x.q, x.k, vn_r, ck_r, G_r, C, 0.125)
+    p = gdr.problem_for(x.q, x.v, x.g, C, scale=0.125, variant=variant)
+    o = torch.full((B, T, H, V), float("nan"), device="cuda", dtype=dtype)
+    gdr.gdr_chunk_output(p, dev(x.q), dev(x.k), dev(vn_r), dev(ck_r), dev(G_r), o)
+    torch.cuda.synchronize()
+    assert gdr.gdr_last_variant() == variant
+    assert scaled_err(o, ref) <= STAGE_TOL[io_name(dtype)]

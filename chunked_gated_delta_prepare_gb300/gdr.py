@@ -30,6 +30,7 @@ STATUS_NAMES = {0: "GDR_OK", 1: "GDR_ERR_NULL", 2: "GDR_ERR_SHAPE", 3: "GDR_ERR_
 DTYPES = {torch.float32: 0, torch.bfloat16: 1}
 VARIANTS = {"auto": 0, "simt": 1, "tensor": 2, "fused": 3}
 EXPORTS = ["gdr_prepare_wy", "gdr_scan_h", "gdr_chunk_output", "gdr_forward", "gdr_forward_workspace_bytes",
+           "gdr_forward_static_scratch",
            "gdr_status_string", "gdr_get_device_status", "gdr_last_variant", "gdr_version"]
 
 
@@ -66,6 +67,7 @@ def load(path: str | None = None):
             "gdr_scan_h": [P, vp, vp, vp, vp, vp, vp, vp, vp, vp],
             "gdr_chunk_output": [P, vp, vp, vp, vp, vp, vp, vp],
             "gdr_forward": [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp],
+            "gdr_forward_static_scratch": [P, vp, vp, vp, vp, vp, vp, vp, vp, vp],
             "gdr_forward_workspace_bytes": [P],
             "gdr_status_string": [ctypes.c_int],
             "gdr_get_device_status": [vp],
@@ -151,6 +153,17 @@ def gdr_forward(p, q, k, v, g, beta, h0, o, h_final, workspace, workspace_bytes,
     _check(load().gdr_forward(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(o),
                               _ptr(h_final), _ptr(workspace), int(workspace_bytes), _stream(stream)),
            "gdr_forward")
+
+
+def gdr_forward_static_scratch(p, q, k, v, g, beta, h0, o, h_final, stream=None):
+    """gdr_forward with the scratch taken from the library's fixed device array
+    (for callers that cannot allocate device memory; see include/gdr.h)."""
+    _check(load().gdr_forward_static_scratch(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                             _ptr(h0), _ptr(o), _ptr(h_final), _stream(stream)),
+           "gdr_forward_static_scratch")
+
+
+STATIC_SCRATCH_BYTES = 64 << 20
 
 
 def gdr_status_string(status: int) -> str:

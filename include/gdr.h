@@ -159,6 +159,33 @@ GDR_API gdr_status gdr_forward(const gdr_problem* p, const void* q, const void* 
                        const float* g, const void* beta, const float* h0, void* o,
                        float* h_final, void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * gdr_forward without a workspace argument, for callers that cannot allocate
+ * device memory themselves (for example a plugin whose host framework owns all
+ * device memory, or a latency-critical loop that must not call cudaMalloc).
+ * The method pages have no counterpart to this call; it is a deployment aid.
+ *
+ * It runs the staged forward (variant AUTO runs the fp32 CUDA-core stages;
+ * SIMT and TENSOR are honoured; FUSED returns GDR_ERR_UNSUPPORTED since that
+ * kernel needs no scratch -- call gdr_forward for it) and takes the scratch from
+ * an array of GDR_STATIC_SCRATCH_BYTES compiled into the library.  Arguments and
+ * outputs are those of gdr_forward.
+ * - A problem whose gdr_forward_workspace_bytes exceeds GDR_STATIC_SCRATCH_BYTES
+ *   is rejected with GDR_ERR_WORKSPACE; nothing is launched.
+ * - Every GPU that loads this part of the library holds that array until the
+ *   process exits.
+ * - All calls on a device share the array: calls whose kernels may overlap on
+ *   the GPU (e.g. on unordered streams) race on it.  Issue them in order.
+ * - The array keeps the previous call's contents; nothing needs clearing,
+ *   because the stages write every scratch byte before reading it.
+ * - The first call on each device looks up the array's device address with
+ *   that device current; make it before any stream capture starts.
+ */
+#define GDR_STATIC_SCRATCH_BYTES (64ull << 20)
+GDR_API gdr_status gdr_forward_static_scratch(const gdr_problem* p, const void* q, const void* k, const void* v,
+                                              const float* g, const void* beta, const float* h0, void* o,
+                                              float* h_final, void* stream);
+
 /* Static, human-readable text for a status code. */
 GDR_API const char* gdr_status_string(gdr_status s);
 

@@ -253,7 +253,7 @@ def run_ours(args, wl):
         u = torch.empty_like(v)
         v_new = torch.empty_like(v)
         h_ckpt = torch.empty(B, NT, H, K, V, device=dev, dtype=q.dtype)
-        sp = gdr.problem_for(q, v, g, C, None, variant)
+        sp = gdr.problem_for(q, v, g, C, None, args.variant)
         kernels = ["prepare", "scan", "output"]
 
         def launches():
@@ -268,6 +268,10 @@ def run_ours(args, wl):
             return [lambda: gdr.gdr_forward(p, q, k, v, g, beta, h0, o, hf, ws if nbytes else None, nbytes)]
 
     calls = launches()
+    stage_variant = []
+    for f in calls:
+        f()
+        stage_variant.append(gdr.gdr_last_variant())
     for _ in range(args.warmup):
         flush.fill_(1)
         for f in calls:
@@ -307,9 +311,8 @@ def run_ours(args, wl):
     dom_name = kernels[dom]
     dom_bytes = algorithmic_bytes(wl, dom_name)
     achieved = dom_bytes / (avg_ms[dom] / 1e3) / 1e9
-    kname = {"prepare": "simt_prepare_kernel", "scan": "simt_scan_kernel", "output": "simt_output_kernel",
-             "forward": "fused_forward_kernel"}[dom_name]
-    traffic = traffic_for(f"{variant}:{dom_name}")
+    kname = f"{'tc' if stage_variant[dom] == 'tensor' else stage_variant[dom]}_{dom_name}_kernel"
+    traffic = traffic_for(kname)
 
     # end to end through the public API: pinned host inputs in, o and h_final back to host
     hx = {n_: t.pin_memory() for n_, t in x.tensors().items() if t is not None}
@@ -344,7 +347,7 @@ def run_ours(args, wl):
                          "frac": achieved / hbm_gbs, "peak_source": f"{peak_kind} HBM copy bandwidth",
                          "traffic": traffic, "algorithmic_bytes_per_launch": dom_bytes,
                          "avg_launch_ms": avg_ms[dom]},
-            "kernel_ms": {kernels[i]: avg_ms[i] for i in range(n)},
+            "kernel_ms": {f"{kernels[i]}[{stage_variant[i]}]": avg_ms[i] for i in range(n)},
             "floor_roofline_frac": (algorithmic_bytes(wl, "forward") / (hbm_gbs * 1e9)) / (total_s / args.steps),
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": n * args.steps,

@@ -58,10 +58,42 @@ gdr_status check_ptrs(std::initializer_list<const void*> required, std::initiali
 
 gdr_status from_cuda(cudaError_t e) { return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA; }
 
-// Only the fp32 CUDA-core variant exists for the staged entry points so far.
-gdr_status pick_stage_variant(const gdr_problem* p) {
-    if (p->variant == GDR_VARIANT_AUTO || p->variant == GDR_VARIANT_SIMT) return GDR_OK;
-    return GDR_ERR_UNSUPPORTED;
+enum class Stage { Prepare, Scan, Output };
+
+// Which kernel family runs a stage: tensor cores where a bf16 kernel exists for
+// it (the default for bf16), the fp32 CUDA-core kernels otherwise.
+bool stage_has_tensor(Stage st) { return st == Stage::Prepare; }
+
+gdr_status pick_stage(const gdr_problem* p, const gdr::Dims& d, Stage st, bool* tensor) {
+    switch (p->variant) {
+        case GDR_VARIANT_SIMT: *tensor = false; return GDR_OK;
+        case GDR_VARIANT_TENSOR:
+            if (!d.bf16 || !stage_has_tensor(st)) return GDR_ERR_UNSUPPORTED;
+            *tensor = true;
+            return GDR_OK;
+        case GDR_VARIANT_AUTO: *tensor = d.bf16 && stage_has_tensor(st); return GDR_OK;
+        default: return GDR_ERR_UNSUPPORTED;
+    }
+}
+
+// Variant a whole forward runs under: "simt" (fp32 CUDA-core kernels for every
+// stage) or "tensor" (bf16 only: each stage on its tensor-core kernel where one
+// exists, on the CUDA-core kernel otherwise).
+gdr_status pick_forward(const gdr_problem* p, const gdr::Dims& d, bool* tensor) {
+    switch (p->variant) {
+        case GDR_VARIANT_SIMT: *tensor = false; return GDR_OK;
+        case GDR_VARIANT_TENSOR:
+            if (!d.bf16) return GDR_ERR_UNSUPPORTED;
+            *tensor = true;
+            return GDR_OK;
+        case GDR_VARIANT_AUTO: *tensor = d.bf16 != 0; return GDR_OK;
+        default: return GDR_ERR_UNSUPPORTED;
+    }
+}
+
+unsigned int* device_error_word() {
+    unsigned int* p = nullptr;
+    return gdr::device_error_ptr(&p) == cudaSuccess ? p : nullptr;
 }
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -95,9 +127,12 @@ gdr_status gdr_prepare_wy(const gdr_problem* p, const void* k, const void* v, co
     gdr_status st = check_problem(p, &d);
     if (st != GDR_OK) return st;
     if ((st = check_ptrs({k, v, g, beta, w, u, g_cum}, {})) != GDR_OK) return st;
-    if ((st = pick_stage_variant(p)) != GDR_OK) return st;
-    st = from_cuda(gdr::simt_prepare(d, k, v, g, beta, w, u, g_cum, (cudaStream_t)stream));
-    if (st == GDR_OK) t_last_variant = "simt";
+    bool tensor = false;
+    if ((st = pick_stage(p, d, Stage::Prepare, &tensor)) != GDR_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    st = from_cuda(tensor ? gdr::tc_prepare(d, k, v, g, beta, w, u, g_cum, s, device_error_word())
+                          : gdr::simt_prepare(d, k, v, g, beta, w, u, g_cum, s));
+    if (st == GDR_OK) t_last_variant = tensor ? "tensor" : "simt";
     return st;
 }
 
@@ -107,9 +142,10 @@ gdr_status gdr_scan_h(const gdr_problem* p, const void* k, const void* w, const 
     gdr_status st = check_problem(p, &d);
     if (st != GDR_OK) return st;
     if ((st = check_ptrs({k, w, u, g_cum, v_new}, {h0, h_ckpt, h_final})) != GDR_OK) return st;
-    if ((st = pick_stage_variant(p)) != GDR_OK) return st;
+    bool tensor = false;
+    if ((st = pick_stage(p, d, Stage::Scan, &tensor)) != GDR_OK) return st;
     st = from_cuda(gdr::simt_scan(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, (cudaStream_t)stream));
-    if (st == GDR_OK) t_last_variant = "simt";
+    if (st == GDR_OK) t_last_variant = tensor ? "tensor" : "simt";
     return st;
 }
 
@@ -119,16 +155,18 @@ gdr_status gdr_chunk_output(const gdr_problem* p, const void* q, const void* k, 
     gdr_status st = check_problem(p, &d);
     if (st != GDR_OK) return st;
     if ((st = check_ptrs({q, k, v_new, h_ckpt, g_cum, o}, {})) != GDR_OK) return st;
-    if ((st = pick_stage_variant(p)) != GDR_OK) return st;
+    bool tensor = false;
+    if ((st = pick_stage(p, d, Stage::Output, &tensor)) != GDR_OK) return st;
     st = from_cuda(gdr::simt_output(d, q, k, v_new, h_ckpt, g_cum, o, (cudaStream_t)stream));
-    if (st == GDR_OK) t_last_variant = "simt";
+    if (st == GDR_OK) t_last_variant = tensor ? "tensor" : "simt";
     return st;
 }
 
 size_t gdr_forward_workspace_bytes(const gdr_problem* p) {
     gdr::Dims d;
     if (check_problem(p, &d) != GDR_OK) return 0;
-    if (pick_stage_variant(p) != GDR_OK) return 0;
+    bool tensor = false;
+    if (pick_forward(p, d, &tensor) != GDR_OK) return 0;
     return plan_staged(d).total;
 }
 
@@ -139,7 +177,8 @@ gdr_status gdr_forward(const gdr_problem* p, const void* q, const void* k, const
     gdr_status st = check_problem(p, &d);
     if (st != GDR_OK) return st;
     if ((st = check_ptrs({q, k, v, g, beta, o}, {h0, h_final})) != GDR_OK) return st;
-    if ((st = pick_stage_variant(p)) != GDR_OK) return st;
+    bool tensor = false;
+    if ((st = pick_forward(p, d, &tensor)) != GDR_OK) return st;
     const StagedWorkspace ws = plan_staged(d);
     if (!workspace || workspace_bytes < ws.total) return GDR_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GDR_ERR_ALIGN;
@@ -150,10 +189,15 @@ gdr_status gdr_forward(const gdr_problem* p, const void* q, const void* k, const
     void* v_new = base + ws.v_new;
     void* h_ckpt = base + ws.h_ckpt;
     cudaStream_t s = (cudaStream_t)stream;
-    if ((st = from_cuda(gdr::simt_prepare(d, k, v, g, beta, w, u, g_cum, s))) != GDR_OK) return st;
+    unsigned int* err = tensor ? device_error_word() : nullptr;
+    if (tensor && stage_has_tensor(Stage::Prepare))
+        st = from_cuda(gdr::tc_prepare(d, k, v, g, beta, w, u, g_cum, s, err));
+    else
+        st = from_cuda(gdr::simt_prepare(d, k, v, g, beta, w, u, g_cum, s));
+    if (st != GDR_OK) return st;
     if ((st = from_cuda(gdr::simt_scan(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, s))) != GDR_OK) return st;
     if ((st = from_cuda(gdr::simt_output(d, q, k, v_new, h_ckpt, g_cum, o, s))) != GDR_OK) return st;
-    t_last_variant = "simt";
+    t_last_variant = tensor ? "tensor" : "simt";
     return GDR_OK;
 }
 

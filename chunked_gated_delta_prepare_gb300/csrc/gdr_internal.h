@@ -25,6 +25,10 @@ cudaError_t simt_scan(const Dims& d, const void* k, const void* w, const void* u
 cudaError_t simt_output(const Dims& d, const void* q, const void* k, const void* v_new, const void* h_ckpt,
                         const float* g_cum, void* o, cudaStream_t s);
 
+// ---- tensor-core kernels (bf16 io only)
+cudaError_t tc_prepare(const Dims& d, const void* k, const void* v, const float* g, const void* beta, void* w,
+                       void* u, float* g_cum, cudaStream_t s, unsigned int* err);
+
 // ---- device error word (device_status.cu)
 // Bounded waits in kernels write a nonzero code here instead of trapping.
 cudaError_t read_and_clear_device_error(unsigned int* code);

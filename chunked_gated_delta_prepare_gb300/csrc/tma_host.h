@@ -1,0 +1,19 @@
+// Host helpers that build TMA descriptors for the library's tensor layouts.
+#pragma once
+
+#include <cuda.h>
+#include <stdint.h>
+
+namespace gdr {
+
+// Generic 4-D bf16 map with 128-byte swizzle (box[0] * 2 bytes must be <= 128).
+bool make_tmap_bf16_4d(CUtensorMap* map, const void* base, const uint64_t dims[4], const uint64_t strides_bytes[3],
+                       const uint32_t box[4]);
+
+// [B,T,H,D] bf16 token tensor; box = 64 columns (of D) x `rows` tokens of one (b, h).
+bool make_tmap_tokens(CUtensorMap* map, const void* base, int B, int T, int H, int D, int rows);
+
+// [B,NT,H,K,V] bf16 checkpoints; box = 64 columns (of V) x all K rows of one (b, c, h).
+bool make_tmap_ckpt(CUtensorMap* map, const void* base, int B, int NT, int H, int K, int V);
+
+}  // namespace gdr

@@ -14,7 +14,7 @@ from gpu_helpers import (H_TOL, O_TOL, all_pairs, check_forward, gpu_forward, io
 pytestmark = pytest.mark.gpu
 
 # every variant gdr_forward offers, with the io dtypes it takes
-FORWARD_VARIANTS = {"simt": (torch.float32, torch.bfloat16)}
+FORWARD_VARIANTS = {"simt": (torch.float32, torch.bfloat16), "tensor": (torch.bfloat16,)}
 SHAPES = [(2, 256, 3, 64, 64, 64), (1, 192, 2, 128, 128, 64), (2, 128, 3, 64, 128, 32),
           (1, 160, 1, 128, 64, 32), (1, 64, 2, 128, 128, 64), (1, 32, 1, 64, 64, 32)]
 

@@ -16,22 +16,42 @@ pytestmark = pytest.mark.gpu
 # (B, T, H, K, V, C): several chunks per head, odd head counts, K != V, both chunk sizes
 SHAPES = [(2, 256, 3, 64, 64, 64), (1, 192, 2, 128, 128, 64), (2, 128, 3, 64, 128, 32),
           (1, 160, 1, 128, 64, 32), (1, 256, 2, 128, 128, 32), (2, 128, 1, 64, 64, 32)]
-# variants that run the staged entry points, with the io dtypes each one takes
-STAGE_VARIANTS = {"simt": (torch.float32, torch.bfloat16)}
+# per stage: the variants that run it, with the io dtypes each one takes
+BOTH = (torch.float32, torch.bfloat16)
+STAGE_VARIANTS = {
+    "prepare": {"simt": BOTH, "tensor": (torch.bfloat16,)},
+    "scan": {"simt": BOTH},
+    "output": {"simt": BOTH},
+}
 
 
-def cases():
-    for shape, per_k, (variant, dtypes) in itertools.product(SHAPES, (False, True), STAGE_VARIANTS.items()):
+def cases(stage):
+    for shape, per_k, (variant, dtypes) in itertools.product(SHAPES, (False, True), STAGE_VARIANTS[stage].items()):
         for dt in dtypes:
             yield pytest.param(shape, per_k, variant, dt,
                                id=f"{'x'.join(map(str, shape))}-{'kda' if per_k else 'gdn'}-{variant}-{io_name(dt)}")
+
+
+@pytest.mark.parametrize("stage", ["scan", "output"])
+def test_tensor_variant_refused_where_no_tensor_kernel(stage):
+    x = make_inputs(1, 64, 1, 64, 64, io_dtype=torch.bfloat16)
+    if "tensor" in STAGE_VARIANTS[stage]:
+        pytest.skip("stage has a tensor-core kernel")
+    p = gdr.problem_for(x.q, x.v, x.g, 64, variant="tensor")
+    t = torch.zeros(64, 1, 64, device="cuda", dtype=torch.bfloat16)
+    with pytest.raises(gdr.GdrError) as e:
+        if stage == "scan":
+            gdr.gdr_scan_h(p, t, t, t, t, None, None, t, None)
+        else:
+            gdr.gdr_chunk_output(p, t, t, t, t, t, t)
+    assert e.value.status == 8
 
 
 def rounded(a, dtype):
     return torch.from_numpy(np.ascontiguousarray(a)).to(dtype)
 
 
-@pytest.mark.parametrize("shape,per_k,variant,dtype", list(cases()))
+@pytest.mark.parametrize("shape,per_k,variant,dtype", list(cases("prepare")))
 def test_prepare_stage(shape, per_k, variant, dtype):
     B, T, H, K, V, C = shape
     x = make_inputs(B, T, H, K, V, per_k_gate=per_k, io_dtype=dtype, with_h0=False, seed=1)
@@ -50,7 +70,7 @@ def test_prepare_stage(shape, per_k, variant, dtype):
     assert scaled_err(u, ref["u"]) <= STAGE_TOL[io]
 
 
-@pytest.mark.parametrize("shape,per_k,variant,dtype", list(cases()))
+@pytest.mark.parametrize("shape,per_k,variant,dtype", list(cases("scan")))
 @pytest.mark.parametrize("with_h0", [False, True])
 def test_scan_stage(shape, per_k, variant, dtype, with_h0):
     B, T, H, K, V, C = shape
@@ -78,7 +98,7 @@ def test_scan_stage(shape, per_k, variant, dtype, with_h0):
         assert scaled_err(h_ckpt[:, 0], h0.numpy()) <= STAGE_TOL[io]
 
 
-@pytest.mark.parametrize("shape,per_k,variant,dtype", list(cases()))
+@pytest.mark.parametrize("shape,per_k,variant,dtype", list(cases("scan")))
 def test_scan_stage_optional_outputs(shape, per_k, variant, dtype):
     """h_ckpt and h_final may be NULL; v_new must not change when they are."""
     B, T, H, K, V, C = shape
@@ -97,7 +117,7 @@ def test_scan_stage_optional_outputs(shape, per_k, variant, dtype):
     assert torch.equal(v1, v2)
 
 
-@pytest.mark.parametrize("shape,per_k,variant,dtype", list(cases()))
+@pytest.mark.parametrize("shape,per_k,variant,dtype", list(cases("output")))
 def test_output_stage(shape, per_k, variant, dtype):
     B, T, H, K, V, C = shape
     x = make_inputs(B, T, H, K, V, per_k_gate=per_k, io_dtype=dtype, with_h0=True, seed=4)

@@ -62,7 +62,7 @@ enum class Stage { Prepare, Scan, Output };
 
 // Which kernel family runs a stage: tensor cores where a bf16 kernel exists for
 // it (the default for bf16), the fp32 CUDA-core kernels otherwise.
-bool stage_has_tensor(Stage st) { return st == Stage::Prepare; }
+bool stage_has_tensor(Stage) { return true; }
 
 gdr_status pick_stage(const gdr_problem* p, const gdr::Dims& d, Stage st, bool* tensor) {
     switch (p->variant) {
@@ -144,7 +144,9 @@ gdr_status gdr_scan_h(const gdr_problem* p, const void* k, const void* w, const 
     if ((st = check_ptrs({k, w, u, g_cum, v_new}, {h0, h_ckpt, h_final})) != GDR_OK) return st;
     bool tensor = false;
     if ((st = pick_stage(p, d, Stage::Scan, &tensor)) != GDR_OK) return st;
-    st = from_cuda(gdr::simt_scan(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, (cudaStream_t)stream));
+    cudaStream_t s = (cudaStream_t)stream;
+    st = from_cuda(tensor ? gdr::tc_scan(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, s, device_error_word())
+                          : gdr::simt_scan(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, s));
     if (st == GDR_OK) t_last_variant = tensor ? "tensor" : "simt";
     return st;
 }
@@ -157,7 +159,9 @@ gdr_status gdr_chunk_output(const gdr_problem* p, const void* q, const void* k, 
     if ((st = check_ptrs({q, k, v_new, h_ckpt, g_cum, o}, {})) != GDR_OK) return st;
     bool tensor = false;
     if ((st = pick_stage(p, d, Stage::Output, &tensor)) != GDR_OK) return st;
-    st = from_cuda(gdr::simt_output(d, q, k, v_new, h_ckpt, g_cum, o, (cudaStream_t)stream));
+    cudaStream_t s = (cudaStream_t)stream;
+    st = from_cuda(tensor ? gdr::tc_output(d, q, k, v_new, h_ckpt, g_cum, o, s, device_error_word())
+                          : gdr::simt_output(d, q, k, v_new, h_ckpt, g_cum, o, s));
     if (st == GDR_OK) t_last_variant = tensor ? "tensor" : "simt";
     return st;
 }
@@ -195,8 +199,16 @@ gdr_status gdr_forward(const gdr_problem* p, const void* q, const void* k, const
     else
         st = from_cuda(gdr::simt_prepare(d, k, v, g, beta, w, u, g_cum, s));
     if (st != GDR_OK) return st;
-    if ((st = from_cuda(gdr::simt_scan(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, s))) != GDR_OK) return st;
-    if ((st = from_cuda(gdr::simt_output(d, q, k, v_new, h_ckpt, g_cum, o, s))) != GDR_OK) return st;
+    if (tensor && stage_has_tensor(Stage::Scan))
+        st = from_cuda(gdr::tc_scan(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, s, err));
+    else
+        st = from_cuda(gdr::simt_scan(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, s));
+    if (st != GDR_OK) return st;
+    if (tensor && stage_has_tensor(Stage::Output))
+        st = from_cuda(gdr::tc_output(d, q, k, v_new, h_ckpt, g_cum, o, s, err));
+    else
+        st = from_cuda(gdr::simt_output(d, q, k, v_new, h_ckpt, g_cum, o, s));
+    if (st != GDR_OK) return st;
     t_last_variant = tensor ? "tensor" : "simt";
     return GDR_OK;
 }

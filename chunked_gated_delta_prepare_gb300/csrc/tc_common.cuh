@@ -37,6 +37,18 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kk) {
     return bw::sdesc_sw128(tile + (uint32_t)(kk * 2048), 8192, 1024);
 }
 
+// The same layouts for a tile of any row count (multiple of 8): atoms are
+// [rows][64] and `rows * 128` bytes apart.
+__device__ __forceinline__ uint32_t tile_off_r(int r, int c, int rows) {
+    return (uint32_t)((c >> 6) * rows * 128) + bw::sw128_offset(r, c & 63);
+}
+__device__ __forceinline__ uint64_t desc_kmajor_r(uint32_t tile, int kk, int rows) {
+    return bw::sdesc_sw128(tile + (uint32_t)((kk >> 2) * rows * 128 + (kk & 3) * 32), 16, 1024);
+}
+__device__ __forceinline__ uint64_t desc_mnmajor_r(uint32_t tile, int kk, int rows) {
+    return bw::sdesc_sw128(tile + (uint32_t)(kk * 2048), (uint32_t)(rows * 128), 1024);
+}
+
 // (I + A)^{-1} for the block-diagonal, strictly lower A of a 64-row tile made of
 // 64/C chunks of C rows (C = 32 or 64).  A and X are fp32 [64][kLd]; X gets the
 // inverse inside each chunk's diagonal block and zeros elsewhere.  R is scratch
@@ -75,9 +87,14 @@ __device__ __forceinline__ void solve_unit_lower(const float* __restrict__ A, fl
             const int p = idx >> 8, e = idx & 255, a = e >> 4, c = e & 15;
             const int ch = p / per_chunk, bi = L + p % per_chunk, bj = bi - L;
             const int ri = ch * C + bi * 16 + a, cj = ch * C + bj * 16 + c;
-            float s = 0.f;
-            for (int m = ch * C + bj * 16; m < ch * C + bi * 16; ++m) s += A[ri * kLd + m] * X[m * kLd + cj];
-            R[p * 272 + a * 17 + c] = s;
+            const int m0 = ch * C + bj * 16;            // the sum runs over L * 16 rows m0 .. m0 + 16L - 1
+            float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+            for (int mm = 0; mm < L * 16; mm += 2) {
+                s0 += A[ri * kLd + m0 + mm] * X[(m0 + mm) * kLd + cj];
+                s1 += A[ri * kLd + m0 + mm + 1] * X[(m0 + mm + 1) * kLd + cj];
+            }
+            R[p * 272 + a * 17 + c] = s0 + s1;
         }
         __syncthreads();
         for (int idx = tid; idx < n; idx += 128) {

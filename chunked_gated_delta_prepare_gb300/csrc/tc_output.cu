@@ -1,0 +1,308 @@
+// Tensor-core chunk output for bf16 io:
+//     o = scale * [ (q * exp(G)) h_c + tril_0(Q~) v' ],   Q~_ij = sum_d q_id k_jd exp(G_id - G_jd)
+// (the output assembly that the re-scan page, "kernel_fun/kda/_kernels/bwd_scan.py",
+// says the forward's epilogue warps performed).
+//
+// One CTA of 128 threads per 64-token tile of one (batch, head), all V columns:
+//   TMA      q, k [64 x K], v' [64 x V], checkpoint(s) h_c [K x V]
+//   MMA 1    S = q k^T                      (M=64, N=64; gated copies for a per-key-dim gate)
+//   SIMT     P = tril_0(S * exp(G_i - G_j)) -> bf16;  q <- q * exp(G) in place
+//   MMA 2    D = (q exp(G)) h_c             (B = checkpoint, MN-major; with C = 32 the
+//                                            tile holds two chunks, each with its own h_c)
+//   MMA 3    D += P v'                      (B = v', MN-major)
+//   SIMT     o = scale * D -> bf16 -> global
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "blackwell.cuh"
+#include "gdr_internal.h"
+#include "tc_common.cuh"
+#include "tma_host.h"
+
+namespace gdr {
+namespace {
+
+using bf16 = __nv_bfloat16;
+using namespace tc;
+
+constexpr float kExpClamp = 60.f;
+constexpr float kExpSafe = 40.f;
+
+template <int K, int V, int C, bool PER_K>
+struct OutLayout {
+    static constexpr int NCH = kTile / C;                          // chunks per tile
+    static constexpr int GW = PER_K ? K : 1;
+    static constexpr uint32_t Q = 0;                               // q, then q exp(G) for chunk 0
+    static constexpr uint32_t Kt = Q + K * 128;
+    static constexpr uint32_t VP = Kt + K * 128;                   // v' [64][V]
+    static constexpr uint32_t Hc = VP + V * 128;                   // checkpoints [NCH][K][V]
+    static constexpr uint32_t P = Hc + NCH * K * V * 2;            // P [64][64]
+    static constexpr uint32_t Q1 = P + 8192;                       // C = 32: q exp(G) for chunk 1
+    static constexpr uint32_t Qa = Q1 + (NCH > 1 ? K * 128 : 0);   // per-key-dim gate: gated copies
+    static constexpr uint32_t Kb = Qa + (PER_K ? K * 128 : 0);
+    static constexpr uint32_t F = Kb + (PER_K ? K * 128 : 0);      // fp32: G [64][GW], flag
+    static constexpr uint32_t bytes = F + 4 * (kTile * GW + 4);
+    static constexpr uint32_t tx = 2 * K * 128 + V * 128 + NCH * K * V * 2;
+    static constexpr uint32_t tmem_cols = 256;                     // S at 0 (64 cols), D at 64 (V cols)
+};
+
+template <int K, int V, int C, bool PER_K>
+__global__ void __launch_bounds__(128, 1)
+tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                 const __grid_constant__ CUtensorMap mvp, const __grid_constant__ CUtensorMap mh,
+                 const float* __restrict__ g_cum, bf16* __restrict__ o, int T, int H, int NT, float scale,
+                 unsigned int* err) {
+    using L = OutLayout<K, V, C, PER_K>;
+    constexpr int GW = L::GW;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float* sG = reinterpret_cast<float*>(sm + L::F);
+    int* sFlag = reinterpret_cast<int*>(sG + kTile * GW);
+    __shared__ uint64_t bar_tma, bar_mma;
+    __shared__ uint32_t tslot;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int t0 = blockIdx.x * kTile, h = blockIdx.y, b = blockIdx.z;
+    const int nvalid = min(kTile, T - t0);
+    auto row = [&](int t) -> int64_t { return ((int64_t)b * T + t0 + t) * H + h; };
+    const uint32_t s_base = bw::smem_u32(sm);
+
+    if (tid == 0) {
+        bw::mbar_init(&bar_tma, 1);
+        bw::mbar_init(&bar_mma, 1);
+        bw::fence_mbar_init();
+        *sFlag = 0;
+    }
+    if (warp == 0) {
+        bw::tmem_alloc(&tslot, L::tmem_cols);
+        bw::tmem_relinquish();
+    }
+    __syncthreads();
+    bw::tc_fence_after();
+    const uint32_t tmem = tslot;
+
+    if (tid == 0) {
+        const int nch = (nvalid + C - 1) / C;   // checkpoints that exist for this tile
+        bw::mbar_arrive_expect_tx(&bar_tma, 2 * K * 128 + V * 128 + nch * K * V * 2);
+#pragma unroll
+        for (int a = 0; a < K / 64; ++a) {
+            bw::tma_load_4d(sm + L::Q + a * 8192, &mq, &bar_tma, a * 64, h, t0, b);
+            bw::tma_load_4d(sm + L::Kt + a * 8192, &mk, &bar_tma, a * 64, h, t0, b);
+        }
+#pragma unroll
+        for (int a = 0; a < V / 64; ++a) bw::tma_load_4d(sm + L::VP + a * 8192, &mvp, &bar_tma, a * 64, h, t0, b);
+        for (int ch = 0; ch < nch; ++ch) {
+            const int c = t0 / C + ch;
+#pragma unroll
+            for (int a = 0; a < V / 64; ++a)
+                bw::tma_load_4d(sm + L::Hc + ch * K * V * 2 + a * K * 128, &mh, &bar_tma, a * 64, 0, h, b * NT + c);
+        }
+    }
+    for (int i = tid; i < kTile * GW; i += 128) {
+        const int t = i / GW;
+        sG[i] = t < nvalid ? g_cum[row(t) * GW + i % GW] : 0.f;
+    }
+    if (L::NCH > 1 && nvalid <= C) {
+        // a half tile: the second chunk's checkpoint is absent; give its rows a zero state
+        for (int i = tid; i < K * V / 8; i += 128)
+            *reinterpret_cast<uint4*>(sm + L::Hc + K * V * 2 + i * 16) = make_uint4(0, 0, 0, 0);
+    }
+    __syncthreads();
+    bool ok = bw::mbar_wait(&bar_tma, 0, err, kDeviceErrTimeout);
+
+    if (PER_K) {
+        for (int i = tid; i < kTile * (K / 8); i += 128) {
+            const int r = i / (K / 8), lc = i % (K / 8);
+            const int ref = (r / C) * C + C / 2;
+            const uint32_t off = (uint32_t)((lc >> 3) * 8192 + r * 128 + (((lc & 7) ^ (r & 7)) << 4));
+            const uint4 rq = *reinterpret_cast<const uint4*>(sm + L::Q + off);
+            const uint4 rk = *reinterpret_cast<const uint4*>(sm + L::Kt + off);
+            const bf16* qv = reinterpret_cast<const bf16*>(&rq);
+            const bf16* kv = reinterpret_cast<const bf16*>(&rk);
+            float fa[8], fb[8];
+            bool big = false;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int d = lc * 8 + e;
+                const float dg = sG[r * K + d] - sG[ref * K + d];
+                big |= fabsf(dg) > kExpSafe;
+                fa[e] = __bfloat162float(qv[e]) * __expf(fminf(fmaxf(dg, -kExpClamp), kExpClamp));
+                fb[e] = __bfloat162float(kv[e]) * __expf(fminf(fmaxf(-dg, -kExpClamp), kExpClamp));
+            }
+            if (big) *sFlag = 1;
+            uint4 pa, pb;
+            pa.x = bw::pack_bf16(fa[0], fa[1]); pa.y = bw::pack_bf16(fa[2], fa[3]);
+            pa.z = bw::pack_bf16(fa[4], fa[5]); pa.w = bw::pack_bf16(fa[6], fa[7]);
+            pb.x = bw::pack_bf16(fb[0], fb[1]); pb.y = bw::pack_bf16(fb[2], fb[3]);
+            pb.z = bw::pack_bf16(fb[4], fb[5]); pb.w = bw::pack_bf16(fb[6], fb[7]);
+            *reinterpret_cast<uint4*>(sm + L::Qa + off) = pa;
+            *reinterpret_cast<uint4*>(sm + L::Kb + off) = pb;
+        }
+        bw::fence_async_shared();
+    }
+    __syncthreads();
+
+    // MMA 1: S = q k^T
+    if (tid == 0 && ok) {
+        bw::tc_fence_after();
+        constexpr uint32_t idesc = bw::idesc_bf16(64, 64, 0, 0);
+        const uint32_t a_t = s_base + (PER_K ? L::Qa : L::Q);
+        const uint32_t b_t = s_base + (PER_K ? L::Kb : L::Kt);
+#pragma unroll
+        for (int kk = 0; kk < K / 16; ++kk) bw::mma_bf16(tmem, desc_kmajor(a_t, kk), desc_kmajor(b_t, kk), idesc, kk > 0);
+        bw::mma_commit(&bar_mma);
+    }
+    ok = ok && bw::mbar_wait(&bar_mma, 0, err, kDeviceErrTimeout);
+    bw::tc_fence_after();
+
+    // P = tril_0(S * gate) -> bf16 K-major [64][64]
+    {
+        const int r = m64_row(warp, lane);
+        float s[64];
+#pragma unroll
+        for (int c0 = 0; c0 < 64; c0 += 16) bw::tmem_ld16(tmem_at(tmem, warp, c0), s + c0);
+        bw::tmem_ld_wait();
+        if (r >= 0) {
+            const int ch0 = (r / C) * C;
+#pragma unroll
+            for (int j = 0; j < 64; j += 8) {
+                float pv[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int jj = j + e;
+                    float x = 0.f;
+                    if (jj >= ch0 && jj <= r) x = PER_K ? s[jj] : s[jj] * __expf(sG[r] - sG[jj]);
+                    pv[e] = x;
+                }
+                uint4 p;
+                p.x = bw::pack_bf16(pv[0], pv[1]); p.y = bw::pack_bf16(pv[2], pv[3]);
+                p.z = bw::pack_bf16(pv[4], pv[5]); p.w = bw::pack_bf16(pv[6], pv[7]);
+                *reinterpret_cast<uint4*>(sm + L::P + bw::sw128_offset(r, j)) = p;
+            }
+        }
+    }
+    bw::tc_fence_before();
+    __syncthreads();
+    if (PER_K && *sFlag) {
+        // exact fp32 P for chunks with extreme gates
+        for (int idx = tid; idx < kTile * kTile; idx += 128) {
+            const int i = idx / kTile, j = idx % kTile;
+            if (j >= (i / C) * C && j <= i) {
+                float acc = 0.f;
+                for (int d = 0; d < K; ++d) {
+                    const float qi = __bfloat162float(*reinterpret_cast<const bf16*>(sm + L::Q + tile_off(i, d)));
+                    const float kj = __bfloat162float(*reinterpret_cast<const bf16*>(sm + L::Kt + tile_off(j, d)));
+                    acc += qi * kj * __expf(sG[i * K + d] - sG[j * K + d]);
+                }
+                *reinterpret_cast<bf16*>(sm + L::P + bw::sw128_offset(i, j)) = __float2bfloat16_rn(acc);
+            }
+        }
+        __syncthreads();
+    }
+    // q exp(G) in place (and, for two chunks per tile, split by chunk into Q and Q1)
+    for (int i = tid; i < kTile * (K / 8); i += 128) {
+        const int r = i / (K / 8), lc = i % (K / 8);
+        const uint32_t off = (uint32_t)((lc >> 3) * 8192 + r * 128 + (((lc & 7) ^ (r & 7)) << 4));
+        const uint4 raw = *reinterpret_cast<const uint4*>(sm + L::Q + off);
+        const bf16* qv = reinterpret_cast<const bf16*>(&raw);
+        float f[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = __bfloat162float(qv[e]) * __expf(PER_K ? sG[r * K + lc * 8 + e] : sG[r]);
+        uint4 p;
+        p.x = bw::pack_bf16(f[0], f[1]); p.y = bw::pack_bf16(f[2], f[3]);
+        p.z = bw::pack_bf16(f[4], f[5]); p.w = bw::pack_bf16(f[6], f[7]);
+        const uint4 zero = make_uint4(0, 0, 0, 0);
+        if (L::NCH > 1) {
+            const bool first = r < C;
+            *reinterpret_cast<uint4*>(sm + L::Q + off) = first ? p : zero;
+            *reinterpret_cast<uint4*>(sm + L::Q1 + off) = first ? zero : p;
+        } else {
+            *reinterpret_cast<uint4*>(sm + L::Q + off) = p;
+        }
+    }
+    bw::fence_async_shared();
+    __syncthreads();
+
+    // MMA 2, 3: D = (q exp(G)) h_c + P v'
+    if (tid == 0 && ok) {
+        bw::tc_fence_after();
+        constexpr uint32_t idesc = bw::idesc_bf16(64, V, 0, 1);
+        const uint32_t d_t = tmem + 64;
+#pragma unroll
+        for (int ch = 0; ch < L::NCH; ++ch) {
+            const uint32_t a_t = s_base + (ch == 0 ? L::Q : L::Q1);
+            const uint32_t b_t = s_base + L::Hc + ch * K * V * 2;
+#pragma unroll
+            for (int kk = 0; kk < K / 16; ++kk)
+                bw::mma_bf16(d_t, desc_kmajor(a_t, kk), desc_mnmajor_r(b_t, kk, K), idesc, (ch > 0 || kk > 0));
+        }
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            bw::mma_bf16(d_t, desc_kmajor(s_base + L::P, kk), desc_mnmajor(s_base + L::VP, kk), idesc, 1);
+        bw::mma_commit(&bar_mma);
+    }
+    ok = ok && bw::mbar_wait(&bar_mma, 1, err, kDeviceErrTimeout);
+    bw::tc_fence_after();
+    {
+        const int r = m64_row(warp, lane);
+        const bool store = r >= 0 && r < nvalid && ok;
+        bf16* orow = o + (store ? row(r) * V : 0);
+#pragma unroll
+        for (int c0 = 0; c0 < V; c0 += 16) {
+            float v16[16];
+            bw::tmem_ld16(tmem_at(tmem, warp, 64 + c0), v16);
+            bw::tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v16[e] *= scale;
+            if (store) store_bf16x16(orow + c0, v16);
+        }
+    }
+    bw::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) bw::tmem_dealloc(tmem, L::tmem_cols);
+}
+
+template <int K, int V, int C, bool PER_K>
+cudaError_t launch_output(const Dims& d, const void* q, const void* k, const void* v_new, const void* h_ckpt,
+                          const float* g_cum, void* o, cudaStream_t s, unsigned int* err) {
+    using L = OutLayout<K, V, C, PER_K>;
+    CUtensorMap mq, mk, mvp, mh;
+    if (!make_tmap_tokens(&mq, q, d.B, d.T, d.H, K, kTile) || !make_tmap_tokens(&mk, k, d.B, d.T, d.H, K, kTile) ||
+        !make_tmap_tokens(&mvp, v_new, d.B, d.T, d.H, V, kTile) || !make_tmap_ckpt(&mh, h_ckpt, d.B, d.NT, d.H, K, V))
+        return cudaErrorInvalidValue;
+    auto kern = tc_output_kernel<K, V, C, PER_K>;
+    const size_t smem = L::bytes + 1024;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const dim3 grid((d.T + kTile - 1) / kTile, d.H, d.B);
+    kern<<<grid, 128, smem, s>>>(mq, mk, mvp, mh, g_cum, (bf16*)o, d.T, d.H, d.NT, d.scale, err);
+    return cudaGetLastError();
+}
+
+template <int K, int V, int C>
+cudaError_t out_gate(const Dims& d, const void* q, const void* k, const void* v_new, const void* h_ckpt,
+                     const float* g_cum, void* o, cudaStream_t s, unsigned int* err) {
+    return d.per_k ? launch_output<K, V, C, true>(d, q, k, v_new, h_ckpt, g_cum, o, s, err)
+                   : launch_output<K, V, C, false>(d, q, k, v_new, h_ckpt, g_cum, o, s, err);
+}
+
+template <int K, int V>
+cudaError_t out_chunk(const Dims& d, const void* q, const void* k, const void* v_new, const void* h_ckpt,
+                      const float* g_cum, void* o, cudaStream_t s, unsigned int* err) {
+    return d.C == 32 ? out_gate<K, V, 32>(d, q, k, v_new, h_ckpt, g_cum, o, s, err)
+                     : out_gate<K, V, 64>(d, q, k, v_new, h_ckpt, g_cum, o, s, err);
+}
+
+}  // namespace
+
+cudaError_t tc_output(const Dims& d, const void* q, const void* k, const void* v_new, const void* h_ckpt,
+                      const float* g_cum, void* o, cudaStream_t s, unsigned int* err) {
+    if (!d.bf16) return cudaErrorInvalidValue;
+    if (d.K == 64 && d.V == 64) return out_chunk<64, 64>(d, q, k, v_new, h_ckpt, g_cum, o, s, err);
+    if (d.K == 64) return out_chunk<64, 128>(d, q, k, v_new, h_ckpt, g_cum, o, s, err);
+    if (d.V == 64) return out_chunk<128, 64>(d, q, k, v_new, h_ckpt, g_cum, o, s, err);
+    return out_chunk<128, 128>(d, q, k, v_new, h_ckpt, g_cum, o, s, err);
+}
+
+}  // namespace gdr

@@ -267,18 +267,24 @@ tc_prepare_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant_
         bf16* wrow = w + (store ? row(r) * K : 0);
         bf16* urow = u + (store ? row(r) * V : 0);
 #pragma unroll
-        for (int c0 = 0; c0 < K; c0 += 16) {
-            float v16[16];
-            bw::tmem_ld16(tmem_at(tmem, warp, c0), v16);
+        for (int c0 = 0; c0 < K; c0 += 64) {
+            float v64[64];
+            bw::tmem_ld32(tmem_at(tmem, warp, c0), v64);
+            bw::tmem_ld32(tmem_at(tmem, warp, c0 + 32), v64 + 32);
             bw::tmem_ld_wait();
-            if (store) store_bf16x16(wrow + c0, v16);
+            if (store)
+#pragma unroll
+                for (int j = 0; j < 64; j += 16) store_bf16x16(wrow + c0 + j, v64 + j);
         }
 #pragma unroll
-        for (int c0 = 0; c0 < V; c0 += 16) {
-            float v16[16];
-            bw::tmem_ld16(tmem_at(tmem, warp, K + c0), v16);
+        for (int c0 = 0; c0 < V; c0 += 64) {
+            float v64[64];
+            bw::tmem_ld32(tmem_at(tmem, warp, K + c0), v64);
+            bw::tmem_ld32(tmem_at(tmem, warp, K + c0 + 32), v64 + 32);
             bw::tmem_ld_wait();
-            if (store) store_bf16x16(urow + c0, v16);
+            if (store)
+#pragma unroll
+                for (int j = 0; j < 64; j += 16) store_bf16x16(urow + c0 + j, v64 + j);
         }
     }
     bw::tc_fence_before();

@@ -20,8 +20,8 @@ SHAPES = [(2, 256, 3, 64, 64, 64), (1, 192, 2, 128, 128, 64), (2, 128, 3, 64, 12
 BOTH = (torch.float32, torch.bfloat16)
 STAGE_VARIANTS = {
     "prepare": {"simt": BOTH, "tensor": (torch.bfloat16,)},
-    "scan": {"simt": BOTH},
-    "output": {"simt": BOTH},
+    "scan": {"simt": BOTH, "tensor": (torch.bfloat16,)},
+    "output": {"simt": BOTH, "tensor": (torch.bfloat16,)},
 }
 
 

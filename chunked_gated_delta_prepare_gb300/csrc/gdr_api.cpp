@@ -145,7 +145,7 @@ gdr_status gdr_scan_h(const gdr_problem* p, const void* k, const void* w, const 
     bool tensor = false;
     if ((st = pick_stage(p, d, Stage::Scan, &tensor)) != GDR_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
-    st = from_cuda(tensor ? gdr::tc_scan(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, s, device_error_word())
+    st = from_cuda(tensor ? gdr::mma_scan(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, s, device_error_word())
                           : gdr::simt_scan(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, s));
     if (st == GDR_OK) t_last_variant = tensor ? "tensor" : "simt";
     return st;
@@ -200,7 +200,7 @@ gdr_status gdr_forward(const gdr_problem* p, const void* q, const void* k, const
         st = from_cuda(gdr::simt_prepare(d, k, v, g, beta, w, u, g_cum, s));
     if (st != GDR_OK) return st;
     if (tensor && stage_has_tensor(Stage::Scan))
-        st = from_cuda(gdr::tc_scan(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, s, err));
+        st = from_cuda(gdr::mma_scan(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, s, err));
     else
         st = from_cuda(gdr::simt_scan(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, s));
     if (st != GDR_OK) return st;

@@ -27,6 +27,11 @@ void fetch_encoder() {
 
 bool make_tmap_bf16_4d(CUtensorMap* map, const void* base, const uint64_t dims[4], const uint64_t strides_bytes[3],
                        const uint32_t box[4]) {
+    return make_tmap_bf16_4d_swz(map, base, dims, strides_bytes, box, true);
+}
+
+bool make_tmap_bf16_4d_swz(CUtensorMap* map, const void* base, const uint64_t dims[4],
+                           const uint64_t strides_bytes[3], const uint32_t box[4], bool swizzle128) {
     std::call_once(g_once, fetch_encoder);
     if (!g_encode) return false;
     cuuint64_t gd[4] = {dims[0], dims[1], dims[2], dims[3]};
@@ -34,7 +39,8 @@ bool make_tmap_bf16_4d(CUtensorMap* map, const void* base, const uint64_t dims[4
     cuuint32_t bx[4] = {box[0], box[1], box[2], box[3]};
     cuuint32_t es[4] = {1, 1, 1, 1};
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), gd, gs, bx, es,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -54,6 +60,21 @@ bool make_tmap_ckpt(CUtensorMap* map, const void* base, int B, int NT, int H, in
     const uint64_t st[3] = {(uint64_t)V * 2, (uint64_t)K * V * 2, (uint64_t)H * K * V * 2};
     const uint32_t box[4] = {64, (uint32_t)K, 1, 1};
     return make_tmap_bf16_4d(map, base, dims, st, box);
+}
+
+// Unswizzled variants: box = `cols` columns (cols * 2 bytes, a multiple of 16) x `rows`.
+bool make_tmap_tokens_plain(CUtensorMap* map, const void* base, int B, int T, int H, int D, int cols, int rows) {
+    const uint64_t dims[4] = {(uint64_t)D, (uint64_t)H, (uint64_t)T, (uint64_t)B};
+    const uint64_t st[3] = {(uint64_t)D * 2, (uint64_t)H * D * 2, (uint64_t)T * H * D * 2};
+    const uint32_t box[4] = {(uint32_t)cols, 1, (uint32_t)rows, 1};
+    return make_tmap_bf16_4d_swz(map, base, dims, st, box, false);
+}
+
+bool make_tmap_ckpt_plain(CUtensorMap* map, const void* base, int B, int NT, int H, int K, int V, int cols) {
+    const uint64_t dims[4] = {(uint64_t)V, (uint64_t)K, (uint64_t)H, (uint64_t)B * NT};
+    const uint64_t st[3] = {(uint64_t)V * 2, (uint64_t)K * V * 2, (uint64_t)H * K * V * 2};
+    const uint32_t box[4] = {(uint32_t)cols, (uint32_t)K, 1, 1};
+    return make_tmap_bf16_4d_swz(map, base, dims, st, box, false);
 }
 
 }  // namespace gdr

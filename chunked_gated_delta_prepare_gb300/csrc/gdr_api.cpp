@@ -130,7 +130,7 @@ gdr_status gdr_prepare_wy(const gdr_problem* p, const void* k, const void* v, co
     bool tensor = false;
     if ((st = pick_stage(p, d, Stage::Prepare, &tensor)) != GDR_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
-    st = from_cuda(tensor ? gdr::tc_prepare(d, k, v, g, beta, w, u, g_cum, s, device_error_word())
+    st = from_cuda(tensor ? gdr::mma_prepare(d, k, v, g, beta, w, u, g_cum, s, device_error_word())
                           : gdr::simt_prepare(d, k, v, g, beta, w, u, g_cum, s));
     if (st == GDR_OK) t_last_variant = tensor ? "tensor" : "simt";
     return st;
@@ -195,7 +195,7 @@ gdr_status gdr_forward(const gdr_problem* p, const void* q, const void* k, const
     cudaStream_t s = (cudaStream_t)stream;
     unsigned int* err = tensor ? device_error_word() : nullptr;
     if (tensor && stage_has_tensor(Stage::Prepare))
-        st = from_cuda(gdr::tc_prepare(d, k, v, g, beta, w, u, g_cum, s, err));
+        st = from_cuda(gdr::mma_prepare(d, k, v, g, beta, w, u, g_cum, s, err));
     else
         st = from_cuda(gdr::simt_prepare(d, k, v, g, beta, w, u, g_cum, s));
     if (st != GDR_OK) return st;

@@ -26,8 +26,8 @@ cudaError_t simt_output(const Dims& d, const void* q, const void* k, const void*
                         const float* g_cum, void* o, cudaStream_t s);
 
 // ---- tensor-core kernels (bf16 io only)
-cudaError_t tc_prepare(const Dims& d, const void* k, const void* v, const float* g, const void* beta, void* w,
-                       void* u, float* g_cum, cudaStream_t s, unsigned int* err);
+cudaError_t mma_prepare(const Dims& d, const void* k, const void* v, const float* g, const void* beta, void* w,
+                        void* u, float* g_cum, cudaStream_t s, unsigned int* err);
 // the scan's recurrence runs on mma.sync (register-resident), see scan_mma.cu
 cudaError_t mma_scan(const Dims& d, const void* k, const void* w, const void* u, const float* g_cum, const float* h0,
                      void* h_ckpt, void* v_new, float* h_final, cudaStream_t s, unsigned int* err);

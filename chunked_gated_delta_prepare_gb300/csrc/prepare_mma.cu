@@ -1,21 +1,24 @@
-// Tensor-core WY prepare for bf16 io ("Reuse P as beta tiles in gated deltanet
-// fused prepare": the gated A, its inverse, w and u per chunk).
+// WY prepare for bf16 io ("Reuse P as beta tiles in gated deltanet fused
+// prepare": the gated A, its inverse, w and u per chunk).
 //
 // One CTA of 128 threads per 64-token tile of one (batch, head): one chunk when
-// C = 64, two when C = 32 (kept apart by the block-diagonal structure).
+// C = 64, two when C = 32 (kept apart by the block-diagonal structure).  Warp w
+// owns tile rows 16w .. 16w+15 of every product.
 //
 //   TMA      k [64 x K], v [64 x V]  -> shared memory (128-byte swizzle)
 //   SIMT     G = chunk-local cumsum of g (written out as g_cum), beta
-//   MMA 1    S = k k^T            (M=64, N=64; per-key-dim gate: gated copies
-//                                  k*exp(G-G_ref) and k*exp(G_ref-G), G_ref the
-//                                  chunk's middle row, keep every factor bounded)
+//   mma      S = k k^T            (per-key-dim gate: gated copies k*exp(G-G_ref)
+//                                  and k*exp(G_ref-G), G_ref the chunk's middle row,
+//                                  keep every factor bounded)
 //   SIMT     A_ij = beta_i S_ij exp(G_i - G_j) (i > j, same chunk), X = (I+A)^{-1}
-//            by blocked forward substitution in fp32, Tb = X diag(beta) in bf16
-//   MMA 2,3  w = Tb (k * exp(G)),  u = Tb v      (M=64, N=K and N=V, MN-major B)
-//   SIMT     TMEM -> bf16 -> global
+//            by blocked forward substitution in fp32
+//   mma      w = (X diag(beta)) (k * exp(G)),  u = (X diag(beta)) v
 //
-// beta is folded into the columns of X, so the k and v tiles feed the MMAs as
-// TMA left them (for the scalar gate k is row-scaled by exp(G) in place).
+// The products are warp-level mma.sync m16n8k16 (bf16 in, fp32 accumulate) fed
+// by ldmatrix from the swizzled tiles: at these sizes (64 x 64 x 128 and
+// 64 x 128 x 64 per tile) a tcgen05 MMA's fixed ~240-cycle cost per K=16 step
+// makes it slower than mma.sync, and without tensor memory more CTAs fit an SM.
+// beta is folded into the columns of X, so v feeds the MMA as TMA left it.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -24,6 +27,7 @@
 #include "gdr_internal.h"
 #include "tc_common.cuh"
 #include "tma_host.h"
+#include "warp_mma.cuh"
 
 namespace gdr {
 namespace {
@@ -36,8 +40,7 @@ struct PrepLayout {
     static constexpr int GW = PER_K ? K : 1;
     static constexpr uint32_t kK = 0;                               // k tile [64][K]
     static constexpr uint32_t kV = kK + K * 128;                    // v tile [64][V]
-    static constexpr uint32_t kT = kV + V * 128;                    // Tb [64][64]
-    static constexpr uint32_t kKa = kT + 8192;                      // KDA: gated k copies
+    static constexpr uint32_t kKa = kV + V * 128;                   // KDA: gated k copies
     static constexpr uint32_t kKb = kKa + (PER_K ? K * 128 : 0);
     static constexpr uint32_t kF = kKb + (PER_K ? K * 128 : 0);     // fp32 region
     // fp32 arrays (float offsets from kF)
@@ -50,8 +53,6 @@ struct PrepLayout {
     static constexpr int fFlag = fR + 3 * 272;           // KDA: exact-path flag
     static constexpr int nF = fFlag + 4;
     static constexpr uint32_t bytes = kF + 4 * nF;
-    static constexpr uint32_t tmem_cols = 256;
-    static_assert(K + V <= 256, "w and u accumulators must fit 256 TMEM columns");
 };
 
 // Exponents of the gated k copies are clamped here; a chunk whose gate moves
@@ -60,8 +61,8 @@ constexpr float kExpClamp = 60.f;
 constexpr float kExpSafe = 40.f;
 
 template <int K, int V, int C, bool PER_K>
-__global__ void __launch_bounds__(128, 1)
-tc_prepare_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
+__global__ void __launch_bounds__(128, 3)
+prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
                   const float* __restrict__ g, const bf16* __restrict__ beta, bf16* __restrict__ w,
                   bf16* __restrict__ u, float* __restrict__ g_cum, int T, int H, unsigned int* err) {
     using L = PrepLayout<K, V, C, PER_K>;
@@ -76,8 +77,7 @@ tc_prepare_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant_
     float* sX = F + L::fX;
     float* sR = F + L::fR;
     int* sFlag = reinterpret_cast<int*>(F + L::fFlag);
-    __shared__ uint64_t bar_tma, bar_mma;
-    __shared__ uint32_t tslot;
+    __shared__ uint64_t bar_tma;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int t0 = blockIdx.x * kTile, h = blockIdx.y, b = blockIdx.z;
@@ -87,17 +87,10 @@ tc_prepare_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant_
 
     if (tid == 0) {
         bw::mbar_init(&bar_tma, 1);
-        bw::mbar_init(&bar_mma, 1);
         bw::fence_mbar_init();
         *sFlag = 0;
     }
-    if (warp == 0) {
-        bw::tmem_alloc(&tslot, L::tmem_cols);
-        bw::tmem_relinquish();
-    }
     __syncthreads();
-    bw::tc_fence_after();
-    const uint32_t tmem = tslot;
 
     if (tid == 0) {
         bw::mbar_arrive_expect_tx(&bar_tma, (K + V) * 128);
@@ -168,38 +161,44 @@ tc_prepare_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant_
     }
     __syncthreads();
 
-    // MMA 1: S = k k^T  (M = 64 rows, N = 64 rows, contraction over K)
-    if (tid == 0 && ok) {
-        bw::tc_fence_after();
-        constexpr uint32_t idesc = bw::idesc_bf16(64, 64, 0, 0);
+    const int g4 = lane >> 2, q4 = lane & 3, mi = lane >> 3, mr = lane & 7;
+    const int i0 = warp * 16 + g4, i1 = i0 + 8;       // the two tile rows of this thread's fragments
+    // S = k k^T for this warp's 16 rows: [16 x 64]
+    {
         const uint32_t a_t = s_base + (PER_K ? L::kKa : L::kK);
         const uint32_t b_t = s_base + (PER_K ? L::kKb : L::kK);
+        float S[8][4];
 #pragma unroll
-        for (int kk = 0; kk < K / 16; ++kk) bw::mma_bf16(tmem, desc_kmajor(a_t, kk), desc_kmajor(b_t, kk), idesc, kk > 0);
-        bw::mma_commit(&bar_mma);
-    }
-    ok = ok && bw::mbar_wait(&bar_mma, 0, err, kDeviceErrTimeout);
-    bw::tc_fence_after();
-
-    // A from S (rows owned by lanes 0..15 of each warp)
-    {
-        const int r = m64_row(warp, lane);
-        float s[64];
+        for (int j = 0; j < 8; ++j) S[j][0] = S[j][1] = S[j][2] = S[j][3] = 0.f;
 #pragma unroll
-        for (int c0 = 0; c0 < 64; c0 += 16) bw::tmem_ld16(tmem_at(tmem, warp, c0), s + c0);
-        bw::tmem_ld_wait();
-        if (r >= 0) {
-            const int ch0 = (r / C) * C;
-            const float br = sB[r];
+        for (int kk = 0; kk < K / 16; ++kk) {
+            uint32_t a[4];
+            wm::ldsm_x4(a_t + tile_off(warp * 16 + 8 * (mi & 1) + mr, 16 * kk + 8 * (mi >> 1)), a);
 #pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                float a = 0.f;
-                if (j >= ch0 && j < r) a = PER_K ? br * s[j] : br * s[j] * __expf(sG[r] - sG[j]);
-                sA[r * kLd + j] = a;
+            for (int jp = 0; jp < 8; jp += 2) {
+                uint32_t bfr[4];
+                wm::ldsm_x4(b_t + tile_off(8 * jp + 8 * (mi >> 1) + mr, 16 * kk + 8 * (mi & 1)), bfr);
+                wm::mma16816(S[jp], a, bfr[0], bfr[1]);
+                wm::mma16816(S[jp + 1], a, bfr[2], bfr[3]);
+            }
+        }
+        // A from S: element (i, j) of this thread's fragments
+        const int c0 = (i0 / C) * C;                 // i0 and i1 share a chunk (16-row blocks never straddle one)
+        const float b0 = sB[i0], b1 = sB[i1];
+#pragma unroll
+        for (int jn = 0; jn < 8; ++jn) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int j = 8 * jn + 2 * q4 + e;
+                const bool in = j >= c0;
+                float a0 = 0.f, a1 = 0.f;
+                if (in && j < i0) a0 = PER_K ? b0 * S[jn][e] : b0 * S[jn][e] * __expf(sG[i0] - sG[j]);
+                if (in && j < i1) a1 = PER_K ? b1 * S[jn][2 + e] : b1 * S[jn][2 + e] * __expf(sG[i1] - sG[j]);
+                sA[i0 * kLd + j] = a0;
+                sA[i1 * kLd + j] = a1;
             }
         }
     }
-    bw::tc_fence_before();
     __syncthreads();
     if (PER_K && *sFlag) {
         // exact fp32 A for chunks with extreme gates: A_ij = beta_i sum_d k_id k_jd exp(G_id - G_jd)
@@ -235,61 +234,50 @@ tc_prepare_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant_
 
     solve_unit_lower<C>(sA, sX, sR, tid);
 
-    // Tb = X diag(beta) -> bf16 K-major A operand [64][64]
-    for (int idx = tid; idx < kTile * kTile; idx += 128) {
-        const int i = idx >> 6, j = idx & 63;
-        *reinterpret_cast<bf16*>(sm + L::kT + bw::sw128_offset(i, j)) = __float2bfloat16_rn(sX[i * kLd + j] * sB[j]);
+    // Tb = X diag(beta) as A fragments of this warp's 16 rows (4 k-tiles of 16 tokens)
+    uint32_t ta[4][4];
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+        const int j0 = 16 * kk + 2 * q4, j1 = j0 + 8;
+        const float bj0 = sB[j0], bj0b = sB[j0 + 1], bj1 = sB[j1], bj1b = sB[j1 + 1];
+        ta[kk][0] = wm::pack2(sX[i0 * kLd + j0] * bj0, sX[i0 * kLd + j0 + 1] * bj0b);
+        ta[kk][1] = wm::pack2(sX[i1 * kLd + j0] * bj0, sX[i1 * kLd + j0 + 1] * bj0b);
+        ta[kk][2] = wm::pack2(sX[i0 * kLd + j1] * bj1, sX[i0 * kLd + j1 + 1] * bj1b);
+        ta[kk][3] = wm::pack2(sX[i1 * kLd + j1] * bj1, sX[i1 * kLd + j1 + 1] * bj1b);
     }
-    bw::fence_async_shared();
-    __syncthreads();
-
-    // MMA 2, 3: w = Tb (k exp(G)) -> TMEM [0, K);  u = Tb v -> TMEM [K, K+V)
-    if (tid == 0 && ok) {
-        bw::tc_fence_after();
-        const uint32_t a_t = s_base + L::kT;
-        const uint32_t bw_t = s_base + (PER_K ? L::kKa : L::kK);
-        const uint32_t bv_t = s_base + L::kV;
+    // out[16 x D] = Tb [16 x 64] * B [64 x D], B = k exp(G) or v read token-major by ldmatrix.trans;
+    // bf16 rows straight to global (rows past T are not stored)
+    auto product_store = [&](uint32_t b_t, bf16* out, int D) {
+        const bool st0 = i0 < nvalid, st1 = i1 < nvalid;
+        bf16* r0 = out + row(st0 ? i0 : 0) * D;
+        bf16* r1 = out + row(st1 ? i1 : 0) * D;
+#pragma unroll 1
+        for (int n0 = 0; n0 < D; n0 += 64) {
+            float acc[8][4];
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-            bw::mma_bf16(tmem, desc_kmajor(a_t, kk), desc_mnmajor(bw_t, kk), bw::idesc_bf16(64, K, 0, 1), kk > 0);
+            for (int j = 0; j < 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-            bw::mma_bf16(tmem + K, desc_kmajor(a_t, kk), desc_mnmajor(bv_t, kk), bw::idesc_bf16(64, V, 0, 1), kk > 0);
-        bw::mma_commit(&bar_mma);
-    }
-    ok = ok && bw::mbar_wait(&bar_mma, 1, err, kDeviceErrTimeout);
-    bw::tc_fence_after();
-
-    // epilogue: w and u rows to global
-    {
-        const int r = m64_row(warp, lane);
-        const bool store = r >= 0 && r < nvalid && ok;
-        bf16* wrow = w + (store ? row(r) * K : 0);
-        bf16* urow = u + (store ? row(r) * V : 0);
+            for (int kk = 0; kk < 4; ++kk) {
 #pragma unroll
-        for (int c0 = 0; c0 < K; c0 += 64) {
-            float v64[64];
-            bw::tmem_ld32(tmem_at(tmem, warp, c0), v64);
-            bw::tmem_ld32(tmem_at(tmem, warp, c0 + 32), v64 + 32);
-            bw::tmem_ld_wait();
-            if (store)
+                for (int jp = 0; jp < 8; jp += 2) {
+                    uint32_t bfr[4];
+                    wm::ldsm_x4_t(b_t + tile_off(16 * kk + 8 * (mi & 1) + mr, n0 + 8 * jp + 8 * (mi >> 1)), bfr);
+                    wm::mma16816(acc[jp], ta[kk], bfr[0], bfr[1]);
+                    wm::mma16816(acc[jp + 1], ta[kk], bfr[2], bfr[3]);
+                }
+            }
+            if (ok) {
 #pragma unroll
-                for (int j = 0; j < 64; j += 16) store_bf16x16(wrow + c0 + j, v64 + j);
+                for (int j = 0; j < 8; ++j) {
+                    const int col = n0 + 8 * j + 2 * q4;
+                    if (st0) *reinterpret_cast<uint32_t*>(r0 + col) = wm::pack2(acc[j][0], acc[j][1]);
+                    if (st1) *reinterpret_cast<uint32_t*>(r1 + col) = wm::pack2(acc[j][2], acc[j][3]);
+                }
+            }
         }
-#pragma unroll
-        for (int c0 = 0; c0 < V; c0 += 64) {
-            float v64[64];
-            bw::tmem_ld32(tmem_at(tmem, warp, K + c0), v64);
-            bw::tmem_ld32(tmem_at(tmem, warp, K + c0 + 32), v64 + 32);
-            bw::tmem_ld_wait();
-            if (store)
-#pragma unroll
-                for (int j = 0; j < 64; j += 16) store_bf16x16(urow + c0 + j, v64 + j);
-        }
-    }
-    bw::tc_fence_before();
-    __syncthreads();
-    if (warp == 0) bw::tmem_dealloc(tmem, L::tmem_cols);
+    };
+    product_store(s_base + (PER_K ? L::kKa : L::kK), w, K);
+    product_store(s_base + L::kV, u, V);
 }
 
 template <int K, int V, int C, bool PER_K>
@@ -299,7 +287,7 @@ cudaError_t launch_prepare(const Dims& d, const void* k, const void* v, const fl
     CUtensorMap mk, mv;
     if (!make_tmap_tokens(&mk, k, d.B, d.T, d.H, K, kTile) || !make_tmap_tokens(&mv, v, d.B, d.T, d.H, V, kTile))
         return cudaErrorInvalidValue;
-    auto kern = tc_prepare_kernel<K, V, C, PER_K>;
+    auto kern = prepare_mma_kernel<K, V, C, PER_K>;
     const size_t smem = L::bytes + 1024;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -324,7 +312,7 @@ cudaError_t pick_chunk(const Dims& d, const void* k, const void* v, const float*
 
 }  // namespace
 
-cudaError_t tc_prepare(const Dims& d, const void* k, const void* v, const float* g, const void* beta, void* w, void* u,
+cudaError_t mma_prepare(const Dims& d, const void* k, const void* v, const float* g, const void* beta, void* w, void* u,
                        float* g_cum, cudaStream_t s, unsigned int* err) {
     if (!d.bf16) return cudaErrorInvalidValue;
     if (d.K == 64 && d.V == 64) return pick_chunk<64, 64>(d, k, v, g, beta, w, u, g_cum, s, err);

@@ -14,8 +14,9 @@
 // and no barrier between the two warps (a tcgen05 MMA costs ~240 SM cycles per
 // K=16 step on this part whatever its shape, which is what this chain cannot afford).
 // Four producer warps stream w and u by TMA and build kg = k exp(G_last - G) and
-// the decay row a chunk ahead into a 2-stage ring; v_new and the checkpoints leave
-// through stmatrix.trans into per-warp staging and TMA stores.
+// the decay row into a 2-stage ring, their global loads two chunks ahead; v_new
+// and the checkpoints leave through stmatrix.trans into per-warp staging and TMA
+// stores.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -94,35 +95,39 @@ scan_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ 
         constexpr int NI = C / RSTEP;
         constexpr int GV = PER_K ? 8 : 1;
         const int lc = pt % LC, r0 = pt / LC;
-        uint4 kr[NI];
-        float gr[NI][GV], gl8[GV];
-        auto load_chunk = [&](int c) {   // all of a chunk's global loads issued together
+        // Two register sets: the global loads of chunk c+2 are in flight while
+        // chunk c+1 is built, so their latency hides behind a whole chunk step.
+        struct Staged {
+            uint4 kr[NI];
+            float gr[NI][GV], gl8[GV];
+        };
+        Staged sa, sb;
+        auto load_chunk = [&](int c, Staged& st) {   // all of a chunk's global loads issued together
             const int t0 = c * C;
             const float* gl = g_cum + row(t0 + C - 1) * GW;
 #pragma unroll
             for (int j = 0; j < NI; ++j) {
                 const int t = r0 + j * RSTEP;
-                kr[j] = *reinterpret_cast<const uint4*>(k + row(t0 + t) * K + lc * 8);
+                st.kr[j] = *reinterpret_cast<const uint4*>(k + row(t0 + t) * K + lc * 8);
                 if constexpr (PER_K) {
                     const float4* gt = reinterpret_cast<const float4*>(g_cum + row(t0 + t) * K + lc * 8);
-                    *reinterpret_cast<float4*>(&gr[j][0]) = gt[0];
-                    *reinterpret_cast<float4*>(&gr[j][4]) = gt[1];
+                    *reinterpret_cast<float4*>(&st.gr[j][0]) = gt[0];
+                    *reinterpret_cast<float4*>(&st.gr[j][4]) = gt[1];
                 } else {
-                    gr[j][0] = g_cum[row(t0 + t)];
+                    st.gr[j][0] = g_cum[row(t0 + t)];
                 }
             }
             if constexpr (PER_K) {
                 const float4* g8 = reinterpret_cast<const float4*>(gl + lc * 8);
-                *reinterpret_cast<float4*>(&gl8[0]) = g8[0];
-                *reinterpret_cast<float4*>(&gl8[4]) = g8[1];
+                *reinterpret_cast<float4*>(&st.gl8[0]) = g8[0];
+                *reinterpret_cast<float4*>(&st.gl8[4]) = g8[1];
             } else {
-                gl8[0] = gl[0];
+                st.gl8[0] = gl[0];
             }
         };
-        if (NT > 0) load_chunk(0);
-        for (int c = 0; c < NT; ++c) {
+        auto produce = [&](int c, const Staged& st) -> bool {
             const int s = c % L::NS;
-            if (!bw::mbar_wait(&empty[s], ((c / L::NS) & 1) ^ 1, err, kDeviceErrTimeout)) break;
+            if (!bw::mbar_wait(&empty[s], ((c / L::NS) & 1) ^ 1, err, kDeviceErrTimeout)) return false;
             const int t0 = c * C;
             if (pt == 0) {
                 bw::mbar_arrive_expect_tx(&full[s], L::tx);
@@ -135,17 +140,17 @@ scan_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ 
                 const float* gl = g_cum + row(t0 + C - 1) * GW;
                 for (int d = pt; d < K; d += kProdThreads) sGL[s * L::GWS + d] = gl[d];
             } else {
-                if (pt == 0) sGL[s * L::GWS] = gl8[0];
+                if (pt == 0) sGL[s * L::GWS] = st.gl8[0];
             }
             unsigned char* kg_t = sm + L::KG + s * L::kKC;
 #pragma unroll
             for (int j = 0; j < NI; ++j) {
                 const int t = r0 + j * RSTEP;
-                const bf16* kv = reinterpret_cast<const bf16*>(&kr[j]);
+                const bf16* kv = reinterpret_cast<const bf16*>(&st.kr[j]);
                 float f[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const float dg = PER_K ? gl8[e % GV] - gr[j][e % GV] : gl8[0] - gr[j][0];
+                    const float dg = PER_K ? st.gl8[e % GV] - st.gr[j][e % GV] : st.gl8[0] - st.gr[j][0];
                     f[e] = __bfloat162float(kv[e]) * __expf(dg);
                 }
                 uint4 p;
@@ -155,7 +160,17 @@ scan_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ 
             }
             bw::fence_async_shared();
             bw::mbar_arrive(&full[s]);
-            if (c + 1 < NT) load_chunk(c + 1);
+            return true;
+        };
+        if (NT > 0) load_chunk(0, sa);
+        if (NT > 1) load_chunk(1, sb);
+        for (int c = 0; c < NT; c += 2) {
+            if (!produce(c, sa)) break;
+            if (c + 2 < NT) load_chunk(c + 2, sa);
+            if (c + 1 < NT) {
+                if (!produce(c + 1, sb)) break;
+                if (c + 3 < NT) load_chunk(c + 3, sb);
+            }
         }
         return;
     }

@@ -56,7 +56,7 @@ extern "C" gdr_status gdr_forward_static_scratch(const gdr_problem* p, const voi
                                                  const float* g, const void* beta, const float* h0, void* o,
                                                  float* h_final, void* stream) {
     if (!p) return GDR_ERR_NULL;
-    if (p->variant == GDR_VARIANT_FUSED) return GDR_ERR_UNSUPPORTED;  // the fused kernel needs no scratch
+    if (p->variant == GDR_VARIANT_FUSED) return GDR_ERR_UNSUPPORTED;  // only the staged variants are offered here
     gdr_problem staged = *p;
     if (staged.variant == GDR_VARIANT_AUTO) staged.variant = GDR_VARIANT_SIMT;
     const size_t need = gdr_forward_workspace_bytes(&staged);

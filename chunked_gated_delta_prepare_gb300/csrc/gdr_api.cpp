@@ -58,31 +58,12 @@ gdr_status check_ptrs(std::initializer_list<const void*> required, std::initiali
 
 gdr_status from_cuda(cudaError_t e) { return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA; }
 
-enum class Stage { Prepare, Scan, Output };
-
-// Which kernel family runs a stage: tensor cores where a bf16 kernel exists for
-// it (the default for bf16), the fp32 CUDA-core kernels otherwise.
-bool stage_has_tensor(Stage) { return true; }
-
-gdr_status pick_stage(const gdr_problem* p, const gdr::Dims& d, Stage st, bool* tensor) {
+// A single stage runs its bf16 tensor-core kernel unless SIMT is asked for.
+gdr_status pick_stage(const gdr_problem* p, const gdr::Dims& d, bool* tensor) {
     switch (p->variant) {
         case GDR_VARIANT_SIMT: *tensor = false; return GDR_OK;
         case GDR_VARIANT_TENSOR:
-            if (!d.bf16 || !stage_has_tensor(st)) return GDR_ERR_UNSUPPORTED;
-            *tensor = true;
-            return GDR_OK;
-        case GDR_VARIANT_AUTO: *tensor = d.bf16 && stage_has_tensor(st); return GDR_OK;
-        default: return GDR_ERR_UNSUPPORTED;
-    }
-}
-
-// Variant a whole forward runs under: "simt" (fp32 CUDA-core kernels for every
-// stage) or "tensor" (bf16 only: each stage on its tensor-core kernel where one
-// exists, on the CUDA-core kernel otherwise).
-gdr_status pick_forward(const gdr_problem* p, const gdr::Dims& d, bool* tensor) {
-    switch (p->variant) {
-        case GDR_VARIANT_SIMT: *tensor = false; return GDR_OK;
-        case GDR_VARIANT_TENSOR:
+        case GDR_VARIANT_FUSED:
             if (!d.bf16) return GDR_ERR_UNSUPPORTED;
             *tensor = true;
             return GDR_OK;
@@ -91,6 +72,31 @@ gdr_status pick_forward(const gdr_problem* p, const gdr::Dims& d, bool* tensor) 
     }
 }
 
+enum class Path { Simt, Tensor, Fused };
+
+// The path a whole forward takes: SIMT (fp32 CUDA-core kernels for every stage),
+// TENSOR (the three bf16 tensor-core stage kernels) or FUSED (the bf16 prepare,
+// then scan and output in one kernel; scalar gate only).
+gdr_status pick_forward(const gdr_problem* p, const gdr::Dims& d, Path* path) {
+    switch (p->variant) {
+        case GDR_VARIANT_SIMT: *path = Path::Simt; return GDR_OK;
+        case GDR_VARIANT_TENSOR:
+            if (!d.bf16) return GDR_ERR_UNSUPPORTED;
+            *path = Path::Tensor;
+            return GDR_OK;
+        case GDR_VARIANT_FUSED:
+            if (!d.bf16 || d.per_k) return GDR_ERR_UNSUPPORTED;
+            *path = Path::Fused;
+            return GDR_OK;
+        case GDR_VARIANT_AUTO:   // the staged tensor-core path measures faster than FUSED today
+            *path = d.bf16 ? Path::Tensor : Path::Simt;
+            return GDR_OK;
+        default: return GDR_ERR_UNSUPPORTED;
+    }
+}
+
+const char* path_name(Path p) { return p == Path::Simt ? "simt" : (p == Path::Tensor ? "tensor" : "fused"); }
+
 unsigned int* device_error_word() {
     unsigned int* p = nullptr;
     return gdr::device_error_ptr(&p) == cudaSuccess ? p : nullptr;
@@ -98,12 +104,12 @@ unsigned int* device_error_word() {
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Staged gdr_forward scratch: g_cum, w, u, v_new, h_ckpt, each 256-byte aligned.
+// gdr_forward scratch: g_cum, w, u and (staged paths) v_new, h_ckpt, each 256-byte aligned.
 struct StagedWorkspace {
     size_t g_cum, w, u, v_new, h_ckpt, total;
 };
 
-StagedWorkspace plan_staged(const gdr::Dims& d) {
+StagedWorkspace plan_staged(const gdr::Dims& d, bool fused) {
     const size_t e = d.bf16 ? 2 : 4;
     const size_t rows = (size_t)d.B * d.T * d.H;
     StagedWorkspace ws;
@@ -111,8 +117,13 @@ StagedWorkspace plan_staged(const gdr::Dims& d) {
     ws.g_cum = off; off = round_up(off + rows * (d.per_k ? d.K : 1) * 4, 256);
     ws.w = off;     off = round_up(off + rows * d.K * e, 256);
     ws.u = off;     off = round_up(off + rows * d.V * e, 256);
-    ws.v_new = off; off = round_up(off + rows * d.V * e, 256);
-    ws.h_ckpt = off; off = round_up(off + (size_t)d.B * d.NT * d.H * d.K * d.V * e, 256);
+    ws.v_new = off;
+    ws.h_ckpt = off;
+    if (!fused) {   // the fused scan/output keeps v' and the checkpoints on chip
+        off = round_up(off + rows * d.V * e, 256);
+        ws.h_ckpt = off;
+        off = round_up(off + (size_t)d.B * d.NT * d.H * d.K * d.V * e, 256);
+    }
     ws.total = off;
     return ws;
 }
@@ -128,7 +139,7 @@ gdr_status gdr_prepare_wy(const gdr_problem* p, const void* k, const void* v, co
     if (st != GDR_OK) return st;
     if ((st = check_ptrs({k, v, g, beta, w, u, g_cum}, {})) != GDR_OK) return st;
     bool tensor = false;
-    if ((st = pick_stage(p, d, Stage::Prepare, &tensor)) != GDR_OK) return st;
+    if ((st = pick_stage(p, d, &tensor)) != GDR_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
     st = from_cuda(tensor ? gdr::mma_prepare(d, k, v, g, beta, w, u, g_cum, s, device_error_word())
                           : gdr::simt_prepare(d, k, v, g, beta, w, u, g_cum, s));
@@ -143,7 +154,7 @@ gdr_status gdr_scan_h(const gdr_problem* p, const void* k, const void* w, const 
     if (st != GDR_OK) return st;
     if ((st = check_ptrs({k, w, u, g_cum, v_new}, {h0, h_ckpt, h_final})) != GDR_OK) return st;
     bool tensor = false;
-    if ((st = pick_stage(p, d, Stage::Scan, &tensor)) != GDR_OK) return st;
+    if ((st = pick_stage(p, d, &tensor)) != GDR_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
     st = from_cuda(tensor ? gdr::mma_scan(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, s, device_error_word())
                           : gdr::simt_scan(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, s));
@@ -158,7 +169,7 @@ gdr_status gdr_chunk_output(const gdr_problem* p, const void* q, const void* k, 
     if (st != GDR_OK) return st;
     if ((st = check_ptrs({q, k, v_new, h_ckpt, g_cum, o}, {})) != GDR_OK) return st;
     bool tensor = false;
-    if ((st = pick_stage(p, d, Stage::Output, &tensor)) != GDR_OK) return st;
+    if ((st = pick_stage(p, d, &tensor)) != GDR_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
     st = from_cuda(tensor ? gdr::tc_output(d, q, k, v_new, h_ckpt, g_cum, o, s, device_error_word())
                           : gdr::simt_output(d, q, k, v_new, h_ckpt, g_cum, o, s));
@@ -169,9 +180,9 @@ gdr_status gdr_chunk_output(const gdr_problem* p, const void* q, const void* k, 
 size_t gdr_forward_workspace_bytes(const gdr_problem* p) {
     gdr::Dims d;
     if (check_problem(p, &d) != GDR_OK) return 0;
-    bool tensor = false;
-    if (pick_forward(p, d, &tensor) != GDR_OK) return 0;
-    return plan_staged(d).total;
+    Path path;
+    if (pick_forward(p, d, &path) != GDR_OK) return 0;
+    return plan_staged(d, path == Path::Fused).total;
 }
 
 gdr_status gdr_forward(const gdr_problem* p, const void* q, const void* k, const void* v, const float* g,
@@ -181,9 +192,9 @@ gdr_status gdr_forward(const gdr_problem* p, const void* q, const void* k, const
     gdr_status st = check_problem(p, &d);
     if (st != GDR_OK) return st;
     if ((st = check_ptrs({q, k, v, g, beta, o}, {h0, h_final})) != GDR_OK) return st;
-    bool tensor = false;
-    if ((st = pick_forward(p, d, &tensor)) != GDR_OK) return st;
-    const StagedWorkspace ws = plan_staged(d);
+    Path path;
+    if ((st = pick_forward(p, d, &path)) != GDR_OK) return st;
+    const StagedWorkspace ws = plan_staged(d, path == Path::Fused);
     if (!workspace || workspace_bytes < ws.total) return GDR_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GDR_ERR_ALIGN;
     char* base = static_cast<char*>(workspace);
@@ -193,24 +204,37 @@ gdr_status gdr_forward(const gdr_problem* p, const void* q, const void* k, const
     void* v_new = base + ws.v_new;
     void* h_ckpt = base + ws.h_ckpt;
     cudaStream_t s = (cudaStream_t)stream;
-    unsigned int* err = tensor ? device_error_word() : nullptr;
-    if (tensor && stage_has_tensor(Stage::Prepare))
-        st = from_cuda(gdr::mma_prepare(d, k, v, g, beta, w, u, g_cum, s, err));
-    else
-        st = from_cuda(gdr::simt_prepare(d, k, v, g, beta, w, u, g_cum, s));
-    if (st != GDR_OK) return st;
-    if (tensor && stage_has_tensor(Stage::Scan))
-        st = from_cuda(gdr::mma_scan(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, s, err));
-    else
-        st = from_cuda(gdr::simt_scan(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, s));
-    if (st != GDR_OK) return st;
-    if (tensor && stage_has_tensor(Stage::Output))
-        st = from_cuda(gdr::tc_output(d, q, k, v_new, h_ckpt, g_cum, o, s, err));
-    else
-        st = from_cuda(gdr::simt_output(d, q, k, v_new, h_ckpt, g_cum, o, s));
-    if (st != GDR_OK) return st;
-    t_last_variant = tensor ? "tensor" : "simt";
+    unsigned int* err = path == Path::Simt ? nullptr : device_error_word();
+    if (path == Path::Simt) {
+        if ((st = from_cuda(gdr::simt_prepare(d, k, v, g, beta, w, u, g_cum, s))) != GDR_OK) return st;
+        if ((st = from_cuda(gdr::simt_scan(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, s))) != GDR_OK) return st;
+        if ((st = from_cuda(gdr::simt_output(d, q, k, v_new, h_ckpt, g_cum, o, s))) != GDR_OK) return st;
+    } else {
+        if ((st = from_cuda(gdr::mma_prepare(d, k, v, g, beta, w, u, g_cum, s, err))) != GDR_OK) return st;
+        if (path == Path::Fused) {
+            if ((st = from_cuda(gdr::mma_scan_output(d, q, k, w, u, g_cum, h0, o, h_final, s, err))) != GDR_OK)
+                return st;
+        } else {
+            if ((st = from_cuda(gdr::mma_scan(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, s, err))) != GDR_OK)
+                return st;
+            if ((st = from_cuda(gdr::tc_output(d, q, k, v_new, h_ckpt, g_cum, o, s, err))) != GDR_OK) return st;
+        }
+    }
+    t_last_variant = path_name(path);
     return GDR_OK;
+}
+
+gdr_status gdr_scan_output(const gdr_problem* p, const void* q, const void* k, const void* w, const void* u,
+                           const float* g_cum, const float* h0, void* o, float* h_final, void* stream) {
+    gdr::Dims d;
+    gdr_status st = check_problem(p, &d);
+    if (st != GDR_OK) return st;
+    if ((st = check_ptrs({q, k, w, u, g_cum, o}, {h0, h_final})) != GDR_OK) return st;
+    if (p->variant == GDR_VARIANT_SIMT || !d.bf16 || d.per_k) return GDR_ERR_UNSUPPORTED;
+    st = from_cuda(gdr::mma_scan_output(d, q, k, w, u, g_cum, h0, o, h_final, (cudaStream_t)stream,
+                                        device_error_word()));
+    if (st == GDR_OK) t_last_variant = "fused";
+    return st;
 }
 
 const char* gdr_status_string(gdr_status s) {

@@ -34,6 +34,11 @@ cudaError_t mma_scan(const Dims& d, const void* k, const void* w, const void* u,
 cudaError_t tc_output(const Dims& d, const void* q, const void* k, const void* v_new, const void* h_ckpt,
                       const float* g_cum, void* o, cudaStream_t s, unsigned int* err);
 
+// scan and output fused (scalar gate, bf16), see fused_mma.cu
+cudaError_t mma_scan_output(const Dims& d, const void* q, const void* k, const void* w, const void* u,
+                            const float* g_cum, const float* h0, void* o, float* h_final, cudaStream_t s,
+                            unsigned int* err);
+
 // ---- device error word (device_status.cu)
 // Bounded waits in kernels write a nonzero code here instead of trapping.
 cudaError_t read_and_clear_device_error(unsigned int* code);

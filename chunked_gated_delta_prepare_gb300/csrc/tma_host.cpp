@@ -32,6 +32,12 @@ bool make_tmap_bf16_4d(CUtensorMap* map, const void* base, const uint64_t dims[4
 
 bool make_tmap_bf16_4d_swz(CUtensorMap* map, const void* base, const uint64_t dims[4],
                            const uint64_t strides_bytes[3], const uint32_t box[4], bool swizzle128) {
+    return make_tmap_bf16_4d_mode(map, base, dims, strides_bytes, box,
+                                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+bool make_tmap_bf16_4d_mode(CUtensorMap* map, const void* base, const uint64_t dims[4],
+                            const uint64_t strides_bytes[3], const uint32_t box[4], CUtensorMapSwizzle swizzle) {
     std::call_once(g_once, fetch_encoder);
     if (!g_encode) return false;
     cuuint64_t gd[4] = {dims[0], dims[1], dims[2], dims[3]};
@@ -39,8 +45,7 @@ bool make_tmap_bf16_4d_swz(CUtensorMap* map, const void* base, const uint64_t di
     cuuint32_t bx[4] = {box[0], box[1], box[2], box[3]};
     cuuint32_t es[4] = {1, 1, 1, 1};
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), gd, gs, bx, es,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -75,6 +80,14 @@ bool make_tmap_ckpt_plain(CUtensorMap* map, const void* base, int B, int NT, int
     const uint64_t st[3] = {(uint64_t)V * 2, (uint64_t)K * V * 2, (uint64_t)H * K * V * 2};
     const uint32_t box[4] = {(uint32_t)cols, (uint32_t)K, 1, 1};
     return make_tmap_bf16_4d_swz(map, base, dims, st, box, false);
+}
+
+// 32-column boxes with the 64-byte swizzle: 16-byte chunk j of row r sits at j ^ ((r >> 1) & 3).
+bool make_tmap_tokens_sw64(CUtensorMap* map, const void* base, int B, int T, int H, int D, int rows) {
+    const uint64_t dims[4] = {(uint64_t)D, (uint64_t)H, (uint64_t)T, (uint64_t)B};
+    const uint64_t st[3] = {(uint64_t)D * 2, (uint64_t)H * D * 2, (uint64_t)T * H * D * 2};
+    const uint32_t box[4] = {32, 1, (uint32_t)rows, 1};
+    return make_tmap_bf16_4d_mode(map, base, dims, st, box, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 }  // namespace gdr

@@ -81,12 +81,14 @@ typedef enum gdr_gate {
     GDR_GATE_PER_K = 1    /* KDA: g [B,T,H,K] */
 } gdr_gate;
 
-/* Which kernels to run.  AUTO picks the fastest variant that supports the problem. */
+/* Which kernels to run.  AUTO picks the fastest measured variant that supports
+ * the problem: TENSOR for bf16 io, SIMT for fp32 io.  The single-stage entry
+ * points run their tensor-core kernel for AUTO, TENSOR and FUSED on bf16 io. */
 typedef enum gdr_variant {
     GDR_VARIANT_AUTO = 0,
     GDR_VARIANT_SIMT = 1,     /* fp32 CUDA-core arithmetic throughout (exact-fp32 path) */
     GDR_VARIANT_TENSOR = 2,   /* staged kernels on the tensor cores (bf16 io only) */
-    GDR_VARIANT_FUSED = 3     /* one fused forward kernel (gdr_forward only; bf16 io only) */
+    GDR_VARIANT_FUSED = 3     /* WY prepare, then scan and output fused (bf16 io, scalar gate) */
 } gdr_variant;
 
 typedef struct gdr_problem {
@@ -140,6 +142,20 @@ GDR_API gdr_status gdr_chunk_output(const gdr_problem* p, const void* q, const v
                             const void* h_ckpt, const float* g_cum, void* o, void* stream);
 
 /*
+ * Stages 2 and 3 fused, for a scalar gate and bf16 io: the state scan of
+ * gdr_scan_h and the chunk output of gdr_chunk_output in one pass, so v' and the
+ * checkpoints never reach device memory.  Per (b, h): h = h0 (zero if NULL); for
+ * each chunk c, v'_c = u_c - w_c h, o_c = scale [ (q exp(G)) h + tril_0(Q~) v'_c ],
+ * h = exp(G_last) h + (k exp(G_last - G))^T v'_c.
+ * Inputs:  q, k, w [B,T,H,K] bf16; u [B,T,H,V] bf16; g_cum [B,T,H] fp32 (the
+ *          chunk-local cumsum, as gdr_prepare_wy writes it); h0 [B,H,K,V] fp32 or NULL.
+ * Outputs: o [B,T,H,V] bf16; h_final [B,H,K,V] fp32 or NULL (not written).
+ * Returns GDR_ERR_UNSUPPORTED for fp32 io or a per-key-dim gate.
+ */
+GDR_API gdr_status gdr_scan_output(const gdr_problem* p, const void* q, const void* k, const void* w, const void* u,
+                                   const float* g_cum, const float* h0, void* o, float* h_final, void* stream);
+
+/*
  * Bytes of device workspace gdr_forward needs for this problem (0 when the
  * variant it would run keeps every intermediate on chip).  Returns 0 for a
  * problem that gdr_forward would reject.
@@ -166,8 +182,8 @@ GDR_API gdr_status gdr_forward(const gdr_problem* p, const void* q, const void* 
  * The method pages have no counterpart to this call; it is a deployment aid.
  *
  * It runs the staged forward (variant AUTO runs the fp32 CUDA-core stages;
- * SIMT and TENSOR are honoured; FUSED returns GDR_ERR_UNSUPPORTED since that
- * kernel needs no scratch -- call gdr_forward for it) and takes the scratch from
+ * SIMT and TENSOR are honoured; FUSED is not offered here and returns
+ * GDR_ERR_UNSUPPORTED -- call gdr_forward for it) and takes the scratch from
  * an array of GDR_STATIC_SCRATCH_BYTES compiled into the library.  Arguments and
  * outputs are those of gdr_forward.
  * - A problem whose gdr_forward_workspace_bytes exceeds GDR_STATIC_SCRATCH_BYTES

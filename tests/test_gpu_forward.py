@@ -14,13 +14,18 @@ from gpu_helpers import (H_TOL, O_TOL, all_pairs, check_forward, gpu_forward, io
 pytestmark = pytest.mark.gpu
 
 # every variant gdr_forward offers, with the io dtypes it takes
-FORWARD_VARIANTS = {"simt": (torch.float32, torch.bfloat16), "tensor": (torch.bfloat16,)}
+FORWARD_VARIANTS = {"simt": (torch.float32, torch.bfloat16), "tensor": (torch.bfloat16,),
+                    "fused": (torch.bfloat16,)}
+# the fused path takes a scalar gate only
+GATES = {"simt": (False, True), "tensor": (False, True), "fused": (False,)}
 SHAPES = [(2, 256, 3, 64, 64, 64), (1, 192, 2, 128, 128, 64), (2, 128, 3, 64, 128, 32),
           (1, 160, 1, 128, 64, 32), (1, 64, 2, 128, 128, 64), (1, 32, 1, 64, 64, 32)]
 
 
 def small_cases():
     for shape, per_k, (variant, dts) in itertools.product(SHAPES, (False, True), FORWARD_VARIANTS.items()):
+        if per_k not in GATES[variant]:
+            continue
         for dt in dts:
             yield pytest.param(shape, per_k, variant, dt,
                                id=f"{'x'.join(map(str, shape))}-{'kda' if per_k else 'gdn'}-{variant}-{io_name(dt)}")
@@ -58,8 +63,8 @@ def test_forward_workload_full_size(wl):
     print(f"{wl.name}: variant={ran} o max-abs {eo:.2e}  h_final rel-F {eh:.2e}")
 
 
-@pytest.mark.parametrize("variant,dtype", [(v, d) for v, ds in FORWARD_VARIANTS.items() for d in ds])
-@pytest.mark.parametrize("per_k", [False, True])
+@pytest.mark.parametrize("variant,dtype,per_k", [(v, d, pk) for v, ds in FORWARD_VARIANTS.items() for d in ds
+                                                  for pk in GATES[v]])
 def test_deterministic_and_exact_scaling(variant, dtype, per_k):
     """Two runs are bitwise equal; scaling (v, h0) by 2 scales (o, h_final) by exactly 2."""
     x = make_inputs(2, 256, 2, 128, 128, per_k_gate=per_k, io_dtype=dtype, with_h0=True, seed=6)
@@ -109,8 +114,8 @@ def _edge_inputs(kind, per_k, dtype):
 
 
 @pytest.mark.parametrize("kind", ["beta_zero", "no_decay", "strong_decay", "single_chunk"])
-@pytest.mark.parametrize("per_k", [False, True])
-@pytest.mark.parametrize("variant,dtype", [(v, d) for v, ds in FORWARD_VARIANTS.items() for d in ds])
+@pytest.mark.parametrize("variant,dtype,per_k", [(v, d, pk) for v, ds in FORWARD_VARIANTS.items() for d in ds
+                                                  for pk in GATES[v]])
 def test_edge_cases(kind, per_k, variant, dtype):
     x = _edge_inputs(kind, per_k, dtype)
     C = 32
@@ -125,6 +130,22 @@ def test_convenience_forward_host_tensors():
     ref = oracle.naive_forward(x.q, x.k, x.v, x.g, x.beta, x.h0, 64, 1 / 8.0, with_ckpt=False)
     assert max_abs(o, ref["o"]) <= O_TOL["bf16"]
     assert rel_frob(hf, ref["h_final"]) <= H_TOL["bf16"]
+
+
+def test_fused_variant_refuses_per_key_gate():
+    x = make_inputs(1, 64, 1, 64, 64, per_k_gate=True, io_dtype=torch.bfloat16, seed=12)
+    with pytest.raises(gdr.GdrError) as e:
+        gpu_forward(x, 64, "fused")
+    assert e.value.status == 8
+
+
+def test_auto_variant_choice():
+    x = make_inputs(1, 128, 2, 64, 64, io_dtype=torch.bfloat16, with_h0=True, seed=13)
+    assert gpu_forward(x, 64, "auto")[2] == "tensor"
+    xk = make_inputs(1, 128, 2, 64, 64, per_k_gate=True, io_dtype=torch.bfloat16, with_h0=True, seed=13)
+    assert gpu_forward(xk, 64, "auto")[2] == "tensor"
+    xf = make_inputs(1, 128, 2, 64, 64, io_dtype=torch.float32, with_h0=True, seed=13)
+    assert gpu_forward(xf, 64, "auto")[2] == "simt"
 
 
 def test_invalid_shape_launches_nothing():

@@ -32,15 +32,15 @@ def cases(stage):
                                id=f"{'x'.join(map(str, shape))}-{'kda' if per_k else 'gdn'}-{variant}-{io_name(dt)}")
 
 
-@pytest.mark.parametrize("stage", ["scan", "output"])
-def test_tensor_variant_refused_where_no_tensor_kernel(stage):
-    x = make_inputs(1, 64, 1, 64, 64, io_dtype=torch.bfloat16)
-    if "tensor" in STAGE_VARIANTS[stage]:
-        pytest.skip("stage has a tensor-core kernel")
+@pytest.mark.parametrize("stage", ["prepare", "scan", "output"])
+def test_tensor_variant_refuses_fp32(stage):
+    x = make_inputs(1, 64, 1, 64, 64, io_dtype=torch.float32)
     p = gdr.problem_for(x.q, x.v, x.g, 64, variant="tensor")
-    t = torch.zeros(64, 1, 64, device="cuda", dtype=torch.bfloat16)
+    t = torch.zeros(64, 1, 64, device="cuda")
     with pytest.raises(gdr.GdrError) as e:
-        if stage == "scan":
+        if stage == "prepare":
+            gdr.gdr_prepare_wy(p, t, t, t, t, t, t, t)
+        elif stage == "scan":
             gdr.gdr_scan_h(p, t, t, t, t, None, None, t, None)
         else:
             gdr.gdr_chunk_output(p, t, t, t, t, t, t)
@@ -131,3 +131,43 @@ def test_output_stage(shape, per_k, variant, dtype):
     torch.cuda.synchronize()
     assert gdr.gdr_last_variant() == variant
     assert scaled_err(o, ref) <= STAGE_TOL[io_name(dtype)]
+
+
+SCAN_OUTPUT_SHAPES = [(2, 256, 3, 64, 64, 64), (1, 192, 2, 128, 128, 64), (2, 128, 3, 64, 128, 32),
+                      (1, 160, 1, 128, 64, 32), (1, 64, 2, 128, 128, 64)]
+
+
+@pytest.mark.parametrize("shape", SCAN_OUTPUT_SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("with_h0", [False, True])
+def test_scan_output_stage(shape, with_h0):
+    """Scan and output fused: o and h_final against the chunked oracle's scan and
+    output stages fed the same rounded w, u, G."""
+    B, T, H, K, V, C = shape
+    dtype = torch.bfloat16
+    x = make_inputs(B, T, H, K, V, io_dtype=dtype, with_h0=with_h0, seed=14)
+    pre = chunked.prepare_wy(x.k, x.v, x.g, x.beta, C)
+    w_r, u_r, G_r = rounded(pre["w"], dtype), rounded(pre["u"], dtype), rounded(pre["G"], torch.float32)
+    h0 = None if x.h0 is None else x.h0 * 20
+    scan = chunked.scan_h(x.k, w_r, u_r, G_r, h0, C)
+    o_ref = chunked.chunk_output(x.q, x.k, scan["v_new"], scan["ckpt"], G_r, C, 0.125)
+    p = gdr.problem_for(x.q, x.v, x.g, C, scale=0.125)
+    o = torch.full((B, T, H, V), float("nan"), device="cuda", dtype=dtype)
+    hf = torch.full((B, H, K, V), float("nan"), device="cuda", dtype=torch.float32)
+    gdr.gdr_scan_output(p, dev(x.q), dev(x.k), dev(w_r), dev(u_r), dev(G_r), dev(h0), o, hf)
+    torch.cuda.synchronize()
+    assert gdr.gdr_last_variant() == "fused"
+    assert scaled_err(o, o_ref) <= STAGE_TOL["bf16"]
+    assert rel_frob(hf, scan["h_final"]) <= STAGE_TOL["bf16"]
+
+
+def test_scan_output_refuses_per_key_gate_and_fp32():
+    x = make_inputs(1, 64, 1, 64, 64, per_k_gate=True, io_dtype=torch.bfloat16)
+    t = torch.zeros(64, 1, 64, device="cuda", dtype=torch.bfloat16)
+    with pytest.raises(gdr.GdrError) as e:
+        gdr.gdr_scan_output(gdr.problem_for(x.q, x.v, x.g, 64), t, t, t, t, t, None, t, None)
+    assert e.value.status == 8
+    xf = make_inputs(1, 64, 1, 64, 64, io_dtype=torch.float32)
+    tf = torch.zeros(64, 1, 64, device="cuda")
+    with pytest.raises(gdr.GdrError) as e:
+        gdr.gdr_scan_output(gdr.problem_for(xf.q, xf.v, xf.g, 64), tf, tf, tf, tf, tf, None, tf, None)
+    assert e.value.status == 8

@@ -252,12 +252,16 @@ def run_ours(args, wl):
         g_cum = torch.empty_like(g)
         w = torch.empty_like(k)
         u = torch.empty_like(v)
+        P = torch.empty(B, T // C, H, C, C, device=dev, dtype=q.dtype) if C == 64 else None
         sp = gdr.problem_for(q, v, g, C, None, args.variant)
         kernels = ["prepare", "scan_output"]
 
         def launches():
-            return [lambda: gdr.gdr_prepare_wy(sp, k, v, g, beta, w, u, g_cum),
-                    lambda: gdr.gdr_scan_output(sp, q, k, w, u, g_cum, h0, o, hf)]
+            if P is None:
+                return [lambda: gdr.gdr_prepare_wy(sp, k, v, g, beta, w, u, g_cum),
+                        lambda: gdr.gdr_scan_output(sp, q, k, w, u, g_cum, None, h0, o, hf)]
+            return [lambda: gdr.gdr_prepare_wyp(sp, q, k, v, g, beta, w, u, g_cum, P),
+                    lambda: gdr.gdr_scan_output(sp, q, k, w, u, g_cum, P, h0, o, hf)]
     elif staged:
         NT = T // C
         e = q.element_size()
@@ -331,14 +335,15 @@ def run_ours(args, wl):
     h2d = sum(t.numel() * t.element_size() for t in hx.values())
     d2h = o.numel() * o.element_size() + hf.numel() * hf.element_size()
     for _ in range(2):
-        gdr.forward(hx["q"], hx["k"], hx["v"], hx["g"], hx["beta"], hx.get("h0"), chunk=C, workspace=ws)
+        gdr.forward(hx["q"], hx["k"], hx["v"], hx["g"], hx["beta"], hx.get("h0"), chunk=C, variant=args.variant,
+                    workspace=ws)
     torch.cuda.synchronize()
     e2e_steps = max(3, min(args.steps, 10))
     barrier(world)
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
         oo, hh = gdr.forward(hx["q"], hx["k"], hx["v"], hx["g"], hx["beta"], hx.get("h0"), chunk=C,
-                             workspace=ws)
+                             variant=args.variant, workspace=ws)
     torch.cuda.synchronize()
     e2e_s = max_over_ranks(time.perf_counter() - t0, world)
     e2e_value = world * B * T * e2e_steps / e2e_s

@@ -13,12 +13,13 @@
 //   warps 0-1   recurrence: each owns 16 value columns of h^T as fp32 mma.sync
 //               accumulators (as in the standalone scan) and, per chunk, stages
 //               bf16 h_c and v'_c in shared memory for the output warps
-//   warps 2..   output, one per 16 tokens of the chunk: S = q k^T, the gated
-//               causal P and q exp(G) stay in registers; o = (q e^G) h_c + P v'
-//               reads h_c and v' from the staging, and leaves by TMA store
+//   warps 2..   output, one per 16 tokens of the chunk: the gated causal P
+//               (S = q k^T computed here, or the tile the prepare wrote) and
+//               q exp(G) stay in registers; o = (q e^G) h_c + P v' reads h_c
+//               and v' from the staging, and leaves by TMA store
 //   2 warps     producer of the recurrence ring: TMA w, u; kg = k exp(G_last - G)
 //               built from global loads issued a chunk ahead; the decay
-//   2 warps     producer of the output ring: TMA q, k; the chunk's G
+//   2 warps     producer of the output ring: TMA q and k (or P); the chunk's G
 //
 // The two rings are separate so the output warps, which trail the recurrence,
 // never hold it back.  Shared tiles read by ldmatrix use 128-byte (k, q, w, kg)
@@ -47,7 +48,7 @@ __device__ __forceinline__ uint32_t sw128(int r, int col, int rows) {
     return (uint32_t)((col >> 6) * rows * 128 + r * 128 + ((((col & 63) >> 3) ^ (r & 7)) << 4));
 }
 
-template <int K, int C>
+template <int K, int C, bool HAS_P>
 struct FLayout {
     static constexpr int NS = 2;
     static constexpr int NOW = C / 16;                  // output warps
@@ -61,24 +62,26 @@ struct FLayout {
     static constexpr uint32_t GLd = U + NS * kU;        // NS x 4 floats (G_last)
     // output ring: q, k, G
     static constexpr uint32_t Q = GLd + 1024;
+    static constexpr uint32_t kKR = HAS_P ? C * C * 2 : kKC;   // P [C][C] or raw k [C][K]
     static constexpr uint32_t KR = Q + NS * kKC;
-    static constexpr uint32_t G = KR + NS * kKC;        // NS x C floats
+    static constexpr uint32_t G = KR + NS * kKR;        // NS x C floats
     // staging
     static constexpr uint32_t HC = G + 1024;            // 2 x [K][32] bf16 h_c
     static constexpr uint32_t VP = HC + 2 * K * kBV * 2;
     static constexpr uint32_t OS = VP + 2 * kU;         // NOW x 2 x [16][32] bf16
     static constexpr uint32_t bytes = OS + NOW * 2 * 16 * kBV * 2;
     static_assert(bytes + 1024 <= 232448, "fused scan/output shared memory");
+    static_assert(!HAS_P || C == 64, "a precomputed P comes in 64 x 64 tiles");
 };
 
-template <int K, int C>
-__global__ void __launch_bounds__(FLayout<K, C>::kThreads, 1)
+template <int K, int C, bool HAS_P>
+__global__ void __launch_bounds__(FLayout<K, C, HAS_P>::kThreads, 1)
 fused_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap mu,
                          const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                          const __grid_constant__ CUtensorMap mo, const bf16* __restrict__ k,
                          const float* __restrict__ g_cum, const float* __restrict__ h0, float* __restrict__ h_final,
                          int T, int H, int V, float scale, unsigned int* err) {
-    using L = FLayout<K, C>;
+    using L = FLayout<K, C, HAS_P>;
     constexpr int NS = L::NS, NOW = L::NOW;
     constexpr int NT8 = C / 8;
     extern __shared__ unsigned char smem_raw[];
@@ -173,12 +176,14 @@ fused_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_co
             if (!bw::mbar_wait(&emptyB[s], ((c / NS) & 1) ^ 1, err, kDeviceErrTimeout)) break;
             const int t0 = c * C;
             if (pt == 0) {
-                bw::mbar_arrive_expect_tx(&fullB[s], 2 * L::kKC);
+                bw::mbar_arrive_expect_tx(&fullB[s], L::kKC + L::kKR);
 #pragma unroll
                 for (int a = 0; a < K / 64; ++a) {
                     bw::tma_load_4d(sm + L::Q + s * L::kKC + a * C * 128, &mq, &fullB[s], a * 64, h, t0, b);
-                    bw::tma_load_4d(sm + L::KR + s * L::kKC + a * C * 128, &mk, &fullB[s], a * 64, h, t0, b);
+                    if constexpr (!HAS_P)
+                        bw::tma_load_4d(sm + L::KR + s * L::kKR + a * C * 128, &mk, &fullB[s], a * 64, h, t0, b);
                 }
+                if constexpr (HAS_P) bw::tma_load_4d(sm + L::KR + s * L::kKR, &mk, &fullB[s], 0, 0, h, b * NT + c);
             }
             if (pt < C) sG[s * C + pt] = g_cum[row(t0 + pt)];
             bw::mbar_arrive(&fullB[s]);
@@ -307,12 +312,22 @@ fused_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_co
         const int t0 = c * C;
         bw::mbar_wait(&fullB[s], (c / NS) & 1, err, kDeviceErrTimeout);
         const uint32_t q_t = s_base + L::Q + s * L::kKC;
-        const uint32_t k_t = s_base + L::KR + s * L::kKC;
+        const uint32_t k_t = s_base + L::KR + s * L::kKR;
         const float* G = sG + s * C;
-        // q fragments (A operand, 16 rows x K) and S = q k^T  [16 x C]
+        const int i0 = r0 + g, i1 = i0 + 8;
+        const float Gi0 = G[i0], Gi1 = G[i1];
+        // q fragments (A operand, 16 rows x K)
         uint32_t qa[K / 16][4];
 #pragma unroll
         for (int kk = 0; kk < K / 16; ++kk) wm::ldsm_x4(q_t + sw128(r0 + 8 * (mi & 1) + mr, 16 * kk + 8 * (mi >> 1), C), qa[kk]);
+        uint32_t pa[C / 16][4];
+        if constexpr (HAS_P) {
+            // P = tril_0(q k^T * exp(G_i - G_j)) precomputed by the prepare: A fragments straight from its tile
+#pragma unroll
+            for (int kk = 0; kk < C / 16; ++kk)
+                wm::ldsm_x4(k_t + sw128(r0 + 8 * (mi & 1) + mr, 16 * kk + 8 * (mi >> 1), C), pa[kk]);
+        } else {
+        // S = q k^T  [16 x C]
         float S[NT8][4];
 #pragma unroll
         for (int j = 0; j < NT8; ++j) S[j][0] = S[j][1] = S[j][2] = S[j][3] = 0.f;
@@ -326,10 +341,7 @@ fused_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_co
                 wm::mma16816(S[jp + 1], qa[kk], bfr[2], bfr[3]);
             }
         }
-        // P = tril_0(S * exp(G_i - G_j)) as A fragments; q exp(G_i) in place
-        const int i0 = r0 + g, i1 = i0 + 8;
-        const float Gi0 = G[i0], Gi1 = G[i1];
-        uint32_t pa[C / 16][4];
+        // P = tril_0(S * exp(G_i - G_j)) as A fragments
 #pragma unroll
         for (int kk = 0; kk < C / 16; ++kk) {
             float pv[2][4];
@@ -348,6 +360,8 @@ fused_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_co
             pa[kk][2] = wm::pack2(pv[1][0], pv[1][1]);
             pa[kk][3] = wm::pack2(pv[1][2], pv[1][3]);
         }
+        }
+        // q exp(G_i) in place
         const float e0 = __expf(Gi0), e1 = __expf(Gi1);
 #pragma unroll
         for (int kk = 0; kk < K / 16; ++kk) {
@@ -416,16 +430,24 @@ fused_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_co
     if (lane == 0) bw::bulk_wait<0>();
 }
 
-template <int K, int C>
+template <int K, int C, bool HAS_P>
 cudaError_t launch(const Dims& d, const void* q, const void* k, const void* w, const void* u, const float* g_cum,
-                   const float* h0, void* o, float* h_final, cudaStream_t s, unsigned int* err) {
-    using L = FLayout<K, C>;
+                   const void* P, const float* h0, void* o, float* h_final, cudaStream_t s, unsigned int* err) {
+    using L = FLayout<K, C, HAS_P>;
     CUtensorMap mw, mu, mq, mk, mo;
     if (!make_tmap_tokens(&mw, w, d.B, d.T, d.H, K, C) || !make_tmap_tokens_sw64(&mu, u, d.B, d.T, d.H, d.V, C) ||
-        !make_tmap_tokens(&mq, q, d.B, d.T, d.H, K, C) || !make_tmap_tokens(&mk, k, d.B, d.T, d.H, K, C) ||
-        !make_tmap_tokens_sw64(&mo, o, d.B, d.T, d.H, d.V, 16))
+        !make_tmap_tokens(&mq, q, d.B, d.T, d.H, K, C) || !make_tmap_tokens_sw64(&mo, o, d.B, d.T, d.H, d.V, 16))
         return cudaErrorInvalidValue;
-    auto kern = fused_scan_output_kernel<K, C>;
+    if constexpr (HAS_P) {
+        // P [B, NT, H, C, C] seen as (C, C, H, B*NT); one C x C box per chunk
+        const uint64_t dims[4] = {(uint64_t)C, (uint64_t)C, (uint64_t)d.H, (uint64_t)d.B * d.NT};
+        const uint64_t st[3] = {(uint64_t)C * 2, (uint64_t)C * C * 2, (uint64_t)d.H * C * C * 2};
+        const uint32_t box[4] = {(uint32_t)C, (uint32_t)C, 1, 1};
+        if (!make_tmap_bf16_4d(&mk, P, dims, st, box)) return cudaErrorInvalidValue;
+    } else {
+        if (!make_tmap_tokens(&mk, k, d.B, d.T, d.H, K, C)) return cudaErrorInvalidValue;
+    }
+    auto kern = fused_scan_output_kernel<K, C, HAS_P>;
     const size_t smem = L::bytes + 1024;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -438,13 +460,17 @@ cudaError_t launch(const Dims& d, const void* q, const void* k, const void* w, c
 }  // namespace
 
 cudaError_t mma_scan_output(const Dims& d, const void* q, const void* k, const void* w, const void* u,
-                            const float* g_cum, const float* h0, void* o, float* h_final, cudaStream_t s,
-                            unsigned int* err) {
-    if (!d.bf16 || d.per_k) return cudaErrorInvalidValue;
-    if (d.K == 64) return d.C == 32 ? launch<64, 32>(d, q, k, w, u, g_cum, h0, o, h_final, s, err)
-                                    : launch<64, 64>(d, q, k, w, u, g_cum, h0, o, h_final, s, err);
-    return d.C == 32 ? launch<128, 32>(d, q, k, w, u, g_cum, h0, o, h_final, s, err)
-                     : launch<128, 64>(d, q, k, w, u, g_cum, h0, o, h_final, s, err);
+                            const float* g_cum, const void* P, const float* h0, void* o, float* h_final,
+                            cudaStream_t s, unsigned int* err) {
+    if (!d.bf16 || d.per_k || (P && d.C != 64)) return cudaErrorInvalidValue;
+    if (P) {
+        return d.K == 64 ? launch<64, 64, true>(d, q, k, w, u, g_cum, P, h0, o, h_final, s, err)
+                         : launch<128, 64, true>(d, q, k, w, u, g_cum, P, h0, o, h_final, s, err);
+    }
+    if (d.K == 64) return d.C == 32 ? launch<64, 32, false>(d, q, k, w, u, g_cum, P, h0, o, h_final, s, err)
+                                    : launch<64, 64, false>(d, q, k, w, u, g_cum, P, h0, o, h_final, s, err);
+    return d.C == 32 ? launch<128, 32, false>(d, q, k, w, u, g_cum, P, h0, o, h_final, s, err)
+                     : launch<128, 64, false>(d, q, k, w, u, g_cum, P, h0, o, h_final, s, err);
 }
 
 }  // namespace gdr

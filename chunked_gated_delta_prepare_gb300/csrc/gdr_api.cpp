@@ -106,7 +106,7 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // gdr_forward scratch: g_cum, w, u and (staged paths) v_new, h_ckpt, each 256-byte aligned.
 struct StagedWorkspace {
-    size_t g_cum, w, u, v_new, h_ckpt, total;
+    size_t g_cum, w, u, v_new, h_ckpt, P, total;
 };
 
 StagedWorkspace plan_staged(const gdr::Dims& d, bool fused) {
@@ -119,10 +119,13 @@ StagedWorkspace plan_staged(const gdr::Dims& d, bool fused) {
     ws.u = off;     off = round_up(off + rows * d.V * e, 256);
     ws.v_new = off;
     ws.h_ckpt = off;
+    ws.P = off;
     if (!fused) {   // the fused scan/output keeps v' and the checkpoints on chip
         off = round_up(off + rows * d.V * e, 256);
         ws.h_ckpt = off;
         off = round_up(off + (size_t)d.B * d.NT * d.H * d.K * d.V * e, 256);
+    } else if (d.C == 64) {   // ... and reads the prepare's gated causal scores
+        off = round_up(off + rows * (size_t)d.C * e, 256);
     }
     ws.total = off;
     return ws;
@@ -210,9 +213,10 @@ gdr_status gdr_forward(const gdr_problem* p, const void* q, const void* k, const
         if ((st = from_cuda(gdr::simt_scan(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, s))) != GDR_OK) return st;
         if ((st = from_cuda(gdr::simt_output(d, q, k, v_new, h_ckpt, g_cum, o, s))) != GDR_OK) return st;
     } else {
-        if ((st = from_cuda(gdr::mma_prepare(d, k, v, g, beta, w, u, g_cum, s, err))) != GDR_OK) return st;
+        void* P = (path == Path::Fused && d.C == 64) ? base + ws.P : nullptr;
+        if ((st = from_cuda(gdr::mma_prepare(d, k, v, g, beta, w, u, g_cum, s, err, q, P))) != GDR_OK) return st;
         if (path == Path::Fused) {
-            if ((st = from_cuda(gdr::mma_scan_output(d, q, k, w, u, g_cum, h0, o, h_final, s, err))) != GDR_OK)
+            if ((st = from_cuda(gdr::mma_scan_output(d, q, k, w, u, g_cum, P, h0, o, h_final, s, err))) != GDR_OK)
                 return st;
         } else {
             if ((st = from_cuda(gdr::mma_scan(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, s, err))) != GDR_OK)
@@ -225,15 +229,28 @@ gdr_status gdr_forward(const gdr_problem* p, const void* q, const void* k, const
 }
 
 gdr_status gdr_scan_output(const gdr_problem* p, const void* q, const void* k, const void* w, const void* u,
-                           const float* g_cum, const float* h0, void* o, float* h_final, void* stream) {
+                           const float* g_cum, const void* P, const float* h0, void* o, float* h_final,
+                           void* stream) {
     gdr::Dims d;
     gdr_status st = check_problem(p, &d);
     if (st != GDR_OK) return st;
-    if ((st = check_ptrs({q, k, w, u, g_cum, o}, {h0, h_final})) != GDR_OK) return st;
-    if (p->variant == GDR_VARIANT_SIMT || !d.bf16 || d.per_k) return GDR_ERR_UNSUPPORTED;
-    st = from_cuda(gdr::mma_scan_output(d, q, k, w, u, g_cum, h0, o, h_final, (cudaStream_t)stream,
+    if ((st = check_ptrs({q, k, w, u, g_cum, o}, {P, h0, h_final})) != GDR_OK) return st;
+    if (p->variant == GDR_VARIANT_SIMT || !d.bf16 || d.per_k || (P && d.C != 64)) return GDR_ERR_UNSUPPORTED;
+    st = from_cuda(gdr::mma_scan_output(d, q, k, w, u, g_cum, P, h0, o, h_final, (cudaStream_t)stream,
                                         device_error_word()));
     if (st == GDR_OK) t_last_variant = "fused";
+    return st;
+}
+
+gdr_status gdr_prepare_wyp(const gdr_problem* p, const void* q, const void* k, const void* v, const float* g,
+                           const void* beta, void* w, void* u, float* g_cum, void* P, void* stream) {
+    gdr::Dims d;
+    gdr_status st = check_problem(p, &d);
+    if (st != GDR_OK) return st;
+    if ((st = check_ptrs({q, k, v, g, beta, w, u, g_cum, P}, {})) != GDR_OK) return st;
+    if (p->variant == GDR_VARIANT_SIMT || !d.bf16 || d.per_k || d.C != 64) return GDR_ERR_UNSUPPORTED;
+    st = from_cuda(gdr::mma_prepare(d, k, v, g, beta, w, u, g_cum, (cudaStream_t)stream, device_error_word(), q, P));
+    if (st == GDR_OK) t_last_variant = "tensor";
     return st;
 }
 

@@ -26,8 +26,11 @@ cudaError_t simt_output(const Dims& d, const void* q, const void* k, const void*
                         const float* g_cum, void* o, cudaStream_t s);
 
 // ---- tensor-core kernels (bf16 io only)
+// with q and P non-NULL (scalar gate, C = 64) it also writes P = tril_0(q k^T * exp(G_i - G_j))
+// per chunk as [B, NT, H, C, C] bf16
 cudaError_t mma_prepare(const Dims& d, const void* k, const void* v, const float* g, const void* beta, void* w,
-                        void* u, float* g_cum, cudaStream_t s, unsigned int* err);
+                        void* u, float* g_cum, cudaStream_t s, unsigned int* err, const void* q = nullptr,
+                        void* P = nullptr);
 // the scan's recurrence runs on mma.sync (register-resident), see scan_mma.cu
 cudaError_t mma_scan(const Dims& d, const void* k, const void* w, const void* u, const float* g_cum, const float* h0,
                      void* h_ckpt, void* v_new, float* h_final, cudaStream_t s, unsigned int* err);
@@ -35,9 +38,10 @@ cudaError_t tc_output(const Dims& d, const void* q, const void* k, const void* v
                       const float* g_cum, void* o, cudaStream_t s, unsigned int* err);
 
 // scan and output fused (scalar gate, bf16), see fused_mma.cu
+// P: the prepare's [B, NT, H, C, C] tiles (C = 64), or NULL to compute q k^T in the kernel
 cudaError_t mma_scan_output(const Dims& d, const void* q, const void* k, const void* w, const void* u,
-                            const float* g_cum, const float* h0, void* o, float* h_final, cudaStream_t s,
-                            unsigned int* err);
+                            const float* g_cum, const void* P, const float* h0, void* o, float* h_final,
+                            cudaStream_t s, unsigned int* err);
 
 // ---- device error word (device_status.cu)
 // Bounded waits in kernels write a nonzero code here instead of trapping.

@@ -5,7 +5,7 @@ kernels.  PyTorch supplies device memory and the current stream.  There is no
 CPU fallback: if the library is missing or cannot load, every call raises.
 
 The functions mirror the C ABI names:
-    gdr_prepare_wy, gdr_scan_h, gdr_chunk_output, gdr_scan_output, gdr_forward,
+    gdr_prepare_wy, gdr_prepare_wyp, gdr_scan_h, gdr_chunk_output, gdr_scan_output, gdr_forward,
     gdr_forward_workspace_bytes, gdr_status_string, gdr_get_device_status,
     gdr_last_variant, gdr_version
 and `forward(...)` is the convenience call that allocates outputs and the
@@ -30,7 +30,7 @@ STATUS_NAMES = {0: "GDR_OK", 1: "GDR_ERR_NULL", 2: "GDR_ERR_SHAPE", 3: "GDR_ERR_
 DTYPES = {torch.float32: 0, torch.bfloat16: 1}
 VARIANTS = {"auto": 0, "simt": 1, "tensor": 2, "fused": 3}
 EXPORTS = ["gdr_prepare_wy", "gdr_scan_h", "gdr_chunk_output", "gdr_forward", "gdr_forward_workspace_bytes",
-           "gdr_forward_static_scratch", "gdr_scan_output",
+           "gdr_forward_static_scratch", "gdr_scan_output", "gdr_prepare_wyp",
            "gdr_status_string", "gdr_get_device_status", "gdr_last_variant", "gdr_version"]
 
 
@@ -68,7 +68,8 @@ def load(path: str | None = None):
             "gdr_chunk_output": [P, vp, vp, vp, vp, vp, vp, vp],
             "gdr_forward": [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp],
             "gdr_forward_static_scratch": [P, vp, vp, vp, vp, vp, vp, vp, vp, vp],
-            "gdr_scan_output": [P, vp, vp, vp, vp, vp, vp, vp, vp, vp],
+            "gdr_scan_output": [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp],
+            "gdr_prepare_wyp": [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp],
             "gdr_forward_workspace_bytes": [P],
             "gdr_status_string": [ctypes.c_int],
             "gdr_get_device_status": [vp],
@@ -146,9 +147,14 @@ def gdr_chunk_output(p, q, k, v_new, h_ckpt, g_cum, o, stream=None):
                                    _ptr(o), _stream(stream)), "gdr_chunk_output")
 
 
-def gdr_scan_output(p, q, k, w, u, g_cum, h0, o, h_final, stream=None):
-    _check(load().gdr_scan_output(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(w), _ptr(u), _ptr(g_cum), _ptr(h0),
-                                  _ptr(o), _ptr(h_final), _stream(stream)), "gdr_scan_output")
+def gdr_scan_output(p, q, k, w, u, g_cum, P, h0, o, h_final, stream=None):
+    _check(load().gdr_scan_output(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(w), _ptr(u), _ptr(g_cum), _ptr(P),
+                                  _ptr(h0), _ptr(o), _ptr(h_final), _stream(stream)), "gdr_scan_output")
+
+
+def gdr_prepare_wyp(p, q, k, v, g, beta, w, u, g_cum, P, stream=None):
+    _check(load().gdr_prepare_wyp(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(w), _ptr(u),
+                                  _ptr(g_cum), _ptr(P), _stream(stream)), "gdr_prepare_wyp")
 
 
 def gdr_forward_workspace_bytes(p) -> int:
@@ -210,7 +216,10 @@ def forward(q, k, v, g, beta, h0=None, *, chunk=64, scale=None, variant="auto", 
     nbytes = gdr_forward_workspace_bytes(p)
     if workspace is None and nbytes:
         workspace = torch.empty(nbytes, device=q.device, dtype=torch.uint8)
-    gdr_forward(p, q, k, v, g, beta, h0, o, hf, workspace, nbytes, stream)
+    # the size handed to the library is what the buffer really holds; the library
+    # refuses (GDR_ERR_WORKSPACE) a buffer smaller than this problem needs
+    have = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    gdr_forward(p, q, k, v, g, beta, h0, o, hf, workspace, have, stream)
     if on_host:
         o = o.to("cpu", non_blocking=False)
         hf = hf.to("cpu") if hf is not None else None

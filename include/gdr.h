@@ -148,12 +148,26 @@ GDR_API gdr_status gdr_chunk_output(const gdr_problem* p, const void* q, const v
  * each chunk c, v'_c = u_c - w_c h, o_c = scale [ (q exp(G)) h + tril_0(Q~) v'_c ],
  * h = exp(G_last) h + (k exp(G_last - G))^T v'_c.
  * Inputs:  q, k, w [B,T,H,K] bf16; u [B,T,H,V] bf16; g_cum [B,T,H] fp32 (the
- *          chunk-local cumsum, as gdr_prepare_wy writes it); h0 [B,H,K,V] fp32 or NULL.
+ *          chunk-local cumsum, as gdr_prepare_wy writes it); P [B,NT,H,C,C] bf16
+ *          as gdr_prepare_wyp writes it, or NULL to form it here (C = 64 for a
+ *          non-NULL P); h0 [B,H,K,V] fp32 or NULL.
  * Outputs: o [B,T,H,V] bf16; h_final [B,H,K,V] fp32 or NULL (not written).
  * Returns GDR_ERR_UNSUPPORTED for fp32 io or a per-key-dim gate.
  */
 GDR_API gdr_status gdr_scan_output(const gdr_problem* p, const void* q, const void* k, const void* w, const void* u,
-                                   const float* g_cum, const float* h0, void* o, float* h_final, void* stream);
+                                   const float* g_cum, const void* P, const float* h0, void* o, float* h_final,
+                                   void* stream);
+
+/*
+ * gdr_prepare_wy plus, per chunk, the gated causal score matrix of the chunk
+ * output, P = tril_0(Q~) with Q~_ij = sum_d q_id k_jd exp(G_i - G_j) (no scale),
+ * so that gdr_scan_output need not form q k^T once per value slice.
+ * Scalar gate, bf16 io and chunk C = 64 only (GDR_ERR_UNSUPPORTED otherwise).
+ * Extra input: q [B,T,H,K] bf16.  Extra output: P [B,NT,H,C,C] bf16, row i of
+ * chunk c holding the scores of query token c*C+i against key tokens c*C+j.
+ */
+GDR_API gdr_status gdr_prepare_wyp(const gdr_problem* p, const void* q, const void* k, const void* v, const float* g,
+                                   const void* beta, void* w, void* u, float* g_cum, void* P, void* stream);
 
 /*
  * Bytes of device workspace gdr_forward needs for this problem (0 when the

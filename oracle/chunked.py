@@ -155,15 +155,25 @@ def scan_h(k, w, u, G, h0, C):
     return dict(ckpt=ckpt, v_new=_from_chunks(v_new), h_final=h)
 
 
-def chunk_output(q, k, v_new, ckpt, G, C, scale):
-    """Stage 3: o = scale [ (q exp(G)) ckpt[c] + tril_0(Q~) v'_c ]."""
-    q, k, v_new, ckpt, G = _f64(q), _f64(k), _f64(v_new), _f64(ckpt), _f64(G)
-    qc, kc, vc = _to_chunks(q, C), _to_chunks(k, C), _to_chunks(v_new, C)
-    Gc = _gate_vec(G, C)
+def gated_causal_scores(q, k, G, C):
+    """tril_0(Q~) per chunk, Q~_ij = sum_d q_id k_jd exp(G_id - G_jd), diagonal included.
+
+    Returned chunked: [B,NT,H,C,C]."""
+    qc, kc = _to_chunks(_f64(q), C), _to_chunks(_f64(k), C)
+    Gc = _gate_vec(_f64(G), C)
     Qt = np.zeros(qc.shape[:-1] + (C,))
     for i in range(C):
         gate = np.exp(Gc[..., i:i + 1, :] - Gc[..., :i + 1, :])    # [...,i+1,1|K]
         Qt[..., i, :i + 1] = np.einsum("...d,...jd->...j", qc[..., i, :], kc[..., :i + 1, :] * gate)
+    return Qt
+
+
+def chunk_output(q, k, v_new, ckpt, G, C, scale):
+    """Stage 3: o = scale [ (q exp(G)) ckpt[c] + tril_0(Q~) v'_c ]."""
+    q, k, v_new, ckpt, G = _f64(q), _f64(k), _f64(v_new), _f64(ckpt), _f64(G)
+    qc, vc = _to_chunks(q, C), _to_chunks(v_new, C)
+    Gc = _gate_vec(G, C)
+    Qt = gated_causal_scores(q, k, G, C)
     inter = (qc * np.exp(Gc)) @ ckpt                       # ckpt [B,NT,H,K,V]
     intra = Qt @ vc
     return _from_chunks(scale * (inter + intra))

@@ -148,6 +148,17 @@ def test_auto_variant_choice():
     assert gpu_forward(xf, 64, "auto")[2] == "simt"
 
 
+def test_convenience_forward_refuses_a_small_workspace():
+    x = make_inputs(1, 128, 2, 64, 64, io_dtype=torch.bfloat16, with_h0=True, seed=16)
+    p = gdr.problem_for(x.q, x.v, x.g, 64, variant="tensor")
+    need = gdr.gdr_forward_workspace_bytes(p)
+    small = torch.empty(need // 2, device="cuda", dtype=torch.uint8)
+    with pytest.raises(gdr.GdrError) as e:
+        gdr.forward(*(t.cuda() for t in (x.q, x.k, x.v, x.g, x.beta, x.h0)), chunk=64, variant="tensor",
+                    workspace=small)
+    assert e.value.status == 5
+
+
 def test_invalid_shape_launches_nothing():
     x = make_inputs(1, 96, 1, 64, 64, io_dtype=torch.bfloat16, seed=11)  # T % C != 0
     with pytest.raises(gdr.GdrError) as e:

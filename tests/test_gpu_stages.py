@@ -153,7 +153,7 @@ def test_scan_output_stage(shape, with_h0):
     p = gdr.problem_for(x.q, x.v, x.g, C, scale=0.125)
     o = torch.full((B, T, H, V), float("nan"), device="cuda", dtype=dtype)
     hf = torch.full((B, H, K, V), float("nan"), device="cuda", dtype=torch.float32)
-    gdr.gdr_scan_output(p, dev(x.q), dev(x.k), dev(w_r), dev(u_r), dev(G_r), dev(h0), o, hf)
+    gdr.gdr_scan_output(p, dev(x.q), dev(x.k), dev(w_r), dev(u_r), dev(G_r), None, dev(h0), o, hf)
     torch.cuda.synchronize()
     assert gdr.gdr_last_variant() == "fused"
     assert scaled_err(o, o_ref) <= STAGE_TOL["bf16"]
@@ -164,10 +164,47 @@ def test_scan_output_refuses_per_key_gate_and_fp32():
     x = make_inputs(1, 64, 1, 64, 64, per_k_gate=True, io_dtype=torch.bfloat16)
     t = torch.zeros(64, 1, 64, device="cuda", dtype=torch.bfloat16)
     with pytest.raises(gdr.GdrError) as e:
-        gdr.gdr_scan_output(gdr.problem_for(x.q, x.v, x.g, 64), t, t, t, t, t, None, t, None)
+        gdr.gdr_scan_output(gdr.problem_for(x.q, x.v, x.g, 64), t, t, t, t, t, None, None, t, None)
     assert e.value.status == 8
     xf = make_inputs(1, 64, 1, 64, 64, io_dtype=torch.float32)
     tf = torch.zeros(64, 1, 64, device="cuda")
     with pytest.raises(gdr.GdrError) as e:
-        gdr.gdr_scan_output(gdr.problem_for(xf.q, xf.v, xf.g, 64), tf, tf, tf, tf, tf, None, tf, None)
+        gdr.gdr_scan_output(gdr.problem_for(xf.q, xf.v, xf.g, 64), tf, tf, tf, tf, tf, None, None, tf, None)
     assert e.value.status == 8
+
+
+@pytest.mark.parametrize("shape", [(2, 256, 3, 64, 64, 64), (1, 192, 2, 128, 128, 64), (1, 320, 1, 128, 64, 64)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_prepare_with_scores_then_scan_output(shape):
+    """gdr_prepare_wyp's P against the oracle's gated causal scores, then
+    gdr_scan_output reading that P against the oracle's scan and output."""
+    B, T, H, K, V, C = shape
+    dtype = torch.bfloat16
+    x = make_inputs(B, T, H, K, V, io_dtype=dtype, with_h0=True, seed=15)
+    p = gdr.problem_for(x.q, x.v, x.g, C, scale=0.125)
+    q, k, v, g, beta = (dev(t) for t in (x.q, x.k, x.v, x.g, x.beta))
+    NT = T // C
+    w = torch.full_like(k, float("nan"))
+    u = torch.full_like(v, float("nan"))
+    g_cum = torch.full_like(g, float("nan"))
+    P = torch.full((B, NT, H, C, C), float("nan"), device="cuda", dtype=dtype)
+    gdr.gdr_prepare_wyp(p, q, k, v, g, beta, w, u, g_cum, P)
+    torch.cuda.synchronize()
+    pre = chunked.prepare_wy(x.k, x.v, x.g, x.beta, C)
+    assert scaled_err(w, pre["w"]) <= STAGE_TOL["bf16"]
+    assert scaled_err(u, pre["u"]) <= STAGE_TOL["bf16"]
+    assert scaled_err(g_cum, pre["G"]) <= 1e-6
+    assert scaled_err(P, chunked.gated_causal_scores(x.q, x.k, pre["G"], C)) <= STAGE_TOL["bf16"]
+    o = torch.full((B, T, H, V), float("nan"), device="cuda", dtype=dtype)
+    hf = torch.full((B, H, K, V), float("nan"), device="cuda", dtype=torch.float32)
+    gdr.gdr_scan_output(p, q, k, w, u, g_cum, P, dev(x.h0), o, hf)
+    torch.cuda.synchronize()
+    w_r, u_r, G_r, P_r = w.cpu(), u.cpu(), g_cum.cpu(), P.cpu()
+    scan = chunked.scan_h(x.k, w_r, u_r, G_r, x.h0, C)
+    # the output with the GPU's P (rounded) in place of the oracle's scores
+    qc = chunked._to_chunks(chunked._f64(x.q), C)
+    vc = chunked._to_chunks(scan["v_new"], C)
+    Gc = chunked._gate_vec(chunked._f64(G_r), C)
+    o_ref = chunked._from_chunks(0.125 * ((qc * np.exp(Gc)) @ scan["ckpt"] + chunked._f64(P_r) @ vc))
+    assert scaled_err(o, o_ref) <= STAGE_TOL["bf16"]
+    assert rel_frob(hf, scan["h_final"]) <= STAGE_TOL["bf16"]

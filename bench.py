@@ -1,6 +1,7 @@
 """Throughput of the chunked gated-delta-rule forward on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+                    [--variant auto|simt|tensor|fused] [--seq-len T]
 
 One step = one whole forward (gate cumsum, WY prepare, state scan, chunk output)
 over one batch of the 32k-token GDN workload (B=1, T=32768, H=32, K=V=128, C=64,
@@ -178,6 +179,12 @@ def max_over_ranks(x: float, world: int) -> float:
     return float(t.item())
 
 
+def weak_scaling_throughput(world: int, tokens_per_rank_step: int, steps: int, slowest_seconds: float) -> float:
+    """Tokens per second of the whole job: every rank runs its own full copy of the
+    workload, so the job processed world x tokens x steps in the slowest rank's time."""
+    return world * tokens_per_rank_step * steps / slowest_seconds
+
+
 # ------------------------------------------------------------------ CPU oracle leg
 
 def oracle_sample(wl, x, n_heads: int):
@@ -315,7 +322,7 @@ def run_ours(args, wl):
         for i in range(n):
             per_kernel_ms[i] += evs[s][i].elapsed_time(evs[s][i + 1])
     total_s = max_over_ranks(sum(step_ms) / 1e3, world)
-    value = world * B * T * args.steps / total_s
+    value = weak_scaling_throughput(world, B * T, args.steps, total_s)
 
     # roofline of the dominant kernel
     hbm_gbs, _, peak_kind = peaks()
@@ -346,7 +353,7 @@ def run_ours(args, wl):
                              variant=args.variant, workspace=ws)
     torch.cuda.synchronize()
     e2e_s = max_over_ranks(time.perf_counter() - t0, world)
-    e2e_value = world * B * T * e2e_steps / e2e_s
+    e2e_value = weak_scaling_throughput(world, B * T, e2e_steps, e2e_s)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -390,10 +397,14 @@ def main():
     ap.add_argument("--cpu-heads", type=int, default=32, help="heads in the CPU-oracle baseline sample")
     ap.add_argument("--ref-heads", type=int, default=4, help="heads per step of --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--seq-len", type=int, default=None,
+                    help="run the workload at another T (small profiling captures only; not a bench line)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     wl = workloads.BY_NAME[args.workload]
+    if args.seq_len is not None:
+        wl = wl.with_tokens(args.seq_len)
     if args.impl == "reference":
         run_reference(args, wl)
     else:

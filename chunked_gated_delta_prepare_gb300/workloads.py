@@ -7,7 +7,7 @@ float64 oracle to check every output.
 """
 from __future__ import annotations
 
-from dataclasses import dataclass
+from dataclasses import dataclass, replace
 
 import torch
 
@@ -36,6 +36,13 @@ class Workload:
     @property
     def gate(self) -> str:
         return "kda" if self.per_k_gate else "gdn"
+
+    def with_tokens(self, T: int) -> "Workload":
+        """The same problem at another sequence length (for small profiling captures)."""
+        if T <= 0 or T % self.chunk:
+            raise ValueError("T must be a positive multiple of the chunk size")
+        name = self.name.replace(f"_t{self.T}_", f"_t{T}_")
+        return replace(self, name=name, T=T)
 
     def describe(self) -> dict:
         return {"workload": self.name, "B": self.B, "T": self.T, "H": self.H,

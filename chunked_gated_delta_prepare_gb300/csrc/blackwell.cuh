@@ -56,13 +56,34 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // while), so this limit is generous for real work and still finite.
 constexpr uint32_t kMaxPolls = 1u << 22;
 
+// Non-blocking check of the same phase: returns at once.  Issued well before its
+// result is needed, it keeps the barrier's latency off a serial chain.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete.  On giving up, sets
 // *err (if not already set) and returns false.
+// Every 4096 failed polls it also looks at *err: once any wait of the launch has
+// given up, the others stop waiting too instead of each running out its own limit.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* err, unsigned int code) {
-    for (uint32_t i = 0; i < kMaxPolls; ++i)
+    for (uint32_t i = 0; i < kMaxPolls; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 4095u) == 4095u && err && *reinterpret_cast<volatile unsigned int*>(err) != 0u) return false;
+    }
     if (err) atomicCAS(err, 0u, code);
     return false;
+}
+
+// Named barrier `id` (1..15; 0 is __syncthreads) over `nthreads` threads, a multiple of 32.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // ------------------------------------------------------------------ fences

@@ -2,21 +2,30 @@
 // "kernel_fun/kda/_kernels/bwd_scan.py", module docstring: hck[c] = h before the
 // update, v' = u - w h, h = exp(decay) h + kg^T v').
 //
-// One CTA per (batch, head, 32 value columns); serial over chunks.  Each of the
-// two recurrence warps owns 16 value columns of h^T (16 x K) as fp32 mma.sync
-// accumulator fragments for the whole sequence, so per chunk
+// One CTA per (batch, head, 32 value columns); serial over chunks.  Four
+// recurrence warps, one per SM sub-partition, split h^T (32 x K) into quarters:
+// warp (vh, kh) owns value columns 16vh..16vh+15 and key rows kh K/2 .. of it as
+// fp32 mma.sync accumulator fragments for the whole sequence.  Per chunk:
 //
-//   D   = h^T w^T                 [16 x C]   A = bf16(h^T) from its own accumulator
-//   v'^T = u^T - D                            u^T fragments by ldmatrix.trans
-//   h^T = exp(G_last) * h^T + v'^T kg   [16 x K]   A = bf16(v'^T) from D, accumulating in place
+//   D_kh  = h^T[:, keys kh] w[:, keys kh]^T     [16 x C]  A = bf16(h^T) from the accumulator
+//   D     = D_0 + D_1                           the two key halves swap partial sums through
+//                                               shared memory behind a 64-thread named barrier
+//   v'^T  = u^T - D                             u^T by ldmatrix.trans
+//   h^T[:, keys kh] = exp(G_last) h^T + (v'^T diag(gamma)) k[:, keys kh]      (scalar gate)
+//                   = exp(G_last) h^T + v'^T kg[:, keys kh]                    (per-key-dim gate)
 //
-// runs as two short dependent mma.sync chains with no shared-memory round trip
-// and no barrier between the two warps (a tcgen05 MMA costs ~240 SM cycles per
-// K=16 step on this part whatever its shape, which is what this chain cannot afford).
-// Four producer warps stream w and u by TMA and build kg = k exp(G_last - G) and
-// the decay row into a 2-stage ring, their global loads two chunks ahead; v_new
-// and the checkpoints leave through stmatrix.trans into per-warp staging and TMA
-// stores.
+// with gamma_t = exp(G_last - G_t).  For the scalar gate the factor moves from
+// k's rows onto v''s columns (kg^T v' = k^T diag(gamma) v'), so k feeds the MMA
+// exactly as TMA loads it and one producer warp (TMA issue plus a C-float gamma
+// row) feeds a 3-stage ring.  The per-key-dim gate cannot be moved that way;
+// there four producer warps build kg = k exp(G_last - G) from global loads
+// issued two chunks ahead.  v_new and the bf16 checkpoints are transposed by
+// stmatrix.trans into a per-warp staging tile and leave as 16-byte global
+// stores (a TMA store costs the issuing warp ~300 cycles of fence, bulk-group
+// wait and issue, too much on this chain); the u tile is 64-byte swizzled, w
+// and k 128-byte swizzled, the staging XOR-swizzled, so every ldmatrix and
+// stmatrix is free of bank conflicts.  The ring's full barrier for chunk c+1 is
+// tested (non-blocking) in the middle of chunk c, so its latency stays off the chain.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -33,43 +42,47 @@ namespace {
 using bf16 = __nv_bfloat16;
 
 constexpr int kBV = 32;        // value columns per CTA
-constexpr int kRecWarps = 2;   // recurrence warps (16 columns each)
-constexpr int kProdThreads = 128;
-constexpr int kThreads = 32 * kRecWarps + kProdThreads;
+constexpr int kRecWarps = 4;   // (value half, key half)
+
+constexpr uint32_t align1k(uint32_t x) { return (x + 1023u) & ~1023u; }
 
 template <int K, int C, bool PER_K>
 struct MScanLayout {
-    static constexpr int NS = 2;
+    static constexpr int NS = 3;                                   // ring stages
+    static constexpr int KH = K / 2;                               // keys per recurrence warp
+    static constexpr int NT8 = C / 8;
     static constexpr int GW = PER_K ? K : 1;
-    static constexpr int GWS = GW < 4 ? 4 : GW;
-    static constexpr uint32_t kKC = C * K * 2;                    // [C][K] bf16, 128-byte swizzle
-    static constexpr uint32_t kU = C * kBV * 2;                   // [C][32] bf16, plain 64-byte rows
-    static constexpr uint32_t kSV = C * 16 * 2;                   // v_new staging [C][16] per warp per buffer
-    static constexpr uint32_t kSH = K * 16 * 2;                   // checkpoint staging [K][16]
+    static constexpr int kProdWarps = PER_K ? 4 : 1;
+    static constexpr int kThreads = 32 * (kRecWarps + kProdWarps);
+    static constexpr uint32_t kKC = C * K * 2;                     // [C][K] bf16, 128-byte swizzle
+    static constexpr uint32_t kU = C * kBV * 2;                    // [C][32] bf16, 64-byte swizzle
+    static constexpr uint32_t kX = NT8 * 512;                      // one warp's partial D, float4 per (n-tile, lane)
+    static constexpr uint32_t kSH = align1k(KH * 32);              // checkpoint staging [KH][16]
+    static constexpr uint32_t kSV = align1k(C / 2 * 32);           // v_new staging [C/2][16]
     static constexpr uint32_t W = 0;
-    static constexpr uint32_t KG = W + NS * kKC;
-    static constexpr uint32_t U = KG + NS * kKC;
-    static constexpr uint32_t SV = U + NS * kU;
-    static constexpr uint32_t SH = SV + kRecWarps * 2 * kSV;
-    static constexpr uint32_t GL = SH + kRecWarps * 2 * kSH;
-    static constexpr uint32_t bytes = GL + NS * 4 * GWS;
-    static constexpr uint32_t tx = kKC + kU;
-    static constexpr uint32_t full_count = kProdThreads + 1;
+    static constexpr uint32_t KB = W + NS * kKC;                   // k (scalar gate) or kg (per-key-dim gate)
+    static constexpr uint32_t U = KB + NS * kKC;
+    static constexpr uint32_t X = U + NS * kU;
+    static constexpr uint32_t SH = X + 2 * kRecWarps * kX;
+    static constexpr uint32_t SV = SH + kRecWarps * kSH;
+    static constexpr uint32_t GAM = SV + kRecWarps * kSV;          // gamma rows [NS][C] (scalar gate)
+    static constexpr uint32_t DEC = GAM + NS * C * 4;              // exp(G_last) [NS][GW]
+    static constexpr uint32_t bytes = DEC + NS * GW * 4;
+    static constexpr uint32_t tx = (PER_K ? 1 : 2) * kKC + kU;
+    static constexpr uint32_t full_count = 32 * kProdWarps + 1;
 };
 
 template <int K, int C, bool PER_K>
-__global__ void __launch_bounds__(kThreads, 1)
-scan_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap mu,
-                const __grid_constant__ CUtensorMap mvn, const __grid_constant__ CUtensorMap mck,
-                const bf16* __restrict__ k, const float* __restrict__ g_cum, const float* __restrict__ h0,
-                int has_ckpt, float* __restrict__ h_final, int T, int H, int V, unsigned int* err) {
+__global__ void __launch_bounds__(MScanLayout<K, C, PER_K>::kThreads, 1)
+scan_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap mk,
+                const __grid_constant__ CUtensorMap mu, const bf16* __restrict__ k, const float* __restrict__ g_cum,
+                const float* __restrict__ h0, bf16* __restrict__ h_ckpt, bf16* __restrict__ v_new,
+                float* __restrict__ h_final, int T, int H, int V, unsigned int* err) {
     using L = MScanLayout<K, C, PER_K>;
-    constexpr int GW = L::GW;
-    constexpr int NJ = K / 8;      // n-tiles of h^T (over K)
-    constexpr int NT8 = C / 8;     // n-tiles of D (over the chunk's tokens)
+    constexpr int GW = L::GW, KH = L::KH, NT8 = L::NT8;
+    constexpr int NJH = KH / 8;    // n-tiles of this warp's part of h^T
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    float* sGL = reinterpret_cast<float*>(sm + L::GL);
     __shared__ uint64_t full[L::NS], empty[L::NS];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -90,86 +103,107 @@ scan_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ 
     if (warp >= kRecWarps) {
         // ---------------------------------------------------------------- producers
         const int pt = tid - 32 * kRecWarps;
-        constexpr int LC = K / 8;
-        constexpr int RSTEP = kProdThreads / LC;
-        constexpr int NI = C / RSTEP;
-        constexpr int GV = PER_K ? 8 : 1;
-        const int lc = pt % LC, r0 = pt / LC;
-        // Two register sets: the global loads of chunk c+2 are in flight while
-        // chunk c+1 is built, so their latency hides behind a whole chunk step.
-        struct Staged {
-            uint4 kr[NI];
-            float gr[NI][GV], gl8[GV];
-        };
-        Staged sa, sb;
-        auto load_chunk = [&](int c, Staged& st) {   // all of a chunk's global loads issued together
-            const int t0 = c * C;
-            const float* gl = g_cum + row(t0 + C - 1) * GW;
+        float* sDec = reinterpret_cast<float*>(sm + L::DEC);
+        if constexpr (!PER_K) {
+            // one warp: TMA w, k, u; gamma_t = exp(G_last - G_t) and exp(G_last) from G
+            float* sGam = reinterpret_cast<float*>(sm + L::GAM);
+            constexpr int GPL = C / 32;                // G values per lane
+            float gn[GPL], gln;                        // next chunk's G, loaded a chunk ahead
+            auto load_g = [&](int c) {
 #pragma unroll
-            for (int j = 0; j < NI; ++j) {
-                const int t = r0 + j * RSTEP;
-                st.kr[j] = *reinterpret_cast<const uint4*>(k + row(t0 + t) * K + lc * 8);
-                if constexpr (PER_K) {
+                for (int i = 0; i < GPL; ++i) gn[i] = g_cum[row(c * C + lane + 32 * i)];
+                gln = g_cum[row(c * C + C - 1)];
+            };
+            if (NT > 0) load_g(0);
+            for (int c = 0; c < NT; ++c) {
+                const int s = c % L::NS;
+                float gc[GPL], glc = gln;
+#pragma unroll
+                for (int i = 0; i < GPL; ++i) gc[i] = gn[i];
+                if (c + 1 < NT) load_g(c + 1);
+                if (!bw::mbar_wait(&empty[s], ((c / L::NS) & 1) ^ 1, err, kDeviceErrTimeout)) break;
+                const int t0 = c * C;
+                if (lane == 0) {
+                    bw::mbar_arrive_expect_tx(&full[s], L::tx);
+#pragma unroll
+                    for (int a = 0; a < K / 64; ++a) {
+                        bw::tma_load_4d(sm + L::W + s * L::kKC + a * C * 128, &mw, &full[s], a * 64, h, t0, b);
+                        bw::tma_load_4d(sm + L::KB + s * L::kKC + a * C * 128, &mk, &full[s], a * 64, h, t0, b);
+                    }
+                    bw::tma_load_4d(sm + L::U + s * L::kU, &mu, &full[s], v0, h, t0, b);
+                    sDec[s] = __expf(glc);
+                }
+#pragma unroll
+                for (int i = 0; i < GPL; ++i) sGam[s * C + lane + 32 * i] = __expf(glc - gc[i]);
+                bw::mbar_arrive(&full[s]);
+            }
+        } else {
+            // four warps: TMA w, u; kg = k exp(G_last - G) built from global loads two chunks ahead
+            constexpr int kProdThreads = 32 * L::kProdWarps;
+            constexpr int LC = K / 8;
+            constexpr int RSTEP = kProdThreads / LC;
+            constexpr int NI = C / RSTEP;
+            const int lc = pt % LC, r0 = pt / LC;
+            struct Staged {
+                uint4 kr[NI];
+                float gr[NI][8], gl8[8];
+            };
+            Staged sa, sb;
+            auto load_chunk = [&](int c, Staged& st) {
+                const int t0 = c * C;
+#pragma unroll
+                for (int j = 0; j < NI; ++j) {
+                    const int t = r0 + j * RSTEP;
+                    st.kr[j] = *reinterpret_cast<const uint4*>(k + row(t0 + t) * K + lc * 8);
                     const float4* gt = reinterpret_cast<const float4*>(g_cum + row(t0 + t) * K + lc * 8);
                     *reinterpret_cast<float4*>(&st.gr[j][0]) = gt[0];
                     *reinterpret_cast<float4*>(&st.gr[j][4]) = gt[1];
-                } else {
-                    st.gr[j][0] = g_cum[row(t0 + t)];
                 }
-            }
-            if constexpr (PER_K) {
-                const float4* g8 = reinterpret_cast<const float4*>(gl + lc * 8);
+                const float4* g8 = reinterpret_cast<const float4*>(g_cum + row(t0 + C - 1) * K + lc * 8);
                 *reinterpret_cast<float4*>(&st.gl8[0]) = g8[0];
                 *reinterpret_cast<float4*>(&st.gl8[4]) = g8[1];
-            } else {
-                st.gl8[0] = gl[0];
-            }
-        };
-        auto produce = [&](int c, const Staged& st) -> bool {
-            const int s = c % L::NS;
-            if (!bw::mbar_wait(&empty[s], ((c / L::NS) & 1) ^ 1, err, kDeviceErrTimeout)) return false;
-            const int t0 = c * C;
-            if (pt == 0) {
-                bw::mbar_arrive_expect_tx(&full[s], L::tx);
+            };
+            auto produce = [&](int c, const Staged& st) -> bool {
+                const int s = c % L::NS;
+                if (!bw::mbar_wait(&empty[s], ((c / L::NS) & 1) ^ 1, err, kDeviceErrTimeout)) return false;
+                const int t0 = c * C;
+                if (pt == 0) {
+                    bw::mbar_arrive_expect_tx(&full[s], L::tx);
 #pragma unroll
-                for (int a = 0; a < K / 64; ++a)
-                    bw::tma_load_4d(sm + L::W + s * L::kKC + a * C * 128, &mw, &full[s], a * 64, h, t0, b);
-                bw::tma_load_4d(sm + L::U + s * L::kU, &mu, &full[s], v0, h, t0, b);
-            }
-            if constexpr (PER_K) {
-                const float* gl = g_cum + row(t0 + C - 1) * GW;
-                for (int d = pt; d < K; d += kProdThreads) sGL[s * L::GWS + d] = gl[d];
-            } else {
-                if (pt == 0) sGL[s * L::GWS] = st.gl8[0];
-            }
-            unsigned char* kg_t = sm + L::KG + s * L::kKC;
-#pragma unroll
-            for (int j = 0; j < NI; ++j) {
-                const int t = r0 + j * RSTEP;
-                const bf16* kv = reinterpret_cast<const bf16*>(&st.kr[j]);
-                float f[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float dg = PER_K ? st.gl8[e % GV] - st.gr[j][e % GV] : st.gl8[0] - st.gr[j][0];
-                    f[e] = __bfloat162float(kv[e]) * __expf(dg);
+                    for (int a = 0; a < K / 64; ++a)
+                        bw::tma_load_4d(sm + L::W + s * L::kKC + a * C * 128, &mw, &full[s], a * 64, h, t0, b);
+                    bw::tma_load_4d(sm + L::U + s * L::kU, &mu, &full[s], v0, h, t0, b);
                 }
-                uint4 p;
-                p.x = bw::pack_bf16(f[0], f[1]); p.y = bw::pack_bf16(f[2], f[3]);
-                p.z = bw::pack_bf16(f[4], f[5]); p.w = bw::pack_bf16(f[6], f[7]);
-                *reinterpret_cast<uint4*>(kg_t + (lc >> 3) * C * 128 + t * 128 + (((lc & 7) ^ (t & 7)) << 4)) = p;
-            }
-            bw::fence_async_shared();
-            bw::mbar_arrive(&full[s]);
-            return true;
-        };
-        if (NT > 0) load_chunk(0, sa);
-        if (NT > 1) load_chunk(1, sb);
-        for (int c = 0; c < NT; c += 2) {
-            if (!produce(c, sa)) break;
-            if (c + 2 < NT) load_chunk(c + 2, sa);
-            if (c + 1 < NT) {
-                if (!produce(c + 1, sb)) break;
-                if (c + 3 < NT) load_chunk(c + 3, sb);
+                if (r0 == 0) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) sDec[s * GW + lc * 8 + e] = __expf(st.gl8[e]);
+                }
+                unsigned char* kg_t = sm + L::KB + s * L::kKC;
+#pragma unroll
+                for (int j = 0; j < NI; ++j) {
+                    const int t = r0 + j * RSTEP;
+                    const bf16* kv = reinterpret_cast<const bf16*>(&st.kr[j]);
+                    float f[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) f[e] = __bfloat162float(kv[e]) * __expf(st.gl8[e] - st.gr[j][e]);
+                    uint4 p;
+                    p.x = bw::pack_bf16(f[0], f[1]); p.y = bw::pack_bf16(f[2], f[3]);
+                    p.z = bw::pack_bf16(f[4], f[5]); p.w = bw::pack_bf16(f[6], f[7]);
+                    *reinterpret_cast<uint4*>(kg_t + (lc >> 3) * C * 128 + t * 128 + (((lc & 7) ^ (t & 7)) << 4)) = p;
+                }
+                bw::fence_async_shared();
+                bw::mbar_arrive(&full[s]);
+                return true;
+            };
+            if (NT > 0) load_chunk(0, sa);
+            if (NT > 1) load_chunk(1, sb);
+            for (int c = 0; c < NT; c += 2) {
+                if (!produce(c, sa)) break;
+                if (c + 2 < NT) load_chunk(c + 2, sa);
+                if (c + 1 < NT) {
+                    if (!produce(c + 1, sb)) break;
+                    if (c + 3 < NT) load_chunk(c + 3, sb);
+                }
             }
         }
         return;
@@ -177,13 +211,17 @@ scan_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ 
 
     // -------------------------------------------------------------------- recurrence warps
     const int g = lane >> 2, q4 = lane & 3;
-    const int vr0 = warp * 16;                         // this warp's columns within the CTA's 32
+    const int vh = warp & 1, kh = warp >> 1;
+    const int vr0 = vh * 16;                           // this warp's columns within the CTA's 32
+    const int d0 = kh * KH;                            // this warp's first key row
     const int mi = lane >> 3, mr = lane & 7;           // ldmatrix/stmatrix: matrix and row this lane addresses
     const int64_t state = ((int64_t)b * H + h) * K;
-    float hT[NJ][4];                                   // h^T[v][d]: (g | g+8, 8j + 2q4 | +1)
+    const float* sGam = reinterpret_cast<const float*>(sm + L::GAM);
+    const float* sDec = reinterpret_cast<const float*>(sm + L::DEC);
+    float hT[NJH][4];                                  // h^T[v][d]: (g | g+8, d0 + 8j + 2q4 | +1)
 #pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-        const int d = 8 * j + 2 * q4;
+    for (int j = 0; j < NJH; ++j) {
+        const int d = d0 + 8 * j + 2 * q4;
         const int va = v0 + vr0 + g, vb = va + 8;
         if (h0) {
             hT[j][0] = h0[(state + d) * V + va];
@@ -194,122 +232,155 @@ scan_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ 
             hT[j][0] = hT[j][1] = hT[j][2] = hT[j][3] = 0.f;
         }
     }
+    // staging rows: 16 bf16 columns (32 bytes), 16-byte halves swapped on every other group of four rows
+    auto stage_off = [](int r, int half) -> uint32_t { return r * 32 + ((half ^ ((r >> 2) & 1)) << 4); };
+    const uint32_t st_h = s_base + L::SH + warp * L::kSH;
+    const uint32_t st_v = s_base + L::SV + warp * L::kSV;
     bool ok = true;
+    bool ready = NT > 0 && bw::mbar_test_wait(&full[0], 0);
     for (int c = 0; c < NT; ++c) {
-        const int s = c % L::NS, hb = c & 1;
+        const int s = c % L::NS;
         const int t0 = c * C;
-        ok = ok && bw::mbar_wait(&full[s], (c / L::NS) & 1, err, kDeviceErrTimeout);
+        if (!ready) ok = ok && bw::mbar_wait(&full[s], (c / L::NS) & 1, err, kDeviceErrTimeout);
         const uint32_t w_t = s_base + L::W + s * L::kKC;
-        const uint32_t kg_t = s_base + L::KG + s * L::kKC;
+        const uint32_t k_t = s_base + L::KB + s * L::kKC;
         const uint32_t u_t = s_base + L::U + s * L::kU;
 
-        // checkpoint c (h before this chunk): stmatrix.trans h^T -> [K][16] staging, TMA store
-        if (has_ckpt) {
-            if (lane == 0) bw::bulk_wait_read<3>();
-            __syncwarp();
-            const uint32_t st = s_base + L::SH + (warp * 2 + hb) * L::kSH;
-#pragma unroll
-            for (int j = 0; j < NJ; j += 2) {
-                const uint32_t r[4] = {wm::pack2(hT[j][0], hT[j][1]), wm::pack2(hT[j][2], hT[j][3]),
-                                       wm::pack2(hT[j + 1][0], hT[j + 1][1]), wm::pack2(hT[j + 1][2], hT[j + 1][3])};
-                const int d = 8 * j + 8 * (mi >> 1) + mr;
-                wm::stsm_x4_t(st + d * 32 + (mi & 1) * 16, r);
-            }
-            bw::fence_async_shared();
-            __syncwarp();
-            if (lane == 0) {
-                bw::tma_store_4d(&mck, sm + L::SH + (warp * 2 + hb) * L::kSH, v0 + vr0, 0, h, b * NT + c);
-                bw::bulk_commit();
-            }
-        }
-
-        // D = h^T w^T  [16 x C]
+        // partial D = h^T[:, my keys] w[:, my keys]^T  [16 x C]
         float D[NT8][4];
 #pragma unroll
         for (int j = 0; j < NT8; ++j) D[j][0] = D[j][1] = D[j][2] = D[j][3] = 0.f;
 #pragma unroll
-        for (int kk = 0; kk < K / 16; ++kk) {
+        for (int kk = 0; kk < KH / 16; ++kk) {
             const uint32_t a[4] = {wm::pack2(hT[2 * kk][0], hT[2 * kk][1]), wm::pack2(hT[2 * kk][2], hT[2 * kk][3]),
                                    wm::pack2(hT[2 * kk + 1][0], hT[2 * kk + 1][1]),
                                    wm::pack2(hT[2 * kk + 1][2], hT[2 * kk + 1][3])};
 #pragma unroll
             for (int jp = 0; jp < NT8; jp += 2) {
-                const int t = 8 * jp + 8 * (mi >> 1) + mr, d = 16 * kk + 8 * (mi & 1);
+                const int t = 8 * jp + 8 * (mi >> 1) + mr, d = d0 + 16 * kk + 8 * (mi & 1);
                 uint32_t bfr[4];
                 wm::ldsm_x4(w_t + (d >> 6) * C * 128 + t * 128 + ((((d & 63) >> 3) ^ (t & 7)) << 4), bfr);
                 wm::mma16816(D[jp], a, bfr[0], bfr[1]);
                 wm::mma16816(D[jp + 1], a, bfr[2], bfr[3]);
             }
         }
-        // v'^T = u^T - D  (u^T in D's fragment layout straight from ldmatrix.trans)
+
+        // checkpoint c (h before this chunk), my [KH x 16] quarter: stmatrix.trans -> staging -> global
+        if (h_ckpt) {
+#pragma unroll
+            for (int j = 0; j < NJH; j += 2) {
+                const uint32_t r[4] = {wm::pack2(hT[j][0], hT[j][1]), wm::pack2(hT[j][2], hT[j][3]),
+                                       wm::pack2(hT[j + 1][0], hT[j + 1][1]), wm::pack2(hT[j + 1][2], hT[j + 1][3])};
+                wm::stsm_x4_t(st_h + stage_off(8 * j + 8 * (mi >> 1) + mr, mi & 1), r);
+            }
+            __syncwarp();
+            bf16* dst = h_ckpt + ((((int64_t)b * NT + c) * H + h) * K + d0) * V + v0 + vr0;
+#pragma unroll
+            for (int i = 0; i < KH / 16; ++i) {
+                const int r = 16 * i + (lane >> 1), half = lane & 1;
+                const uint4 x = wm::lds128(st_h + stage_off(r, half));
+                *reinterpret_cast<uint4*>(dst + (int64_t)r * V + 8 * half) = x;
+            }
+        }
+
+        // u^T fragments (D's layout) ahead of the exchange
+        uint32_t ur[NT8 / 2][4];
 #pragma unroll
         for (int jp = 0; jp < NT8; jp += 2) {
             const int t = 8 * jp + 8 * (mi >> 1) + mr;
-            uint32_t ur[4];
-            wm::ldsm_x4_t(u_t + t * 64 + (vr0 + 8 * (mi & 1)) * 2, ur);
+            const int ch = (vr0 >> 3) + (mi & 1);
+            wm::ldsm_x4_t(u_t + t * 64 + ((ch ^ ((t >> 1) & 3)) << 4), ur[jp / 2]);
+        }
+
+        // D = D_0 + D_1: swap partial sums with the other key half of the same value columns
+        {
+            unsigned char* xb = sm + L::X + (c & 1) * kRecWarps * L::kX;
+            float4* mine = reinterpret_cast<float4*>(xb + warp * L::kX) + lane;
+            const float4* other = reinterpret_cast<const float4*>(xb + (warp ^ 2) * L::kX) + lane;
+#pragma unroll
+            for (int j = 0; j < NT8; ++j) mine[32 * j] = make_float4(D[j][0], D[j][1], D[j][2], D[j][3]);
+            bw::named_bar_sync(1 + vh, 64);
+            if (c + 1 < NT) ready = bw::mbar_test_wait(&full[(c + 1) % L::NS], ((c + 1) / L::NS) & 1);
+#pragma unroll
+            for (int j = 0; j < NT8; ++j) {
+                const float4 o = other[32 * j];
+                D[j][0] += o.x; D[j][1] += o.y; D[j][2] += o.z; D[j][3] += o.w;
+            }
+        }
+        // v'^T = u^T - D
+#pragma unroll
+        for (int jp = 0; jp < NT8; jp += 2) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const __nv_bfloat162 uv = *reinterpret_cast<const __nv_bfloat162*>(&ur[e]);
+                const __nv_bfloat162 uv = *reinterpret_cast<const __nv_bfloat162*>(&ur[jp / 2][e]);
                 float* dd = D[jp + (e >> 1)] + 2 * (e & 1);
                 dd[0] = __bfloat162float(uv.x) - dd[0];
                 dd[1] = __bfloat162float(uv.y) - dd[1];
             }
         }
-        // v_new: stmatrix.trans v'^T -> [C][16] staging, TMA store
-        {
-            if (lane == 0) {
-                if (has_ckpt) bw::bulk_wait_read<3>(); else bw::bulk_wait_read<1>();
-            }
-            __syncwarp();
-            const uint32_t st = s_base + L::SV + (warp * 2 + hb) * L::kSV;
-#pragma unroll
-            for (int jp = 0; jp < NT8; jp += 2) {
-                const uint32_t r[4] = {wm::pack2(D[jp][0], D[jp][1]), wm::pack2(D[jp][2], D[jp][3]),
-                                       wm::pack2(D[jp + 1][0], D[jp + 1][1]), wm::pack2(D[jp + 1][2], D[jp + 1][3])};
-                const int t = 8 * jp + 8 * (mi >> 1) + mr;
-                wm::stsm_x4_t(st + t * 32 + (mi & 1) * 16, r);
-            }
-            bw::fence_async_shared();
-            __syncwarp();
-            if (lane == 0) {
-                bw::tma_store_4d(&mvn, sm + L::SV + (warp * 2 + hb) * L::kSV, v0 + vr0, h, t0, b);
-                bw::bulk_commit();
-            }
-        }
-        // h^T = exp(G_last) h^T + v'^T kg
-        const float* gl = sGL + s * L::GWS;
+
+        // h^T[:, my keys] = exp(G_last) h^T + (v'^T diag(gamma)) k   |   + v'^T kg
         if constexpr (PER_K) {
+            const float* dec = sDec + s * GW + d0;
 #pragma unroll
-            for (int j = 0; j < NJ; ++j) {
-                const float e0 = __expf(gl[8 * j + 2 * q4]), e1 = __expf(gl[8 * j + 2 * q4 + 1]);
-                hT[j][0] *= e0; hT[j][1] *= e1; hT[j][2] *= e0; hT[j][3] *= e1;
+            for (int j = 0; j < NJH; ++j) {
+                const float2 e = *reinterpret_cast<const float2*>(dec + 8 * j + 2 * q4);
+                hT[j][0] *= e.x; hT[j][1] *= e.y; hT[j][2] *= e.x; hT[j][3] *= e.y;
             }
         } else {
-            const float e = __expf(gl[0]);
+            const float e = sDec[s];
 #pragma unroll
-            for (int j = 0; j < NJ; ++j) { hT[j][0] *= e; hT[j][1] *= e; hT[j][2] *= e; hT[j][3] *= e; }
+            for (int j = 0; j < NJH; ++j) { hT[j][0] *= e; hT[j][1] *= e; hT[j][2] *= e; hT[j][3] *= e; }
         }
 #pragma unroll
         for (int kk = 0; kk < C / 16; ++kk) {
-            const uint32_t a[4] = {wm::pack2(D[2 * kk][0], D[2 * kk][1]), wm::pack2(D[2 * kk][2], D[2 * kk][3]),
-                                   wm::pack2(D[2 * kk + 1][0], D[2 * kk + 1][1]),
-                                   wm::pack2(D[2 * kk + 1][2], D[2 * kk + 1][3])};
+            float x0 = 1.f, x1 = 1.f, y0 = 1.f, y1 = 1.f;
+            if constexpr (!PER_K) {
+                const float2 ga = *reinterpret_cast<const float2*>(sGam + s * C + 16 * kk + 2 * q4);
+                const float2 gb = *reinterpret_cast<const float2*>(sGam + s * C + 16 * kk + 8 + 2 * q4);
+                x0 = ga.x; x1 = ga.y; y0 = gb.x; y1 = gb.y;
+            }
+            const uint32_t a[4] = {wm::pack2(D[2 * kk][0] * x0, D[2 * kk][1] * x1),
+                                   wm::pack2(D[2 * kk][2] * x0, D[2 * kk][3] * x1),
+                                   wm::pack2(D[2 * kk + 1][0] * y0, D[2 * kk + 1][1] * y1),
+                                   wm::pack2(D[2 * kk + 1][2] * y0, D[2 * kk + 1][3] * y1)};
 #pragma unroll
-            for (int jp = 0; jp < NJ; jp += 2) {
-                const int t = 16 * kk + 8 * (mi & 1) + mr, d = 8 * jp + 8 * (mi >> 1);
+            for (int jp = 0; jp < NJH; jp += 2) {
+                const int t = 16 * kk + 8 * (mi & 1) + mr, d = d0 + 8 * jp + 8 * (mi >> 1);
                 uint32_t bfr[4];
-                wm::ldsm_x4_t(kg_t + (d >> 6) * C * 128 + t * 128 + ((((d & 63) >> 3) ^ (t & 7)) << 4), bfr);
+                wm::ldsm_x4_t(k_t + (d >> 6) * C * 128 + t * 128 + ((((d & 63) >> 3) ^ (t & 7)) << 4), bfr);
                 wm::mma16816(hT[jp], a, bfr[0], bfr[1]);
                 wm::mma16816(hT[jp + 1], a, bfr[2], bfr[3]);
             }
         }
         __syncwarp();
         if (lane == 0) bw::mbar_arrive(&empty[s]);
+
+        // v_new: this key half stores tokens kh C/2 .. of v'^T; stmatrix.trans -> staging -> global
+        {
+#pragma unroll
+            for (int jp = 0; jp < NT8; jp += 2) {
+                if ((jp >= NT8 / 2) != (kh == 1)) continue;   // static register indices, runtime half
+                const int jq = jp - kh * (NT8 / 2);
+                const uint32_t r[4] = {wm::pack2(D[jp][0], D[jp][1]), wm::pack2(D[jp][2], D[jp][3]),
+                                       wm::pack2(D[jp + 1][0], D[jp + 1][1]), wm::pack2(D[jp + 1][2], D[jp + 1][3])};
+                wm::stsm_x4_t(st_v + stage_off(8 * jq + 8 * (mi >> 1) + mr, mi & 1), r);
+            }
+            __syncwarp();
+            bf16* dst = v_new + (((int64_t)b * T + t0 + kh * (C / 2)) * H + h) * V + v0 + vr0;
+#pragma unroll
+            for (int i = 0; i < C / 32; ++i) {
+                const int r = 16 * i + (lane >> 1), half = lane & 1;
+                const uint4 x = wm::lds128(st_v + stage_off(r, half));
+                *reinterpret_cast<uint4*>(dst + (int64_t)r * H * V + 8 * half) = x;
+            }
+            __syncwarp();
+        }
     }
     if (h_final) {
 #pragma unroll
-        for (int j = 0; j < NJ; ++j) {
-            const int d = 8 * j + 2 * q4;
+        for (int j = 0; j < NJH; ++j) {
+            const int d = d0 + 8 * j + 2 * q4;
             const int va = v0 + vr0 + g, vb = va + 8;
             h_final[(state + d) * V + va] = hT[j][0];
             h_final[(state + d + 1) * V + va] = hT[j][1];
@@ -317,7 +388,6 @@ scan_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ 
             h_final[(state + d + 1) * V + vb] = hT[j][3];
         }
     }
-    if (lane == 0) bw::bulk_wait<0>();
     (void)ok;
 }
 
@@ -325,22 +395,17 @@ template <int K, int C, bool PER_K>
 cudaError_t launch(const Dims& d, const void* k, const void* w, const void* u, const float* g_cum, const float* h0,
                    void* h_ckpt, void* v_new, float* h_final, cudaStream_t s, unsigned int* err) {
     using L = MScanLayout<K, C, PER_K>;
-    CUtensorMap mw, mu, mvn, mck;
-    if (!make_tmap_tokens(&mw, w, d.B, d.T, d.H, K, C) ||
-        !make_tmap_tokens_plain(&mu, u, d.B, d.T, d.H, d.V, kBV, C) ||
-        !make_tmap_tokens_plain(&mvn, v_new, d.B, d.T, d.H, d.V, 16, C))
-        return cudaErrorInvalidValue;
-    // without checkpoints the map is never used; point it at v_new so it still encodes
-    if (!(h_ckpt ? make_tmap_ckpt_plain(&mck, h_ckpt, d.B, d.NT, d.H, K, d.V, 16)
-                 : make_tmap_tokens_plain(&mck, v_new, d.B, d.T, d.H, d.V, 16, C)))
+    CUtensorMap mw, mk, mu;
+    if (!make_tmap_tokens(&mw, w, d.B, d.T, d.H, K, C) || !make_tmap_tokens(&mk, k, d.B, d.T, d.H, K, C) ||
+        !make_tmap_tokens_sw64(&mu, u, d.B, d.T, d.H, d.V, C))
         return cudaErrorInvalidValue;
     auto kern = scan_mma_kernel<K, C, PER_K>;
     const size_t smem = L::bytes + 1024;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const dim3 grid(d.V / kBV, d.H, d.B);
-    kern<<<grid, kThreads, smem, s>>>(mw, mu, mvn, mck, (const bf16*)k, g_cum, h0, h_ckpt != nullptr, h_final, d.T,
-                                      d.H, d.V, err);
+    kern<<<grid, L::kThreads, smem, s>>>(mw, mk, mu, (const bf16*)k, g_cum, h0, (bf16*)h_ckpt, (bf16*)v_new,
+                                         h_final, d.T, d.H, d.V, err);
     return cudaGetLastError();
 }
 

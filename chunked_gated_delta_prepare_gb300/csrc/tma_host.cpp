@@ -90,4 +90,22 @@ bool make_tmap_tokens_sw64(CUtensorMap* map, const void* base, int B, int T, int
     return make_tmap_bf16_4d_mode(map, base, dims, st, box, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
+// Boxes of `cols` columns x `rows` tokens of one (b, h) with the given swizzle.
+bool make_tmap_tokens_box(CUtensorMap* map, const void* base, int B, int T, int H, int D, int cols, int rows,
+                          CUtensorMapSwizzle swizzle) {
+    const uint64_t dims[4] = {(uint64_t)D, (uint64_t)H, (uint64_t)T, (uint64_t)B};
+    const uint64_t st[3] = {(uint64_t)D * 2, (uint64_t)H * D * 2, (uint64_t)T * H * D * 2};
+    const uint32_t box[4] = {(uint32_t)cols, 1, (uint32_t)rows, 1};
+    return make_tmap_bf16_4d_mode(map, base, dims, st, box, swizzle);
+}
+
+// Checkpoint boxes of `cols` columns (of V) x `rows` key rows of one (b, c, h).
+bool make_tmap_ckpt_box(CUtensorMap* map, const void* base, int B, int NT, int H, int K, int V, int cols, int rows,
+                        CUtensorMapSwizzle swizzle) {
+    const uint64_t dims[4] = {(uint64_t)V, (uint64_t)K, (uint64_t)H, (uint64_t)B * NT};
+    const uint64_t st[3] = {(uint64_t)V * 2, (uint64_t)K * V * 2, (uint64_t)H * K * V * 2};
+    const uint32_t box[4] = {(uint32_t)cols, (uint32_t)rows, 1, 1};
+    return make_tmap_bf16_4d_mode(map, base, dims, st, box, swizzle);
+}
+
 }  // namespace gdr

@@ -29,4 +29,11 @@ bool make_tmap_ckpt_plain(CUtensorMap* map, const void* base, int B, int NT, int
 // 32 columns x `rows` tokens with the 64-byte swizzle (16-byte chunk j of row r at j ^ ((r >> 1) & 3)).
 bool make_tmap_tokens_sw64(CUtensorMap* map, const void* base, int B, int T, int H, int D, int rows);
 
+// General boxes: `cols` columns x `rows` tokens (or key rows of a checkpoint), any swizzle.
+// 32-byte swizzle: 16-byte chunk j of row r of a 32-byte-row box sits at j ^ ((r >> 2) & 1).
+bool make_tmap_tokens_box(CUtensorMap* map, const void* base, int B, int T, int H, int D, int cols, int rows,
+                          CUtensorMapSwizzle swizzle);
+bool make_tmap_ckpt_box(CUtensorMap* map, const void* base, int B, int NT, int H, int K, int V, int cols, int rows,
+                        CUtensorMapSwizzle swizzle);
+
 }  // namespace gdr

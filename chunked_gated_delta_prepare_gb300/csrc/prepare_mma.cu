@@ -2,23 +2,31 @@
 // prepare": the gated A, its inverse, w and u per chunk).
 //
 // One CTA of 128 threads per 64-token tile of one (batch, head): one chunk when
-// C = 64, two when C = 32 (kept apart by the block-diagonal structure).  Warp w
-// owns tile rows 16w .. 16w+15 of every product.
+// C = 64, two when C = 32 (kept apart by the block-diagonal structure).  Warp I
+// owns tile rows 16I .. 16I+15 ("block row I") of every matrix, in registers.
 //
 //   TMA      k [64 x K], v [64 x V]  -> shared memory (128-byte swizzle)
 //   SIMT     G = chunk-local cumsum of g (written out as g_cum), beta
 //   mma      S = k k^T            (per-key-dim gate: gated copies k*exp(G-G_ref)
 //                                  and k*exp(G_ref-G), G_ref the chunk's middle row,
 //                                  keep every factor bounded)
-//   SIMT     A_ij = beta_i S_ij exp(G_i - G_j) (i > j, same chunk), X = (I+A)^{-1}
-//            by blocked forward substitution in fp32
-//   mma      w = (X diag(beta)) (k * exp(G)),  u = (X diag(beta)) v
+//   regs     A_ij = beta_i S_ij exp(G_i - G_j) (i > j, same chunk), in S's fragments
+//   solve    X = (I+A)^{-1} by blocks of 16: each warp inverts its diagonal block
+//            in fp32, then level by level (distance from the diagonal)
+//                X_IJ = -X_II sum_{M=J}^{I-1} A_IM X_MJ
+//            on mma.sync with every operand split into bf16 hi + lo parts
+//            (hi*hi + hi*lo + lo*hi: about 16 bits of mantissa, fp32-like), only
+//            the 16 x 16 X blocks passing through shared memory
+//   mma      w = (X diag(beta exp(G))) k,  u = (X diag(beta)) v   (scalar gate)
+//            w = (X diag(beta)) (k * exp(G)), u as above       (per-key-dim gate)
+//            each warp skipping the k-steps where its row of X is zero
 //
 // The products are warp-level mma.sync m16n8k16 (bf16 in, fp32 accumulate) fed
 // by ldmatrix from the swizzled tiles: at these sizes (64 x 64 x 128 and
 // 64 x 128 x 64 per tile) a tcgen05 MMA's fixed ~240-cycle cost per K=16 step
 // makes it slower than mma.sync, and without tensor memory more CTAs fit an SM.
-// beta is folded into the columns of X, so v feeds the MMA as TMA left it.
+// beta (and, for a scalar gate, exp(G)) is folded into the columns of X, so k
+// and v feed the MMA as TMA left them.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -43,20 +51,74 @@ struct PrepLayout {
     static constexpr uint32_t kQ = kV + V * 128;                    // q tile [64][K] (with P)
     static constexpr uint32_t kKa = kQ + (WITH_P ? K * 128 : 0);    // KDA: gated k copies
     static constexpr uint32_t kKb = kKa + (PER_K ? K * 128 : 0);
-    static constexpr uint32_t kF = kKb + (PER_K ? K * 128 : 0);     // fp32 region
-    // fp32 arrays (float offsets from kF)
-    static constexpr int fG = 0;                         // G [64][GW]
-    static constexpr int fB = fG + 64 * GW;              // beta [64]
-    static constexpr int fA = fB + 64;                   // A [64][65]
-    static constexpr int fX = fA + kTile * kLd;          // X [64][65]
-    static constexpr int fR = fX + kTile * kLd;          // solve scratch [3][16][17]
-    static constexpr int fFlag = fR + 3 * 272;           // KDA: exact-path flag
-    static constexpr int nF = fFlag + 4;
-    static constexpr uint32_t bytes = kF + 4 * nF;
-    static constexpr uint32_t kStageBytes = (K + V) * 128;          // w, u staging reuses the fp32 region
-    static_assert(4 * nF >= kStageBytes, "fp32 region must hold the w/u staging");
+    static constexpr uint32_t kF = kKb + (PER_K ? K * 128 : 0);     // scratch region (reused as the w/u staging)
+    // byte offsets from kF
+    static constexpr uint32_t fG = 0;                                // G [64][GW] fp32
+    static constexpr uint32_t fB = fG + 64 * GW * 4;                 // beta [64] fp32
+    static constexpr uint32_t fE = fB + 64 * 4;                      // exp(G) [64] fp32 (scalar gate)
+    static constexpr uint32_t fFlag = fE + 64 * 4;                   // KDA: exact-path flag
+    static constexpr uint32_t fD = fFlag + 16;                       // per warp: A_II, X_II fp32 [16][17] each
+    static constexpr uint32_t kDw = 2 * 16 * 17 * 4;
+    static constexpr uint32_t fXs = (fD + 4 * kDw + 1023) & ~1023u;  // X blocks (M, J): hi, lo bf16 [16][16] each
+    static constexpr uint32_t kXb = 2 * 512;
+    static constexpr uint32_t fSs = fXs + 16 * kXb;                  // per warp: S_IJ hi, lo bf16 [16][16]
+    static constexpr uint32_t fA = fSs + 4 * kXb;                    // KDA exact path: A fp32 [64][65]
+    static constexpr uint32_t scratch = fA + (PER_K ? 64 * 65 * 4 : 0);
+    static constexpr uint32_t kStageBytes = (K + V) * 128;          // w, u staging
+    static constexpr uint32_t region = scratch > kStageBytes ? scratch : kStageBytes;
+    static constexpr uint32_t bytes = kF + region;
     static_assert(!WITH_P || (C == 64 && !PER_K), "P is produced for 64-token chunks and a scalar gate");
 };
+
+// 16 x 16 bf16 block with 32-byte rows: the 16-byte halves swap on every other
+// group of four rows, so 8-row ldmatrix/stmatrix accesses are conflict-free.
+__device__ __forceinline__ uint32_t blk_off(int r, int half) { return r * 32 + ((half ^ ((r >> 2) & 1)) << 4); }
+
+// bf16 hi + lo split of an fp32 pair, packed as mma operands.
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+    const float2 hf = __bfloat1622float2(h);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = wm::pack2(x0 - hf.x, x1 - hf.y);
+}
+
+// A-operand (k-tile) hi/lo parts of a 16 x 16 block held as two C fragments (n-tiles 0, 1).
+__device__ __forceinline__ void split_afrag(const float (&c0)[4], const float (&c1)[4], uint32_t (&hi)[4],
+                                            uint32_t (&lo)[4]) {
+    split2(c0[0], c0[1], hi[0], lo[0]);
+    split2(c0[2], c0[3], hi[1], lo[1]);
+    split2(c1[0], c1[1], hi[2], lo[2]);
+    split2(c1[2], c1[3], hi[3], lo[3]);
+}
+
+// Stores a 16 x 16 block held as two C fragments into hi and lo bf16 blocks (stmatrix).
+__device__ __forceinline__ void store_block_split(uint32_t hi_addr, uint32_t lo_addr, const float (&c0)[4],
+                                                  const float (&c1)[4], int mi, int mr) {
+    uint32_t hi[4], lo[4];
+    split_afrag(c0, c1, hi, lo);
+    const uint32_t off = blk_off(8 * (mi & 1) + mr, mi >> 1);
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(hi_addr + off), "r"(hi[0]),
+                 "r"(hi[1]), "r"(hi[2]), "r"(hi[3])
+                 : "memory");
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(lo_addr + off), "r"(lo[0]),
+                 "r"(lo[1]), "r"(lo[2]), "r"(lo[3])
+                 : "memory");
+}
+
+// acc[2][4] += A (hi, lo) * B, B the 16 x 16 block stored row-major [k][n] as hi and lo parts.
+__device__ __forceinline__ void mma_block_split(float (&acc)[2][4], const uint32_t (&ahi)[4], const uint32_t (&alo)[4],
+                                                uint32_t bhi_addr, uint32_t blo_addr, int mi, int mr) {
+    const uint32_t off = blk_off(8 * (mi & 1) + mr, mi >> 1);
+    uint32_t bh[4], bl[4];
+    wm::ldsm_x4_t(bhi_addr + off, bh);
+    wm::ldsm_x4_t(blo_addr + off, bl);
+    wm::mma16816(acc[0], ahi, bh[0], bh[1]);
+    wm::mma16816(acc[1], ahi, bh[2], bh[3]);
+    wm::mma16816(acc[0], ahi, bl[0], bl[1]);
+    wm::mma16816(acc[1], ahi, bl[2], bl[3]);
+    wm::mma16816(acc[0], alo, bh[0], bh[1]);
+    wm::mma16816(acc[1], alo, bh[2], bh[3]);
+}
 
 // Exponents of the gated k copies are clamped here; a chunk whose gate moves
 // by more than kExpSafe from its middle row takes the exact fp32 path for A.
@@ -74,12 +136,10 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
     constexpr int GW = L::GW;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    float* F = reinterpret_cast<float*>(sm + L::kF);
-    float* sG = F + L::fG;
-    float* sB = F + L::fB;
-    float* sA = F + L::fA;
-    float* sX = F + L::fX;
-    float* sR = F + L::fR;
+    unsigned char* F = sm + L::kF;
+    float* sG = reinterpret_cast<float*>(F + L::fG);
+    float* sB = reinterpret_cast<float*>(F + L::fB);
+    float* sE = reinterpret_cast<float*>(F + L::fE);
     int* sFlag = reinterpret_cast<int*>(F + L::fFlag);
     __shared__ uint64_t bar_tma;
 
@@ -126,6 +186,8 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
         if (C == 64) x1 += __shfl_sync(0xffffffffu, x0, 31);   // one chunk spans both halves
         sG[lane] = x0;
         sG[32 + lane] = x1;
+        sE[lane] = __expf(x0);
+        sE[32 + lane] = __expf(x1);
         if (lane < nvalid) g_cum[row(lane)] = x0;
         if (32 + lane < nvalid) g_cum[row(32 + lane)] = x1;
     }
@@ -180,6 +242,7 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
 
     const int g4 = lane >> 2, q4 = lane & 3, mi = lane >> 3, mr = lane & 7;
     const int i0 = warp * 16 + g4, i1 = i0 + 8;       // the two tile rows of this thread's fragments
+    float Af[8][4];                                   // A block row of this warp as C fragments
     // S = k k^T for this warp's 16 rows: [16 x 64]
     {
         const uint32_t a_t = s_base + (PER_K ? L::kKa : L::kK);
@@ -233,7 +296,7 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
                              : "memory");
             }
         }
-        // A from S: element (i, j) of this thread's fragments
+        // A from S, in place: element (i, j) of this thread's fragments
         const int c0 = (i0 / C) * C;                 // i0 and i1 share a chunk (16-row blocks never straddle one)
         const float b0 = sB[i0], b1 = sB[i1];
 #pragma unroll
@@ -245,63 +308,180 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
                 float a0 = 0.f, a1 = 0.f;
                 if (in && j < i0) a0 = PER_K ? b0 * S[jn][e] : b0 * S[jn][e] * __expf(sG[i0] - sG[j]);
                 if (in && j < i1) a1 = PER_K ? b1 * S[jn][2 + e] : b1 * S[jn][2 + e] * __expf(sG[i1] - sG[j]);
-                sA[i0 * kLd + j] = a0;
-                sA[i1 * kLd + j] = a1;
+                Af[jn][e] = a0;
+                Af[jn][2 + e] = a1;
             }
         }
     }
-    __syncthreads();
-    if (PER_K && *sFlag) {
-        // exact fp32 A for chunks with extreme gates: A_ij = beta_i sum_d k_id k_jd exp(G_id - G_jd)
-        for (int idx = tid; idx < kTile * kTile; idx += 128) {
-            const int i = idx / kTile, j = idx % kTile;
-            if (j >= (i / C) * C && j < i) {
-                float acc = 0.f;
-                for (int d = 0; d < K; ++d) {
-                    const float ki = __bfloat162float(*reinterpret_cast<const bf16*>(sm + L::kK + tile_off(i, d)));
-                    const float kj = __bfloat162float(*reinterpret_cast<const bf16*>(sm + L::kK + tile_off(j, d)));
-                    acc += ki * kj * __expf(sG[i * K + d] - sG[j * K + d]);
-                }
-                sA[i * kLd + j] = sB[i] * acc;
-            }
-        }
+    if (PER_K) {
         __syncthreads();
-    }
-
-    // B operand of w: k * exp(G), row-scaled in place (scalar gate) or into Ka (per-key-dim gate)
-    for (int i = tid; i < kTile * (K / 8); i += 128) {
-        const int r = i / (K / 8), lc = i % (K / 8);
-        const uint32_t off = (uint32_t)((lc >> 3) * 8192 + r * 128 + (((lc & 7) ^ (r & 7)) << 4));
-        const uint4 raw = *reinterpret_cast<const uint4*>(sm + L::kK + off);
-        const bf16* kv = reinterpret_cast<const bf16*>(&raw);
-        float f[8];
+        if (*sFlag) {
+            // exact fp32 A for chunks with extreme gates: A_ij = beta_i sum_d k_id k_jd exp(G_id - G_jd)
+            float* sA = reinterpret_cast<float*>(F + L::fA);
+            for (int idx = tid; idx < kTile * kTile; idx += 128) {
+                const int i = idx / kTile, j = idx % kTile;
+                float a = 0.f;
+                if (j >= (i / C) * C && j < i) {
+                    float acc = 0.f;
+                    for (int d = 0; d < K; ++d) {
+                        const float ki = __bfloat162float(*reinterpret_cast<const bf16*>(sm + L::kK + tile_off(i, d)));
+                        const float kj = __bfloat162float(*reinterpret_cast<const bf16*>(sm + L::kK + tile_off(j, d)));
+                        acc += ki * kj * __expf(sG[i * K + d] - sG[j * K + d]);
+                    }
+                    a = sB[i] * acc;
+                }
+                sA[i * 65 + j] = a;
+            }
+            __syncthreads();
 #pragma unroll
-        for (int e = 0; e < 8; ++e) f[e] = __bfloat162float(kv[e]) * __expf(PER_K ? sG[r * K + lc * 8 + e] : sG[r]);
-        uint4 p;
-        p.x = bw::pack_bf16(f[0], f[1]); p.y = bw::pack_bf16(f[2], f[3]);
-        p.z = bw::pack_bf16(f[4], f[5]); p.w = bw::pack_bf16(f[6], f[7]);
-        *reinterpret_cast<uint4*>(sm + (PER_K ? L::kKa : L::kK) + off) = p;
-    }
-
-    solve_unit_lower<C>(sA, sX, sR, tid);
-
-    // Tb = X diag(beta) as A fragments of this warp's 16 rows (4 k-tiles of 16 tokens)
-    uint32_t ta[4][4];
+            for (int jn = 0; jn < 8; ++jn) {
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-        const int j0 = 16 * kk + 2 * q4, j1 = j0 + 8;
-        const float bj0 = sB[j0], bj0b = sB[j0 + 1], bj1 = sB[j1], bj1b = sB[j1 + 1];
-        ta[kk][0] = wm::pack2(sX[i0 * kLd + j0] * bj0, sX[i0 * kLd + j0 + 1] * bj0b);
-        ta[kk][1] = wm::pack2(sX[i1 * kLd + j0] * bj0, sX[i1 * kLd + j0 + 1] * bj0b);
-        ta[kk][2] = wm::pack2(sX[i0 * kLd + j1] * bj1, sX[i0 * kLd + j1 + 1] * bj1b);
-        ta[kk][3] = wm::pack2(sX[i1 * kLd + j1] * bj1, sX[i1 * kLd + j1 + 1] * bj1b);
+                for (int e = 0; e < 2; ++e) {
+                    const int j = 8 * jn + 2 * q4 + e;
+                    Af[jn][e] = sA[i0 * 65 + j];
+                    Af[jn][2 + e] = sA[i1 * 65 + j];
+                }
+            }
+        }
+        // B operand of w: k * exp(G) per element, into Ka (its gated copy is no longer needed)
+        for (int i = tid; i < kTile * (K / 8); i += 128) {
+            const int r = i / (K / 8), lc = i % (K / 8);
+            const uint32_t off = (uint32_t)((lc >> 3) * 8192 + r * 128 + (((lc & 7) ^ (r & 7)) << 4));
+            const uint4 raw = *reinterpret_cast<const uint4*>(sm + L::kK + off);
+            const bf16* kv = reinterpret_cast<const bf16*>(&raw);
+            float f[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = __bfloat162float(kv[e]) * __expf(sG[r * K + lc * 8 + e]);
+            uint4 p;
+            p.x = bw::pack_bf16(f[0], f[1]); p.y = bw::pack_bf16(f[2], f[3]);
+            p.z = bw::pack_bf16(f[4], f[5]); p.w = bw::pack_bf16(f[6], f[7]);
+            *reinterpret_cast<uint4*>(sm + L::kKa + off) = p;
+        }
     }
-    // the fp32 scratch is dead from here on: it becomes the bf16 staging of w and u
+
+    // ---- X = (I + A)^{-1}: this warp's block row I = warp, blocks X_IJ for J0 <= J <= I
+    constexpr int NB = C / 16;                        // 16-row blocks per chunk
+    const int I = warp, J0 = (I / NB) * NB;           // first block of this warp's chunk
+    float Xr[4][2][4];                                // X_IJ as C fragments (n-tiles of block column J)
+#pragma unroll
+    for (int J = 0; J < 4; ++J)
+#pragma unroll
+        for (int n = 0; n < 2; ++n) Xr[J][n][0] = Xr[J][n][1] = Xr[J][n][2] = Xr[J][n][3] = 0.f;
+    const uint32_t xs_base = s_base + L::kF + L::fXs;            // block (M, J) at (4M + J) * kXb: hi, then lo
+    {
+        // diagonal block: A_II to shared memory, 16 lanes invert it column by column in fp32
+        float* dA = reinterpret_cast<float*>(F + L::fD + warp * L::kDw);
+        float* dX = dA + 16 * 17;
+#pragma unroll
+        for (int J = 0; J < 4; ++J) {
+            if (J != I) continue;
+#pragma unroll
+            for (int n = 0; n < 2; ++n) {
+                const int cc = 8 * n + 2 * q4;
+                dA[g4 * 17 + cc] = Af[2 * J + n][0];
+                dA[g4 * 17 + cc + 1] = Af[2 * J + n][1];
+                dA[(g4 + 8) * 17 + cc] = Af[2 * J + n][2];
+                dA[(g4 + 8) * 17 + cc + 1] = Af[2 * J + n][3];
+            }
+        }
+        __syncwarp();
+        if (lane < 16) {
+            const int c = lane;
+            float x[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                float s = (i == c) ? 1.f : 0.f;
+#pragma unroll
+                for (int j = 0; j < i; ++j) s -= dA[i * 17 + j] * x[j];
+                x[i] = (i < c) ? 0.f : s;
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) dX[i * 17 + c] = x[i];
+        }
+        __syncwarp();
+#pragma unroll
+        for (int J = 0; J < 4; ++J) {
+            if (J != I) continue;
+#pragma unroll
+            for (int n = 0; n < 2; ++n) {
+                const int cc = 8 * n + 2 * q4;
+                Xr[J][n][0] = dX[g4 * 17 + cc];
+                Xr[J][n][1] = dX[g4 * 17 + cc + 1];
+                Xr[J][n][2] = dX[(g4 + 8) * 17 + cc];
+                Xr[J][n][3] = dX[(g4 + 8) * 17 + cc + 1];
+            }
+            if (NB > 1) store_block_split(xs_base + (4 * I + J) * L::kXb, xs_base + (4 * I + J) * L::kXb + 512,
+                                          Xr[J][0], Xr[J][1], mi, mr);
+        }
+    }
+    // X_II as split A operands (left factor of every off-diagonal block of this row)
+    uint32_t xdh[4], xdl[4];
+#pragma unroll
+    for (int J = 0; J < 4; ++J)
+        if (J == I) split_afrag(Xr[J][0], Xr[J][1], xdh, xdl);
+#pragma unroll
+    for (int Lv = 1; Lv < NB; ++Lv) {
+        __syncthreads();                              // blocks of distance < Lv are in shared memory
+        if (I - J0 >= Lv) {
+            const int J = I - Lv;
+            // S_IJ = sum_{M=J}^{I-1} A_IM X_MJ
+            float Sb[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+            for (int M = 0; M < 3; ++M) {
+                if (M < J || M >= I) continue;
+                uint32_t ah[4], al[4];
+                split_afrag(Af[2 * M], Af[2 * M + 1], ah, al);
+                const uint32_t xb = xs_base + (4 * M + J) * L::kXb;
+                mma_block_split(Sb, ah, al, xb, xb + 512, mi, mr);
+            }
+            // X_IJ = -X_II S_IJ  (S_IJ back through this warp's block scratch as the B operand)
+            const uint32_t sb = s_base + L::kF + L::fSs + warp * L::kXb;
+            store_block_split(sb, sb + 512, Sb[0], Sb[1], mi, mr);
+            __syncwarp();
+            float Xb[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            mma_block_split(Xb, xdh, xdl, sb, sb + 512, mi, mr);
+#pragma unroll
+            for (int Jc = 0; Jc < 3; ++Jc) {
+                if (Jc != J) continue;
+#pragma unroll
+                for (int n = 0; n < 2; ++n)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) Xr[Jc][n][e] = -Xb[n][e];
+                if (Lv + 1 < NB)   // a later level reads it
+                    store_block_split(xs_base + (4 * I + Jc) * L::kXb, xs_base + (4 * I + Jc) * L::kXb + 512,
+                                      Xr[Jc][0], Xr[Jc][1], mi, mr);
+            }
+        }
+    }
+
+    // Tb fragments: X diag(beta) for u; X diag(beta exp(G)) for w (scalar gate) or X diag(beta) (per-key-dim)
+    uint32_t tu[4][4], tw[4][4];
+#pragma unroll
+    for (int J = 0; J < 4; ++J) {
+        const int j0 = 16 * J + 2 * q4, j1 = j0 + 8;
+        const float2 ba = *reinterpret_cast<const float2*>(sB + j0), bb = *reinterpret_cast<const float2*>(sB + j1);
+        tu[J][0] = wm::pack2(Xr[J][0][0] * ba.x, Xr[J][0][1] * ba.y);
+        tu[J][1] = wm::pack2(Xr[J][0][2] * ba.x, Xr[J][0][3] * ba.y);
+        tu[J][2] = wm::pack2(Xr[J][1][0] * bb.x, Xr[J][1][1] * bb.y);
+        tu[J][3] = wm::pack2(Xr[J][1][2] * bb.x, Xr[J][1][3] * bb.y);
+        if constexpr (PER_K) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) tw[J][e] = tu[J][e];
+        } else {
+            const float2 ea = *reinterpret_cast<const float2*>(sE + j0), eb = *reinterpret_cast<const float2*>(sE + j1);
+            tw[J][0] = wm::pack2(Xr[J][0][0] * ba.x * ea.x, Xr[J][0][1] * ba.y * ea.y);
+            tw[J][1] = wm::pack2(Xr[J][0][2] * ba.x * ea.x, Xr[J][0][3] * ba.y * ea.y);
+            tw[J][2] = wm::pack2(Xr[J][1][0] * bb.x * eb.x, Xr[J][1][1] * bb.y * eb.y);
+            tw[J][3] = wm::pack2(Xr[J][1][2] * bb.x * eb.x, Xr[J][1][3] * bb.y * eb.y);
+        }
+    }
+    // the scratch is dead from here on: it becomes the bf16 staging of w and u
     __syncthreads();
     unsigned char* stage = sm + L::kF;
-    // out[16 x D] = Tb [16 x 64] * B [64 x D], B = k exp(G) or v read token-major by ldmatrix.trans;
-    // bf16 results to the staging tile (128-byte swizzle, 64-column atoms) by stmatrix
-    auto product_stage = [&](uint32_t b_t, uint32_t st, int D) {
+    // out[16 x D] = T [16 x 64] * B [64 x D], B = k (or k exp(G)) or v read token-major by ldmatrix.trans;
+    // k-steps outside J0 .. I multiply zeros and are skipped.  bf16 results to the staging tile
+    // (128-byte swizzle, 64-column atoms) by stmatrix
+    auto product_stage = [&](const uint32_t (&ta)[4][4], uint32_t b_t, uint32_t st, int D) {
 #pragma unroll 1
         for (int n0 = 0; n0 < D; n0 += 64) {
             float acc[8][4];
@@ -309,6 +489,7 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
             for (int j = 0; j < 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
+                if (kk < J0 || kk > I) continue;
 #pragma unroll
                 for (int jp = 0; jp < 8; jp += 2) {
                     uint32_t bfr[4];
@@ -330,8 +511,8 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
         }
     };
     const uint32_t st_w = bw::smem_u32(stage), st_u = st_w + K * 128;
-    product_stage(s_base + (PER_K ? L::kKa : L::kK), st_w, K);
-    product_stage(s_base + L::kV, st_u, V);
+    product_stage(tw, s_base + (PER_K ? L::kKa : L::kK), st_w, K);
+    product_stage(tu, s_base + L::kV, st_u, V);
     bw::fence_async_shared();
     __syncthreads();
     if (tid == 0 && ok) {

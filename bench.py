@@ -259,7 +259,7 @@ def run_ours(args, wl):
         g_cum = torch.empty_like(g)
         w = torch.empty_like(k)
         u = torch.empty_like(v)
-        P = torch.empty(B, T // C, H, C, C, device=dev, dtype=q.dtype) if C == 64 else None
+        P = torch.empty(B, T // C, H, C, C, device=dev, dtype=q.dtype) if C == 64 and args.p_from == "prepare" else None
         sp = gdr.problem_for(q, v, g, C, None, args.variant)
         kernels = ["prepare", "scan_output"]
 
@@ -397,6 +397,8 @@ def main():
     ap.add_argument("--cpu-heads", type=int, default=32, help="heads in the CPU-oracle baseline sample")
     ap.add_argument("--ref-heads", type=int, default=4, help="heads per step of --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--p-from", choices=["prepare", "scan"], default="prepare",
+                    help="fused path: gated scores P written by the prepare, or formed inside the scan kernel")
     ap.add_argument("--seq-len", type=int, default=None,
                     help="run the workload at another T (small profiling captures only; not a bench line)")
     args = ap.parse_args()

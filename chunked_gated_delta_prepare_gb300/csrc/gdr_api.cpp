@@ -88,8 +88,13 @@ gdr_status pick_forward(const gdr_problem* p, const gdr::Dims& d, Path* path) {
             if (!d.bf16 || d.per_k) return GDR_ERR_UNSUPPORTED;
             *path = Path::Fused;
             return GDR_OK;
-        case GDR_VARIANT_AUTO:   // the staged tensor-core path measures faster than FUSED today
-            *path = d.bf16 ? Path::Tensor : Path::Simt;
+        case GDR_VARIANT_AUTO:
+            // bf16 with a scalar gate and 64-token chunks: FUSED (its prepare also writes the gated
+            // scores, so scan and output run as one kernel) measures fastest; other bf16 problems
+            // take the staged tensor-core kernels; fp32 the exact CUDA-core path
+            if (!d.bf16) *path = Path::Simt;
+            else if (!d.per_k && d.C == 64) *path = Path::Fused;
+            else *path = Path::Tensor;
             return GDR_OK;
         default: return GDR_ERR_UNSUPPORTED;
     }

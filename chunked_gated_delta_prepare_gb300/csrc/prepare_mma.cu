@@ -31,6 +31,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
 #include "blackwell.cuh"
 #include "gdr_internal.h"
 #include "tc_common.cuh"
@@ -51,7 +53,7 @@ struct PrepLayout {
     static constexpr uint32_t kQ = kV + V * 128;                    // q tile [64][K] (with P)
     static constexpr uint32_t kKa = kQ + (WITH_P ? K * 128 : 0);    // KDA: gated k copies
     static constexpr uint32_t kKb = kKa + (PER_K ? K * 128 : 0);
-    static constexpr uint32_t kF = kKb + (PER_K ? K * 128 : 0);     // scratch region (reused as the w/u staging)
+    static constexpr uint32_t kF = kKb + (PER_K ? K * 128 : 0);     // fp32 / block scratch
     // byte offsets from kF
     static constexpr uint32_t fG = 0;                                // G [64][GW] fp32
     static constexpr uint32_t fB = fG + 64 * GW * 4;                 // beta [64] fp32
@@ -59,16 +61,17 @@ struct PrepLayout {
     static constexpr uint32_t fFlag = fE + 64 * 4;                   // KDA: exact-path flag
     static constexpr uint32_t fD = fFlag + 16;                       // per warp: A_II, X_II fp32 [16][17] each
     static constexpr uint32_t kDw = 2 * 16 * 17 * 4;
-    static constexpr uint32_t fXs = (fD + 4 * kDw + 1023) & ~1023u;  // X blocks (M, J): hi, lo bf16 [16][16] each
+    static constexpr uint32_t fXs = (fD + 4 * kDw + 1023) & ~1023u;  // X blocks (M, J), J <= M: hi, lo bf16 [16][16]
     static constexpr uint32_t kXb = 2 * 512;
-    static constexpr uint32_t fSs = fXs + 16 * kXb;                  // per warp: S_IJ hi, lo bf16 [16][16]
+    static constexpr uint32_t fSs = fXs + 10 * kXb;                  // per warp: S_IJ hi, lo bf16 [16][16]
     static constexpr uint32_t fA = fSs + 4 * kXb;                    // KDA exact path: A fp32 [64][65]
     static constexpr uint32_t scratch = fA + (PER_K ? 64 * 65 * 4 : 0);
-    static constexpr uint32_t kStageBytes = (K + V) * 128;          // w, u staging
-    static constexpr uint32_t region = scratch > kStageBytes ? scratch : kStageBytes;
-    static constexpr uint32_t bytes = kF + region;
+    static constexpr uint32_t bytes = kF + scratch;
     static_assert(!WITH_P || (C == 64 && !PER_K), "P is produced for 64-token chunks and a scalar gate");
 };
+
+// Slot of X block (M, J), J <= M, in the packed lower-triangular store.
+__device__ __forceinline__ int xslot(int M, int J) { return M * (M + 1) / 2 + J; }
 
 // 16 x 16 bf16 block with 32-byte rows: the 16-byte halves swap on every other
 // group of four rows, so 8-row ldmatrix/stmatrix accesses are conflict-free.
@@ -126,7 +129,7 @@ constexpr float kExpClamp = 60.f;
 constexpr float kExpSafe = 40.f;
 
 template <int K, int V, int C, bool PER_K, bool WITH_P>
-__global__ void __launch_bounds__(128, WITH_P ? 2 : 3)
+__global__ void __launch_bounds__(128, 3)
 prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
                    const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap mu,
                    const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mp,
@@ -247,53 +250,19 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
     {
         const uint32_t a_t = s_base + (PER_K ? L::kKa : L::kK);
         const uint32_t b_t = s_base + (PER_K ? L::kKb : L::kK);
-        float S[8][4], Pq[WITH_P ? 8 : 1][4];
+        float S[8][4];
 #pragma unroll
         for (int j = 0; j < 8; ++j) S[j][0] = S[j][1] = S[j][2] = S[j][3] = 0.f;
-        if constexpr (WITH_P) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) Pq[j][0] = Pq[j][1] = Pq[j][2] = Pq[j][3] = 0.f;
-        }
 #pragma unroll
         for (int kk = 0; kk < K / 16; ++kk) {
-            uint32_t a[4], aq[4];
+            uint32_t a[4];
             wm::ldsm_x4(a_t + tile_off(warp * 16 + 8 * (mi & 1) + mr, 16 * kk + 8 * (mi >> 1)), a);
-            if constexpr (WITH_P)
-                wm::ldsm_x4(s_base + L::kQ + tile_off(warp * 16 + 8 * (mi & 1) + mr, 16 * kk + 8 * (mi >> 1)), aq);
 #pragma unroll
             for (int jp = 0; jp < 8; jp += 2) {
                 uint32_t bfr[4];
                 wm::ldsm_x4(b_t + tile_off(8 * jp + 8 * (mi >> 1) + mr, 16 * kk + 8 * (mi & 1)), bfr);
                 wm::mma16816(S[jp], a, bfr[0], bfr[1]);
                 wm::mma16816(S[jp + 1], a, bfr[2], bfr[3]);
-                if constexpr (WITH_P) {
-                    wm::mma16816(Pq[jp % (WITH_P ? 8 : 1)], aq, bfr[0], bfr[1]);
-                    wm::mma16816(Pq[(jp + 1) % (WITH_P ? 8 : 1)], aq, bfr[2], bfr[3]);
-                }
-            }
-        }
-        if constexpr (WITH_P) {
-            // P = tril_0(q k^T * exp(G_i - G_j)) -> bf16 into the q tile's place (q is no longer needed),
-            // as a [64][64] tile in the 128-byte swizzle; stored with w and u below
-#pragma unroll
-            for (int jp = 0; jp < 8; jp += 2) {
-                float pv[2][4];
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int jn = jp + hh, j0 = 8 * jn + 2 * q4;
-                    const float* PjR = Pq[jn % (WITH_P ? 8 : 1)];
-                    pv[hh][0] = j0 <= i0 ? PjR[0] * __expf(sG[i0] - sG[j0]) : 0.f;
-                    pv[hh][1] = j0 + 1 <= i0 ? PjR[1] * __expf(sG[i0] - sG[j0 + 1]) : 0.f;
-                    pv[hh][2] = j0 <= i1 ? PjR[2] * __expf(sG[i1] - sG[j0]) : 0.f;
-                    pv[hh][3] = j0 + 1 <= i1 ? PjR[3] * __expf(sG[i1] - sG[j0 + 1]) : 0.f;
-                }
-                const uint32_t r[4] = {wm::pack2(pv[0][0], pv[0][1]), wm::pack2(pv[0][2], pv[0][3]),
-                                       wm::pack2(pv[1][0], pv[1][1]), wm::pack2(pv[1][2], pv[1][3])};
-                __syncwarp();
-                asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(
-                                 s_base + L::kQ + tile_off(warp * 16 + 8 * (mi & 1) + mr, 8 * jp + 8 * (mi >> 1))),
-                             "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
-                             : "memory");
             }
         }
         // A from S, in place: element (i, j) of this thread's fragments
@@ -311,6 +280,46 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
                 Af[jn][e] = a0;
                 Af[jn][2 + e] = a1;
             }
+        }
+    }
+    if constexpr (WITH_P) {
+        // P = tril_0(q k^T * exp(G_i - G_j)) for this warp's rows (key blocks past the diagonal are
+        // zero and skipped) -> bf16 into the q tile's place (each warp overwrites only its own rows of
+        // q, after reading them), as a [64][64] tile in the 128-byte swizzle; stored with w and u below
+        float Pq[8][4];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) Pq[j][0] = Pq[j][1] = Pq[j][2] = Pq[j][3] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < K / 16; ++kk) {
+            uint32_t aq[4];
+            wm::ldsm_x4(s_base + L::kQ + tile_off(warp * 16 + 8 * (mi & 1) + mr, 16 * kk + 8 * (mi >> 1)), aq);
+#pragma unroll
+            for (int jp = 0; jp < 8; jp += 2) {
+                if (jp / 2 > warp) continue;
+                uint32_t bfr[4];
+                wm::ldsm_x4(s_base + L::kK + tile_off(8 * jp + 8 * (mi >> 1) + mr, 16 * kk + 8 * (mi & 1)), bfr);
+                wm::mma16816(Pq[jp], aq, bfr[0], bfr[1]);
+                wm::mma16816(Pq[jp + 1], aq, bfr[2], bfr[3]);
+            }
+        }
+#pragma unroll
+        for (int jp = 0; jp < 8; jp += 2) {
+            float pv[2][4];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int jn = jp + hh, j0 = 8 * jn + 2 * q4;
+                pv[hh][0] = j0 <= i0 ? Pq[jn][0] * __expf(sG[i0] - sG[j0]) : 0.f;
+                pv[hh][1] = j0 + 1 <= i0 ? Pq[jn][1] * __expf(sG[i0] - sG[j0 + 1]) : 0.f;
+                pv[hh][2] = j0 <= i1 ? Pq[jn][2] * __expf(sG[i1] - sG[j0]) : 0.f;
+                pv[hh][3] = j0 + 1 <= i1 ? Pq[jn][3] * __expf(sG[i1] - sG[j0 + 1]) : 0.f;
+            }
+            const uint32_t r[4] = {wm::pack2(pv[0][0], pv[0][1]), wm::pack2(pv[0][2], pv[0][3]),
+                                   wm::pack2(pv[1][0], pv[1][1]), wm::pack2(pv[1][2], pv[1][3])};
+            __syncwarp();
+            asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(
+                             s_base + L::kQ + tile_off(warp * 16 + 8 * (mi & 1) + mr, 8 * jp + 8 * (mi >> 1))),
+                         "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
+                         : "memory");
         }
     }
     if (PER_K) {
@@ -367,7 +376,7 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
     for (int J = 0; J < 4; ++J)
 #pragma unroll
         for (int n = 0; n < 2; ++n) Xr[J][n][0] = Xr[J][n][1] = Xr[J][n][2] = Xr[J][n][3] = 0.f;
-    const uint32_t xs_base = s_base + L::kF + L::fXs;            // block (M, J) at (4M + J) * kXb: hi, then lo
+    const uint32_t xs_base = s_base + L::kF + L::fXs;            // block (M, J) at xslot(M, J) * kXb: hi, then lo
     {
         // diagonal block: A_II to shared memory, 16 lanes invert it column by column in fp32
         float* dA = reinterpret_cast<float*>(F + L::fD + warp * L::kDw);
@@ -410,7 +419,7 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
                 Xr[J][n][2] = dX[(g4 + 8) * 17 + cc];
                 Xr[J][n][3] = dX[(g4 + 8) * 17 + cc + 1];
             }
-            if (NB > 1) store_block_split(xs_base + (4 * I + J) * L::kXb, xs_base + (4 * I + J) * L::kXb + 512,
+            if (NB > 1) store_block_split(xs_base + xslot(I, J) * L::kXb, xs_base + xslot(I, J) * L::kXb + 512,
                                           Xr[J][0], Xr[J][1], mi, mr);
         }
     }
@@ -431,7 +440,7 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
                 if (M < J || M >= I) continue;
                 uint32_t ah[4], al[4];
                 split_afrag(Af[2 * M], Af[2 * M + 1], ah, al);
-                const uint32_t xb = xs_base + (4 * M + J) * L::kXb;
+                const uint32_t xb = xs_base + xslot(M, J) * L::kXb;
                 mma_block_split(Sb, ah, al, xb, xb + 512, mi, mr);
             }
             // X_IJ = -X_II S_IJ  (S_IJ back through this warp's block scratch as the B operand)
@@ -448,7 +457,7 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
 #pragma unroll
                     for (int e = 0; e < 4; ++e) Xr[Jc][n][e] = -Xb[n][e];
                 if (Lv + 1 < NB)   // a later level reads it
-                    store_block_split(xs_base + (4 * I + Jc) * L::kXb, xs_base + (4 * I + Jc) * L::kXb + 512,
+                    store_block_split(xs_base + xslot(I, Jc) * L::kXb, xs_base + xslot(I, Jc) * L::kXb + 512,
                                       Xr[Jc][0], Xr[Jc][1], mi, mr);
             }
         }
@@ -475,52 +484,59 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
             tw[J][3] = wm::pack2(Xr[J][1][2] * bb.x * eb.x, Xr[J][1][3] * bb.y * eb.y);
         }
     }
-    // the scratch is dead from here on: it becomes the bf16 staging of w and u
-    __syncthreads();
-    unsigned char* stage = sm + L::kF;
     // out[16 x D] = T [16 x 64] * B [64 x D], B = k (or k exp(G)) or v read token-major by ldmatrix.trans;
-    // k-steps outside J0 .. I multiply zeros and are skipped.  bf16 results to the staging tile
-    // (128-byte swizzle, 64-column atoms) by stmatrix
-    auto product_stage = [&](const uint32_t (&ta)[4][4], uint32_t b_t, uint32_t st, int D) {
-#pragma unroll 1
-        for (int n0 = 0; n0 < D; n0 += 64) {
-            float acc[8][4];
+    // k-steps outside J0 .. I multiply zeros and are skipped
+    auto product = [&](const uint32_t (&ta)[4][4], uint32_t b_t, int n0, float (&acc)[8][4]) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+        for (int j = 0; j < 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                if (kk < J0 || kk > I) continue;
-#pragma unroll
-                for (int jp = 0; jp < 8; jp += 2) {
-                    uint32_t bfr[4];
-                    wm::ldsm_x4_t(b_t + tile_off(16 * kk + 8 * (mi & 1) + mr, n0 + 8 * jp + 8 * (mi >> 1)), bfr);
-                    wm::mma16816(acc[jp], ta[kk], bfr[0], bfr[1]);
-                    wm::mma16816(acc[jp + 1], ta[kk], bfr[2], bfr[3]);
-                }
-            }
+        for (int kk = 0; kk < 4; ++kk) {
+            if (kk < J0 || kk > I) continue;
 #pragma unroll
             for (int jp = 0; jp < 8; jp += 2) {
-                const uint32_t r[4] = {wm::pack2(acc[jp][0], acc[jp][1]), wm::pack2(acc[jp][2], acc[jp][3]),
-                                       wm::pack2(acc[jp + 1][0], acc[jp + 1][1]),
-                                       wm::pack2(acc[jp + 1][2], acc[jp + 1][3])};
-                asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(
-                                 st + tile_off(warp * 16 + 8 * (mi & 1) + mr, n0 + 8 * jp + 8 * (mi >> 1))),
-                             "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
-                             : "memory");
+                uint32_t bfr[4];
+                wm::ldsm_x4_t(b_t + tile_off(16 * kk + 8 * (mi & 1) + mr, n0 + 8 * jp + 8 * (mi >> 1)), bfr);
+                wm::mma16816(acc[jp], ta[kk], bfr[0], bfr[1]);
+                wm::mma16816(acc[jp + 1], ta[kk], bfr[2], bfr[3]);
             }
         }
     };
-    const uint32_t st_w = bw::smem_u32(stage), st_u = st_w + K * 128;
-    product_stage(tw, s_base + (PER_K ? L::kKa : L::kK), st_w, K);
-    product_stage(tu, s_base + L::kV, st_u, V);
+    // bf16 results into a tile of the same layout (128-byte swizzle, 64-column atoms) by stmatrix
+    auto stage_out = [&](uint32_t st, int n0, const float (&acc)[8][4]) {
+#pragma unroll
+        for (int jp = 0; jp < 8; jp += 2) {
+            const uint32_t r[4] = {wm::pack2(acc[jp][0], acc[jp][1]), wm::pack2(acc[jp][2], acc[jp][3]),
+                                   wm::pack2(acc[jp + 1][0], acc[jp + 1][1]), wm::pack2(acc[jp + 1][2], acc[jp + 1][3])};
+            asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(
+                             st + tile_off(warp * 16 + 8 * (mi & 1) + mr, n0 + 8 * jp + 8 * (mi >> 1))),
+                         "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
+                         : "memory");
+        }
+    };
+    // One tile at a time, the result replacing the tile it was computed from: products of all its
+    // 64-column atoms into registers, a barrier (every warp is done reading it), then the results over it.
+    // This keeps the CTA at three per SM (no separate staging region).
+    auto product_in_place = [&](const uint32_t (&ta)[4][4], uint32_t tile, auto dcols) {
+        constexpr int D = decltype(dcols)::value;
+        float acc[D / 64][8][4];
+#pragma unroll
+        for (int a = 0; a < D / 64; ++a) product(ta, tile, 64 * a, acc[a]);
+        __syncthreads();
+#pragma unroll
+        for (int a = 0; a < D / 64; ++a) stage_out(tile, 64 * a, acc[a]);
+    };
+    // w over the tile it reads (k, or its scaled copy Ka), then u over v
+    const uint32_t w_tile = PER_K ? L::kKa : L::kK;
+    product_in_place(tw, s_base + w_tile, std::integral_constant<int, K>{});
+    product_in_place(tu, s_base + L::kV, std::integral_constant<int, V>{});
     bw::fence_async_shared();
     __syncthreads();
     if (tid == 0 && ok) {
         // rows past T are clipped by the tensor maps
 #pragma unroll
-        for (int a = 0; a < K / 64; ++a) bw::tma_store_4d(&mw, stage + a * 8192, a * 64, h, t0, b);
+        for (int a = 0; a < K / 64; ++a) bw::tma_store_4d(&mw, sm + w_tile + a * 8192, a * 64, h, t0, b);
 #pragma unroll
-        for (int a = 0; a < V / 64; ++a) bw::tma_store_4d(&mu, stage + K * 128 + a * 8192, a * 64, h, t0, b);
+        for (int a = 0; a < V / 64; ++a) bw::tma_store_4d(&mu, sm + L::kV + a * 8192, a * 64, h, t0, b);
         if constexpr (WITH_P) bw::tma_store_4d(&mp, sm + L::kQ, 0, 0, h, b * (T / C) + t0 / C);
         bw::bulk_commit();
         bw::bulk_wait_read<0>();

@@ -82,8 +82,9 @@ typedef enum gdr_gate {
 } gdr_gate;
 
 /* Which kernels to run.  AUTO picks the fastest measured variant that supports
- * the problem: TENSOR for bf16 io, SIMT for fp32 io.  The single-stage entry
- * points run their tensor-core kernel for AUTO, TENSOR and FUSED on bf16 io. */
+ * the problem: FUSED for bf16 io with a scalar gate and 64-token chunks, TENSOR
+ * for other bf16 problems, SIMT for fp32 io.  The single-stage entry points run
+ * their tensor-core kernel for AUTO, TENSOR and FUSED on bf16 io. */
 typedef enum gdr_variant {
     GDR_VARIANT_AUTO = 0,
     GDR_VARIANT_SIMT = 1,     /* fp32 CUDA-core arithmetic throughout (exact-fp32 path) */

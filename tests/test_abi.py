@@ -114,6 +114,17 @@ def test_workspace_size_formula(lib):
         assert lib.gdr_forward_workspace_bytes(ctypes.byref(p)) == want
 
 
+def test_fused_workspace_size_formula(lib):
+    # g_cum, w, u, then (64-token chunks) the gated scores P [B, NT, H, 64, 64] bf16; no v_new or checkpoints
+    r = lambda x: (x + 255) // 256 * 256
+    for (B, T, H, K, V, C) in [(1, 256, 2, 64, 64, 64), (2, 4096, 8, 64, 64, 32), (1, 32768, 32, 128, 128, 64)]:
+        rows = B * T * H
+        want = r(rows * 4) + r(rows * K * 2) + r(rows * V * 2) + (r(rows * C * 2) if C == 64 else 0)
+        for variant in ("fused", "auto" if C == 64 else "fused"):
+            p = gdr.make_problem(B, T, H, K, V, C, 1, False, variant=variant)
+            assert lib.gdr_forward_workspace_bytes(ctypes.byref(p)) == want
+
+
 def test_stage_entry_points_validate(lib):
     p = good()
     P = ctypes.byref(p)

@@ -141,7 +141,8 @@ def test_fused_variant_refuses_per_key_gate():
 
 def test_auto_variant_choice():
     x = make_inputs(1, 128, 2, 64, 64, io_dtype=torch.bfloat16, with_h0=True, seed=13)
-    assert gpu_forward(x, 64, "auto")[2] == "tensor"
+    assert gpu_forward(x, 64, "auto")[2] == "fused"
+    assert gpu_forward(x, 32, "auto")[2] == "tensor"
     xk = make_inputs(1, 128, 2, 64, 64, per_k_gate=True, io_dtype=torch.bfloat16, with_h0=True, seed=13)
     assert gpu_forward(xk, 64, "auto")[2] == "tensor"
     xf = make_inputs(1, 128, 2, 64, 64, io_dtype=torch.float32, with_h0=True, seed=13)

@@ -52,15 +52,18 @@ def peaks():
 
 # Algorithmic HBM bytes per (token, head) of each kernel, and per (batch, head)
 # for the state.  e = io bytes, GW = 4 (scalar gate) or 4K (per-key-dim gate).
-def algorithmic_bytes(wl, kernel: str) -> int:
+# with_p: the prepare also reads q and writes the gated scores P (C x C per
+# chunk, so C e bytes per token), which the fused scan/output kernel reads.
+def algorithmic_bytes(wl, kernel: str, with_p: bool = False) -> int:
     e = 2 if wl.io == "bf16" else 4
     K, V, C = wl.K, wl.V, wl.chunk
     gw = 4 * (K if wl.per_k_gate else 1)
     th = wl.B * wl.T * wl.H
     bh = wl.B * wl.H
     state = (4 * K * V if wl.with_h0 else 0) + 4 * K * V
-    if kernel == "prepare":      # read k, v, g, beta; write w, u, g_cum
-        per = 2 * K * e + 2 * V * e + 2 * gw + e
+    p_bytes = C * e if with_p else 0
+    if kernel == "prepare":      # read k, v, g, beta (+ q); write w, u, g_cum (+ P)
+        per = 2 * K * e + 2 * V * e + 2 * gw + e + (K * e + p_bytes if with_p else 0)
         return th * per
     if kernel == "scan":         # read k, w, u, g_cum; write v_new, checkpoint (K*V*e per chunk)
         per = 2 * K * e + 2 * V * e + gw + (K * V * e) // C
@@ -68,8 +71,8 @@ def algorithmic_bytes(wl, kernel: str) -> int:
     if kernel == "output":       # read q, k, v_new, g_cum, checkpoint; write o
         per = 2 * K * e + 2 * V * e + gw + (K * V * e) // C
         return th * per
-    if kernel == "scan_output":  # read q, k, w, u, g_cum; write o; state in and out
-        per = 3 * K * e + 2 * V * e + gw
+    if kernel == "scan_output":  # read q, k, w, u, g_cum (+ P); write o; state in and out
+        per = 3 * K * e + 2 * V * e + gw + p_bytes
         return th * per + bh * state
     if kernel == "forward":      # the I/O floor: read q, k, v, g, beta, h0; write o, h_final
         per = 2 * K * e + 2 * V * e + gw + e
@@ -254,6 +257,7 @@ def run_ours(args, wl):
     torch.cuda.synchronize()
     variant = gdr.gdr_last_variant()
     staged = variant != "fused"
+    P = None
     if variant == "fused":
         # the two kernels gdr_forward runs on this path, called one by one so each can be timed
         g_cum = torch.empty_like(g)
@@ -329,7 +333,7 @@ def run_ours(args, wl):
     avg_ms = [t / args.steps for t in per_kernel_ms]
     dom = max(range(n), key=lambda i: avg_ms[i])
     dom_name = kernels[dom]
-    dom_bytes = algorithmic_bytes(wl, dom_name)
+    dom_bytes = algorithmic_bytes(wl, dom_name, with_p=variant == "fused" and P is not None)
     achieved = dom_bytes / (avg_ms[dom] / 1e3) / 1e9
     kname = {"prepare": "prepare_mma_kernel", "scan": "scan_mma_kernel", "output": "tc_output_kernel",
              "scan_output": "fused_scan_output_kernel"}[dom_name]

@@ -59,14 +59,21 @@ struct PrepLayout {
     static constexpr uint32_t fB = fG + 64 * GW * 4;                 // beta [64] fp32
     static constexpr uint32_t fE = fB + 64 * 4;                      // exp(G) [64] fp32 (scalar gate)
     static constexpr uint32_t fFlag = fE + 64 * 4;                   // KDA: exact-path flag
-    static constexpr uint32_t fD = fFlag + 16;                       // per warp: A_II, X_II fp32 [16][17] each
+    // The solve's scratch.  With a per-key-dim gate and K = 128 it reuses the 32 KB of G, dead by then
+    // (the last reader is the k exp(G) rescale, a barrier before the solve): two CTAs per SM.
     static constexpr uint32_t kDw = 2 * 16 * 17 * 4;
+    static constexpr uint32_t kSolveBytes = ((4 * kDw + 1023) & ~1023u) + 14 * 2 * 512;
+    static constexpr bool kAliasG = PER_K && 64 * GW * 4 >= kSolveBytes;
+    static constexpr uint32_t fD = kAliasG ? 0 : fFlag + 16;         // per warp: A_II, X_II fp32 [16][17] each
     static constexpr uint32_t fXs = (fD + 4 * kDw + 1023) & ~1023u;  // X blocks (M, J), J <= M: hi, lo bf16 [16][16]
     static constexpr uint32_t kXb = 2 * 512;
     static constexpr uint32_t fSs = fXs + 10 * kXb;                  // per warp: S_IJ hi, lo bf16 [16][16]
-    static constexpr uint32_t fA = fSs + 4 * kXb;                    // KDA exact path: A fp32 [64][65]
-    static constexpr uint32_t scratch = fA + (PER_K ? 64 * 65 * 4 : 0);
+    static constexpr uint32_t solve_end = fSs + 4 * kXb;
+    static constexpr uint32_t scratch = kAliasG ? fFlag + 16 : solve_end;
     static constexpr uint32_t bytes = kF + scratch;
+    static_assert(!kAliasG || solve_end <= 64 * GW * 4, "the solve's scratch fits in G's space");
+    // KDA exact path: A fp32 [64][64] over the Ka and Kb tiles (dead once S = Ka Kb^T is formed)
+    static_assert(!PER_K || 64 * 64 * 4 <= 2 * K * 128, "the exact A fits over Ka and Kb");
     static_assert(!WITH_P || (C == 64 && !PER_K), "P is produced for 64-token chunks and a scalar gate");
 };
 
@@ -326,7 +333,7 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
         __syncthreads();
         if (*sFlag) {
             // exact fp32 A for chunks with extreme gates: A_ij = beta_i sum_d k_id k_jd exp(G_id - G_jd)
-            float* sA = reinterpret_cast<float*>(F + L::fA);
+            float* sA = reinterpret_cast<float*>(sm + L::kKa);   // over the dead Ka and Kb tiles
             for (int idx = tid; idx < kTile * kTile; idx += 128) {
                 const int i = idx / kTile, j = idx % kTile;
                 float a = 0.f;
@@ -339,7 +346,7 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
                     }
                     a = sB[i] * acc;
                 }
-                sA[i * 65 + j] = a;
+                sA[i * 64 + j] = a;
             }
             __syncthreads();
 #pragma unroll
@@ -347,10 +354,11 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int j = 8 * jn + 2 * q4 + e;
-                    Af[jn][e] = sA[i0 * 65 + j];
-                    Af[jn][2 + e] = sA[i1 * 65 + j];
+                    Af[jn][e] = sA[i0 * 64 + j];
+                    Af[jn][2 + e] = sA[i1 * 64 + j];
                 }
             }
+            __syncthreads();   // every warp has its A before Ka is rewritten below
         }
         // B operand of w: k * exp(G) per element, into Ka (its gated copy is no longer needed)
         for (int i = tid; i < kTile * (K / 8); i += 128) {
@@ -366,6 +374,7 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
             p.z = bw::pack_bf16(f[4], f[5]); p.w = bw::pack_bf16(f[6], f[7]);
             *reinterpret_cast<uint4*>(sm + L::kKa + off) = p;
         }
+        __syncthreads();       // G is dead: the solve's scratch reuses its space
     }
 
     // ---- X = (I + A)^{-1}: this warp's block row I = warp, blocks X_IJ for J0 <= J <= I

@@ -33,16 +33,18 @@ template <int K, int V, int C, bool PER_K>
 struct OutLayout {
     static constexpr int NCH = kTile / C;                          // chunks per tile
     static constexpr int GW = PER_K ? K : 1;
+    // With a per-key-dim gate the gate is read from global memory (L2) where needed instead of
+    // being staged (32 KB), k's gated copy is written over k, and P over that once S is formed:
+    // two CTAs per SM.
     static constexpr uint32_t Q = 0;                               // q, then q exp(G) for chunk 0
-    static constexpr uint32_t Kt = Q + K * 128;
+    static constexpr uint32_t Kt = Q + K * 128;                    // k (per-key-dim gate: then k exp(Gref - G))
     static constexpr uint32_t VP = Kt + K * 128;                   // v' [64][V]
     static constexpr uint32_t Hc = VP + V * 128;                   // checkpoints [NCH][K][V]
-    static constexpr uint32_t P = Hc + NCH * K * V * 2;            // P [64][64]
-    static constexpr uint32_t Q1 = P + 8192;                       // C = 32: q exp(G) for chunk 1
-    static constexpr uint32_t Qa = Q1 + (NCH > 1 ? K * 128 : 0);   // per-key-dim gate: gated copies
-    static constexpr uint32_t Kb = Qa + (PER_K ? K * 128 : 0);
-    static constexpr uint32_t F = Kb + (PER_K ? K * 128 : 0);      // fp32: G [64][GW], flag
-    static constexpr uint32_t bytes = F + 4 * (kTile * GW + 4);
+    static constexpr uint32_t P = PER_K ? Kt : Hc + NCH * K * V * 2;   // P [64][64]
+    static constexpr uint32_t Q1 = PER_K ? Hc + NCH * K * V * 2 : P + 8192;   // C = 32: q exp(G) for chunk 1
+    static constexpr uint32_t Qa = Q1 + (NCH > 1 ? K * 128 : 0);   // per-key-dim gate: q exp(G - Gref)
+    static constexpr uint32_t F = Qa + (PER_K ? K * 128 : 0);      // fp32: G [64] (scalar gate), flag
+    static constexpr uint32_t bytes = F + 4 * ((PER_K ? 0 : kTile) + 4);
     static constexpr uint32_t tx = 2 * K * 128 + V * 128 + NCH * K * V * 2;
     static constexpr uint32_t tmem_cols = 256;                     // S at 0 (64 cols), D at 64 (V cols)
 };
@@ -51,14 +53,14 @@ template <int K, int V, int C, bool PER_K>
 __global__ void __launch_bounds__(128, 1)
 tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                  const __grid_constant__ CUtensorMap mvp, const __grid_constant__ CUtensorMap mh,
-                 const float* __restrict__ g_cum, bf16* __restrict__ o, int T, int H, int NT, float scale,
-                 unsigned int* err) {
+                 const float* __restrict__ g_cum, const bf16* __restrict__ k_raw, bf16* __restrict__ o, int T,
+                 int H, int NT, float scale, unsigned int* err) {
     using L = OutLayout<K, V, C, PER_K>;
     constexpr int GW = L::GW;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float* sG = reinterpret_cast<float*>(sm + L::F);
-    int* sFlag = reinterpret_cast<int*>(sG + kTile * GW);
+    int* sFlag = reinterpret_cast<int*>(sG + (PER_K ? 0 : kTile));
     __shared__ uint64_t bar_tma, bar_mma;
     __shared__ uint32_t tslot;
 
@@ -66,6 +68,18 @@ tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
     const int t0 = blockIdx.x * kTile, h = blockIdx.y, b = blockIdx.z;
     const int nvalid = min(kTile, T - t0);
     auto row = [&](int t) -> int64_t { return ((int64_t)b * T + t0 + t) * H + h; };
+    // per-key-dim gate: 8 consecutive G values of tile row t from global memory (zero past T)
+    auto g8 = [&](int t, int d0, float* out) {
+        if (t < nvalid) {
+            const float4* src = reinterpret_cast<const float4*>(g_cum + row(t) * K + d0);
+            const float4 a = src[0], c = src[1];
+            out[0] = a.x; out[1] = a.y; out[2] = a.z; out[3] = a.w;
+            out[4] = c.x; out[5] = c.y; out[6] = c.z; out[7] = c.w;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) out[e] = 0.f;
+        }
+    };
     const uint32_t s_base = bw::smem_u32(sm);
 
     if (tid == 0) {
@@ -99,10 +113,8 @@ tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
                 bw::tma_load_4d(sm + L::Hc + ch * K * V * 2 + a * K * 128, &mh, &bar_tma, a * 64, 0, h, b * NT + c);
         }
     }
-    for (int i = tid; i < kTile * GW; i += 128) {
-        const int t = i / GW;
-        sG[i] = t < nvalid ? g_cum[row(t) * GW + i % GW] : 0.f;
-    }
+    if constexpr (!PER_K)
+        for (int i = tid; i < kTile; i += 128) sG[i] = i < nvalid ? g_cum[row(i)] : 0.f;
     if (L::NCH > 1 && nvalid <= C) {
         // a half tile: the second chunk's checkpoint is absent; give its rows a zero state
         for (int i = tid; i < K * V / 8; i += 128)
@@ -120,12 +132,13 @@ tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
             const uint4 rk = *reinterpret_cast<const uint4*>(sm + L::Kt + off);
             const bf16* qv = reinterpret_cast<const bf16*>(&rq);
             const bf16* kv = reinterpret_cast<const bf16*>(&rk);
-            float fa[8], fb[8];
+            float fa[8], fb[8], gr[8], gf[8];
+            g8(r, lc * 8, gr);
+            g8(ref, lc * 8, gf);
             bool big = false;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                const int d = lc * 8 + e;
-                const float dg = sG[r * K + d] - sG[ref * K + d];
+                const float dg = gr[e] - gf[e];
                 big |= fabsf(dg) > kExpSafe;
                 fa[e] = __bfloat162float(qv[e]) * __expf(fminf(fmaxf(dg, -kExpClamp), kExpClamp));
                 fb[e] = __bfloat162float(kv[e]) * __expf(fminf(fmaxf(-dg, -kExpClamp), kExpClamp));
@@ -137,7 +150,7 @@ tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
             pb.x = bw::pack_bf16(fb[0], fb[1]); pb.y = bw::pack_bf16(fb[2], fb[3]);
             pb.z = bw::pack_bf16(fb[4], fb[5]); pb.w = bw::pack_bf16(fb[6], fb[7]);
             *reinterpret_cast<uint4*>(sm + L::Qa + off) = pa;
-            *reinterpret_cast<uint4*>(sm + L::Kb + off) = pb;
+            *reinterpret_cast<uint4*>(sm + L::Kt + off) = pb;   // over k: each thread rewrites what it read
         }
         bw::fence_async_shared();
     }
@@ -148,7 +161,7 @@ tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         bw::tc_fence_after();
         constexpr uint32_t idesc = bw::idesc_bf16(64, 64, 0, 0);
         const uint32_t a_t = s_base + (PER_K ? L::Qa : L::Q);
-        const uint32_t b_t = s_base + (PER_K ? L::Kb : L::Kt);
+        const uint32_t b_t = s_base + L::Kt;
 #pragma unroll
         for (int kk = 0; kk < K / 16; ++kk) bw::mma_bf16(tmem, desc_kmajor(a_t, kk), desc_kmajor(b_t, kk), idesc, kk > 0);
         bw::mma_commit(&bar_mma);
@@ -172,7 +185,10 @@ tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
                 for (int e = 0; e < 8; ++e) {
                     const int jj = j + e;
                     float x = 0.f;
-                    if (jj >= ch0 && jj <= r) x = PER_K ? s[jj] : s[jj] * __expf(sG[r] - sG[jj]);
+                    if (jj >= ch0 && jj <= r) {
+                        if constexpr (PER_K) x = s[jj];
+                        else x = s[jj] * __expf(sG[r] - sG[jj]);
+                    }
                     pv[e] = x;
                 }
                 uint4 p;
@@ -192,8 +208,11 @@ tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
                 float acc = 0.f;
                 for (int d = 0; d < K; ++d) {
                     const float qi = __bfloat162float(*reinterpret_cast<const bf16*>(sm + L::Q + tile_off(i, d)));
-                    const float kj = __bfloat162float(*reinterpret_cast<const bf16*>(sm + L::Kt + tile_off(j, d)));
-                    acc += qi * kj * __expf(sG[i * K + d] - sG[j * K + d]);
+                    // k's tile now holds its gated copy: raw k and G come from global memory (rare path)
+                    const float kj = j < nvalid ? __bfloat162float(k_raw[row(j) * K + d]) : 0.f;
+                    const float gi = i < nvalid ? g_cum[row(i) * K + d] : 0.f;
+                    const float gj = j < nvalid ? g_cum[row(j) * K + d] : 0.f;
+                    acc += qi * kj * __expf(gi - gj);
                 }
                 *reinterpret_cast<bf16*>(sm + L::P + bw::sw128_offset(i, j)) = __float2bfloat16_rn(acc);
             }
@@ -206,9 +225,15 @@ tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         const uint32_t off = (uint32_t)((lc >> 3) * 8192 + r * 128 + (((lc & 7) ^ (r & 7)) << 4));
         const uint4 raw = *reinterpret_cast<const uint4*>(sm + L::Q + off);
         const bf16* qv = reinterpret_cast<const bf16*>(&raw);
-        float f[8];
+        float f[8], gr[8];
+        if constexpr (PER_K) {
+            g8(r, lc * 8, gr);
+        } else {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) f[e] = __bfloat162float(qv[e]) * __expf(PER_K ? sG[r * K + lc * 8 + e] : sG[r]);
+            for (int e = 0; e < 8; ++e) gr[e] = sG[r];
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = __bfloat162float(qv[e]) * __expf(gr[e]);
         uint4 p;
         p.x = bw::pack_bf16(f[0], f[1]); p.y = bw::pack_bf16(f[2], f[3]);
         p.z = bw::pack_bf16(f[4], f[5]); p.w = bw::pack_bf16(f[6], f[7]);
@@ -276,7 +301,7 @@ cudaError_t launch_output(const Dims& d, const void* q, const void* k, const voi
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const dim3 grid((d.T + kTile - 1) / kTile, d.H, d.B);
-    kern<<<grid, 128, smem, s>>>(mq, mk, mvp, mh, g_cum, (bf16*)o, d.T, d.H, d.NT, d.scale, err);
+    kern<<<grid, 128, smem, s>>>(mq, mk, mvp, mh, g_cum, (const bf16*)k, (bf16*)o, d.T, d.H, d.NT, d.scale, err);
     return cudaGetLastError();
 }
 

@@ -85,7 +85,7 @@ def naive_forward(q, k, v, g, beta, h0, C, scale, *, with_ckpt=True, nthreads=No
     per_k = 1 if g.ndim == 4 else 0
     o = np.zeros((B, T, H, V))
     hf = np.zeros((B, H, K, V))
-    ck = np.zeros((B, T // C, H, K, V)) if with_ckpt else None
+    ck = np.zeros((B, -(-T // C), H, K, V)) if with_ckpt else None
     nthreads = host_cores() if nthreads is None else int(nthreads)
     if vblock is None:  # enough work items for every thread
         items_per_vblock = B * H

@@ -33,6 +33,14 @@ k_beta = k * beta with no exp(G) and leaves the construction of A_g out.  Only
 w = Tinv (k * beta * exp(G)) makes v' = u - w h equal to the token recurrence's
 delta, so that form is used (the page's fragment is not followed there).
 
+A sequence whose length T is not a multiple of C ends in a partial chunk.  It
+is handled as if padded with tokens that have beta = 0, g = 0 and zero q, k, v:
+such a token leaves the state unchanged (S_t = exp(0) S_{t-1} + 0), so the
+padding changes no result; outputs are cut back to T tokens and the partial
+chunk has its checkpoint like any other (NT = ceil(T / C)).  In the chunked
+cumulative gate a padded token repeats the last real value (the cumsum of a
+zero g), which keeps every exp(G_i - G_j) bounded.
+
 Layouts follow the library boundary (head dim last):
   q, k, w [B,T,H,K]; v, u, v_new, o [B,T,H,V]; g, G [B,T,H] or [B,T,H,K];
   beta [B,T,H]; h0, h_final [B,H,K,V]; ckpt [B,NT,H,K,V].
@@ -66,6 +74,20 @@ def _from_chunks(y):
     return np.moveaxis(y, 2, 3).reshape(B, NT * C, H, *rest)
 
 
+def _pad_tokens(x, C, edge=False):
+    """Pad [B,T,...] along the token axis to a multiple of C: zeros, or copies of the last token."""
+    T = x.shape[1]
+    pad = -T % C
+    if pad == 0:
+        return x
+    fill = np.repeat(x[:, -1:], pad, axis=1) if edge else np.zeros((x.shape[0], pad) + x.shape[2:])
+    return np.concatenate([x, fill], axis=1)
+
+
+def _ragged(T, C):
+    return T % C != 0
+
+
 def _gate_vec(G, C):
     """Chunked gate with a trailing key axis: [B,NT,H,C,1] (scalar) or [B,NT,H,C,K]."""
     Gc = _to_chunks(G, C)
@@ -76,8 +98,8 @@ def chunk_cumsum(g, C):
     """Stage 0: G[t] = sum of g[s] for s from the start of t's chunk up to t (inclusive)."""
     g = _f64(g)
     B, T = g.shape[:2]
-    if T % C:
-        raise ValueError("T must be a multiple of the chunk size")
+    if _ragged(T, C):
+        return chunk_cumsum(_pad_tokens(g, C), C)[:, :T]
     gc = g.reshape(B, T // C, C, *g.shape[2:])
     return np.cumsum(gc, axis=2).reshape(g.shape)
 
@@ -103,6 +125,8 @@ def gated_A(k, beta, G, C):
     """A_ij = beta_i sum_d k_id k_jd exp(G_id - G_jd) for i > j, zero elsewhere.
 
     Returned chunked: [B,NT,H,C,C]."""
+    if _ragged(k.shape[1], C):
+        return gated_A(_pad_tokens(_f64(k), C), _pad_tokens(_f64(beta), C), _pad_tokens(_f64(G), C, edge=True), C)
     kc = _to_chunks(_f64(k), C)                 # [B,NT,H,C,K]
     bc = _to_chunks(_f64(beta), C)              # [B,NT,H,C]
     Gc = _gate_vec(_f64(G), C)                  # [B,NT,H,C,1|K]
@@ -119,6 +143,10 @@ def prepare_wy(k, v, g, beta, C):
     """Stage 0 + 1.  Returns dict(G, A, Tinv, w, u); G/w/u in boundary layout,
     A and Tinv chunked [B,NT,H,C,C]."""
     k, v, beta = _f64(k), _f64(v), _f64(beta)
+    T = k.shape[1]
+    if _ragged(T, C):
+        p = prepare_wy(_pad_tokens(k, C), _pad_tokens(v, C), _pad_tokens(_f64(g), C), _pad_tokens(beta, C), C)
+        return dict(p, G=p["G"][:, :T], w=p["w"][:, :T], u=p["u"][:, :T])
     G = chunk_cumsum(g, C)
     A = gated_A(k, beta, G, C)
     Tinv = forward_substitution_inverse(A)
@@ -137,6 +165,10 @@ def scan_h(k, w, u, G, h0, C):
 
     Returns dict(ckpt [B,NT,H,K,V], v_new [B,T,H,V], h_final [B,H,K,V])."""
     k, w, u, G = _f64(k), _f64(w), _f64(u), _f64(G)
+    if _ragged(k.shape[1], C):
+        T = k.shape[1]
+        s = scan_h(_pad_tokens(k, C), _pad_tokens(w, C), _pad_tokens(u, C), _pad_tokens(G, C, edge=True), h0, C)
+        return dict(s, v_new=s["v_new"][:, :T])
     B, T, H, K = k.shape
     V = u.shape[-1]
     NT = T // C
@@ -159,6 +191,9 @@ def gated_causal_scores(q, k, G, C):
     """tril_0(Q~) per chunk, Q~_ij = sum_d q_id k_jd exp(G_id - G_jd), diagonal included.
 
     Returned chunked: [B,NT,H,C,C]."""
+    if _ragged(q.shape[1], C):
+        return gated_causal_scores(_pad_tokens(_f64(q), C), _pad_tokens(_f64(k), C),
+                                   _pad_tokens(_f64(G), C, edge=True), C)
     qc, kc = _to_chunks(_f64(q), C), _to_chunks(_f64(k), C)
     Gc = _gate_vec(_f64(G), C)
     Qt = np.zeros(qc.shape[:-1] + (C,))
@@ -171,6 +206,10 @@ def gated_causal_scores(q, k, G, C):
 def chunk_output(q, k, v_new, ckpt, G, C, scale):
     """Stage 3: o = scale [ (q exp(G)) ckpt[c] + tril_0(Q~) v'_c ]."""
     q, k, v_new, ckpt, G = _f64(q), _f64(k), _f64(v_new), _f64(ckpt), _f64(G)
+    if _ragged(q.shape[1], C):
+        T = q.shape[1]
+        return chunk_output(_pad_tokens(q, C), _pad_tokens(k, C), _pad_tokens(v_new, C), ckpt,
+                            _pad_tokens(G, C, edge=True), C, scale)[:, :T]
     qc, vc = _to_chunks(q, C), _to_chunks(v_new, C)
     Gc = _gate_vec(G, C)
     Qt = gated_causal_scores(q, k, G, C)

@@ -34,7 +34,8 @@
  * Layouts (all float64, contiguous, head dim last):
  *   q, k [B,T,H,K]; v [B,T,H,V]; g [B,T,H] or [B,T,H,K]; beta [B,T,H];
  *   h0 [B,H,K,V] or NULL; o [B,T,H,V]; h_final [B,H,K,V];
- *   ckpt [B,NT,H,K,V] or NULL (NT = T / C).
+ *   ckpt [B,NT,H,K,V] or NULL (NT = ceil(T / C); a last, partial chunk has its
+ *   checkpoint like any other).
  */
 #include <math.h>
 #include <pthread.h>
@@ -72,7 +73,7 @@ static void run_item(const job_t *J, int64_t item) {
     }
     for (int64_t t = 0; t < T; ++t) {
         if (J->ckpt && (t % C) == 0) {
-            double *dst = J->ckpt + (((b * (T / C) + t / C) * H + h) * K) * V;
+            double *dst = J->ckpt + (((b * ((T + C - 1) / C) + t / C) * H + h) * K) * V;
             for (int64_t i = 0; i < K; ++i)
                 for (int64_t jj = 0; jj < nj; ++jj) dst[i * V + j0 + jj] = S[i * nj + jj];
         }
@@ -139,7 +140,6 @@ int oracle_naive_forward(int64_t B, int64_t T, int64_t H, int64_t K, int64_t V, 
                          double *o, double *h_final, double *ckpt,
                          int64_t vblock, int nthreads) {
     if (B <= 0 || T <= 0 || H <= 0 || K <= 0 || V <= 0 || C <= 0) return -1;
-    if (ckpt && (T % C) != 0) return -1;
     if (!q || !k || !v || !g || !beta || !o || !h_final) return -1;
     job_t J;
     memset(&J, 0, sizeof(J));

@@ -288,3 +288,59 @@ def test_stage_functions_compose():
     assert np.array_equal(o, full["o"])
     np.testing.assert_allclose(p["G"][:, 15], d["g"][:, :16].sum(axis=1), atol=1e-15)
     np.testing.assert_allclose(p["G"][:, 16], d["g"][:, 16], atol=0)   # restarts each chunk
+
+
+# ---------------------------------------------------------------- a partial last chunk
+
+@pytest.mark.parametrize("per_k", [False, True])
+@pytest.mark.parametrize("T,C", [(100, 32), (77, 64), (13, 16), (130, 64)])
+def test_partial_last_chunk_matches_explicit_matrices(per_k, T, C):
+    # the explicit matrix recurrence knows nothing of chunks, so a ragged tail that the
+    # chunked form got wrong (a lost token, a bad cumsum pad, a skipped checkpoint) shows here
+    d = small(per_k, T=T, K=6, V=5, seed=T + C)
+    eo, ehf = explicit_matrix_recurrence(d, 0.4)
+    n, c = both(d, C, 0.4)
+    for r in (n, c):
+        assert r["o"].shape == (2, T, 3, 5)
+        np.testing.assert_allclose(r["o"], eo, atol=1e-11)
+        np.testing.assert_allclose(r["h_final"], ehf, atol=1e-11)
+    assert n["ckpt"].shape[1] == -(-T // C) and c["ckpt"].shape[1] == -(-T // C)
+    assert np.abs(n["ckpt"] - c["ckpt"]).max() <= 1e-11
+
+
+@pytest.mark.parametrize("per_k", [False, True])
+def test_partial_chunk_checkpoint_is_the_prefix_state(per_k):
+    # the last (partial) chunk's checkpoint is the state after the whole chunks before it
+    T, C = 100, 32
+    d = small(per_k, T=T, seed=41)
+    full = oracle.naive_forward(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], C, 0.5)
+    T1 = (T // C) * C
+    pre = {n: (x[:, :T1] if n != "h0" else x) for n, x in d.items()}
+    r = oracle.naive_forward(pre["q"], pre["k"], pre["v"], pre["g"], pre["beta"], pre["h0"], C, 0.5)
+    np.testing.assert_allclose(full["ckpt"][:, -1], r["h_final"], atol=1e-12)
+    np.testing.assert_allclose(full["ckpt"][:, :-1], r["ckpt"], atol=1e-12)
+
+
+@pytest.mark.parametrize("per_k", [False, True])
+def test_ragged_chunk_size_invariance(per_k):
+    d = small(per_k, T=90, seed=42)
+    outs = [oracle.forward_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], C, 0.5)
+            for C in (1, 7, 16, 64, 128)]
+    for r in outs[1:]:
+        assert np.abs(r["o"] - outs[0]["o"]).max() <= 1e-10
+        assert np.abs(r["h_final"] - outs[0]["h_final"]).max() <= 1e-10
+
+
+@pytest.mark.parametrize("per_k", [False, True])
+def test_zero_tokens_are_identity_updates(per_k):
+    # beta = 0 and g = 0 make S_t = S_{t-1}: appending such tokens leaves h_final as it was
+    d = small(per_k, T=40, seed=43)
+    r = oracle.naive_forward(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], 8, 0.5)
+    e = {n: (np.concatenate([x, np.zeros((x.shape[0], 9) + x.shape[2:])], axis=1) if n != "h0" else x)
+         for n, x in d.items()}
+    e["q"][:, 40:] = 1.0   # any q reads the unchanged state
+    re = oracle.naive_forward(e["q"], e["k"], e["v"], e["g"], e["beta"], e["h0"], 8, 0.5)
+    np.testing.assert_allclose(re["h_final"], r["h_final"], atol=1e-13)
+    np.testing.assert_allclose(re["o"][:, :40], r["o"], atol=1e-13)
+    np.testing.assert_allclose(re["o"][:, 40:], 0.5 * np.einsum("bhkv,btk->bthv", r["h_final"],
+                                                                np.ones((2, 9, 8))), atol=1e-12)

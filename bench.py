@@ -263,7 +263,7 @@ def run_ours(args, wl):
         g_cum = torch.empty_like(g)
         w = torch.empty_like(k)
         u = torch.empty_like(v)
-        P = torch.empty(B, T // C, H, C, C, device=dev, dtype=q.dtype) if C == 64 and args.p_from == "prepare" else None
+        P = torch.empty(B, -(-T // C), H, C, C, device=dev, dtype=q.dtype) if C == 64 and args.p_from == "prepare" else None
         sp = gdr.problem_for(q, v, g, C, None, args.variant)
         kernels = ["prepare", "scan_output"]
 
@@ -274,7 +274,7 @@ def run_ours(args, wl):
             return [lambda: gdr.gdr_prepare_wyp(sp, q, k, v, g, beta, w, u, g_cum, P),
                     lambda: gdr.gdr_scan_output(sp, q, k, w, u, g_cum, P, h0, o, hf)]
     elif staged:
-        NT = T // C
+        NT = -(-T // C)
         e = q.element_size()
         # the same three kernels gdr_forward runs, called one by one so each can be timed
         g_cum = torch.empty_like(g)

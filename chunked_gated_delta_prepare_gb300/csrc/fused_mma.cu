@@ -103,9 +103,9 @@ fused_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_co
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int v0 = blockIdx.x * kBV, h = blockIdx.y, b = blockIdx.z;
-    const int NT = T / C;
+    const int NT = (T + C - 1) / C;                  // a last, partial chunk runs as zero tokens past T
     const int g = lane >> 2, q4 = lane & 3, mi = lane >> 3, mr = lane & 7;
-    auto row = [&](int t) -> int64_t { return ((int64_t)b * T + t) * H + h; };
+    auto row = [&](int t) -> int64_t { return ((int64_t)b * T + min(t, T - 1)) * H + h; };   // G past T: its last value
 
     if (tid == 0) {
         for (int s = 0; s < NSA; ++s) {
@@ -454,7 +454,7 @@ fused_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_co
         for (int i = 0; i < 2; ++i) {
             const int rr = 8 * i + (lane >> 2), ch = lane & 3;
             const uint4 x = wm::lds128(os + sw64(rr, ch));
-            *reinterpret_cast<uint4*>(dst + (int64_t)rr * H * V + 8 * ch) = x;
+            if (t0 + r0 + rr < T) *reinterpret_cast<uint4*>(dst + (int64_t)rr * H * V + 8 * ch) = x;
         }
         __syncwarp();
     }

@@ -27,7 +27,6 @@ gdr_status check_problem(const gdr_problem* p, gdr::Dims* d) {
     if (p->B <= 0 || p->T <= 0 || p->H <= 0 || p->K <= 0 || p->V <= 0 || p->chunk <= 0) return GDR_ERR_SHAPE;
     if ((p->K != 64 && p->K != 128) || (p->V != 64 && p->V != 128)) return GDR_ERR_SHAPE;
     if (p->chunk != 32 && p->chunk != 64) return GDR_ERR_SHAPE;
-    if (p->T % p->chunk != 0) return GDR_ERR_SHAPE;
     // grid and 32-bit dims limits: T, B*T*H fit int32; H and B*(V/32) fit a grid y/z extent
     if (p->T > INT32_MAX || p->H > kMaxGridYZ || p->B * (p->V / 32) > kMaxGridYZ) return GDR_ERR_SHAPE;
     if (p->B > INT32_MAX / p->T || p->B * p->T > INT32_MAX / p->H) return GDR_ERR_SHAPE;
@@ -39,7 +38,7 @@ gdr_status check_problem(const gdr_problem* p, gdr::Dims* d) {
     d->K = (int)p->K;
     d->V = (int)p->V;
     d->C = (int)p->chunk;
-    d->NT = d->T / d->C;
+    d->NT = (d->T + d->C - 1) / d->C;   // a last, partial chunk counts
     d->per_k = p->gate == GDR_GATE_PER_K;
     d->bf16 = p->io_dtype == GDR_BF16;
     d->scale = p->scale > 0.f ? p->scale : 1.0f / std::sqrt((float)p->K);
@@ -129,8 +128,8 @@ StagedWorkspace plan_staged(const gdr::Dims& d, bool fused) {
         off = round_up(off + rows * d.V * e, 256);
         ws.h_ckpt = off;
         off = round_up(off + (size_t)d.B * d.NT * d.H * d.K * d.V * e, 256);
-    } else if (d.C == 64) {   // ... and reads the prepare's gated causal scores
-        off = round_up(off + rows * (size_t)d.C * e, 256);
+    } else if (d.C == 64) {   // ... and reads the prepare's gated causal scores [B, NT, H, C, C]
+        off = round_up(off + (size_t)d.B * d.NT * d.H * d.C * d.C * e, 256);
     }
     ws.total = off;
     return ws;

@@ -546,7 +546,7 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
         for (int a = 0; a < K / 64; ++a) bw::tma_store_4d(&mw, sm + w_tile + a * 8192, a * 64, h, t0, b);
 #pragma unroll
         for (int a = 0; a < V / 64; ++a) bw::tma_store_4d(&mu, sm + L::kV + a * 8192, a * 64, h, t0, b);
-        if constexpr (WITH_P) bw::tma_store_4d(&mp, sm + L::kQ, 0, 0, h, b * (T / C) + t0 / C);
+        if constexpr (WITH_P) bw::tma_store_4d(&mp, sm + L::kQ, 0, 0, h, b * ((T + C - 1) / C) + t0 / C);
         bw::bulk_commit();
         bw::bulk_wait_read<0>();
     }

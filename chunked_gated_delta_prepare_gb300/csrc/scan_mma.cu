@@ -87,9 +87,10 @@ scan_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ 
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int v0 = blockIdx.x * kBV, h = blockIdx.y, b = blockIdx.z;
-    const int NT = T / C;
+    const int NT = (T + C - 1) / C;                  // a last, partial chunk runs as zero tokens past T
     const uint32_t s_base = bw::smem_u32(sm);
     auto row = [&](int t) -> int64_t { return ((int64_t)b * T + t) * H + h; };
+    auto rowc = [&](int t) -> int64_t { return row(min(t, T - 1)); };   // G past T repeats its last value
 
     if (tid == 0) {
         for (int s = 0; s < L::NS; ++s) {
@@ -111,8 +112,8 @@ scan_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ 
             float gn[GPL], gln;                        // next chunk's G, loaded a chunk ahead
             auto load_g = [&](int c) {
 #pragma unroll
-                for (int i = 0; i < GPL; ++i) gn[i] = g_cum[row(c * C + lane + 32 * i)];
-                gln = g_cum[row(c * C + C - 1)];
+                for (int i = 0; i < GPL; ++i) gn[i] = g_cum[rowc(c * C + lane + 32 * i)];
+                gln = g_cum[rowc(c * C + C - 1)];
             };
             if (NT > 0) load_g(0);
             for (int c = 0; c < NT; ++c) {
@@ -154,12 +155,13 @@ scan_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ 
 #pragma unroll
                 for (int j = 0; j < NI; ++j) {
                     const int t = r0 + j * RSTEP;
-                    st.kr[j] = *reinterpret_cast<const uint4*>(k + row(t0 + t) * K + lc * 8);
-                    const float4* gt = reinterpret_cast<const float4*>(g_cum + row(t0 + t) * K + lc * 8);
+                    st.kr[j] = t0 + t < T ? *reinterpret_cast<const uint4*>(k + row(t0 + t) * K + lc * 8)
+                                          : make_uint4(0u, 0u, 0u, 0u);
+                    const float4* gt = reinterpret_cast<const float4*>(g_cum + rowc(t0 + t) * K + lc * 8);
                     *reinterpret_cast<float4*>(&st.gr[j][0]) = gt[0];
                     *reinterpret_cast<float4*>(&st.gr[j][4]) = gt[1];
                 }
-                const float4* g8 = reinterpret_cast<const float4*>(g_cum + row(t0 + C - 1) * K + lc * 8);
+                const float4* g8 = reinterpret_cast<const float4*>(g_cum + rowc(t0 + C - 1) * K + lc * 8);
                 *reinterpret_cast<float4*>(&st.gl8[0]) = g8[0];
                 *reinterpret_cast<float4*>(&st.gl8[4]) = g8[1];
             };
@@ -372,7 +374,7 @@ scan_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ 
             for (int i = 0; i < C / 32; ++i) {
                 const int r = 16 * i + (lane >> 1), half = lane & 1;
                 const uint4 x = wm::lds128(st_v + stage_off(r, half));
-                *reinterpret_cast<uint4*>(dst + (int64_t)r * H * V + 8 * half) = x;
+                if (t0 + kh * (C / 2) + r < T) *reinterpret_cast<uint4*>(dst + (int64_t)r * H * V + 8 * half) = x;
             }
             __syncwarp();
         }

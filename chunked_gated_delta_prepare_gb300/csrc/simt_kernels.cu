@@ -54,11 +54,13 @@ simt_prepare_kernel(Dims d, const IO* __restrict__ k, const IO* __restrict__ v, 
     const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x;
     const int64_t tok0 = (int64_t)b * d.T + (int64_t)c * C;   // first token of this chunk
+    const int nv = min(C, d.T - c * C);                       // tokens of the chunk before T
     auto row = [&](int t) { return (tok0 + t) * H + h; };    // (token, head) row index
 
-    for (int i = tid; i < C * GW; i += kThreads) Gs[i] = g[row(i / GW) * GW + i % GW];
-    for (int i = tid; i < C; i += kThreads) bs[i] = ld(beta, row(i));
-    for (int i = tid; i < C * K; i += kThreads) ks[(i / K) * KP + i % K] = ld(k, row(i / K) * K + i % K);
+    // tokens past T (a last, partial chunk) read as g = 0, beta = 0, k = v = 0
+    for (int i = tid; i < C * GW; i += kThreads) Gs[i] = i / GW < nv ? g[row(i / GW) * GW + i % GW] : 0.f;
+    for (int i = tid; i < C; i += kThreads) bs[i] = i < nv ? ld(beta, row(i)) : 0.f;
+    for (int i = tid; i < C * K; i += kThreads) ks[(i / K) * KP + i % K] = i / K < nv ? ld(k, row(i / K) * K + i % K) : 0.f;
     __syncthreads();
     // chunk-local inclusive cumsum, one thread per gate column
     for (int col = tid; col < GW; col += kThreads) {
@@ -66,7 +68,7 @@ simt_prepare_kernel(Dims d, const IO* __restrict__ k, const IO* __restrict__ v, 
         for (int t = 0; t < C; ++t) {
             run += Gs[t * GW + col];
             Gs[t * GW + col] = run;
-            g_cum[row(t) * GW + col] = run;
+            if (t < nv) g_cum[row(t) * GW + col] = run;
         }
     }
     __syncthreads();
@@ -110,12 +112,12 @@ simt_prepare_kernel(Dims d, const IO* __restrict__ k, const IO* __restrict__ v, 
         const int i = idx / K, e = idx % K;
         float s = 0.f;
         for (int j = 0; j <= i; ++j) s += Xs[i * CP + j] * ys[j * YP + e];
-        st(w, row(i) * K + e, s);
+        if (i < nv) st(w, row(i) * K + e, s);
     }
     __syncthreads();
     for (int i = tid; i < C * V; i += kThreads) {
         const int t = i / V, e = i % V;
-        ys[t * YP + e] = ld(v, row(t) * V + e) * bs[t];
+        ys[t * YP + e] = t < nv ? ld(v, row(t) * V + e) * bs[t] : 0.f;
     }
     __syncthreads();
     // u = X (v * beta)
@@ -123,7 +125,7 @@ simt_prepare_kernel(Dims d, const IO* __restrict__ k, const IO* __restrict__ v, 
         const int i = idx / V, e = idx % V;
         float s = 0.f;
         for (int j = 0; j <= i; ++j) s += Xs[i * CP + j] * ys[j * YP + e];
-        st(u, row(i) * V + e, s);
+        if (i < nv) st(u, row(i) * V + e, s);
     }
 }
 
@@ -159,8 +161,9 @@ simt_scan_kernel(Dims d, const IO* __restrict__ k, const IO* __restrict__ w, con
     }
     for (int c = 0; c < d.NT; ++c) {
         const int64_t tok0 = (int64_t)b * d.T + (int64_t)c * C;
+        const int nv = min(C, d.T - c * C);   // a last, partial chunk: zero w, k, u past T, G held at its last value
         auto row = [&](int t) { return (tok0 + t) * H + h; };
-        for (int i = tid; i < GW; i += kThreads) Gl[i] = g_cum[row(C - 1) * GW + i];
+        for (int i = tid; i < GW; i += kThreads) Gl[i] = g_cum[row(nv - 1) * GW + i];
         __syncthreads();
         if (h_ckpt) {
             const int64_t ck = (((int64_t)b * d.NT + c) * H + h) * K * V;
@@ -170,10 +173,11 @@ simt_scan_kernel(Dims d, const IO* __restrict__ k, const IO* __restrict__ w, con
         for (int i = tid; i < C * K; i += kThreads) {
             const int t = i / K, e = i % K;
             const int gi = PER_K ? e : 0;
-            ws[t * KP + e] = ld(w, row(t) * K + e);
-            kgs[t * KP + e] = ld(k, row(t) * K + e) * expf(Gl[gi] - g_cum[row(t) * GW + gi]);
+            ws[t * KP + e] = t < nv ? ld(w, row(t) * K + e) : 0.f;
+            kgs[t * KP + e] = t < nv ? ld(k, row(t) * K + e) * expf(Gl[gi] - g_cum[row(t) * GW + gi]) : 0.f;
         }
-        for (int i = tid; i < C * BV; i += kThreads) us[(i / BV) * BVP + i % BV] = ld(u, row(i / BV) * V + v0 + i % BV);
+        for (int i = tid; i < C * BV; i += kThreads)
+            us[(i / BV) * BVP + i % BV] = i / BV < nv ? ld(u, row(i / BV) * V + v0 + i % BV) : 0.f;
         __syncthreads();
         // v' = u - w h
         for (int idx = tid; idx < C * BV; idx += kThreads) {
@@ -182,7 +186,7 @@ simt_scan_kernel(Dims d, const IO* __restrict__ k, const IO* __restrict__ w, con
             for (int e = 0; e < K; ++e) s += ws[t * KP + e] * hs[e * BV + j];
             const float vp = us[t * BVP + j] - s;
             vps[t * BVP + j] = vp;
-            st(v_new, row(t) * V + v0 + j, vp);
+            if (t < nv) st(v_new, row(t) * V + v0 + j, vp);
         }
         __syncthreads();
         // h = exp(G_last) * h + kg^T v'
@@ -225,13 +229,16 @@ simt_output_kernel(Dims d, const IO* __restrict__ q, const IO* __restrict__ k, c
     const int64_t tok0 = (int64_t)b * d.T + (int64_t)c * C;
     auto row = [&](int t) { return (tok0 + t) * H + h; };
     const int64_t ck = (((int64_t)b * d.NT + c) * H + h) * K * V;
+    const int nv = min(C, d.T - c * C);   // a last, partial chunk: zero q, k, v' past T, G held at its last value
 
     for (int i = tid; i < C * K; i += kThreads) {
-        qs[(i / K) * KP + i % K] = ld(q, row(i / K) * K + i % K);
-        ks[(i / K) * KP + i % K] = ld(k, row(i / K) * K + i % K);
+        const bool in = i / K < nv;
+        qs[(i / K) * KP + i % K] = in ? ld(q, row(i / K) * K + i % K) : 0.f;
+        ks[(i / K) * KP + i % K] = in ? ld(k, row(i / K) * K + i % K) : 0.f;
     }
-    for (int i = tid; i < C * GW; i += kThreads) Gs[i] = g_cum[row(i / GW) * GW + i % GW];
-    for (int i = tid; i < C * VT; i += kThreads) vps[(i / VT) * VTP + i % VT] = ld(v_new, row(i / VT) * V + v0 + i % VT);
+    for (int i = tid; i < C * GW; i += kThreads) Gs[i] = g_cum[row(min(i / GW, nv - 1)) * GW + i % GW];
+    for (int i = tid; i < C * VT; i += kThreads)
+        vps[(i / VT) * VTP + i % VT] = i / VT < nv ? ld(v_new, row(i / VT) * V + v0 + i % VT) : 0.f;
     for (int i = tid; i < K * VT; i += kThreads) hs[i] = ld(h_ckpt, ck + (int64_t)(i / VT) * V + v0 + i % VT);
     __syncthreads();
     // Q~_ij = sum_d q_id k_jd exp(G_id - G_jd), j <= i
@@ -262,7 +269,7 @@ simt_output_kernel(Dims d, const IO* __restrict__ q, const IO* __restrict__ k, c
         float s = 0.f;
         for (int e = 0; e < K; ++e) s += qs[i * KP + e] * hs[e * VT + j];
         for (int t = 0; t <= i; ++t) s += Qt[i * CP + t] * vps[t * VTP + j];
-        st(o, row(i) * V + v0 + j, d.scale * s);
+        if (i < nv) st(o, row(i) * V + v0 + j, d.scale * s);
     }
 }
 

@@ -29,7 +29,8 @@
  * - Layouts are contiguous, head dim last ("head-last", as the re-scan page's
  *   host wrapper takes them): q, k, w [B,T,H,K]; v, u, v_new, o [B,T,H,V];
  *   g, g_cum [B,T,H] (scalar gate) or [B,T,H,K] (per-key-dim gate), always fp32;
- *   beta [B,T,H]; h0, h_final [B,H,K,V] fp32; h_ckpt [B,NT,H,K,V] with NT = T/C.
+ *   beta [B,T,H]; h0, h_final [B,H,K,V] fp32; h_ckpt [B,NT,H,K,V] with
+ *   NT = ceil(T/C).
  * - "io" tensors (q, k, v, beta, w, u, v_new, o, h_ckpt) have the problem's
  *   io_dtype: fp32 or bf16.  g, g_cum, h0 and h_final are always fp32.
  * - g is the natural-log per-token decay (<= 0 for a decaying state); the
@@ -39,8 +40,14 @@
  *   GDR_ERR_CUDA.  Waits inside kernels are bounded: if one gives up, the kernel
  *   records GDR_ERR_DEVICE_TIMEOUT in a device error word and exits; read it with
  *   gdr_get_device_status().
- * - Supported: K, V in {64, 128}; chunk C in {32, 64}; T % C == 0; B, H, T >= 1;
+ * - Supported: K, V in {64, 128}; chunk C in {32, 64}; B, H, T >= 1, any T;
  *   every pointer 16-byte aligned.
+ * - A T that is not a multiple of C ends in a partial chunk.  It is computed as
+ *   if the sequence went on to a multiple of C with tokens of beta = 0, g = 0
+ *   and zero q, k, v: each such token leaves the state as it is (S_t = S_{t-1}),
+ *   so every result equals that of the unpadded delta rule.  Nothing past T is
+ *   read or written; the partial chunk has its checkpoint (the state before its
+ *   first token) like any other chunk.
  * - Thread safety: calls may be made from several host threads.  The only
  *   per-call host state is the name of the kernel variant that ran, which is
  *   kept per host thread (gdr_last_variant).

@@ -67,7 +67,7 @@ def good():
 
 
 @pytest.mark.parametrize("field,value,code", [
-    ("T", 100, 2), ("T", 0, 2), ("B", 0, 2), ("H", -1, 2), ("K", 96, 2), ("V", 32, 2), ("chunk", 16, 2),
+    ("T", 0, 2), ("T", -5, 2), ("B", 0, 2), ("H", -1, 2), ("K", 96, 2), ("V", 32, 2), ("chunk", 16, 2),
     ("chunk", 0, 2), ("H", 70000, 2), ("io_dtype", 7, 3), ("gate", 2, 3), ("variant", 9, 9),
     ("scale", float("nan"), 9), ("scale", float("inf"), 9),
 ])
@@ -114,6 +114,24 @@ def test_workspace_size_formula(lib):
         assert lib.gdr_forward_workspace_bytes(ctypes.byref(p)) == want
 
 
+def test_partial_last_chunk_is_accepted_and_checkpointed():
+    # T = 100 with 64-token chunks: two chunks, the second one partial, each with a checkpoint
+    r = lambda x: (x + 255) // 256 * 256
+    p = gdr.make_problem(2, 100, 3, 64, 128, 64, 1, False, variant="tensor")
+    rows = 2 * 100 * 3
+    want = r(rows * 4) + r(rows * 64 * 2) + 2 * r(rows * 128 * 2) + r(2 * 2 * 3 * 64 * 128 * 2)
+    assert lib_bytes(p) == want
+    # the fused path's gated scores are per chunk: [B, NT, H, C, C]
+    p = gdr.make_problem(2, 100, 3, 64, 128, 64, 1, False, variant="fused")
+    assert lib_bytes(p) == r(rows * 4) + r(rows * 64 * 2) + r(rows * 128 * 2) + r(2 * 2 * 3 * 64 * 64 * 2)
+    for T in (1, 31, 33, 65):
+        assert lib_bytes(gdr.make_problem(1, T, 1, 64, 64, 32, 0, True, variant="simt")) > 0
+
+
+def lib_bytes(p):
+    return gdr.load().gdr_forward_workspace_bytes(ctypes.byref(p))
+
+
 def test_fused_workspace_size_formula(lib):
     # g_cum, w, u, then (64-token chunks) the gated scores P [B, NT, H, 64, 64] bf16; no v_new or checkpoints
     r = lambda x: (x + 255) // 256 * 256
@@ -133,7 +151,7 @@ def test_stage_entry_points_validate(lib):
     assert lib.gdr_scan_h(P, 16, 16, 16, 16, None, None, None, None, None) == 1      # v_new required
     assert lib.gdr_scan_h(P, 16, 16, 16, 16, 8, None, 16, None, None) == 4           # h0 misaligned
     assert lib.gdr_chunk_output(P, 16, 16, 16, None, 16, 16, None) == 1              # h_ckpt required
-    p.T = 96
+    p.V = 96
     assert lib.gdr_chunk_output(P, 16, 16, 16, 16, 16, 16, None) == 2
 
 

@@ -105,5 +105,7 @@ def test_seq_len_override_keeps_the_problem_shape():
     wl = workloads.THROUGHPUT.with_tokens(4096)
     assert (wl.B, wl.T, wl.H, wl.K, wl.V, wl.chunk) == (1, 4096, 32, 128, 128, 64)
     assert wl.name == "gdn_bf16_b1_t4096_h32_d128_c64"
+    wl = workloads.THROUGHPUT.with_tokens(100)          # a partial last chunk is a valid problem
+    assert (wl.T, wl.NT) == (100, 2)
     with pytest.raises(ValueError):
-        workloads.THROUGHPUT.with_tokens(100)
+        workloads.THROUGHPUT.with_tokens(0)

@@ -19,7 +19,10 @@ FORWARD_VARIANTS = {"simt": (torch.float32, torch.bfloat16), "tensor": (torch.bf
 # the fused path takes a scalar gate only
 GATES = {"simt": (False, True), "tensor": (False, True), "fused": (False,)}
 SHAPES = [(2, 256, 3, 64, 64, 64), (1, 192, 2, 128, 128, 64), (2, 128, 3, 64, 128, 32),
-          (1, 160, 1, 128, 64, 32), (1, 64, 2, 128, 128, 64), (1, 32, 1, 64, 64, 32)]
+          (1, 160, 1, 128, 64, 32), (1, 64, 2, 128, 128, 64), (1, 32, 1, 64, 64, 32),
+          # a last, partial chunk: 36 of 64 tokens; 13 of 32 (the second half of a 64-token
+          # tile past T); a lone 20-token chunk; 22 of 32 with two batches
+          (2, 100, 3, 64, 64, 64), (1, 77, 2, 128, 128, 32), (1, 20, 1, 128, 64, 64), (2, 150, 1, 64, 128, 32)]
 
 
 def small_cases():
@@ -110,10 +113,46 @@ def _edge_inputs(kind, per_k, dtype):
         g.fill_(-20.0)
     elif kind == "single_chunk":
         return GdrInputs(q=x.q[:, :32], k=x.k[:, :32], v=x.v[:, :32], g=x.g[:, :32], beta=x.beta[:, :32], h0=x.h0)
+    elif kind == "single_token":
+        return GdrInputs(q=x.q[:, :1], k=x.k[:, :1], v=x.v[:, :1], g=x.g[:, :1], beta=x.beta[:, :1], h0=x.h0 * 20)
+    elif kind == "ragged_strong_decay":   # 3 of 32 tokens in the last chunk, every gate at its floor
+        g.fill_(-20.0)
+        return GdrInputs(q=x.q[:, :99], k=x.k[:, :99], v=x.v[:, :99], g=g[:, :99], beta=x.beta[:, :99],
+                         h0=x.h0 * 20)
     return GdrInputs(q=x.q, k=x.k, v=x.v, g=g, beta=beta, h0=x.h0 * 20)
 
 
-@pytest.mark.parametrize("kind", ["beta_zero", "no_decay", "strong_decay", "single_chunk"])
+def _padded(t, T, Tb):
+    """A device copy of t [1, T, ...] in a buffer of Tb >= T tokens whose tail is NaN."""
+    out = torch.full((1, Tb) + tuple(t.shape[2:]), float("nan"), device="cuda", dtype=t.dtype)
+    out[:, :T] = t.to("cuda")
+    return out
+
+
+@pytest.mark.parametrize("T,C", [(100, 64), (77, 32), (1, 64), (33, 32)])
+@pytest.mark.parametrize("variant,dtype,per_k", [(v, d, pk) for v, ds in FORWARD_VARIANTS.items() for d in ds
+                                                  for pk in GATES[v]])
+def test_partial_chunk_touches_nothing_past_T(T, C, variant, dtype, per_k):
+    """Inputs and output sit in buffers with room for whole chunks, NaN past T: a read
+    past T would turn the results NaN and a write past T would overwrite the NaN tail."""
+    H, K, V = 2, 64, 128
+    Tb = -(-T // C) * C + C
+    x = make_inputs(1, T, H, K, V, per_k_gate=per_k, io_dtype=dtype, with_h0=True, seed=21 + T)
+    q, k, v, g, beta = (_padded(t, T, Tb) for t in (x.q, x.k, x.v, x.g, x.beta))
+    p = gdr.make_problem(1, T, H, K, V, C, dtype, per_k, None, variant)
+    o = torch.full((1, Tb, H, V), float("nan"), device="cuda", dtype=dtype)
+    hf = torch.full((1, H, K, V), float("nan"), device="cuda", dtype=torch.float32)
+    nbytes = gdr.gdr_forward_workspace_bytes(p)
+    ws = torch.empty(nbytes, device="cuda", dtype=torch.uint8)
+    gdr.gdr_forward(p, q, k, v, g, beta, x.h0.to("cuda"), o, hf, ws, nbytes)
+    torch.cuda.synchronize()
+    assert gdr.gdr_get_device_status() == 0 and gdr.gdr_last_variant() == variant
+    assert torch.isnan(o[:, T:].float()).all()
+    check_forward(x, o[:, :T], hf, all_pairs(1, H), C, 1.0 / np.sqrt(K), io_name(dtype))
+
+
+@pytest.mark.parametrize("kind", ["beta_zero", "no_decay", "strong_decay", "single_chunk", "single_token",
+                                  "ragged_strong_decay"])
 @pytest.mark.parametrize("variant,dtype,per_k", [(v, d, pk) for v, ds in FORWARD_VARIANTS.items() for d in ds
                                                   for pk in GATES[v]])
 def test_edge_cases(kind, per_k, variant, dtype):
@@ -161,7 +200,7 @@ def test_convenience_forward_refuses_a_small_workspace():
 
 
 def test_invalid_shape_launches_nothing():
-    x = make_inputs(1, 96, 1, 64, 64, io_dtype=torch.bfloat16, seed=11)  # T % C != 0
+    x = make_inputs(1, 96, 1, 64, 32, io_dtype=torch.bfloat16, seed=11)  # V = 32 is not offered
     with pytest.raises(gdr.GdrError) as e:
         gpu_forward(x, 64, "auto")
     assert e.value.status == 2

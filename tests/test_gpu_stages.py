@@ -15,7 +15,9 @@ pytestmark = pytest.mark.gpu
 
 # (B, T, H, K, V, C): several chunks per head, odd head counts, K != V, both chunk sizes
 SHAPES = [(2, 256, 3, 64, 64, 64), (1, 192, 2, 128, 128, 64), (2, 128, 3, 64, 128, 32),
-          (1, 160, 1, 128, 64, 32), (1, 256, 2, 128, 128, 32), (2, 128, 1, 64, 64, 32)]
+          (1, 160, 1, 128, 64, 32), (1, 256, 2, 128, 128, 32), (2, 128, 1, 64, 64, 32),
+          # a last, partial chunk (T not a multiple of C)
+          (2, 100, 3, 64, 64, 64), (1, 77, 2, 128, 128, 32), (1, 20, 1, 128, 64, 64)]
 # per stage: the variants that run it, with the io dtypes each one takes
 BOTH = (torch.float32, torch.bfloat16)
 STAGE_VARIANTS = {
@@ -81,7 +83,7 @@ def test_scan_stage(shape, per_k, variant, dtype, with_h0):
     h0 = None if x.h0 is None else x.h0 * 20          # a state large enough to matter
     ref = chunked.scan_h(x.k, w_r, u_r, G_r, h0, C)
     p = gdr.problem_for(x.q, x.v, x.g, C, variant=variant)
-    NT = T // C
+    NT = -(-T // C)
     h_ckpt = torch.full((B, NT, H, K, V), float("nan"), device="cuda", dtype=dtype)
     v_new = torch.full((B, T, H, V), float("nan"), device="cuda", dtype=dtype)
     h_final = torch.full((B, H, K, V), float("nan"), device="cuda", dtype=torch.float32)
@@ -109,7 +111,7 @@ def test_scan_stage_optional_outputs(shape, per_k, variant, dtype):
     args = (dev(x.k), dev(w_r), dev(u_r), dev(G_r), dev(x.h0))
     v1 = torch.empty(B, T, H, V, device="cuda", dtype=dtype)
     v2 = torch.empty_like(v1)
-    hc = torch.empty(B, T // C, H, K, V, device="cuda", dtype=dtype)
+    hc = torch.empty(B, -(-T // C), H, K, V, device="cuda", dtype=dtype)
     hf = torch.empty(B, H, K, V, device="cuda", dtype=torch.float32)
     gdr.gdr_scan_h(p, *args, hc, v1, hf)
     gdr.gdr_scan_h(p, *args, None, v2, None)
@@ -134,7 +136,8 @@ def test_output_stage(shape, per_k, variant, dtype):
 
 
 SCAN_OUTPUT_SHAPES = [(2, 256, 3, 64, 64, 64), (1, 192, 2, 128, 128, 64), (2, 128, 3, 64, 128, 32),
-                      (1, 160, 1, 128, 64, 32), (1, 64, 2, 128, 128, 64)]
+                      (1, 160, 1, 128, 64, 32), (1, 64, 2, 128, 128, 64), (2, 100, 3, 64, 64, 64),
+                      (1, 77, 1, 128, 128, 32)]
 
 
 @pytest.mark.parametrize("shape", SCAN_OUTPUT_SHAPES, ids=lambda s: "x".join(map(str, s)))
@@ -173,7 +176,8 @@ def test_scan_output_refuses_per_key_gate_and_fp32():
     assert e.value.status == 8
 
 
-@pytest.mark.parametrize("shape", [(2, 256, 3, 64, 64, 64), (1, 192, 2, 128, 128, 64), (1, 320, 1, 128, 64, 64)],
+@pytest.mark.parametrize("shape", [(2, 256, 3, 64, 64, 64), (1, 192, 2, 128, 128, 64), (1, 320, 1, 128, 64, 64),
+                                   (2, 100, 2, 128, 128, 64), (2, 20, 1, 64, 64, 64)],
                          ids=lambda s: "x".join(map(str, s)))
 def test_prepare_with_scores_then_scan_output(shape):
     """gdr_prepare_wyp's P against the oracle's gated causal scores, then
@@ -183,7 +187,7 @@ def test_prepare_with_scores_then_scan_output(shape):
     x = make_inputs(B, T, H, K, V, io_dtype=dtype, with_h0=True, seed=15)
     p = gdr.problem_for(x.q, x.v, x.g, C, scale=0.125)
     q, k, v, g, beta = (dev(t) for t in (x.q, x.k, x.v, x.g, x.beta))
-    NT = T // C
+    NT = -(-T // C)
     w = torch.full_like(k, float("nan"))
     u = torch.full_like(v, float("nan"))
     g_cum = torch.full_like(g, float("nan"))
@@ -202,9 +206,10 @@ def test_prepare_with_scores_then_scan_output(shape):
     w_r, u_r, G_r, P_r = w.cpu(), u.cpu(), g_cum.cpu(), P.cpu()
     scan = chunked.scan_h(x.k, w_r, u_r, G_r, x.h0, C)
     # the output with the GPU's P (rounded) in place of the oracle's scores
-    qc = chunked._to_chunks(chunked._f64(x.q), C)
-    vc = chunked._to_chunks(scan["v_new"], C)
-    Gc = chunked._gate_vec(chunked._f64(G_r), C)
-    o_ref = chunked._from_chunks(0.125 * ((qc * np.exp(Gc)) @ scan["ckpt"] + chunked._f64(P_r) @ vc))
+    # (a partial last chunk: zero q and v' past T, G held at its last value, then cut back to T)
+    qc = chunked._to_chunks(chunked._pad_tokens(chunked._f64(x.q), C), C)
+    vc = chunked._to_chunks(chunked._pad_tokens(scan["v_new"], C), C)
+    Gc = chunked._gate_vec(chunked._pad_tokens(chunked._f64(G_r), C, edge=True), C)
+    o_ref = chunked._from_chunks(0.125 * ((qc * np.exp(Gc)) @ scan["ckpt"] + chunked._f64(P_r) @ vc))[:, :T]
     assert scaled_err(o, o_ref) <= STAGE_TOL["bf16"]
     assert rel_frob(hf, scan["h_final"]) <= STAGE_TOL["bf16"]

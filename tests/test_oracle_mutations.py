@@ -165,3 +165,107 @@ def test_naive_mutant_is_caught(what, old, new, tmp_path):
     assert src.count(old) == 1, f"mutation site not found: {old!r}"
     idx = NAIVE_MUTANTS.index((what, old, new))
     assert _naive_pins_fail(_build_naive(src.replace(old, new), tmp_path, str(idx)))
+
+
+# ------------------------------------------------------------ backward: token reverse mode (C) mutants
+
+ADJ_SRC = os.path.join(ROOT, "oracle", "naive_adjoint.c")
+CHUNKED_BWD_SRC = os.path.join(ROOT, "oracle", "chunked_backward.py")
+
+ADJ_MUTANTS = [
+    ("read-out gradient dropped", "dS[i * V + j] += J->scale * qt[i] * dot[j];", ";"),
+    ("dq read from the state before the token", "s += St[i * V + j] * dot[j];", "s += Sprev[i * V + j] * dot[j];"),
+    ("dbeta taken on delta instead of r", "db += r[j] * dd[j];", "db += bt * r[j] * dd[j];"),
+    ("k's path through r sign flipped", "dkt[i] -= s;", "dkt[i] += s;"),
+    ("k dr^T term dropped from dS~", "dSt[i * V + j] = dS[i * V + j] - kt[i] * dr[j];",
+     "dSt[i * V + j] = dS[i * V + j];"),
+    ("state gradient not decayed", "dS[i * V + j] = dec[i] * dSt[i * V + j];", "dS[i * V + j] = dSt[i * V + j];"),
+]
+
+
+def _adjoint_pins_fail(lib) -> bool:
+    from test_oracle_backward_pins import GRADS, autograd_grads, problem
+    for per_k in (False, True):
+        d, do, dhf = problem(per_k, B=1, T=24, seed=31)
+        ref = autograd_grads(d, do, dhf, 0.45)
+        got = oracle.naive_backward(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], do, dhf, 8, 0.45, lib=lib)
+        for name in GRADS:
+            if np.abs(got[name] - ref[name]).max() > 1e-10 * max(np.abs(ref[name]).max(), 1.0):
+                return True
+    return False
+
+
+def _build_adjoint(src: str, tmp_path, tag: str):
+    c = tmp_path / f"adj_{tag}.c"
+    so = tmp_path / f"adj_{tag}.so"
+    c.write_text(src)
+    subprocess.check_call(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-pthread", str(c), "-o", str(so), "-lm"])
+    return oracle.load_adjoint_library(str(so))
+
+
+def test_unmutated_adjoint_passes_the_pins(tmp_path):
+    with open(ADJ_SRC) as f:
+        assert not _adjoint_pins_fail(_build_adjoint(f.read(), tmp_path, "none"))
+
+
+@pytest.mark.parametrize("what,old,new", ADJ_MUTANTS, ids=[m[0] for m in ADJ_MUTANTS])
+def test_adjoint_mutant_is_caught(what, old, new, tmp_path):
+    with open(ADJ_SRC) as f:
+        src = f.read()
+    assert src.count(old) == 1, f"mutation site not found: {old!r}"
+    assert _adjoint_pins_fail(_build_adjoint(src.replace(old, new), tmp_path, str(ADJ_MUTANTS.index((what, old, new)))))
+
+
+# ------------------------------------------------------------ backward: chunked (numpy) mutants
+
+CHUNKED_BWD_MUTANTS = [
+    ("v' gradient misses the state path", "dvp = dlc[:, c] + kg @ dh", "dvp = dlc[:, c]"),
+    ("reverse scan not decayed", "np.exp(G_last)[..., :, None] * dh", "dh"),
+    ("output score gradient not causal", "dQt = scale * (doc @ np.swapaxes(vpc, -1, -2)) * mask",
+     "dQt = scale * (doc @ np.swapaxes(vpc, -1, -2))"),
+    ("kg's gate gradient sign flipped", "- kc * Rq - dkg * kg", "- kc * Rq + dkg * kg"),
+    ("state decay missing from the last row's gate gradient",
+     " + np.exp(G_L[..., 0, :]) * (h * dhn).sum(axis=-1)", ""),
+    ("dA keeps its diagonal", "dA = np.tril(-TiT @ dT @ TiT, -1)", "dA = np.tril(-TiT @ dT @ TiT)"),
+    ("beta's path through A dropped", " + (dA * M).sum(-1)", ""),
+    ("padded rows' gate gradient lost", "out[:, T - 1] += dG[:, T:].sum(axis=1)", "pass"),
+    ("inclusive instead of reverse cumsum",
+     "out = np.flip(np.cumsum(np.flip(dc, axis=2), axis=2), axis=2).reshape(pad.shape)[:, :T]",
+     "out = np.cumsum(dc, axis=2).reshape(pad.shape)[:, :T]"),
+]
+
+
+def _chunked_bwd_pins_fail(mod) -> bool:
+    from test_oracle_backward_pins import GRADS, problem
+    for per_k in (False, True):
+        for T, C in ((64, 16), (100, 32)):
+            d, do, dhf = problem(per_k, T=T, seed=33 + T)
+            ref = oracle.naive_backward(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], do, dhf, C, 0.4)
+            try:
+                got = mod.backward_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], do, dhf, C, 0.4)
+            except Exception:
+                return True
+            for name in GRADS:
+                if np.abs(got[name] - ref[name]).max() > 1e-10 * max(np.abs(ref[name]).max(), 1.0):
+                    return True
+    return False
+
+
+def _load_chunked_bwd(src: str):
+    mod = types.ModuleType("oracle.chunked_backward_mutant")
+    mod.__package__ = "oracle"
+    exec(compile(src, "chunked_backward_mutant.py", "exec"), mod.__dict__)
+    return mod
+
+
+def test_unmutated_chunked_backward_passes_the_pins():
+    with open(CHUNKED_BWD_SRC) as f:
+        assert not _chunked_bwd_pins_fail(_load_chunked_bwd(f.read()))
+
+
+@pytest.mark.parametrize("what,old,new", CHUNKED_BWD_MUTANTS, ids=[m[0] for m in CHUNKED_BWD_MUTANTS])
+def test_chunked_backward_mutant_is_caught(what, old, new):
+    with open(CHUNKED_BWD_SRC) as f:
+        src = f.read()
+    assert src.count(old) == 1, f"mutation site not found: {old!r}"
+    assert _chunked_bwd_pins_fail(_load_chunked_bwd(src.replace(old, new)))

@@ -135,6 +135,49 @@ StagedWorkspace plan_staged(const gdr::Dims& d, bool fused) {
     return ws;
 }
 
+// gdr_backward scratch: the forward's g_cum, w, u, v_new, h_ckpt (io dtype), then the
+// backward's fp32 intermediates, each 256-byte aligned.
+struct BackwardWorkspace {
+    size_t g_cum, w, u, v_new, h_ckpt, dv_loc, dv_new, dh_ckpt, dk_part, dw, dG_part, total;
+};
+
+BackwardWorkspace plan_backward(const gdr::Dims& d) {
+    const size_t e = d.bf16 ? 2 : 4;
+    const size_t rows = (size_t)d.B * d.T * d.H;
+    const size_t gw = d.per_k ? d.K : 1;
+    const size_t states = (size_t)d.B * d.NT * d.H * d.K * d.V;
+    BackwardWorkspace ws;
+    size_t off = 0;
+    auto take = [&](size_t* field, size_t bytes) { *field = off; off = round_up(off + bytes, 256); };
+    take(&ws.g_cum, rows * gw * 4);
+    take(&ws.w, rows * d.K * e);
+    take(&ws.u, rows * d.V * e);
+    take(&ws.v_new, rows * d.V * e);
+    take(&ws.h_ckpt, states * e);
+    take(&ws.dv_loc, rows * d.V * 4);
+    take(&ws.dv_new, rows * d.V * 4);
+    take(&ws.dh_ckpt, states * 4);
+    take(&ws.dk_part, rows * d.K * 4);
+    take(&ws.dw, rows * d.K * 4);
+    take(&ws.dG_part, rows * gw * 4);
+    ws.total = off;
+    return ws;
+}
+
+// The backward's forward re-scan: tensor-core kernels for bf16 (AUTO, TENSOR), CUDA-core ones
+// for SIMT and fp32; FUSED keeps no checkpoints and is not offered.
+gdr_status pick_backward(const gdr_problem* p, const gdr::Dims& d, bool* tensor) {
+    switch (p->variant) {
+        case GDR_VARIANT_SIMT: *tensor = false; return GDR_OK;
+        case GDR_VARIANT_TENSOR:
+            if (!d.bf16) return GDR_ERR_UNSUPPORTED;
+            *tensor = true;
+            return GDR_OK;
+        case GDR_VARIANT_AUTO: *tensor = d.bf16 != 0; return GDR_OK;
+        default: return GDR_ERR_UNSUPPORTED;
+    }
+}
+
 }  // namespace
 
 extern "C" {
@@ -256,6 +299,115 @@ gdr_status gdr_prepare_wyp(const gdr_problem* p, const void* q, const void* k, c
     st = from_cuda(gdr::mma_prepare(d, k, v, g, beta, w, u, g_cum, (cudaStream_t)stream, device_error_word(), q, P));
     if (st == GDR_OK) t_last_variant = "tensor";
     return st;
+}
+
+gdr_status gdr_bwd_dv_local(const gdr_problem* p, const void* q, const void* k, const float* g_cum,
+                            const void* d_o, float* dv_loc, void* stream) {
+    gdr::Dims d;
+    gdr_status st = check_problem(p, &d);
+    if (st != GDR_OK) return st;
+    if ((st = check_ptrs({q, k, g_cum, d_o, dv_loc}, {})) != GDR_OK) return st;
+    st = from_cuda(gdr::simt_bwd_dv_local(d, q, k, g_cum, d_o, dv_loc, (cudaStream_t)stream));
+    if (st == GDR_OK) t_last_variant = "simt";
+    return st;
+}
+
+gdr_status gdr_bwd_scan_dh(const gdr_problem* p, const void* q, const void* k, const void* w, const float* g_cum,
+                           const void* d_o, const float* dv_loc, const float* dh_final, float* dh_ckpt,
+                           float* dv_new, float* dh0, void* stream) {
+    gdr::Dims d;
+    gdr_status st = check_problem(p, &d);
+    if (st != GDR_OK) return st;
+    if ((st = check_ptrs({q, k, w, g_cum, d_o, dv_loc, dh_ckpt, dv_new}, {dh_final, dh0})) != GDR_OK) return st;
+    st = from_cuda(gdr::simt_bwd_scan_dh(d, q, k, w, g_cum, d_o, dv_loc, dh_final, dh_ckpt, dv_new, dh0,
+                                         (cudaStream_t)stream));
+    if (st == GDR_OK) t_last_variant = "simt";
+    return st;
+}
+
+gdr_status gdr_bwd_dqkwg(const gdr_problem* p, const void* q, const void* k, const void* v_new, const float* g_cum,
+                         const void* h_ckpt, const float* dh_ckpt, const void* d_o, const float* dv_new, void* dq,
+                         float* dk_part, float* dw, float* dG_part, void* stream) {
+    gdr::Dims d;
+    gdr_status st = check_problem(p, &d);
+    if (st != GDR_OK) return st;
+    if ((st = check_ptrs({q, k, v_new, g_cum, h_ckpt, dh_ckpt, d_o, dv_new, dq, dk_part, dw, dG_part}, {})) != GDR_OK)
+        return st;
+    st = from_cuda(gdr::simt_bwd_dqkwg(d, q, k, v_new, g_cum, h_ckpt, dh_ckpt, d_o, dv_new, dq, dk_part, dw,
+                                       dG_part, (cudaStream_t)stream));
+    if (st == GDR_OK) t_last_variant = "simt";
+    return st;
+}
+
+gdr_status gdr_bwd_wy(const gdr_problem* p, const void* k, const void* v, const void* beta, const float* g_cum,
+                      const float* dw, const float* dv_new, const float* dk_part, const float* dG_part, void* dk,
+                      void* dv, void* dbeta, float* dg, void* stream) {
+    gdr::Dims d;
+    gdr_status st = check_problem(p, &d);
+    if (st != GDR_OK) return st;
+    if ((st = check_ptrs({k, v, beta, g_cum, dw, dv_new, dk_part, dG_part, dk, dv, dbeta, dg}, {})) != GDR_OK)
+        return st;
+    st = from_cuda(gdr::simt_bwd_wy(d, k, v, beta, g_cum, dw, dv_new, dk_part, dG_part, dk, dv, dbeta, dg,
+                                    (cudaStream_t)stream));
+    if (st == GDR_OK) t_last_variant = "simt";
+    return st;
+}
+
+size_t gdr_backward_workspace_bytes(const gdr_problem* p) {
+    gdr::Dims d;
+    if (check_problem(p, &d) != GDR_OK) return 0;
+    bool tensor = false;
+    if (pick_backward(p, d, &tensor) != GDR_OK) return 0;
+    return plan_backward(d).total;
+}
+
+gdr_status gdr_backward(const gdr_problem* p, const void* q, const void* k, const void* v, const float* g,
+                        const void* beta, const float* h0, const void* d_o, const float* dh_final, void* dq,
+                        void* dk, void* dv, float* dg, void* dbeta, float* dh0, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+    gdr::Dims d;
+    gdr_status st = check_problem(p, &d);
+    if (st != GDR_OK) return st;
+    if ((st = check_ptrs({q, k, v, g, beta, d_o, dq, dk, dv, dg, dbeta}, {h0, dh_final, dh0})) != GDR_OK) return st;
+    bool tensor = false;
+    if ((st = pick_backward(p, d, &tensor)) != GDR_OK) return st;
+    const BackwardWorkspace ws = plan_backward(d);
+    if (!workspace || workspace_bytes < ws.total) return GDR_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GDR_ERR_ALIGN;
+    char* base = static_cast<char*>(workspace);
+    float* g_cum = reinterpret_cast<float*>(base + ws.g_cum);
+    void* w = base + ws.w;
+    void* u = base + ws.u;
+    void* v_new = base + ws.v_new;
+    void* h_ckpt = base + ws.h_ckpt;
+    float* dv_loc = reinterpret_cast<float*>(base + ws.dv_loc);
+    float* dv_new = reinterpret_cast<float*>(base + ws.dv_new);
+    float* dh_ckpt = reinterpret_cast<float*>(base + ws.dh_ckpt);
+    float* dk_part = reinterpret_cast<float*>(base + ws.dk_part);
+    float* dw = reinterpret_cast<float*>(base + ws.dw);
+    float* dG_part = reinterpret_cast<float*>(base + ws.dG_part);
+    cudaStream_t s = (cudaStream_t)stream;
+    // forward prepare and re-scan: G, w, u, the checkpoints and v'
+    if (tensor) {
+        unsigned int* err = device_error_word();
+        if ((st = from_cuda(gdr::mma_prepare(d, k, v, g, beta, w, u, g_cum, s, err))) != GDR_OK) return st;
+        if ((st = from_cuda(gdr::mma_scan(d, k, w, u, g_cum, h0, h_ckpt, v_new, nullptr, s, err))) != GDR_OK) return st;
+    } else {
+        if ((st = from_cuda(gdr::simt_prepare(d, k, v, g, beta, w, u, g_cum, s))) != GDR_OK) return st;
+        if ((st = from_cuda(gdr::simt_scan(d, k, w, u, g_cum, h0, h_ckpt, v_new, nullptr, s))) != GDR_OK) return st;
+    }
+    if ((st = from_cuda(gdr::simt_bwd_dv_local(d, q, k, g_cum, d_o, dv_loc, s))) != GDR_OK) return st;
+    if ((st = from_cuda(gdr::simt_bwd_scan_dh(d, q, k, w, g_cum, d_o, dv_loc, dh_final, dh_ckpt, dv_new, dh0, s))) !=
+        GDR_OK)
+        return st;
+    if ((st = from_cuda(gdr::simt_bwd_dqkwg(d, q, k, v_new, g_cum, h_ckpt, dh_ckpt, d_o, dv_new, dq, dk_part, dw,
+                                            dG_part, s))) != GDR_OK)
+        return st;
+    if ((st = from_cuda(gdr::simt_bwd_wy(d, k, v, beta, g_cum, dw, dv_new, dk_part, dG_part, dk, dv, dbeta, dg, s))) !=
+        GDR_OK)
+        return st;
+    t_last_variant = tensor ? "tensor" : "simt";
+    return GDR_OK;
 }
 
 const char* gdr_status_string(gdr_status s) {

@@ -43,6 +43,20 @@ cudaError_t mma_scan_output(const Dims& d, const void* q, const void* k, const v
                             const float* g_cum, const void* P, const float* h0, void* o, float* h_final,
                             cudaStream_t s, unsigned int* err);
 
+// ---- backward stages on the CUDA cores (simt_backward.cu): every shape and io dtype;
+// intermediates fp32, see include/gdr.h for each stage's definition
+cudaError_t simt_bwd_dv_local(const Dims& d, const void* q, const void* k, const float* g_cum, const void* d_o,
+                              float* dv_loc, cudaStream_t s);
+cudaError_t simt_bwd_scan_dh(const Dims& d, const void* q, const void* k, const void* w, const float* g_cum,
+                             const void* d_o, const float* dv_loc, const float* dh_final, float* dh_ckpt,
+                             float* dv_new, float* dh0, cudaStream_t s);
+cudaError_t simt_bwd_dqkwg(const Dims& d, const void* q, const void* k, const void* v_new, const float* g_cum,
+                           const void* h_ckpt, const float* dh_ckpt, const void* d_o, const float* dv_new,
+                           void* dq, float* dk_part, float* dw, float* dG_part, cudaStream_t s);
+cudaError_t simt_bwd_wy(const Dims& d, const void* k, const void* v, const void* beta, const float* g_cum,
+                        const float* dw, const float* du, const float* dk_part, const float* dG_part, void* dk,
+                        void* dv, void* dbeta, float* dg, cudaStream_t s);
+
 // ---- device error word (device_status.cu)
 // Bounded waits in kernels write a nonzero code here instead of trapping.
 cudaError_t read_and_clear_device_error(unsigned int* code);

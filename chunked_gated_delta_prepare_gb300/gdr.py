@@ -6,10 +6,11 @@ CPU fallback: if the library is missing or cannot load, every call raises.
 
 The functions mirror the C ABI names:
     gdr_prepare_wy, gdr_prepare_wyp, gdr_scan_h, gdr_chunk_output, gdr_scan_output, gdr_forward,
-    gdr_forward_workspace_bytes, gdr_status_string, gdr_get_device_status,
+    gdr_forward_workspace_bytes, gdr_bwd_dv_local, gdr_bwd_scan_dh, gdr_bwd_dqkwg, gdr_bwd_wy,
+    gdr_backward, gdr_backward_workspace_bytes, gdr_status_string, gdr_get_device_status,
     gdr_last_variant, gdr_version
-and `forward(...)` is the convenience call that allocates outputs and the
-workspace (and, given CPU tensors, copies them to the GPU and the results back).
+and `forward(...)` / `backward(...)` are the convenience calls that allocate outputs and
+the workspace (and, given CPU tensors, copy them to the GPU and the results back).
 """
 from __future__ import annotations
 
@@ -31,6 +32,8 @@ DTYPES = {torch.float32: 0, torch.bfloat16: 1}
 VARIANTS = {"auto": 0, "simt": 1, "tensor": 2, "fused": 3}
 EXPORTS = ["gdr_prepare_wy", "gdr_scan_h", "gdr_chunk_output", "gdr_forward", "gdr_forward_workspace_bytes",
            "gdr_forward_static_scratch", "gdr_scan_output", "gdr_prepare_wyp",
+           "gdr_bwd_dv_local", "gdr_bwd_scan_dh", "gdr_bwd_dqkwg", "gdr_bwd_wy", "gdr_backward",
+           "gdr_backward_workspace_bytes",
            "gdr_status_string", "gdr_get_device_status", "gdr_last_variant", "gdr_version"]
 
 
@@ -71,6 +74,12 @@ def load(path: str | None = None):
             "gdr_scan_output": [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp],
             "gdr_prepare_wyp": [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp],
             "gdr_forward_workspace_bytes": [P],
+            "gdr_bwd_dv_local": [P, vp, vp, vp, vp, vp, vp],
+            "gdr_bwd_scan_dh": [P] + [vp] * 11,
+            "gdr_bwd_dqkwg": [P] + [vp] * 13,
+            "gdr_bwd_wy": [P] + [vp] * 13,
+            "gdr_backward": [P] + [vp] * 15 + [ctypes.c_size_t, vp],
+            "gdr_backward_workspace_bytes": [P],
             "gdr_status_string": [ctypes.c_int],
             "gdr_get_device_status": [vp],
             "gdr_last_variant": [],
@@ -81,6 +90,7 @@ def load(path: str | None = None):
             f.argtypes = args
             f.restype = ctypes.c_int
         lib.gdr_forward_workspace_bytes.restype = ctypes.c_size_t
+        lib.gdr_backward_workspace_bytes.restype = ctypes.c_size_t
         lib.gdr_status_string.restype = ctypes.c_char_p
         lib.gdr_last_variant.restype = ctypes.c_char_p
         if path is None:
@@ -224,6 +234,60 @@ def forward(q, k, v, g, beta, h0=None, *, chunk=64, scale=None, variant="auto", 
         o = o.to("cpu", non_blocking=False)
         hf = hf.to("cpu") if hf is not None else None
     return o, hf
+
+
+def gdr_bwd_dv_local(p, q, k, g_cum, d_o, dv_loc, stream=None):
+    _check(load().gdr_bwd_dv_local(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(g_cum), _ptr(d_o), _ptr(dv_loc),
+                                   _stream(stream)), "gdr_bwd_dv_local")
+
+
+def gdr_bwd_scan_dh(p, q, k, w, g_cum, d_o, dv_loc, dh_final, dh_ckpt, dv_new, dh0, stream=None):
+    _check(load().gdr_bwd_scan_dh(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(w), _ptr(g_cum), _ptr(d_o),
+                                  _ptr(dv_loc), _ptr(dh_final), _ptr(dh_ckpt), _ptr(dv_new), _ptr(dh0),
+                                  _stream(stream)), "gdr_bwd_scan_dh")
+
+
+def gdr_bwd_dqkwg(p, q, k, v_new, g_cum, h_ckpt, dh_ckpt, d_o, dv_new, dq, dk_part, dw, dG_part, stream=None):
+    _check(load().gdr_bwd_dqkwg(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v_new), _ptr(g_cum), _ptr(h_ckpt),
+                                _ptr(dh_ckpt), _ptr(d_o), _ptr(dv_new), _ptr(dq), _ptr(dk_part), _ptr(dw),
+                                _ptr(dG_part), _stream(stream)), "gdr_bwd_dqkwg")
+
+
+def gdr_bwd_wy(p, k, v, beta, g_cum, dw, dv_new, dk_part, dG_part, dk, dv, dbeta, dg, stream=None):
+    _check(load().gdr_bwd_wy(ctypes.byref(p), _ptr(k), _ptr(v), _ptr(beta), _ptr(g_cum), _ptr(dw), _ptr(dv_new),
+                             _ptr(dk_part), _ptr(dG_part), _ptr(dk), _ptr(dv), _ptr(dbeta), _ptr(dg),
+                             _stream(stream)), "gdr_bwd_wy")
+
+
+def gdr_backward_workspace_bytes(p) -> int:
+    return int(load().gdr_backward_workspace_bytes(ctypes.byref(p)))
+
+
+def gdr_backward(p, q, k, v, g, beta, h0, d_o, dh_final, dq, dk, dv, dg, dbeta, dh0, workspace, workspace_bytes,
+                 stream=None):
+    _check(load().gdr_backward(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
+                               _ptr(d_o), _ptr(dh_final), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dbeta),
+                               _ptr(dh0), _ptr(workspace), int(workspace_bytes), _stream(stream)), "gdr_backward")
+
+
+def backward(q, k, v, g, beta, h0, d_o, dh_final=None, *, chunk=64, scale=None, variant="auto", workspace=None,
+             stream=None):
+    """dq, dk, dv, dg, dbeta, dh0 = backward(q, k, v, g, beta, h0, do, dh_final): the gradient of
+    forward's (o, h_final) against do and dh_final, on device tensors."""
+    p = problem_for(q, v, g, chunk, scale, variant)
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    dq, dk = torch.empty_like(q), torch.empty_like(k)
+    dv = torch.empty_like(v)
+    dg = torch.empty_like(g)
+    dbeta = torch.empty_like(beta)
+    dh0 = torch.empty(B, H, K, V, device=q.device, dtype=torch.float32)
+    nbytes = gdr_backward_workspace_bytes(p)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 1), device=q.device, dtype=torch.uint8)
+    have = workspace.numel() * workspace.element_size()
+    gdr_backward(p, q, k, v, g, beta, h0, d_o, dh_final, dq, dk, dv, dg, dbeta, dh0, workspace, have, stream)
+    return dq, dk, dv, dg, dbeta, dh0
 
 
 def default_scale(K: int) -> float:

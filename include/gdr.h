@@ -71,7 +71,7 @@ extern "C" {
 typedef enum gdr_status {
     GDR_OK = 0,
     GDR_ERR_NULL = 1,            /* a required pointer is NULL */
-    GDR_ERR_SHAPE = 2,           /* a size is <= 0, T % chunk != 0, K/V/chunk unsupported */
+    GDR_ERR_SHAPE = 2,           /* a size is <= 0, or K/V/chunk unsupported */
     GDR_ERR_DTYPE = 3,           /* io_dtype or gate kind not known */
     GDR_ERR_ALIGN = 4,           /* a pointer is not 16-byte aligned */
     GDR_ERR_WORKSPACE = 5,       /* workspace NULL or smaller than gdr_forward_workspace_bytes */
@@ -223,6 +223,90 @@ GDR_API gdr_status gdr_forward(const gdr_problem* p, const void* q, const void* 
 GDR_API gdr_status gdr_forward_static_scratch(const gdr_problem* p, const void* q, const void* k, const void* v,
                                               const float* g, const void* beta, const float* h0, void* o,
                                               float* h_final, void* stream);
+
+/*
+ * ---------------------------------------------------------------- backward
+ * The gradient of the forward above.  Given do = dL/do [B,T,H,V] (io dtype)
+ * and dh_final = dL/dh_final [B,H,K,V] (fp32, or NULL for zero), it returns
+ * dq, dk [B,T,H,K], dv [B,T,H,V] and dbeta [B,T,H] in the io dtype,
+ * dg (the shape of g) and dh0 [B,H,K,V] in fp32.
+ *
+ * Steps:
+ * - The forward prepare (gdr_prepare_wy) and the forward re-scan (gdr_scan_h)
+ *   run again. They rebuild G, w, the checkpoints h_c and v', as the backward
+ *   page's first stage does ("kernel_fun/kda/_kernels/bwd_scan.py", module
+ *   docstring: the forward re-scan that feeds the gradient stages).
+ * - Then come the four stages below, each the derivative of one line of the
+ *   chunked forward. Rows i, j are tokens of one chunk; G_L is the chunk's
+ *   last row; dh_next = dL/d(state after the chunk).
+ *   L(X, Y)_i = sum_j X_ij Y_j e^(G_i - G_j) and
+ *   R(X, Y)_j = sum_i X_ij Y_i e^(G_i - G_j), elementwise over the key dim.
+ *
+ * A partial last chunk is read as in the forward. The gate gradient of its
+ * padding goes to token T - 1, whose G the padding repeats.
+ * The four stages run on the CUDA cores in fp32 for every variant.  The
+ * re-scan runs the tensor-core kernels for bf16 io (variants AUTO and
+ * TENSOR), or the CUDA-core ones (variant SIMT, and fp32 io).  The variant
+ * FUSED is not offered here (GDR_ERR_UNSUPPORTED).
+ */
+
+/* dv_loc = scale tril_0(Q~)^T do per chunk.  Inputs q, k, do io; g_cum fp32.
+ * Output dv_loc [B,T,H,V] fp32. */
+GDR_API gdr_status gdr_bwd_dv_local(const gdr_problem* p, const void* q, const void* k, const float* g_cum,
+                                    const void* d_o, float* dv_loc, void* stream);
+
+/* The reverse state scan.  dh = dh_final (zero if NULL), then for c = NT-1 .. 0:
+ *     dh_ckpt[c] = dh                               (gradient of the state after chunk c)
+ *     dv'_c      = dv_loc_c + (k exp(G_L - G)) dh   -> dv_new
+ *     dh         = exp(G_L) dh + scale (q exp(G))^T do_c - w_c^T dv'_c
+ * and dh0 = dh.  Inputs q, k, w, do io; g_cum, dv_loc, dh_final fp32.
+ * Outputs dh_ckpt [B,NT,H,K,V], dv_new [B,T,H,V], dh0 [B,H,K,V], all fp32;
+ * dh0 may be NULL (not written). */
+GDR_API gdr_status gdr_bwd_scan_dh(const gdr_problem* p, const void* q, const void* k, const void* w,
+                                   const float* g_cum, const void* d_o, const float* dv_loc,
+                                   const float* dh_final, float* dh_ckpt, float* dv_new, float* dh0, void* stream);
+
+/* Per chunk, with h = h_ckpt[c], dhn = dh_ckpt[c], dqg = scale do h^T,
+ * dQ~ = scale tril_0(do v'^T), dkg = v' dhn^T, kg = k exp(G_L - G):
+ *     dq      = dqg exp(G) + L(dQ~, k)                                 (io; final)
+ *     dk_part = R(dQ~, q) + dkg exp(G_L - G)                           fp32
+ *     dw      = -dv' h^T                                               fp32
+ *     dG_part = dqg q exp(G) + q L(dQ~, k) - k R(dQ~, q) - dkg kg      fp32, the shape of g
+ *               (+ sum_i dkg_i kg_i + exp(G_L) sum_v h dhn on the chunk's last token;
+ *                a scalar gate sums over the key dim)
+ * Inputs q, k, v_new, h_ckpt, do io; g_cum, dh_ckpt, dv_new fp32. */
+GDR_API gdr_status gdr_bwd_dqkwg(const gdr_problem* p, const void* q, const void* k, const void* v_new,
+                                 const float* g_cum, const void* h_ckpt, const float* dh_ckpt, const void* d_o,
+                                 const float* dv_new, void* dq, float* dk_part, float* dw, float* dG_part,
+                                 void* stream);
+
+/* The WY backward, with (I + A)^{-1} rebuilt from k, beta, g_cum and du = dv_new:
+ *     dkb = Tinv^T dw, dvb = Tinv^T du, dA = strict_lower(-Tinv^T (dw kb^T + du vb^T) Tinv^T),
+ *     Y = beta_i dA_ij, M = A with beta = 1
+ *     dk    = dk_part + beta exp(G) dkb + L(Y, k) + R(Y, k)             (io)
+ *     dv    = beta dvb                                                  (io)
+ *     dbeta = sum_d dkb k exp(G) + sum_v dvb v + sum_j dA_ij M_ij      (io)
+ *     dg    = reverse cumsum over each chunk of dG_part + dkb kb + k L(Y, k) - k R(Y, k)   (fp32)
+ * Inputs k, v, beta io; g_cum, dw, dv_new, dk_part, dG_part fp32. */
+GDR_API gdr_status gdr_bwd_wy(const gdr_problem* p, const void* k, const void* v, const void* beta,
+                              const float* g_cum, const float* dw, const float* dv_new, const float* dk_part,
+                              const float* dG_part, void* dk, void* dv, void* dbeta, float* dg, void* stream);
+
+/* Bytes of device workspace gdr_backward needs (0 for a problem it would reject). */
+GDR_API size_t gdr_backward_workspace_bytes(const gdr_problem* p);
+
+/*
+ * The whole backward: every stage above in order.
+ * Inputs:  q, k, v, g, beta, h0 as gdr_forward took them; do [B,T,H,V] io;
+ *          dh_final [B,H,K,V] fp32 or NULL (zero).
+ * Outputs: dq, dk [B,T,H,K] io; dv [B,T,H,V] io; dg (shape of g) fp32;
+ *          dbeta [B,T,H] io; dh0 [B,H,K,V] fp32 or NULL (not written).
+ * workspace: at least gdr_backward_workspace_bytes(p) bytes, 256-byte aligned.
+ */
+GDR_API gdr_status gdr_backward(const gdr_problem* p, const void* q, const void* k, const void* v, const float* g,
+                                const void* beta, const float* h0, const void* d_o, const float* dh_final,
+                                void* dq, void* dk, void* dv, float* dg, void* dbeta, float* dh0,
+                                void* workspace, size_t workspace_bytes, void* stream);
 
 /* Static, human-readable text for a status code. */
 GDR_API const char* gdr_status_string(gdr_status s);

@@ -40,6 +40,24 @@ def test_library_exports_every_declared_symbol(lib):
     assert set(gdr.EXPORTS) <= set(declared_functions())
 
 
+def declared_arity():
+    """name -> number of parameters, from the prototypes in include/gdr.h."""
+    with open(HEADER) as f:
+        src = f.read()
+    out = {}
+    for m in re.finditer(r"^GDR_API\s+[\w\s\*]+?\b(gdr_\w+)\s*\(([^)]*)\)", src, flags=re.M):
+        params = m.group(2).strip()
+        out[m.group(1)] = 0 if params in ("", "void") else len(params.split(","))
+    return out
+
+
+def test_binding_arity_matches_the_header(lib):
+    arity = declared_arity()
+    assert len(arity) == len(declared_functions())
+    for name, n in arity.items():
+        assert len(getattr(lib, name).argtypes) == n, name
+
+
 def test_status_strings(lib):
     for code in range(10):
         s = gdr.gdr_status_string(code)

@@ -237,6 +237,83 @@ def run_reference(args, wl):
 
 # ------------------------------------------------------------------ GPU leg
 
+def time_backward(args, wl, x, dev, flush, stream, world):
+    """gdr_backward's six launches on the same workload, called one by one through their
+    C-ABI entry points (as gdr_backward calls them) so each can be timed; the upstream
+    gradients do and dh_final are seeded normals."""
+    B, T, H, K, V, C = wl.B, wl.T, wl.H, wl.K, wl.V, wl.chunk
+    q, k, v, g, beta = (t.to(dev) for t in (x.q, x.k, x.v, x.g, x.beta))
+    h0 = x.h0.to(dev) if x.h0 is not None else None
+    gen = torch.Generator().manual_seed(7)
+    d_o = torch.randn(B, T, H, V, generator=gen).to(q.dtype).to(dev)
+    dhf = torch.randn(B, H, K, V, generator=gen).to(dev)
+    p = gdr.problem_for(q, v, g, C, None, args.variant)
+    if gdr.gdr_backward_workspace_bytes(p) == 0:
+        return None
+    NT = -(-T // C)
+    f32 = dict(device=dev, dtype=torch.float32)
+    g_cum, w, u, v_new = torch.empty_like(g), torch.empty_like(k), torch.empty_like(v), torch.empty_like(v)
+    h_ckpt = torch.empty(B, NT, H, K, V, device=dev, dtype=q.dtype)
+    dv_loc, dv_new = torch.empty(B, T, H, V, **f32), torch.empty(B, T, H, V, **f32)
+    dh_ckpt = torch.empty(B, NT, H, K, V, **f32)
+    dk_part, dw = torch.empty(B, T, H, K, **f32), torch.empty(B, T, H, K, **f32)
+    dG_part = torch.empty(g.shape, **f32)
+    dq, dk, dv, dbeta = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(beta)
+    dg, dh0 = torch.empty(g.shape, **f32), torch.empty(B, H, K, V, **f32)
+    fast = q.dtype == torch.bfloat16 and g.dim() == 3 and C == 64 and args.variant in ("auto", "tensor")
+    if fast:
+        # the tensor-core path gdr_backward takes here: four launches, bf16 intermediates
+        P = torch.empty(B, NT, H, C, C, device=dev, dtype=q.dtype)
+        tinv = torch.empty(B, NT, H, C, C, device=dev, dtype=q.dtype)
+        dh_ckpt16 = torch.empty(B, NT, H, K, V, device=dev, dtype=q.dtype)
+        dv_new16 = torch.empty(B, T, H, V, device=dev, dtype=q.dtype)
+        names = ["prepare", "rescan", "scan_dh", "wy_dqkg"]
+        calls = [lambda: gdr.gdr_bwd_prepare(p, q, k, v, g, beta, w, u, g_cum, P, tinv),
+                 lambda: gdr.gdr_scan_h(p, k, w, u, g_cum, h0, h_ckpt, v_new, None),
+                 lambda: gdr.gdr_bwd_scan_dh_p(p, q, k, w, g_cum, P, d_o, dhf, dh_ckpt16, dv_new16, dh0),
+                 lambda: gdr.gdr_bwd_wy_dqkg(p, q, k, v, beta, g_cum, w, u, tinv, v_new, h_ckpt, d_o, dv_new16,
+                                             dh_ckpt16, dq, dk, dv, dbeta, dg)]
+    else:
+        names = ["prepare", "rescan", "dv_local", "scan_dh", "dqkwg", "wy"]
+        calls = [lambda: gdr.gdr_prepare_wy(p, k, v, g, beta, w, u, g_cum),
+                 lambda: gdr.gdr_scan_h(p, k, w, u, g_cum, h0, h_ckpt, v_new, None),
+                 lambda: gdr.gdr_bwd_dv_local(p, q, k, g_cum, d_o, dv_loc),
+                 lambda: gdr.gdr_bwd_scan_dh(p, q, k, w, g_cum, d_o, dv_loc, dhf, dh_ckpt, dv_new, dh0),
+                 lambda: gdr.gdr_bwd_dqkwg(p, q, k, v_new, g_cum, h_ckpt, dh_ckpt, d_o, dv_new, dq, dk_part, dw,
+                                           dG_part),
+                 lambda: gdr.gdr_bwd_wy(p, k, v, beta, g_cum, dw, dv_new, dk_part, dG_part, dk, dv, dbeta, dg)]
+    ran = []
+    for f in calls:
+        f()
+        ran.append(gdr.gdr_last_variant())
+    steps = max(3, min(args.steps, 10))
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        for f in calls:
+            f()
+    torch.cuda.synchronize()
+    n = len(calls)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)] for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for s in range(steps):
+        flush.fill_(s & 0xFF)
+        evs[s][0].record(stream)
+        for i, f in enumerate(calls):
+            f()
+            evs[s][i + 1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    if gdr.gdr_get_device_status() != 0:
+        raise RuntimeError("device status set after the backward's timed region")
+    per = [sum(evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(steps)) / steps for i in range(n)]
+    total_s = max_over_ranks(sum(evs[s][0].elapsed_time(evs[s][n]) for s in range(steps)) / 1e3, world)
+    return {"ms_per_step": 1e3 * total_s / steps, "steps": steps,
+            "value": weak_scaling_throughput(world, B * T, steps, total_s), "unit": "tokens/s",
+            "kernel_ms": {f"{names[i]}[{ran[i]}]": per[i] for i in range(n)}, "gpu_launches": n * steps,
+            "upstream": "do ~ N(0,1) in the io dtype, dh_final ~ N(0,1) fp32, seed 7"}
+
+
 def run_ours(args, wl):
     world, rank, local = dist_setup()
     dev = torch.device("cuda", local)
@@ -359,6 +436,8 @@ def run_ours(args, wl):
     e2e_s = max_over_ranks(time.perf_counter() - t0, world)
     e2e_value = weak_scaling_throughput(world, B * T, e2e_steps, e2e_s)
 
+    bwd = None if args.no_backward else time_backward(args, wl, x, dev, flush, stream, world)
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = oracle_sample(wl, x, max(1, min(wl.B * wl.H, args.cpu_heads)))
@@ -381,6 +460,8 @@ def run_ours(args, wl):
             "gpu_launches": n * args.steps,
             "clocks": clk.summary(),
         }
+        if bwd is not None:
+            line["backward"] = bwd
         if cpu is not None:
             line["cpu_baseline"] = {"value": cpu["tokens_per_s"], "unit": "tokens/s", "cores": cpu["cores"],
                                     "kind": "oracle", "sample": cpu["sample"]}
@@ -401,6 +482,7 @@ def main():
     ap.add_argument("--cpu-heads", type=int, default=32, help="heads in the CPU-oracle baseline sample")
     ap.add_argument("--ref-heads", type=int, default=4, help="heads per step of --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-backward", action="store_true", help="skip timing the backward pass")
     ap.add_argument("--p-from", choices=["prepare", "scan"], default="prepare",
                     help="fused path: gated scores P written by the prepare, or formed inside the scan kernel")
     ap.add_argument("--seq-len", type=int, default=None,

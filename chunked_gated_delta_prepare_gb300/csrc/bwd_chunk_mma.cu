@@ -1,0 +1,475 @@
+// The backward's per-chunk stage for bf16 io, a scalar gate and 64-token
+// chunks: every gradient that needs only the chunk's own tiles, in one kernel
+// (the pages' backward names this stage wy_dqkg: the WY backward fused with dq,
+// dk and the gate gradient; "kernel_fun/kda/_kernels/bwd_scan.py", host wrapper).
+//
+// Per chunk (rows i, j; G the chunk-local cumsum of g, G_L its last row,
+// Gam_ij = exp(G_i - G_j); h = h_ckpt[c], dhn = dh_ckpt[c]; T = (I + A)^{-1}):
+//
+//   dqg = scale do h^T,  dkg = v' dhn^T,  dw = -dv' h^T
+//   Xq  = scale (do v'^T) * Gam, strictly lower;  its diagonal d_i = scale do_i . v'_i
+//   dq  = dqg e^G + Xq k + d_i k_i
+//   dk  = dkg e^(G_L - G) + Xq^T q + d_i q_i + beta e^G dkb + Y k + Y^T k
+//   dkb = T^T dw,  dvb = T^T dv',  dv = beta dvb
+//   dA  = strict_lower(-(dkb w^T + dvb u^T))      (w = T kb, u = T vb make T^T dT T^T collapse to this)
+//   Y   = beta_i dA_ij Gam_ij
+//   dbeta_i = sum_d dkb k e^G + sum_v dvb v + sum_j dA_ij M_ij,  M = Gam * (k k^T)
+//   dG_i = sum_d [dqg q e^G + q (Xq k) - k (Xq^T q) - dkg k e^(G_L - G) + dkb kb + k (Y k) - k (Y^T k)]
+//          (+ on the chunk's last token: sum of the dkg kg terms of the other rows + e^(G_L) sum h dhn)
+//   dg  = reverse cumsum of dG over the chunk
+//
+// The diagonal of the output scores and the last token's own dkg kg term cancel
+// exactly in dG and are left out of it (fp32 rounding of those O(1) pairs would
+// otherwise swamp a small dG).  One CTA of eight warps per (chunk, head,
+// batch); the tiles sit in shared memory as padded bf16 rows (a row stride of
+// D + 8 elements keeps every ldmatrix free of bank conflicts) and every product
+// is a warp-level mma.sync m16n8k16 with fp32 accumulation.  Warp w owns the
+// 16-row block w % 4 and half (w / 4) of the columns of every [C x D] result,
+// so dq and dk accumulate in registers across all their terms.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "gdr_internal.h"
+#include "warp_mma.cuh"
+
+namespace gdr {
+namespace {
+
+using bf16 = __nv_bfloat16;
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// acc[j] += opA(rows 16 rb .. +15, all kd) opB(all kd, cols 16 (cb0 + j) .. +15) for j < NCW.
+// A row-major [M][lda] (AT: stored as [K][lda], i.e. A^T row-major); B stored [K][ldb] (BT: [N][ldb]).
+template <int NCW, int KD, bool AT, bool BT>
+__device__ __forceinline__ void wgemm(float (&acc)[NCW][2][4], uint32_t A, int lda, uint32_t B, int ldb, int rb,
+                                      int cb0, int mi, int mr) {
+#pragma unroll
+    for (int k0 = 0; k0 < KD; k0 += 16) {
+        uint32_t a[4];
+        if constexpr (AT) wm::ldsm_x4_t(A + 2u * ((k0 + 8 * (mi >> 1) + mr) * lda + 16 * rb + 8 * (mi & 1)), a);
+        else wm::ldsm_x4(A + 2u * ((16 * rb + 8 * (mi & 1) + mr) * lda + k0 + 8 * (mi >> 1)), a);
+#pragma unroll
+        for (int j = 0; j < NCW; ++j) {
+            const int n0 = 16 * (cb0 + j);
+            uint32_t bb[4];
+            if constexpr (BT) wm::ldsm_x4(B + 2u * ((n0 + 8 * (mi >> 1) + mr) * ldb + k0 + 8 * (mi & 1)), bb);
+            else wm::ldsm_x4_t(B + 2u * ((k0 + 8 * (mi & 1) + mr) * ldb + n0 + 8 * (mi >> 1)), bb);
+            wm::mma16816(acc[j][0], a, bb[0], bb[1]);
+            wm::mma16816(acc[j][1], a, bb[2], bb[3]);
+        }
+    }
+}
+
+template <int NCW>
+__device__ __forceinline__ void zero(float (&acc)[NCW][2][4]) {
+#pragma unroll
+    for (int j = 0; j < NCW; ++j)
+#pragma unroll
+        for (int n = 0; n < 2; ++n) acc[j][n][0] = acc[j][n][1] = acc[j][n][2] = acc[j][n][3] = 0.f;
+}
+
+// Calls f(row, col, value&) for every element of a warp's tiles (rows 16 rb + ..., cols 16 (cb0 + j) + ...).
+template <int NCW, typename F>
+__device__ __forceinline__ void each(float (&acc)[NCW][2][4], int rb, int cb0, int g4, int q4, F&& f) {
+#pragma unroll
+    for (int j = 0; j < NCW; ++j)
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) f(16 * rb + g4 + 8 * (e >> 1), 16 * (cb0 + j) + 8 * n + 2 * q4 + (e & 1), acc[j][n][e]);
+}
+
+// rows x D bf16 from global rows of stride gs elements into shared [rows][D + 8]; rows >= nrows read as
+// zero.  Asynchronous 16-byte copies (cp.async), so every copy of a phase is in flight at once; the
+// caller waits with cp_async_wait_all() and a barrier.
+template <int D>
+__device__ __forceinline__ void load_tile(bf16* dst, const bf16* src, int64_t gs, int rows, int nrows, int tid) {
+    constexpr int per = D / 8;
+    for (int idx = tid; idx < rows * per; idx += kThreads) {
+        const int r = idx / per, c8 = idx % per;
+        bf16* d = dst + r * (D + 8) + 8 * c8;
+        if (r < nrows)
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(d)), "l"(src + r * gs + 8 * c8)
+                         : "memory");
+        else
+            *reinterpret_cast<uint4*>(d) = make_uint4(0, 0, 0, 0);
+    }
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+__device__ __forceinline__ float bf(const bf16* p) { return __bfloat162float(*p); }
+
+// sum over the four lanes of a quad (the lanes holding one row's columns), then into the row's shared slot
+__device__ __forceinline__ void row_add(float* slot, float v, int q4) {
+    v += __shfl_xor_sync(0xffffffffu, v, 1);
+    v += __shfl_xor_sync(0xffffffffu, v, 2);
+    if (q4 == 0) atomicAdd(slot, v);
+}
+
+template <int K, int V>
+struct ChunkLayout {
+    static constexpr int C = 64;
+    static constexpr int LK = K + 8, LV = V + 8, LC = C + 8;
+    static constexpr uint32_t rq = 0;                              // q; later w
+    static constexpr uint32_t rk = rq + C * LK * 2;                // k
+    static constexpr uint32_t rdo = rk + C * LK * 2;               // do; later v
+    static constexpr uint32_t rvp = rdo + C * LV * 2;              // v'; later u
+    static constexpr uint32_t rdv = rvp + C * LV * 2;              // dv'
+    static constexpr uint32_t rh = rdv + C * LV * 2;               // h [K][V]; later dkb [C][K]
+    static constexpr uint32_t rdh = rh + K * LV * 2;               // dhn [K][V]; later dvb [C][V]
+    static constexpr uint32_t rw = rdh + K * LV * 2;               // dw [C][K]
+    static constexpr uint32_t rx = rw + C * LK * 2;                // Xq; later T
+    static constexpr uint32_t ry = rx + C * LC * 2;                // Y
+    static constexpr uint32_t rf = ry + C * LC * 2;                // fp32 rows
+    static constexpr uint32_t bytes = rf + 8 * C * 4;
+    static_assert(C * LK <= K * LV, "dkb fits over h");
+};
+
+template <int K, int V>
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_chunk_mma_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* __restrict__ v,
+                     const bf16* __restrict__ beta, const float* __restrict__ g_cum, const bf16* __restrict__ w,
+                     const bf16* __restrict__ u, const bf16* __restrict__ tinv, const bf16* __restrict__ v_new,
+                     const bf16* __restrict__ h_ckpt, const bf16* __restrict__ d_o, const bf16* __restrict__ dv_new,
+                     const bf16* __restrict__ dh_ckpt, bf16* __restrict__ dq, bf16* __restrict__ dk,
+                     bf16* __restrict__ dv, bf16* __restrict__ dbeta, float* __restrict__ dg, int T, int H,
+                     float scale) {
+    using L = ChunkLayout<K, V>;
+    constexpr int C = L::C, LK = L::LK, LV = L::LV, LC = L::LC;
+    constexpr int NK = K / 32, NV = V / 32, NC = C / 32;   // 16-column blocks per warp
+    extern __shared__ __align__(128) unsigned char sm[];
+    bf16* Qs = reinterpret_cast<bf16*>(sm + L::rq);
+    bf16* Ks = reinterpret_cast<bf16*>(sm + L::rk);
+    bf16* DOs = reinterpret_cast<bf16*>(sm + L::rdo);
+    bf16* VPs = reinterpret_cast<bf16*>(sm + L::rvp);
+    bf16* DVs = reinterpret_cast<bf16*>(sm + L::rdv);
+    bf16* Hs = reinterpret_cast<bf16*>(sm + L::rh);
+    bf16* DHs = reinterpret_cast<bf16*>(sm + L::rdh);
+    bf16* DWs = reinterpret_cast<bf16*>(sm + L::rw);
+    bf16* Xs = reinterpret_cast<bf16*>(sm + L::rx);
+    bf16* Ys = reinterpret_cast<bf16*>(sm + L::ry);
+    float* sG = reinterpret_cast<float*>(sm + L::rf);
+    float* sEG = sG + C;      // e^G
+    float* sGam = sEG + C;    // e^(G_L - G)
+    float* sB = sGam + C;     // beta
+    float* sdG = sB + C;      // gate gradient per row
+    float* sdB = sdG + C;     // dbeta per row
+    float* sDiag = sdB + C;   // scale do_i . v'_i
+    float* sS = sDiag + C;    // [0]: sum of dkg kg over the other rows, [1]: sum h dhn
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g4 = lane >> 2, q4 = lane & 3, mi = lane >> 3, mr = lane & 7;
+    const int rb = warp & 3, half = warp >> 2;
+    const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int NT = (T + C - 1) / C;
+    const int t0 = c * C, nv = min(C, T - t0);
+    const int64_t tok0 = ((int64_t)b * T + t0) * H + h;      // row of token t0, head h
+    const int64_t st_off = (((int64_t)b * NT + c) * H + h);  // this chunk's [K][V] / [C][C] block index
+
+    // ---- gate rows and beta
+    if (tid < C) {
+        const int i = tid;
+        const float G = g_cum[((int64_t)b * T + t0 + min(i, nv - 1)) * H + h];
+        const float GL = g_cum[((int64_t)b * T + t0 + nv - 1) * H + h];
+        sG[i] = G;
+        sEG[i] = __expf(G);
+        sGam[i] = __expf(GL - G);
+        sB[i] = i < nv ? __bfloat162float(beta[tok0 + (int64_t)i * H]) : 0.f;
+        sdG[i] = 0.f;
+        sdB[i] = 0.f;
+        if (i < 2) sS[i] = 0.f;
+    }
+    // ---- phase 1 tiles
+    load_tile<V>(Hs, h_ckpt + st_off * K * V, V, K, K, tid);
+    load_tile<V>(DOs, d_o + tok0 * V, (int64_t)H * V, C, nv, tid);
+    load_tile<V>(DHs, dh_ckpt + st_off * K * V, V, K, K, tid);
+    load_tile<V>(VPs, v_new + tok0 * V, (int64_t)H * V, C, nv, tid);
+    load_tile<V>(DVs, dv_new + tok0 * V, (int64_t)H * V, C, nv, tid);
+    load_tile<K>(Qs, q + tok0 * K, (int64_t)H * K, C, nv, tid);
+    load_tile<K>(Ks, k + tok0 * K, (int64_t)H * K, C, nv, tid);
+    cp_async_wait_all();
+    __syncthreads();
+
+    const uint32_t aQ = smem_addr(Qs), aK = smem_addr(Ks), aDO = smem_addr(DOs), aVP = smem_addr(VPs);
+    const uint32_t aDV = smem_addr(DVs), aH = smem_addr(Hs), aDH = smem_addr(DHs), aDW = smem_addr(DWs);
+    const uint32_t aX = smem_addr(Xs), aY = smem_addr(Ys);
+    const int ck = half * NK, cv = half * NV, cc = half * NC;   // this warp's first column block
+
+    float accQ[NK][2][4], accK[NK][2][4], tmp[NK][2][4];
+    // dqg = do h^T: the e^G-scaled part of dq, and its gate term
+    zero(accQ);
+    wgemm<NK, V, false, true>(accQ, aDO, LV, aH, LV, rb, ck, mi, mr);
+    {
+        float rs0 = 0.f, rs1 = 0.f;
+        each(accQ, rb, ck, g4, q4, [&](int r, int col, float& x) {
+            const float y = scale * x * sEG[r];
+            const float t = y * bf(Qs + r * LK + col);
+            if (r & 8) rs1 += t; else rs0 += t;
+            x = y;
+        });
+        row_add(sdG + 16 * rb + g4, rs0, q4);
+        row_add(sdG + 16 * rb + g4 + 8, rs1, q4);
+    }
+    // dkg = v' dhn^T: dk's e^(G_L - G) part; the gate terms go to the rows, the last row takes their sum
+    zero(accK);
+    wgemm<NK, V, false, true>(accK, aVP, LV, aDH, LV, rb, ck, mi, mr);
+    {
+        float rs0 = 0.f, rs1 = 0.f, tot = 0.f;
+        each(accK, rb, ck, g4, q4, [&](int r, int col, float& x) {
+            const float kg = bf(Ks + r * LK + col) * sGam[r];
+            const float t = r == nv - 1 ? 0.f : x * kg;
+            if (r & 8) rs1 -= t; else rs0 -= t;
+            tot += t;
+            x *= sGam[r];
+        });
+        row_add(sdG + 16 * rb + g4, rs0, q4);
+        row_add(sdG + 16 * rb + g4 + 8, rs1, q4);
+        for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+        if (lane == 0) atomicAdd(sS, tot);
+    }
+    // dw = -dv' h^T -> bf16 tile
+    zero(tmp);
+    wgemm<NK, V, false, true>(tmp, aDV, LV, aH, LV, rb, ck, mi, mr);
+    each(tmp, rb, ck, g4, q4, [&](int r, int col, float& x) { DWs[r * LK + col] = __float2bfloat16_rn(-x); });
+    // Xq = scale (do v'^T) Gam, strictly lower, with its diagonal apart
+    {
+        float xq[NC][2][4];
+        zero(xq);
+        wgemm<NC, V, false, true>(xq, aDO, LV, aVP, LV, rb, cc, mi, mr);
+        each(xq, rb, cc, g4, q4, [&](int r, int col, float& x) {
+            const float y = scale * x;
+            if (col == r) sDiag[r] = y;
+            Xs[r * LC + col] = __float2bfloat16_rn(col < r ? y * __expf(sG[r] - sG[col]) : 0.f);
+        });
+    }
+    // sum h dhn, eight elements per step
+    {
+        float s = 0.f;
+        for (int idx = tid; idx < K * V / 8; idx += kThreads) {
+            const int d = idx / (V / 8), x = 8 * (idx % (V / 8));
+            const uint4 a = *reinterpret_cast<const uint4*>(Hs + d * LV + x);
+            const uint4 e = *reinterpret_cast<const uint4*>(DHs + d * LV + x);
+            const uint32_t av[4] = {a.x, a.y, a.z, a.w}, ev[4] = {e.x, e.y, e.z, e.w};
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+                s += __uint_as_float(av[m] << 16) * __uint_as_float(ev[m] << 16) +
+                     __uint_as_float(av[m] & 0xffff0000u) * __uint_as_float(ev[m] & 0xffff0000u);
+        }
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (lane == 0) atomicAdd(sS + 1, s);
+    }
+    __syncthreads();
+
+    // ---- phase 2: the output scores' other factors
+    zero(tmp);
+    wgemm<NK, C, false, false>(tmp, aX, LC, aK, LK, rb, ck, mi, mr);      // Xq k
+    {
+        float rs0 = 0.f, rs1 = 0.f;
+        each(tmp, rb, ck, g4, q4, [&](int r, int col, float& x) {
+            const float t = bf(Qs + r * LK + col) * x;
+            if (r & 8) rs1 += t; else rs0 += t;
+        });
+        row_add(sdG + 16 * rb + g4, rs0, q4);
+        row_add(sdG + 16 * rb + g4 + 8, rs1, q4);
+    }
+#pragma unroll
+    for (int j = 0; j < NK; ++j)
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) accQ[j][n][e] += tmp[j][n][e];
+    // dq done: + d_i k_i, stored
+    each(accQ, rb, ck, g4, q4, [&](int r, int col, float& x) {
+        x += sDiag[r] * bf(Ks + r * LK + col);
+        if (r < nv) dq[(tok0 + (int64_t)r * H) * K + col] = __float2bfloat16_rn(x);
+    });
+    zero(tmp);
+    wgemm<NK, C, true, false>(tmp, aX, LC, aQ, LK, rb, ck, mi, mr);       // Xq^T q
+    {
+        float rs0 = 0.f, rs1 = 0.f;
+        each(tmp, rb, ck, g4, q4, [&](int r, int col, float& x) {
+            const float t = bf(Ks + r * LK + col) * x;
+            if (r & 8) rs1 -= t; else rs0 -= t;
+        });
+        row_add(sdG + 16 * rb + g4, rs0, q4);
+        row_add(sdG + 16 * rb + g4 + 8, rs1, q4);
+    }
+    each(tmp, rb, ck, g4, q4, [&](int r, int col, float& x) { x += sDiag[r] * bf(Qs + r * LK + col); });
+#pragma unroll
+    for (int j = 0; j < NK; ++j)
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) accK[j][n][e] += tmp[j][n][e];
+    __syncthreads();
+
+    // ---- phase 3: the WY backward
+    bf16* Ws = Qs;
+    bf16* Vs = DOs;
+    bf16* Us = VPs;
+    bf16* Ts = Xs;
+    bf16* DKBs = Hs;
+    bf16* DVBs = DHs;
+    load_tile<C>(Ts, tinv + st_off * C * C, C, C, C, tid);
+    load_tile<K>(Ws, w + tok0 * K, (int64_t)H * K, C, nv, tid);
+    load_tile<V>(Vs, v + tok0 * V, (int64_t)H * V, C, nv, tid);
+    load_tile<V>(Us, u + tok0 * V, (int64_t)H * V, C, nv, tid);
+    cp_async_wait_all();
+    __syncthreads();
+    const uint32_t aT = smem_addr(Ts), aW = smem_addr(Ws), aU = smem_addr(Us);
+    // dkb = T^T dw
+    zero(tmp);
+    wgemm<NK, C, true, false>(tmp, aT, LC, aDW, LK, rb, ck, mi, mr);
+    {
+        float rb0 = 0.f, rb1 = 0.f, rg0 = 0.f, rg1 = 0.f;
+        each(tmp, rb, ck, g4, q4, [&](int r, int col, float& x) {
+            const float ke = bf(Ks + r * LK + col) * sEG[r];
+            const float db = x * ke, dgv = x * sB[r] * ke;
+            if (r & 8) { rb1 += db; rg1 += dgv; } else { rb0 += db; rg0 += dgv; }
+            DKBs[r * LK + col] = __float2bfloat16_rn(x);
+            x *= sB[r] * sEG[r];
+        });
+        row_add(sdB + 16 * rb + g4, rb0, q4);
+        row_add(sdB + 16 * rb + g4 + 8, rb1, q4);
+        row_add(sdG + 16 * rb + g4, rg0, q4);
+        row_add(sdG + 16 * rb + g4 + 8, rg1, q4);
+    }
+#pragma unroll
+    for (int j = 0; j < NK; ++j)
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) accK[j][n][e] += tmp[j][n][e];
+    // dvb = T^T dv': dv = beta dvb
+    {
+        float tv[NV][2][4];
+        zero(tv);
+        wgemm<NV, C, true, false>(tv, aT, LC, aDV, LV, rb, cv, mi, mr);
+        float r0 = 0.f, r1 = 0.f;
+        each(tv, rb, cv, g4, q4, [&](int r, int col, float& x) {
+            const float t = x * bf(Vs + r * LV + col);
+            if (r & 8) r1 += t; else r0 += t;
+            DVBs[r * LV + col] = __float2bfloat16_rn(x);
+            if (r < nv) dv[(tok0 + (int64_t)r * H) * V + col] = __float2bfloat16_rn(sB[r] * x);
+        });
+        row_add(sdB + 16 * rb + g4, r0, q4);
+        row_add(sdB + 16 * rb + g4 + 8, r1, q4);
+    }
+    __syncthreads();
+    // dA = strict_lower(-(dkb w^T + dvb u^T)); dbeta's A term against M = Gam (k k^T); Y = beta dA Gam
+    {
+        float da[NC][2][4], m[NC][2][4];
+        zero(da);
+        zero(m);
+        wgemm<NC, K, false, true>(da, smem_addr(DKBs), LK, aW, LK, rb, cc, mi, mr);
+        wgemm<NC, V, false, true>(da, smem_addr(DVBs), LV, aU, LV, rb, cc, mi, mr);
+        wgemm<NC, K, false, true>(m, aK, LK, aK, LK, rb, cc, mi, mr);
+        float r0 = 0.f, r1 = 0.f;
+#pragma unroll
+        for (int j = 0; j < NC; ++j)
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int r = 16 * rb + g4 + 8 * (e >> 1), col = 16 * (cc + j) + 8 * n + 2 * q4 + (e & 1);
+                    const float gam = col < r ? __expf(sG[r] - sG[col]) : 0.f;
+                    const float a = -da[j][n][e];
+                    const float t = a * m[j][n][e] * gam;
+                    if (r & 8) r1 += t; else r0 += t;
+                    Ys[r * LC + col] = __float2bfloat16_rn(sB[r] * a * gam);
+                }
+        row_add(sdB + 16 * rb + g4, r0, q4);
+        row_add(sdB + 16 * rb + g4 + 8, r1, q4);
+    }
+    __syncthreads();
+    // dk += Y k + Y^T k; their gate terms
+    zero(tmp);
+    wgemm<NK, C, false, false>(tmp, aY, LC, aK, LK, rb, ck, mi, mr);
+    {
+        float rs0 = 0.f, rs1 = 0.f;
+        each(tmp, rb, ck, g4, q4, [&](int r, int col, float& x) {
+            const float t = bf(Ks + r * LK + col) * x;
+            if (r & 8) rs1 += t; else rs0 += t;
+        });
+        row_add(sdG + 16 * rb + g4, rs0, q4);
+        row_add(sdG + 16 * rb + g4 + 8, rs1, q4);
+    }
+#pragma unroll
+    for (int j = 0; j < NK; ++j)
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) accK[j][n][e] += tmp[j][n][e];
+    zero(tmp);
+    wgemm<NK, C, true, false>(tmp, aY, LC, aK, LK, rb, ck, mi, mr);
+    {
+        float rs0 = 0.f, rs1 = 0.f;
+        each(tmp, rb, ck, g4, q4, [&](int r, int col, float& x) {
+            const float t = bf(Ks + r * LK + col) * x;
+            if (r & 8) rs1 -= t; else rs0 -= t;
+        });
+        row_add(sdG + 16 * rb + g4, rs0, q4);
+        row_add(sdG + 16 * rb + g4 + 8, rs1, q4);
+    }
+#pragma unroll
+    for (int j = 0; j < NK; ++j)
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) accK[j][n][e] += tmp[j][n][e];
+    each(accK, rb, ck, g4, q4, [&](int r, int col, float& x) {
+        if (r < nv) dk[(tok0 + (int64_t)r * H) * K + col] = __float2bfloat16_rn(x);
+    });
+    __syncthreads();
+
+    // ---- phase 4: the last token's gate terms, the reverse cumsum, dbeta
+    if (tid == 0) {
+        sdG[nv - 1] += sS[0] + __expf(sG[nv - 1]) * sS[1];
+        float run = 0.f;
+        for (int i = C - 1; i >= 0; --i) {
+            run += sdG[i];
+            if (i < nv) dg[tok0 + (int64_t)i * H] = run;
+        }
+    }
+    if (tid < nv) dbeta[tok0 + (int64_t)tid * H] = __float2bfloat16_rn(sdB[tid]);
+}
+
+template <int K, int V>
+cudaError_t launch(const Dims& d, const void* q, const void* k, const void* v, const void* beta, const float* g_cum,
+                   const void* w, const void* u, const void* tinv, const void* v_new, const void* h_ckpt,
+                   const void* d_o, const void* dv_new, const void* dh_ckpt, void* dq, void* dk, void* dv,
+                   void* dbeta, float* dg, cudaStream_t s) {
+    using L = ChunkLayout<K, V>;
+    auto kern = bwd_chunk_mma_kernel<K, V>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::bytes);
+    if (e != cudaSuccess) return e;
+    const dim3 grid(d.NT, d.H, d.B);
+    kern<<<grid, kThreads, L::bytes, s>>>((const bf16*)q, (const bf16*)k, (const bf16*)v, (const bf16*)beta, g_cum,
+                                          (const bf16*)w, (const bf16*)u, (const bf16*)tinv, (const bf16*)v_new,
+                                          (const bf16*)h_ckpt, (const bf16*)d_o, (const bf16*)dv_new,
+                                          (const bf16*)dh_ckpt, (bf16*)dq, (bf16*)dk, (bf16*)dv, (bf16*)dbeta, dg,
+                                          d.T, d.H, d.scale);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t mma_bwd_chunk(const Dims& d, const void* q, const void* k, const void* v, const void* beta,
+                          const float* g_cum, const void* w, const void* u, const void* tinv, const void* v_new,
+                          const void* h_ckpt, const void* d_o, const void* dv_new, const void* dh_ckpt, void* dq,
+                          void* dk, void* dv, void* dbeta, float* dg, cudaStream_t s) {
+    if (!d.bf16 || d.per_k || d.C != 64) return cudaErrorInvalidValue;
+#define GDR_CHUNK_ARGS d, q, k, v, beta, g_cum, w, u, tinv, v_new, h_ckpt, d_o, dv_new, dh_ckpt, dq, dk, dv, dbeta, dg, s
+    if (d.K == 64 && d.V == 64) return launch<64, 64>(GDR_CHUNK_ARGS);
+    if (d.K == 64 && d.V == 128) return launch<64, 128>(GDR_CHUNK_ARGS);
+    if (d.K == 128 && d.V == 64) return launch<128, 64>(GDR_CHUNK_ARGS);
+    return launch<128, 128>(GDR_CHUNK_ARGS);
+#undef GDR_CHUNK_ARGS
+}
+
+}  // namespace gdr

@@ -138,15 +138,20 @@ StagedWorkspace plan_staged(const gdr::Dims& d, bool fused) {
 // gdr_backward scratch: the forward's g_cum, w, u, v_new, h_ckpt (io dtype), then the
 // backward's fp32 intermediates, each 256-byte aligned.
 struct BackwardWorkspace {
-    size_t g_cum, w, u, v_new, h_ckpt, dv_loc, dv_new, dh_ckpt, dk_part, dw, dG_part, total;
+    size_t g_cum, w, u, v_new, h_ckpt, dv_loc, dv_new, dh_ckpt, dk_part, dw, dG_part, P, tinv, total;
 };
 
-BackwardWorkspace plan_backward(const gdr::Dims& d) {
+// The backward's paths: the CUDA-core stages after a re-scan on the CUDA cores (SIMT) or on
+// the tensor cores (TENSOR), or every step on the tensor cores (FAST: bf16, scalar gate, C = 64).
+enum class BwdPath { Simt, Tensor, Fast };
+
+BackwardWorkspace plan_backward(const gdr::Dims& d, BwdPath path) {
     const size_t e = d.bf16 ? 2 : 4;
     const size_t rows = (size_t)d.B * d.T * d.H;
     const size_t gw = d.per_k ? d.K : 1;
     const size_t states = (size_t)d.B * d.NT * d.H * d.K * d.V;
-    BackwardWorkspace ws;
+    const size_t tiles = (size_t)d.B * d.NT * d.H * d.C * d.C;
+    BackwardWorkspace ws{};
     size_t off = 0;
     auto take = [&](size_t* field, size_t bytes) { *field = off; off = round_up(off + bytes, 256); };
     take(&ws.g_cum, rows * gw * 4);
@@ -154,26 +159,35 @@ BackwardWorkspace plan_backward(const gdr::Dims& d) {
     take(&ws.u, rows * d.V * e);
     take(&ws.v_new, rows * d.V * e);
     take(&ws.h_ckpt, states * e);
-    take(&ws.dv_loc, rows * d.V * 4);
-    take(&ws.dv_new, rows * d.V * 4);
-    take(&ws.dh_ckpt, states * 4);
-    take(&ws.dk_part, rows * d.K * 4);
-    take(&ws.dw, rows * d.K * 4);
-    take(&ws.dG_part, rows * gw * 4);
+    if (path == BwdPath::Fast) {   // bf16 gradients of v' and of the states; the prepare's P and T
+        take(&ws.dv_new, rows * d.V * 2);
+        take(&ws.dh_ckpt, states * 2);
+        take(&ws.P, tiles * 2);
+        take(&ws.tinv, tiles * 2);
+    } else {
+        take(&ws.dv_loc, rows * d.V * 4);
+        take(&ws.dv_new, rows * d.V * 4);
+        take(&ws.dh_ckpt, states * 4);
+        take(&ws.dk_part, rows * d.K * 4);
+        take(&ws.dw, rows * d.K * 4);
+        take(&ws.dG_part, rows * gw * 4);
+    }
     ws.total = off;
     return ws;
 }
 
-// The backward's forward re-scan: tensor-core kernels for bf16 (AUTO, TENSOR), CUDA-core ones
-// for SIMT and fp32; FUSED keeps no checkpoints and is not offered.
-gdr_status pick_backward(const gdr_problem* p, const gdr::Dims& d, bool* tensor) {
+// AUTO and TENSOR take FAST where it applies; FUSED keeps no checkpoints and is not offered.
+gdr_status pick_backward(const gdr_problem* p, const gdr::Dims& d, BwdPath* path) {
+    const bool fast = d.bf16 && !d.per_k && d.C == 64;
     switch (p->variant) {
-        case GDR_VARIANT_SIMT: *tensor = false; return GDR_OK;
+        case GDR_VARIANT_SIMT: *path = BwdPath::Simt; return GDR_OK;
         case GDR_VARIANT_TENSOR:
             if (!d.bf16) return GDR_ERR_UNSUPPORTED;
-            *tensor = true;
+            *path = fast ? BwdPath::Fast : BwdPath::Tensor;
             return GDR_OK;
-        case GDR_VARIANT_AUTO: *tensor = d.bf16 != 0; return GDR_OK;
+        case GDR_VARIANT_AUTO:
+            *path = !d.bf16 ? BwdPath::Simt : (fast ? BwdPath::Fast : BwdPath::Tensor);
+            return GDR_OK;
         default: return GDR_ERR_UNSUPPORTED;
     }
 }
@@ -353,12 +367,56 @@ gdr_status gdr_bwd_wy(const gdr_problem* p, const void* k, const void* v, const 
     return st;
 }
 
+gdr_status gdr_bwd_prepare(const gdr_problem* p, const void* q, const void* k, const void* v, const float* g,
+                           const void* beta, void* w, void* u, float* g_cum, void* P, void* tinv, void* stream) {
+    gdr::Dims d;
+    gdr_status st = check_problem(p, &d);
+    if (st != GDR_OK) return st;
+    if ((st = check_ptrs({q, k, v, g, beta, w, u, g_cum, P, tinv}, {})) != GDR_OK) return st;
+    if (p->variant == GDR_VARIANT_SIMT || !d.bf16 || d.per_k || d.C != 64) return GDR_ERR_UNSUPPORTED;
+    st = from_cuda(gdr::mma_prepare(d, k, v, g, beta, w, u, g_cum, (cudaStream_t)stream, device_error_word(), q, P,
+                                    tinv));
+    if (st == GDR_OK) t_last_variant = "tensor";
+    return st;
+}
+
+gdr_status gdr_bwd_scan_dh_p(const gdr_problem* p, const void* q, const void* k, const void* w, const float* g_cum,
+                             const void* P, const void* d_o, const float* dh_final, void* dh_ckpt, void* dv_new,
+                             float* dh0, void* stream) {
+    gdr::Dims d;
+    gdr_status st = check_problem(p, &d);
+    if (st != GDR_OK) return st;
+    if ((st = check_ptrs({q, k, w, g_cum, P, d_o, dh_ckpt, dv_new}, {dh_final, dh0})) != GDR_OK) return st;
+    if (p->variant == GDR_VARIANT_SIMT || !d.bf16 || d.per_k || d.C != 64) return GDR_ERR_UNSUPPORTED;
+    st = from_cuda(gdr::mma_bwd_scan(d, q, k, w, g_cum, P, d_o, dh_final, dh_ckpt, dv_new, dh0, (cudaStream_t)stream,
+                                     device_error_word()));
+    if (st == GDR_OK) t_last_variant = "tensor";
+    return st;
+}
+
+gdr_status gdr_bwd_wy_dqkg(const gdr_problem* p, const void* q, const void* k, const void* v, const void* beta,
+                           const float* g_cum, const void* w, const void* u, const void* tinv, const void* v_new,
+                           const void* h_ckpt, const void* d_o, const void* dv_new, const void* dh_ckpt, void* dq,
+                           void* dk, void* dv, void* dbeta, float* dg, void* stream) {
+    gdr::Dims d;
+    gdr_status st = check_problem(p, &d);
+    if (st != GDR_OK) return st;
+    if ((st = check_ptrs({q, k, v, beta, g_cum, w, u, tinv, v_new, h_ckpt, d_o, dv_new, dh_ckpt, dq, dk, dv, dbeta,
+                          dg}, {})) != GDR_OK)
+        return st;
+    if (p->variant == GDR_VARIANT_SIMT || !d.bf16 || d.per_k || d.C != 64) return GDR_ERR_UNSUPPORTED;
+    st = from_cuda(gdr::mma_bwd_chunk(d, q, k, v, beta, g_cum, w, u, tinv, v_new, h_ckpt, d_o, dv_new, dh_ckpt, dq, dk,
+                                      dv, dbeta, dg, (cudaStream_t)stream));
+    if (st == GDR_OK) t_last_variant = "tensor";
+    return st;
+}
+
 size_t gdr_backward_workspace_bytes(const gdr_problem* p) {
     gdr::Dims d;
     if (check_problem(p, &d) != GDR_OK) return 0;
-    bool tensor = false;
-    if (pick_backward(p, d, &tensor) != GDR_OK) return 0;
-    return plan_backward(d).total;
+    BwdPath path;
+    if (pick_backward(p, d, &path) != GDR_OK) return 0;
+    return plan_backward(d, path).total;
 }
 
 gdr_status gdr_backward(const gdr_problem* p, const void* q, const void* k, const void* v, const float* g,
@@ -369,9 +427,10 @@ gdr_status gdr_backward(const gdr_problem* p, const void* q, const void* k, cons
     gdr_status st = check_problem(p, &d);
     if (st != GDR_OK) return st;
     if ((st = check_ptrs({q, k, v, g, beta, d_o, dq, dk, dv, dg, dbeta}, {h0, dh_final, dh0})) != GDR_OK) return st;
-    bool tensor = false;
-    if ((st = pick_backward(p, d, &tensor)) != GDR_OK) return st;
-    const BackwardWorkspace ws = plan_backward(d);
+    BwdPath path;
+    if ((st = pick_backward(p, d, &path)) != GDR_OK) return st;
+    const bool tensor = path != BwdPath::Simt;
+    const BackwardWorkspace ws = plan_backward(d, path);
     if (!workspace || workspace_bytes < ws.total) return GDR_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GDR_ERR_ALIGN;
     char* base = static_cast<char*>(workspace);
@@ -387,6 +446,22 @@ gdr_status gdr_backward(const gdr_problem* p, const void* q, const void* k, cons
     float* dw = reinterpret_cast<float*>(base + ws.dw);
     float* dG_part = reinterpret_cast<float*>(base + ws.dG_part);
     cudaStream_t s = (cudaStream_t)stream;
+    if (path == BwdPath::Fast) {
+        // every step on the tensor cores: prepare (+ P and T), re-scan, reverse scan, per-chunk stage
+        unsigned int* err = device_error_word();
+        void* P = base + ws.P;
+        void* tinv = base + ws.tinv;
+        if ((st = from_cuda(gdr::mma_prepare(d, k, v, g, beta, w, u, g_cum, s, err, q, P, tinv))) != GDR_OK) return st;
+        if ((st = from_cuda(gdr::mma_scan(d, k, w, u, g_cum, h0, h_ckpt, v_new, nullptr, s, err))) != GDR_OK) return st;
+        if ((st = from_cuda(gdr::mma_bwd_scan(d, q, k, w, g_cum, P, d_o, dh_final, dh_ckpt, dv_new, dh0, s, err))) !=
+            GDR_OK)
+            return st;
+        if ((st = from_cuda(gdr::mma_bwd_chunk(d, q, k, v, beta, g_cum, w, u, tinv, v_new, h_ckpt, d_o, dv_new, dh_ckpt,
+                                               dq, dk, dv, dbeta, dg, s))) != GDR_OK)
+            return st;
+        t_last_variant = "tensor";
+        return GDR_OK;
+    }
     // forward prepare and re-scan: G, w, u, the checkpoints and v'
     if (tensor) {
         unsigned int* err = device_error_word();

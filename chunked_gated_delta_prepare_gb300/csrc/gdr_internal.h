@@ -27,10 +27,10 @@ cudaError_t simt_output(const Dims& d, const void* q, const void* k, const void*
 
 // ---- tensor-core kernels (bf16 io only)
 // with q and P non-NULL (scalar gate, C = 64) it also writes P = tril_0(q k^T * exp(G_i - G_j))
-// per chunk as [B, NT, H, C, C] bf16
+// per chunk as [B, NT, H, C, C] bf16; with tinv non-NULL, (I + A)^{-1} per chunk, [B, NT, H, C, C] bf16
 cudaError_t mma_prepare(const Dims& d, const void* k, const void* v, const float* g, const void* beta, void* w,
                         void* u, float* g_cum, cudaStream_t s, unsigned int* err, const void* q = nullptr,
-                        void* P = nullptr);
+                        void* P = nullptr, void* tinv = nullptr);
 // the scan's recurrence runs on mma.sync (register-resident), see scan_mma.cu
 cudaError_t mma_scan(const Dims& d, const void* k, const void* w, const void* u, const float* g_cum, const float* h0,
                      void* h_ckpt, void* v_new, float* h_final, cudaStream_t s, unsigned int* err);
@@ -56,6 +56,18 @@ cudaError_t simt_bwd_dqkwg(const Dims& d, const void* q, const void* k, const vo
 cudaError_t simt_bwd_wy(const Dims& d, const void* k, const void* v, const void* beta, const float* g_cum,
                         const float* dw, const float* du, const float* dk_part, const float* dG_part, void* dk,
                         void* dv, void* dbeta, float* dg, cudaStream_t s);
+
+// ---- backward on the tensor cores (bf16 io, scalar gate, C = 64)
+// reverse scan: dv' = scale P^T do + (k gamma) dh, dh = e^(G_L) dh + scale (q e^G)^T do - w^T dv';
+// dh_ckpt [B,NT,H,K,V] and dv_new [B,T,H,V] bf16 (bwd_scan_mma.cu)
+cudaError_t mma_bwd_scan(const Dims& d, const void* q, const void* k, const void* w, const float* g_cum, const void* P,
+                         const void* d_o, const float* dh_final, void* dh_ckpt, void* dv_new, float* dh0,
+                         cudaStream_t s, unsigned int* err);
+// the per-chunk stage (dq, dk, dv, dbeta, dg) from the chunk's tiles and T = (I + A)^{-1} (bwd_chunk_mma.cu)
+cudaError_t mma_bwd_chunk(const Dims& d, const void* q, const void* k, const void* v, const void* beta,
+                          const float* g_cum, const void* w, const void* u, const void* tinv, const void* v_new,
+                          const void* h_ckpt, const void* d_o, const void* dv_new, const void* dh_ckpt, void* dq,
+                          void* dk, void* dv, void* dbeta, float* dg, cudaStream_t s);
 
 // ---- device error word (device_status.cu)
 // Bounded waits in kernels write a nonzero code here instead of trapping.

@@ -141,7 +141,7 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
                    const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap mu,
                    const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mp,
                    const float* __restrict__ g, const bf16* __restrict__ beta, float* __restrict__ g_cum,
-                   int T, int H, unsigned int* err) {
+                   bf16* __restrict__ tinv, int T, int H, unsigned int* err) {
     using L = PrepLayout<K, V, C, PER_K, WITH_P>;
     constexpr int GW = L::GW;
     extern __shared__ unsigned char smem_raw[];
@@ -472,6 +472,23 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
         }
     }
 
+    // X itself, for the backward's WY stage: [B, NT, H, C, C] bf16, this warp's 16 rows of its chunk
+    if (tinv && t0 + (I / NB) * C < T) {
+        const int ci = t0 / C + I / NB;
+        bf16* dst = tinv + (((int64_t)b * ((T + C - 1) / C) + ci) * H + h) * C * C;
+        const int r0 = 16 * (I - J0) + g4;
+#pragma unroll
+        for (int J = 0; J < 4; ++J) {
+            if (J < J0 || J >= J0 + NB) continue;
+#pragma unroll
+            for (int n = 0; n < 2; ++n) {
+                const int col = 16 * (J - J0) + 8 * n + 2 * q4;
+                *reinterpret_cast<uint32_t*>(dst + (int64_t)r0 * C + col) = wm::pack2(Xr[J][n][0], Xr[J][n][1]);
+                *reinterpret_cast<uint32_t*>(dst + (int64_t)(r0 + 8) * C + col) = wm::pack2(Xr[J][n][2], Xr[J][n][3]);
+            }
+        }
+    }
+
     // Tb fragments: X diag(beta) for u; X diag(beta exp(G)) for w (scalar gate) or X diag(beta) (per-key-dim)
     uint32_t tu[4][4], tw[4][4];
 #pragma unroll
@@ -554,7 +571,7 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
 
 template <int K, int V, int C, bool PER_K, bool WITH_P>
 cudaError_t launch_prepare(const Dims& d, const void* q, const void* k, const void* v, const float* g,
-                           const void* beta, void* w, void* u, float* g_cum, void* P, cudaStream_t s,
+                           const void* beta, void* w, void* u, float* g_cum, void* P, void* tinv, cudaStream_t s,
                            unsigned int* err) {
     using L = PrepLayout<K, V, C, PER_K, WITH_P>;
     CUtensorMap mk, mv, mw, mu, mq, mp;
@@ -576,37 +593,38 @@ cudaError_t launch_prepare(const Dims& d, const void* q, const void* k, const vo
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const dim3 grid((d.T + kTile - 1) / kTile, d.H, d.B);
-    kern<<<grid, 128, smem, s>>>(mk, mv, mw, mu, mq, mp, g, (const bf16*)beta, g_cum, d.T, d.H, err);
+    kern<<<grid, 128, smem, s>>>(mk, mv, mw, mu, mq, mp, g, (const bf16*)beta, g_cum, (bf16*)tinv, d.T, d.H, err);
     return cudaGetLastError();
 }
 
 template <int K, int V, int C>
 cudaError_t pick_gate(const Dims& d, const void* q, const void* k, const void* v, const float* g, const void* beta,
-                      void* w, void* u, float* g_cum, void* P, cudaStream_t s, unsigned int* err) {
-    if (d.per_k) return launch_prepare<K, V, C, true, false>(d, q, k, v, g, beta, w, u, g_cum, P, s, err);
+                      void* w, void* u, float* g_cum, void* P, void* tinv, cudaStream_t s, unsigned int* err) {
+    if (d.per_k) return launch_prepare<K, V, C, true, false>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err);
     if constexpr (C == 64) {
-        if (P) return launch_prepare<K, V, C, false, true>(d, q, k, v, g, beta, w, u, g_cum, P, s, err);
+        if (P) return launch_prepare<K, V, C, false, true>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err);
     }
-    return launch_prepare<K, V, C, false, false>(d, q, k, v, g, beta, w, u, g_cum, P, s, err);
+    return launch_prepare<K, V, C, false, false>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err);
 }
 
 template <int K, int V>
 cudaError_t pick_chunk(const Dims& d, const void* q, const void* k, const void* v, const float* g, const void* beta,
-                       void* w, void* u, float* g_cum, void* P, cudaStream_t s, unsigned int* err) {
-    return d.C == 32 ? pick_gate<K, V, 32>(d, q, k, v, g, beta, w, u, g_cum, P, s, err)
-                     : pick_gate<K, V, 64>(d, q, k, v, g, beta, w, u, g_cum, P, s, err);
+                       void* w, void* u, float* g_cum, void* P, void* tinv, cudaStream_t s, unsigned int* err) {
+    return d.C == 32 ? pick_gate<K, V, 32>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err)
+                     : pick_gate<K, V, 64>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err);
 }
 
 }  // namespace
 
 cudaError_t mma_prepare(const Dims& d, const void* k, const void* v, const float* g, const void* beta, void* w,
-                        void* u, float* g_cum, cudaStream_t s, unsigned int* err, const void* q, void* P) {
+                        void* u, float* g_cum, cudaStream_t s, unsigned int* err, const void* q, void* P,
+                        void* tinv) {
     if (!d.bf16) return cudaErrorInvalidValue;
     if (P && (d.per_k || d.C != 64 || !q)) return cudaErrorInvalidValue;
-    if (d.K == 64 && d.V == 64) return pick_chunk<64, 64>(d, q, k, v, g, beta, w, u, g_cum, P, s, err);
-    if (d.K == 64 && d.V == 128) return pick_chunk<64, 128>(d, q, k, v, g, beta, w, u, g_cum, P, s, err);
-    if (d.K == 128 && d.V == 64) return pick_chunk<128, 64>(d, q, k, v, g, beta, w, u, g_cum, P, s, err);
-    return pick_chunk<128, 128>(d, q, k, v, g, beta, w, u, g_cum, P, s, err);
+    if (d.K == 64 && d.V == 64) return pick_chunk<64, 64>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err);
+    if (d.K == 64 && d.V == 128) return pick_chunk<64, 128>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err);
+    if (d.K == 128 && d.V == 64) return pick_chunk<128, 64>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err);
+    return pick_chunk<128, 128>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err);
 }
 
 }  // namespace gdr

@@ -7,7 +7,8 @@ CPU fallback: if the library is missing or cannot load, every call raises.
 The functions mirror the C ABI names:
     gdr_prepare_wy, gdr_prepare_wyp, gdr_scan_h, gdr_chunk_output, gdr_scan_output, gdr_forward,
     gdr_forward_workspace_bytes, gdr_bwd_dv_local, gdr_bwd_scan_dh, gdr_bwd_dqkwg, gdr_bwd_wy,
-    gdr_backward, gdr_backward_workspace_bytes, gdr_status_string, gdr_get_device_status,
+    gdr_bwd_prepare, gdr_bwd_scan_dh_p, gdr_bwd_wy_dqkg, gdr_backward, gdr_backward_workspace_bytes,
+    gdr_status_string, gdr_get_device_status,
     gdr_last_variant, gdr_version
 and `forward(...)` / `backward(...)` are the convenience calls that allocate outputs and
 the workspace (and, given CPU tensors, copy them to the GPU and the results back).
@@ -33,7 +34,7 @@ VARIANTS = {"auto": 0, "simt": 1, "tensor": 2, "fused": 3}
 EXPORTS = ["gdr_prepare_wy", "gdr_scan_h", "gdr_chunk_output", "gdr_forward", "gdr_forward_workspace_bytes",
            "gdr_forward_static_scratch", "gdr_scan_output", "gdr_prepare_wyp",
            "gdr_bwd_dv_local", "gdr_bwd_scan_dh", "gdr_bwd_dqkwg", "gdr_bwd_wy", "gdr_backward",
-           "gdr_backward_workspace_bytes",
+           "gdr_backward_workspace_bytes", "gdr_bwd_prepare", "gdr_bwd_scan_dh_p", "gdr_bwd_wy_dqkg",
            "gdr_status_string", "gdr_get_device_status", "gdr_last_variant", "gdr_version"]
 
 
@@ -80,6 +81,9 @@ def load(path: str | None = None):
             "gdr_bwd_wy": [P] + [vp] * 13,
             "gdr_backward": [P] + [vp] * 15 + [ctypes.c_size_t, vp],
             "gdr_backward_workspace_bytes": [P],
+            "gdr_bwd_prepare": [P] + [vp] * 11,
+            "gdr_bwd_scan_dh_p": [P] + [vp] * 11,
+            "gdr_bwd_wy_dqkg": [P] + [vp] * 19,
             "gdr_status_string": [ctypes.c_int],
             "gdr_get_device_status": [vp],
             "gdr_last_variant": [],
@@ -257,6 +261,25 @@ def gdr_bwd_wy(p, k, v, beta, g_cum, dw, dv_new, dk_part, dG_part, dk, dv, dbeta
     _check(load().gdr_bwd_wy(ctypes.byref(p), _ptr(k), _ptr(v), _ptr(beta), _ptr(g_cum), _ptr(dw), _ptr(dv_new),
                              _ptr(dk_part), _ptr(dG_part), _ptr(dk), _ptr(dv), _ptr(dbeta), _ptr(dg),
                              _stream(stream)), "gdr_bwd_wy")
+
+
+def gdr_bwd_prepare(p, q, k, v, g, beta, w, u, g_cum, P, tinv, stream=None):
+    _check(load().gdr_bwd_prepare(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(w), _ptr(u),
+                                  _ptr(g_cum), _ptr(P), _ptr(tinv), _stream(stream)), "gdr_bwd_prepare")
+
+
+def gdr_bwd_scan_dh_p(p, q, k, w, g_cum, P, d_o, dh_final, dh_ckpt, dv_new, dh0, stream=None):
+    _check(load().gdr_bwd_scan_dh_p(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(w), _ptr(g_cum), _ptr(P), _ptr(d_o),
+                                    _ptr(dh_final), _ptr(dh_ckpt), _ptr(dv_new), _ptr(dh0), _stream(stream)),
+           "gdr_bwd_scan_dh_p")
+
+
+def gdr_bwd_wy_dqkg(p, q, k, v, beta, g_cum, w, u, tinv, v_new, h_ckpt, d_o, dv_new, dh_ckpt, dq, dk, dv, dbeta, dg,
+                    stream=None):
+    _check(load().gdr_bwd_wy_dqkg(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g_cum), _ptr(w),
+                                  _ptr(u), _ptr(tinv), _ptr(v_new), _ptr(h_ckpt), _ptr(d_o), _ptr(dv_new),
+                                  _ptr(dh_ckpt), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbeta), _ptr(dg),
+                                  _stream(stream)), "gdr_bwd_wy_dqkg")
 
 
 def gdr_backward_workspace_bytes(p) -> int:

@@ -244,10 +244,17 @@ GDR_API gdr_status gdr_forward_static_scratch(const gdr_problem* p, const void* 
  *
  * A partial last chunk is read as in the forward. The gate gradient of its
  * padding goes to token T - 1, whose G the padding repeats.
- * The four stages run on the CUDA cores in fp32 for every variant.  The
- * re-scan runs the tensor-core kernels for bf16 io (variants AUTO and
- * TENSOR), or the CUDA-core ones (variant SIMT, and fp32 io).  The variant
- * FUSED is not offered here (GDR_ERR_UNSUPPORTED).
+ *
+ * Two sets of kernels compute these stages.
+ * - On the CUDA cores in fp32 (entry points gdr_bwd_dv_local, gdr_bwd_scan_dh,
+ *   gdr_bwd_dqkwg, gdr_bwd_wy; fp32 intermediates): every shape, both dtypes.
+ *   Variant SIMT re-scans on the CUDA cores too.  For bf16 io, variants AUTO
+ *   and TENSOR re-scan on the tensor cores, then run these stages whenever the
+ *   tensor-core set below does not apply.
+ * - On the tensor cores (gdr_bwd_prepare, gdr_bwd_scan_dh_p,
+ *   gdr_bwd_wy_dqkg; bf16 intermediates): bf16 io, a scalar gate and C = 64,
+ *   which variants AUTO and TENSOR take.
+ * The variant FUSED is not offered here (GDR_ERR_UNSUPPORTED).
  */
 
 /* dv_loc = scale tril_0(Q~)^T do per chunk.  Inputs q, k, do io; g_cum fp32.
@@ -291,6 +298,32 @@ GDR_API gdr_status gdr_bwd_dqkwg(const gdr_problem* p, const void* q, const void
 GDR_API gdr_status gdr_bwd_wy(const gdr_problem* p, const void* k, const void* v, const void* beta,
                               const float* g_cum, const float* dw, const float* dv_new, const float* dk_part,
                               const float* dG_part, void* dk, void* dv, void* dbeta, float* dg, void* stream);
+
+/* The tensor-core stages (bf16 io, scalar gate, C = 64; GDR_ERR_UNSUPPORTED otherwise). */
+
+/* gdr_prepare_wyp plus T = (I + A)^{-1} of every chunk: tinv [B,NT,H,C,C] bf16, row i of chunk c
+ * holding row i of T.  Other arguments as gdr_prepare_wyp. */
+GDR_API gdr_status gdr_bwd_prepare(const gdr_problem* p, const void* q, const void* k, const void* v, const float* g,
+                                   const void* beta, void* w, void* u, float* g_cum, void* P, void* tinv,
+                                   void* stream);
+
+/* The reverse scan of gdr_bwd_scan_dh with dv_loc = scale P^T do formed inside from the prepare's P.
+ * Inputs q, k, w, do bf16; g_cum fp32; P [B,NT,H,C,C] bf16; dh_final fp32 or NULL.
+ * Outputs dh_ckpt [B,NT,H,K,V] bf16, dv_new [B,T,H,V] bf16, dh0 fp32 or NULL. */
+GDR_API gdr_status gdr_bwd_scan_dh_p(const gdr_problem* p, const void* q, const void* k, const void* w,
+                                     const float* g_cum, const void* P, const void* d_o, const float* dh_final,
+                                     void* dh_ckpt, void* dv_new, float* dh0, void* stream);
+
+/* gdr_bwd_dqkwg and gdr_bwd_wy in one pass per chunk (the pages' wy_dqkg), T read from tinv
+ * instead of rebuilt; the WY term of dA is -(dkb w^T + dvb u^T), which equals
+ * -Tinv^T (dw kb^T + du vb^T) Tinv^T because w = Tinv kb and u = Tinv vb.
+ * Inputs q, k, v, beta, w, u, tinv, v_new, h_ckpt, do, dv_new, dh_ckpt bf16; g_cum fp32.
+ * Outputs dq, dk, dv, dbeta bf16; dg fp32. */
+GDR_API gdr_status gdr_bwd_wy_dqkg(const gdr_problem* p, const void* q, const void* k, const void* v,
+                                   const void* beta, const float* g_cum, const void* w, const void* u,
+                                   const void* tinv, const void* v_new, const void* h_ckpt, const void* d_o,
+                                   const void* dv_new, const void* dh_ckpt, void* dq, void* dk, void* dv,
+                                   void* dbeta, float* dg, void* stream);
 
 /* Bytes of device workspace gdr_backward needs (0 for a problem it would reject). */
 GDR_API size_t gdr_backward_workspace_bytes(const gdr_problem* p);

@@ -280,3 +280,88 @@ def test_stage_wy(shape, per_k, dtype):
     assert scaled_err(dv, y["dv"]) <= tol
     assert scaled_err(dbeta, y["dbeta"]) <= tol
     assert scaled_err(dg, cb.reverse_cumsum(dG_ref, C, per_k)) <= tol
+
+
+# ---------------------------------------------------------------- tensor-core stages (bf16, scalar gate, C = 64)
+
+FAST_SHAPES = [(2, 128, 3, 64, 64, 64), (1, 192, 2, 128, 128, 64), (2, 100, 2, 128, 64, 64), (1, 256, 1, 64, 128, 64)]
+
+
+def _fast_setup(shape, seed):
+    B, T, H, K, V, C = shape
+    x = make_inputs(B, T, H, K, V, io_dtype=torch.bfloat16, with_h0=True, seed=seed)
+    do, dhf = upstream(x, seed + 1)
+    full = cb.backward_chunked(x.q, x.k, x.v, x.g, x.beta, x.h0 * 20, do, dhf, C, 0.125)
+    p = gdr.problem_for(x.q, x.v, x.g, C, scale=0.125, variant="tensor")
+    return x, do, dhf, full, p
+
+
+@pytest.mark.parametrize("shape", FAST_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_tensor_stage_prepare_with_inverse(shape):
+    x, _, _, full, p = _fast_setup(shape, 70)
+    B, T, H, K, V, C = shape
+    NT = -(-T // C)
+    q, k, v, g, beta = (dev(t) for t in (x.q, x.k, x.v, x.g, x.beta))
+    nan = float("nan")
+    w, u, g_cum = torch.full_like(k, nan), torch.full_like(v, nan), torch.full_like(g, nan)
+    P = torch.full((B, NT, H, C, C), nan, device="cuda", dtype=torch.bfloat16)
+    tinv = torch.full((B, NT, H, C, C), nan, device="cuda", dtype=torch.bfloat16)
+    gdr.gdr_bwd_prepare(p, q, k, v, g, beta, w, u, g_cum, P, tinv)
+    torch.cuda.synchronize()
+    assert gdr.gdr_last_variant() == "tensor"
+    A = chunked.gated_A(x.k, x.beta, full["G"], C)
+    assert scaled_err(tinv, chunked.forward_substitution_inverse(A)) <= STAGE_TOL["bf16"]
+    assert scaled_err(P, chunked.gated_causal_scores(x.q, x.k, full["G"], C)) <= STAGE_TOL["bf16"]
+    assert scaled_err(w, full["w"]) <= STAGE_TOL["bf16"] and scaled_err(u, full["u"]) <= STAGE_TOL["bf16"]
+
+
+@pytest.mark.parametrize("shape", FAST_SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("with_dhf", [False, True])
+def test_tensor_stage_reverse_scan(shape, with_dhf):
+    x, do, dhf, full, p = _fast_setup(shape, 72)
+    B, T, H, K, V, C = shape
+    dhf = dhf if with_dhf else None
+    G_r, w_r = rounded(full["G"], torch.float32), rounded(full["w"], torch.bfloat16)
+    P_r = rounded(chunked.gated_causal_scores(x.q, x.k, G_r, C), torch.bfloat16)
+    dl = cb.dv_local(x.q, x.k, G_r, do, C, 0.125)
+    ref = cb.scan_dh(x.q, x.k, w_r, G_r, do, dl, dhf, C, 0.125)
+    NT = -(-T // C)
+    nan = float("nan")
+    dh_ckpt = torch.full((B, NT, H, K, V), nan, device="cuda", dtype=torch.bfloat16)
+    dv_new = torch.full((B, T, H, V), nan, device="cuda", dtype=torch.bfloat16)
+    dh0 = torch.full((B, H, K, V), nan, device="cuda")
+    gdr.gdr_bwd_scan_dh_p(p, dev(x.q), dev(x.k), dev(w_r), dev(G_r), dev(P_r), dev(do), dev(dhf), dh_ckpt, dv_new, dh0)
+    torch.cuda.synchronize()
+    assert gdr.gdr_get_device_status() == 0
+    tol = STAGE_TOL["bf16"]
+    assert scaled_err(dh_ckpt, ref["dh_ckpt"]) <= tol
+    assert scaled_err(dv_new, ref["dv_new"]) <= tol
+    assert scaled_err(dh0, ref["dh0"]) <= tol
+
+
+@pytest.mark.parametrize("shape", FAST_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_tensor_stage_wy_dqkg(shape):
+    x, do, _, full, p = _fast_setup(shape, 74)
+    B, T, H, K, V, C = shape
+    bf = torch.bfloat16
+    G_r = rounded(full["G"], torch.float32)
+    w_r, u_r, vn_r, hc_r = (rounded(full[n], bf) for n in ("w", "u", "v_new", "h_ckpt"))
+    dvn_r, dhc_r = rounded(full["dv_new"], bf), rounded(full["dh_ckpt"], bf)
+    A = chunked.gated_A(x.k, x.beta, G_r, C)
+    tinv_r = rounded(chunked.forward_substitution_inverse(A), bf)
+    a = cb.dqkwg(x.q, x.k, vn_r, w_r, G_r, hc_r, dhc_r, do, dvn_r, C, 0.125)
+    y = cb.wy_backward(x.k, x.v, x.beta, G_r, a["dw"], dvn_r, C)
+    nan = float("nan")
+    dq, dk, dv = torch.full(x.q.shape, nan, device="cuda", dtype=bf), torch.full(x.k.shape, nan, device="cuda",
+                                                                                   dtype=bf), \
+        torch.full(x.v.shape, nan, device="cuda", dtype=bf)
+    dbeta, dg = torch.full(x.beta.shape, nan, device="cuda", dtype=bf), torch.full(x.g.shape, nan, device="cuda")
+    gdr.gdr_bwd_wy_dqkg(p, dev(x.q), dev(x.k), dev(x.v), dev(x.beta), dev(G_r), dev(w_r), dev(u_r), dev(tinv_r),
+                        dev(vn_r), dev(hc_r), dev(do), dev(dvn_r), dev(dhc_r), dq, dk, dv, dbeta, dg)
+    torch.cuda.synchronize()
+    tol = STAGE_TOL["bf16"]
+    assert scaled_err(dq, a["dq"]) <= tol
+    assert scaled_err(dk, a["dk"] + y["dk"]) <= tol
+    assert scaled_err(dv, y["dv"]) <= tol
+    assert scaled_err(dbeta, y["dbeta"]) <= tol
+    assert scaled_err(dg, cb.reverse_cumsum(a["dG"] + y["dG"], C, False)) <= tol

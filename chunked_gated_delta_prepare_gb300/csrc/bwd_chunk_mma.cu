@@ -23,9 +23,12 @@
 // otherwise swamp a small dG).  One CTA of eight warps per (chunk, head,
 // batch); the tiles sit in shared memory as padded bf16 rows (a row stride of
 // D + 8 elements keeps every ldmatrix free of bank conflicts) and every product
-// is a warp-level mma.sync m16n8k16 with fp32 accumulation.  Warp w owns the
-// 16-row block w % 4 and half (w / 4) of the columns of every [C x D] result,
-// so dq and dk accumulate in registers across all their terms.
+// is a warp-level mma.sync m16n8k16 with fp32 accumulation.  Eight warps:
+// warp w owns the 16-row block w % 4 and the column half w / 4 of every
+// [C x D] result, so dq and dk accumulate in registers across all their terms
+// (sixteen warps with column quarters measured no faster).  Tile loads are
+// cp.async groups issued in the order the products need them, and the WY
+// phase's tiles are in flight during the output-score phase.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -37,6 +40,7 @@ namespace {
 
 using bf16 = __nv_bfloat16;
 constexpr int kThreads = 256;
+constexpr int kColGroups = kThreads / 32 / 4;   // warps sharing each 16-row block
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -100,7 +104,9 @@ __device__ __forceinline__ void load_tile(bf16* dst, const bf16* src, int64_t gs
     }
 }
 
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 __device__ __forceinline__ float bf(const bf16* p) { return __bfloat162float(*p); }
 
@@ -115,19 +121,27 @@ template <int K, int V>
 struct ChunkLayout {
     static constexpr int C = 64;
     static constexpr int LK = K + 8, LV = V + 8, LC = C + 8;
-    static constexpr uint32_t rq = 0;                              // q; later w
+    static constexpr uint32_t rq = 0;                              // q
     static constexpr uint32_t rk = rq + C * LK * 2;                // k
     static constexpr uint32_t rdo = rk + C * LK * 2;               // do; later v
     static constexpr uint32_t rvp = rdo + C * LV * 2;              // v'; later u
     static constexpr uint32_t rdv = rvp + C * LV * 2;              // dv'
-    static constexpr uint32_t rh = rdv + C * LV * 2;               // h [K][V]; later dkb [C][K]
-    static constexpr uint32_t rdh = rh + K * LV * 2;               // dhn [K][V]; later dvb [C][V]
+    static constexpr uint32_t rh = rdv + C * LV * 2;               // h [K][V]; later dkb [C][K] (+ T)
+    static constexpr uint32_t rdh = rh + K * LV * 2;               // dhn [K][V]; later dvb [C][V] (+ w)
     static constexpr uint32_t rw = rdh + K * LV * 2;               // dw [C][K]
-    static constexpr uint32_t rx = rw + C * LK * 2;                // Xq; later T
+    static constexpr uint32_t rx = rw + C * LK * 2;                // Xq
     static constexpr uint32_t ry = rx + C * LC * 2;                // Y
     static constexpr uint32_t rf = ry + C * LC * 2;                // fp32 rows
-    static constexpr uint32_t bytes = rf + 8 * C * 4;
+    // the WY phase's T and w, prefetched during phase 2: behind dkb in h's space and behind dvb in
+    // dhn's space where those have room, else in space of their own
+    static constexpr bool kTinH = K * LV * 2 >= C * LK * 2 + C * LC * 2;
+    static constexpr bool kWinDH = K * LV * 2 >= C * LV * 2 + C * LK * 2;
+    static constexpr uint32_t rextra = rf + 8 * C * 4;
+    static constexpr uint32_t rt = kTinH ? rh + C * LK * 2 : rextra;
+    static constexpr uint32_t rw2 = kWinDH ? rdh + C * LV * 2 : rextra + (kTinH ? 0 : C * LC * 2);
+    static constexpr uint32_t bytes = rextra + (kTinH ? 0 : C * LC * 2) + (kWinDH ? 0 : C * LK * 2);
     static_assert(C * LK <= K * LV, "dkb fits over h");
+    static_assert(bytes <= 227 * 1024, "shared memory");
 };
 
 template <int K, int V>
@@ -141,7 +155,7 @@ bwd_chunk_mma_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
                      float scale) {
     using L = ChunkLayout<K, V>;
     constexpr int C = L::C, LK = L::LK, LV = L::LV, LC = L::LC;
-    constexpr int NK = K / 32, NV = V / 32, NC = C / 32;   // 16-column blocks per warp
+    constexpr int NK = K / 16 / kColGroups, NV = V / 16 / kColGroups, NC = C / 16 / kColGroups;   // blocks per warp
     extern __shared__ __align__(128) unsigned char sm[];
     bf16* Qs = reinterpret_cast<bf16*>(sm + L::rq);
     bf16* Ks = reinterpret_cast<bf16*>(sm + L::rk);
@@ -164,7 +178,7 @@ bwd_chunk_mma_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g4 = lane >> 2, q4 = lane & 3, mi = lane >> 3, mr = lane & 7;
-    const int rb = warp & 3, half = warp >> 2;
+    const int rb = warp & 3, cg = warp >> 2;
     const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int NT = (T + C - 1) / C;
     const int t0 = c * C, nv = min(C, T - t0);
@@ -185,25 +199,48 @@ bwd_chunk_mma_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
         if (i < 2) sS[i] = 0.f;
     }
     // ---- phase 1 tiles
+    // in three groups, in the order the products need them
     load_tile<V>(Hs, h_ckpt + st_off * K * V, V, K, K, tid);
     load_tile<V>(DOs, d_o + tok0 * V, (int64_t)H * V, C, nv, tid);
-    load_tile<V>(DHs, dh_ckpt + st_off * K * V, V, K, K, tid);
+    cp_async_commit();
     load_tile<V>(VPs, v_new + tok0 * V, (int64_t)H * V, C, nv, tid);
+    load_tile<V>(DHs, dh_ckpt + st_off * K * V, V, K, K, tid);
+    cp_async_commit();
     load_tile<V>(DVs, dv_new + tok0 * V, (int64_t)H * V, C, nv, tid);
     load_tile<K>(Qs, q + tok0 * K, (int64_t)H * K, C, nv, tid);
     load_tile<K>(Ks, k + tok0 * K, (int64_t)H * K, C, nv, tid);
-    cp_async_wait_all();
-    __syncthreads();
+    cp_async_commit();
 
     const uint32_t aQ = smem_addr(Qs), aK = smem_addr(Ks), aDO = smem_addr(DOs), aVP = smem_addr(VPs);
     const uint32_t aDV = smem_addr(DVs), aH = smem_addr(Hs), aDH = smem_addr(DHs), aDW = smem_addr(DWs);
     const uint32_t aX = smem_addr(Xs), aY = smem_addr(Ys);
-    const int ck = half * NK, cv = half * NV, cc = half * NC;   // this warp's first column block
+    const int ck = cg * NK, cv = cg * NV, cc = cg * NC;   // this warp's first column block
 
     float accQ[NK][2][4], accK[NK][2][4], tmp[NK][2][4];
-    // dqg = do h^T: the e^G-scaled part of dq, and its gate term
+    // dqg = do h^T (h, do landed)
+    cp_async_wait<2>();
+    __syncthreads();
     zero(accQ);
     wgemm<NK, V, false, true>(accQ, aDO, LV, aH, LV, rb, ck, mi, mr);
+    // dkg = v' dhn^T and the output scores do v'^T (v', dhn landed)
+    cp_async_wait<1>();
+    __syncthreads();
+    zero(accK);
+    wgemm<NK, V, false, true>(accK, aVP, LV, aDH, LV, rb, ck, mi, mr);
+    // Xq = scale (do v'^T) Gam, strictly lower, with its diagonal apart
+    {
+        float xq[NC][2][4];
+        zero(xq);
+        wgemm<NC, V, false, true>(xq, aDO, LV, aVP, LV, rb, cc, mi, mr);
+        each(xq, rb, cc, g4, q4, [&](int r, int col, float& x) {
+            const float y = scale * x;
+            if (col == r) sDiag[r] = y;
+            Xs[r * LC + col] = __float2bfloat16_rn(col < r ? y * __expf(sG[r] - sG[col]) : 0.f);
+        });
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+    // dq's e^G-scaled part and its gate term
     {
         float rs0 = 0.f, rs1 = 0.f;
         each(accQ, rb, ck, g4, q4, [&](int r, int col, float& x) {
@@ -215,9 +252,7 @@ bwd_chunk_mma_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
         row_add(sdG + 16 * rb + g4, rs0, q4);
         row_add(sdG + 16 * rb + g4 + 8, rs1, q4);
     }
-    // dkg = v' dhn^T: dk's e^(G_L - G) part; the gate terms go to the rows, the last row takes their sum
-    zero(accK);
-    wgemm<NK, V, false, true>(accK, aVP, LV, aDH, LV, rb, ck, mi, mr);
+    // dk's e^(G_L - G) part from dkg; the gate terms go to the rows, the last row takes their sum
     {
         float rs0 = 0.f, rs1 = 0.f, tot = 0.f;
         each(accK, rb, ck, g4, q4, [&](int r, int col, float& x) {
@@ -236,17 +271,6 @@ bwd_chunk_mma_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
     zero(tmp);
     wgemm<NK, V, false, true>(tmp, aDV, LV, aH, LV, rb, ck, mi, mr);
     each(tmp, rb, ck, g4, q4, [&](int r, int col, float& x) { DWs[r * LK + col] = __float2bfloat16_rn(-x); });
-    // Xq = scale (do v'^T) Gam, strictly lower, with its diagonal apart
-    {
-        float xq[NC][2][4];
-        zero(xq);
-        wgemm<NC, V, false, true>(xq, aDO, LV, aVP, LV, rb, cc, mi, mr);
-        each(xq, rb, cc, g4, q4, [&](int r, int col, float& x) {
-            const float y = scale * x;
-            if (col == r) sDiag[r] = y;
-            Xs[r * LC + col] = __float2bfloat16_rn(col < r ? y * __expf(sG[r] - sG[col]) : 0.f);
-        });
-    }
     // sum h dhn, eight elements per step
     {
         float s = 0.f;
@@ -264,6 +288,16 @@ bwd_chunk_mma_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
         if (lane == 0) atomicAdd(sS + 1, s);
     }
     __syncthreads();
+    // the WY phase's tiles, in flight during phase 2 (h, dhn, do and v' are dead now)
+    bf16* Ws = reinterpret_cast<bf16*>(sm + L::rw2);
+    bf16* Vs = DOs;
+    bf16* Us = VPs;
+    bf16* Ts = reinterpret_cast<bf16*>(sm + L::rt);
+    load_tile<C>(Ts, tinv + st_off * C * C, C, C, C, tid);
+    load_tile<K>(Ws, w + tok0 * K, (int64_t)H * K, C, nv, tid);
+    load_tile<V>(Vs, v + tok0 * V, (int64_t)H * V, C, nv, tid);
+    load_tile<V>(Us, u + tok0 * V, (int64_t)H * V, C, nv, tid);
+    cp_async_commit();
 
     // ---- phase 2: the output scores' other factors
     zero(tmp);
@@ -309,17 +343,9 @@ bwd_chunk_mma_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
     __syncthreads();
 
     // ---- phase 3: the WY backward
-    bf16* Ws = Qs;
-    bf16* Vs = DOs;
-    bf16* Us = VPs;
-    bf16* Ts = Xs;
     bf16* DKBs = Hs;
     bf16* DVBs = DHs;
-    load_tile<C>(Ts, tinv + st_off * C * C, C, C, C, tid);
-    load_tile<K>(Ws, w + tok0 * K, (int64_t)H * K, C, nv, tid);
-    load_tile<V>(Vs, v + tok0 * V, (int64_t)H * V, C, nv, tid);
-    load_tile<V>(Us, u + tok0 * V, (int64_t)H * V, C, nv, tid);
-    cp_async_wait_all();
+    cp_async_wait<0>();
     __syncthreads();
     const uint32_t aT = smem_addr(Ts), aW = smem_addr(Ws), aU = smem_addr(Us);
     // dkb = T^T dw

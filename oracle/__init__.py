@@ -107,8 +107,13 @@ def host_cores() -> int:
 
 def naive_forward(q, k, v, g, beta, h0, C, scale, *, with_ckpt=True, nthreads=None, vblock=None,
                   lib=None):
-    """Token recurrence in float64.  Returns dict(o, h_final[, ckpt]) as numpy arrays."""
-    q, k, v, g, beta = (chunked._f64(x) for x in (q, k, v, g, beta))
+    """Token recurrence in float64.  Returns dict(o, h_final[, ckpt]) as numpy arrays.
+
+    q and k may have fewer heads than v (grouped value heads): value head hv reads
+    the q and k of head hv // (HV / H)."""
+    HV = chunked._f64(v).shape[2]
+    q, k = chunked._expand_heads(q, HV), chunked._expand_heads(k, HV)
+    v, g, beta = (chunked._f64(x) for x in (v, g, beta))
     h0 = chunked._f64(h0)
     B, T, H, K = k.shape
     V = v.shape[-1]
@@ -137,8 +142,13 @@ def naive_backward(q, k, v, g, beta, h0, do, dh_final, C, scale, *, nthreads=Non
     """Gradients of (o, h_final) by reverse mode over the token recurrence, in float64.
 
     `do` is the loss gradient with respect to o [B,T,H,V]; `dh_final` with respect
-    to h_final [B,H,K,V] (None: zero).  Returns dict(dq, dk, dv, dg, dbeta, dh0)."""
-    q, k, v, g, beta, do = (chunked._f64(x) for x in (q, k, v, g, beta, do))
+    to h_final [B,H,K,V] (None: zero).  Returns dict(dq, dk, dv, dg, dbeta, dh0).
+
+    With grouped value heads (q, k of fewer heads than v) each value head reads
+    its group's q and k, and dq, dk of a shared head sum over the group."""
+    HV, Hqk = chunked._f64(v).shape[2], chunked._f64(q).shape[2]
+    q, k = chunked._expand_heads(q, HV), chunked._expand_heads(k, HV)
+    v, g, beta, do = (chunked._f64(x) for x in (v, g, beta, do))
     h0, dh_final = chunked._f64(h0), chunked._f64(dh_final)
     B, T, H, K = k.shape
     V = v.shape[-1]
@@ -153,4 +163,6 @@ def naive_backward(q, k, v, g, beta, h0, do, dh_final, C, scale, *, nthreads=Non
                                    _ptr(out["dg"]), _ptr(out["dbeta"]), _ptr(out["dh0"]), nthreads)
     if rc != 0:
         raise ValueError("oracle_naive_backward rejected its arguments")
+    from .chunked_backward import group_sum
+    out["dq"], out["dk"] = group_sum(out["dq"], Hqk), group_sum(out["dk"], Hqk)
     return out

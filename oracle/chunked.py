@@ -41,9 +41,15 @@ chunk has its checkpoint like any other (NT = ceil(T / C)).  In the chunked
 cumulative gate a padded token repeats the last real value (the cumsum of a
 zero g), which keeps every exp(G_i - G_j) bounded.
 
+Grouped value heads: q and k may have fewer heads (H) than the value-side
+tensors (HV = G H: v, g, beta, w, u, v', o, the states).  Value head hv then
+reads the q and k of head hv // G, the plain meaning of a group sharing its
+queries and keys; every stage expands q and k to HV heads that way before it
+computes.  (The scan page indexes its tensors by value head, kv heads shared.)
+
 Layouts follow the library boundary (head dim last):
-  q, k, w [B,T,H,K]; v, u, v_new, o [B,T,H,V]; g, G [B,T,H] or [B,T,H,K];
-  beta [B,T,H]; h0, h_final [B,H,K,V]; ckpt [B,NT,H,K,V].
+  q, k [B,T,H,K]; w [B,T,HV,K]; v, u, v_new, o [B,T,HV,V]; g, G [B,T,HV] or
+  [B,T,HV,K]; beta [B,T,HV]; h0, h_final [B,HV,K,V]; ckpt [B,NT,HV,K,V].
 All arrays are numpy float64.
 """
 from __future__ import annotations
@@ -88,6 +94,17 @@ def _ragged(T, C):
     return T % C != 0
 
 
+def _expand_heads(x, HV):
+    """q or k of H heads as read by HV = G H value heads: value head hv reads head hv // G."""
+    x = _f64(x)
+    H = x.shape[2]
+    if H == HV:
+        return x
+    if HV % H:
+        raise ValueError("the value heads must be a multiple of the q/k heads")
+    return np.repeat(x, HV // H, axis=2)
+
+
 def _gate_vec(G, C):
     """Chunked gate with a trailing key axis: [B,NT,H,C,1] (scalar) or [B,NT,H,C,K]."""
     Gc = _to_chunks(G, C)
@@ -125,6 +142,7 @@ def gated_A(k, beta, G, C):
     """A_ij = beta_i sum_d k_id k_jd exp(G_id - G_jd) for i > j, zero elsewhere.
 
     Returned chunked: [B,NT,H,C,C]."""
+    k = _expand_heads(k, _f64(beta).shape[2])
     if _ragged(k.shape[1], C):
         return gated_A(_pad_tokens(_f64(k), C), _pad_tokens(_f64(beta), C), _pad_tokens(_f64(G), C, edge=True), C)
     kc = _to_chunks(_f64(k), C)                 # [B,NT,H,C,K]
@@ -142,7 +160,7 @@ def gated_A(k, beta, G, C):
 def prepare_wy(k, v, g, beta, C):
     """Stage 0 + 1.  Returns dict(G, A, Tinv, w, u); G/w/u in boundary layout,
     A and Tinv chunked [B,NT,H,C,C]."""
-    k, v, beta = _f64(k), _f64(v), _f64(beta)
+    k, v, beta = _expand_heads(k, _f64(beta).shape[2]), _f64(v), _f64(beta)
     T = k.shape[1]
     if _ragged(T, C):
         p = prepare_wy(_pad_tokens(k, C), _pad_tokens(v, C), _pad_tokens(_f64(g), C), _pad_tokens(beta, C), C)
@@ -164,7 +182,7 @@ def scan_h(k, w, u, G, h0, C):
     """Stage 2: the serial inter-chunk state scan.
 
     Returns dict(ckpt [B,NT,H,K,V], v_new [B,T,H,V], h_final [B,H,K,V])."""
-    k, w, u, G = _f64(k), _f64(w), _f64(u), _f64(G)
+    k, w, u, G = _expand_heads(k, _f64(w).shape[2]), _f64(w), _f64(u), _f64(G)
     if _ragged(k.shape[1], C):
         T = k.shape[1]
         s = scan_h(_pad_tokens(k, C), _pad_tokens(w, C), _pad_tokens(u, C), _pad_tokens(G, C, edge=True), h0, C)
@@ -191,6 +209,7 @@ def gated_causal_scores(q, k, G, C):
     """tril_0(Q~) per chunk, Q~_ij = sum_d q_id k_jd exp(G_id - G_jd), diagonal included.
 
     Returned chunked: [B,NT,H,C,C]."""
+    q, k = _expand_heads(q, _f64(G).shape[2]), _expand_heads(k, _f64(G).shape[2])
     if _ragged(q.shape[1], C):
         return gated_causal_scores(_pad_tokens(_f64(q), C), _pad_tokens(_f64(k), C),
                                    _pad_tokens(_f64(G), C, edge=True), C)
@@ -205,7 +224,8 @@ def gated_causal_scores(q, k, G, C):
 
 def chunk_output(q, k, v_new, ckpt, G, C, scale):
     """Stage 3: o = scale [ (q exp(G)) ckpt[c] + tril_0(Q~) v'_c ]."""
-    q, k, v_new, ckpt, G = _f64(q), _f64(k), _f64(v_new), _f64(ckpt), _f64(G)
+    HV = _f64(v_new).shape[2]
+    q, k, v_new, ckpt, G = _expand_heads(q, HV), _expand_heads(k, HV), _f64(v_new), _f64(ckpt), _f64(G)
     if _ragged(q.shape[1], C):
         T = q.shape[1]
         return chunk_output(_pad_tokens(q, C), _pad_tokens(k, C), _pad_tokens(v_new, C), ckpt,

@@ -43,6 +43,10 @@ where L(X, Y)_i = sum_j X_ij Y_j e^(G_i - G_j) and R(X, Y)_j = sum_i X_ij Y_i e^
 elementwise over the key dim.  For a scalar gate every e^G is a scalar per row
 and dG is summed over the key dim.
 
+With grouped value heads (q, k of H heads shared by HV = G H value heads, as in
+chunked.py) every stage works per value head on q and k expanded to HV heads,
+and dq and dk of a shared head are the sums over its group (`group_sum`).
+
 A partial last chunk is padded as in chunked.py (beta = 0, g = 0, zero q, k, v,
 do; G repeats its last value).  A padded row's G is a copy of G at row T - 1,
 so the gate gradient of the padded rows is added to row T - 1 before the
@@ -52,8 +56,17 @@ from __future__ import annotations
 
 import numpy as np
 
-from .chunked import (_f64, _from_chunks, _gate_vec, _pad_tokens, _ragged, _to_chunks,
+from .chunked import (_expand_heads, _f64, _from_chunks, _gate_vec, _pad_tokens, _ragged, _to_chunks,
                       forward_substitution_inverse, gated_A, gated_causal_scores, prepare_wy, scan_h)
+
+
+def group_sum(x, H):
+    """[B,T,HV,...] per value head -> [B,T,H,...]: the gradient of a head its group shares."""
+    x = _f64(x)
+    B, T, HV = x.shape[:3]
+    if HV == H:
+        return x
+    return x.reshape(B, T, H, HV // H, *x.shape[3:]).sum(axis=3)
 
 
 def _last_row_fold(dG, T):
@@ -83,6 +96,7 @@ def _pairwise(X, Yl, Yr, Gc):
 
 def dv_local(q, k, G, do, C, scale):
     """scale tril0(Qt)^T do, per chunk: [B,T,H,V]."""
+    q, k = _expand_heads(q, _f64(do).shape[2]), _expand_heads(k, _f64(do).shape[2])
     T = q.shape[1]
     if _ragged(T, C):
         qp, kp, dop, Gp = _pad_all(C, q, k, do, G, edge_last=True)
@@ -95,6 +109,7 @@ def dv_local(q, k, G, do, C, scale):
 def scan_dh(q, k, w, G, do, dv_loc, dh_final, C, scale):
     """Reverse scan.  Returns dict(dh_ckpt [B,NT,H,K,V] (gradient of the state after
     each chunk), dv_new [B,T,H,V] (gradient of v'), dh0 [B,H,K,V])."""
+    q, k = _expand_heads(q, _f64(w).shape[2]), _expand_heads(k, _f64(w).shape[2])
     T = q.shape[1]
     if _ragged(T, C):
         qp, kp, wp, dop, dvp, Gp = _pad_all(C, q, k, w, do, dv_loc, G, edge_last=True)
@@ -124,7 +139,8 @@ def dqkwg(q, k, v_new, w, G, h_ckpt, dh_ckpt, do, dv_new, C, scale):
     """Per-chunk gradients through the output, the state update and v' = u - w h.
 
     Returns dict(dq, dk, dw) [B,T,H,K] and dG [B,T,H,K] (per key dim, before the
-    sum a scalar gate takes)."""
+    sum a scalar gate takes); dq and dk per value head."""
+    q, k = _expand_heads(q, _f64(w).shape[2]), _expand_heads(k, _f64(w).shape[2])
     T = q.shape[1]
     if _ragged(T, C):
         qp, kp, vp, wp, dop, dvp, Gp = _pad_all(C, q, k, v_new, w, do, dv_new, G, edge_last=True)
@@ -156,7 +172,8 @@ def dqkwg(q, k, v_new, w, G, h_ckpt, dh_ckpt, do, dv_new, C, scale):
 def wy_backward(k, v, beta, G, dw, du, C):
     """Gradients through w = Tinv (beta k e^G) and u = Tinv (beta v), with Tinv rebuilt.
 
-    Returns dict(dk [B,T,H,K], dv [B,T,H,V], dbeta [B,T,H], dG [B,T,H,K])."""
+    Returns dict(dk [B,T,H,K] per value head, dv [B,T,H,V], dbeta [B,T,H], dG [B,T,H,K])."""
+    k = _expand_heads(k, _f64(beta).shape[2])
     T = k.shape[1]
     if _ragged(T, C):
         kp, vp, bp, dwp, dup, Gp = _pad_all(C, k, v, beta, dw, du, G, edge_last=True)
@@ -202,6 +219,7 @@ def reverse_cumsum(dG, C, per_k):
 def backward_chunked(q, k, v, g, beta, h0, do, dh_final, C, scale):
     """All stages.  Returns dict(dq, dk, dv, dg, dbeta, dh0) and every intermediate."""
     per_k = _f64(g).ndim == 4
+    Hqk = _f64(q).shape[2]
     p = prepare_wy(k, v, g, beta, C)
     s = scan_h(k, p["w"], p["u"], p["G"], h0, C)
     dl = dv_local(q, k, p["G"], do, C, scale)
@@ -211,5 +229,5 @@ def backward_chunked(q, k, v, g, beta, h0, do, dh_final, C, scale):
     dG = a["dG"] + y["dG"]
     return dict(G=p["G"], w=p["w"], u=p["u"], v_new=s["v_new"], h_ckpt=s["ckpt"], dv_local=dl,
                 dh_ckpt=b["dh_ckpt"], dv_new=b["dv_new"], dw=a["dw"], dG=dG,
-                dq=a["dq"], dk=a["dk"] + y["dk"], dv=y["dv"], dbeta=y["dbeta"],
+                dq=group_sum(a["dq"], Hqk), dk=group_sum(a["dk"] + y["dk"], Hqk), dv=y["dv"], dbeta=y["dbeta"],
                 dg=reverse_cumsum(dG, C, per_k), dh0=b["dh0"])

@@ -179,3 +179,48 @@ def test_chunked_stage_invariants():
     np.testing.assert_array_equal(r["dh_ckpt"][:, -1], dhf)          # the last chunk sees dh_final
     # dg is the reverse cumsum of dG within each chunk: its chunk-first rows hold the chunk sums
     np.testing.assert_allclose(r["dg"][:, ::16], r["dG"].reshape(2, 4, 16, 2, 6).sum(axis=2), atol=1e-12)
+
+
+# ---------------------------------------------------------------- grouped value heads
+
+def grouped_problem(per_k, *, B=1, T=9, H=1, G=2, K=3, V=2, seed=60):
+    d, do, dhf = problem(per_k, B=B, T=T, H=H * G, K=K, V=V, seed=seed)
+    rng = np.random.default_rng(seed)
+    d["q"] = rng.standard_normal((B, T, H, K))
+    d["k"] = rng.standard_normal((B, T, H, K)) / np.sqrt(K)
+    return d, do, dhf
+
+
+@pytest.mark.parametrize("per_k", [False, True])
+def test_grouped_adjoint_matches_finite_differences(per_k):
+    # dq and dk of a shared head are the sums over its group: checked against central
+    # differences of the grouped forward
+    d, do, dhf = grouped_problem(per_k)
+
+    def loss():
+        r = oracle.naive_forward(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], 4, 0.6, with_ckpt=False)
+        return float((r["o"] * do).sum() + (r["h_final"] * dhf).sum())
+
+    got = adjoint(d, do, dhf, 4, 0.6)
+    assert got["dq"].shape == d["q"].shape and got["dk"].shape == d["k"].shape
+    for name in GRADS:
+        x = d[INPUT_OF[name]]
+        fd = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            old = x[idx]
+            x[idx] = old + 1e-6
+            lp = loss()
+            x[idx] = old - 1e-6
+            lm = loss()
+            x[idx] = old
+            fd[idx] = (lp - lm) / 2e-6
+        assert rel(got[name], fd) <= 1e-7, name
+
+
+@pytest.mark.parametrize("per_k", [False, True])
+def test_grouped_chunked_backward_equals_token_reverse_mode(per_k):
+    d, do, dhf = grouped_problem(per_k, B=2, T=70, H=2, G=2, K=6, V=5, seed=61)
+    n = adjoint(d, do, dhf, 16, 0.4)
+    c = cb.backward_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], do, dhf, 16, 0.4)
+    for name in GRADS:
+        assert rel(c[name], n[name]) <= 1e-10, name

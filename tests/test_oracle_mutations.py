@@ -269,3 +269,23 @@ def test_chunked_backward_mutant_is_caught(what, old, new):
         src = f.read()
     assert src.count(old) == 1, f"mutation site not found: {old!r}"
     assert _chunked_bwd_pins_fail(_load_chunked_bwd(src.replace(old, new)))
+
+
+# ------------------------------------------------------------ grouped value heads
+
+def test_grouping_by_remainder_is_caught():
+    # a value head reading q/k head hv % H (np.tile) instead of hv // G (np.repeat)
+    with open(CHUNKED_SRC) as f:
+        src = f.read()
+    old = "return np.repeat(x, HV // H, axis=2)"
+    assert src.count(old) == 1
+    mod = _load_chunked(src.replace(old, "return np.tile(x, (1, 1, HV // H) + (1,) * (x.ndim - 3))"))
+    from test_oracle_pins import explicit_matrix_recurrence, grouped
+    d = grouped(False, H=2, G=2, seed=53)
+    got = mod.forward_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], 8, 0.4)
+    hv, G = 1, 2                      # value head 1 belongs to q/k head 0
+    one = dict(q=d["q"][:, :, hv // G: hv // G + 1], k=d["k"][:, :, hv // G: hv // G + 1],
+               v=d["v"][:, :, hv:hv + 1], g=d["g"][:, :, hv:hv + 1], beta=d["beta"][:, :, hv:hv + 1],
+               h0=d["h0"][:, hv:hv + 1])
+    eo, _ = explicit_matrix_recurrence(one, 0.4)
+    assert np.abs(got["o"][:, :, hv:hv + 1] - eo).max() > 1e-6

@@ -344,3 +344,47 @@ def test_zero_tokens_are_identity_updates(per_k):
     np.testing.assert_allclose(re["o"][:, :40], r["o"], atol=1e-13)
     np.testing.assert_allclose(re["o"][:, 40:], 0.5 * np.einsum("bhkv,btk->bthv", r["h_final"],
                                                                 np.ones((2, 9, 8))), atol=1e-12)
+
+
+# ---------------------------------------------------------------- grouped value heads
+
+def grouped(per_k, *, B=2, T=40, H=2, G=3, K=6, V=5, seed=0):
+    """q, k with H heads; v, g, beta, h0 with H*G value heads."""
+    x = make_inputs(B, T, H * G, K, V, per_k_gate=per_k, io_dtype=torch.float32, with_h0=True, seed=seed)
+    d = {n: t.double().numpy() for n, t in x.tensors().items()}
+    d["h0"] = d["h0"] * 10.0
+    rng = np.random.default_rng(seed)
+    d["q"] = rng.standard_normal((B, T, H, K)) / np.sqrt(K)
+    d["k"] = rng.standard_normal((B, T, H, K))
+    d["k"] /= np.linalg.norm(d["k"], axis=-1, keepdims=True)
+    return d
+
+
+@pytest.mark.parametrize("per_k", [False, True])
+def test_grouped_heads_match_a_per_value_head_recurrence(per_k):
+    # each value head hv runs the plain recurrence on the q and k of head hv // G (indexed here
+    # directly, not through the oracle's expansion), with its own v, g, beta and state
+    d = grouped(per_k, seed=51)
+    B, T, HV = d["v"].shape[:3]
+    H = d["q"].shape[2]
+    G = HV // H
+    n = oracle.naive_forward(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], 16, 0.4)
+    c = oracle.forward_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], 16, 0.4)
+    for hv in range(HV):
+        one = dict(q=d["q"][:, :, hv // G: hv // G + 1], k=d["k"][:, :, hv // G: hv // G + 1],
+                   v=d["v"][:, :, hv:hv + 1], g=d["g"][:, :, hv:hv + 1], beta=d["beta"][:, :, hv:hv + 1],
+                   h0=d["h0"][:, hv:hv + 1])
+        eo, eh = explicit_matrix_recurrence(one, 0.4)
+        for r in (n, c):
+            np.testing.assert_allclose(r["o"][:, :, hv:hv + 1], eo, atol=1e-11)
+            np.testing.assert_allclose(r["h_final"][:, hv:hv + 1], eh, atol=1e-11)
+
+
+def test_grouped_heads_with_equal_value_sides_agree():
+    # value heads of one group that share v, g, beta and h0 as well give identical results
+    d = grouped(True, H=1, G=2, seed=52)
+    for n in ("v", "g", "beta"):
+        d[n][:, :, 1] = d[n][:, :, 0]
+    d["h0"][:, 1] = d["h0"][:, 0]
+    r = oracle.naive_forward(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], 8, 0.5)
+    assert np.array_equal(r["o"][:, :, 0], r["o"][:, :, 1])

@@ -151,7 +151,7 @@ bwd_chunk_mma_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
                      const bf16* __restrict__ u, const bf16* __restrict__ tinv, const bf16* __restrict__ v_new,
                      const bf16* __restrict__ h_ckpt, const bf16* __restrict__ d_o, const bf16* __restrict__ dv_new,
                      const bf16* __restrict__ dh_ckpt, bf16* __restrict__ dq, bf16* __restrict__ dk,
-                     bf16* __restrict__ dv, bf16* __restrict__ dbeta, float* __restrict__ dg, int T, int H,
+                     bf16* __restrict__ dv, bf16* __restrict__ dbeta, float* __restrict__ dg, int T, int H, int G,
                      float scale) {
     using L = ChunkLayout<K, V>;
     constexpr int C = L::C, LK = L::LK, LV = L::LV, LC = L::LC;
@@ -183,6 +183,8 @@ bwd_chunk_mma_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
     const int NT = (T + C - 1) / C;
     const int t0 = c * C, nv = min(C, T - t0);
     const int64_t tok0 = ((int64_t)b * T + t0) * H + h;      // row of token t0, head h
+    const int Hk = H / G;
+    const int64_t ktok0 = ((int64_t)b * T + t0) * Hk + h / G; // q and k: row of token t0, q/k head h / G
     const int64_t st_off = (((int64_t)b * NT + c) * H + h);  // this chunk's [K][V] / [C][C] block index
 
     // ---- gate rows and beta
@@ -207,8 +209,8 @@ bwd_chunk_mma_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
     load_tile<V>(DHs, dh_ckpt + st_off * K * V, V, K, K, tid);
     cp_async_commit();
     load_tile<V>(DVs, dv_new + tok0 * V, (int64_t)H * V, C, nv, tid);
-    load_tile<K>(Qs, q + tok0 * K, (int64_t)H * K, C, nv, tid);
-    load_tile<K>(Ks, k + tok0 * K, (int64_t)H * K, C, nv, tid);
+    load_tile<K>(Qs, q + ktok0 * K, (int64_t)Hk * K, C, nv, tid);
+    load_tile<K>(Ks, k + ktok0 * K, (int64_t)Hk * K, C, nv, tid);
     cp_async_commit();
 
     const uint32_t aQ = smem_addr(Qs), aK = smem_addr(Ks), aDO = smem_addr(DOs), aVP = smem_addr(VPs);
@@ -479,7 +481,7 @@ cudaError_t launch(const Dims& d, const void* q, const void* k, const void* v, c
                                           (const bf16*)w, (const bf16*)u, (const bf16*)tinv, (const bf16*)v_new,
                                           (const bf16*)h_ckpt, (const bf16*)d_o, (const bf16*)dv_new,
                                           (const bf16*)dh_ckpt, (bf16*)dq, (bf16*)dk, (bf16*)dv, (bf16*)dbeta, dg,
-                                          d.T, d.H, d.scale);
+                                          d.T, d.H, d.G, d.scale);
     return cudaGetLastError();
 }
 

@@ -80,7 +80,7 @@ bwd_scan_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constan
                     const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mdo,
                     const __grid_constant__ CUtensorMap mp, const float* __restrict__ g_cum,
                     const float* __restrict__ dh_final, bf16* __restrict__ dh_ckpt, bf16* __restrict__ dv_new,
-                    float* __restrict__ dh0, int T, int H, int V, float scale, unsigned int* err) {
+                    float* __restrict__ dh0, int T, int H, int V, int G, float scale, unsigned int* err) {
     using L = RScanLayout<K, C>;
     constexpr int KH = L::KH, NT8 = L::NT8;
     constexpr int NJH = KH / 8;
@@ -117,9 +117,9 @@ bwd_scan_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constan
                 bw::mbar_arrive_expect_tx(&full[s], L::tx);
 #pragma unroll
                 for (int a = 0; a < K / 64; ++a) {
-                    bw::tma_load_4d(sm + L::KB + s * L::kKC + a * C * 128, &mk, &full[s], a * 64, h, t0, b);
+                    bw::tma_load_4d(sm + L::KB + s * L::kKC + a * C * 128, &mk, &full[s], a * 64, h / G, t0, b);
                     bw::tma_load_4d(sm + L::WB + s * L::kKC + a * C * 128, &mw, &full[s], a * 64, h, t0, b);
-                    bw::tma_load_4d(sm + L::QB + s * L::kKC + a * C * 128, &mq, &full[s], a * 64, h, t0, b);
+                    bw::tma_load_4d(sm + L::QB + s * L::kKC + a * C * 128, &mq, &full[s], a * 64, h / G, t0, b);
                 }
                 bw::tma_load_4d(sm + L::DB + s * L::kD, &mdo, &full[s], v0, h, t0, b);
                 bw::tma_load_4d(sm + L::PB + s * L::kP, &mp, &full[s], 0, 0, h, b * NT + c);
@@ -370,8 +370,8 @@ cudaError_t launch(const Dims& d, const void* q, const void* k, const void* w, c
     const uint64_t dims[4] = {(uint64_t)C, (uint64_t)C, (uint64_t)d.H, (uint64_t)d.B * d.NT};
     const uint64_t st[3] = {(uint64_t)C * 2, (uint64_t)C * C * 2, (uint64_t)d.H * C * C * 2};
     const uint32_t box[4] = {64, 64, 1, 1};
-    if (!make_tmap_tokens(&mk, k, d.B, d.T, d.H, K, C) || !make_tmap_tokens(&mw, w, d.B, d.T, d.H, K, C) ||
-        !make_tmap_tokens(&mq, q, d.B, d.T, d.H, K, C) || !make_tmap_tokens_sw64(&mdo, d_o, d.B, d.T, d.H, d.V, C) ||
+    if (!make_tmap_tokens(&mk, k, d.B, d.T, d.Hk, K, C) || !make_tmap_tokens(&mw, w, d.B, d.T, d.H, K, C) ||
+        !make_tmap_tokens(&mq, q, d.B, d.T, d.Hk, K, C) || !make_tmap_tokens_sw64(&mdo, d_o, d.B, d.T, d.H, d.V, C) ||
         !make_tmap_bf16_4d(&mp, P, dims, st, box))
         return cudaErrorInvalidValue;
     auto kern = bwd_scan_mma_kernel<K, C>;
@@ -380,7 +380,7 @@ cudaError_t launch(const Dims& d, const void* q, const void* k, const void* w, c
     if (e != cudaSuccess) return e;
     const dim3 grid(d.V / kBV, d.H, d.B);
     kern<<<grid, L::kThreads, smem, s>>>(mk, mw, mq, mdo, mp, g_cum, dh_final, (bf16*)dh_ckpt, (bf16*)dv_new, dh0,
-                                         d.T, d.H, d.V, d.scale, err);
+                                         d.T, d.H, d.V, d.G, d.scale, err);
     return cudaGetLastError();
 }
 

@@ -92,7 +92,7 @@ fused_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_co
                          const __grid_constant__ CUtensorMap mu, const __grid_constant__ CUtensorMap mq,
                          const __grid_constant__ CUtensorMap mpk, const float* __restrict__ g_cum,
                          const float* __restrict__ h0, bf16* __restrict__ o, float* __restrict__ h_final, int T,
-                         int H, int V, float scale, unsigned int* err) {
+                         int H, int V, int G, float scale, unsigned int* err) {
     using L = FLayout<K, C, HAS_P>;
     constexpr int NSA = L::NSA, NSB = L::NSB, NOW = L::NOW, NT8 = L::NT8, KH = L::KH;
     constexpr int NJH = KH / 8;
@@ -149,7 +149,7 @@ fused_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_co
 #pragma unroll
                 for (int a = 0; a < K / 64; ++a) {
                     bw::tma_load_4d(sm + L::W + s * L::kKC + a * C * 128, &mw, &fullA[s], a * 64, h, t0, b);
-                    bw::tma_load_4d(sm + L::KB + s * L::kKC + a * C * 128, &mk, &fullA[s], a * 64, h, t0, b);
+                    bw::tma_load_4d(sm + L::KB + s * L::kKC + a * C * 128, &mk, &fullA[s], a * 64, h / G, t0, b);
                 }
                 bw::tma_load_4d(sm + L::U + s * L::kU, &mu, &fullA[s], v0, h, t0, b);
                 sDec[s] = __expf(glc);
@@ -174,9 +174,9 @@ fused_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_co
                 bw::mbar_arrive_expect_tx(&fullB[s], L::tx_b);
 #pragma unroll
                 for (int a = 0; a < K / 64; ++a) {
-                    bw::tma_load_4d(sm + L::Q + s * L::kKC + a * C * 128, &mq, &fullB[s], a * 64, h, t0, b);
+                    bw::tma_load_4d(sm + L::Q + s * L::kKC + a * C * 128, &mq, &fullB[s], a * 64, h / G, t0, b);
                     if constexpr (!HAS_P)
-                        bw::tma_load_4d(sm + L::PK + s * L::kPK + a * C * 128, &mpk, &fullB[s], a * 64, h, t0, b);
+                        bw::tma_load_4d(sm + L::PK + s * L::kPK + a * C * 128, &mpk, &fullB[s], a * 64, h / G, t0, b);
                 }
                 if constexpr (HAS_P) bw::tma_load_4d(sm + L::PK + s * L::kPK, &mpk, &fullB[s], 0, 0, h, b * NT + c);
             }
@@ -466,8 +466,8 @@ cudaError_t launch(const Dims& d, const void* q, const void* k, const void* w, c
                    const void* P, const float* h0, void* o, float* h_final, cudaStream_t s, unsigned int* err) {
     using L = FLayout<K, C, HAS_P>;
     CUtensorMap mw, mk, mu, mq, mpk;
-    if (!make_tmap_tokens(&mw, w, d.B, d.T, d.H, K, C) || !make_tmap_tokens(&mk, k, d.B, d.T, d.H, K, C) ||
-        !make_tmap_tokens_sw64(&mu, u, d.B, d.T, d.H, d.V, C) || !make_tmap_tokens(&mq, q, d.B, d.T, d.H, K, C))
+    if (!make_tmap_tokens(&mw, w, d.B, d.T, d.H, K, C) || !make_tmap_tokens(&mk, k, d.B, d.T, d.Hk, K, C) ||
+        !make_tmap_tokens_sw64(&mu, u, d.B, d.T, d.H, d.V, C) || !make_tmap_tokens(&mq, q, d.B, d.T, d.Hk, K, C))
         return cudaErrorInvalidValue;
     if constexpr (HAS_P) {
         // P [B, NT, H, C, C] seen as (C, C, H, B*NT); one 64 x 64 box per chunk
@@ -483,8 +483,8 @@ cudaError_t launch(const Dims& d, const void* q, const void* k, const void* w, c
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const dim3 grid(d.V / kBV, d.H, d.B);
-    kern<<<grid, L::kThreads, smem, s>>>(mw, mk, mu, mq, mpk, g_cum, h0, (bf16*)o, h_final, d.T, d.H, d.V, d.scale,
-                                         err);
+    kern<<<grid, L::kThreads, smem, s>>>(mw, mk, mu, mq, mpk, g_cum, h0, (bf16*)o, h_final, d.T, d.H, d.V, d.G,
+                                         d.scale, err);
     return cudaGetLastError();
 }
 

@@ -27,14 +27,19 @@ gdr_status check_problem(const gdr_problem* p, gdr::Dims* d) {
     if (p->B <= 0 || p->T <= 0 || p->H <= 0 || p->K <= 0 || p->V <= 0 || p->chunk <= 0) return GDR_ERR_SHAPE;
     if ((p->K != 64 && p->K != 128) || (p->V != 64 && p->V != 128)) return GDR_ERR_SHAPE;
     if (p->chunk != 32 && p->chunk != 64) return GDR_ERR_SHAPE;
-    // grid and 32-bit dims limits: T, B*T*H fit int32; H and B*(V/32) fit a grid y/z extent
-    if (p->T > INT32_MAX || p->H > kMaxGridYZ || p->B * (p->V / 32) > kMaxGridYZ) return GDR_ERR_SHAPE;
-    if (p->B > INT32_MAX / p->T || p->B * p->T > INT32_MAX / p->H) return GDR_ERR_SHAPE;
+    // grouped value heads: HV value heads share the H q/k heads in groups of HV / H
+    const int64_t HV = p->HV > 0 ? p->HV : p->H;
+    if (p->HV < 0 || HV % p->H != 0) return GDR_ERR_SHAPE;
+    // grid and 32-bit dims limits: T, B*T*HV fit int32; HV and B*(V/32) fit a grid y/z extent
+    if (p->T > INT32_MAX || HV > kMaxGridYZ || p->B * (p->V / 32) > kMaxGridYZ) return GDR_ERR_SHAPE;
+    if (p->B > INT32_MAX / p->T || p->B * p->T > INT32_MAX / HV) return GDR_ERR_SHAPE;
     if (std::isnan(p->scale) || std::isinf(p->scale)) return GDR_ERR_ARG;
     if (p->variant < GDR_VARIANT_AUTO || p->variant > GDR_VARIANT_FUSED) return GDR_ERR_ARG;
     d->B = (int)p->B;
     d->T = (int)p->T;
-    d->H = (int)p->H;
+    d->H = (int)HV;
+    d->Hk = (int)p->H;
+    d->G = (int)(HV / p->H);
     d->K = (int)p->K;
     d->V = (int)p->V;
     d->C = (int)p->chunk;
@@ -138,7 +143,7 @@ StagedWorkspace plan_staged(const gdr::Dims& d, bool fused) {
 // gdr_backward scratch: the forward's g_cum, w, u, v_new, h_ckpt (io dtype), then the
 // backward's fp32 intermediates, each 256-byte aligned.
 struct BackwardWorkspace {
-    size_t g_cum, w, u, v_new, h_ckpt, dv_loc, dv_new, dh_ckpt, dk_part, dw, dG_part, P, tinv, total;
+    size_t g_cum, w, u, v_new, h_ckpt, dv_loc, dv_new, dh_ckpt, dk_part, dw, dG_part, P, tinv, dq_v, dk_v, total;
 };
 
 // The backward's paths: the CUDA-core stages after a re-scan on the CUDA cores (SIMT) or on
@@ -171,6 +176,10 @@ BackwardWorkspace plan_backward(const gdr::Dims& d, BwdPath path) {
         take(&ws.dk_part, rows * d.K * 4);
         take(&ws.dw, rows * d.K * 4);
         take(&ws.dG_part, rows * gw * 4);
+    }
+    if (d.G > 1) {   // per-value-head dq and dk, summed over each group at the end
+        take(&ws.dq_v, rows * d.K * e);
+        take(&ws.dk_v, rows * d.K * e);
     }
     ws.total = off;
     return ws;
@@ -411,6 +420,17 @@ gdr_status gdr_bwd_wy_dqkg(const gdr_problem* p, const void* q, const void* k, c
     return st;
 }
 
+gdr_status gdr_bwd_group_sum(const gdr_problem* p, const void* dq_v, const void* dk_v, void* dq, void* dk,
+                             void* stream) {
+    gdr::Dims d;
+    gdr_status st = check_problem(p, &d);
+    if (st != GDR_OK) return st;
+    if ((st = check_ptrs({dq_v, dk_v, dq, dk}, {})) != GDR_OK) return st;
+    st = from_cuda(gdr::group_sum_heads(d, dq_v, dk_v, dq, dk, (cudaStream_t)stream));
+    if (st == GDR_OK) t_last_variant = "simt";
+    return st;
+}
+
 size_t gdr_backward_workspace_bytes(const gdr_problem* p) {
     gdr::Dims d;
     if (check_problem(p, &d) != GDR_OK) return 0;
@@ -446,6 +466,13 @@ gdr_status gdr_backward(const gdr_problem* p, const void* q, const void* k, cons
     float* dw = reinterpret_cast<float*>(base + ws.dw);
     float* dG_part = reinterpret_cast<float*>(base + ws.dG_part);
     cudaStream_t s = (cudaStream_t)stream;
+    // grouped value heads: the stages write per-value-head dq and dk, summed over each group at the end
+    void* const dq_out = dq;
+    void* const dk_out = dk;
+    if (d.G > 1) {
+        dq = base + ws.dq_v;
+        dk = base + ws.dk_v;
+    }
     if (path == BwdPath::Fast) {
         // every step on the tensor cores: prepare (+ P and T), re-scan, reverse scan, per-chunk stage
         unsigned int* err = device_error_word();
@@ -459,6 +486,7 @@ gdr_status gdr_backward(const gdr_problem* p, const void* q, const void* k, cons
         if ((st = from_cuda(gdr::mma_bwd_chunk(d, q, k, v, beta, g_cum, w, u, tinv, v_new, h_ckpt, d_o, dv_new, dh_ckpt,
                                                dq, dk, dv, dbeta, dg, s))) != GDR_OK)
             return st;
+        if (d.G > 1 && (st = from_cuda(gdr::group_sum_heads(d, dq, dk, dq_out, dk_out, s))) != GDR_OK) return st;
         t_last_variant = "tensor";
         return GDR_OK;
     }
@@ -481,6 +509,7 @@ gdr_status gdr_backward(const gdr_problem* p, const void* q, const void* k, cons
     if ((st = from_cuda(gdr::simt_bwd_wy(d, k, v, beta, g_cum, dw, dv_new, dk_part, dG_part, dk, dv, dbeta, dg, s))) !=
         GDR_OK)
         return st;
+    if (d.G > 1 && (st = from_cuda(gdr::group_sum_heads(d, dq, dk, dq_out, dk_out, s))) != GDR_OK) return st;
     t_last_variant = tensor ? "tensor" : "simt";
     return GDR_OK;
 }

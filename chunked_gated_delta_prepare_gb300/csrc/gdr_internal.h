@@ -12,6 +12,7 @@ namespace gdr {
 // Validated problem sizes, as every launcher receives them.
 struct Dims {
     int B, T, H, K, V, C, NT;
+    int Hk, G;      // q/k heads and the group size H / Hk: value head h reads q and k of head h / G
     int per_k;      // 1: per-key-dim gate (g is [B,T,H,K]); 0: scalar gate
     int bf16;       // 1: io tensors are bf16; 0: fp32
     float scale;    // resolved output scale
@@ -56,6 +57,9 @@ cudaError_t simt_bwd_dqkwg(const Dims& d, const void* q, const void* k, const vo
 cudaError_t simt_bwd_wy(const Dims& d, const void* k, const void* v, const void* beta, const float* g_cum,
                         const float* dw, const float* du, const float* dk_part, const float* dG_part, void* dk,
                         void* dv, void* dbeta, float* dg, cudaStream_t s);
+
+// grouped value heads: dq, dk [B,T,Hk,K] = sums over each group of dq_v, dk_v [B,T,H,K] (io dtype)
+cudaError_t group_sum_heads(const Dims& d, const void* dq_v, const void* dk_v, void* dq, void* dk, cudaStream_t s);
 
 // ---- backward on the tensor cores (bf16 io, scalar gate, C = 64)
 // reverse scan: dv' = scale P^T do + (k gamma) dh, dh = e^(G_L) dh + scale (q e^G)^T do - w^T dv';

@@ -141,7 +141,7 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
                    const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap mu,
                    const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mp,
                    const float* __restrict__ g, const bf16* __restrict__ beta, float* __restrict__ g_cum,
-                   bf16* __restrict__ tinv, int T, int H, unsigned int* err) {
+                   bf16* __restrict__ tinv, int T, int H, int G, unsigned int* err) {
     using L = PrepLayout<K, V, C, PER_K, WITH_P>;
     constexpr int GW = L::GW;
     extern __shared__ unsigned char smem_raw[];
@@ -169,12 +169,12 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
     if (tid == 0) {
         bw::mbar_arrive_expect_tx(&bar_tma, (K + V + (WITH_P ? K : 0)) * 128);
 #pragma unroll
-        for (int a = 0; a < K / 64; ++a) bw::tma_load_4d(sm + L::kK + a * 8192, &mk, &bar_tma, a * 64, h, t0, b);
+        for (int a = 0; a < K / 64; ++a) bw::tma_load_4d(sm + L::kK + a * 8192, &mk, &bar_tma, a * 64, h / G, t0, b);
 #pragma unroll
         for (int a = 0; a < V / 64; ++a) bw::tma_load_4d(sm + L::kV + a * 8192, &mv, &bar_tma, a * 64, h, t0, b);
         if constexpr (WITH_P) {
 #pragma unroll
-            for (int a = 0; a < K / 64; ++a) bw::tma_load_4d(sm + L::kQ + a * 8192, &mq, &bar_tma, a * 64, h, t0, b);
+            for (int a = 0; a < K / 64; ++a) bw::tma_load_4d(sm + L::kQ + a * 8192, &mq, &bar_tma, a * 64, h / G, t0, b);
         }
     }
     // beta; g (rows past T read as zero)
@@ -575,7 +575,8 @@ cudaError_t launch_prepare(const Dims& d, const void* q, const void* k, const vo
                            unsigned int* err) {
     using L = PrepLayout<K, V, C, PER_K, WITH_P>;
     CUtensorMap mk, mv, mw, mu, mq, mp;
-    if (!make_tmap_tokens(&mk, k, d.B, d.T, d.H, K, kTile) || !make_tmap_tokens(&mv, v, d.B, d.T, d.H, V, kTile) ||
+    // q and k have the Hk q/k heads; every other token tensor the H value heads
+    if (!make_tmap_tokens(&mk, k, d.B, d.T, d.Hk, K, kTile) || !make_tmap_tokens(&mv, v, d.B, d.T, d.H, V, kTile) ||
         !make_tmap_tokens(&mw, w, d.B, d.T, d.H, K, kTile) || !make_tmap_tokens(&mu, u, d.B, d.T, d.H, V, kTile))
         return cudaErrorInvalidValue;
     mq = mk;
@@ -585,7 +586,7 @@ cudaError_t launch_prepare(const Dims& d, const void* q, const void* k, const vo
         const uint64_t dims[4] = {(uint64_t)C, (uint64_t)C, (uint64_t)d.H, (uint64_t)d.B * d.NT};
         const uint64_t st[3] = {(uint64_t)C * 2, (uint64_t)C * C * 2, (uint64_t)d.H * C * C * 2};
         const uint32_t box[4] = {64, 64, 1, 1};
-        if (!make_tmap_tokens(&mq, q, d.B, d.T, d.H, K, kTile) || !make_tmap_bf16_4d(&mp, P, dims, st, box))
+        if (!make_tmap_tokens(&mq, q, d.B, d.T, d.Hk, K, kTile) || !make_tmap_bf16_4d(&mp, P, dims, st, box))
             return cudaErrorInvalidValue;
     }
     auto kern = prepare_mma_kernel<K, V, C, PER_K, WITH_P>;
@@ -593,7 +594,8 @@ cudaError_t launch_prepare(const Dims& d, const void* q, const void* k, const vo
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const dim3 grid((d.T + kTile - 1) / kTile, d.H, d.B);
-    kern<<<grid, 128, smem, s>>>(mk, mv, mw, mu, mq, mp, g, (const bf16*)beta, g_cum, (bf16*)tinv, d.T, d.H, err);
+    kern<<<grid, 128, smem, s>>>(mk, mv, mw, mu, mq, mp, g, (const bf16*)beta, g_cum, (bf16*)tinv, d.T, d.H, d.G,
+                                 err);
     return cudaGetLastError();
 }
 

@@ -77,7 +77,7 @@ __global__ void __launch_bounds__(MScanLayout<K, C, PER_K>::kThreads, 1)
 scan_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap mk,
                 const __grid_constant__ CUtensorMap mu, const bf16* __restrict__ k, const float* __restrict__ g_cum,
                 const float* __restrict__ h0, bf16* __restrict__ h_ckpt, bf16* __restrict__ v_new,
-                float* __restrict__ h_final, int T, int H, int V, unsigned int* err) {
+                float* __restrict__ h_final, int T, int H, int V, int G, unsigned int* err) {
     using L = MScanLayout<K, C, PER_K>;
     constexpr int GW = L::GW, KH = L::KH, NT8 = L::NT8;
     constexpr int NJH = KH / 8;    // n-tiles of this warp's part of h^T
@@ -91,6 +91,7 @@ scan_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ 
     const uint32_t s_base = bw::smem_u32(sm);
     auto row = [&](int t) -> int64_t { return ((int64_t)b * T + t) * H + h; };
     auto rowc = [&](int t) -> int64_t { return row(min(t, T - 1)); };   // G past T repeats its last value
+    auto krow = [&](int t) -> int64_t { return ((int64_t)b * T + t) * (H / G) + h / G; };   // k: q/k head h / G
 
     if (tid == 0) {
         for (int s = 0; s < L::NS; ++s) {
@@ -129,7 +130,7 @@ scan_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ 
 #pragma unroll
                     for (int a = 0; a < K / 64; ++a) {
                         bw::tma_load_4d(sm + L::W + s * L::kKC + a * C * 128, &mw, &full[s], a * 64, h, t0, b);
-                        bw::tma_load_4d(sm + L::KB + s * L::kKC + a * C * 128, &mk, &full[s], a * 64, h, t0, b);
+                        bw::tma_load_4d(sm + L::KB + s * L::kKC + a * C * 128, &mk, &full[s], a * 64, h / G, t0, b);
                     }
                     bw::tma_load_4d(sm + L::U + s * L::kU, &mu, &full[s], v0, h, t0, b);
                     sDec[s] = __expf(glc);
@@ -155,7 +156,7 @@ scan_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ 
 #pragma unroll
                 for (int j = 0; j < NI; ++j) {
                     const int t = r0 + j * RSTEP;
-                    st.kr[j] = t0 + t < T ? *reinterpret_cast<const uint4*>(k + row(t0 + t) * K + lc * 8)
+                    st.kr[j] = t0 + t < T ? *reinterpret_cast<const uint4*>(k + krow(t0 + t) * K + lc * 8)
                                           : make_uint4(0u, 0u, 0u, 0u);
                     const float4* gt = reinterpret_cast<const float4*>(g_cum + rowc(t0 + t) * K + lc * 8);
                     *reinterpret_cast<float4*>(&st.gr[j][0]) = gt[0];
@@ -398,7 +399,7 @@ cudaError_t launch(const Dims& d, const void* k, const void* w, const void* u, c
                    void* h_ckpt, void* v_new, float* h_final, cudaStream_t s, unsigned int* err) {
     using L = MScanLayout<K, C, PER_K>;
     CUtensorMap mw, mk, mu;
-    if (!make_tmap_tokens(&mw, w, d.B, d.T, d.H, K, C) || !make_tmap_tokens(&mk, k, d.B, d.T, d.H, K, C) ||
+    if (!make_tmap_tokens(&mw, w, d.B, d.T, d.H, K, C) || !make_tmap_tokens(&mk, k, d.B, d.T, d.Hk, K, C) ||
         !make_tmap_tokens_sw64(&mu, u, d.B, d.T, d.H, d.V, C))
         return cudaErrorInvalidValue;
     auto kern = scan_mma_kernel<K, C, PER_K>;
@@ -407,7 +408,7 @@ cudaError_t launch(const Dims& d, const void* k, const void* w, const void* u, c
     if (e != cudaSuccess) return e;
     const dim3 grid(d.V / kBV, d.H, d.B);
     kern<<<grid, L::kThreads, smem, s>>>(mw, mk, mu, (const bf16*)k, g_cum, h0, (bf16*)h_ckpt, (bf16*)v_new,
-                                         h_final, d.T, d.H, d.V, err);
+                                         h_final, d.T, d.H, d.V, d.G, err);
     return cudaGetLastError();
 }
 

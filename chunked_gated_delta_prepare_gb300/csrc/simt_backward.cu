@@ -33,6 +33,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include "gdr_internal.h"
 
 namespace gdr {
@@ -70,11 +72,12 @@ bwd_dv_local_kernel(Dims d, const IO* __restrict__ q, const IO* __restrict__ k, 
     const int64_t tok0 = (int64_t)b * d.T + (int64_t)c * C;
     const int nv = min(C, d.T - c * C);
     auto row = [&](int t) { return (tok0 + t) * H + h; };
+    auto krow = [&](int t) { return (tok0 + t) * d.Hk + h / d.G; };   // q, k: q/k head h / G
 
     for (int i = tid; i < C * K; i += kThreads) {
         const bool in = i / K < nv;
-        qs[(i / K) * KP + i % K] = in ? ld(q, row(i / K) * K + i % K) : 0.f;
-        ks[(i / K) * KP + i % K] = in ? ld(k, row(i / K) * K + i % K) : 0.f;
+        qs[(i / K) * KP + i % K] = in ? ld(q, krow(i / K) * K + i % K) : 0.f;
+        ks[(i / K) * KP + i % K] = in ? ld(k, krow(i / K) * K + i % K) : 0.f;
     }
     for (int i = tid; i < C * GW; i += kThreads) Gs[i] = g_cum[row(min(i / GW, nv - 1)) * GW + i % GW];
     for (int i = tid; i < C * VT; i += kThreads)
@@ -137,6 +140,7 @@ bwd_scan_dh_kernel(Dims d, const IO* __restrict__ q, const IO* __restrict__ k, c
         const int64_t tok0 = (int64_t)b * d.T + (int64_t)c * C;
         const int nv = min(C, d.T - c * C);
         auto row = [&](int t) { return (tok0 + t) * H + h; };
+        auto krow = [&](int t) { return (tok0 + t) * d.Hk + h / d.G; };   // q, k: q/k head h / G
         for (int i = tid; i < GW; i += kThreads) Gl[i] = g_cum[row(nv - 1) * GW + i];
         __syncthreads();
         const int64_t ck = (((int64_t)b * d.NT + c) * H + h) * K * V;
@@ -146,9 +150,9 @@ bwd_scan_dh_kernel(Dims d, const IO* __restrict__ q, const IO* __restrict__ k, c
             const int gi = PER_K ? e : 0;
             const bool in = t < nv;
             const float G = in ? g_cum[row(t) * GW + gi] : 0.f;
-            qgs[t * KP + e] = in ? ld(q, row(t) * K + e) * expf(G) : 0.f;
+            qgs[t * KP + e] = in ? ld(q, krow(t) * K + e) * expf(G) : 0.f;
             ws[t * KP + e] = in ? ld(w, row(t) * K + e) : 0.f;
-            kgs[t * KP + e] = in ? ld(k, row(t) * K + e) * expf(Gl[gi] - G) : 0.f;
+            kgs[t * KP + e] = in ? ld(k, krow(t) * K + e) * expf(Gl[gi] - G) : 0.f;
         }
         for (int i = tid; i < C * BV; i += kThreads) {
             const int t = i / BV, j = i % BV;
@@ -212,6 +216,7 @@ bwd_dqkwg_kernel(Dims d, const IO* __restrict__ q, const IO* __restrict__ k, con
     const int64_t tok0 = (int64_t)b * d.T + (int64_t)c * C;
     const int nv = min(C, d.T - c * C);
     auto row = [&](int t) { return (tok0 + t) * H + h; };
+    auto krow = [&](int t) { return (tok0 + t) * d.Hk + h / d.G; };   // q, k: q/k head h / G
     const int64_t ck = (((int64_t)b * d.NT + c) * H + h) * K * V;
 
     for (int i = tid; i < C * V; i += kThreads) {
@@ -240,8 +245,8 @@ bwd_dqkwg_kernel(Dims d, const IO* __restrict__ q, const IO* __restrict__ k, con
         for (int i = tid; i < C * KT; i += kThreads) {
             const int t = i / KT, e = i % KT;
             const bool in = t < nv;
-            qt[t * KTP + e] = in ? ld(q, row(t) * K + e0 + e) : 0.f;
-            kt[t * KTP + e] = in ? ld(k, row(t) * K + e0 + e) : 0.f;
+            qt[t * KTP + e] = in ? ld(q, krow(t) * K + e0 + e) : 0.f;
+            kt[t * KTP + e] = in ? ld(k, krow(t) * K + e0 + e) : 0.f;
             Gt[t * KTP + e] = g_cum[row(min(t, nv - 1)) * GW + (PER_K ? e0 + e : 0)];
         }
         __syncthreads();
@@ -327,8 +332,9 @@ bwd_wy_kernel(Dims d, const IO* __restrict__ k, const IO* __restrict__ v, const 
     const int64_t tok0 = (int64_t)b * d.T + (int64_t)c * C;
     const int nv = min(C, d.T - c * C);
     auto row = [&](int t) { return (tok0 + t) * H + h; };
+    auto krow = [&](int t) { return (tok0 + t) * d.Hk + h / d.G; };   // q, k: q/k head h / G
 
-    for (int i = tid; i < C * K; i += kThreads) ks[(i / K) * KP + i % K] = i / K < nv ? ld(k, row(i / K) * K + i % K) : 0.f;
+    for (int i = tid; i < C * K; i += kThreads) ks[(i / K) * KP + i % K] = i / K < nv ? ld(k, krow(i / K) * K + i % K) : 0.f;
     for (int i = tid; i < C * GW; i += kThreads) Gs[i] = g_cum[row(min(i / GW, nv - 1)) * GW + i % GW];
     for (int i = tid; i < C; i += kThreads) {
         bs[i] = i < nv ? ld(beta, row(i)) : 0.f;
@@ -489,6 +495,21 @@ bwd_wy_kernel(Dims d, const IO* __restrict__ k, const IO* __restrict__ v, const 
     }
 }
 
+// ------------------------------------------------------------------ group sum
+// Grouped value heads: dq and dk of a q/k head are the sums over its group of the
+// per-value-head gradients.  in [B,T,Hk*G,K] -> out [B,T,Hk,K], summed in fp32.
+template <typename IO>
+__global__ void __launch_bounds__(kThreads)
+group_sum_kernel(const IO* __restrict__ in, IO* __restrict__ out, int64_t rows_out, int G, int K) {
+    const int64_t n = rows_out * K;
+    for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < n; i += (int64_t)gridDim.x * kThreads) {
+        const int64_t r = i / K, x = i % K;
+        float s = 0.f;
+        for (int gi = 0; gi < G; ++gi) s += ld(in, (r * G + gi) * K + x);
+        st(out, i, s);
+    }
+}
+
 template <typename Kern>
 cudaError_t allow_smem(Kern kern, size_t smem) {
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -580,6 +601,25 @@ cudaError_t simt_bwd_wy(const Dims& d, const void* k, const void* v, const void*
     } while (0)
     GDR_DISPATCH(LAUNCH);
 #undef LAUNCH
+    return cudaGetLastError();
+}
+
+}  // namespace gdr
+
+namespace gdr {
+
+cudaError_t group_sum_heads(const Dims& d, const void* dq_v, const void* dk_v, void* dq, void* dk, cudaStream_t s) {
+    const int64_t rows_out = (int64_t)d.B * d.T * d.Hk;
+    const int blocks = (int)std::min<int64_t>((rows_out * d.K + kThreads - 1) / kThreads, 152 * 16);
+    if (d.bf16) {
+        group_sum_kernel<__nv_bfloat16><<<blocks, kThreads, 0, s>>>((const __nv_bfloat16*)dq_v, (__nv_bfloat16*)dq,
+                                                                   rows_out, d.G, d.K);
+        group_sum_kernel<__nv_bfloat16><<<blocks, kThreads, 0, s>>>((const __nv_bfloat16*)dk_v, (__nv_bfloat16*)dk,
+                                                                   rows_out, d.G, d.K);
+    } else {
+        group_sum_kernel<float><<<blocks, kThreads, 0, s>>>((const float*)dq_v, (float*)dq, rows_out, d.G, d.K);
+        group_sum_kernel<float><<<blocks, kThreads, 0, s>>>((const float*)dk_v, (float*)dk, rows_out, d.G, d.K);
+    }
     return cudaGetLastError();
 }
 

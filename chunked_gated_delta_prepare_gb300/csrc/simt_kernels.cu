@@ -55,12 +55,13 @@ simt_prepare_kernel(Dims d, const IO* __restrict__ k, const IO* __restrict__ v, 
     const int tid = threadIdx.x;
     const int64_t tok0 = (int64_t)b * d.T + (int64_t)c * C;   // first token of this chunk
     const int nv = min(C, d.T - c * C);                       // tokens of the chunk before T
-    auto row = [&](int t) { return (tok0 + t) * H + h; };    // (token, head) row index
+    auto row = [&](int t) { return (tok0 + t) * H + h; };                 // (token, value head) row index
+    auto krow = [&](int t) { return (tok0 + t) * d.Hk + h / d.G; };   // q, k: q/k head h / G
 
     // tokens past T (a last, partial chunk) read as g = 0, beta = 0, k = v = 0
     for (int i = tid; i < C * GW; i += kThreads) Gs[i] = i / GW < nv ? g[row(i / GW) * GW + i % GW] : 0.f;
     for (int i = tid; i < C; i += kThreads) bs[i] = i < nv ? ld(beta, row(i)) : 0.f;
-    for (int i = tid; i < C * K; i += kThreads) ks[(i / K) * KP + i % K] = i / K < nv ? ld(k, row(i / K) * K + i % K) : 0.f;
+    for (int i = tid; i < C * K; i += kThreads) ks[(i / K) * KP + i % K] = i / K < nv ? ld(k, krow(i / K) * K + i % K) : 0.f;
     __syncthreads();
     // chunk-local inclusive cumsum, one thread per gate column
     for (int col = tid; col < GW; col += kThreads) {
@@ -163,6 +164,7 @@ simt_scan_kernel(Dims d, const IO* __restrict__ k, const IO* __restrict__ w, con
         const int64_t tok0 = (int64_t)b * d.T + (int64_t)c * C;
         const int nv = min(C, d.T - c * C);   // a last, partial chunk: zero w, k, u past T, G held at its last value
         auto row = [&](int t) { return (tok0 + t) * H + h; };
+        auto krow = [&](int t) { return (tok0 + t) * d.Hk + h / d.G; };   // q, k: q/k head h / G
         for (int i = tid; i < GW; i += kThreads) Gl[i] = g_cum[row(nv - 1) * GW + i];
         __syncthreads();
         if (h_ckpt) {
@@ -174,7 +176,7 @@ simt_scan_kernel(Dims d, const IO* __restrict__ k, const IO* __restrict__ w, con
             const int t = i / K, e = i % K;
             const int gi = PER_K ? e : 0;
             ws[t * KP + e] = t < nv ? ld(w, row(t) * K + e) : 0.f;
-            kgs[t * KP + e] = t < nv ? ld(k, row(t) * K + e) * expf(Gl[gi] - g_cum[row(t) * GW + gi]) : 0.f;
+            kgs[t * KP + e] = t < nv ? ld(k, krow(t) * K + e) * expf(Gl[gi] - g_cum[row(t) * GW + gi]) : 0.f;
         }
         for (int i = tid; i < C * BV; i += kThreads)
             us[(i / BV) * BVP + i % BV] = i / BV < nv ? ld(u, row(i / BV) * V + v0 + i % BV) : 0.f;
@@ -228,13 +230,14 @@ simt_output_kernel(Dims d, const IO* __restrict__ q, const IO* __restrict__ k, c
     const int tid = threadIdx.x;
     const int64_t tok0 = (int64_t)b * d.T + (int64_t)c * C;
     auto row = [&](int t) { return (tok0 + t) * H + h; };
+    auto krow = [&](int t) { return (tok0 + t) * d.Hk + h / d.G; };   // q, k: q/k head h / G
     const int64_t ck = (((int64_t)b * d.NT + c) * H + h) * K * V;
     const int nv = min(C, d.T - c * C);   // a last, partial chunk: zero q, k, v' past T, G held at its last value
 
     for (int i = tid; i < C * K; i += kThreads) {
         const bool in = i / K < nv;
-        qs[(i / K) * KP + i % K] = in ? ld(q, row(i / K) * K + i % K) : 0.f;
-        ks[(i / K) * KP + i % K] = in ? ld(k, row(i / K) * K + i % K) : 0.f;
+        qs[(i / K) * KP + i % K] = in ? ld(q, krow(i / K) * K + i % K) : 0.f;
+        ks[(i / K) * KP + i % K] = in ? ld(k, krow(i / K) * K + i % K) : 0.f;
     }
     for (int i = tid; i < C * GW; i += kThreads) Gs[i] = g_cum[row(min(i / GW, nv - 1)) * GW + i % GW];
     for (int i = tid; i < C * VT; i += kThreads)

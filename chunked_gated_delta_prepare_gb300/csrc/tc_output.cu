@@ -54,7 +54,7 @@ __global__ void __launch_bounds__(128, 1)
 tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                  const __grid_constant__ CUtensorMap mvp, const __grid_constant__ CUtensorMap mh,
                  const float* __restrict__ g_cum, const bf16* __restrict__ k_raw, bf16* __restrict__ o, int T,
-                 int H, int NT, float scale, unsigned int* err) {
+                 int H, int NT, int G, float scale, unsigned int* err) {
     using L = OutLayout<K, V, C, PER_K>;
     constexpr int GW = L::GW;
     extern __shared__ unsigned char smem_raw[];
@@ -68,6 +68,7 @@ tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
     const int t0 = blockIdx.x * kTile, h = blockIdx.y, b = blockIdx.z;
     const int nvalid = min(kTile, T - t0);
     auto row = [&](int t) -> int64_t { return ((int64_t)b * T + t0 + t) * H + h; };
+    auto krow = [&](int t) -> int64_t { return ((int64_t)b * T + t0 + t) * (H / G) + h / G; };   // q/k head h / G
     // per-key-dim gate: 8 consecutive G values of tile row t from global memory; past T the last
     // row's (q and k are zero there, and a bounded gap keeps the exp range check quiet)
     auto g8 = [&](int t, int d0, float* out) {
@@ -97,8 +98,8 @@ tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         bw::mbar_arrive_expect_tx(&bar_tma, 2 * K * 128 + V * 128 + nch * K * V * 2);
 #pragma unroll
         for (int a = 0; a < K / 64; ++a) {
-            bw::tma_load_4d(sm + L::Q + a * 8192, &mq, &bar_tma, a * 64, h, t0, b);
-            bw::tma_load_4d(sm + L::Kt + a * 8192, &mk, &bar_tma, a * 64, h, t0, b);
+            bw::tma_load_4d(sm + L::Q + a * 8192, &mq, &bar_tma, a * 64, h / G, t0, b);
+            bw::tma_load_4d(sm + L::Kt + a * 8192, &mk, &bar_tma, a * 64, h / G, t0, b);
         }
 #pragma unroll
         for (int a = 0; a < V / 64; ++a) bw::tma_load_4d(sm + L::VP + a * 8192, &mvp, &bar_tma, a * 64, h, t0, b);
@@ -205,7 +206,7 @@ tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
                 for (int d = 0; d < K; ++d) {
                     const float qi = __bfloat162float(*reinterpret_cast<const bf16*>(sm + L::Q + tile_off(i, d)));
                     // k's tile now holds its gated copy: raw k and G come from global memory (rare path)
-                    const float kj = j < nvalid ? __bfloat162float(k_raw[row(j) * K + d]) : 0.f;
+                    const float kj = j < nvalid ? __bfloat162float(k_raw[krow(j) * K + d]) : 0.f;
                     const float gi = i < nvalid ? g_cum[row(i) * K + d] : 0.f;
                     const float gj = j < nvalid ? g_cum[row(j) * K + d] : 0.f;
                     acc += qi * kj * __expf(gi - gj);
@@ -289,7 +290,7 @@ cudaError_t launch_output(const Dims& d, const void* q, const void* k, const voi
                           const float* g_cum, void* o, cudaStream_t s, unsigned int* err) {
     using L = OutLayout<K, V, C, PER_K>;
     CUtensorMap mq, mk, mvp, mh;
-    if (!make_tmap_tokens(&mq, q, d.B, d.T, d.H, K, kTile) || !make_tmap_tokens(&mk, k, d.B, d.T, d.H, K, kTile) ||
+    if (!make_tmap_tokens(&mq, q, d.B, d.T, d.Hk, K, kTile) || !make_tmap_tokens(&mk, k, d.B, d.T, d.Hk, K, kTile) ||
         !make_tmap_tokens(&mvp, v_new, d.B, d.T, d.H, V, kTile) || !make_tmap_ckpt(&mh, h_ckpt, d.B, d.NT, d.H, K, V))
         return cudaErrorInvalidValue;
     auto kern = tc_output_kernel<K, V, C, PER_K>;
@@ -297,7 +298,8 @@ cudaError_t launch_output(const Dims& d, const void* q, const void* k, const voi
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const dim3 grid((d.T + kTile - 1) / kTile, d.H, d.B);
-    kern<<<grid, 128, smem, s>>>(mq, mk, mvp, mh, g_cum, (const bf16*)k, (bf16*)o, d.T, d.H, d.NT, d.scale, err);
+    kern<<<grid, 128, smem, s>>>(mq, mk, mvp, mh, g_cum, (const bf16*)k, (bf16*)o, d.T, d.H, d.NT, d.G, d.scale,
+                                 err);
     return cudaGetLastError();
 }
 

@@ -35,6 +35,7 @@ EXPORTS = ["gdr_prepare_wy", "gdr_scan_h", "gdr_chunk_output", "gdr_forward", "g
            "gdr_forward_static_scratch", "gdr_scan_output", "gdr_prepare_wyp",
            "gdr_bwd_dv_local", "gdr_bwd_scan_dh", "gdr_bwd_dqkwg", "gdr_bwd_wy", "gdr_backward",
            "gdr_backward_workspace_bytes", "gdr_bwd_prepare", "gdr_bwd_scan_dh_p", "gdr_bwd_wy_dqkg",
+           "gdr_bwd_group_sum",
            "gdr_status_string", "gdr_get_device_status", "gdr_last_variant", "gdr_version"]
 
 
@@ -47,7 +48,8 @@ class GdrError(RuntimeError):
 class gdr_problem(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int64), ("T", ctypes.c_int64), ("H", ctypes.c_int64), ("K", ctypes.c_int64),
                 ("V", ctypes.c_int64), ("chunk", ctypes.c_int64), ("io_dtype", ctypes.c_int32),
-                ("gate", ctypes.c_int32), ("scale", ctypes.c_float), ("variant", ctypes.c_int32)]
+                ("gate", ctypes.c_int32), ("scale", ctypes.c_float), ("variant", ctypes.c_int32),
+                ("HV", ctypes.c_int64)]
 
 
 _lib = None
@@ -84,6 +86,7 @@ def load(path: str | None = None):
             "gdr_bwd_prepare": [P] + [vp] * 11,
             "gdr_bwd_scan_dh_p": [P] + [vp] * 11,
             "gdr_bwd_wy_dqkg": [P] + [vp] * 19,
+            "gdr_bwd_group_sum": [P] + [vp] * 5,
             "gdr_status_string": [ctypes.c_int],
             "gdr_get_device_status": [vp],
             "gdr_last_variant": [],
@@ -131,17 +134,19 @@ def _check(status: int, where: str):
 
 
 def make_problem(B, T, H, K, V, chunk, io_dtype=torch.bfloat16, per_k_gate=False, scale=None,
-                 variant="auto") -> gdr_problem:
+                 variant="auto", HV=0) -> gdr_problem:
+    """H: q/k heads; HV: value heads (a multiple of H; 0 means H)."""
     dt = DTYPES[io_dtype] if isinstance(io_dtype, torch.dtype) else int(io_dtype)
     return gdr_problem(B=B, T=T, H=H, K=K, V=V, chunk=chunk, io_dtype=dt, gate=1 if per_k_gate else 0,
                        scale=-1.0 if scale is None else float(scale),
-                       variant=VARIANTS[variant] if isinstance(variant, str) else int(variant))
+                       variant=VARIANTS[variant] if isinstance(variant, str) else int(variant), HV=HV)
 
 
 def problem_for(q, v, g, chunk, scale=None, variant="auto") -> gdr_problem:
+    """The problem of tensors q [B,T,H,K], v [B,T,HV,V] and g; HV > H means grouped value heads."""
     B, T, H, K = q.shape
-    V = v.shape[-1]
-    return make_problem(B, T, H, K, V, chunk, q.dtype, g.dim() == 4, scale, variant)
+    HV, V = v.shape[2], v.shape[-1]
+    return make_problem(B, T, H, K, V, chunk, q.dtype, g.dim() == 4, scale, variant, HV=HV if HV != H else 0)
 
 
 # ---------------------------------------------------------------- raw entry points
@@ -223,8 +228,8 @@ def forward(q, k, v, g, beta, h0=None, *, chunk=64, scale=None, variant="auto", 
         q, k, v, g, beta = (t.to(dev, non_blocking=True) for t in (q, k, v, g, beta))
         h0 = h0.to(dev, non_blocking=True) if h0 is not None else None
     p = problem_for(q, v, g, chunk, scale, variant)
-    B, T, H, K = q.shape
-    V = v.shape[-1]
+    B, T, _, K = q.shape
+    H, V = v.shape[2], v.shape[-1]            # value heads
     o = torch.empty(B, T, H, V, device=q.device, dtype=q.dtype)
     hf = torch.empty(B, H, K, V, device=q.device, dtype=torch.float32) if want_h_final else None
     nbytes = gdr_forward_workspace_bytes(p)
@@ -282,6 +287,11 @@ def gdr_bwd_wy_dqkg(p, q, k, v, beta, g_cum, w, u, tinv, v_new, h_ckpt, d_o, dv_
                                   _stream(stream)), "gdr_bwd_wy_dqkg")
 
 
+def gdr_bwd_group_sum(p, dq_v, dk_v, dq, dk, stream=None):
+    _check(load().gdr_bwd_group_sum(ctypes.byref(p), _ptr(dq_v), _ptr(dk_v), _ptr(dq), _ptr(dk), _stream(stream)),
+           "gdr_bwd_group_sum")
+
+
 def gdr_backward_workspace_bytes(p) -> int:
     return int(load().gdr_backward_workspace_bytes(ctypes.byref(p)))
 
@@ -298,8 +308,8 @@ def backward(q, k, v, g, beta, h0, d_o, dh_final=None, *, chunk=64, scale=None, 
     """dq, dk, dv, dg, dbeta, dh0 = backward(q, k, v, g, beta, h0, do, dh_final): the gradient of
     forward's (o, h_final) against do and dh_final, on device tensors."""
     p = problem_for(q, v, g, chunk, scale, variant)
-    B, T, H, K = q.shape
-    V = v.shape[-1]
+    B, T, _, K = q.shape
+    H, V = v.shape[2], v.shape[-1]            # value heads
     dq, dk = torch.empty_like(q), torch.empty_like(k)
     dv = torch.empty_like(v)
     dg = torch.empty_like(g)

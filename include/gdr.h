@@ -27,10 +27,14 @@
  *   as void*; NULL is the legacy default stream) and returns as soon as the
  *   launches are queued.
  * - Layouts are contiguous, head dim last ("head-last", as the re-scan page's
- *   host wrapper takes them): q, k, w [B,T,H,K]; v, u, v_new, o [B,T,H,V];
- *   g, g_cum [B,T,H] (scalar gate) or [B,T,H,K] (per-key-dim gate), always fp32;
- *   beta [B,T,H]; h0, h_final [B,H,K,V] fp32; h_ckpt [B,NT,H,K,V] with
- *   NT = ceil(T/C).
+ *   host wrapper takes them): q, k [B,T,H,K]; w [B,T,HV,K]; v, u, v_new, o
+ *   [B,T,HV,V]; g, g_cum [B,T,HV] (scalar gate) or [B,T,HV,K] (per-key-dim
+ *   gate), always fp32; beta [B,T,HV]; h0, h_final [B,HV,K,V] fp32; h_ckpt
+ *   [B,NT,HV,K,V] with NT = ceil(T/C).  Every per-head tensor below that is not
+ *   q or k is indexed by the value head.
+ * - Grouped value heads: HV = G H value heads share the H q/k heads, value
+ *   head hv reading the q and k of head hv / G (the scan page indexes its
+ *   tensors by value head this way).  HV = H (or 0) is the ungrouped case.
  * - "io" tensors (q, k, v, beta, w, u, v_new, o, h_ckpt) have the problem's
  *   io_dtype: fp32 or bf16.  g, g_cum, h0 and h_final are always fp32.
  * - g is the natural-log per-token decay (<= 0 for a decaying state); the
@@ -106,6 +110,7 @@ typedef struct gdr_problem {
     int32_t gate;       /* gdr_gate */
     float scale;        /* output scale; <= 0 selects 1/sqrt(K) */
     int32_t variant;    /* gdr_variant */
+    int64_t HV;         /* value heads, a multiple of H; 0 means HV = H (see below) */
 } gdr_problem;
 
 /*
@@ -324,6 +329,14 @@ GDR_API gdr_status gdr_bwd_wy_dqkg(const gdr_problem* p, const void* q, const vo
                                    const void* tinv, const void* v_new, const void* h_ckpt, const void* d_o,
                                    const void* dv_new, const void* dh_ckpt, void* dq, void* dk, void* dv,
                                    void* dbeta, float* dg, void* stream);
+
+/* Grouped value heads (HV > H): the stage entry points above (gdr_bwd_dqkwg's dq, gdr_bwd_wy's
+ * dk, gdr_bwd_wy_dqkg's dq and dk) write these per value head, [B,T,HV,K] in the io dtype; the
+ * gradient of a shared q/k head is the sum over its group, which this call forms:
+ * dq [B,T,H,K] = sum over g < HV/H of dq_v[:, :, h*(HV/H) + g], and the same for dk.
+ * gdr_backward does this itself. */
+GDR_API gdr_status gdr_bwd_group_sum(const gdr_problem* p, const void* dq_v, const void* dk_v, void* dq, void* dk,
+                                     void* stream);
 
 /* Bytes of device workspace gdr_backward needs (0 for a problem it would reject). */
 GDR_API size_t gdr_backward_workspace_bytes(const gdr_problem* p);

@@ -57,8 +57,8 @@ def gpu_forward(x, C, variant="auto", scale=None, want_h_final=True, h0="inputs"
     q, k, v, g, beta = (dev(t) for t in (x.q, x.k, x.v, x.g, x.beta))
     h0d = dev(x.h0) if h0 == "inputs" else dev(h0)
     p = gdr.problem_for(q, v, g, C, scale, variant)
-    B, T, H, K = q.shape
-    V = v.shape[-1]
+    B, T, _, K = q.shape
+    H, V = v.shape[2], v.shape[-1]            # value heads
     o = torch.full((B, T, H, V), float("nan"), device="cuda", dtype=q.dtype)
     hf = torch.full((B, H, K, V), float("nan"), device="cuda", dtype=torch.float32) if want_h_final else None
     nbytes = gdr.gdr_forward_workspace_bytes(p)
@@ -70,13 +70,19 @@ def gpu_forward(x, C, variant="auto", scale=None, want_h_final=True, h0="inputs"
 
 
 def sample_heads(x, pairs):
-    """Slice the inputs down to the given (b, h) pairs, as a batch of single-head problems."""
+    """Slice the inputs down to the given (b, h) pairs of value heads, as a batch of single-head
+    problems (with grouped value heads, value head h reads the q and k of head h // G)."""
+    G = x.v.shape[2] // x.q.shape[2]
+
     def tokens(t):   # [B,T,H,...] -> [P,T,1,...]
         return torch.stack([t[b, :, h] for b, h in pairs]).unsqueeze(2)
 
+    def qk(t):
+        return torch.stack([t[b, :, h // G] for b, h in pairs]).unsqueeze(2)
+
     def state(t):    # [B,H,K,V] -> [P,1,K,V]
         return None if t is None else torch.stack([t[b, h] for b, h in pairs]).unsqueeze(1)
-    return dict(q=tokens(x.q), k=tokens(x.k), v=tokens(x.v), g=tokens(x.g), beta=tokens(x.beta),
+    return dict(q=qk(x.q), k=qk(x.k), v=tokens(x.v), g=tokens(x.g), beta=tokens(x.beta),
                 h0=state(x.h0))
 
 
@@ -104,3 +110,11 @@ def check_forward(x, o, hf, pairs, C, scale, io):
 
 def all_pairs(B, H):
     return [(b, h) for b in range(B) for h in range(H)]
+
+
+def grouped_inputs(B, T, H, G, K, V, *, per_k_gate=False, io_dtype=torch.bfloat16, with_h0=True, seed=0):
+    """Inputs with H q/k heads shared by H * G value heads (grouped value heads)."""
+    from chunked_gated_delta_prepare_gb300.inputs import GdrInputs, make_inputs
+    x = make_inputs(B, T, H * G, K, V, per_k_gate=per_k_gate, io_dtype=io_dtype, with_h0=with_h0, seed=seed)
+    return GdrInputs(q=x.q[:, :, ::G].contiguous(), k=x.k[:, :, ::G].contiguous(), v=x.v, g=x.g, beta=x.beta,
+                     h0=x.h0)

@@ -21,7 +21,7 @@ import oracle
 from oracle import chunked, chunked_backward as cb
 from chunked_gated_delta_prepare_gb300 import gdr, workloads
 from chunked_gated_delta_prepare_gb300.inputs import GdrInputs, make_inputs, make_workload_inputs
-from gpu_helpers import STAGE_TOL, all_pairs, dev, gather_heads, io_name, sample_heads, scaled_err
+from gpu_helpers import STAGE_TOL, all_pairs, dev, gather_heads, grouped_inputs, io_name, sample_heads, scaled_err
 
 pytestmark = pytest.mark.gpu
 
@@ -36,7 +36,7 @@ VARIANTS = {"simt": (torch.float32, torch.bfloat16), "tensor": (torch.bfloat16,)
 def upstream(x, seed):
     """do (io dtype) and dh_final (fp32) for the inputs x, seeded."""
     gen = torch.Generator().manual_seed(seed)
-    B, T, H, _ = x.q.shape
+    B, T, H = x.v.shape[:3]
     K, V = x.k.shape[-1], x.v.shape[-1]
     do = torch.randn(B, T, H, V, generator=gen).to(x.q.dtype)
     dhf = torch.randn(B, H, K, V, generator=gen)
@@ -46,8 +46,8 @@ def upstream(x, seed):
 def gpu_backward(x, do, dhf, C, variant, scale=None, want_dh0=True):
     q, k, v, g, beta, h0, d_o = (dev(t) for t in (x.q, x.k, x.v, x.g, x.beta, x.h0, do))
     p = gdr.problem_for(q, v, g, C, scale, variant)
-    B, T, H, K = q.shape
-    V = v.shape[-1]
+    B, T, _, K = q.shape
+    H, V = v.shape[2], v.shape[-1]            # value heads
     nan = float("nan")
     outs = dict(dq=torch.full_like(q, nan), dk=torch.full_like(k, nan), dv=torch.full_like(v, nan),
                 dg=torch.full_like(g, nan), dbeta=torch.full_like(beta, nan),
@@ -365,3 +365,23 @@ def test_tensor_stage_wy_dqkg(shape):
     assert scaled_err(dv, y["dv"]) <= tol
     assert scaled_err(dbeta, y["dbeta"]) <= tol
     assert scaled_err(dg, cb.reverse_cumsum(a["dG"] + y["dG"], C, False)) <= tol
+
+
+# ---------------------------------------------------------------- grouped value heads
+
+GROUPED = [(1, 128, 2, 2, 64, 64, 64), (2, 100, 1, 2, 128, 128, 64), (1, 96, 1, 3, 64, 128, 32)]
+
+
+@pytest.mark.parametrize("shape", GROUPED, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("variant,dtype,per_k", [("simt", torch.float32, False), ("simt", torch.float32, True),
+                                                  ("tensor", torch.bfloat16, False), ("tensor", torch.bfloat16, True)])
+def test_grouped_value_heads_backward(shape, variant, dtype, per_k):
+    B, T, H, G, K, V, C = shape
+    x = grouped_inputs(B, T, H, G, K, V, per_k_gate=per_k, io_dtype=dtype, seed=80)
+    do, dhf = upstream(x, 81)
+    got, ran = gpu_backward(x, do, dhf, C, variant)
+    assert ran == variant and got["dq"].shape == x.q.shape
+    ref = reference(x, do, dhf, C, 1.0 / np.sqrt(K))
+    for name in GRADS:
+        err = scaled_err(got[name], ref[name])
+        assert np.isfinite(err) and err <= BWD_TOL[io_name(dtype)], f"{name}: {err:.3e}"

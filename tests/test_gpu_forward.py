@@ -9,7 +9,8 @@ import torch
 import oracle
 from chunked_gated_delta_prepare_gb300 import gdr, workloads
 from chunked_gated_delta_prepare_gb300.inputs import GdrInputs, make_inputs, make_workload_inputs
-from gpu_helpers import (H_TOL, O_TOL, all_pairs, check_forward, gpu_forward, io_name, max_abs, rel_frob)
+from gpu_helpers import (H_TOL, O_TOL, all_pairs, check_forward, gpu_forward, grouped_inputs, io_name, max_abs,
+                         rel_frob)
 
 pytestmark = pytest.mark.gpu
 
@@ -204,3 +205,20 @@ def test_invalid_shape_launches_nothing():
     with pytest.raises(gdr.GdrError) as e:
         gpu_forward(x, 64, "auto")
     assert e.value.status == 2
+
+
+# ---------------------------------------------------------------- grouped value heads
+
+GROUPED = [(2, 128, 2, 2, 64, 64, 64), (1, 100, 1, 4, 128, 128, 64), (1, 96, 2, 2, 128, 64, 32)]
+
+
+@pytest.mark.parametrize("shape", GROUPED, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("variant,dtype,per_k", [(v, d, pk) for v, ds in FORWARD_VARIANTS.items() for d in ds
+                                                  for pk in GATES[v]])
+def test_grouped_value_heads_forward(shape, variant, dtype, per_k):
+    # H q/k heads shared by H * G value heads: every value head against the oracle
+    B, T, H, G, K, V, C = shape
+    x = grouped_inputs(B, T, H, G, K, V, per_k_gate=per_k, io_dtype=dtype, seed=82)
+    o, hf, ran = gpu_forward(x, C, variant)
+    assert ran == variant and o.shape == (B, T, H * G, V)
+    check_forward(x, o, hf, all_pairs(B, H * G), C, 1.0 / np.sqrt(K), io_name(dtype))

@@ -22,7 +22,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // Checks the descriptor and fills Dims.  Does not look at pointers.
 gdr_status check_problem(const gdr_problem* p, gdr::Dims* d) {
     if (!p) return GDR_ERR_NULL;
-    if (p->io_dtype != GDR_F32 && p->io_dtype != GDR_BF16) return GDR_ERR_DTYPE;
+    if (p->io_dtype != GDR_F32 && p->io_dtype != GDR_BF16 && p->io_dtype != GDR_F16) return GDR_ERR_DTYPE;
     if (p->gate != GDR_GATE_SCALAR && p->gate != GDR_GATE_PER_K) return GDR_ERR_DTYPE;
     if (p->B <= 0 || p->T <= 0 || p->H <= 0 || p->K <= 0 || p->V <= 0 || p->chunk <= 0) return GDR_ERR_SHAPE;
     if ((p->K != 64 && p->K != 128) || (p->V != 64 && p->V != 128)) return GDR_ERR_SHAPE;
@@ -46,6 +46,7 @@ gdr_status check_problem(const gdr_problem* p, gdr::Dims* d) {
     d->NT = (d->T + d->C - 1) / d->C;   // a last, partial chunk counts
     d->per_k = p->gate == GDR_GATE_PER_K;
     d->bf16 = p->io_dtype == GDR_BF16;
+    d->f16 = p->io_dtype == GDR_F16;   // runs the CUDA-core kernels only
     d->scale = p->scale > 0.f ? p->scale : 1.0f / std::sqrt((float)p->K);
     return GDR_OK;
 }
@@ -119,7 +120,7 @@ struct StagedWorkspace {
 };
 
 StagedWorkspace plan_staged(const gdr::Dims& d, bool fused) {
-    const size_t e = d.bf16 ? 2 : 4;
+    const size_t e = (d.bf16 || d.f16) ? 2 : 4;
     const size_t rows = (size_t)d.B * d.T * d.H;
     StagedWorkspace ws;
     size_t off = 0;
@@ -151,7 +152,7 @@ struct BackwardWorkspace {
 enum class BwdPath { Simt, Tensor, Fast };
 
 BackwardWorkspace plan_backward(const gdr::Dims& d, BwdPath path) {
-    const size_t e = d.bf16 ? 2 : 4;
+    const size_t e = (d.bf16 || d.f16) ? 2 : 4;
     const size_t rows = (size_t)d.B * d.T * d.H;
     const size_t gw = d.per_k ? d.K : 1;
     const size_t states = (size_t)d.B * d.NT * d.H * d.K * d.V;

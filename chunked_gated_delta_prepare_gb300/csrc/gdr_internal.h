@@ -14,7 +14,8 @@ struct Dims {
     int B, T, H, K, V, C, NT;
     int Hk, G;      // q/k heads and the group size H / Hk: value head h reads q and k of head h / G
     int per_k;      // 1: per-key-dim gate (g is [B,T,H,K]); 0: scalar gate
-    int bf16;       // 1: io tensors are bf16; 0: fp32
+    int bf16;       // 1: io tensors are bf16 (the tensor-core kernels take these)
+    int f16;        // 1: io tensors are fp16 (CUDA-core kernels only); bf16 = f16 = 0: fp32
     float scale;    // resolved output scale
 };
 

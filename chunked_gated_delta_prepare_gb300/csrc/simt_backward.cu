@@ -31,6 +31,7 @@
 // are fp32; q, k, v, beta, do, w, v' and h in the problem's io dtype; gradients
 // of the io tensors in the io dtype, dg and dh0 in fp32.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -47,6 +48,8 @@ __device__ __forceinline__ float ld(const float* p, int64_t i) { return p[i]; }
 __device__ __forceinline__ float ld(const __nv_bfloat16* p, int64_t i) { return __bfloat162float(p[i]); }
 __device__ __forceinline__ void st(float* p, int64_t i, float x) { p[i] = x; }
 __device__ __forceinline__ void st(__nv_bfloat16* p, int64_t i, float x) { p[i] = __float2bfloat16_rn(x); }
+__device__ __forceinline__ float ld(const __half* p, int64_t i) { return __half2float(p[i]); }
+__device__ __forceinline__ void st(__half* p, int64_t i, float x) { p[i] = __float2half_rn(x); }
 
 // ------------------------------------------------------------------ dv_local
 // One CTA per (chunk, head, batch * value tile of 64).  Shared (fp32):
@@ -519,6 +522,8 @@ cudaError_t allow_smem(Kern kern, size_t smem) {
     do {                                                                                      \
         if (d.bf16) {                                                                         \
             if (d.per_k) LAUNCH(__nv_bfloat16, true); else LAUNCH(__nv_bfloat16, false);      \
+        } else if (d.f16) {                                                                   \
+            if (d.per_k) LAUNCH(__half, true); else LAUNCH(__half, false);                    \
         } else {                                                                              \
             if (d.per_k) LAUNCH(float, true); else LAUNCH(float, false);                      \
         }                                                                                     \
@@ -616,6 +621,9 @@ cudaError_t group_sum_heads(const Dims& d, const void* dq_v, const void* dk_v, v
                                                                    rows_out, d.G, d.K);
         group_sum_kernel<__nv_bfloat16><<<blocks, kThreads, 0, s>>>((const __nv_bfloat16*)dk_v, (__nv_bfloat16*)dk,
                                                                    rows_out, d.G, d.K);
+    } else if (d.f16) {
+        group_sum_kernel<__half><<<blocks, kThreads, 0, s>>>((const __half*)dq_v, (__half*)dq, rows_out, d.G, d.K);
+        group_sum_kernel<__half><<<blocks, kThreads, 0, s>>>((const __half*)dk_v, (__half*)dk, rows_out, d.G, d.K);
     } else {
         group_sum_kernel<float><<<blocks, kThreads, 0, s>>>((const float*)dq_v, (float*)dq, rows_out, d.G, d.K);
         group_sum_kernel<float><<<blocks, kThreads, 0, s>>>((const float*)dk_v, (float*)dk, rows_out, d.G, d.K);

@@ -14,6 +14,7 @@
 //       ckpt[c] = h;  v' = u - w h;  h = exp(G_last) * h + (k * exp(G_last - G))^T v'
 //   output: o = scale [ (q * exp(G)) ckpt[c] + tril_0(Q~) v' ],  Q~_ij = sum_d q_id k_jd exp(G_id - G_jd)
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "gdr_internal.h"
@@ -27,6 +28,8 @@ __device__ __forceinline__ float ld(const float* p, int64_t i) { return p[i]; }
 __device__ __forceinline__ float ld(const __nv_bfloat16* p, int64_t i) { return __bfloat162float(p[i]); }
 __device__ __forceinline__ void st(float* p, int64_t i, float x) { p[i] = x; }
 __device__ __forceinline__ void st(__nv_bfloat16* p, int64_t i, float x) { p[i] = __float2bfloat16_rn(x); }
+__device__ __forceinline__ float ld(const __half* p, int64_t i) { return __half2float(p[i]); }
+__device__ __forceinline__ void st(__half* p, int64_t i, float x) { p[i] = __float2half_rn(x); }
 
 // ------------------------------------------------------------------ prepare
 // One CTA per (chunk, head, batch).  Shared memory (fp32):
@@ -299,6 +302,8 @@ cudaError_t simt_prepare(const Dims& d, const void* k, const void* v, const floa
     } while (0)
     if (d.bf16) {
         if (d.per_k) GDR_LAUNCH_PREP(__nv_bfloat16, true); else GDR_LAUNCH_PREP(__nv_bfloat16, false);
+    } else if (d.f16) {
+        if (d.per_k) GDR_LAUNCH_PREP(__half, true); else GDR_LAUNCH_PREP(__half, false);
     } else {
         if (d.per_k) GDR_LAUNCH_PREP(float, true); else GDR_LAUNCH_PREP(float, false);
     }
@@ -322,6 +327,8 @@ cudaError_t simt_scan(const Dims& d, const void* k, const void* w, const void* u
     } while (0)
     if (d.bf16) {
         if (d.per_k) GDR_LAUNCH_SCAN(__nv_bfloat16, true); else GDR_LAUNCH_SCAN(__nv_bfloat16, false);
+    } else if (d.f16) {
+        if (d.per_k) GDR_LAUNCH_SCAN(__half, true); else GDR_LAUNCH_SCAN(__half, false);
     } else {
         if (d.per_k) GDR_LAUNCH_SCAN(float, true); else GDR_LAUNCH_SCAN(float, false);
     }
@@ -346,6 +353,8 @@ cudaError_t simt_output(const Dims& d, const void* q, const void* k, const void*
     } while (0)
     if (d.bf16) {
         if (d.per_k) GDR_LAUNCH_OUT(__nv_bfloat16, true); else GDR_LAUNCH_OUT(__nv_bfloat16, false);
+    } else if (d.f16) {
+        if (d.per_k) GDR_LAUNCH_OUT(__half, true); else GDR_LAUNCH_OUT(__half, false);
     } else {
         if (d.per_k) GDR_LAUNCH_OUT(float, true); else GDR_LAUNCH_OUT(float, false);
     }

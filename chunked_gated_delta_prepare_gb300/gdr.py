@@ -29,7 +29,7 @@ GDR_OK = 0
 STATUS_NAMES = {0: "GDR_OK", 1: "GDR_ERR_NULL", 2: "GDR_ERR_SHAPE", 3: "GDR_ERR_DTYPE", 4: "GDR_ERR_ALIGN",
                 5: "GDR_ERR_WORKSPACE", 6: "GDR_ERR_CUDA", 7: "GDR_ERR_DEVICE_TIMEOUT",
                 8: "GDR_ERR_UNSUPPORTED", 9: "GDR_ERR_ARG"}
-DTYPES = {torch.float32: 0, torch.bfloat16: 1}
+DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
 VARIANTS = {"auto": 0, "simt": 1, "tensor": 2, "fused": 3}
 EXPORTS = ["gdr_prepare_wy", "gdr_scan_h", "gdr_chunk_output", "gdr_forward", "gdr_forward_workspace_bytes",
            "gdr_forward_static_scratch", "gdr_scan_output", "gdr_prepare_wyp",

@@ -36,7 +36,7 @@
  *   head hv reading the q and k of head hv / G (the scan page indexes its
  *   tensors by value head this way).  HV = H (or 0) is the ungrouped case.
  * - "io" tensors (q, k, v, beta, w, u, v_new, o, h_ckpt) have the problem's
- *   io_dtype: fp32 or bf16.  g, g_cum, h0 and h_final are always fp32.
+ *   io_dtype: fp32, bf16 or fp16.  g, g_cum, h0 and h_final are always fp32.
  * - g is the natural-log per-token decay (<= 0 for a decaying state); the
  *   library takes its chunk-local inclusive cumsum itself.
  * - Argument errors are detected before anything is launched and returned as a
@@ -85,7 +85,8 @@ typedef enum gdr_status {
     GDR_ERR_ARG = 9              /* another invalid argument (e.g. a NaN scale) */
 } gdr_status;
 
-typedef enum gdr_dtype { GDR_F32 = 0, GDR_BF16 = 1 } gdr_dtype;
+/* fp16 io runs the CUDA-core kernels (variant AUTO or SIMT); the tensor-core kernels take bf16. */
+typedef enum gdr_dtype { GDR_F32 = 0, GDR_BF16 = 1, GDR_F16 = 2 } gdr_dtype;
 
 typedef enum gdr_gate {
     GDR_GATE_SCALAR = 0,  /* GDN: g [B,T,H] */

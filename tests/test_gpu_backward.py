@@ -25,7 +25,7 @@ from gpu_helpers import STAGE_TOL, all_pairs, dev, gather_heads, grouped_inputs,
 
 pytestmark = pytest.mark.gpu
 
-BWD_TOL = {"bf16": 2e-2, "f32": 1e-4}
+BWD_TOL = {"bf16": 2e-2, "f16": 2e-2, "f32": 1e-4}
 GRADS = ("dq", "dk", "dv", "dg", "dbeta", "dh0")
 # (B, T, H, K, V, C): several chunks, both chunk sizes, K != V, and partial last chunks
 SHAPES = [(2, 256, 3, 64, 64, 64), (1, 192, 2, 128, 128, 64), (2, 128, 3, 64, 128, 32),
@@ -385,3 +385,17 @@ def test_grouped_value_heads_backward(shape, variant, dtype, per_k):
     for name in GRADS:
         err = scaled_err(got[name], ref[name])
         assert np.isfinite(err) and err <= BWD_TOL[io_name(dtype)], f"{name}: {err:.3e}"
+
+
+@pytest.mark.parametrize("shape", SHAPES[:5], ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("per_k", [False, True])
+def test_fp16_io_backward(shape, per_k):
+    B, T, H, K, V, C = shape
+    x = make_inputs(B, T, H, K, V, per_k_gate=per_k, io_dtype=torch.float16, with_h0=True, seed=92)
+    do, dhf = upstream(x, 93)
+    got, ran = gpu_backward(x, do, dhf, C, "auto")
+    assert ran == "simt" and got["dq"].dtype == torch.float16
+    ref = reference(x, do, dhf, C, 1.0 / np.sqrt(K))
+    for name in GRADS:
+        err = scaled_err(got[name], ref[name])
+        assert np.isfinite(err) and err <= BWD_TOL["f16"], f"{name}: {err:.3e}"

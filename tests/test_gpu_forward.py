@@ -222,3 +222,25 @@ def test_grouped_value_heads_forward(shape, variant, dtype, per_k):
     o, hf, ran = gpu_forward(x, C, variant)
     assert ran == variant and o.shape == (B, T, H * G, V)
     check_forward(x, o, hf, all_pairs(B, H * G), C, 1.0 / np.sqrt(K), io_name(dtype))
+
+
+# ---------------------------------------------------------------- fp16 io
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("per_k", [False, True])
+@pytest.mark.parametrize("variant", ["auto", "simt"])
+def test_fp16_io_forward(shape, per_k, variant):
+    # fp16 runs the CUDA-core kernels (the AUTO choice for it)
+    B, T, H, K, V, C = shape
+    x = make_inputs(B, T, H, K, V, per_k_gate=per_k, io_dtype=torch.float16, with_h0=True, seed=90)
+    o, hf, ran = gpu_forward(x, C, variant)
+    assert ran == "simt" and o.dtype == torch.float16
+    check_forward(x, o, hf, all_pairs(B, H), C, 1.0 / np.sqrt(K), "f16")
+
+
+@pytest.mark.parametrize("variant", ["tensor", "fused"])
+def test_fp16_io_refused_by_the_tensor_core_variants(variant):
+    x = make_inputs(1, 64, 1, 64, 64, io_dtype=torch.float16, seed=91)
+    with pytest.raises(gdr.GdrError) as e:
+        gpu_forward(x, 64, variant)
+    assert e.value.status == 8

@@ -135,7 +135,9 @@ __device__ __forceinline__ void mma_block_split(float (&acc)[2][4], const uint32
 constexpr float kExpClamp = 60.f;
 constexpr float kExpSafe = 40.f;
 
-template <int K, int V, int C, bool PER_K, bool WITH_P>
+// EXTRA: grouped value heads (q/k head h / G) or the backward's T output.  The plain forward takes
+// the variant without either (its schedule measured slower with them compiled in).
+template <int K, int V, int C, bool PER_K, bool WITH_P, bool EXTRA>
 __global__ void __launch_bounds__(128, 3)
 prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
                    const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap mu,
@@ -155,6 +157,7 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int t0 = blockIdx.x * kTile, h = blockIdx.y, b = blockIdx.z;
+    const int hk = EXTRA ? h / G : h;                 // q/k head of value head h
     const int nvalid = min(kTile, T - t0);
     auto row = [&](int t) -> int64_t { return ((int64_t)b * T + t0 + t) * H + h; };
     const uint32_t s_base = bw::smem_u32(sm);
@@ -169,12 +172,12 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
     if (tid == 0) {
         bw::mbar_arrive_expect_tx(&bar_tma, (K + V + (WITH_P ? K : 0)) * 128);
 #pragma unroll
-        for (int a = 0; a < K / 64; ++a) bw::tma_load_4d(sm + L::kK + a * 8192, &mk, &bar_tma, a * 64, h / G, t0, b);
+        for (int a = 0; a < K / 64; ++a) bw::tma_load_4d(sm + L::kK + a * 8192, &mk, &bar_tma, a * 64, hk, t0, b);
 #pragma unroll
         for (int a = 0; a < V / 64; ++a) bw::tma_load_4d(sm + L::kV + a * 8192, &mv, &bar_tma, a * 64, h, t0, b);
         if constexpr (WITH_P) {
 #pragma unroll
-            for (int a = 0; a < K / 64; ++a) bw::tma_load_4d(sm + L::kQ + a * 8192, &mq, &bar_tma, a * 64, h / G, t0, b);
+            for (int a = 0; a < K / 64; ++a) bw::tma_load_4d(sm + L::kQ + a * 8192, &mq, &bar_tma, a * 64, hk, t0, b);
         }
     }
     // beta; g (rows past T read as zero)
@@ -473,7 +476,7 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
     }
 
     // X itself, for the backward's WY stage: [B, NT, H, C, C] bf16, this warp's 16 rows of its chunk
-    if (tinv && t0 + (I / NB) * C < T) {
+    if (EXTRA && tinv && t0 + (I / NB) * C < T) {
         const int ci = t0 / C + I / NB;
         bf16* dst = tinv + (((int64_t)b * ((T + C - 1) / C) + ci) * H + h) * C * C;
         const int r0 = 16 * (I - J0) + g4;
@@ -569,10 +572,10 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
     }
 }
 
-template <int K, int V, int C, bool PER_K, bool WITH_P>
-cudaError_t launch_prepare(const Dims& d, const void* q, const void* k, const void* v, const float* g,
-                           const void* beta, void* w, void* u, float* g_cum, void* P, void* tinv, cudaStream_t s,
-                           unsigned int* err) {
+template <int K, int V, int C, bool PER_K, bool WITH_P, bool EXTRA>
+cudaError_t launch_prepare_v(const Dims& d, const void* q, const void* k, const void* v, const float* g,
+                             const void* beta, void* w, void* u, float* g_cum, void* P, void* tinv, cudaStream_t s,
+                             unsigned int* err) {
     using L = PrepLayout<K, V, C, PER_K, WITH_P>;
     CUtensorMap mk, mv, mw, mu, mq, mp;
     // q and k have the Hk q/k heads; every other token tensor the H value heads
@@ -589,7 +592,7 @@ cudaError_t launch_prepare(const Dims& d, const void* q, const void* k, const vo
         if (!make_tmap_tokens(&mq, q, d.B, d.T, d.Hk, K, kTile) || !make_tmap_bf16_4d(&mp, P, dims, st, box))
             return cudaErrorInvalidValue;
     }
-    auto kern = prepare_mma_kernel<K, V, C, PER_K, WITH_P>;
+    auto kern = prepare_mma_kernel<K, V, C, PER_K, WITH_P, EXTRA>;
     const size_t smem = L::bytes + 1024;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -597,6 +600,15 @@ cudaError_t launch_prepare(const Dims& d, const void* q, const void* k, const vo
     kern<<<grid, 128, smem, s>>>(mk, mv, mw, mu, mq, mp, g, (const bf16*)beta, g_cum, (bf16*)tinv, d.T, d.H, d.G,
                                  err);
     return cudaGetLastError();
+}
+
+template <int K, int V, int C, bool PER_K, bool WITH_P>
+cudaError_t launch_prepare(const Dims& d, const void* q, const void* k, const void* v, const float* g,
+                           const void* beta, void* w, void* u, float* g_cum, void* P, void* tinv, cudaStream_t s,
+                           unsigned int* err) {
+    if (d.G != 1 || tinv)
+        return launch_prepare_v<K, V, C, PER_K, WITH_P, true>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err);
+    return launch_prepare_v<K, V, C, PER_K, WITH_P, false>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err);
 }
 
 template <int K, int V, int C>

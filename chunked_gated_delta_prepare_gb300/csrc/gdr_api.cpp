@@ -170,6 +170,13 @@ BackwardWorkspace plan_backward(const gdr::Dims& d, BwdPath path) {
         take(&ws.dh_ckpt, states * 2);
         take(&ws.P, tiles * 2);
         take(&ws.tinv, tiles * 2);
+    } else if (path == BwdPath::Tensor) {   // bf16 dv_loc, v' and state gradients; fp32 per-chunk partials
+        take(&ws.dv_loc, rows * d.V * 2);
+        take(&ws.dv_new, rows * d.V * 2);
+        take(&ws.dh_ckpt, states * 2);
+        take(&ws.dk_part, rows * d.K * 4);
+        take(&ws.dw, rows * d.K * 4);
+        take(&ws.dG_part, rows * gw * 4);
     } else {
         take(&ws.dv_loc, rows * d.V * 4);
         take(&ws.dv_new, rows * d.V * 4);
@@ -350,30 +357,59 @@ gdr_status gdr_bwd_scan_dh(const gdr_problem* p, const void* q, const void* k, c
 }
 
 gdr_status gdr_bwd_dqkwg(const gdr_problem* p, const void* q, const void* k, const void* v_new, const float* g_cum,
-                         const void* h_ckpt, const float* dh_ckpt, const void* d_o, const float* dv_new, void* dq,
+                         const void* h_ckpt, const void* dh_ckpt, const void* d_o, const void* dv_new, void* dq,
                          float* dk_part, float* dw, float* dG_part, void* stream) {
     gdr::Dims d;
     gdr_status st = check_problem(p, &d);
     if (st != GDR_OK) return st;
     if ((st = check_ptrs({q, k, v_new, g_cum, h_ckpt, dh_ckpt, d_o, dv_new, dq, dk_part, dw, dG_part}, {})) != GDR_OK)
         return st;
+    // the tensor path's intermediates (bf16 io, variants other than SIMT) are bf16
+    const bool inter16 = d.bf16 && p->variant != GDR_VARIANT_SIMT;
     st = from_cuda(gdr::simt_bwd_dqkwg(d, q, k, v_new, g_cum, h_ckpt, dh_ckpt, d_o, dv_new, dq, dk_part, dw,
-                                       dG_part, (cudaStream_t)stream));
+                                       dG_part, (cudaStream_t)stream, inter16));
     if (st == GDR_OK) t_last_variant = "simt";
     return st;
 }
 
 gdr_status gdr_bwd_wy(const gdr_problem* p, const void* k, const void* v, const void* beta, const float* g_cum,
-                      const float* dw, const float* dv_new, const float* dk_part, const float* dG_part, void* dk,
+                      const float* dw, const void* dv_new, const float* dk_part, const float* dG_part, void* dk,
                       void* dv, void* dbeta, float* dg, void* stream) {
     gdr::Dims d;
     gdr_status st = check_problem(p, &d);
     if (st != GDR_OK) return st;
     if ((st = check_ptrs({k, v, beta, g_cum, dw, dv_new, dk_part, dG_part, dk, dv, dbeta, dg}, {})) != GDR_OK)
         return st;
+    const bool inter16 = d.bf16 && p->variant != GDR_VARIANT_SIMT;
     st = from_cuda(gdr::simt_bwd_wy(d, k, v, beta, g_cum, dw, dv_new, dk_part, dG_part, dk, dv, dbeta, dg,
-                                    (cudaStream_t)stream));
+                                    (cudaStream_t)stream, inter16));
     if (st == GDR_OK) t_last_variant = "simt";
+    return st;
+}
+
+gdr_status gdr_bwd_dv_local_tc(const gdr_problem* p, const void* q, const void* k, const float* g_cum,
+                               const void* d_o, void* dv_loc, void* stream) {
+    gdr::Dims d;
+    gdr_status st = check_problem(p, &d);
+    if (st != GDR_OK) return st;
+    if ((st = check_ptrs({q, k, g_cum, d_o, dv_loc}, {})) != GDR_OK) return st;
+    if (p->variant == GDR_VARIANT_SIMT || !d.bf16) return GDR_ERR_UNSUPPORTED;
+    st = from_cuda(gdr::mma_bwd_dv_local(d, q, k, g_cum, d_o, dv_loc, (cudaStream_t)stream));
+    if (st == GDR_OK) t_last_variant = "tensor";
+    return st;
+}
+
+gdr_status gdr_bwd_scan_dh_tc(const gdr_problem* p, const void* q, const void* k, const void* w, const float* g_cum,
+                              const void* dv_loc, const void* d_o, const float* dh_final, void* dh_ckpt,
+                              void* dv_new, float* dh0, void* stream) {
+    gdr::Dims d;
+    gdr_status st = check_problem(p, &d);
+    if (st != GDR_OK) return st;
+    if ((st = check_ptrs({q, k, w, g_cum, dv_loc, d_o, dh_ckpt, dv_new}, {dh_final, dh0})) != GDR_OK) return st;
+    if (p->variant == GDR_VARIANT_SIMT || !d.bf16) return GDR_ERR_UNSUPPORTED;
+    st = from_cuda(gdr::mma_bwd_scan_dl(d, q, k, w, g_cum, dv_loc, d_o, dh_final, dh_ckpt, dv_new, dh0,
+                                        (cudaStream_t)stream, device_error_word()));
+    if (st == GDR_OK) t_last_variant = "tensor";
     return st;
 }
 
@@ -496,6 +532,20 @@ gdr_status gdr_backward(const gdr_problem* p, const void* q, const void* k, cons
         unsigned int* err = device_error_word();
         if ((st = from_cuda(gdr::mma_prepare(d, k, v, g, beta, w, u, g_cum, s, err))) != GDR_OK) return st;
         if ((st = from_cuda(gdr::mma_scan(d, k, w, u, g_cum, h0, h_ckpt, v_new, nullptr, s, err))) != GDR_OK) return st;
+        // the local term and the reverse scan on the tensor cores; the per-chunk stages on the CUDA cores
+        if ((st = from_cuda(gdr::mma_bwd_dv_local(d, q, k, g_cum, d_o, dv_loc, s))) != GDR_OK) return st;
+        if ((st = from_cuda(gdr::mma_bwd_scan_dl(d, q, k, w, g_cum, dv_loc, d_o, dh_final, dh_ckpt, dv_new, dh0, s,
+                                                 err))) != GDR_OK)
+            return st;
+        if ((st = from_cuda(gdr::simt_bwd_dqkwg(d, q, k, v_new, g_cum, h_ckpt, dh_ckpt, d_o, dv_new, dq, dk_part, dw,
+                                                dG_part, s, true))) != GDR_OK)
+            return st;
+        if ((st = from_cuda(gdr::simt_bwd_wy(d, k, v, beta, g_cum, dw, dv_new, dk_part, dG_part, dk, dv, dbeta, dg, s,
+                                             true))) != GDR_OK)
+            return st;
+        if (d.G > 1 && (st = from_cuda(gdr::group_sum_heads(d, dq, dk, dq_out, dk_out, s))) != GDR_OK) return st;
+        t_last_variant = "tensor";
+        return GDR_OK;
     } else {
         if ((st = from_cuda(gdr::simt_prepare(d, k, v, g, beta, w, u, g_cum, s))) != GDR_OK) return st;
         if ((st = from_cuda(gdr::simt_scan(d, k, w, u, g_cum, h0, h_ckpt, v_new, nullptr, s))) != GDR_OK) return st;

@@ -52,12 +52,13 @@ cudaError_t simt_bwd_dv_local(const Dims& d, const void* q, const void* k, const
 cudaError_t simt_bwd_scan_dh(const Dims& d, const void* q, const void* k, const void* w, const float* g_cum,
                              const void* d_o, const float* dv_loc, const float* dh_final, float* dh_ckpt,
                              float* dv_new, float* dh0, cudaStream_t s);
+// inter16: dh_ckpt and dv_new (du) are in the io dtype (from the tensor-core reverse scan), else fp32
 cudaError_t simt_bwd_dqkwg(const Dims& d, const void* q, const void* k, const void* v_new, const float* g_cum,
-                           const void* h_ckpt, const float* dh_ckpt, const void* d_o, const float* dv_new,
-                           void* dq, float* dk_part, float* dw, float* dG_part, cudaStream_t s);
+                           const void* h_ckpt, const void* dh_ckpt, const void* d_o, const void* dv_new,
+                           void* dq, float* dk_part, float* dw, float* dG_part, cudaStream_t s, bool inter16 = false);
 cudaError_t simt_bwd_wy(const Dims& d, const void* k, const void* v, const void* beta, const float* g_cum,
-                        const float* dw, const float* du, const float* dk_part, const float* dG_part, void* dk,
-                        void* dv, void* dbeta, float* dg, cudaStream_t s);
+                        const float* dw, const void* du, const float* dk_part, const float* dG_part, void* dk,
+                        void* dv, void* dbeta, float* dg, cudaStream_t s, bool inter16 = false);
 
 // grouped value heads: dq, dk [B,T,Hk,K] = sums over each group of dq_v, dk_v [B,T,H,K] (io dtype)
 cudaError_t group_sum_heads(const Dims& d, const void* dq_v, const void* dk_v, void* dq, void* dk, cudaStream_t s);
@@ -68,6 +69,14 @@ cudaError_t group_sum_heads(const Dims& d, const void* dq_v, const void* dk_v, v
 cudaError_t mma_bwd_scan(const Dims& d, const void* q, const void* k, const void* w, const float* g_cum, const void* P,
                          const void* d_o, const float* dh_final, void* dh_ckpt, void* dv_new, float* dh0,
                          cudaStream_t s, unsigned int* err);
+// the reverse scan with the local term precomputed: dv' = dv_loc + kg dh; dv_loc [B,T,H,V] bf16;
+// either gate, C = 32 or 64 (bwd_scan_mma.cu)
+cudaError_t mma_bwd_scan_dl(const Dims& d, const void* q, const void* k, const void* w, const float* g_cum,
+                            const void* dv_loc, const void* d_o, const float* dh_final, void* dh_ckpt, void* dv_new,
+                            float* dh0, cudaStream_t s, unsigned int* err);
+// dv_loc = scale tril_0(Q~)^T do per chunk, bf16 (bwd_dvloc_mma.cu)
+cudaError_t mma_bwd_dv_local(const Dims& d, const void* q, const void* k, const float* g_cum, const void* d_o,
+                             void* dv_loc, cudaStream_t s);
 // the per-chunk stage (dq, dk, dv, dbeta, dg) from the chunk's tiles and T = (I + A)^{-1} (bwd_chunk_mma.cu)
 cudaError_t mma_bwd_chunk(const Dims& d, const void* q, const void* k, const void* v, const void* beta,
                           const float* g_cum, const void* w, const void* u, const void* tinv, const void* v_new,

@@ -192,11 +192,13 @@ bwd_scan_dh_kernel(Dims d, const IO* __restrict__ q, const IO* __restrict__ k, c
 // ------------------------------------------------------------------ dqkwg
 // One CTA per (chunk, head, batch).  Shared (fp32): dos/vps/dvs [C][V+1], dQt [C][C+1],
 // then per pass over 32 key columns: hs/dhs [32][V+1], qt/kt/Gt/dGt/tt [C][33]; dGrow [C].
-template <typename IO, bool PER_K>
+// IT: the type of the reverse scan's dh checkpoints and dv' (fp32 from the CUDA-core scan, bf16 from
+// the tensor-core one)
+template <typename IO, bool PER_K, typename IT>
 __global__ void __launch_bounds__(kThreads)
 bwd_dqkwg_kernel(Dims d, const IO* __restrict__ q, const IO* __restrict__ k, const IO* __restrict__ v_new,
-                 const float* __restrict__ g_cum, const IO* __restrict__ h_ckpt, const float* __restrict__ dh_ckpt,
-                 const IO* __restrict__ d_o, const float* __restrict__ dv_new, IO* __restrict__ dq,
+                 const float* __restrict__ g_cum, const IO* __restrict__ h_ckpt, const IT* __restrict__ dh_ckpt,
+                 const IO* __restrict__ d_o, const IT* __restrict__ dv_new, IO* __restrict__ dq,
                  float* __restrict__ dk_part, float* __restrict__ dw, float* __restrict__ dG_part) {
     extern __shared__ float smem[];
     constexpr int KT = kTile, KTP = kTile + 1;
@@ -227,7 +229,7 @@ bwd_dqkwg_kernel(Dims d, const IO* __restrict__ q, const IO* __restrict__ k, con
         const bool in = t < nv;
         dos[t * VP + x] = in ? ld(d_o, row(t) * V + x) : 0.f;
         vps[t * VP + x] = in ? ld(v_new, row(t) * V + x) : 0.f;
-        dvs[t * VP + x] = in ? dv_new[row(t) * V + x] : 0.f;
+        dvs[t * VP + x] = in ? ld(dv_new, row(t) * V + x) : 0.f;
     }
     for (int i = tid; i < C; i += kThreads) dGrow[i] = 0.f;
     __syncthreads();
@@ -243,7 +245,7 @@ bwd_dqkwg_kernel(Dims d, const IO* __restrict__ q, const IO* __restrict__ k, con
         for (int i = tid; i < KT * V; i += kThreads) {
             const int e = i / V, x = i % V;
             hs[e * VP + x] = ld(h_ckpt, ck + (int64_t)(e0 + e) * V + x);
-            dhs[e * VP + x] = dh_ckpt[ck + (int64_t)(e0 + e) * V + x];
+            dhs[e * VP + x] = ld(dh_ckpt, ck + (int64_t)(e0 + e) * V + x);
         }
         for (int i = tid; i < C * KT; i += kThreads) {
             const int t = i / KT, e = i % KT;
@@ -308,10 +310,10 @@ bwd_dqkwg_kernel(Dims d, const IO* __restrict__ q, const IO* __restrict__ k, con
 // ------------------------------------------------------------------ wy
 // One CTA per (chunk, head, batch).  Shared (fp32): ks [C][K+1], Gs [C][GW], bs [C],
 // Ms/Xs/Ds/Ps [C][C+1], then per pass over 32 columns: at/bt/ct [C][33]; dbs/dGrow [C].
-template <typename IO, bool PER_K>
+template <typename IO, bool PER_K, typename IT>
 __global__ void __launch_bounds__(kThreads)
 bwd_wy_kernel(Dims d, const IO* __restrict__ k, const IO* __restrict__ v, const IO* __restrict__ beta,
-              const float* __restrict__ g_cum, const float* __restrict__ dw, const float* __restrict__ du,
+              const float* __restrict__ g_cum, const float* __restrict__ dw, const IT* __restrict__ du,
               const float* __restrict__ dk_part, const float* __restrict__ dG_part, IO* __restrict__ dk,
               IO* __restrict__ dv, IO* __restrict__ dbeta, float* __restrict__ dg) {
     extern __shared__ float smem[];
@@ -382,7 +384,7 @@ bwd_wy_kernel(Dims d, const IO* __restrict__ k, const IO* __restrict__ v, const 
                 at[t * KTP + e] = in ? dw[row(t) * K + p0 + e] : 0.f;
                 bt[t * KTP + e] = bs[t] * ks[t * KP + p0 + e] * expf(Gs[t * GW + (PER_K ? p0 + e : 0)]);
             } else {
-                at[t * KTP + e] = in ? du[row(t) * V + p0 - K + e] : 0.f;
+                at[t * KTP + e] = in ? ld(du, row(t) * V + p0 - K + e) : 0.f;
                 bt[t * KTP + e] = in ? bs[t] * ld(v, row(t) * V + p0 - K + e) : 0.f;
             }
         }
@@ -469,7 +471,7 @@ bwd_wy_kernel(Dims d, const IO* __restrict__ k, const IO* __restrict__ v, const 
         for (int i = tid; i < C * KT; i += kThreads) {
             const int t = i / KT, x = i % KT;
             const bool in = t < nv;
-            at[t * KTP + x] = in ? du[row(t) * V + x0 + x] : 0.f;
+            at[t * KTP + x] = in ? ld(du, row(t) * V + x0 + x) : 0.f;
             ct[t * KTP + x] = in ? ld(v, row(t) * V + x0 + x) : 0.f;
         }
         __syncthreads();
@@ -570,42 +572,52 @@ cudaError_t simt_bwd_scan_dh(const Dims& d, const void* q, const void* k, const 
 }
 
 cudaError_t simt_bwd_dqkwg(const Dims& d, const void* q, const void* k, const void* v_new, const float* g_cum,
-                           const void* h_ckpt, const float* dh_ckpt, const void* d_o, const float* dv_new,
-                           void* dq, float* dk_part, float* dw, float* dG_part, cudaStream_t s) {
+                           const void* h_ckpt, const void* dh_ckpt, const void* d_o, const void* dv_new,
+                           void* dq, float* dk_part, float* dw, float* dG_part, cudaStream_t s, bool inter16) {
     const size_t C = d.C, V = d.V;
     const size_t smem = sizeof(float) * (3 * C * (V + 1) + C * (C + 1) + 2 * (size_t)kTile * (V + 1) +
                                          5 * C * (kTile + 1) + C);
     const dim3 grid(d.NT, d.H, d.B);
-#define LAUNCH(IO, PK)                                                                                       \
-    do {                                                                                                        \
-        auto kern = bwd_dqkwg_kernel<IO, PK>;                                                               \
+#define LAUNCH_IT(IO, PK, IT)                                                                                \
+    do {                                                                                                     \
+        auto kern = bwd_dqkwg_kernel<IO, PK, IT>;                                                            \
         cudaError_t e = allow_smem(kern, smem);                                                              \
         if (e != cudaSuccess) return e;                                                                      \
         kern<<<grid, kThreads, smem, s>>>(d, (const IO*)q, (const IO*)k, (const IO*)v_new, g_cum,            \
-                                          (const IO*)h_ckpt, dh_ckpt, (const IO*)d_o, dv_new, (IO*)dq,       \
-                                          dk_part, dw, dG_part);                                             \
+                                          (const IO*)h_ckpt, (const IT*)dh_ckpt, (const IO*)d_o,             \
+                                          (const IT*)dv_new, (IO*)dq, dk_part, dw, dG_part);                 \
+    } while (0)
+#define LAUNCH(IO, PK)                                                                                       \
+    do {                                                                                                     \
+        if (inter16) LAUNCH_IT(IO, PK, IO); else LAUNCH_IT(IO, PK, float);                                 \
     } while (0)
     GDR_DISPATCH(LAUNCH);
 #undef LAUNCH
+#undef LAUNCH_IT
     return cudaGetLastError();
 }
 
 cudaError_t simt_bwd_wy(const Dims& d, const void* k, const void* v, const void* beta, const float* g_cum,
-                        const float* dw, const float* du, const float* dk_part, const float* dG_part, void* dk,
-                        void* dv, void* dbeta, float* dg, cudaStream_t s) {
+                        const float* dw, const void* du, const float* dk_part, const float* dG_part, void* dk,
+                        void* dv, void* dbeta, float* dg, cudaStream_t s, bool inter16) {
     const size_t C = d.C, K = d.K, GW = d.per_k ? d.K : 1;
     const size_t smem = sizeof(float) * (C * (K + 1) + C * GW + C + 4 * C * (C + 1) + 3 * C * (kTile + 1) + 2 * C);
     const dim3 grid(d.NT, d.H, d.B);
-#define LAUNCH(IO, PK)                                                                                    \
+#define LAUNCH_IT(IO, PK, IT)                                                                                \
     do {                                                                                                     \
-        auto kern = bwd_wy_kernel<IO, PK>;                                                               \
-        cudaError_t e = allow_smem(kern, smem);                                                           \
-        if (e != cudaSuccess) return e;                                                                   \
-        kern<<<grid, kThreads, smem, s>>>(d, (const IO*)k, (const IO*)v, (const IO*)beta, g_cum, dw, du,  \
-                                          dk_part, dG_part, (IO*)dk, (IO*)dv, (IO*)dbeta, dg);            \
+        auto kern = bwd_wy_kernel<IO, PK, IT>;                                                               \
+        cudaError_t e = allow_smem(kern, smem);                                                              \
+        if (e != cudaSuccess) return e;                                                                      \
+        kern<<<grid, kThreads, smem, s>>>(d, (const IO*)k, (const IO*)v, (const IO*)beta, g_cum, dw,         \
+                                          (const IT*)du, dk_part, dG_part, (IO*)dk, (IO*)dv, (IO*)dbeta, dg); \
+    } while (0)
+#define LAUNCH(IO, PK)                                                                                       \
+    do {                                                                                                     \
+        if (inter16) LAUNCH_IT(IO, PK, IO); else LAUNCH_IT(IO, PK, float);                                 \
     } while (0)
     GDR_DISPATCH(LAUNCH);
 #undef LAUNCH
+#undef LAUNCH_IT
     return cudaGetLastError();
 }
 

@@ -35,7 +35,7 @@ EXPORTS = ["gdr_prepare_wy", "gdr_scan_h", "gdr_chunk_output", "gdr_forward", "g
            "gdr_forward_static_scratch", "gdr_scan_output", "gdr_prepare_wyp",
            "gdr_bwd_dv_local", "gdr_bwd_scan_dh", "gdr_bwd_dqkwg", "gdr_bwd_wy", "gdr_backward",
            "gdr_backward_workspace_bytes", "gdr_bwd_prepare", "gdr_bwd_scan_dh_p", "gdr_bwd_wy_dqkg",
-           "gdr_bwd_group_sum",
+           "gdr_bwd_group_sum", "gdr_bwd_dv_local_tc", "gdr_bwd_scan_dh_tc",
            "gdr_status_string", "gdr_get_device_status", "gdr_last_variant", "gdr_version"]
 
 
@@ -87,6 +87,8 @@ def load(path: str | None = None):
             "gdr_bwd_scan_dh_p": [P] + [vp] * 11,
             "gdr_bwd_wy_dqkg": [P] + [vp] * 19,
             "gdr_bwd_group_sum": [P] + [vp] * 5,
+            "gdr_bwd_dv_local_tc": [P] + [vp] * 6,
+            "gdr_bwd_scan_dh_tc": [P] + [vp] * 11,
             "gdr_status_string": [ctypes.c_int],
             "gdr_get_device_status": [vp],
             "gdr_last_variant": [],
@@ -285,6 +287,17 @@ def gdr_bwd_wy_dqkg(p, q, k, v, beta, g_cum, w, u, tinv, v_new, h_ckpt, d_o, dv_
                                   _ptr(u), _ptr(tinv), _ptr(v_new), _ptr(h_ckpt), _ptr(d_o), _ptr(dv_new),
                                   _ptr(dh_ckpt), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbeta), _ptr(dg),
                                   _stream(stream)), "gdr_bwd_wy_dqkg")
+
+
+def gdr_bwd_dv_local_tc(p, q, k, g_cum, d_o, dv_loc, stream=None):
+    _check(load().gdr_bwd_dv_local_tc(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(g_cum), _ptr(d_o), _ptr(dv_loc),
+                                      _stream(stream)), "gdr_bwd_dv_local_tc")
+
+
+def gdr_bwd_scan_dh_tc(p, q, k, w, g_cum, dv_loc, d_o, dh_final, dh_ckpt, dv_new, dh0, stream=None):
+    _check(load().gdr_bwd_scan_dh_tc(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(w), _ptr(g_cum), _ptr(dv_loc), _ptr(d_o),
+                                     _ptr(dh_final), _ptr(dh_ckpt), _ptr(dv_new), _ptr(dh0), _stream(stream)),
+           "gdr_bwd_scan_dh_tc")
 
 
 def gdr_bwd_group_sum(p, dq_v, dk_v, dq, dk, stream=None):

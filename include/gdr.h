@@ -260,6 +260,10 @@ GDR_API gdr_status gdr_forward_static_scratch(const gdr_problem* p, const void* 
  * - On the tensor cores (gdr_bwd_prepare, gdr_bwd_scan_dh_p,
  *   gdr_bwd_wy_dqkg; bf16 intermediates): bf16 io, a scalar gate and C = 64,
  *   which variants AUTO and TENSOR take.
+ * - For other bf16 problems (a per-key-dim gate, or C = 32), AUTO and TENSOR
+ *   run the local term and the reverse scan on the tensor cores
+ *   (gdr_bwd_dv_local_tc, gdr_bwd_scan_dh_tc, bf16 intermediates) and the
+ *   per-chunk stages on the CUDA cores.
  * The variant FUSED is not offered here (GDR_ERR_UNSUPPORTED).
  */
 
@@ -287,10 +291,10 @@ GDR_API gdr_status gdr_bwd_scan_dh(const gdr_problem* p, const void* q, const vo
  *     dG_part = dqg q exp(G) + q L(dQ~, k) - k R(dQ~, q) - dkg kg      fp32, the shape of g
  *               (+ sum_i dkg_i kg_i + exp(G_L) sum_v h dhn on the chunk's last token;
  *                a scalar gate sums over the key dim)
- * Inputs q, k, v_new, h_ckpt, do io; g_cum, dh_ckpt, dv_new fp32. */
+ * Inputs q, k, v_new, h_ckpt, do io; g_cum fp32; dh_ckpt, dv_new fp32 (see below). */
 GDR_API gdr_status gdr_bwd_dqkwg(const gdr_problem* p, const void* q, const void* k, const void* v_new,
-                                 const float* g_cum, const void* h_ckpt, const float* dh_ckpt, const void* d_o,
-                                 const float* dv_new, void* dq, float* dk_part, float* dw, float* dG_part,
+                                 const float* g_cum, const void* h_ckpt, const void* dh_ckpt, const void* d_o,
+                                 const void* dv_new, void* dq, float* dk_part, float* dw, float* dG_part,
                                  void* stream);
 
 /* The WY backward, with (I + A)^{-1} rebuilt from k, beta, g_cum and du = dv_new:
@@ -300,10 +304,14 @@ GDR_API gdr_status gdr_bwd_dqkwg(const gdr_problem* p, const void* q, const void
  *     dv    = beta dvb                                                  (io)
  *     dbeta = sum_d dkb k exp(G) + sum_v dvb v + sum_j dA_ij M_ij      (io)
  *     dg    = reverse cumsum over each chunk of dG_part + dkb kb + k L(Y, k) - k R(Y, k)   (fp32)
- * Inputs k, v, beta io; g_cum, dw, dv_new, dk_part, dG_part fp32. */
+ * Inputs k, v, beta io; g_cum, dw, dk_part, dG_part fp32; dv_new fp32 (see below). */
 GDR_API gdr_status gdr_bwd_wy(const gdr_problem* p, const void* k, const void* v, const void* beta,
-                              const float* g_cum, const float* dw, const float* dv_new, const float* dk_part,
+                              const float* g_cum, const float* dw, const void* dv_new, const float* dk_part,
                               const float* dG_part, void* dk, void* dv, void* dbeta, float* dg, void* stream);
+
+/* dh_ckpt and dv_new of gdr_bwd_dqkwg and gdr_bwd_wy are fp32 (as gdr_bwd_scan_dh writes them), or,
+ * for bf16 io with a variant other than SIMT, bf16 (as gdr_bwd_scan_dh_tc and gdr_bwd_scan_dh_p
+ * write them). */
 
 /* The tensor-core stages (bf16 io, scalar gate, C = 64; GDR_ERR_UNSUPPORTED otherwise). */
 
@@ -330,6 +338,21 @@ GDR_API gdr_status gdr_bwd_wy_dqkg(const gdr_problem* p, const void* q, const vo
                                    const void* tinv, const void* v_new, const void* h_ckpt, const void* d_o,
                                    const void* dv_new, const void* dh_ckpt, void* dq, void* dk, void* dv,
                                    void* dbeta, float* dg, void* stream);
+
+/* The local term and the reverse scan on the tensor cores for the problems the fused per-chunk
+ * stage does not take (a per-key-dim gate, or C = 32); bf16 io, GDR_ERR_UNSUPPORTED otherwise.
+ * gdr_bwd_dv_local_tc: dv_loc = scale tril_0(Q~)^T do per chunk, [B,T,H,V] bf16.  For a per-key-dim
+ * gate Q~ is formed from q exp(G - G_ref) and k exp(G_ref - G) around the chunk's middle row, and
+ * exactly in fp32 for a chunk whose gate moves further than that keeps bounded.
+ * gdr_bwd_scan_dh_tc: the reverse scan of gdr_bwd_scan_dh with dv_loc in bf16 and dh_ckpt, dv_new
+ * written in bf16.  gdr_backward runs these, then gdr_bwd_dqkwg and gdr_bwd_wy's kernels reading
+ * the bf16 dh_ckpt and dv_new. */
+GDR_API gdr_status gdr_bwd_dv_local_tc(const gdr_problem* p, const void* q, const void* k, const float* g_cum,
+                                       const void* d_o, void* dv_loc, void* stream);
+GDR_API gdr_status gdr_bwd_scan_dh_tc(const gdr_problem* p, const void* q, const void* k, const void* w,
+                                      const float* g_cum, const void* dv_loc, const void* d_o,
+                                      const float* dh_final, void* dh_ckpt, void* dv_new, float* dh0,
+                                      void* stream);
 
 /* Grouped value heads (HV > H): the stage entry points above (gdr_bwd_dqkwg's dq, gdr_bwd_wy's
  * dk, gdr_bwd_wy_dqkg's dq and dk) write these per value head, [B,T,HV,K] in the io dtype; the

@@ -399,3 +399,45 @@ def test_fp16_io_backward(shape, per_k):
     for name in GRADS:
         err = scaled_err(got[name], ref[name])
         assert np.isfinite(err) and err <= BWD_TOL["f16"], f"{name}: {err:.3e}"
+
+
+# ---------------------------------------------------------------- tensor-core local term and reverse scan
+
+TC_SHAPES = [(2, 128, 3, 64, 64, 64), (1, 192, 2, 128, 128, 32), (2, 100, 2, 128, 64, 64), (1, 77, 1, 64, 128, 32)]
+
+
+@pytest.mark.parametrize("shape", TC_SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("per_k", [False, True])
+def test_tensor_stage_dv_local(shape, per_k):
+    x, do, _, full, _ = _stage_setup(shape, per_k, torch.bfloat16, 94)
+    C = shape[-1]
+    p = gdr.problem_for(x.q, x.v, x.g, C, scale=0.125, variant="tensor")
+    G_r = rounded(full["G"], torch.float32)
+    out = torch.full(x.v.shape, float("nan"), device="cuda", dtype=torch.bfloat16)
+    gdr.gdr_bwd_dv_local_tc(p, dev(x.q), dev(x.k), dev(G_r), dev(do), out)
+    torch.cuda.synchronize()
+    assert scaled_err(out, cb.dv_local(x.q, x.k, G_r, do, C, 0.125)) <= STAGE_TOL["bf16"]
+
+
+@pytest.mark.parametrize("shape", TC_SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("per_k", [False, True])
+def test_tensor_stage_reverse_scan_from_dv_local(shape, per_k):
+    x, do, dhf, full, _ = _stage_setup(shape, per_k, torch.bfloat16, 96)
+    B, T, H, K, V, C = shape
+    p = gdr.problem_for(x.q, x.v, x.g, C, scale=0.125, variant="tensor")
+    G_r, w_r = rounded(full["G"], torch.float32), rounded(full["w"], torch.bfloat16)
+    dl_r = rounded(cb.dv_local(x.q, x.k, G_r, do, C, 0.125), torch.bfloat16)
+    ref = cb.scan_dh(x.q, x.k, w_r, G_r, do, dl_r, dhf, C, 0.125)
+    NT = -(-T // C)
+    nan = float("nan")
+    dh_ckpt = torch.full((B, NT, H, K, V), nan, device="cuda", dtype=torch.bfloat16)
+    dv_new = torch.full((B, T, H, V), nan, device="cuda", dtype=torch.bfloat16)
+    dh0 = torch.full((B, H, K, V), nan, device="cuda")
+    gdr.gdr_bwd_scan_dh_tc(p, dev(x.q), dev(x.k), dev(w_r), dev(G_r), dev(dl_r), dev(do), dev(dhf), dh_ckpt, dv_new,
+                           dh0)
+    torch.cuda.synchronize()
+    assert gdr.gdr_get_device_status() == 0
+    tol = STAGE_TOL["bf16"]
+    assert scaled_err(dh_ckpt, ref["dh_ckpt"]) <= tol
+    assert scaled_err(dv_new, ref["dv_new"]) <= tol
+    assert scaled_err(dh0, ref["dh0"]) <= tol

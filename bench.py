@@ -260,8 +260,21 @@ def time_backward(args, wl, x, dev, flush, stream, world):
     dG_part = torch.empty(g.shape, **f32)
     dq, dk, dv, dbeta = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(beta)
     dg, dh0 = torch.empty(g.shape, **f32), torch.empty(B, H, K, V, **f32)
-    fast = q.dtype == torch.bfloat16 and g.dim() == 3 and C == 64 and args.variant in ("auto", "tensor")
-    if fast:
+    fast = q.dtype == torch.bfloat16 and g.dim() == 3 and args.variant in ("auto", "tensor")
+    if fast and C == 32:
+        # the tensor-core path at 32-token chunks: the local term from its own kernel
+        tinv = torch.empty(B, NT, H, C, C, device=dev, dtype=q.dtype)
+        dv_loc16 = torch.empty(B, T, H, V, device=dev, dtype=q.dtype)
+        dh_ckpt16 = torch.empty(B, NT, H, K, V, device=dev, dtype=q.dtype)
+        dv_new16 = torch.empty(B, T, H, V, device=dev, dtype=q.dtype)
+        names = ["prepare", "rescan", "dv_local", "scan_dh", "wy_dqkg"]
+        calls = [lambda: gdr.gdr_bwd_prepare(p, q, k, v, g, beta, w, u, g_cum, None, tinv),
+                 lambda: gdr.gdr_scan_h(p, k, w, u, g_cum, h0, h_ckpt, v_new, None),
+                 lambda: gdr.gdr_bwd_dv_local_tc(p, q, k, g_cum, d_o, dv_loc16),
+                 lambda: gdr.gdr_bwd_scan_dh_tc(p, q, k, w, g_cum, dv_loc16, d_o, dhf, dh_ckpt16, dv_new16, dh0),
+                 lambda: gdr.gdr_bwd_wy_dqkg(p, q, k, v, beta, g_cum, w, u, tinv, v_new, h_ckpt, d_o, dv_new16,
+                                             dh_ckpt16, dq, dk, dv, dbeta, dg)]
+    elif fast:
         # the tensor-core path gdr_backward takes here: four launches, bf16 intermediates
         P = torch.empty(B, NT, H, C, C, device=dev, dtype=q.dtype)
         tinv = torch.empty(B, NT, H, C, C, device=dev, dtype=q.dtype)

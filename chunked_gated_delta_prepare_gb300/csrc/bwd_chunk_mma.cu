@@ -1,5 +1,5 @@
-// The backward's per-chunk stage for bf16 io, a scalar gate and 64-token
-// chunks: every gradient that needs only the chunk's own tiles, in one kernel
+// The backward's per-chunk stage for bf16 io and a scalar gate (32- or 64-token
+// chunks): every gradient that needs only the chunk's own tiles, in one kernel
 // (the pages' backward names this stage wy_dqkg: the WY backward fused with dq,
 // dk and the gate gradient; "kernel_fun/kda/_kernels/bwd_scan.py", host wrapper).
 //
@@ -24,8 +24,8 @@
 // batch); the tiles sit in shared memory as padded bf16 rows (a row stride of
 // D + 8 elements keeps every ldmatrix free of bank conflicts) and every product
 // is a warp-level mma.sync m16n8k16 with fp32 accumulation.  Eight warps:
-// warp w owns the 16-row block w % 4 and the column half w / 4 of every
-// [C x D] result, so dq and dk accumulate in registers across all their terms
+// warp w owns the 16-row block w % (C/16) and the column group w / (C/16) of
+// every [C x D] result, so dq and dk accumulate in registers across all their terms
 // (sixteen warps with column quarters measured no faster).  Tile loads are
 // cp.async groups issued in the order the products need them, and the WY
 // phase's tiles are in flight during the output-score phase.
@@ -42,11 +42,9 @@ namespace {
 using bf16 = __nv_bfloat16;
 using namespace cm;
 constexpr int kThreads = 256;
-constexpr int kColGroups = kThreads / 32 / 4;   // warps sharing each 16-row block
 
-template <int K, int V>
+template <int K, int V, int C>
 struct ChunkLayout {
-    static constexpr int C = 64;
     static constexpr int LK = K + 8, LV = V + 8, LC = C + 8;
     static constexpr uint32_t rq = 0;                              // q
     static constexpr uint32_t rk = rq + C * LK * 2;                // k
@@ -71,7 +69,7 @@ struct ChunkLayout {
     static_assert(bytes <= 227 * 1024, "shared memory");
 };
 
-template <int K, int V>
+template <int K, int V, int C>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_chunk_mma_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* __restrict__ v,
                      const bf16* __restrict__ beta, const float* __restrict__ g_cum, const bf16* __restrict__ w,
@@ -80,9 +78,11 @@ bwd_chunk_mma_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
                      const bf16* __restrict__ dh_ckpt, bf16* __restrict__ dq, bf16* __restrict__ dk,
                      bf16* __restrict__ dv, bf16* __restrict__ dbeta, float* __restrict__ dg, int T, int H, int G,
                      float scale) {
-    using L = ChunkLayout<K, V>;
-    constexpr int C = L::C, LK = L::LK, LV = L::LV, LC = L::LC;
-    constexpr int NK = K / 16 / kColGroups, NV = V / 16 / kColGroups, NC = C / 16 / kColGroups;   // blocks per warp
+    using L = ChunkLayout<K, V, C>;
+    constexpr int LK = L::LK, LV = L::LV, LC = L::LC;
+    constexpr int RB = C / 16, CG = 8 / RB;             // 16-row blocks; warps sharing each
+    constexpr int NK = K / 16 / CG, NV = V / 16 / CG;   // 16-column blocks per warp
+    constexpr int NCB = C / 16, NC = NCB >= CG ? NCB / CG : 1;   // C x C results: some warps idle at C = 32
     extern __shared__ __align__(128) unsigned char sm[];
     bf16* Qs = reinterpret_cast<bf16*>(sm + L::rq);
     bf16* Ks = reinterpret_cast<bf16*>(sm + L::rk);
@@ -105,7 +105,7 @@ bwd_chunk_mma_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g4 = lane >> 2, q4 = lane & 3, mi = lane >> 3, mr = lane & 7;
-    const int rb = warp & 3, cg = warp >> 2;
+    const int rb = warp % RB, cg = warp / RB;
     const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int NT = (T + C - 1) / C;
     const int t0 = c * C, nv = min(C, T - t0);
@@ -144,6 +144,7 @@ bwd_chunk_mma_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
     const uint32_t aDV = smem_addr(DVs), aH = smem_addr(Hs), aDH = smem_addr(DHs), aDW = smem_addr(DWs);
     const uint32_t aX = smem_addr(Xs), aY = smem_addr(Ys);
     const int ck = cg * NK, cv = cg * NV, cc = cg * NC;   // this warp's first column block
+    const bool cc_active = cc < NCB;                      // a column block of the C x C results
 
     float accQ[NK][2][4], accK[NK][2][4], tmp[NK][2][4];
     // dqg = do h^T (h, do landed)
@@ -157,7 +158,7 @@ bwd_chunk_mma_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
     zero(accK);
     wgemm<NK, V, false, true>(accK, aVP, LV, aDH, LV, rb, ck, mi, mr);
     // Xq = scale (do v'^T) Gam, strictly lower, with its diagonal apart
-    {
+    if (cc_active) {
         float xq[NC][2][4];
         zero(xq);
         wgemm<NC, V, false, true>(xq, aDO, LV, aVP, LV, rb, cc, mi, mr);
@@ -317,7 +318,7 @@ bwd_chunk_mma_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
     }
     __syncthreads();
     // dA = strict_lower(-(dkb w^T + dvb u^T)); dbeta's A term against M = Gam (k k^T); Y = beta dA Gam
-    {
+    if (cc_active) {
         float da[NC][2][4], m[NC][2][4];
         zero(da);
         zero(m);
@@ -394,13 +395,13 @@ bwd_chunk_mma_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
     if (tid < nv) dbeta[tok0 + (int64_t)tid * H] = __float2bfloat16_rn(sdB[tid]);
 }
 
-template <int K, int V>
+template <int K, int V, int C>
 cudaError_t launch(const Dims& d, const void* q, const void* k, const void* v, const void* beta, const float* g_cum,
                    const void* w, const void* u, const void* tinv, const void* v_new, const void* h_ckpt,
                    const void* d_o, const void* dv_new, const void* dh_ckpt, void* dq, void* dk, void* dv,
                    void* dbeta, float* dg, cudaStream_t s) {
-    using L = ChunkLayout<K, V>;
-    auto kern = bwd_chunk_mma_kernel<K, V>;
+    using L = ChunkLayout<K, V, C>;
+    auto kern = bwd_chunk_mma_kernel<K, V, C>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::bytes);
     if (e != cudaSuccess) return e;
     const dim3 grid(d.NT, d.H, d.B);
@@ -418,12 +419,18 @@ cudaError_t mma_bwd_chunk(const Dims& d, const void* q, const void* k, const voi
                           const float* g_cum, const void* w, const void* u, const void* tinv, const void* v_new,
                           const void* h_ckpt, const void* d_o, const void* dv_new, const void* dh_ckpt, void* dq,
                           void* dk, void* dv, void* dbeta, float* dg, cudaStream_t s) {
-    if (!d.bf16 || d.per_k || d.C != 64) return cudaErrorInvalidValue;
+    if (!d.bf16 || d.per_k) return cudaErrorInvalidValue;
 #define GDR_CHUNK_ARGS d, q, k, v, beta, g_cum, w, u, tinv, v_new, h_ckpt, d_o, dv_new, dh_ckpt, dq, dk, dv, dbeta, dg, s
-    if (d.K == 64 && d.V == 64) return launch<64, 64>(GDR_CHUNK_ARGS);
-    if (d.K == 64 && d.V == 128) return launch<64, 128>(GDR_CHUNK_ARGS);
-    if (d.K == 128 && d.V == 64) return launch<128, 64>(GDR_CHUNK_ARGS);
-    return launch<128, 128>(GDR_CHUNK_ARGS);
+    if (d.C == 32) {
+        if (d.K == 64 && d.V == 64) return launch<64, 64, 32>(GDR_CHUNK_ARGS);
+        if (d.K == 64 && d.V == 128) return launch<64, 128, 32>(GDR_CHUNK_ARGS);
+        if (d.K == 128 && d.V == 64) return launch<128, 64, 32>(GDR_CHUNK_ARGS);
+        return launch<128, 128, 32>(GDR_CHUNK_ARGS);
+    }
+    if (d.K == 64 && d.V == 64) return launch<64, 64, 64>(GDR_CHUNK_ARGS);
+    if (d.K == 64 && d.V == 128) return launch<64, 128, 64>(GDR_CHUNK_ARGS);
+    if (d.K == 128 && d.V == 64) return launch<128, 64, 64>(GDR_CHUNK_ARGS);
+    return launch<128, 128, 64>(GDR_CHUNK_ARGS);
 #undef GDR_CHUNK_ARGS
 }
 

@@ -165,10 +165,11 @@ BackwardWorkspace plan_backward(const gdr::Dims& d, BwdPath path) {
     take(&ws.u, rows * d.V * e);
     take(&ws.v_new, rows * d.V * e);
     take(&ws.h_ckpt, states * e);
-    if (path == BwdPath::Fast) {   // bf16 gradients of v' and of the states; the prepare's P and T
+    if (path == BwdPath::Fast) {   // bf16 gradients of v' and of the states; T; P (C = 64) or dv_loc (C = 32)
         take(&ws.dv_new, rows * d.V * 2);
         take(&ws.dh_ckpt, states * 2);
-        take(&ws.P, tiles * 2);
+        if (d.C == 64) take(&ws.P, tiles * 2);
+        else take(&ws.dv_loc, rows * d.V * 2);
         take(&ws.tinv, tiles * 2);
     } else if (path == BwdPath::Tensor) {   // bf16 dv_loc, v' and state gradients; fp32 per-chunk partials
         take(&ws.dv_loc, rows * d.V * 2);
@@ -195,7 +196,7 @@ BackwardWorkspace plan_backward(const gdr::Dims& d, BwdPath path) {
 
 // AUTO and TENSOR take FAST where it applies; FUSED keeps no checkpoints and is not offered.
 gdr_status pick_backward(const gdr_problem* p, const gdr::Dims& d, BwdPath* path) {
-    const bool fast = d.bf16 && !d.per_k && d.C == 64;
+    const bool fast = d.bf16 && !d.per_k;
     switch (p->variant) {
         case GDR_VARIANT_SIMT: *path = BwdPath::Simt; return GDR_OK;
         case GDR_VARIANT_TENSOR:
@@ -418,10 +419,10 @@ gdr_status gdr_bwd_prepare(const gdr_problem* p, const void* q, const void* k, c
     gdr::Dims d;
     gdr_status st = check_problem(p, &d);
     if (st != GDR_OK) return st;
-    if ((st = check_ptrs({q, k, v, g, beta, w, u, g_cum, P, tinv}, {})) != GDR_OK) return st;
-    if (p->variant == GDR_VARIANT_SIMT || !d.bf16 || d.per_k || d.C != 64) return GDR_ERR_UNSUPPORTED;
-    st = from_cuda(gdr::mma_prepare(d, k, v, g, beta, w, u, g_cum, (cudaStream_t)stream, device_error_word(), q, P,
-                                    tinv));
+    if ((st = check_ptrs({q, k, v, g, beta, w, u, g_cum, tinv}, {P})) != GDR_OK) return st;
+    if (p->variant == GDR_VARIANT_SIMT || !d.bf16 || d.per_k || (P && d.C != 64)) return GDR_ERR_UNSUPPORTED;
+    st = from_cuda(gdr::mma_prepare(d, k, v, g, beta, w, u, g_cum, (cudaStream_t)stream, device_error_word(),
+                                    P ? q : nullptr, P, tinv));
     if (st == GDR_OK) t_last_variant = "tensor";
     return st;
 }
@@ -450,7 +451,7 @@ gdr_status gdr_bwd_wy_dqkg(const gdr_problem* p, const void* q, const void* k, c
     if ((st = check_ptrs({q, k, v, beta, g_cum, w, u, tinv, v_new, h_ckpt, d_o, dv_new, dh_ckpt, dq, dk, dv, dbeta,
                           dg}, {})) != GDR_OK)
         return st;
-    if (p->variant == GDR_VARIANT_SIMT || !d.bf16 || d.per_k || d.C != 64) return GDR_ERR_UNSUPPORTED;
+    if (p->variant == GDR_VARIANT_SIMT || !d.bf16 || d.per_k) return GDR_ERR_UNSUPPORTED;
     st = from_cuda(gdr::mma_bwd_chunk(d, q, k, v, beta, g_cum, w, u, tinv, v_new, h_ckpt, d_o, dv_new, dh_ckpt, dq, dk,
                                       dv, dbeta, dg, (cudaStream_t)stream));
     if (st == GDR_OK) t_last_variant = "tensor";
@@ -513,13 +514,27 @@ gdr_status gdr_backward(const gdr_problem* p, const void* q, const void* k, cons
     if (path == BwdPath::Fast) {
         // every step on the tensor cores: prepare (+ P and T), re-scan, reverse scan, per-chunk stage
         unsigned int* err = device_error_word();
-        void* P = base + ws.P;
         void* tinv = base + ws.tinv;
-        if ((st = from_cuda(gdr::mma_prepare(d, k, v, g, beta, w, u, g_cum, s, err, q, P, tinv))) != GDR_OK) return st;
-        if ((st = from_cuda(gdr::mma_scan(d, k, w, u, g_cum, h0, h_ckpt, v_new, nullptr, s, err))) != GDR_OK) return st;
-        if ((st = from_cuda(gdr::mma_bwd_scan(d, q, k, w, g_cum, P, d_o, dh_final, dh_ckpt, dv_new, dh0, s, err))) !=
-            GDR_OK)
-            return st;
+        if (d.C == 64) {   // the prepare's gated scores P give the reverse scan its local term
+            void* P = base + ws.P;
+            if ((st = from_cuda(gdr::mma_prepare(d, k, v, g, beta, w, u, g_cum, s, err, q, P, tinv))) != GDR_OK)
+                return st;
+            if ((st = from_cuda(gdr::mma_scan(d, k, w, u, g_cum, h0, h_ckpt, v_new, nullptr, s, err))) != GDR_OK)
+                return st;
+            if ((st = from_cuda(gdr::mma_bwd_scan(d, q, k, w, g_cum, P, d_o, dh_final, dh_ckpt, dv_new, dh0, s,
+                                                  err))) != GDR_OK)
+                return st;
+        } else {           // C = 32: the local term from its own kernel
+            if ((st = from_cuda(gdr::mma_prepare(d, k, v, g, beta, w, u, g_cum, s, err, nullptr, nullptr, tinv))) !=
+                GDR_OK)
+                return st;
+            if ((st = from_cuda(gdr::mma_scan(d, k, w, u, g_cum, h0, h_ckpt, v_new, nullptr, s, err))) != GDR_OK)
+                return st;
+            if ((st = from_cuda(gdr::mma_bwd_dv_local(d, q, k, g_cum, d_o, dv_loc, s))) != GDR_OK) return st;
+            if ((st = from_cuda(gdr::mma_bwd_scan_dl(d, q, k, w, g_cum, dv_loc, d_o, dh_final, dh_ckpt, dv_new, dh0, s,
+                                                     err))) != GDR_OK)
+                return st;
+        }
         if ((st = from_cuda(gdr::mma_bwd_chunk(d, q, k, v, beta, g_cum, w, u, tinv, v_new, h_ckpt, d_o, dv_new, dh_ckpt,
                                                dq, dk, dv, dbeta, dg, s))) != GDR_OK)
             return st;

@@ -257,13 +257,13 @@ GDR_API gdr_status gdr_forward_static_scratch(const gdr_problem* p, const void* 
  *   Variant SIMT re-scans on the CUDA cores too.  For bf16 io, variants AUTO
  *   and TENSOR re-scan on the tensor cores, then run these stages whenever the
  *   tensor-core set below does not apply.
- * - On the tensor cores (gdr_bwd_prepare, gdr_bwd_scan_dh_p,
- *   gdr_bwd_wy_dqkg; bf16 intermediates): bf16 io, a scalar gate and C = 64,
- *   which variants AUTO and TENSOR take.
- * - For other bf16 problems (a per-key-dim gate, or C = 32), AUTO and TENSOR
- *   run the local term and the reverse scan on the tensor cores
- *   (gdr_bwd_dv_local_tc, gdr_bwd_scan_dh_tc, bf16 intermediates) and the
- *   per-chunk stages on the CUDA cores.
+ * - On the tensor cores (gdr_bwd_prepare, gdr_bwd_scan_dh_p or, for C = 32,
+ *   gdr_bwd_dv_local_tc and gdr_bwd_scan_dh_tc, then gdr_bwd_wy_dqkg; bf16
+ *   intermediates): bf16 io with a scalar gate, which variants AUTO and TENSOR
+ *   take.
+ * - For a per-key-dim gate with bf16 io, AUTO and TENSOR run the local term and
+ *   the reverse scan on the tensor cores (gdr_bwd_dv_local_tc,
+ *   gdr_bwd_scan_dh_tc) and the per-chunk stages on the CUDA cores.
  * The variant FUSED is not offered here (GDR_ERR_UNSUPPORTED).
  */
 
@@ -313,10 +313,11 @@ GDR_API gdr_status gdr_bwd_wy(const gdr_problem* p, const void* k, const void* v
  * for bf16 io with a variant other than SIMT, bf16 (as gdr_bwd_scan_dh_tc and gdr_bwd_scan_dh_p
  * write them). */
 
-/* The tensor-core stages (bf16 io, scalar gate, C = 64; GDR_ERR_UNSUPPORTED otherwise). */
+/* The tensor-core stages (bf16 io, scalar gate; GDR_ERR_UNSUPPORTED otherwise). */
 
 /* gdr_prepare_wyp plus T = (I + A)^{-1} of every chunk: tinv [B,NT,H,C,C] bf16, row i of chunk c
- * holding row i of T.  Other arguments as gdr_prepare_wyp. */
+ * holding row i of T.  Other arguments as gdr_prepare_wyp; P may be NULL (not written), and must
+ * be for C = 32. */
 GDR_API gdr_status gdr_bwd_prepare(const gdr_problem* p, const void* q, const void* k, const void* v, const float* g,
                                    const void* beta, void* w, void* u, float* g_cum, void* P, void* tinv,
                                    void* stream);

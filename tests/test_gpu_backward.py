@@ -341,6 +341,10 @@ def test_tensor_stage_reverse_scan(shape, with_dhf):
 
 @pytest.mark.parametrize("shape", FAST_SHAPES, ids=lambda s: "x".join(map(str, s)))
 def test_tensor_stage_wy_dqkg(shape):
+    _wy_dqkg_case(shape)
+
+
+def _wy_dqkg_case(shape):
     x, do, _, full, p = _fast_setup(shape, 74)
     B, T, H, K, V, C = shape
     bf = torch.bfloat16
@@ -441,3 +445,10 @@ def test_tensor_stage_reverse_scan_from_dv_local(shape, per_k):
     assert scaled_err(dh_ckpt, ref["dh_ckpt"]) <= tol
     assert scaled_err(dv_new, ref["dv_new"]) <= tol
     assert scaled_err(dh0, ref["dh0"]) <= tol
+
+
+@pytest.mark.parametrize("shape", [(2, 128, 3, 64, 64, 32), (1, 96, 2, 128, 128, 32), (1, 77, 2, 128, 64, 32)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_tensor_stage_wy_dqkg_at_32_token_chunks(shape):
+    # the same per-chunk stage at C = 32 (two 16-row blocks, warps sharing the columns four ways)
+    _wy_dqkg_case(shape)

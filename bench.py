@@ -238,7 +238,7 @@ def run_reference(args, wl):
 # ------------------------------------------------------------------ GPU leg
 
 def time_backward(args, wl, x, dev, flush, stream, world):
-    """gdr_backward's six launches on the same workload, called one by one through their
+    """gdr_backward's launches on the same workload, called one by one through their
     C-ABI entry points (as gdr_backward calls them) so each can be timed; the upstream
     gradients do and dh_final are seeded normals."""
     B, T, H, K, V, C = wl.B, wl.T, wl.H, wl.K, wl.V, wl.chunk
@@ -287,19 +287,25 @@ def time_backward(args, wl, x, dev, flush, stream, world):
                  lambda: gdr.gdr_bwd_wy_dqkg(p, q, k, v, beta, g_cum, w, u, tinv, v_new, h_ckpt, d_o, dv_new16,
                                              dh_ckpt16, dq, dk, dv, dbeta, dg)]
     elif q.dtype == torch.bfloat16 and args.variant in ("auto", "tensor"):
-        # the tensor path for the other bf16 problems: the local term and the reverse scan on the
-        # tensor cores (bf16 intermediates), the per-chunk stages on the CUDA cores
+        # a per-key-dim gate: every stage on the tensor cores (bf16 intermediates); the CUDA-core
+        # per-chunk stages run over the chunks the tensor-core one flags (with this workload's gate
+        # none is, and their CTAs return at once)
+        tinv = torch.empty(B, NT, H, C, C, device=dev, dtype=q.dtype)
+        flags = torch.empty(B, NT, H, device=dev, dtype=torch.int32)
         dv_loc16 = torch.empty(B, T, H, V, device=dev, dtype=q.dtype)
         dh_ckpt16 = torch.empty(B, NT, H, K, V, device=dev, dtype=q.dtype)
         dv_new16 = torch.empty(B, T, H, V, device=dev, dtype=q.dtype)
-        names = ["prepare", "rescan", "dv_local", "scan_dh", "dqkwg", "wy"]
-        calls = [lambda: gdr.gdr_prepare_wy(p, k, v, g, beta, w, u, g_cum),
+        names = ["prepare", "rescan", "dv_local", "scan_dh", "wy_dqkg", "dqkwg_flagged", "wy_flagged"]
+        calls = [lambda: gdr.gdr_bwd_prepare(p, q, k, v, g, beta, w, u, g_cum, None, tinv),
                  lambda: gdr.gdr_scan_h(p, k, w, u, g_cum, h0, h_ckpt, v_new, None),
                  lambda: gdr.gdr_bwd_dv_local_tc(p, q, k, g_cum, d_o, dv_loc16),
                  lambda: gdr.gdr_bwd_scan_dh_tc(p, q, k, w, g_cum, dv_loc16, d_o, dhf, dh_ckpt16, dv_new16, dh0),
+                 lambda: gdr.gdr_bwd_wy_dqkg(p, q, k, v, beta, g_cum, w, u, tinv, v_new, h_ckpt, d_o, dv_new16,
+                                             dh_ckpt16, dq, dk, dv, dbeta, dg, flags),
                  lambda: gdr.gdr_bwd_dqkwg(p, q, k, v_new, g_cum, h_ckpt, dh_ckpt16, d_o, dv_new16, dq, dk_part, dw,
-                                           dG_part),
-                 lambda: gdr.gdr_bwd_wy(p, k, v, beta, g_cum, dw, dv_new16, dk_part, dG_part, dk, dv, dbeta, dg)]
+                                           dG_part, flags),
+                 lambda: gdr.gdr_bwd_wy(p, k, v, beta, g_cum, dw, dv_new16, dk_part, dG_part, dk, dv, dbeta, dg,
+                                        flags)]
     else:
         names = ["prepare", "rescan", "dv_local", "scan_dh", "dqkwg", "wy"]
         calls = [lambda: gdr.gdr_prepare_wy(p, k, v, g, beta, w, u, g_cum),

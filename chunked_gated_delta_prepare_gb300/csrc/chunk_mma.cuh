@@ -60,6 +60,18 @@ __device__ __forceinline__ void each(float (&acc)[NCW][2][4], int rb, int cb0, i
             for (int e = 0; e < 4; ++e) f(16 * rb + g4 + 8 * (e >> 1), 16 * (cb0 + j) + 8 * n + 2 * q4 + (e & 1), acc[j][n][e]);
 }
 
+// Calls f(j, n, e, row, col) for every element index of a warp's tiles, for epilogues over several
+// accumulators with the same tiling.
+template <int NCW, typename F>
+__device__ __forceinline__ void each_at(int rb, int cb0, int g4, int q4, F&& f) {
+#pragma unroll
+    for (int j = 0; j < NCW; ++j)
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) f(j, n, e, 16 * rb + g4 + 8 * (e >> 1), 16 * (cb0 + j) + 8 * n + 2 * q4 + (e & 1));
+}
+
 // rows x D bf16 from global rows of stride gs elements into shared [rows][D + 8]; rows >= nrows read as
 // zero.  Asynchronous 16-byte copies (cp.async), so every copy of a phase is in flight at once; the
 // caller waits with cp_async_wait_all() and a barrier.

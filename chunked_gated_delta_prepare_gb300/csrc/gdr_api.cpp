@@ -144,11 +144,13 @@ StagedWorkspace plan_staged(const gdr::Dims& d, bool fused) {
 // gdr_backward scratch: the forward's g_cum, w, u, v_new, h_ckpt (io dtype), then the
 // backward's fp32 intermediates, each 256-byte aligned.
 struct BackwardWorkspace {
-    size_t g_cum, w, u, v_new, h_ckpt, dv_loc, dv_new, dh_ckpt, dk_part, dw, dG_part, P, tinv, dq_v, dk_v, total;
+    size_t g_cum, w, u, v_new, h_ckpt, dv_loc, dv_new, dh_ckpt, dk_part, dw, dG_part, P, tinv, flags, dq_v, dk_v,
+        total;
 };
 
-// The backward's paths: the CUDA-core stages after a re-scan on the CUDA cores (SIMT) or on
-// the tensor cores (TENSOR), or every step on the tensor cores (FAST: bf16, scalar gate, C = 64).
+// The backward's paths: every stage on the CUDA cores (SIMT); every stage on the tensor cores for a
+// scalar gate (FAST: bf16); the same for a per-key-dim gate with the CUDA-core per-chunk stages
+// finishing the chunks whose gate the split-gate products cannot take (TENSOR: bf16).
 enum class BwdPath { Simt, Tensor, Fast };
 
 BackwardWorkspace plan_backward(const gdr::Dims& d, BwdPath path) {
@@ -171,10 +173,14 @@ BackwardWorkspace plan_backward(const gdr::Dims& d, BwdPath path) {
         if (d.C == 64) take(&ws.P, tiles * 2);
         else take(&ws.dv_loc, rows * d.V * 2);
         take(&ws.tinv, tiles * 2);
-    } else if (path == BwdPath::Tensor) {   // bf16 dv_loc, v' and state gradients; fp32 per-chunk partials
+    } else if (path == BwdPath::Tensor) {
+        // bf16 dv_loc, v' and state gradients; T; the per-chunk flags and the fp32 partials of the chunks the
+        // CUDA cores finish
         take(&ws.dv_loc, rows * d.V * 2);
         take(&ws.dv_new, rows * d.V * 2);
         take(&ws.dh_ckpt, states * 2);
+        take(&ws.tinv, tiles * 2);
+        take(&ws.flags, (size_t)d.B * d.NT * d.H * 4);
         take(&ws.dk_part, rows * d.K * 4);
         take(&ws.dw, rows * d.K * 4);
         take(&ws.dG_part, rows * gw * 4);
@@ -359,7 +365,7 @@ gdr_status gdr_bwd_scan_dh(const gdr_problem* p, const void* q, const void* k, c
 
 gdr_status gdr_bwd_dqkwg(const gdr_problem* p, const void* q, const void* k, const void* v_new, const float* g_cum,
                          const void* h_ckpt, const void* dh_ckpt, const void* d_o, const void* dv_new, void* dq,
-                         float* dk_part, float* dw, float* dG_part, void* stream) {
+                         float* dk_part, float* dw, float* dG_part, const int* only, void* stream) {
     gdr::Dims d;
     gdr_status st = check_problem(p, &d);
     if (st != GDR_OK) return st;
@@ -368,14 +374,14 @@ gdr_status gdr_bwd_dqkwg(const gdr_problem* p, const void* q, const void* k, con
     // the tensor path's intermediates (bf16 io, variants other than SIMT) are bf16
     const bool inter16 = d.bf16 && p->variant != GDR_VARIANT_SIMT;
     st = from_cuda(gdr::simt_bwd_dqkwg(d, q, k, v_new, g_cum, h_ckpt, dh_ckpt, d_o, dv_new, dq, dk_part, dw,
-                                       dG_part, (cudaStream_t)stream, inter16));
+                                       dG_part, (cudaStream_t)stream, inter16, only));
     if (st == GDR_OK) t_last_variant = "simt";
     return st;
 }
 
 gdr_status gdr_bwd_wy(const gdr_problem* p, const void* k, const void* v, const void* beta, const float* g_cum,
                       const float* dw, const void* dv_new, const float* dk_part, const float* dG_part, void* dk,
-                      void* dv, void* dbeta, float* dg, void* stream) {
+                      void* dv, void* dbeta, float* dg, const int* only, void* stream) {
     gdr::Dims d;
     gdr_status st = check_problem(p, &d);
     if (st != GDR_OK) return st;
@@ -383,7 +389,7 @@ gdr_status gdr_bwd_wy(const gdr_problem* p, const void* k, const void* v, const 
         return st;
     const bool inter16 = d.bf16 && p->variant != GDR_VARIANT_SIMT;
     st = from_cuda(gdr::simt_bwd_wy(d, k, v, beta, g_cum, dw, dv_new, dk_part, dG_part, dk, dv, dbeta, dg,
-                                    (cudaStream_t)stream, inter16));
+                                    (cudaStream_t)stream, inter16, only));
     if (st == GDR_OK) t_last_variant = "simt";
     return st;
 }
@@ -420,7 +426,7 @@ gdr_status gdr_bwd_prepare(const gdr_problem* p, const void* q, const void* k, c
     gdr_status st = check_problem(p, &d);
     if (st != GDR_OK) return st;
     if ((st = check_ptrs({q, k, v, g, beta, w, u, g_cum, tinv}, {P})) != GDR_OK) return st;
-    if (p->variant == GDR_VARIANT_SIMT || !d.bf16 || d.per_k || (P && d.C != 64)) return GDR_ERR_UNSUPPORTED;
+    if (p->variant == GDR_VARIANT_SIMT || !d.bf16 || (P && (d.per_k || d.C != 64))) return GDR_ERR_UNSUPPORTED;
     st = from_cuda(gdr::mma_prepare(d, k, v, g, beta, w, u, g_cum, (cudaStream_t)stream, device_error_word(),
                                     P ? q : nullptr, P, tinv));
     if (st == GDR_OK) t_last_variant = "tensor";
@@ -444,16 +450,23 @@ gdr_status gdr_bwd_scan_dh_p(const gdr_problem* p, const void* q, const void* k,
 gdr_status gdr_bwd_wy_dqkg(const gdr_problem* p, const void* q, const void* k, const void* v, const void* beta,
                            const float* g_cum, const void* w, const void* u, const void* tinv, const void* v_new,
                            const void* h_ckpt, const void* d_o, const void* dv_new, const void* dh_ckpt, void* dq,
-                           void* dk, void* dv, void* dbeta, float* dg, void* stream) {
+                           void* dk, void* dv, void* dbeta, float* dg, int* exact_flags, void* stream) {
     gdr::Dims d;
     gdr_status st = check_problem(p, &d);
     if (st != GDR_OK) return st;
     if ((st = check_ptrs({q, k, v, beta, g_cum, w, u, tinv, v_new, h_ckpt, d_o, dv_new, dh_ckpt, dq, dk, dv, dbeta,
                           dg}, {})) != GDR_OK)
         return st;
-    if (p->variant == GDR_VARIANT_SIMT || !d.bf16 || d.per_k) return GDR_ERR_UNSUPPORTED;
-    st = from_cuda(gdr::mma_bwd_chunk(d, q, k, v, beta, g_cum, w, u, tinv, v_new, h_ckpt, d_o, dv_new, dh_ckpt, dq, dk,
-                                      dv, dbeta, dg, (cudaStream_t)stream));
+    if (p->variant == GDR_VARIANT_SIMT || !d.bf16) return GDR_ERR_UNSUPPORTED;
+    if (d.per_k) {
+        if (!exact_flags) return GDR_ERR_NULL;
+        if ((reinterpret_cast<uintptr_t>(exact_flags) & 3u) != 0) return GDR_ERR_ALIGN;
+        st = from_cuda(gdr::mma_bwd_chunk_kda(d, q, k, v, beta, g_cum, w, u, tinv, v_new, h_ckpt, d_o, dv_new,
+                                              dh_ckpt, dq, dk, dv, dbeta, dg, exact_flags, (cudaStream_t)stream));
+    } else {
+        st = from_cuda(gdr::mma_bwd_chunk(d, q, k, v, beta, g_cum, w, u, tinv, v_new, h_ckpt, d_o, dv_new, dh_ckpt, dq,
+                                          dk, dv, dbeta, dg, (cudaStream_t)stream));
+    }
     if (st == GDR_OK) t_last_variant = "tensor";
     return st;
 }
@@ -544,19 +557,27 @@ gdr_status gdr_backward(const gdr_problem* p, const void* q, const void* k, cons
     }
     // forward prepare and re-scan: G, w, u, the checkpoints and v'
     if (tensor) {
+        // a per-key-dim gate: prepare (+ T), re-scan, local term, reverse scan and the per-chunk stage on the
+        // tensor cores; the CUDA-core per-chunk stages finish the chunks that stage flags
         unsigned int* err = device_error_word();
-        if ((st = from_cuda(gdr::mma_prepare(d, k, v, g, beta, w, u, g_cum, s, err))) != GDR_OK) return st;
+        void* tinv = base + ws.tinv;
+        int* flags = reinterpret_cast<int*>(base + ws.flags);
+        if ((st = from_cuda(gdr::mma_prepare(d, k, v, g, beta, w, u, g_cum, s, err, nullptr, nullptr, tinv))) !=
+            GDR_OK)
+            return st;
         if ((st = from_cuda(gdr::mma_scan(d, k, w, u, g_cum, h0, h_ckpt, v_new, nullptr, s, err))) != GDR_OK) return st;
-        // the local term and the reverse scan on the tensor cores; the per-chunk stages on the CUDA cores
         if ((st = from_cuda(gdr::mma_bwd_dv_local(d, q, k, g_cum, d_o, dv_loc, s))) != GDR_OK) return st;
         if ((st = from_cuda(gdr::mma_bwd_scan_dl(d, q, k, w, g_cum, dv_loc, d_o, dh_final, dh_ckpt, dv_new, dh0, s,
                                                  err))) != GDR_OK)
             return st;
+        if ((st = from_cuda(gdr::mma_bwd_chunk_kda(d, q, k, v, beta, g_cum, w, u, tinv, v_new, h_ckpt, d_o, dv_new,
+                                                   dh_ckpt, dq, dk, dv, dbeta, dg, flags, s))) != GDR_OK)
+            return st;
         if ((st = from_cuda(gdr::simt_bwd_dqkwg(d, q, k, v_new, g_cum, h_ckpt, dh_ckpt, d_o, dv_new, dq, dk_part, dw,
-                                                dG_part, s, true))) != GDR_OK)
+                                                dG_part, s, true, flags))) != GDR_OK)
             return st;
         if ((st = from_cuda(gdr::simt_bwd_wy(d, k, v, beta, g_cum, dw, dv_new, dk_part, dG_part, dk, dv, dbeta, dg, s,
-                                             true))) != GDR_OK)
+                                             true, flags))) != GDR_OK)
             return st;
         if (d.G > 1 && (st = from_cuda(gdr::group_sum_heads(d, dq, dk, dq_out, dk_out, s))) != GDR_OK) return st;
         t_last_variant = "tensor";

@@ -52,13 +52,17 @@ cudaError_t simt_bwd_dv_local(const Dims& d, const void* q, const void* k, const
 cudaError_t simt_bwd_scan_dh(const Dims& d, const void* q, const void* k, const void* w, const float* g_cum,
                              const void* d_o, const float* dv_loc, const float* dh_final, float* dh_ckpt,
                              float* dv_new, float* dh0, cudaStream_t s);
-// inter16: dh_ckpt and dv_new (du) are in the io dtype (from the tensor-core reverse scan), else fp32
+// inter16: dh_ckpt and dv_new (du) are in the io dtype (from the tensor-core reverse scan), else fp32.
+// only: NULL, or per-chunk flags [B][NT][H]; a chunk whose flag is 0 is skipped (the tensor-core
+// per-chunk stage for a per-key gate flags the chunks it leaves to these two).
 cudaError_t simt_bwd_dqkwg(const Dims& d, const void* q, const void* k, const void* v_new, const float* g_cum,
                            const void* h_ckpt, const void* dh_ckpt, const void* d_o, const void* dv_new,
-                           void* dq, float* dk_part, float* dw, float* dG_part, cudaStream_t s, bool inter16 = false);
+                           void* dq, float* dk_part, float* dw, float* dG_part, cudaStream_t s, bool inter16 = false,
+                           const int* only = nullptr);
 cudaError_t simt_bwd_wy(const Dims& d, const void* k, const void* v, const void* beta, const float* g_cum,
                         const float* dw, const void* du, const float* dk_part, const float* dG_part, void* dk,
-                        void* dv, void* dbeta, float* dg, cudaStream_t s, bool inter16 = false);
+                        void* dv, void* dbeta, float* dg, cudaStream_t s, bool inter16 = false,
+                        const int* only = nullptr);
 
 // grouped value heads: dq, dk [B,T,Hk,K] = sums over each group of dq_v, dk_v [B,T,H,K] (io dtype)
 cudaError_t group_sum_heads(const Dims& d, const void* dq_v, const void* dk_v, void* dq, void* dk, cudaStream_t s);
@@ -82,6 +86,13 @@ cudaError_t mma_bwd_chunk(const Dims& d, const void* q, const void* k, const voi
                           const float* g_cum, const void* w, const void* u, const void* tinv, const void* v_new,
                           const void* h_ckpt, const void* d_o, const void* dv_new, const void* dh_ckpt, void* dq,
                           void* dk, void* dv, void* dbeta, float* dg, cudaStream_t s);
+// The same stage for a per-key-dim gate (bf16 io, C = 32 or 64).  exact_flags [B][NT][H]: set to 1 for a
+// chunk whose gate moves more than the kernel's exponent bound from the chunk's middle row (nothing of that
+// chunk is written; simt_bwd_dqkwg and simt_bwd_wy with only = exact_flags complete it), else 0.
+cudaError_t mma_bwd_chunk_kda(const Dims& d, const void* q, const void* k, const void* v, const void* beta,
+                              const float* g_cum, const void* w, const void* u, const void* tinv, const void* v_new,
+                              const void* h_ckpt, const void* d_o, const void* dv_new, const void* dh_ckpt, void* dq,
+                              void* dk, void* dv, void* dbeta, float* dg, int* exact_flags, cudaStream_t s);
 
 // ---- device error word (device_status.cu)
 // Bounded waits in kernels write a nonzero code here instead of trapping.

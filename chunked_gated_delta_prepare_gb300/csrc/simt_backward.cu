@@ -199,7 +199,8 @@ __global__ void __launch_bounds__(kThreads)
 bwd_dqkwg_kernel(Dims d, const IO* __restrict__ q, const IO* __restrict__ k, const IO* __restrict__ v_new,
                  const float* __restrict__ g_cum, const IO* __restrict__ h_ckpt, const IT* __restrict__ dh_ckpt,
                  const IO* __restrict__ d_o, const IT* __restrict__ dv_new, IO* __restrict__ dq,
-                 float* __restrict__ dk_part, float* __restrict__ dw, float* __restrict__ dG_part) {
+                 float* __restrict__ dk_part, float* __restrict__ dw, float* __restrict__ dG_part,
+                 const int* __restrict__ only) {
     extern __shared__ float smem[];
     constexpr int KT = kTile, KTP = kTile + 1;
     const int C = d.C, K = d.K, V = d.V, H = d.H;
@@ -223,6 +224,7 @@ bwd_dqkwg_kernel(Dims d, const IO* __restrict__ q, const IO* __restrict__ k, con
     auto row = [&](int t) { return (tok0 + t) * H + h; };
     auto krow = [&](int t) { return (tok0 + t) * d.Hk + h / d.G; };   // q, k: q/k head h / G
     const int64_t ck = (((int64_t)b * d.NT + c) * H + h) * K * V;
+    if (only && !only[((int64_t)b * d.NT + c) * H + h]) return;   // a chunk another stage has done
 
     for (int i = tid; i < C * V; i += kThreads) {
         const int t = i / V, x = i % V;
@@ -315,7 +317,7 @@ __global__ void __launch_bounds__(kThreads)
 bwd_wy_kernel(Dims d, const IO* __restrict__ k, const IO* __restrict__ v, const IO* __restrict__ beta,
               const float* __restrict__ g_cum, const float* __restrict__ dw, const IT* __restrict__ du,
               const float* __restrict__ dk_part, const float* __restrict__ dG_part, IO* __restrict__ dk,
-              IO* __restrict__ dv, IO* __restrict__ dbeta, float* __restrict__ dg) {
+              IO* __restrict__ dv, IO* __restrict__ dbeta, float* __restrict__ dg, const int* __restrict__ only) {
     extern __shared__ float smem[];
     constexpr int KT = kTile, KTP = kTile + 1;
     const int C = d.C, K = d.K, V = d.V, H = d.H;
@@ -338,6 +340,7 @@ bwd_wy_kernel(Dims d, const IO* __restrict__ k, const IO* __restrict__ v, const 
     const int nv = min(C, d.T - c * C);
     auto row = [&](int t) { return (tok0 + t) * H + h; };
     auto krow = [&](int t) { return (tok0 + t) * d.Hk + h / d.G; };   // q, k: q/k head h / G
+    if (only && !only[((int64_t)b * d.NT + c) * H + h]) return;   // a chunk another stage has done
 
     for (int i = tid; i < C * K; i += kThreads) ks[(i / K) * KP + i % K] = i / K < nv ? ld(k, krow(i / K) * K + i % K) : 0.f;
     for (int i = tid; i < C * GW; i += kThreads) Gs[i] = g_cum[row(min(i / GW, nv - 1)) * GW + i % GW];
@@ -573,7 +576,8 @@ cudaError_t simt_bwd_scan_dh(const Dims& d, const void* q, const void* k, const 
 
 cudaError_t simt_bwd_dqkwg(const Dims& d, const void* q, const void* k, const void* v_new, const float* g_cum,
                            const void* h_ckpt, const void* dh_ckpt, const void* d_o, const void* dv_new,
-                           void* dq, float* dk_part, float* dw, float* dG_part, cudaStream_t s, bool inter16) {
+                           void* dq, float* dk_part, float* dw, float* dG_part, cudaStream_t s, bool inter16,
+                           const int* only) {
     const size_t C = d.C, V = d.V;
     const size_t smem = sizeof(float) * (3 * C * (V + 1) + C * (C + 1) + 2 * (size_t)kTile * (V + 1) +
                                          5 * C * (kTile + 1) + C);
@@ -585,7 +589,7 @@ cudaError_t simt_bwd_dqkwg(const Dims& d, const void* q, const void* k, const vo
         if (e != cudaSuccess) return e;                                                                      \
         kern<<<grid, kThreads, smem, s>>>(d, (const IO*)q, (const IO*)k, (const IO*)v_new, g_cum,            \
                                           (const IO*)h_ckpt, (const IT*)dh_ckpt, (const IO*)d_o,             \
-                                          (const IT*)dv_new, (IO*)dq, dk_part, dw, dG_part);                 \
+                                          (const IT*)dv_new, (IO*)dq, dk_part, dw, dG_part, only);           \
     } while (0)
 #define LAUNCH(IO, PK)                                                                                       \
     do {                                                                                                     \
@@ -599,7 +603,7 @@ cudaError_t simt_bwd_dqkwg(const Dims& d, const void* q, const void* k, const vo
 
 cudaError_t simt_bwd_wy(const Dims& d, const void* k, const void* v, const void* beta, const float* g_cum,
                         const float* dw, const void* du, const float* dk_part, const float* dG_part, void* dk,
-                        void* dv, void* dbeta, float* dg, cudaStream_t s, bool inter16) {
+                        void* dv, void* dbeta, float* dg, cudaStream_t s, bool inter16, const int* only) {
     const size_t C = d.C, K = d.K, GW = d.per_k ? d.K : 1;
     const size_t smem = sizeof(float) * (C * (K + 1) + C * GW + C + 4 * C * (C + 1) + 3 * C * (kTile + 1) + 2 * C);
     const dim3 grid(d.NT, d.H, d.B);
@@ -609,7 +613,8 @@ cudaError_t simt_bwd_wy(const Dims& d, const void* k, const void* v, const void*
         cudaError_t e = allow_smem(kern, smem);                                                              \
         if (e != cudaSuccess) return e;                                                                      \
         kern<<<grid, kThreads, smem, s>>>(d, (const IO*)k, (const IO*)v, (const IO*)beta, g_cum, dw,         \
-                                          (const IT*)du, dk_part, dG_part, (IO*)dk, (IO*)dv, (IO*)dbeta, dg); \
+                                          (const IT*)du, dk_part, dG_part, (IO*)dk, (IO*)dv, (IO*)dbeta, dg, \
+                                          only);                                                             \
     } while (0)
 #define LAUNCH(IO, PK)                                                                                       \
     do {                                                                                                     \

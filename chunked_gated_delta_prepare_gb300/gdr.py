@@ -79,13 +79,13 @@ def load(path: str | None = None):
             "gdr_forward_workspace_bytes": [P],
             "gdr_bwd_dv_local": [P, vp, vp, vp, vp, vp, vp],
             "gdr_bwd_scan_dh": [P] + [vp] * 11,
-            "gdr_bwd_dqkwg": [P] + [vp] * 13,
-            "gdr_bwd_wy": [P] + [vp] * 13,
+            "gdr_bwd_dqkwg": [P] + [vp] * 14,
+            "gdr_bwd_wy": [P] + [vp] * 14,
             "gdr_backward": [P] + [vp] * 15 + [ctypes.c_size_t, vp],
             "gdr_backward_workspace_bytes": [P],
             "gdr_bwd_prepare": [P] + [vp] * 11,
             "gdr_bwd_scan_dh_p": [P] + [vp] * 11,
-            "gdr_bwd_wy_dqkg": [P] + [vp] * 19,
+            "gdr_bwd_wy_dqkg": [P] + [vp] * 20,
             "gdr_bwd_group_sum": [P] + [vp] * 5,
             "gdr_bwd_dv_local_tc": [P] + [vp] * 6,
             "gdr_bwd_scan_dh_tc": [P] + [vp] * 11,
@@ -258,15 +258,16 @@ def gdr_bwd_scan_dh(p, q, k, w, g_cum, d_o, dv_loc, dh_final, dh_ckpt, dv_new, d
                                   _stream(stream)), "gdr_bwd_scan_dh")
 
 
-def gdr_bwd_dqkwg(p, q, k, v_new, g_cum, h_ckpt, dh_ckpt, d_o, dv_new, dq, dk_part, dw, dG_part, stream=None):
+def gdr_bwd_dqkwg(p, q, k, v_new, g_cum, h_ckpt, dh_ckpt, d_o, dv_new, dq, dk_part, dw, dG_part, only=None,
+                  stream=None):
     _check(load().gdr_bwd_dqkwg(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v_new), _ptr(g_cum), _ptr(h_ckpt),
                                 _ptr(dh_ckpt), _ptr(d_o), _ptr(dv_new), _ptr(dq), _ptr(dk_part), _ptr(dw),
-                                _ptr(dG_part), _stream(stream)), "gdr_bwd_dqkwg")
+                                _ptr(dG_part), _ptr(only), _stream(stream)), "gdr_bwd_dqkwg")
 
 
-def gdr_bwd_wy(p, k, v, beta, g_cum, dw, dv_new, dk_part, dG_part, dk, dv, dbeta, dg, stream=None):
+def gdr_bwd_wy(p, k, v, beta, g_cum, dw, dv_new, dk_part, dG_part, dk, dv, dbeta, dg, only=None, stream=None):
     _check(load().gdr_bwd_wy(ctypes.byref(p), _ptr(k), _ptr(v), _ptr(beta), _ptr(g_cum), _ptr(dw), _ptr(dv_new),
-                             _ptr(dk_part), _ptr(dG_part), _ptr(dk), _ptr(dv), _ptr(dbeta), _ptr(dg),
+                             _ptr(dk_part), _ptr(dG_part), _ptr(dk), _ptr(dv), _ptr(dbeta), _ptr(dg), _ptr(only),
                              _stream(stream)), "gdr_bwd_wy")
 
 
@@ -282,11 +283,11 @@ def gdr_bwd_scan_dh_p(p, q, k, w, g_cum, P, d_o, dh_final, dh_ckpt, dv_new, dh0,
 
 
 def gdr_bwd_wy_dqkg(p, q, k, v, beta, g_cum, w, u, tinv, v_new, h_ckpt, d_o, dv_new, dh_ckpt, dq, dk, dv, dbeta, dg,
-                    stream=None):
+                    exact_flags=None, stream=None):
     _check(load().gdr_bwd_wy_dqkg(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g_cum), _ptr(w),
                                   _ptr(u), _ptr(tinv), _ptr(v_new), _ptr(h_ckpt), _ptr(d_o), _ptr(dv_new),
                                   _ptr(dh_ckpt), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbeta), _ptr(dg),
-                                  _stream(stream)), "gdr_bwd_wy_dqkg")
+                                  _ptr(exact_flags), _stream(stream)), "gdr_bwd_wy_dqkg")
 
 
 def gdr_bwd_dv_local_tc(p, q, k, g_cum, d_o, dv_loc, stream=None):

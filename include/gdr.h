@@ -261,9 +261,11 @@ GDR_API gdr_status gdr_forward_static_scratch(const gdr_problem* p, const void* 
  *   gdr_bwd_dv_local_tc and gdr_bwd_scan_dh_tc, then gdr_bwd_wy_dqkg; bf16
  *   intermediates): bf16 io with a scalar gate, which variants AUTO and TENSOR
  *   take.
- * - For a per-key-dim gate with bf16 io, AUTO and TENSOR run the local term and
- *   the reverse scan on the tensor cores (gdr_bwd_dv_local_tc,
- *   gdr_bwd_scan_dh_tc) and the per-chunk stages on the CUDA cores.
+ * - For a per-key-dim gate with bf16 io, AUTO and TENSOR run gdr_bwd_prepare,
+ *   gdr_bwd_dv_local_tc, gdr_bwd_scan_dh_tc and gdr_bwd_wy_dqkg on the tensor
+ *   cores.  The last leaves a chunk whose gate moves too far within it for the
+ *   split-gate products to gdr_bwd_dqkwg and gdr_bwd_wy (argument only), which
+ *   compute that chunk exactly in fp32.
  * The variant FUSED is not offered here (GDR_ERR_UNSUPPORTED).
  */
 
@@ -283,6 +285,9 @@ GDR_API gdr_status gdr_bwd_scan_dh(const gdr_problem* p, const void* q, const vo
                                    const float* g_cum, const void* d_o, const float* dv_loc,
                                    const float* dh_final, float* dh_ckpt, float* dv_new, float* dh0, void* stream);
 
+/* only: NULL (every chunk), or flags [B,NT,H] int32 as gdr_bwd_wy_dqkg writes them: gdr_bwd_dqkwg and
+ * gdr_bwd_wy then compute, and write, only the chunks whose flag is nonzero. */
+
 /* Per chunk, with h = h_ckpt[c], dhn = dh_ckpt[c], dqg = scale do h^T,
  * dQ~ = scale tril_0(do v'^T), dkg = v' dhn^T, kg = k exp(G_L - G):
  *     dq      = dqg exp(G) + L(dQ~, k)                                 (io; final)
@@ -295,7 +300,7 @@ GDR_API gdr_status gdr_bwd_scan_dh(const gdr_problem* p, const void* q, const vo
 GDR_API gdr_status gdr_bwd_dqkwg(const gdr_problem* p, const void* q, const void* k, const void* v_new,
                                  const float* g_cum, const void* h_ckpt, const void* dh_ckpt, const void* d_o,
                                  const void* dv_new, void* dq, float* dk_part, float* dw, float* dG_part,
-                                 void* stream);
+                                 const int* only, void* stream);
 
 /* The WY backward, with (I + A)^{-1} rebuilt from k, beta, g_cum and du = dv_new:
  *     dkb = Tinv^T dw, dvb = Tinv^T du, dA = strict_lower(-Tinv^T (dw kb^T + du vb^T) Tinv^T),
@@ -307,17 +312,18 @@ GDR_API gdr_status gdr_bwd_dqkwg(const gdr_problem* p, const void* q, const void
  * Inputs k, v, beta io; g_cum, dw, dk_part, dG_part fp32; dv_new fp32 (see below). */
 GDR_API gdr_status gdr_bwd_wy(const gdr_problem* p, const void* k, const void* v, const void* beta,
                               const float* g_cum, const float* dw, const void* dv_new, const float* dk_part,
-                              const float* dG_part, void* dk, void* dv, void* dbeta, float* dg, void* stream);
+                              const float* dG_part, void* dk, void* dv, void* dbeta, float* dg, const int* only,
+                              void* stream);
 
 /* dh_ckpt and dv_new of gdr_bwd_dqkwg and gdr_bwd_wy are fp32 (as gdr_bwd_scan_dh writes them), or,
  * for bf16 io with a variant other than SIMT, bf16 (as gdr_bwd_scan_dh_tc and gdr_bwd_scan_dh_p
  * write them). */
 
-/* The tensor-core stages (bf16 io, scalar gate; GDR_ERR_UNSUPPORTED otherwise). */
+/* The tensor-core stages (bf16 io; GDR_ERR_UNSUPPORTED otherwise). */
 
 /* gdr_prepare_wyp plus T = (I + A)^{-1} of every chunk: tinv [B,NT,H,C,C] bf16, row i of chunk c
  * holding row i of T.  Other arguments as gdr_prepare_wyp; P may be NULL (not written), and must
- * be for C = 32. */
+ * be for C = 32 or a per-key-dim gate (q is then unused). */
 GDR_API gdr_status gdr_bwd_prepare(const gdr_problem* p, const void* q, const void* k, const void* v, const float* g,
                                    const void* beta, void* w, void* u, float* g_cum, void* P, void* tinv,
                                    void* stream);
@@ -332,13 +338,17 @@ GDR_API gdr_status gdr_bwd_scan_dh_p(const gdr_problem* p, const void* q, const 
 /* gdr_bwd_dqkwg and gdr_bwd_wy in one pass per chunk (the pages' wy_dqkg), T read from tinv
  * instead of rebuilt; the WY term of dA is -(dkb w^T + dvb u^T), which equals
  * -Tinv^T (dw kb^T + du vb^T) Tinv^T because w = Tinv kb and u = Tinv vb.
+ * A per-key-dim gate enters every C x C product through q exp(G - G_ref), k exp(G_ref - G) and
+ * k exp(G - G_ref), G_ref the chunk's middle row; exact_flags [B,NT,H] int32 (required for that gate,
+ * ignored for a scalar one) gets 1 for a chunk whose gate moves more than 40 from that row (nothing
+ * of it written: gdr_bwd_dqkwg and gdr_bwd_wy with only = exact_flags do it), else 0.
  * Inputs q, k, v, beta, w, u, tinv, v_new, h_ckpt, do, dv_new, dh_ckpt bf16; g_cum fp32.
  * Outputs dq, dk, dv, dbeta bf16; dg fp32. */
 GDR_API gdr_status gdr_bwd_wy_dqkg(const gdr_problem* p, const void* q, const void* k, const void* v,
                                    const void* beta, const float* g_cum, const void* w, const void* u,
                                    const void* tinv, const void* v_new, const void* h_ckpt, const void* d_o,
                                    const void* dv_new, const void* dh_ckpt, void* dq, void* dk, void* dv,
-                                   void* dbeta, float* dg, void* stream);
+                                   void* dbeta, float* dg, int* exact_flags, void* stream);
 
 /* The local term and the reverse scan on the tensor cores for the problems the fused per-chunk
  * stage does not take (a per-key-dim gate, or C = 32); bf16 io, GDR_ERR_UNSUPPORTED otherwise.

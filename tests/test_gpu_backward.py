@@ -287,9 +287,13 @@ def test_stage_wy(shape, per_k, dtype):
 FAST_SHAPES = [(2, 128, 3, 64, 64, 64), (1, 192, 2, 128, 128, 64), (2, 100, 2, 128, 64, 64), (1, 256, 1, 64, 128, 64)]
 
 
-def _fast_setup(shape, seed):
+def _fast_setup(shape, seed, per_k=False, strong_head=None):
     B, T, H, K, V, C = shape
-    x = make_inputs(B, T, H, K, V, io_dtype=torch.bfloat16, with_h0=True, seed=seed)
+    x = make_inputs(B, T, H, K, V, per_k_gate=per_k, io_dtype=torch.bfloat16, with_h0=True, seed=seed)
+    if strong_head is not None:   # one head's gate 100 times stronger: its chunks span far more than e^40
+        g = x.g.clone()
+        g[:, :, strong_head] *= 100.0
+        x = GdrInputs(q=x.q, k=x.k, v=x.v, g=g, beta=x.beta, h0=x.h0)
     do, dhf = upstream(x, seed + 1)
     full = cb.backward_chunked(x.q, x.k, x.v, x.g, x.beta, x.h0 * 20, do, dhf, C, 0.125)
     p = gdr.problem_for(x.q, x.v, x.g, C, scale=0.125, variant="tensor")
@@ -344,9 +348,10 @@ def test_tensor_stage_wy_dqkg(shape):
     _wy_dqkg_case(shape)
 
 
-def _wy_dqkg_case(shape):
-    x, do, _, full, p = _fast_setup(shape, 74)
+def _wy_dqkg_case(shape, per_k=False, strong_head=None):
+    x, do, _, full, p = _fast_setup(shape, 74, per_k, strong_head)
     B, T, H, K, V, C = shape
+    NT = -(-T // C)
     bf = torch.bfloat16
     G_r = rounded(full["G"], torch.float32)
     w_r, u_r, vn_r, hc_r = (rounded(full[n], bf) for n in ("w", "u", "v_new", "h_ckpt"))
@@ -360,15 +365,32 @@ def _wy_dqkg_case(shape):
                                                                                    dtype=bf), \
         torch.full(x.v.shape, nan, device="cuda", dtype=bf)
     dbeta, dg = torch.full(x.beta.shape, nan, device="cuda", dtype=bf), torch.full(x.g.shape, nan, device="cuda")
-    gdr.gdr_bwd_wy_dqkg(p, dev(x.q), dev(x.k), dev(x.v), dev(x.beta), dev(G_r), dev(w_r), dev(u_r), dev(tinv_r),
-                        dev(vn_r), dev(hc_r), dev(do), dev(dvn_r), dev(dhc_r), dq, dk, dv, dbeta, dg)
+    flags = torch.full((B, NT, H), -1, device="cuda", dtype=torch.int32) if per_k else None
+    args = [dev(x.q), dev(x.k), dev(x.v), dev(x.beta), dev(G_r), dev(w_r), dev(u_r), dev(tinv_r), dev(vn_r),
+            dev(hc_r), dev(do), dev(dvn_r), dev(dhc_r)]
+    gdr.gdr_bwd_wy_dqkg(p, *args, dq, dk, dv, dbeta, dg, flags)
+    if per_k:
+        torch.cuda.synchronize()
+        f = flags.cpu()
+        assert set(f.unique().tolist()) <= {0, 1}
+        if strong_head is None:
+            assert int(f.sum()) == 0
+        else:   # the strong head's chunks, and only they, go to the CUDA-core stages
+            assert int(f[:, :, strong_head].sum()) > 0 and int(f.sum()) == int(f[:, :, strong_head].sum())
+        # the flagged chunks, exactly in fp32 (the entry points read bf16 intermediates, variant tensor)
+        dk_part, dw = torch.empty(x.k.shape, device="cuda"), torch.empty(x.k.shape, device="cuda")
+        dG_part = torch.empty(x.g.shape, device="cuda")
+        gdr.gdr_bwd_dqkwg(p, dev(x.q), dev(x.k), dev(vn_r), dev(G_r), dev(hc_r), dev(dhc_r), dev(do), dev(dvn_r),
+                          dq, dk_part, dw, dG_part, flags)
+        gdr.gdr_bwd_wy(p, dev(x.k), dev(x.v), dev(x.beta), dev(G_r), dw, dev(dvn_r), dk_part, dG_part, dk, dv, dbeta,
+                       dg, flags)
     torch.cuda.synchronize()
     tol = STAGE_TOL["bf16"]
     assert scaled_err(dq, a["dq"]) <= tol
     assert scaled_err(dk, a["dk"] + y["dk"]) <= tol
     assert scaled_err(dv, y["dv"]) <= tol
     assert scaled_err(dbeta, y["dbeta"]) <= tol
-    assert scaled_err(dg, cb.reverse_cumsum(a["dG"] + y["dG"], C, False)) <= tol
+    assert scaled_err(dg, cb.reverse_cumsum(a["dG"] + y["dG"], C, per_k)) <= tol
 
 
 # ---------------------------------------------------------------- grouped value heads
@@ -452,3 +474,49 @@ def test_tensor_stage_reverse_scan_from_dv_local(shape, per_k):
 def test_tensor_stage_wy_dqkg_at_32_token_chunks(shape):
     # the same per-chunk stage at C = 32 (two 16-row blocks, warps sharing the columns four ways)
     _wy_dqkg_case(shape)
+
+
+KDA_STAGE_SHAPES = [(2, 128, 3, 64, 64, 64), (1, 192, 2, 128, 128, 64), (2, 100, 2, 128, 64, 64),
+                    (1, 256, 1, 64, 128, 64), (2, 128, 3, 64, 64, 32), (1, 96, 2, 128, 128, 32),
+                    (1, 77, 2, 128, 64, 32)]
+
+
+@pytest.mark.parametrize("shape", KDA_STAGE_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_tensor_stage_wy_dqkg_per_key_gate(shape):
+    # the per-key-dim gate's per-chunk stage: split-gate tiles around each chunk's middle row
+    _wy_dqkg_case(shape, per_k=True)
+
+
+@pytest.mark.parametrize("shape", KDA_STAGE_SHAPES[:3] + KDA_STAGE_SHAPES[5:], ids=lambda s: "x".join(map(str, s)))
+def test_tensor_stage_wy_dqkg_per_key_gate_flagged_chunks(shape):
+    # one head decays too fast for the split-gate products: its chunks are flagged and finished
+    # by the CUDA-core stages, the other heads' chunks are not touched by them
+    _wy_dqkg_case(shape, per_k=True, strong_head=0)
+
+
+@pytest.mark.parametrize("shape", [(1, 128, 3, 64, 64, 64), (2, 100, 2, 128, 128, 32)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_backward_per_key_gate_mixed_spread(shape):
+    # gdr_backward end to end with one head's chunks on the exact stages and the rest on the tensor cores
+    B, T, H, K, V, C = shape
+    x = make_inputs(B, T, H, K, V, per_k_gate=True, io_dtype=torch.bfloat16, with_h0=True, seed=98)
+    g = x.g.clone()
+    g[:, :, 1] *= 100.0
+    x = GdrInputs(q=x.q, k=x.k, v=x.v, g=g, beta=x.beta, h0=x.h0 * 20)
+    do, dhf = upstream(x, 99)
+    got, ran = gpu_backward(x, do, dhf, C, "tensor")
+    assert ran == "tensor"
+    ref = reference(x, do, dhf, C, 1.0 / np.sqrt(K))
+    for name in GRADS:
+        err = scaled_err(got[name], ref[name])
+        assert np.isfinite(err) and err <= BWD_TOL["bf16"], f"{name}: {err:.3e}"
+
+
+def test_wy_dqkg_per_key_gate_needs_its_flags():
+    x = make_inputs(1, 64, 1, 64, 64, per_k_gate=True, io_dtype=torch.bfloat16, seed=100)
+    p = gdr.problem_for(x.q, x.v, x.g, 64, variant="tensor")
+    t = torch.zeros(64, 1, 64, device="cuda", dtype=torch.bfloat16)
+    gf = torch.zeros(1, 64, 1, 64, device="cuda")
+    with pytest.raises(gdr.GdrError) as e:
+        gdr.gdr_bwd_wy_dqkg(p, t, t, t, t, gf, t, t, t, t, t, t, t, t, t, t, t, t, gf, None)
+    assert e.value.status == 1

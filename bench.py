@@ -54,7 +54,7 @@ def peaks():
 # for the state.  e = io bytes, GW = 4 (scalar gate) or 4K (per-key-dim gate).
 # with_p: the prepare also reads q and writes the gated scores P (C x C per
 # chunk, so C e bytes per token), which the fused scan/output kernel reads.
-def algorithmic_bytes(wl, kernel: str, with_p: bool = False) -> int:
+def algorithmic_bytes(wl, kernel: str, with_p: bool = False, segs: int = 1) -> int:
     e = 2 if wl.io == "bf16" else 4
     K, V, C = wl.K, wl.V, wl.chunk
     gw = 4 * (K if wl.per_k_gate else 1)
@@ -74,6 +74,11 @@ def algorithmic_bytes(wl, kernel: str, with_p: bool = False) -> int:
     if kernel == "scan_output":  # read q, k, w, u, g_cum (+ P); write o; state in and out
         per = 3 * K * e + 2 * V * e + gw + p_bytes
         return th * per + bh * state
+    if kernel == "transfer":     # read k, w, u, g_cum; write each segment's M [K,K] and Z [K,V] (fp32)
+        per = 2 * K * e + V * e + gw
+        return th * per + segs * bh * 4 * (K * K + K * V)
+    if kernel == "combine":      # read M, Z (and h0); write the segment starts and h_final (fp32)
+        return segs * bh * 4 * (K * K + 2 * K * V) + bh * state
     if kernel == "forward":      # the I/O floor: read q, k, v, g, beta, h0; write o, h_final
         per = 2 * K * e + 2 * V * e + gw + e
         return th * per + bh * state
@@ -354,7 +359,8 @@ def run_ours(args, wl):
     q, k, v, g, beta = (t.to(dev) for t in (x.q, x.k, x.v, x.g, x.beta))
     h0 = x.h0.to(dev) if x.h0 is not None else None
     B, T, H, K, V, C = wl.B, wl.T, wl.H, wl.K, wl.V, wl.chunk
-    p = gdr.problem_for(q, v, g, C, None, args.variant)
+    p = gdr.problem_for(q, v, g, C, None, args.variant, args.segments)
+    S = gdr.gdr_forward_segments(p)
     o = torch.empty(B, T, H, V, device=dev, dtype=q.dtype)
     hf = torch.empty(B, H, K, V, device=dev, dtype=torch.float32)
     nbytes = gdr.gdr_forward_workspace_bytes(p)
@@ -368,21 +374,35 @@ def run_ours(args, wl):
     variant = gdr.gdr_last_variant()
     staged = variant != "fused"
     P = None
+    # the segment-parallel scan (S > 1): every segment's map, the stitch, then the scan of all
+    # segments at once on the view of B S sequences of T / S tokens
+    seg_calls, seg_names, vp = [], [], None
+    if S > 1:
+        Hk = q.shape[2]
+        M = torch.empty(B, S, H, K, K, device=dev)
+        Z = torch.empty(B, S, H, K, V, device=dev)
+        starts = torch.empty(B, S, H, K, V, device=dev)
+        vp = gdr.problem_for(q, v, g, C, None, args.variant, 1)
+        vp.B, vp.T = B * S, T // S
+        seg_names = ["transfer", "combine"]
+        seg_calls = [lambda: gdr.gdr_scan_transfer(sp, k, w, u, g_cum, S, M, Z),
+                     lambda: gdr.gdr_scan_combine(sp, S, M, Z, h0, starts, hf)]
+        del Hk
     if variant == "fused":
         # the two kernels gdr_forward runs on this path, called one by one so each can be timed
         g_cum = torch.empty_like(g)
         w = torch.empty_like(k)
         u = torch.empty_like(v)
         P = torch.empty(B, -(-T // C), H, C, C, device=dev, dtype=q.dtype) if C == 64 and args.p_from == "prepare" else None
-        sp = gdr.problem_for(q, v, g, C, None, args.variant)
-        kernels = ["prepare", "scan_output"]
+        sp = gdr.problem_for(q, v, g, C, None, args.variant, 1)
+        kernels = ["prepare"] + seg_names + ["scan_output"]
 
         def launches():
-            if P is None:
-                return [lambda: gdr.gdr_prepare_wy(sp, k, v, g, beta, w, u, g_cum),
-                        lambda: gdr.gdr_scan_output(sp, q, k, w, u, g_cum, None, h0, o, hf)]
-            return [lambda: gdr.gdr_prepare_wyp(sp, q, k, v, g, beta, w, u, g_cum, P),
-                    lambda: gdr.gdr_scan_output(sp, q, k, w, u, g_cum, P, h0, o, hf)]
+            prep = (lambda: gdr.gdr_prepare_wy(sp, k, v, g, beta, w, u, g_cum)) if P is None else \
+                (lambda: gdr.gdr_prepare_wyp(sp, q, k, v, g, beta, w, u, g_cum, P))
+            if vp is not None:
+                return [prep] + seg_calls + [lambda: gdr.gdr_scan_output(vp, q, k, w, u, g_cum, P, starts, o, None)]
+            return [prep, lambda: gdr.gdr_scan_output(sp, q, k, w, u, g_cum, P, h0, o, hf)]
     elif staged:
         NT = -(-T // C)
         e = q.element_size()
@@ -392,13 +412,16 @@ def run_ours(args, wl):
         u = torch.empty_like(v)
         v_new = torch.empty_like(v)
         h_ckpt = torch.empty(B, NT, H, K, V, device=dev, dtype=q.dtype)
-        sp = gdr.problem_for(q, v, g, C, None, args.variant)
-        kernels = ["prepare", "scan", "output"]
+        sp = gdr.problem_for(q, v, g, C, None, args.variant, 1)
+        kernels = ["prepare"] + seg_names + ["scan", "output"]
 
         def launches():
-            return [lambda: gdr.gdr_prepare_wy(sp, k, v, g, beta, w, u, g_cum),
-                    lambda: gdr.gdr_scan_h(sp, k, w, u, g_cum, h0, h_ckpt, v_new, hf),
-                    lambda: gdr.gdr_chunk_output(sp, q, k, v_new, h_ckpt, g_cum, o)]
+            if vp is not None:
+                scan = lambda: gdr.gdr_scan_h(vp, k, w, u, g_cum, starts, h_ckpt, v_new, None)
+            else:
+                scan = lambda: gdr.gdr_scan_h(sp, k, w, u, g_cum, h0, h_ckpt, v_new, hf)
+            return [lambda: gdr.gdr_prepare_wy(sp, k, v, g, beta, w, u, g_cum)] + seg_calls + \
+                [scan, lambda: gdr.gdr_chunk_output(sp, q, k, v_new, h_ckpt, g_cum, o)]
         del e
 
     calls = launches()
@@ -443,10 +466,11 @@ def run_ours(args, wl):
     avg_ms = [t / args.steps for t in per_kernel_ms]
     dom = max(range(n), key=lambda i: avg_ms[i])
     dom_name = kernels[dom]
-    dom_bytes = algorithmic_bytes(wl, dom_name, with_p=variant == "fused" and P is not None)
+    dom_bytes = algorithmic_bytes(wl, dom_name, with_p=variant == "fused" and P is not None, segs=S)
     achieved = dom_bytes / (avg_ms[dom] / 1e3) / 1e9
     kname = {"prepare": "prepare_mma_kernel", "scan": "scan_mma_kernel", "output": "tc_output_kernel",
-             "scan_output": "fused_scan_output_kernel"}[dom_name]
+             "scan_output": "fused_scan_output_kernel", "transfer": "scan_mma_kernel<transfer>",
+             "combine": "segment_combine_kernel"}[dom_name]
     if stage_variant[dom] == "simt":
         kname = f"simt_{dom_name}_kernel"
     traffic = traffic_for(kname)
@@ -457,14 +481,14 @@ def run_ours(args, wl):
     d2h = o.numel() * o.element_size() + hf.numel() * hf.element_size()
     for _ in range(2):
         gdr.forward(hx["q"], hx["k"], hx["v"], hx["g"], hx["beta"], hx.get("h0"), chunk=C, variant=args.variant,
-                    workspace=ws)
+                    workspace=ws, segments=args.segments)
     torch.cuda.synchronize()
     e2e_steps = max(3, min(args.steps, 10))
     barrier(world)
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
         oo, hh = gdr.forward(hx["q"], hx["k"], hx["v"], hx["g"], hx["beta"], hx.get("h0"), chunk=C,
-                             variant=args.variant, workspace=ws)
+                             variant=args.variant, workspace=ws, segments=args.segments)
     torch.cuda.synchronize()
     e2e_s = max_over_ranks(time.perf_counter() - t0, world)
     e2e_value = weak_scaling_throughput(world, B * T, e2e_steps, e2e_s)
@@ -482,7 +506,7 @@ def run_ours(args, wl):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.io == "bf16" else "f32",
             "data": "synthetic (seeded; q,k unit-norm, v N(0,1), beta sigmoid, g logsigmoid/16)",
             "config": dict(wl.describe(), variant=variant, l2="256 MiB buffer overwritten before every timed step",
-                           kernels_per_step=n),
+                           kernels_per_step=n, segments=S),
             "roofline": {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
                          "frac": achieved / hbm_gbs, "peak_source": f"{peak_kind} HBM copy bandwidth",
                          "traffic": traffic, "algorithmic_bytes_per_launch": dom_bytes,
@@ -512,6 +536,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=workloads.THROUGHPUT.name, choices=sorted(workloads.BY_NAME))
     ap.add_argument("--variant", default="auto", choices=sorted(gdr.VARIANTS))
+    ap.add_argument("--segments", type=int, default=0,
+                    help="segment-parallel scan: 0 = the library's choice, 1 = serial, S = S segments")
     ap.add_argument("--cpu-heads", type=int, default=32, help="heads in the CPU-oracle baseline sample")
     ap.add_argument("--ref-heads", type=int, default=4, help="heads per step of --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -35,6 +35,7 @@ gdr_status check_problem(const gdr_problem* p, gdr::Dims* d) {
     if (p->B > INT32_MAX / p->T || p->B * p->T > INT32_MAX / HV) return GDR_ERR_SHAPE;
     if (std::isnan(p->scale) || std::isinf(p->scale)) return GDR_ERR_ARG;
     if (p->variant < GDR_VARIANT_AUTO || p->variant > GDR_VARIANT_FUSED) return GDR_ERR_ARG;
+    if (p->segments < 0) return GDR_ERR_ARG;
     d->B = (int)p->B;
     d->T = (int)p->T;
     d->H = (int)HV;
@@ -114,12 +115,50 @@ unsigned int* device_error_word() {
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// gdr_forward scratch: g_cum, w, u and (staged paths) v_new, h_ckpt, each 256-byte aligned.
+// The segment-parallel scan: the sequence of each (b, h) splits into S segments of NT / S chunks.
+// Viewed as B S sequences of T / S tokens, every [B, T, ...] and [B, NT, ...] tensor keeps its memory
+// layout, so the scan kernels run the segments as a larger batch.
+gdr::Dims segment_view(const gdr::Dims& d, int S) {
+    gdr::Dims v = d;
+    v.B = d.B * S;
+    v.T = d.T / S;
+    v.NT = d.NT / S;
+    return v;
+}
+
+// S for gdr_forward.  Explicit (p->segments > 1): it must divide NT, with whole chunks.  Automatic
+// (0): when the serial scan's grid, B HV V/32 CTAs, fills less than half the GPU, the largest
+// divisor of NT that keeps the segmented grid within one wave of 152 SMs and every segment at least
+// kSegMinChunks chunks long.  The CUDA-core path is never segmented.
+constexpr int kSmCount = 152;
+constexpr int kSegMinChunks = 16;
+
+gdr_status resolve_segments(const gdr_problem* p, const gdr::Dims& d, Path path, int* S) {
+    *S = 1;
+    if (p->segments == 1 || path == Path::Simt) return GDR_OK;
+    if (p->segments > 1) {
+        if (d.T % d.C != 0 || d.NT % p->segments != 0 || p->segments > kMaxGridYZ / d.B) return GDR_ERR_ARG;
+        *S = (int)p->segments;
+        return GDR_OK;
+    }
+    const int64_t base = (int64_t)d.B * d.H * (d.V / 32);
+    if (d.T % d.C != 0 || 2 * base > kSmCount) return GDR_OK;
+    for (int cand = d.NT / kSegMinChunks; cand >= 2; --cand) {
+        if (d.NT % cand == 0 && cand * base <= kSmCount && cand <= kMaxGridYZ / d.B) {
+            *S = cand;
+            break;
+        }
+    }
+    return GDR_OK;
+}
+
+// gdr_forward scratch: g_cum, w, u and (staged paths) v_new, h_ckpt, (S > 1) the segment maps and
+// starts, each 256-byte aligned.
 struct StagedWorkspace {
-    size_t g_cum, w, u, v_new, h_ckpt, P, total;
+    size_t g_cum, w, u, v_new, h_ckpt, P, seg_m, seg_z, seg_h, total;
 };
 
-StagedWorkspace plan_staged(const gdr::Dims& d, bool fused) {
+StagedWorkspace plan_staged(const gdr::Dims& d, bool fused, int S) {
     const size_t e = (d.bf16 || d.f16) ? 2 : 4;
     const size_t rows = (size_t)d.B * d.T * d.H;
     StagedWorkspace ws;
@@ -136,6 +175,13 @@ StagedWorkspace plan_staged(const gdr::Dims& d, bool fused) {
         off = round_up(off + (size_t)d.B * d.NT * d.H * d.K * d.V * e, 256);
     } else if (d.C == 64) {   // ... and reads the prepare's gated causal scores [B, NT, H, C, C]
         off = round_up(off + (size_t)d.B * d.NT * d.H * d.C * d.C * e, 256);
+    }
+    ws.seg_m = ws.seg_z = ws.seg_h = off;
+    if (S > 1) {   // M [B S, H, K, K], Z and the segment starts [B S, H, K, V], fp32
+        const size_t maps = (size_t)d.B * S * d.H * d.K;
+        ws.seg_z = round_up(off + maps * d.K * 4, 256);
+        ws.seg_h = round_up(ws.seg_z + maps * d.V * 4, 256);
+        off = round_up(ws.seg_h + maps * d.V * 4, 256);
     }
     ws.total = off;
     return ws;
@@ -250,6 +296,32 @@ gdr_status gdr_scan_h(const gdr_problem* p, const void* k, const void* w, const 
     return st;
 }
 
+gdr_status gdr_scan_transfer(const gdr_problem* p, const void* k, const void* w, const void* u, const float* g_cum,
+                             int32_t segments, float* M, float* Z, void* stream) {
+    gdr::Dims d;
+    gdr_status st = check_problem(p, &d);
+    if (st != GDR_OK) return st;
+    if ((st = check_ptrs({k, w, u, g_cum, M, Z}, {})) != GDR_OK) return st;
+    if (p->variant == GDR_VARIANT_SIMT || !d.bf16) return GDR_ERR_UNSUPPORTED;
+    if (segments < 1 || d.T % d.C != 0 || d.NT % segments != 0 || segments > kMaxGridYZ / d.B) return GDR_ERR_ARG;
+    st = from_cuda(gdr::mma_scan_transfer(segment_view(d, segments), k, w, u, g_cum, M, Z, (cudaStream_t)stream,
+                                          device_error_word()));
+    if (st == GDR_OK) t_last_variant = "tensor";
+    return st;
+}
+
+gdr_status gdr_scan_combine(const gdr_problem* p, int32_t segments, const float* M, const float* Z, const float* h0,
+                            float* h_start, float* h_final, void* stream) {
+    gdr::Dims d;
+    gdr_status st = check_problem(p, &d);
+    if (st != GDR_OK) return st;
+    if ((st = check_ptrs({M, Z, h_start}, {h0, h_final})) != GDR_OK) return st;
+    if (segments < 1 || segments > kMaxGridYZ / d.B) return GDR_ERR_ARG;
+    st = from_cuda(gdr::segment_combine(d, segments, M, Z, h0, h_start, h_final, (cudaStream_t)stream));
+    if (st == GDR_OK) t_last_variant = "simt";
+    return st;
+}
+
 gdr_status gdr_chunk_output(const gdr_problem* p, const void* q, const void* k, const void* v_new,
                             const void* h_ckpt, const float* g_cum, void* o, void* stream) {
     gdr::Dims d;
@@ -269,8 +341,18 @@ size_t gdr_forward_workspace_bytes(const gdr_problem* p) {
     gdr::Dims d;
     if (check_problem(p, &d) != GDR_OK) return 0;
     Path path;
-    if (pick_forward(p, d, &path) != GDR_OK) return 0;
-    return plan_staged(d, path == Path::Fused).total;
+    int S = 1;
+    if (pick_forward(p, d, &path) != GDR_OK || resolve_segments(p, d, path, &S) != GDR_OK) return 0;
+    return plan_staged(d, path == Path::Fused, S).total;
+}
+
+int gdr_forward_segments(const gdr_problem* p) {
+    gdr::Dims d;
+    if (check_problem(p, &d) != GDR_OK) return 0;
+    Path path;
+    int S = 1;
+    if (pick_forward(p, d, &path) != GDR_OK || resolve_segments(p, d, path, &S) != GDR_OK) return 0;
+    return S;
 }
 
 gdr_status gdr_forward(const gdr_problem* p, const void* q, const void* k, const void* v, const float* g,
@@ -282,7 +364,9 @@ gdr_status gdr_forward(const gdr_problem* p, const void* q, const void* k, const
     if ((st = check_ptrs({q, k, v, g, beta, o}, {h0, h_final})) != GDR_OK) return st;
     Path path;
     if ((st = pick_forward(p, d, &path)) != GDR_OK) return st;
-    const StagedWorkspace ws = plan_staged(d, path == Path::Fused);
+    int S = 1;
+    if ((st = resolve_segments(p, d, path, &S)) != GDR_OK) return st;
+    const StagedWorkspace ws = plan_staged(d, path == Path::Fused, S);
     if (!workspace || workspace_bytes < ws.total) return GDR_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GDR_ERR_ALIGN;
     char* base = static_cast<char*>(workspace);
@@ -300,11 +384,26 @@ gdr_status gdr_forward(const gdr_problem* p, const void* q, const void* k, const
     } else {
         void* P = (path == Path::Fused && d.C == 64) ? base + ws.P : nullptr;
         if ((st = from_cuda(gdr::mma_prepare(d, k, v, g, beta, w, u, g_cum, s, err, q, P))) != GDR_OK) return st;
+        // segments: every segment's map from a zero state, the starts stitched serially, then the
+        // scan (and output) of all segments at once from their starts
+        gdr::Dims ds = d;
+        const float* hs = h0;
+        float* hf = h_final;
+        if (S > 1) {
+            ds = segment_view(d, S);
+            float* m = reinterpret_cast<float*>(base + ws.seg_m);
+            float* z = reinterpret_cast<float*>(base + ws.seg_z);
+            float* starts = reinterpret_cast<float*>(base + ws.seg_h);
+            if ((st = from_cuda(gdr::mma_scan_transfer(ds, k, w, u, g_cum, m, z, s, err))) != GDR_OK) return st;
+            if ((st = from_cuda(gdr::segment_combine(d, S, m, z, h0, starts, h_final, s))) != GDR_OK) return st;
+            hs = starts;
+            hf = nullptr;
+        }
         if (path == Path::Fused) {
-            if ((st = from_cuda(gdr::mma_scan_output(d, q, k, w, u, g_cum, P, h0, o, h_final, s, err))) != GDR_OK)
+            if ((st = from_cuda(gdr::mma_scan_output(ds, q, k, w, u, g_cum, P, hs, o, hf, s, err))) != GDR_OK)
                 return st;
         } else {
-            if ((st = from_cuda(gdr::mma_scan(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, s, err))) != GDR_OK)
+            if ((st = from_cuda(gdr::mma_scan(ds, k, w, u, g_cum, hs, h_ckpt, v_new, hf, s, err))) != GDR_OK)
                 return st;
             if ((st = from_cuda(gdr::tc_output(d, q, k, v_new, h_ckpt, g_cum, o, s, err))) != GDR_OK) return st;
         }

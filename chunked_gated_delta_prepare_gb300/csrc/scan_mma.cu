@@ -46,9 +46,13 @@ constexpr int kRecWarps = 4;   // (value half, key half)
 
 constexpr uint32_t align1k(uint32_t x) { return (x + 1023u) & ~1023u; }
 
-template <int K, int C, bool PER_K>
+// TRANSFER (the segment maps) writes no checkpoint and no v', so it needs no staging.  At K = 128,
+// C = 64 it also runs a 2-stage ring: 106 KB instead of 157 KB, so two CTAs share an SM (scalar
+// gate; measured 0.088 ms against 0.107 ms for 256 CTAs, though 10% slower per chunk at one CTA
+// per SM).  The smaller tiles fit two CTAs with three stages.
+template <int K, int C, bool PER_K, bool TRANSFER = false>
 struct MScanLayout {
-    static constexpr int NS = 3;                                   // ring stages
+    static constexpr int NS = TRANSFER && K == 128 && C == 64 ? 2 : 3;   // ring stages
     static constexpr int KH = K / 2;                               // keys per recurrence warp
     static constexpr int NT8 = C / 8;
     static constexpr int GW = PER_K ? K : 1;
@@ -64,8 +68,8 @@ struct MScanLayout {
     static constexpr uint32_t U = KB + NS * kKC;
     static constexpr uint32_t X = U + NS * kU;
     static constexpr uint32_t SH = X + 2 * kRecWarps * kX;
-    static constexpr uint32_t SV = SH + kRecWarps * kSH;
-    static constexpr uint32_t GAM = SV + kRecWarps * kSV;          // gamma rows [NS][C] (scalar gate)
+    static constexpr uint32_t SV = SH + (TRANSFER ? 0 : kRecWarps * kSH);
+    static constexpr uint32_t GAM = SV + (TRANSFER ? 0 : kRecWarps * kSV);   // gamma rows [NS][C] (scalar gate)
     static constexpr uint32_t DEC = GAM + NS * C * 4;              // exp(G_last) [NS][GW]
     static constexpr uint32_t bytes = DEC + NS * GW * 4;
     static constexpr uint32_t tx = (PER_K ? 1 : 2) * kKC + kU;
@@ -75,13 +79,19 @@ struct MScanLayout {
 // GENERAL: a partial last chunk or grouped value heads.  Whole chunks of ungrouped heads take
 // the variant without those guards (the per-key-dim producers' guarded loads measured 60%
 // slower on whole chunks).
-template <int K, int C, bool PER_K, bool GENERAL>
-__global__ void __launch_bounds__(MScanLayout<K, C, PER_K>::kThreads, 1)
+// TRANSFER: the affine map of every segment of the segment-parallel scan, h_end = M h_start + Z.
+// The columns of h evolve independently, so the grid gets K/32 more column slices: slices below
+// V/32 run u's columns from a zero state (their final state is Z, written to h_final), the others
+// run the columns of the identity with u = 0 (their final state is M, written to m_out [.., K, K]).
+// No checkpoint and no v' is written.
+template <int K, int C, bool PER_K, bool GENERAL, bool TRANSFER>
+__global__ void __launch_bounds__(MScanLayout<K, C, PER_K, TRANSFER>::kThreads, TRANSFER && !PER_K ? 2 : 1)
 scan_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap mk,
                 const __grid_constant__ CUtensorMap mu, const bf16* __restrict__ k, const float* __restrict__ g_cum,
                 const float* __restrict__ h0, bf16* __restrict__ h_ckpt, bf16* __restrict__ v_new,
-                float* __restrict__ h_final, int T, int H, int V, int G, unsigned int* err) {
-    using L = MScanLayout<K, C, PER_K>;
+                float* __restrict__ h_final, float* __restrict__ m_out, int T, int H, int V, int G,
+                unsigned int* err) {
+    using L = MScanLayout<K, C, PER_K, TRANSFER>;
     constexpr int GW = L::GW, KH = L::KH, NT8 = L::NT8;
     constexpr int NJH = KH / 8;    // n-tiles of this warp's part of h^T
     extern __shared__ unsigned char smem_raw[];
@@ -89,7 +99,9 @@ scan_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ 
     __shared__ uint64_t full[L::NS], empty[L::NS];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int v0 = blockIdx.x * kBV, h = blockIdx.y, b = blockIdx.z;
+    const bool mcols = TRANSFER && (int)blockIdx.x >= V / kBV;   // a slice of the identity's columns
+    const int v0 = (mcols ? (int)blockIdx.x - V / kBV : (int)blockIdx.x) * kBV, h = blockIdx.y, b = blockIdx.z;
+    const uint32_t tx = mcols ? L::tx - L::kU : L::tx;           // u = 0 there: no u tile
     const int NT = GENERAL ? (T + C - 1) / C : T / C;   // a last, partial chunk runs as zero tokens past T
     const uint32_t s_base = bw::smem_u32(sm);
     auto row = [&](int t) -> int64_t { return ((int64_t)b * T + t) * H + h; };
@@ -132,13 +144,13 @@ scan_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ 
                 if (!bw::mbar_wait(&empty[s], ((c / L::NS) & 1) ^ 1, err, kDeviceErrTimeout)) break;
                 const int t0 = c * C;
                 if (lane == 0) {
-                    bw::mbar_arrive_expect_tx(&full[s], L::tx);
+                    bw::mbar_arrive_expect_tx(&full[s], tx);
 #pragma unroll
                     for (int a = 0; a < K / 64; ++a) {
                         bw::tma_load_4d(sm + L::W + s * L::kKC + a * C * 128, &mw, &full[s], a * 64, h, t0, b);
                         bw::tma_load_4d(sm + L::KB + s * L::kKC + a * C * 128, &mk, &full[s], a * 64, hk, t0, b);
                     }
-                    bw::tma_load_4d(sm + L::U + s * L::kU, &mu, &full[s], v0, h, t0, b);
+                    if (!mcols) bw::tma_load_4d(sm + L::U + s * L::kU, &mu, &full[s], v0, h, t0, b);
                     sDec[s] = __expf(glc);
                 }
 #pragma unroll
@@ -177,11 +189,11 @@ scan_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ 
                 if (!bw::mbar_wait(&empty[s], ((c / L::NS) & 1) ^ 1, err, kDeviceErrTimeout)) return false;
                 const int t0 = c * C;
                 if (pt == 0) {
-                    bw::mbar_arrive_expect_tx(&full[s], L::tx);
+                    bw::mbar_arrive_expect_tx(&full[s], tx);
 #pragma unroll
                     for (int a = 0; a < K / 64; ++a)
                         bw::tma_load_4d(sm + L::W + s * L::kKC + a * C * 128, &mw, &full[s], a * 64, h, t0, b);
-                    bw::tma_load_4d(sm + L::U + s * L::kU, &mu, &full[s], v0, h, t0, b);
+                    if (!mcols) bw::tma_load_4d(sm + L::U + s * L::kU, &mu, &full[s], v0, h, t0, b);
                 }
                 if (r0 == 0) {
 #pragma unroll
@@ -232,7 +244,12 @@ scan_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ 
     for (int j = 0; j < NJH; ++j) {
         const int d = d0 + 8 * j + 2 * q4;
         const int va = v0 + vr0 + g, vb = va + 8;
-        if (h0) {
+        if (TRANSFER) {   // Z from a zero state; M from the identity (column va of I has its 1 in row va)
+            hT[j][0] = mcols && d == va ? 1.f : 0.f;
+            hT[j][1] = mcols && d + 1 == va ? 1.f : 0.f;
+            hT[j][2] = mcols && d == vb ? 1.f : 0.f;
+            hT[j][3] = mcols && d + 1 == vb ? 1.f : 0.f;
+        } else if (h0) {
             hT[j][0] = h0[(state + d) * V + va];
             hT[j][1] = h0[(state + d + 1) * V + va];
             hT[j][2] = h0[(state + d) * V + vb];
@@ -294,11 +311,16 @@ scan_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ 
 
         // u^T fragments (D's layout) ahead of the exchange
         uint32_t ur[NT8 / 2][4];
+        if (mcols) {
 #pragma unroll
-        for (int jp = 0; jp < NT8; jp += 2) {
-            const int t = 8 * jp + 8 * (mi >> 1) + mr;
-            const int ch = (vr0 >> 3) + (mi & 1);
-            wm::ldsm_x4_t(u_t + t * 64 + ((ch ^ ((t >> 1) & 3)) << 4), ur[jp / 2]);
+            for (int jp = 0; jp < NT8; jp += 2) ur[jp / 2][0] = ur[jp / 2][1] = ur[jp / 2][2] = ur[jp / 2][3] = 0u;
+        } else {
+#pragma unroll
+            for (int jp = 0; jp < NT8; jp += 2) {
+                const int t = 8 * jp + 8 * (mi >> 1) + mr;
+                const int ch = (vr0 >> 3) + (mi & 1);
+                wm::ldsm_x4_t(u_t + t * 64 + ((ch ^ ((t >> 1) & 3)) << 4), ur[jp / 2]);
+            }
         }
 
         // D = D_0 + D_1: swap partial sums with the other key half of the same value columns
@@ -366,7 +388,7 @@ scan_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ 
         if (lane == 0) bw::mbar_arrive(&empty[s]);
 
         // v_new: this key half stores tokens kh C/2 .. of v'^T; stmatrix.trans -> staging -> global
-        {
+        if constexpr (!TRANSFER) {
 #pragma unroll
             for (int jp = 0; jp < NT8; jp += 2) {
                 if ((jp >= NT8 / 2) != (kh == 1)) continue;   // static register indices, runtime half
@@ -388,50 +410,60 @@ scan_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ 
         }
     }
     if (h_final) {
+        float* out = mcols ? m_out : h_final;
+        const int ld = mcols ? K : V;
 #pragma unroll
         for (int j = 0; j < NJH; ++j) {
             const int d = d0 + 8 * j + 2 * q4;
             const int va = v0 + vr0 + g, vb = va + 8;
-            h_final[(state + d) * V + va] = hT[j][0];
-            h_final[(state + d + 1) * V + va] = hT[j][1];
-            h_final[(state + d) * V + vb] = hT[j][2];
-            h_final[(state + d + 1) * V + vb] = hT[j][3];
+            out[(state + d) * ld + va] = hT[j][0];
+            out[(state + d + 1) * ld + va] = hT[j][1];
+            out[(state + d) * ld + vb] = hT[j][2];
+            out[(state + d + 1) * ld + vb] = hT[j][3];
         }
     }
     (void)ok;
 }
 
-template <int K, int C, bool PER_K, bool GENERAL>
+template <int K, int C, bool PER_K, bool GENERAL, bool TRANSFER>
 cudaError_t launch_v(const Dims& d, const void* k, const void* w, const void* u, const float* g_cum, const float* h0,
-                     void* h_ckpt, void* v_new, float* h_final, cudaStream_t s, unsigned int* err) {
-    using L = MScanLayout<K, C, PER_K>;
+                     void* h_ckpt, void* v_new, float* h_final, float* m_out, cudaStream_t s, unsigned int* err) {
+    using L = MScanLayout<K, C, PER_K, TRANSFER>;
     CUtensorMap mw, mk, mu;
     if (!make_tmap_tokens(&mw, w, d.B, d.T, d.H, K, C) || !make_tmap_tokens(&mk, k, d.B, d.T, d.Hk, K, C) ||
         !make_tmap_tokens_sw64(&mu, u, d.B, d.T, d.H, d.V, C))
         return cudaErrorInvalidValue;
-    auto kern = scan_mma_kernel<K, C, PER_K, GENERAL>;
+    auto kern = scan_mma_kernel<K, C, PER_K, GENERAL, TRANSFER>;
     const size_t smem = L::bytes + 1024;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const dim3 grid(d.V / kBV, d.H, d.B);
+    const dim3 grid(d.V / kBV + (TRANSFER ? K / kBV : 0), d.H, d.B);
     kern<<<grid, L::kThreads, smem, s>>>(mw, mk, mu, (const bf16*)k, g_cum, h0, (bf16*)h_ckpt, (bf16*)v_new,
-                                         h_final, d.T, d.H, d.V, d.G, err);
+                                         h_final, m_out, d.T, d.H, d.V, d.G, err);
     return cudaGetLastError();
 }
 
-template <int K, int C, bool PER_K>
+template <int K, int C, bool PER_K, bool TRANSFER>
 cudaError_t launch(const Dims& d, const void* k, const void* w, const void* u, const float* g_cum, const float* h0,
-                   void* h_ckpt, void* v_new, float* h_final, cudaStream_t s, unsigned int* err) {
+                   void* h_ckpt, void* v_new, float* h_final, float* m_out, cudaStream_t s, unsigned int* err) {
     if (d.T % C != 0 || d.G != 1)
-        return launch_v<K, C, PER_K, true>(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, s, err);
-    return launch_v<K, C, PER_K, false>(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, s, err);
+        return launch_v<K, C, PER_K, true, TRANSFER>(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, m_out, s, err);
+    return launch_v<K, C, PER_K, false, TRANSFER>(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, m_out, s, err);
 }
 
-template <int K, int C>
-cudaError_t gate(const Dims& d, const void* k, const void* w, const void* u, const float* g_cum, const float* h0,
-                 void* h_ckpt, void* v_new, float* h_final, cudaStream_t s, unsigned int* err) {
-    return d.per_k ? launch<K, C, true>(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, s, err)
-                   : launch<K, C, false>(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, s, err);
+template <bool TRANSFER>
+cudaError_t dispatch(const Dims& d, const void* k, const void* w, const void* u, const float* g_cum, const float* h0,
+                     void* h_ckpt, void* v_new, float* h_final, float* m_out, cudaStream_t s, unsigned int* err) {
+#define GDR_SCAN_ARGS d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, m_out, s, err
+    if (d.K == 64) {
+        if (d.C == 32)
+            return d.per_k ? launch<64, 32, true, TRANSFER>(GDR_SCAN_ARGS) : launch<64, 32, false, TRANSFER>(GDR_SCAN_ARGS);
+        return d.per_k ? launch<64, 64, true, TRANSFER>(GDR_SCAN_ARGS) : launch<64, 64, false, TRANSFER>(GDR_SCAN_ARGS);
+    }
+    if (d.C == 32)
+        return d.per_k ? launch<128, 32, true, TRANSFER>(GDR_SCAN_ARGS) : launch<128, 32, false, TRANSFER>(GDR_SCAN_ARGS);
+    return d.per_k ? launch<128, 64, true, TRANSFER>(GDR_SCAN_ARGS) : launch<128, 64, false, TRANSFER>(GDR_SCAN_ARGS);
+#undef GDR_SCAN_ARGS
 }
 
 }  // namespace
@@ -439,12 +471,13 @@ cudaError_t gate(const Dims& d, const void* k, const void* w, const void* u, con
 cudaError_t mma_scan(const Dims& d, const void* k, const void* w, const void* u, const float* g_cum, const float* h0,
                      void* h_ckpt, void* v_new, float* h_final, cudaStream_t s, unsigned int* err) {
     if (!d.bf16) return cudaErrorInvalidValue;
-    if (d.K == 64) {
-        return d.C == 32 ? gate<64, 32>(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, s, err)
-                         : gate<64, 64>(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, s, err);
-    }
-    return d.C == 32 ? gate<128, 32>(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, s, err)
-                     : gate<128, 64>(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, s, err);
+    return dispatch<false>(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, nullptr, s, err);
+}
+
+cudaError_t mma_scan_transfer(const Dims& d, const void* k, const void* w, const void* u, const float* g_cum,
+                              float* m_out, float* z_out, cudaStream_t s, unsigned int* err) {
+    if (!d.bf16 || !m_out || !z_out) return cudaErrorInvalidValue;
+    return dispatch<true>(d, k, w, u, g_cum, nullptr, nullptr, nullptr, z_out, m_out, s, err);
 }
 
 }  // namespace gdr

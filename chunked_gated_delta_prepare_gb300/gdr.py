@@ -5,8 +5,8 @@ kernels.  PyTorch supplies device memory and the current stream.  There is no
 CPU fallback: if the library is missing or cannot load, every call raises.
 
 The functions mirror the C ABI names:
-    gdr_prepare_wy, gdr_prepare_wyp, gdr_scan_h, gdr_chunk_output, gdr_scan_output, gdr_forward,
-    gdr_forward_workspace_bytes, gdr_bwd_dv_local, gdr_bwd_scan_dh, gdr_bwd_dqkwg, gdr_bwd_wy,
+    gdr_prepare_wy, gdr_prepare_wyp, gdr_scan_h, gdr_scan_transfer, gdr_scan_combine, gdr_chunk_output,
+    gdr_scan_output, gdr_forward, gdr_forward_workspace_bytes, gdr_forward_segments, gdr_bwd_dv_local, gdr_bwd_scan_dh, gdr_bwd_dqkwg, gdr_bwd_wy,
     gdr_bwd_prepare, gdr_bwd_scan_dh_p, gdr_bwd_wy_dqkg, gdr_backward, gdr_backward_workspace_bytes,
     gdr_status_string, gdr_get_device_status,
     gdr_last_variant, gdr_version
@@ -35,7 +35,8 @@ EXPORTS = ["gdr_prepare_wy", "gdr_scan_h", "gdr_chunk_output", "gdr_forward", "g
            "gdr_forward_static_scratch", "gdr_scan_output", "gdr_prepare_wyp",
            "gdr_bwd_dv_local", "gdr_bwd_scan_dh", "gdr_bwd_dqkwg", "gdr_bwd_wy", "gdr_backward",
            "gdr_backward_workspace_bytes", "gdr_bwd_prepare", "gdr_bwd_scan_dh_p", "gdr_bwd_wy_dqkg",
-           "gdr_bwd_group_sum", "gdr_bwd_dv_local_tc", "gdr_bwd_scan_dh_tc",
+           "gdr_bwd_group_sum", "gdr_bwd_dv_local_tc", "gdr_bwd_scan_dh_tc", "gdr_scan_transfer",
+           "gdr_scan_combine", "gdr_forward_segments",
            "gdr_status_string", "gdr_get_device_status", "gdr_last_variant", "gdr_version"]
 
 
@@ -49,7 +50,7 @@ class gdr_problem(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int64), ("T", ctypes.c_int64), ("H", ctypes.c_int64), ("K", ctypes.c_int64),
                 ("V", ctypes.c_int64), ("chunk", ctypes.c_int64), ("io_dtype", ctypes.c_int32),
                 ("gate", ctypes.c_int32), ("scale", ctypes.c_float), ("variant", ctypes.c_int32),
-                ("HV", ctypes.c_int64)]
+                ("HV", ctypes.c_int64), ("segments", ctypes.c_int32)]
 
 
 _lib = None
@@ -89,6 +90,9 @@ def load(path: str | None = None):
             "gdr_bwd_group_sum": [P] + [vp] * 5,
             "gdr_bwd_dv_local_tc": [P] + [vp] * 6,
             "gdr_bwd_scan_dh_tc": [P] + [vp] * 11,
+            "gdr_scan_transfer": [P, vp, vp, vp, vp, ctypes.c_int32, vp, vp, vp],
+            "gdr_scan_combine": [P, ctypes.c_int32, vp, vp, vp, vp, vp, vp],
+            "gdr_forward_segments": [P],
             "gdr_status_string": [ctypes.c_int],
             "gdr_get_device_status": [vp],
             "gdr_last_variant": [],
@@ -136,19 +140,22 @@ def _check(status: int, where: str):
 
 
 def make_problem(B, T, H, K, V, chunk, io_dtype=torch.bfloat16, per_k_gate=False, scale=None,
-                 variant="auto", HV=0) -> gdr_problem:
-    """H: q/k heads; HV: value heads (a multiple of H; 0 means H)."""
+                 variant="auto", HV=0, segments=0) -> gdr_problem:
+    """H: q/k heads; HV: value heads (a multiple of H; 0 means H); segments: gdr_forward's
+    segment-parallel scan (0 = the library's choice, 1 = off, S = S segments)."""
     dt = DTYPES[io_dtype] if isinstance(io_dtype, torch.dtype) else int(io_dtype)
     return gdr_problem(B=B, T=T, H=H, K=K, V=V, chunk=chunk, io_dtype=dt, gate=1 if per_k_gate else 0,
                        scale=-1.0 if scale is None else float(scale),
-                       variant=VARIANTS[variant] if isinstance(variant, str) else int(variant), HV=HV)
+                       variant=VARIANTS[variant] if isinstance(variant, str) else int(variant), HV=HV,
+                       segments=int(segments))
 
 
-def problem_for(q, v, g, chunk, scale=None, variant="auto") -> gdr_problem:
+def problem_for(q, v, g, chunk, scale=None, variant="auto", segments=0) -> gdr_problem:
     """The problem of tensors q [B,T,H,K], v [B,T,HV,V] and g; HV > H means grouped value heads."""
     B, T, H, K = q.shape
     HV, V = v.shape[2], v.shape[-1]
-    return make_problem(B, T, H, K, V, chunk, q.dtype, g.dim() == 4, scale, variant, HV=HV if HV != H else 0)
+    return make_problem(B, T, H, K, V, chunk, q.dtype, g.dim() == 4, scale, variant, HV=HV if HV != H else 0,
+                        segments=segments)
 
 
 # ---------------------------------------------------------------- raw entry points
@@ -156,6 +163,20 @@ def problem_for(q, v, g, chunk, scale=None, variant="auto") -> gdr_problem:
 def gdr_prepare_wy(p, k, v, g, beta, w, u, g_cum, stream=None):
     _check(load().gdr_prepare_wy(ctypes.byref(p), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(w), _ptr(u),
                                  _ptr(g_cum), _stream(stream)), "gdr_prepare_wy")
+
+
+def gdr_scan_transfer(p, k, w, u, g_cum, segments, M, Z, stream=None):
+    _check(load().gdr_scan_transfer(ctypes.byref(p), _ptr(k), _ptr(w), _ptr(u), _ptr(g_cum), int(segments), _ptr(M),
+                                    _ptr(Z), _stream(stream)), "gdr_scan_transfer")
+
+
+def gdr_scan_combine(p, segments, M, Z, h0, h_start, h_final, stream=None):
+    _check(load().gdr_scan_combine(ctypes.byref(p), int(segments), _ptr(M), _ptr(Z), _ptr(h0), _ptr(h_start),
+                                   _ptr(h_final), _stream(stream)), "gdr_scan_combine")
+
+
+def gdr_forward_segments(p) -> int:
+    return int(load().gdr_forward_segments(ctypes.byref(p)))
 
 
 def gdr_scan_h(p, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, stream=None):
@@ -218,7 +239,7 @@ def gdr_version() -> int:
 # ---------------------------------------------------------------- convenience
 
 def forward(q, k, v, g, beta, h0=None, *, chunk=64, scale=None, variant="auto", want_h_final=True,
-            workspace=None, stream=None):
+            workspace=None, stream=None, segments=0):
     """o, h_final = forward(q, k, v, g, beta, h0).
 
     Device tensors are used in place.  CPU tensors are copied to the current
@@ -229,7 +250,7 @@ def forward(q, k, v, g, beta, h0=None, *, chunk=64, scale=None, variant="auto", 
         dev = torch.device("cuda", torch.cuda.current_device())
         q, k, v, g, beta = (t.to(dev, non_blocking=True) for t in (q, k, v, g, beta))
         h0 = h0.to(dev, non_blocking=True) if h0 is not None else None
-    p = problem_for(q, v, g, chunk, scale, variant)
+    p = problem_for(q, v, g, chunk, scale, variant, segments)
     B, T, _, K = q.shape
     H, V = v.shape[2], v.shape[-1]            # value heads
     o = torch.empty(B, T, H, V, device=q.device, dtype=q.dtype)

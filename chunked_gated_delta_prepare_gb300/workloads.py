@@ -58,7 +58,13 @@ KDA_BF16_T8K = Workload("kda_bf16_b2_t8192_h16_d128_c64", 2, 8192, 16, 128, 128,
 GDN_BF16_T32K = Workload("gdn_bf16_b1_t32768_h32_d128_c64", 1, 32768, 32, 128, 128, 64, False, "bf16", True)
 
 ALL = [GDN_F32_T256, GDN_BF16_T2K, GDN_BF16_C32, KDA_BF16_T8K, GDN_BF16_T32K]
-BY_NAME = {w.name: w for w in ALL}
+
+# Not one of the five problem configurations: the throughput workload's sequence with one eighth of
+# its heads.  Its serial scan fills 16 of 152 SMs, the case the segment-parallel scan is for.
+GDN_BF16_T32K_H4 = Workload("gdn_bf16_b1_t32768_h4_d128_c64", 1, 32768, 4, 128, 128, 64, False, "bf16", True)
+EXTRA = [GDN_BF16_T32K_H4]
+
+BY_NAME = {w.name: w for w in ALL + EXTRA}
 
 # The long-context GDN problem is the one throughput is quoted on.
 THROUGHPUT = GDN_BF16_T32K

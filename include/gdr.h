@@ -112,6 +112,8 @@ typedef struct gdr_problem {
     float scale;        /* output scale; <= 0 selects 1/sqrt(K) */
     int32_t variant;    /* gdr_variant */
     int64_t HV;         /* value heads, a multiple of H; 0 means HV = H (see below) */
+    int32_t segments;   /* gdr_forward on the tensor cores: scan each sequence as this many segments
+                           in parallel (see gdr_scan_transfer); 0 = chosen from the problem, 1 = off */
 } gdr_problem;
 
 /*
@@ -144,6 +146,39 @@ GDR_API gdr_status gdr_prepare_wy(const gdr_problem* p, const void* k, const voi
 GDR_API gdr_status gdr_scan_h(const gdr_problem* p, const void* k, const void* w, const void* u,
                       const float* g_cum, const float* h0, void* h_ckpt, void* v_new,
                       float* h_final, void* stream);
+
+/*
+ * The segment-parallel scan, for few sequences and heads at long T.  One chunk of the
+ * scan above is affine in h: h <- A_c h + B_c, A_c = diag(exp(G_last)) - kg^T w [K,K],
+ * B_c = kg^T u [K,V].  So NT / S consecutive chunks are one map h_end = M h_start + Z,
+ * and the S segments of a sequence can be scanned at once once their starting states
+ * are known.  (The pages scan serially; this is the algebra of the recurrence they give.)
+ *
+ * gdr_scan_transfer: for every segment s of every (b, h), M [B,S,H,K,K] = the product of
+ * its A_c (later chunks on the left) and Z [B,S,H,K,V] = the state the segment leaves from
+ * a zero state, both fp32.  Inputs as gdr_scan_h; bf16 io, whole chunks (T % C == 0) and
+ * NT % segments == 0 (GDR_ERR_ARG otherwise); the variant SIMT is GDR_ERR_UNSUPPORTED.
+ *
+ * gdr_scan_combine: h_start[b,0] = h0 (zero if NULL), h_start[b,s+1] = M_s h_start[b,s] + Z_s,
+ * h_final = M_{S-1} h_start[b,S-1] + Z_{S-1}; h_start [B,S,H,K,V] fp32, h_final [B,H,K,V] fp32
+ * or NULL.  fp32 on the CUDA cores; any io dtype (the maps are fp32).
+ *
+ * With h_start in hand, gdr_scan_h or gdr_scan_output run every segment at once on the
+ * problem with B S sequences of T / S tokens and h0 = h_start: every [B,T,...] and
+ * [B,NT,...] tensor has the same memory layout in that view.  gdr_forward does all of
+ * this itself when gdr_forward_segments(p) > 1.
+ */
+GDR_API gdr_status gdr_scan_transfer(const gdr_problem* p, const void* k, const void* w, const void* u,
+                                     const float* g_cum, int32_t segments, float* M, float* Z, void* stream);
+GDR_API gdr_status gdr_scan_combine(const gdr_problem* p, int32_t segments, const float* M, const float* Z,
+                                    const float* h0, float* h_start, float* h_final, void* stream);
+
+/* The number of segments gdr_forward scans this problem in: p->segments when that is > 1 (it must
+ * divide NT, with T % C == 0), 1 for p->segments == 1 and on the CUDA-core path, and for 0 a choice
+ * from the problem: when B * HV * V / 32 (the serial scan's CTAs) is at most 76, the largest divisor
+ * of NT whose segments keep at least 16 chunks and whose segmented grid fits 152 SMs.  0 for a
+ * problem gdr_forward would reject. */
+GDR_API int gdr_forward_segments(const gdr_problem* p);
 
 /*
  * Stage 3: chunk output.  Per (b, h, chunk c), with G = g_cum of the chunk:

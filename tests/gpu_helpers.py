@@ -53,11 +53,11 @@ def problem(x, C, variant="auto", scale=None):
     return gdr.problem_for(x.q, x.v, x.g, C, scale, variant)
 
 
-def gpu_forward(x, C, variant="auto", scale=None, want_h_final=True, h0="inputs"):
+def gpu_forward(x, C, variant="auto", scale=None, want_h_final=True, h0="inputs", segments=0):
     """gdr_forward through the C ABI on device copies of the inputs."""
     q, k, v, g, beta = (dev(t) for t in (x.q, x.k, x.v, x.g, x.beta))
     h0d = dev(x.h0) if h0 == "inputs" else dev(h0)
-    p = gdr.problem_for(q, v, g, C, scale, variant)
+    p = gdr.problem_for(q, v, g, C, scale, variant, segments)
     B, T, _, K = q.shape
     H, V = v.shape[2], v.shape[-1]            # value heads
     o = torch.full((B, T, H, V), float("nan"), device="cuda", dtype=q.dtype)

@@ -157,8 +157,32 @@ def test_fused_workspace_size_formula(lib):
         rows = B * T * H
         want = r(rows * 4) + r(rows * K * 2) + r(rows * V * 2) + (r(rows * C * 2) if C == 64 else 0)
         for variant in ("fused", "auto" if C == 64 else "fused"):
-            p = gdr.make_problem(B, T, H, K, V, C, 1, False, variant=variant)
+            p = gdr.make_problem(B, T, H, K, V, C, 1, False, variant=variant, segments=1)
             assert lib.gdr_forward_workspace_bytes(ctypes.byref(p)) == want
+
+
+def test_segment_choice_and_workspace(lib):
+    # automatic segments: only when the serial scan's B H V/32 CTAs fill at most half of 152 SMs; the
+    # largest divisor S of NT with S B H V/32 <= 152 and NT / S >= 16
+    r = lambda x: (x + 255) // 256 * 256
+    seg = lambda *a, **kw: lib.gdr_forward_segments(ctypes.byref(gdr.make_problem(*a, **kw)))
+    assert seg(1, 32768, 32, 128, 128, 64, 1, False) == 1                   # 128 CTAs: serial
+    assert seg(1, 32768, 4, 128, 128, 64, 1, False) == 8                    # 16 CTAs: 152 // 16 = 9 -> 8
+    assert seg(2, 4096, 8, 64, 64, 32, 1, False) == 4                       # 32 CTAs, NT = 128
+    assert seg(1, 2048, 1, 128, 128, 64, 1, True) == 2                      # NT = 32: segments of 16 chunks
+    assert seg(1, 1024, 1, 128, 128, 64, 1, False) == 1                     # too short
+    assert seg(1, 32768, 4, 128, 128, 64, 1, False, segments=1) == 1
+    assert seg(1, 32768, 4, 128, 128, 64, 1, False, segments=32) == 32     # explicit
+    assert seg(1, 32768, 4, 128, 128, 64, 0, False) == 1                    # fp32: the CUDA-core path
+    assert seg(1, 32768, 4, 128, 128, 64, 1, False, segments=3) == 0        # does not divide NT
+    assert seg(1, 32760, 4, 128, 128, 64, 1, False, segments=2) == 0        # a partial chunk
+    assert seg(1, 32768, 4, 128, 128, 64, 1, False, segments=-1) == 0
+    B, T, H, K, V, C, S = 1, 32768, 4, 128, 128, 64, 8
+    rows = B * T * H
+    base = r(rows * 4) + r(rows * K * 2) + r(rows * V * 2) + r(rows * C * 2)
+    maps = B * S * H * K
+    p = gdr.make_problem(B, T, H, K, V, C, 1, False)
+    assert lib.gdr_forward_workspace_bytes(ctypes.byref(p)) == base + r(maps * K * 4) + 2 * r(maps * V * 4)
 
 
 def test_stage_entry_points_validate(lib):

@@ -289,3 +289,57 @@ def test_grouping_by_remainder_is_caught():
                h0=d["h0"][:, hv:hv + 1])
     eo, _ = explicit_matrix_recurrence(one, 0.4)
     assert np.abs(got["o"][:, :, hv:hv + 1] - eo).max() > 1e-6
+
+
+# ------------------------------------------------------------ segment maps
+
+SEGMENTS_SRC = os.path.join(ROOT, "oracle", "segments.py")
+
+SEGMENT_MUTANTS = [
+    ("chunk maps composed in the wrong order", "m = A[:, c] @ m", "m = m @ A[:, c]"),
+    ("Z not carried through later chunks", "z = A[:, c] @ z + Bc[:, c]", "z = z + Bc[:, c]"),
+    ("decay dropped from the chunk map", 'A = np.einsum("...d,de->...de", decay, np.eye(K)) - ',
+     "A = np.eye(K) - "),
+    ("kg without its gate", "kg = kc * np.exp(G_last - Gc)", "kg = kc"),
+    ("segment start recorded after its update", "        starts[:, s] = h\n        h = M[:, s] @ h + Z[:, s]",
+     "        h = M[:, s] @ h + Z[:, s]\n        starts[:, s] = h"),
+]
+
+
+def _segment_pins_fail(mod) -> bool:
+    import test_oracle_segment_pins as pins
+    checks = [lambda: pins.test_one_token_chunks_are_reflections()]
+    for per_k in (False, True):
+        checks.append(lambda per_k=per_k: pins.test_no_delta_step_leaves_the_decay(per_k))
+        checks.append(lambda per_k=per_k: pins.test_stitched_maps_reproduce_the_serial_scan(per_k, 16, 4))
+    saved = pins.segments
+    pins.segments = mod
+    try:
+        for check in checks:
+            try:
+                check()
+            except Exception:
+                return True
+        return False
+    finally:
+        pins.segments = saved
+
+
+def _load_segments(src: str):
+    mod = types.ModuleType("oracle.segments_mutant")
+    mod.__package__ = "oracle"
+    exec(compile(src, "segments_mutant.py", "exec"), mod.__dict__)
+    return mod
+
+
+def test_unmutated_segments_pass_the_pins():
+    with open(SEGMENTS_SRC) as f:
+        assert not _segment_pins_fail(_load_segments(f.read()))
+
+
+@pytest.mark.parametrize("what,old,new", SEGMENT_MUTANTS, ids=[m[0] for m in SEGMENT_MUTANTS])
+def test_segment_mutant_is_caught(what, old, new):
+    with open(SEGMENTS_SRC) as f:
+        src = f.read()
+    assert src.count(old) == 1, f"mutation site not found: {old!r}"
+    assert _segment_pins_fail(_load_segments(src.replace(old, new)))

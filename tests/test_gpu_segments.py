@@ -131,3 +131,15 @@ def test_segment_arguments_are_checked():
     with pytest.raises(gdr.GdrError) as e:
         gdr.gdr_scan_transfer(gdr.problem_for(x.q, x.v, x.g, 64), t, t, t, gf, 3, m, m)
     assert e.value.status == 9
+
+
+def test_low_head_count_workload_full_size():
+    # the 32k-token sequence with 4 heads: the library picks 8 segments; two heads checked on every token
+    from chunked_gated_delta_prepare_gb300 import workloads
+    from chunked_gated_delta_prepare_gb300.inputs import make_workload_inputs
+    wl = workloads.GDN_BF16_T32K_H4
+    x = make_workload_inputs(wl)
+    assert gdr.gdr_forward_segments(gdr.problem_for(x.q, x.v, x.g, wl.chunk)) == 8
+    o, hf, ran = gpu_forward(x, wl.chunk)
+    assert ran == "fused" and torch.isfinite(o).all() and torch.isfinite(hf).all()
+    check_forward(x, o, hf, [(0, 0), (0, 3)], wl.chunk, 1.0 / np.sqrt(wl.K), wl.io)

@@ -139,13 +139,14 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def traffic_for(kernel_name: str):
-    """DRAM bytes per launch from the committed ncu summary, or None when the kernel
-    source changed after the counters were taken."""
+def traffic_for(kernel_name: str, workload: str):
+    """DRAM bytes per launch of a kernel on a workload from the committed ncu summary, or
+    None when there is no record or the kernel source changed after the counters were taken."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
         with open(path) as f:
-            rec = json.load(f)[kernel_name]
+            recs = json.load(f)["records"]
+        rec = next(r for r in recs if r["kernel"] == kernel_name and r["workload"] == workload)
         src = os.path.join(ROOT, rec["source"])
         with open(src, "rb") as f:
             digest = hashlib.sha256(f.read()).hexdigest()
@@ -473,7 +474,7 @@ def run_ours(args, wl):
              "combine": "segment_combine_kernel"}[dom_name]
     if stage_variant[dom] == "simt":
         kname = f"simt_{dom_name}_kernel"
-    traffic = traffic_for(kname)
+    traffic = traffic_for(kname, wl.name)
 
     # end to end through the public API: pinned host inputs in, o and h_final back to host
     hx = {n_: t.pin_memory() for n_, t in x.tensors().items() if t is not None}

@@ -253,7 +253,7 @@ def time_backward(args, wl, x, dev, flush, stream, world):
     gen = torch.Generator().manual_seed(7)
     d_o = torch.randn(B, T, H, V, generator=gen).to(q.dtype).to(dev)
     dhf = torch.randn(B, H, K, V, generator=gen).to(dev)
-    p = gdr.problem_for(q, v, g, C, None, args.variant)
+    p = gdr.problem_for(q, v, g, C, None, args.variant, args.segments)
     if gdr.gdr_backward_workspace_bytes(p) == 0:
         return None
     NT = -(-T // C)
@@ -267,7 +267,18 @@ def time_backward(args, wl, x, dev, flush, stream, world):
     dq, dk, dv, dbeta = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(beta)
     dg, dh0 = torch.empty(g.shape, **f32), torch.empty(B, H, K, V, **f32)
     fast = q.dtype == torch.bfloat16 and g.dim() == 3 and args.variant in ("auto", "tensor")
-    if fast and C == 32:
+    S = gdr.gdr_forward_segments(p) if q.dtype == torch.bfloat16 and args.variant != "simt" else 1
+    launches_per_call = 1
+    if S > 1:
+        # segment-parallel: gdr_backward as one call (prepare, transfer, stitch, re-scan, [local term],
+        # reverse scan twice around the reverse stitch, the per-chunk stage [+ its two filtered stages])
+        nbytes = gdr.gdr_backward_workspace_bytes(p)
+        ws = torch.empty(nbytes, device=dev, dtype=torch.uint8)
+        hf0 = h0
+        launches_per_call = 8 + (0 if fast and C == 64 else 1) + (0 if fast else 2)
+        names = [f"backward_segmented_S{S}"]
+        calls = [lambda: gdr.gdr_backward(p, q, k, v, g, beta, hf0, d_o, dhf, dq, dk, dv, dg, dbeta, dh0, ws, nbytes)]
+    elif fast and C == 32:
         # the tensor-core path at 32-token chunks: the local term from its own kernel
         tinv = torch.empty(B, NT, H, C, C, device=dev, dtype=q.dtype)
         dv_loc16 = torch.empty(B, T, H, V, device=dev, dtype=q.dtype)
@@ -349,7 +360,8 @@ def time_backward(args, wl, x, dev, flush, stream, world):
     total_s = max_over_ranks(sum(evs[s][0].elapsed_time(evs[s][n]) for s in range(steps)) / 1e3, world)
     return {"ms_per_step": 1e3 * total_s / steps, "steps": steps,
             "value": weak_scaling_throughput(world, B * T, steps, total_s), "unit": "tokens/s",
-            "kernel_ms": {f"{names[i]}[{ran[i]}]": per[i] for i in range(n)}, "gpu_launches": n * steps,
+            "kernel_ms": {f"{names[i]}[{ran[i]}]": per[i] for i in range(n)},
+            "gpu_launches": n * launches_per_call * steps, "segments": S,
             "upstream": "do ~ N(0,1) in the io dtype, dh_final ~ N(0,1) fp32, seed 7"}
 
 

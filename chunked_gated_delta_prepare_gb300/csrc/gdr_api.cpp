@@ -133,9 +133,9 @@ gdr::Dims segment_view(const gdr::Dims& d, int S) {
 constexpr int kSmCount = 152;
 constexpr int kSegMinChunks = 16;
 
-gdr_status resolve_segments(const gdr_problem* p, const gdr::Dims& d, Path path, int* S) {
+gdr_status resolve_segments(const gdr_problem* p, const gdr::Dims& d, bool tensor, int* S) {
     *S = 1;
-    if (p->segments == 1 || path == Path::Simt) return GDR_OK;
+    if (p->segments == 1 || !tensor) return GDR_OK;
     if (p->segments > 1) {
         if (d.T % d.C != 0 || d.NT % p->segments != 0 || p->segments > kMaxGridYZ / d.B) return GDR_ERR_ARG;
         *S = (int)p->segments;
@@ -191,7 +191,7 @@ StagedWorkspace plan_staged(const gdr::Dims& d, bool fused, int S) {
 // backward's fp32 intermediates, each 256-byte aligned.
 struct BackwardWorkspace {
     size_t g_cum, w, u, v_new, h_ckpt, dv_loc, dv_new, dh_ckpt, dk_part, dw, dG_part, P, tinv, flags, dq_v, dk_v,
-        total;
+        seg_m, seg_z, seg_h, seg_zb, seg_e, total;
 };
 
 // The backward's paths: every stage on the CUDA cores (SIMT); every stage on the tensor cores for a
@@ -199,7 +199,7 @@ struct BackwardWorkspace {
 // finishing the chunks whose gate the split-gate products cannot take (TENSOR: bf16).
 enum class BwdPath { Simt, Tensor, Fast };
 
-BackwardWorkspace plan_backward(const gdr::Dims& d, BwdPath path) {
+BackwardWorkspace plan_backward(const gdr::Dims& d, BwdPath path, int S) {
     const size_t e = (d.bf16 || d.f16) ? 2 : 4;
     const size_t rows = (size_t)d.B * d.T * d.H;
     const size_t gw = d.per_k ? d.K : 1;
@@ -241,6 +241,14 @@ BackwardWorkspace plan_backward(const gdr::Dims& d, BwdPath path) {
     if (d.G > 1) {   // per-value-head dq and dk, summed over each group at the end
         take(&ws.dq_v, rows * d.K * e);
         take(&ws.dk_v, rows * d.K * e);
+    }
+    if (S > 1) {     // the segment maps, the re-scan's segment starts, the reverse scan's offsets and ends
+        const size_t maps = (size_t)d.B * S * d.H * d.K;
+        take(&ws.seg_m, maps * d.K * 4);
+        take(&ws.seg_z, maps * d.V * 4);
+        take(&ws.seg_h, maps * d.V * 4);
+        take(&ws.seg_zb, maps * d.V * 4);
+        take(&ws.seg_e, maps * d.V * 4);
     }
     ws.total = off;
     return ws;
@@ -322,6 +330,18 @@ gdr_status gdr_scan_combine(const gdr_problem* p, int32_t segments, const float*
     return st;
 }
 
+gdr_status gdr_scan_combine_reverse(const gdr_problem* p, int32_t segments, const float* M, const float* Zb,
+                                    const float* dh_final, float* ends, float* dh0, void* stream) {
+    gdr::Dims d;
+    gdr_status st = check_problem(p, &d);
+    if (st != GDR_OK) return st;
+    if ((st = check_ptrs({M, Zb, ends}, {dh_final, dh0})) != GDR_OK) return st;
+    if (segments < 1 || segments > kMaxGridYZ / d.B) return GDR_ERR_ARG;
+    st = from_cuda(gdr::segment_combine(d, segments, M, Zb, dh_final, ends, dh0, (cudaStream_t)stream, true));
+    if (st == GDR_OK) t_last_variant = "simt";
+    return st;
+}
+
 gdr_status gdr_chunk_output(const gdr_problem* p, const void* q, const void* k, const void* v_new,
                             const void* h_ckpt, const float* g_cum, void* o, void* stream) {
     gdr::Dims d;
@@ -342,7 +362,7 @@ size_t gdr_forward_workspace_bytes(const gdr_problem* p) {
     if (check_problem(p, &d) != GDR_OK) return 0;
     Path path;
     int S = 1;
-    if (pick_forward(p, d, &path) != GDR_OK || resolve_segments(p, d, path, &S) != GDR_OK) return 0;
+    if (pick_forward(p, d, &path) != GDR_OK || resolve_segments(p, d, path != Path::Simt, &S) != GDR_OK) return 0;
     return plan_staged(d, path == Path::Fused, S).total;
 }
 
@@ -351,7 +371,7 @@ int gdr_forward_segments(const gdr_problem* p) {
     if (check_problem(p, &d) != GDR_OK) return 0;
     Path path;
     int S = 1;
-    if (pick_forward(p, d, &path) != GDR_OK || resolve_segments(p, d, path, &S) != GDR_OK) return 0;
+    if (pick_forward(p, d, &path) != GDR_OK || resolve_segments(p, d, path != Path::Simt, &S) != GDR_OK) return 0;
     return S;
 }
 
@@ -365,7 +385,7 @@ gdr_status gdr_forward(const gdr_problem* p, const void* q, const void* k, const
     Path path;
     if ((st = pick_forward(p, d, &path)) != GDR_OK) return st;
     int S = 1;
-    if ((st = resolve_segments(p, d, path, &S)) != GDR_OK) return st;
+    if ((st = resolve_segments(p, d, path != Path::Simt, &S)) != GDR_OK) return st;
     const StagedWorkspace ws = plan_staged(d, path == Path::Fused, S);
     if (!workspace || workspace_bytes < ws.total) return GDR_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GDR_ERR_ALIGN;
@@ -585,8 +605,9 @@ size_t gdr_backward_workspace_bytes(const gdr_problem* p) {
     gdr::Dims d;
     if (check_problem(p, &d) != GDR_OK) return 0;
     BwdPath path;
-    if (pick_backward(p, d, &path) != GDR_OK) return 0;
-    return plan_backward(d, path).total;
+    int S = 1;
+    if (pick_backward(p, d, &path) != GDR_OK || resolve_segments(p, d, path != BwdPath::Simt, &S) != GDR_OK) return 0;
+    return plan_backward(d, path, S).total;
 }
 
 gdr_status gdr_backward(const gdr_problem* p, const void* q, const void* k, const void* v, const float* g,
@@ -600,7 +621,9 @@ gdr_status gdr_backward(const gdr_problem* p, const void* q, const void* k, cons
     BwdPath path;
     if ((st = pick_backward(p, d, &path)) != GDR_OK) return st;
     const bool tensor = path != BwdPath::Simt;
-    const BackwardWorkspace ws = plan_backward(d, path);
+    int S = 1;
+    if ((st = resolve_segments(p, d, tensor, &S)) != GDR_OK) return st;
+    const BackwardWorkspace ws = plan_backward(d, path, S);
     if (!workspace || workspace_bytes < ws.total) return GDR_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GDR_ERR_ALIGN;
     char* base = static_cast<char*>(workspace);
@@ -623,6 +646,30 @@ gdr_status gdr_backward(const gdr_problem* p, const void* q, const void* k, cons
         dq = base + ws.dq_v;
         dk = base + ws.dk_v;
     }
+    // The two serial scans, segment-parallel when S > 1.  The re-scan as the forward does it; the reverse
+    // scan once from a zero gradient at every segment end (its dh0 per segment are the offsets Zb), the
+    // reverse stitch with the forward maps transposed, then again from the stitched segment ends.
+    float* seg_m = reinterpret_cast<float*>(base + ws.seg_m);
+    float* seg_z = reinterpret_cast<float*>(base + ws.seg_z);
+    float* seg_h = reinterpret_cast<float*>(base + ws.seg_h);
+    float* seg_zb = reinterpret_cast<float*>(base + ws.seg_zb);
+    float* seg_e = reinterpret_cast<float*>(base + ws.seg_e);
+    auto rescan = [&](unsigned int* err) -> gdr_status {
+        if (S == 1) return from_cuda(gdr::mma_scan(d, k, w, u, g_cum, h0, h_ckpt, v_new, nullptr, s, err));
+        const gdr::Dims ds = segment_view(d, S);
+        gdr_status r = from_cuda(gdr::mma_scan_transfer(ds, k, w, u, g_cum, seg_m, seg_z, s, err));
+        if (r == GDR_OK) r = from_cuda(gdr::segment_combine(d, S, seg_m, seg_z, h0, seg_h, nullptr, s));
+        if (r == GDR_OK) r = from_cuda(gdr::mma_scan(ds, k, w, u, g_cum, seg_h, h_ckpt, v_new, nullptr, s, err));
+        return r;
+    };
+    auto reverse_scan = [&](auto run) -> gdr_status {   // run(dims, dh_final, dh0)
+        if (S == 1) return run(d, dh_final, dh0);
+        const gdr::Dims ds = segment_view(d, S);
+        gdr_status r = run(ds, nullptr, seg_zb);
+        if (r == GDR_OK) r = from_cuda(gdr::segment_combine(d, S, seg_m, seg_zb, dh_final, seg_e, dh0, s, true));
+        if (r == GDR_OK) r = run(ds, seg_e, nullptr);
+        return r;
+    };
     if (path == BwdPath::Fast) {
         // every step on the tensor cores: prepare (+ P and T), re-scan, reverse scan, per-chunk stage
         unsigned int* err = device_error_word();
@@ -631,21 +678,22 @@ gdr_status gdr_backward(const gdr_problem* p, const void* q, const void* k, cons
             void* P = base + ws.P;
             if ((st = from_cuda(gdr::mma_prepare(d, k, v, g, beta, w, u, g_cum, s, err, q, P, tinv))) != GDR_OK)
                 return st;
-            if ((st = from_cuda(gdr::mma_scan(d, k, w, u, g_cum, h0, h_ckpt, v_new, nullptr, s, err))) != GDR_OK)
-                return st;
-            if ((st = from_cuda(gdr::mma_bwd_scan(d, q, k, w, g_cum, P, d_o, dh_final, dh_ckpt, dv_new, dh0, s,
-                                                  err))) != GDR_OK)
-                return st;
+            if ((st = rescan(err)) != GDR_OK) return st;
+            st = reverse_scan([&](const gdr::Dims& dd, const float* dhf, float* dh0o) {
+                return from_cuda(gdr::mma_bwd_scan(dd, q, k, w, g_cum, P, d_o, dhf, dh_ckpt, dv_new, dh0o, s, err));
+            });
+            if (st != GDR_OK) return st;
         } else {           // C = 32: the local term from its own kernel
             if ((st = from_cuda(gdr::mma_prepare(d, k, v, g, beta, w, u, g_cum, s, err, nullptr, nullptr, tinv))) !=
                 GDR_OK)
                 return st;
-            if ((st = from_cuda(gdr::mma_scan(d, k, w, u, g_cum, h0, h_ckpt, v_new, nullptr, s, err))) != GDR_OK)
-                return st;
+            if ((st = rescan(err)) != GDR_OK) return st;
             if ((st = from_cuda(gdr::mma_bwd_dv_local(d, q, k, g_cum, d_o, dv_loc, s))) != GDR_OK) return st;
-            if ((st = from_cuda(gdr::mma_bwd_scan_dl(d, q, k, w, g_cum, dv_loc, d_o, dh_final, dh_ckpt, dv_new, dh0, s,
-                                                     err))) != GDR_OK)
-                return st;
+            st = reverse_scan([&](const gdr::Dims& dd, const float* dhf, float* dh0o) {
+                return from_cuda(gdr::mma_bwd_scan_dl(dd, q, k, w, g_cum, dv_loc, d_o, dhf, dh_ckpt, dv_new, dh0o, s,
+                                                      err));
+            });
+            if (st != GDR_OK) return st;
         }
         if ((st = from_cuda(gdr::mma_bwd_chunk(d, q, k, v, beta, g_cum, w, u, tinv, v_new, h_ckpt, d_o, dv_new, dh_ckpt,
                                                dq, dk, dv, dbeta, dg, s))) != GDR_OK)
@@ -664,11 +712,12 @@ gdr_status gdr_backward(const gdr_problem* p, const void* q, const void* k, cons
         if ((st = from_cuda(gdr::mma_prepare(d, k, v, g, beta, w, u, g_cum, s, err, nullptr, nullptr, tinv))) !=
             GDR_OK)
             return st;
-        if ((st = from_cuda(gdr::mma_scan(d, k, w, u, g_cum, h0, h_ckpt, v_new, nullptr, s, err))) != GDR_OK) return st;
+        if ((st = rescan(err)) != GDR_OK) return st;
         if ((st = from_cuda(gdr::mma_bwd_dv_local(d, q, k, g_cum, d_o, dv_loc, s))) != GDR_OK) return st;
-        if ((st = from_cuda(gdr::mma_bwd_scan_dl(d, q, k, w, g_cum, dv_loc, d_o, dh_final, dh_ckpt, dv_new, dh0, s,
-                                                 err))) != GDR_OK)
-            return st;
+        st = reverse_scan([&](const gdr::Dims& dd, const float* dhf, float* dh0o) {
+            return from_cuda(gdr::mma_bwd_scan_dl(dd, q, k, w, g_cum, dv_loc, d_o, dhf, dh_ckpt, dv_new, dh0o, s, err));
+        });
+        if (st != GDR_OK) return st;
         if ((st = from_cuda(gdr::mma_bwd_chunk_kda(d, q, k, v, beta, g_cum, w, u, tinv, v_new, h_ckpt, d_o, dv_new,
                                                    dh_ckpt, dq, dk, dv, dbeta, dg, flags, s))) != GDR_OK)
             return st;

@@ -38,11 +38,13 @@ cudaError_t mma_scan(const Dims& d, const void* k, const void* w, const void* u,
                      void* h_ckpt, void* v_new, float* h_final, cudaStream_t s, unsigned int* err);
 // the segment-parallel scan: on the segment view (B S sequences of T / S tokens), every segment's affine
 // map h_end = M h_start + Z (M [B S, H, K, K], Z [B S, H, K, V], fp32), then the serial stitch of the maps
-// into the segments' starting states h_start [B S, H, K, V] and h_final [B, H, K, V] (NULL: not written)
+// into the segments' starting states h_start [B S, H, K, V] and h_final [B, H, K, V] (NULL: not written).
+// reverse: the backward's stitch, end[S-1] = h0 (dh_final), end[s-1] = M_s^T end[s] + Z_s, into h_start
+// (the segment ends) and h_final (dh0).
 cudaError_t mma_scan_transfer(const Dims& d_view, const void* k, const void* w, const void* u, const float* g_cum,
                               float* m_out, float* z_out, cudaStream_t s, unsigned int* err);
 cudaError_t segment_combine(const Dims& d, int S, const float* M, const float* Z, const float* h0, float* h_start,
-                            float* h_final, cudaStream_t s);
+                            float* h_final, cudaStream_t s, bool reverse = false);
 cudaError_t tc_output(const Dims& d, const void* q, const void* k, const void* v_new, const void* h_ckpt,
                       const float* g_cum, void* o, cudaStream_t s, unsigned int* err);
 

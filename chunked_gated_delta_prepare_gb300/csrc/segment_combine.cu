@@ -7,6 +7,12 @@
 //   h_start[0] = h0 (zero if NULL);  h_start[s + 1] = M_s h_start[s] + Z_s;
 //   h_final = M_{S-1} h_start[S-1] + Z_{S-1}
 //
+// REVERSE stitches the backward's state gradient the other way: the reverse
+// scan maps the gradient at a segment's end to the one at its start by M_s^T
+// (the transpose of the forward map) plus Zb_s, so
+//
+//   end[S-1] = dh_final (zero if NULL);  end[s-1] = M_s^T end[s] + Zb_s;  dh0 = M_0^T end[0] + Zb_0.
+//
 // The chain is serial in s, so its latency is the cost: narrow column slices
 // give many CTAs, and M_{s+1} and Z_{s+1} stream into shared memory (cp.async,
 // double-buffered) while step s computes.  A warp owns K/8 rows of the output;
@@ -31,7 +37,9 @@ __device__ __forceinline__ void cp16(void* dst, const void* src) {
 __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
-template <int K>
+// h0: the forward's h0 or the backward's dh_final; h_start: the segment starts (forward) or ends
+// (REVERSE); h_final: h_final (forward) or dh0 (REVERSE)
+template <int K, bool REVERSE>
 __global__ void __launch_bounds__(kThreads)
 segment_combine_kernel(const float* __restrict__ M, const float* __restrict__ Z, const float* __restrict__ h0,
                        float* __restrict__ h_start, float* __restrict__ h_final, int S, int H, int V) {
@@ -47,13 +55,15 @@ segment_combine_kernel(const float* __restrict__ M, const float* __restrict__ Z,
     const int v0 = blockIdx.x * kCB, h = blockIdx.y, b = blockIdx.z;
     const int64_t hb = ((int64_t)b * H + h) * K * V;
 
-    // M_s and the CTA's 8 columns of Z_s into buffer s & 1
-    auto prefetch = [&](int s) {
+    // step i of the chain handles segment s(i): i forward, S - 1 - i in REVERSE; buffers alternate with i
+    auto seg_of = [&](int i) { return REVERSE ? S - 1 - i : i; };
+    auto prefetch_step = [&](int i) {
+        const int s = seg_of(i);
         const int64_t seg = ((int64_t)b * S + s) * H + h;
         const float* Mg = M + seg * K * K;
         const float* Zg = Z + seg * K * V + v0;
-        float* md = Ms + (s & 1) * K * LM;
-        float* zd = Zs + (s & 1) * K * kCB;
+        float* md = Ms + (i & 1) * K * LM;
+        float* zd = Zs + (i & 1) * K * kCB;
         for (int e = tid; e < K * K / 4; e += kThreads) {
             const int row = e / (K / 4), c4 = e % (K / 4);
             cp16(md + row * LM + 4 * c4, Mg + (int64_t)row * K + 4 * c4);
@@ -62,23 +72,24 @@ segment_combine_kernel(const float* __restrict__ M, const float* __restrict__ Z,
             cp16(zd + (e >> 1) * kCB + 4 * (e & 1), Zg + (int64_t)(e >> 1) * V + 4 * (e & 1));
         cp_commit();
     };
-    prefetch(0);
+    prefetch_step(0);
     for (int e = tid; e < K * kCB; e += kThreads)
         hs[e] = h0 ? h0[hb + (int64_t)(e / kCB) * V + v0 + e % kCB] : 0.f;
-    for (int s = 0; s < S; ++s) {
-        const float* hcur = hs + (s & 1) * K * kCB;
-        float* hnext = hs + ((s + 1) & 1) * K * kCB;
+    for (int i = 0; i < S; ++i) {
+        const int s = seg_of(i);
+        const float* hcur = hs + (i & 1) * K * kCB;
+        float* hnext = hs + ((i + 1) & 1) * K * kCB;
         cp_wait_all();
-        __syncthreads();   // M_s, Z_s and h_s in place; every thread is done with step s - 1's buffers
-        if (s + 1 < S) prefetch(s + 1);
-        // h_start[s]: this CTA's [K x 8] slice
+        __syncthreads();   // M, Z and h of this step in place; every thread is done with the last step's buffers
+        if (i + 1 < S) prefetch_step(i + 1);
+        // this step's boundary value (a segment's start, or in REVERSE its end): this CTA's [K x 8] slice
         {
             const int64_t sb = (((int64_t)b * S + s) * H + h) * K * V;
             for (int e = tid; e < K * 2; e += kThreads)
                 *reinterpret_cast<float4*>(h_start + sb + (int64_t)(e >> 1) * V + v0 + 4 * (e & 1)) =
                     *reinterpret_cast<const float4*>(hcur + (e >> 1) * kCB + 4 * (e & 1));
         }
-        const float* Mc = Ms + (s & 1) * K * LM;
+        const float* Mc = Ms + (i & 1) * K * LM;
         float acc[RG][kCB];
 #pragma unroll
         for (int g = 0; g < RG; ++g)
@@ -90,15 +101,16 @@ segment_combine_kernel(const float* __restrict__ M, const float* __restrict__ Z,
             const float4 h1v = *reinterpret_cast<const float4*>(hcur + j * kCB + 4);
 #pragma unroll
             for (int g = 0; g < RG; ++g) {
-                const float m = Mc[(warp * RPW + 8 * g + r) * LM + j];
+                const int row = warp * RPW + 8 * g + r;
+                const float m = REVERSE ? Mc[j * LM + row] : Mc[row * LM + j];   // M^T in REVERSE
                 acc[g][0] = fmaf(m, h0v.x, acc[g][0]); acc[g][1] = fmaf(m, h0v.y, acc[g][1]);
                 acc[g][2] = fmaf(m, h0v.z, acc[g][2]); acc[g][3] = fmaf(m, h0v.w, acc[g][3]);
                 acc[g][4] = fmaf(m, h1v.x, acc[g][4]); acc[g][5] = fmaf(m, h1v.y, acc[g][5]);
                 acc[g][6] = fmaf(m, h1v.z, acc[g][6]); acc[g][7] = fmaf(m, h1v.w, acc[g][7]);
             }
         }
-        // the four partial sums of each row, then + Z_s into h_{s+1}
-        const float* Zc = Zs + (s & 1) * K * kCB;
+        // the four partial sums of each row, then + Z_s into the next step's value
+        const float* Zc = Zs + (i & 1) * K * kCB;
 #pragma unroll
         for (int g = 0; g < RG; ++g) {
 #pragma unroll
@@ -120,17 +132,17 @@ segment_combine_kernel(const float* __restrict__ M, const float* __restrict__ Z,
     }
     __syncthreads();
     if (h_final) {
-        const float* hl = hs + (S & 1) * K * kCB;
+        const float* hl = hs + (S & 1) * K * kCB;   // written by the last step
         for (int e = tid; e < K * 2; e += kThreads)
             *reinterpret_cast<float4*>(h_final + hb + (int64_t)(e >> 1) * V + v0 + 4 * (e & 1)) =
                 *reinterpret_cast<const float4*>(hl + (e >> 1) * kCB + 4 * (e & 1));
     }
 }
 
-template <int K>
+template <int K, bool REVERSE>
 cudaError_t launch(const Dims& d, int S, const float* M, const float* Z, const float* h0, float* h_start,
                    float* h_final, cudaStream_t s) {
-    auto kern = segment_combine_kernel<K>;
+    auto kern = segment_combine_kernel<K, REVERSE>;
     const size_t smem = sizeof(float) * (2 * K * (K + 4) + 4 * K * kCB);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -142,10 +154,13 @@ cudaError_t launch(const Dims& d, int S, const float* M, const float* Z, const f
 }  // namespace
 
 cudaError_t segment_combine(const Dims& d, int S, const float* M, const float* Z, const float* h0, float* h_start,
-                            float* h_final, cudaStream_t s) {
+                            float* h_final, cudaStream_t s, bool reverse) {
     if (S < 1) return cudaErrorInvalidValue;
-    return d.K == 64 ? launch<64>(d, S, M, Z, h0, h_start, h_final, s)
-                     : launch<128>(d, S, M, Z, h0, h_start, h_final, s);
+    if (reverse)
+        return d.K == 64 ? launch<64, true>(d, S, M, Z, h0, h_start, h_final, s)
+                         : launch<128, true>(d, S, M, Z, h0, h_start, h_final, s);
+    return d.K == 64 ? launch<64, false>(d, S, M, Z, h0, h_start, h_final, s)
+                     : launch<128, false>(d, S, M, Z, h0, h_start, h_final, s);
 }
 
 }  // namespace gdr

@@ -5,7 +5,8 @@ kernels.  PyTorch supplies device memory and the current stream.  There is no
 CPU fallback: if the library is missing or cannot load, every call raises.
 
 The functions mirror the C ABI names:
-    gdr_prepare_wy, gdr_prepare_wyp, gdr_scan_h, gdr_scan_transfer, gdr_scan_combine, gdr_chunk_output,
+    gdr_prepare_wy, gdr_prepare_wyp, gdr_scan_h, gdr_scan_transfer, gdr_scan_combine, gdr_scan_combine_reverse,
+    gdr_chunk_output,
     gdr_scan_output, gdr_forward, gdr_forward_workspace_bytes, gdr_forward_segments, gdr_bwd_dv_local, gdr_bwd_scan_dh, gdr_bwd_dqkwg, gdr_bwd_wy,
     gdr_bwd_prepare, gdr_bwd_scan_dh_p, gdr_bwd_wy_dqkg, gdr_backward, gdr_backward_workspace_bytes,
     gdr_status_string, gdr_get_device_status,
@@ -36,7 +37,7 @@ EXPORTS = ["gdr_prepare_wy", "gdr_scan_h", "gdr_chunk_output", "gdr_forward", "g
            "gdr_bwd_dv_local", "gdr_bwd_scan_dh", "gdr_bwd_dqkwg", "gdr_bwd_wy", "gdr_backward",
            "gdr_backward_workspace_bytes", "gdr_bwd_prepare", "gdr_bwd_scan_dh_p", "gdr_bwd_wy_dqkg",
            "gdr_bwd_group_sum", "gdr_bwd_dv_local_tc", "gdr_bwd_scan_dh_tc", "gdr_scan_transfer",
-           "gdr_scan_combine", "gdr_forward_segments",
+           "gdr_scan_combine", "gdr_scan_combine_reverse", "gdr_forward_segments",
            "gdr_status_string", "gdr_get_device_status", "gdr_last_variant", "gdr_version"]
 
 
@@ -92,6 +93,7 @@ def load(path: str | None = None):
             "gdr_bwd_scan_dh_tc": [P] + [vp] * 11,
             "gdr_scan_transfer": [P, vp, vp, vp, vp, ctypes.c_int32, vp, vp, vp],
             "gdr_scan_combine": [P, ctypes.c_int32, vp, vp, vp, vp, vp, vp],
+            "gdr_scan_combine_reverse": [P, ctypes.c_int32, vp, vp, vp, vp, vp, vp],
             "gdr_forward_segments": [P],
             "gdr_status_string": [ctypes.c_int],
             "gdr_get_device_status": [vp],
@@ -173,6 +175,11 @@ def gdr_scan_transfer(p, k, w, u, g_cum, segments, M, Z, stream=None):
 def gdr_scan_combine(p, segments, M, Z, h0, h_start, h_final, stream=None):
     _check(load().gdr_scan_combine(ctypes.byref(p), int(segments), _ptr(M), _ptr(Z), _ptr(h0), _ptr(h_start),
                                    _ptr(h_final), _stream(stream)), "gdr_scan_combine")
+
+
+def gdr_scan_combine_reverse(p, segments, M, Zb, dh_final, ends, dh0, stream=None):
+    _check(load().gdr_scan_combine_reverse(ctypes.byref(p), int(segments), _ptr(M), _ptr(Zb), _ptr(dh_final),
+                                           _ptr(ends), _ptr(dh0), _stream(stream)), "gdr_scan_combine_reverse")
 
 
 def gdr_forward_segments(p) -> int:
@@ -339,10 +346,10 @@ def gdr_backward(p, q, k, v, g, beta, h0, d_o, dh_final, dq, dk, dv, dg, dbeta, 
 
 
 def backward(q, k, v, g, beta, h0, d_o, dh_final=None, *, chunk=64, scale=None, variant="auto", workspace=None,
-             stream=None):
+             stream=None, segments=0):
     """dq, dk, dv, dg, dbeta, dh0 = backward(q, k, v, g, beta, h0, do, dh_final): the gradient of
     forward's (o, h_final) against do and dh_final, on device tensors."""
-    p = problem_for(q, v, g, chunk, scale, variant)
+    p = problem_for(q, v, g, chunk, scale, variant, segments)
     B, T, _, K = q.shape
     H, V = v.shape[2], v.shape[-1]            # value heads
     dq, dk = torch.empty_like(q), torch.empty_like(k)

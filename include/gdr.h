@@ -173,7 +173,18 @@ GDR_API gdr_status gdr_scan_transfer(const gdr_problem* p, const void* k, const 
 GDR_API gdr_status gdr_scan_combine(const gdr_problem* p, int32_t segments, const float* M, const float* Z,
                                     const float* h0, float* h_start, float* h_final, void* stream);
 
-/* The number of segments gdr_forward scans this problem in: p->segments when that is > 1 (it must
+/* The backward's stitch.  The reverse state scan (gdr_bwd_scan_dh and its tensor-core forms) is affine
+ * the other way: a segment maps the state gradient at its end to the one at its start by M^T, M its
+ * forward map from gdr_scan_transfer, plus Zb, the gradient it leaves at its start from a zero gradient
+ * at its end (the reverse scan's dh0 on the segment problem with dh_final = NULL).  From the last
+ * segment: ends[b,S-1] = dh_final (zero if NULL), ends[b,s-1] = M_s^T ends[b,s] + Zb_s, and
+ * dh0 = M_0^T ends[b,0] + Zb_0.  ends [B,S,H,K,V] fp32 (each segment's dh_final for the reverse scan on
+ * the segment problem), dh0 [B,H,K,V] fp32 or NULL; fp32 on the CUDA cores.  gdr_backward does all
+ * of this itself when gdr_forward_segments(p) > 1. */
+GDR_API gdr_status gdr_scan_combine_reverse(const gdr_problem* p, int32_t segments, const float* M, const float* Zb,
+                                            const float* dh_final, float* ends, float* dh0, void* stream);
+
+/* The number of segments gdr_forward (and, on the tensor cores, gdr_backward) scans this problem in: p->segments when that is > 1 (it must
  * divide NT, with T % C == 0), 1 for p->segments == 1 and on the CUDA-core path, and for 0 a choice
  * from the problem: when B * HV * V / 32 (the serial scan's CTAs) is at most 76, the largest divisor
  * of NT whose segments keep at least 16 chunks and whose segmented grid fits 152 SMs.  0 for a

@@ -26,6 +26,14 @@ gives every segment's starting state, after which the segments can be scanned
 independently.  The pages scan serially and do not split the scan; this is
 the plain algebra of the recurrence they state, written out chunk by chunk.
 
+The backward's reverse scan is affine the other way round: per chunk
+dh_before = A_c^T dh_after + b_c (with b_c = scale (q e^G)^T do - w^T dv_loc), so
+a segment maps the gradient at its end to the one at its start by M^T, the
+transpose of its forward map, plus Z_b, the gradient the segment leaves at its
+start from a zero gradient at its end.  Stitching from the last segment,
+
+    end[S-1] = dh_final,   end[s-1] = M_s^T end[s] + Zb_s,   dh0 = M_0^T end[0] + Zb_0.
+
 Layouts: k [B,T,H,K] (q/k heads, expanded to the value heads as in
 oracle.chunked), w [B,T,HV,K], u [B,T,HV,V], G [B,T,HV] or [B,T,HV,K];
 M [B,S,HV,K,K], Z [B,S,HV,K,V], h_start [B,S,HV,K,V].  T must be a multiple
@@ -91,3 +99,16 @@ def stitch(M, Z, h0):
         starts[:, s] = h
         h = M[:, s] @ h + Z[:, s]
     return starts, h
+
+
+def stitch_reverse(M, Zb, dh_final):
+    """(ends [B,S,H,K,V], dh0 [B,H,K,V]): the state gradient at the end of every segment and at
+    the start of the sequence, from the forward maps M and the backward offsets Zb (dh_final None: zero)."""
+    M, Zb = np.asarray(M, dtype=np.float64), np.asarray(Zb, dtype=np.float64)
+    B, S, H, K, V = Zb.shape
+    e = np.zeros((B, H, K, V)) if dh_final is None else np.asarray(dh_final, dtype=np.float64).copy()
+    ends = np.zeros((B, S, H, K, V))
+    for s in range(S - 1, -1, -1):
+        ends[:, s] = e
+        e = np.swapaxes(M[:, s], -1, -2) @ e + Zb[:, s]
+    return ends, e

@@ -43,9 +43,9 @@ def upstream(x, seed):
     return do, dhf
 
 
-def gpu_backward(x, do, dhf, C, variant, scale=None, want_dh0=True):
+def gpu_backward(x, do, dhf, C, variant, scale=None, want_dh0=True, segments=0):
     q, k, v, g, beta, h0, d_o = (dev(t) for t in (x.q, x.k, x.v, x.g, x.beta, x.h0, do))
-    p = gdr.problem_for(q, v, g, C, scale, variant)
+    p = gdr.problem_for(q, v, g, C, scale, variant, segments)
     B, T, _, K = q.shape
     H, V = v.shape[2], v.shape[-1]            # value heads
     nan = float("nan")

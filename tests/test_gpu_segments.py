@@ -143,3 +143,71 @@ def test_low_head_count_workload_full_size():
     o, hf, ran = gpu_forward(x, wl.chunk)
     assert ran == "fused" and torch.isfinite(o).all() and torch.isfinite(hf).all()
     check_forward(x, o, hf, [(0, 0), (0, 3)], wl.chunk, 1.0 / np.sqrt(wl.K), wl.io)
+
+
+# ---------------------------------------------------------------- the backward's segments
+
+@pytest.mark.parametrize("K,V", [(64, 64), (128, 128), (128, 64)])
+@pytest.mark.parametrize("with_dhf", [False, True])
+def test_reverse_stitch(K, V, with_dhf):
+    B, H, S = 2, 2, 6
+    rng = np.random.default_rng(120)
+    M = np.eye(K) * 0.9 + rng.standard_normal((B, S, H, K, K)) * 0.05
+    Zb = rng.standard_normal((B, S, H, K, V))
+    dhf = rng.standard_normal((B, H, K, V)) if with_dhf else None
+    ends_ref, dh0_ref = segments.stitch_reverse(M, Zb, dhf)
+    prob = gdr.make_problem(B, 64 * S, H, K, V, 64, torch.bfloat16)
+    ends = torch.full((B, S, H, K, V), float("nan"), device="cuda")
+    dh0 = torch.full((B, H, K, V), float("nan"), device="cuda")
+    f32 = lambda a: None if a is None else torch.from_numpy(a).float().cuda()
+    gdr.gdr_scan_combine_reverse(prob, S, f32(M), f32(Zb), f32(dhf), ends, dh0)
+    torch.cuda.synchronize()
+    assert scaled_err(ends, ends_ref) <= STAGE_TOL["f32"]
+    assert scaled_err(dh0, dh0_ref) <= STAGE_TOL["f32"]
+
+
+# (B, T, H, K, V, C, S, per_k): the scalar gate at C = 64 (local term from P) and C = 32 (its own
+# kernel), the per-key gate (exactly flagged chunks included by the strong-decay case below)
+BACKWARD_CASES = [(1, 2048, 2, 128, 128, 64, 4, False), (2, 1024, 1, 64, 64, 64, 8, False),
+                  (1, 1024, 2, 64, 128, 32, 4, False), (1, 2048, 2, 128, 128, 64, 4, True),
+                  (2, 1024, 1, 128, 64, 32, 2, True)]
+
+
+@pytest.mark.parametrize("case", BACKWARD_CASES, ids=lambda c: "x".join(map(str, c[:7])) + ("-kda" if c[7] else "-gdn"))
+def test_segmented_backward(case):
+    from test_gpu_backward import BWD_TOL, GRADS, gpu_backward, reference, upstream
+    B, T, H, K, V, C, S, per_k = case
+    x = make_inputs(B, T, H, K, V, per_k_gate=per_k, io_dtype=torch.bfloat16, with_h0=True, seed=121)
+    do, dhf = upstream(x, 122)
+    assert gdr.gdr_forward_segments(gdr.problem_for(x.q, x.v, x.g, C, variant="tensor", segments=S)) == S
+    got, ran = gpu_backward(x, do, dhf, C, "tensor", segments=S)
+    assert ran == "tensor"
+    ref = reference(x, do, dhf, C, 1.0 / np.sqrt(K))
+    for name in GRADS:
+        err = scaled_err(got[name], ref[name])
+        assert np.isfinite(err) and err <= BWD_TOL["bf16"], f"{name}: {err:.3e}"
+
+
+def test_segmented_backward_grouped_heads_strong_decay_and_no_final_gradient():
+    from test_gpu_backward import BWD_TOL, GRADS, gpu_backward, reference, upstream
+    from chunked_gated_delta_prepare_gb300.inputs import GdrInputs
+    x = grouped_inputs(1, 2048, 1, 2, 128, 128, per_k_gate=True, seed=123)
+    g = x.g.clone()
+    g[:, :, 1] *= 100.0                 # the second value head's chunks go to the exact per-chunk stages
+    x = GdrInputs(q=x.q, k=x.k, v=x.v, g=g, beta=x.beta, h0=x.h0)
+    do, _ = upstream(x, 124)
+    got, _ = gpu_backward(x, do, None, 64, "tensor", segments=4)
+    ref = reference(x, do, None, 64, 1.0 / np.sqrt(128))
+    for name in GRADS:
+        err = scaled_err(got[name], ref[name])
+        assert np.isfinite(err) and err <= BWD_TOL["bf16"], f"{name}: {err:.3e}"
+
+
+def test_automatic_segments_backward():
+    from test_gpu_backward import BWD_TOL, GRADS, gpu_backward, reference, upstream
+    x = make_inputs(1, 2048, 1, 128, 128, io_dtype=torch.bfloat16, with_h0=True, seed=125)
+    do, dhf = upstream(x, 126)
+    got, _ = gpu_backward(x, do, dhf, 64, "auto")
+    ref = reference(x, do, dhf, 64, 1.0 / np.sqrt(128))
+    for name in GRADS:
+        assert scaled_err(got[name], ref[name]) <= BWD_TOL["bf16"], name

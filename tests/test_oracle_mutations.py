@@ -303,6 +303,8 @@ SEGMENT_MUTANTS = [
     ("kg without its gate", "kg = kc * np.exp(G_last - Gc)", "kg = kc"),
     ("segment start recorded after its update", "        starts[:, s] = h\n        h = M[:, s] @ h + Z[:, s]",
      "        h = M[:, s] @ h + Z[:, s]\n        starts[:, s] = h"),
+    ("reverse stitch without the transpose", "e = np.swapaxes(M[:, s], -1, -2) @ e + Zb[:, s]", "e = M[:, s] @ e + Zb[:, s]"),
+    ("reverse stitch in forward order", "for s in range(S - 1, -1, -1):", "for s in range(S):"),
 ]
 
 
@@ -312,6 +314,7 @@ def _segment_pins_fail(mod) -> bool:
     for per_k in (False, True):
         checks.append(lambda per_k=per_k: pins.test_no_delta_step_leaves_the_decay(per_k))
         checks.append(lambda per_k=per_k: pins.test_stitched_maps_reproduce_the_serial_scan(per_k, 16, 4))
+        checks.append(lambda per_k=per_k: pins.test_reverse_stitch_reproduces_the_serial_reverse_scan(per_k, 16, 4))
     saved = pins.segments
     pins.segments = mod
     try:

@@ -5,6 +5,8 @@
   recurrence chunk by chunk instead of composing matrices.
 - With beta = 0 there is no delta step: every map is the decay alone,
   M = diag(exp(sum of g over the segment)) and Z = 0, a closed form in the raw g.
+- The reverse stitch (transposed maps, last segment first) reproduces the
+  backward oracle's serial reverse scan at every segment end and its dh0.
 - One-token chunks with g = 0, beta = 2 and unit keys: a chunk is the textbook
   rank-one delta update S <- (I - 2 k k^T) S + 2 k v^T, so M = I - 2 k k^T, a
   reflection (M M = I, det M = -1), and Z = 2 k v^T.
@@ -14,7 +16,7 @@ import pytest
 import torch
 
 from chunked_gated_delta_prepare_gb300.inputs import make_inputs
-from oracle import chunked, segments
+from oracle import chunked, chunked_backward, segments
 
 
 def _problem(per_k, B=2, T=128, H=2, HV=None, K=8, V=6, seed=61):
@@ -88,3 +90,30 @@ def test_one_token_chunks_are_reflections():
         assert np.abs(M[0, t, 0] @ M[0, t, 0] - np.eye(K)).max() <= 1e-13
         assert abs(np.linalg.det(M[0, t, 0]) + 1.0) <= 1e-12
         assert np.abs(Z[0, t, 0] - 2 * np.outer(kk, v[0, t, 0])).max() <= 1e-14
+
+
+@pytest.mark.parametrize("per_k", [False, True])
+@pytest.mark.parametrize("C,S", [(16, 4), (8, 8)])
+def test_reverse_stitch_reproduces_the_serial_reverse_scan(per_k, C, S):
+    d = _problem(per_k, seed=65)
+    rng = np.random.default_rng(66)
+    B, T, H, K = d["k"].shape
+    V = d["v"].shape[-1]
+    do = rng.standard_normal((B, T, H, V))
+    dhf = rng.standard_normal((B, H, K, V))
+    scale = 0.3
+    p = chunked.prepare_wy(d["k"], d["v"], d["g"], d["beta"], C)
+    dl = chunked_backward.dv_local(d["q"], d["k"], p["G"], do, C, scale)
+    ref = chunked_backward.scan_dh(d["q"], d["k"], p["w"], p["G"], do, dl, dhf, C, scale)
+    M, _ = segments.segment_maps(d["k"], p["w"], p["u"], p["G"], C, S)
+    L = T // S
+    zb = np.stack([chunked_backward.scan_dh(d["q"][:, s * L:(s + 1) * L], d["k"][:, s * L:(s + 1) * L],
+                                            p["w"][:, s * L:(s + 1) * L], p["G"][:, s * L:(s + 1) * L],
+                                            do[:, s * L:(s + 1) * L], dl[:, s * L:(s + 1) * L], None, C,
+                                            scale)["dh0"] for s in range(S)], axis=1)
+    ends, dh0 = segments.stitch_reverse(M, zb, dhf)
+    n = (T // C) // S
+    tol = 1e-11 * np.abs(ref["dh0"]).max()
+    for s in range(S):
+        assert np.abs(ends[:, s] - ref["dh_ckpt"][:, (s + 1) * n - 1]).max() <= tol
+    assert np.abs(dh0 - ref["dh0"]).max() <= tol

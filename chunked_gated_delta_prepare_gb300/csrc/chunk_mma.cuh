@@ -72,6 +72,37 @@ __device__ __forceinline__ void each_at(int rb, int cb0, int g4, int q4, F&& f) 
             for (int e = 0; e < 4; ++e) f(j, n, e, 16 * rb + g4 + 8 * (e >> 1), 16 * (cb0 + j) + 8 * n + 2 * q4 + (e & 1));
 }
 
+// Calls f(row, col, x0&, x1&) for every pair of adjacent columns (col, col + 1) of a warp's tiles: the
+// two accumulator elements a thread holds side by side, so a bf16x2 load or store serves both.
+template <int NCW, typename F>
+__device__ __forceinline__ void each2(float (&acc)[NCW][2][4], int rb, int cb0, int g4, int q4, F&& f) {
+#pragma unroll
+    for (int j = 0; j < NCW; ++j)
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                f(16 * rb + g4 + 8 * h, 16 * (cb0 + j) + 8 * n + 2 * q4, acc[j][n][2 * h], acc[j][n][2 * h + 1]);
+}
+
+__device__ __forceinline__ float2 bf2(const bf16* p) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+}
+__device__ __forceinline__ void st_bf2(bf16* p, float x0, float x1) {
+    *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(x0, x1);
+}
+
+// rows x D bf16 from shared [rows][D + 8] to global rows of stride gs elements, rows < nrows only:
+// 16-byte loads and stores, consecutive threads on consecutive 16-byte pieces of a row.
+template <int D, int NTHR>
+__device__ __forceinline__ void store_tile(bf16* dst, int64_t gs, const bf16* src, int nrows, int tid) {
+    constexpr int per = D / 8;
+    for (int idx = tid; idx < nrows * per; idx += NTHR) {
+        const int r = idx / per, c8 = idx % per;
+        *reinterpret_cast<uint4*>(dst + r * gs + 8 * c8) = *reinterpret_cast<const uint4*>(src + r * (D + 8) + 8 * c8);
+    }
+}
+
 // rows x D bf16 from global rows of stride gs elements into shared [rows][D + 8]; rows >= nrows read as
 // zero.  Asynchronous 16-byte copies (cp.async), so every copy of a phase is in flight at once; the
 // caller waits with cp_async_wait_all() and a barrier.
@@ -86,6 +117,32 @@ __device__ __forceinline__ void load_tile(bf16* dst, const bf16* src, int64_t gs
                          : "memory");
         else
             *reinterpret_cast<uint4*>(d) = make_uint4(0, 0, 0, 0);
+    }
+}
+
+// One row of bytes (a multiple of 16, both addresses 16-byte aligned) by the bulk-copy engine, completing
+// on the mbarrier as transaction bytes.
+__device__ __forceinline__ void bulk_row(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_addr(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
+}
+
+// rows x D bf16 from global rows of stride gs elements into shared [rows][D + 8], one bulk copy per row
+// (thread (r + off) % NTHR takes row r), completing on bar with nrows * D * 2 bytes; rows >= nrows are
+// zeroed with plain stores (visible to other threads after the next CTA barrier).
+// off rotates the rows over the threads, so several tiles issued together spread over the CTA.
+template <int D, int NTHR>
+__device__ __forceinline__ void bulk_tile(bf16* dst, const bf16* src, int64_t gs, int rows, int nrows, int tid,
+                                          uint64_t* bar, int off = 0) {
+    for (int r = ((tid - off) % NTHR + NTHR) % NTHR; r < rows; r += NTHR) {
+        if (r < nrows) {
+            bulk_row(dst + r * (D + 8), src + r * gs, D * 2, bar);
+        } else {
+#pragma unroll
+            for (int c8 = 0; c8 < D / 8; ++c8) *reinterpret_cast<uint4*>(dst + r * (D + 8) + 8 * c8) = make_uint4(0, 0, 0, 0);
+        }
     }
 }
 

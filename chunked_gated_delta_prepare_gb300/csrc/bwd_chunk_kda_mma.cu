@@ -166,6 +166,8 @@ bwd_chunk_kda_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
     auto E = [&](int r, int d) { return bf(Es + r * LK + d); };
 
     float accQ[NK][2][4], accK[NK][2][4], accG[NK][2][4], tmp[NK][2][4];
+    float br[2] = {0.f, 0.f};   // dbeta's partial sums for rows 16 rb + g4 and + 8, reduced once at the end
+    auto f2 = [](const float* p) { return *reinterpret_cast<const float2*>(p); };
     cp_async_wait<2>();
     __syncthreads();
     zero(accQ);
@@ -179,20 +181,31 @@ bwd_chunk_kda_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
         float xq[NC][2][4];
         zero(xq);
         wgemm<NC, V, false, true>(xq, aDO, LV, aVP, LV, rb, cc, mi, mr);
-        each(xq, rb, cc, g4, q4, [&](int r, int col, float& x) {
-            const float y = scale * x;
-            if (col == r) sDiag[r] = y;
-            Xs[r * LC + col] = __float2bfloat16_rn(col < r ? y : 0.f);
+        each2(xq, rb, cc, g4, q4, [&](int r, int col, float& x0, float& x1) {
+            const float y0 = scale * x0, y1 = scale * x1;
+            if (col == r) sDiag[r] = y0;
+            if (col + 1 == r) sDiag[r] = y1;
+            st_bf2(Xs + r * LC + col, col < r ? y0 : 0.f, col + 1 < r ? y1 : 0.f);
         });
     }
     cp_async_wait<0>();
     __syncthreads();
-    // Qa = q E over q, Kb = k / E over k
-    for (int i = tid; i < C * K; i += kThreads) {
-        const int r = i / K, d = i % K;
-        const float e = E(r, d);
-        Qs[r * LK + d] = __float2bfloat16_rn(bf(Qs + r * LK + d) * e);
-        Ks[r * LK + d] = __float2bfloat16_rn(__fdividef(bf(Ks + r * LK + d), e));
+    // Qa = q E over q, Kb = k / E over k, eight elements at a time
+    for (int i = tid; i < C * (K / 8); i += kThreads) {
+        const int off = (i / (K / 8)) * LK + 8 * (i % (K / 8));
+        uint4 qv = *reinterpret_cast<const uint4*>(Qs + off), kv = *reinterpret_cast<const uint4*>(Ks + off);
+        const uint4 ev = *reinterpret_cast<const uint4*>(Es + off);
+        __nv_bfloat162* qp = reinterpret_cast<__nv_bfloat162*>(&qv);
+        __nv_bfloat162* kp = reinterpret_cast<__nv_bfloat162*>(&kv);
+        const __nv_bfloat162* ep = reinterpret_cast<const __nv_bfloat162*>(&ev);
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const float2 e = __bfloat1622float2(ep[m]), a = __bfloat1622float2(qp[m]), c2 = __bfloat1622float2(kp[m]);
+            qp[m] = __floats2bfloat162_rn(a.x * e.x, a.y * e.y);
+            kp[m] = __floats2bfloat162_rn(__fdividef(c2.x, e.x), __fdividef(c2.y, e.y));
+        }
+        *reinterpret_cast<uint4*>(Qs + off) = qv;
+        *reinterpret_cast<uint4*>(Ks + off) = kv;
     }
     // sum_v h dhn per key row
     {
@@ -215,11 +228,15 @@ bwd_chunk_kda_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
     // dw = -dv' h^T -> bf16 tile
     zero(tmp);
     wgemm<NK, V, false, true>(tmp, aDV, LV, aH, LV, rb, ck, mi, mr);
-    each(tmp, rb, ck, g4, q4, [&](int r, int col, float& x) { DWs[r * LK + col] = __float2bfloat16_rn(-x); });
+    each2(tmp, rb, ck, g4, q4, [&](int r, int col, float& x0, float& x1) { st_bf2(DWs + r * LK + col, -x0, -x1); });
     __syncthreads();   // Qa, Kb formed
     // accQ = scale dqg e^(G_ref): times E it is dq's e^G part, times Qa its gate term; phase 2 adds
     // Xq Kb, which goes the same two ways
-    each(accQ, rb, ck, g4, q4, [&](int r, int col, float& x) { x *= scale * sEref[col]; });
+    each2(accQ, rb, ck, g4, q4, [&](int r, int col, float& x0, float& x1) {
+        const float2 er = f2(sEref + col);
+        x0 *= scale * er.x;
+        x1 *= scale * er.y;
+    });
     // dk's e^(G_L - G) part from dkg (kg = k e^(G_L - G) = Kb e^(G_L - G_ref)); the last row takes the
     // other rows' kg gate terms, per key column (its own cancels)
 #pragma unroll
@@ -228,13 +245,18 @@ bwd_chunk_kda_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
         for (int n = 0; n < 2; ++n) {
             float cs0 = 0.f, cs1 = 0.f;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int r = 16 * rb + g4 + 8 * (e >> 1), col = 16 * (ck + j) + 8 * n + 2 * q4 + (e & 1);
-                const float x = accK[j][n][e];
-                const float t = r == nv - 1 ? 0.f : x * bf(Ks + r * LK + col) * sEgl[col];
-                accG[j][n][e] = -t;                                            // dG's first term
-                if (e & 1) cs1 += t; else cs0 += t;
-                accK[j][n][e] = __fdividef(x * sEgl[col], E(r, col));
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const int r = 16 * rb + g4 + 8 * h2, col = 16 * (ck + j) + 8 * n + 2 * q4, e = 2 * h2;
+                const float x0 = accK[j][n][e], x1 = accK[j][n][e + 1];
+                const float2 kb = bf2(Ks + r * LK + col), ev = bf2(Es + r * LK + col), egl = f2(sEgl + col);
+                const float t0 = r == nv - 1 ? 0.f : x0 * kb.x * egl.x;
+                const float t1 = r == nv - 1 ? 0.f : x1 * kb.y * egl.y;
+                accG[j][n][e] = -t0;                                           // dG's first terms
+                accG[j][n][e + 1] = -t1;
+                cs0 += t0;
+                cs1 += t1;
+                accK[j][n][e] = __fdividef(x0 * egl.x, ev.x);
+                accK[j][n][e + 1] = __fdividef(x1 * egl.y, ev.y);
             }
             // a column's 16 rows sit in the 8 lanes that share q4
 #pragma unroll
@@ -261,22 +283,28 @@ bwd_chunk_kda_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
     cp_async_commit();
 
     // ---- phase 2: the output scores' other factors
+    bf16* DQs = Hs;   // dq staged over the dead h (later dkb's space) for 16-byte row stores
     wgemm<NK, C, false, false>(accQ, aX, LC, aK, LK, rb, ck, mi, mr);     // + Xq Kb
-    each_at<NK>(rb, ck, g4, q4, [&](int j, int n, int e, int r, int col) {
-        const float x = accQ[j][n][e];
-        accG[j][n][e] += bf(Qs + r * LK + col) * x;                           // (dqg e^G + L) q
+    each2_at<NK>(rb, ck, g4, q4, [&](int j, int n, int e, int r, int col) {
+        const float x0 = accQ[j][n][e], x1 = accQ[j][n][e + 1];
+        const float2 qa = bf2(Qs + r * LK + col), kb = bf2(Ks + r * LK + col), ev = bf2(Es + r * LK + col);
+        accG[j][n][e] += qa.x * x0;                                           // (dqg e^G + L) q
+        accG[j][n][e + 1] += qa.y * x1;
         // dq done: E (scale dqg e^(G_ref) + Xq Kb) + d_i k_i (k = Kb E)
-        const float y = E(r, col) * (x + sDiag[r] * bf(Ks + r * LK + col));
-        if (r < nv) dq[(tok0 + (int64_t)r * H) * K + col] = __float2bfloat16_rn(y);
+        st_bf2(DQs + r * LK + col, ev.x * (x0 + sDiag[r] * kb.x), ev.y * (x1 + sDiag[r] * kb.y));
     });
     zero(tmp);
     wgemm<NK, C, true, false>(tmp, aX, LC, aQ, LK, rb, ck, mi, mr);       // Xq^T Qa
-    each_at<NK>(rb, ck, g4, q4, [&](int j, int n, int e, int r, int col) {
-        const float x = tmp[j][n][e], qa = bf(Qs + r * LK + col);
-        accG[j][n][e] -= bf(Ks + r * LK + col) * x;                           // k R = Kb (Xq^T Qa)
-        accK[j][n][e] += __fdividef(x + sDiag[r] * qa, E(r, col));            // R + d_i q_i (q = Qa / E)
+    each2_at<NK>(rb, ck, g4, q4, [&](int j, int n, int e, int r, int col) {
+        const float x0 = tmp[j][n][e], x1 = tmp[j][n][e + 1];
+        const float2 qa = bf2(Qs + r * LK + col), kb = bf2(Ks + r * LK + col), ev = bf2(Es + r * LK + col);
+        accG[j][n][e] -= kb.x * x0;                                           // k R = Kb (Xq^T Qa)
+        accG[j][n][e + 1] -= kb.y * x1;
+        accK[j][n][e] += __fdividef(x0 + sDiag[r] * qa.x, ev.x);              // R + d_i q_i (q = Qa / E)
+        accK[j][n][e + 1] += __fdividef(x1 + sDiag[r] * qa.y, ev.y);
     });
     __syncthreads();
+    store_tile<K, kThreads>(dq + tok0 * K, (int64_t)H * K, DQs, nv, tid);
     // k again, over Qa, for Ka = k E
     load_tile<K, kThreads>(Qs, k + ktok0 * K, (int64_t)Hk * K, C, nv, tid);
     cp_async_commit();
@@ -285,47 +313,51 @@ bwd_chunk_kda_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
     bf16* DKBs = Hs;
     bf16* DVBs = DHs;
     cp_async_wait<1>();
-    __syncthreads();
+    __syncthreads();   // the WY tiles landed; dq's staging has been read
     const uint32_t aT = smem_addr(Ts), aW = smem_addr(Ws), aU = smem_addr(Us);
     // dvb = T^T dv': dv = beta dvb (needs no Ka: it covers the k reload)
     {
         float tv[NV][2][4];
         zero(tv);
         wgemm<NV, C, true, false>(tv, aT, LC, aDV, LV, rb, cv, mi, mr);
-        float r0 = 0.f, r1 = 0.f;
-        each(tv, rb, cv, g4, q4, [&](int r, int col, float& x) {
-            const float t = x * bf(Vs + r * LV + col);
-            if (r & 8) r1 += t; else r0 += t;
-            DVBs[r * LV + col] = __float2bfloat16_rn(x);
-            if (r < nv) dv[(tok0 + (int64_t)r * H) * V + col] = __float2bfloat16_rn(sB[r] * x);
+        each2(tv, rb, cv, g4, q4, [&](int r, int col, float& x0, float& x1) {
+            const float2 vv = bf2(Vs + r * LV + col);
+            br[(r >> 3) & 1] += x0 * vv.x + x1 * vv.y;
+            st_bf2(DVBs + r * LV + col, x0, x1);
+            if (r < nv) st_bf2(dv + (tok0 + (int64_t)r * H) * V + col, sB[r] * x0, sB[r] * x1);
         });
-        row_add(sdB + 16 * rb + g4, r0, q4);
-        row_add(sdB + 16 * rb + g4 + 8, r1, q4);
     }
     zero(tmp);
     wgemm<NK, C, true, false>(tmp, aT, LC, aDW, LK, rb, ck, mi, mr);      // dkb = T^T dw
     cp_async_wait<0>();
     __syncthreads();
-    // Ka = k E in place
-    for (int i = tid; i < C * K; i += kThreads) {
-        const int r = i / K, d = i % K;
-        Qs[r * LK + d] = __float2bfloat16_rn(bf(Qs + r * LK + d) * E(r, d));
+    // Ka = k E in place, eight elements at a time
+    for (int i = tid; i < C * (K / 8); i += kThreads) {
+        const int off = (i / (K / 8)) * LK + 8 * (i % (K / 8));
+        uint4 kv = *reinterpret_cast<const uint4*>(Qs + off);
+        const uint4 ev = *reinterpret_cast<const uint4*>(Es + off);
+        __nv_bfloat162* kp = reinterpret_cast<__nv_bfloat162*>(&kv);
+        const __nv_bfloat162* ep = reinterpret_cast<const __nv_bfloat162*>(&ev);
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const float2 e = __bfloat1622float2(ep[m]), a = __bfloat1622float2(kp[m]);
+            kp[m] = __floats2bfloat162_rn(a.x * e.x, a.y * e.y);
+        }
+        *reinterpret_cast<uint4*>(Qs + off) = kv;
     }
     __syncthreads();
     // dkb's epilogue: dk += beta e^G dkb, dbeta += dkb . k e^G, dG += dkb kb (k e^G = Ka e^(G_ref))
-    {
-        float rb0 = 0.f, rb1 = 0.f;
-        each_at<NK>(rb, ck, g4, q4, [&](int j, int n, int e, int r, int col) {
-            const float x = tmp[j][n][e];
-            const float keg = bf(Qs + r * LK + col) * sEref[col];
-            if (r & 8) rb1 += x * keg; else rb0 += x * keg;
-            accG[j][n][e] += x * sB[r] * keg;
-            accK[j][n][e] += sB[r] * E(r, col) * sEref[col] * x;
-            DKBs[r * LK + col] = __float2bfloat16_rn(x);
-        });
-        row_add(sdB + 16 * rb + g4, rb0, q4);
-        row_add(sdB + 16 * rb + g4 + 8, rb1, q4);
-    }
+    each2_at<NK>(rb, ck, g4, q4, [&](int j, int n, int e, int r, int col) {
+        const float x0 = tmp[j][n][e], x1 = tmp[j][n][e + 1];
+        const float2 ka = bf2(Qs + r * LK + col), ev = bf2(Es + r * LK + col), er = f2(sEref + col);
+        const float keg0 = ka.x * er.x, keg1 = ka.y * er.y;
+        br[(r >> 3) & 1] += x0 * keg0 + x1 * keg1;
+        accG[j][n][e] += x0 * sB[r] * keg0;
+        accG[j][n][e + 1] += x1 * sB[r] * keg1;
+        accK[j][n][e] += sB[r] * ev.x * er.x * x0;
+        accK[j][n][e + 1] += sB[r] * ev.y * er.y * x1;
+        st_bf2(DKBs + r * LK + col, x0, x1);
+    });
     __syncthreads();
     const uint32_t aKa = aQ;
     // dA = strict_lower(-(dkb w^T + dvb u^T)); dbeta's A term against M = Ka Kb^T; Y = beta dA
@@ -336,37 +368,45 @@ bwd_chunk_kda_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
         wgemm<NC, K, false, true>(da, smem_addr(DKBs), LK, aW, LK, rb, cc, mi, mr);
         wgemm<NC, V, false, true>(da, smem_addr(DVBs), LV, aU, LV, rb, cc, mi, mr);
         wgemm<NC, K, false, true>(m, aKa, LK, aK, LK, rb, cc, mi, mr);
-        float r0 = 0.f, r1 = 0.f;
-        each_at<NC>(rb, cc, g4, q4, [&](int j, int n, int e, int r, int col) {
-            const float a = col < r ? -da[j][n][e] : 0.f;
-            const float t = a * m[j][n][e];
-            if (r & 8) r1 += t; else r0 += t;
-            Ys[r * LC + col] = __float2bfloat16_rn(sB[r] * a);
+        each2_at<NC>(rb, cc, g4, q4, [&](int j, int n, int e, int r, int col) {
+            const float a0 = col < r ? -da[j][n][e] : 0.f, a1 = col + 1 < r ? -da[j][n][e + 1] : 0.f;
+            br[(r >> 3) & 1] += a0 * m[j][n][e] + a1 * m[j][n][e + 1];
+            st_bf2(Ys + r * LC + col, sB[r] * a0, sB[r] * a1);
         });
-        row_add(sdB + 16 * rb + g4, r0, q4);
-        row_add(sdB + 16 * rb + g4 + 8, r1, q4);
     }
     __syncthreads();
     zero(tmp);
     wgemm<NK, C, false, false>(tmp, aY, LC, aK, LK, rb, ck, mi, mr);      // Y Kb
-    each_at<NK>(rb, ck, g4, q4, [&](int j, int n, int e, int r, int col) {
-        const float x = tmp[j][n][e];
-        accK[j][n][e] += E(r, col) * x;                                       // L(Y, k)
-        accG[j][n][e] += bf(Qs + r * LK + col) * x;                           // k L(Y, k) = Ka (Y Kb)
+    each2_at<NK>(rb, ck, g4, q4, [&](int j, int n, int e, int r, int col) {
+        const float x0 = tmp[j][n][e], x1 = tmp[j][n][e + 1];
+        const float2 ka = bf2(Qs + r * LK + col), ev = bf2(Es + r * LK + col);
+        accK[j][n][e] += ev.x * x0;                                           // L(Y, k)
+        accK[j][n][e + 1] += ev.y * x1;
+        accG[j][n][e] += ka.x * x0;                                           // k L(Y, k) = Ka (Y Kb)
+        accG[j][n][e + 1] += ka.y * x1;
     });
     zero(tmp);
     wgemm<NK, C, true, false>(tmp, aY, LC, aKa, LK, rb, ck, mi, mr);      // Y^T Ka
-    each_at<NK>(rb, ck, g4, q4, [&](int j, int n, int e, int r, int col) {
-        const float x = tmp[j][n][e];
-        accG[j][n][e] -= bf(Ks + r * LK + col) * x;                           // k R(Y, k) = Kb (Y^T Ka)
-        const float y = accK[j][n][e] + __fdividef(x, E(r, col));             // + R(Y, k): dk done
-        if (r < nv) dk[(tok0 + (int64_t)r * H) * K + col] = __float2bfloat16_rn(y);
+    bf16* DKS = Hs;   // dk staged over the dead dkb for 16-byte row stores
+    each2_at<NK>(rb, ck, g4, q4, [&](int j, int n, int e, int r, int col) {
+        const float x0 = tmp[j][n][e], x1 = tmp[j][n][e + 1];
+        const float2 kb = bf2(Ks + r * LK + col), ev = bf2(Es + r * LK + col);
+        accG[j][n][e] -= kb.x * x0;                                           // k R(Y, k) = Kb (Y^T Ka)
+        accG[j][n][e + 1] -= kb.y * x1;
+        st_bf2(DKS + r * LK + col, accK[j][n][e] + __fdividef(x0, ev.x),        // + R(Y, k): dk done
+               accK[j][n][e + 1] + __fdividef(x1, ev.y));
     });
+    row_add(sdB + 16 * rb + g4, br[0], q4);
+    row_add(sdB + 16 * rb + g4 + 8, br[1], q4);
     __syncthreads();
+    store_tile<K, kThreads>(dk + tok0 * K, (int64_t)H * K, DKS, nv, tid);
+    __syncthreads();   // dk's staging read before dG goes over it
 
     // ---- phase 4: dG through shared memory, the last row's terms, the reverse cumsum per key column
     float* dGs = reinterpret_cast<float*>(sm + L::rh);                    // [C][K] fp32 over dead h and dhn
-    each(accG, rb, ck, g4, q4, [&](int r, int col, float& x) { dGs[r * K + col] = x; });
+    each2(accG, rb, ck, g4, q4, [&](int r, int col, float& x0, float& x1) {
+        *reinterpret_cast<float2*>(dGs + r * K + col) = make_float2(x0, x1);
+    });
     __syncthreads();
     for (int d = tid; d < K; d += kThreads) {
         dGs[(nv - 1) * K + d] += sTcol[d] + sEgl[d] * sEref[d] * sHdh[d];  // e^(G_L) = e^(G_L - G_ref) e^(G_ref)

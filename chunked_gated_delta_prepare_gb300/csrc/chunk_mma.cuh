@@ -85,6 +85,18 @@ __device__ __forceinline__ void each2(float (&acc)[NCW][2][4], int rb, int cb0, 
                 f(16 * rb + g4 + 8 * h, 16 * (cb0 + j) + 8 * n + 2 * q4, acc[j][n][2 * h], acc[j][n][2 * h + 1]);
 }
 
+// Calls f(j, n, e, row, col) for every pair (e, e + 1) of a warp's accumulator elements: (row, col) and
+// (row, col + 1), for epilogues over several accumulators with the same tiling.
+template <int NCW, typename F>
+__device__ __forceinline__ void each2_at(int rb, int cb0, int g4, int q4, F&& f) {
+#pragma unroll
+    for (int j = 0; j < NCW; ++j)
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) f(j, n, 2 * h, 16 * rb + g4 + 8 * h, 16 * (cb0 + j) + 8 * n + 2 * q4);
+}
+
 __device__ __forceinline__ float2 bf2(const bf16* p) {
     return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
 }

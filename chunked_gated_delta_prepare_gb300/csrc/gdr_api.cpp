@@ -583,8 +583,11 @@ gdr_status gdr_bwd_wy_dqkg(const gdr_problem* p, const void* q, const void* k, c
         st = from_cuda(gdr::mma_bwd_chunk_kda(d, q, k, v, beta, g_cum, w, u, tinv, v_new, h_ckpt, d_o, dv_new,
                                               dh_ckpt, dq, dk, dv, dbeta, dg, exact_flags, (cudaStream_t)stream));
     } else {
-        st = from_cuda(gdr::mma_bwd_chunk(d, q, k, v, beta, g_cum, w, u, tinv, v_new, h_ckpt, d_o, dv_new, dh_ckpt, dq,
-                                          dk, dv, dbeta, dg, (cudaStream_t)stream));
+        st = from_cuda(d.C == 64 ? gdr::mma_bwd_chunk_tma(d, q, k, v, beta, g_cum, w, u, tinv, v_new, h_ckpt, d_o,
+                                                          dv_new, dh_ckpt, dq, dk, dv, dbeta, dg, (cudaStream_t)stream,
+                                                          device_error_word())
+                                 : gdr::mma_bwd_chunk(d, q, k, v, beta, g_cum, w, u, tinv, v_new, h_ckpt, d_o, dv_new,
+                                                      dh_ckpt, dq, dk, dv, dbeta, dg, (cudaStream_t)stream));
     }
     if (st == GDR_OK) t_last_variant = "tensor";
     return st;
@@ -695,9 +698,11 @@ gdr_status gdr_backward(const gdr_problem* p, const void* q, const void* k, cons
             });
             if (st != GDR_OK) return st;
         }
-        if ((st = from_cuda(gdr::mma_bwd_chunk(d, q, k, v, beta, g_cum, w, u, tinv, v_new, h_ckpt, d_o, dv_new, dh_ckpt,
-                                               dq, dk, dv, dbeta, dg, s))) != GDR_OK)
-            return st;
+        st = from_cuda(d.C == 64 ? gdr::mma_bwd_chunk_tma(d, q, k, v, beta, g_cum, w, u, tinv, v_new, h_ckpt, d_o,
+                                                          dv_new, dh_ckpt, dq, dk, dv, dbeta, dg, s, err)
+                                 : gdr::mma_bwd_chunk(d, q, k, v, beta, g_cum, w, u, tinv, v_new, h_ckpt, d_o, dv_new,
+                                                      dh_ckpt, dq, dk, dv, dbeta, dg, s));
+        if (st != GDR_OK) return st;
         if (d.G > 1 && (st = from_cuda(gdr::group_sum_heads(d, dq, dk, dq_out, dk_out, s))) != GDR_OK) return st;
         t_last_variant = "tensor";
         return GDR_OK;

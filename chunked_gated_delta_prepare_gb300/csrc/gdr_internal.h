@@ -95,6 +95,12 @@ cudaError_t mma_bwd_chunk(const Dims& d, const void* q, const void* k, const voi
                           const float* g_cum, const void* w, const void* u, const void* tinv, const void* v_new,
                           const void* h_ckpt, const void* d_o, const void* dv_new, const void* dh_ckpt, void* dq,
                           void* dk, void* dv, void* dbeta, float* dg, cudaStream_t s);
+// The same stage at C = 64 fed by TMA from swizzled tiles, persistent with the next chunk's tiles prefetched
+// (bwd_chunk_tma.cu); err: the device error word for its bounded barrier waits.
+cudaError_t mma_bwd_chunk_tma(const Dims& d, const void* q, const void* k, const void* v, const void* beta,
+                              const float* g_cum, const void* w, const void* u, const void* tinv, const void* v_new,
+                              const void* h_ckpt, const void* d_o, const void* dv_new, const void* dh_ckpt, void* dq,
+                              void* dk, void* dv, void* dbeta, float* dg, cudaStream_t s, unsigned int* err);
 // The same stage for a per-key-dim gate (bf16 io, C = 32 or 64).  exact_flags [B][NT][H]: set to 1 for a
 // chunk whose gate moves more than the kernel's exponent bound from the chunk's middle row (nothing of that
 // chunk is written; simt_bwd_dqkwg and simt_bwd_wy with only = exact_flags complete it), else 0.

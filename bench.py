@@ -492,16 +492,19 @@ def run_ours(args, wl):
     hx = {n_: t.pin_memory() for n_, t in x.tensors().items() if t is not None}
     h2d = sum(t.numel() * t.element_size() for t in hx.values())
     d2h = o.numel() * o.element_size() + hf.numel() * hf.element_size()
+    o_host = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)     # the caller's result buffers, pinned once
+    hf_host = torch.empty(hf.shape, dtype=hf.dtype, pin_memory=True)
     for _ in range(2):
         gdr.forward(hx["q"], hx["k"], hx["v"], hx["g"], hx["beta"], hx.get("h0"), chunk=C, variant=args.variant,
-                    workspace=ws, segments=args.segments)
+                    workspace=ws, segments=args.segments, out=o_host, h_final_out=hf_host)
     torch.cuda.synchronize()
     e2e_steps = max(3, min(args.steps, 10))
     barrier(world)
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
         oo, hh = gdr.forward(hx["q"], hx["k"], hx["v"], hx["g"], hx["beta"], hx.get("h0"), chunk=C,
-                             variant=args.variant, workspace=ws, segments=args.segments)
+                             variant=args.variant, workspace=ws, segments=args.segments, out=o_host,
+                             h_final_out=hf_host)
     torch.cuda.synchronize()
     e2e_s = max_over_ranks(time.perf_counter() - t0, world)
     e2e_value = weak_scaling_throughput(world, B * T, e2e_steps, e2e_s)

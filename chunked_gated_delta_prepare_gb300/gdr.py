@@ -245,14 +245,97 @@ def gdr_version() -> int:
 
 # ---------------------------------------------------------------- convenience
 
+def _host_pieces(T: int, chunk: int, pieces: int):
+    """Token ranges of whole chunks (the last one may end in a partial chunk) for a pipelined forward."""
+    nt = -(-T // chunk)
+    n = max(1, min(pieces, nt))
+    per = -(-nt // n) * chunk
+    return [(t0, min(T, t0 + per)) for t0 in range(0, T, per)]
+
+
+def _forward_host_pipelined(q, k, v, g, beta, h0, chunk, scale, variant, want_h_final, stream, segments, out,
+                            h_final_out, pieces, workspace):
+    """forward() for host tensors, in token pieces of whole chunks: piece i's inputs go to the device on one
+    stream while piece i - 1 computes on the current stream (from the state piece i - 2 left) and piece
+    i - 2's output returns on a third.  The chunking and the fp32 state carried between pieces are those of
+    one call over the whole sequence, so the results are the same."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    B, T, Hq, K = q.shape
+    H, V = v.shape[2], v.shape[-1]
+    cs = torch.cuda.current_stream() if stream is None else stream
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    o = out if out is not None else torch.empty(B, T, H, V, dtype=q.dtype, pin_memory=True)
+    ranges = _host_pieces(T, chunk, pieces)
+    Tp = ranges[0][1] - ranges[0][0]
+    srcs = (q, k, v, g, beta)
+
+    def piece_buffers():
+        return [torch.empty((B, Tp) + tuple(t.shape[2:]), dtype=t.dtype, device=dev) for t in srcs] + \
+               [torch.empty(B, Tp, H, V, dtype=q.dtype, device=dev)]
+    bufs = [piece_buffers(), piece_buffers()]
+    states = [torch.empty(B, H, K, V, dtype=torch.float32, device=dev) for _ in range(2)]
+    h_prev = h0.to(dev, non_blocking=True) if h0 is not None else None
+    in_free = [torch.cuda.Event(), torch.cuda.Event()]     # piece buffers free for the next upload
+    out_free = [torch.cuda.Event(), torch.cuda.Event()]    # output buffers read by the download
+    ws = workspace
+    for i, (t0, t1) in enumerate(ranges):
+        bi, n = i % 2, t1 - t0
+        buf = bufs[bi]
+        with torch.cuda.stream(up):
+            if i >= 2:
+                up.wait_event(in_free[bi])
+            for d, src in zip(buf[:5], srcs):
+                for b in range(B):
+                    d[b, :n].copy_(src[b, t0:t1], non_blocking=True)
+            ready = torch.cuda.Event()
+            ready.record(up)
+        cs.wait_event(ready)
+        if i >= 2:
+            cs.wait_event(out_free[bi])
+        with torch.cuda.stream(cs):
+            views = [t[:, :n] if n == Tp else t[:, :n].contiguous() for t in buf]
+            p = problem_for(views[0], views[2], views[3], chunk, scale, variant, segments)
+            nbytes = gdr_forward_workspace_bytes(p)
+            if nbytes and (ws is None or ws.numel() * ws.element_size() < nbytes):
+                ws = torch.empty(nbytes, device=dev, dtype=torch.uint8)
+            hs = states[bi]
+            gdr_forward(p, *views[:5], h_prev, views[5], hs, ws, 0 if ws is None else ws.numel() * ws.element_size(),
+                        cs)
+            h_prev = hs
+            in_free[bi].record(cs)
+            done = torch.cuda.Event()
+            done.record(cs)
+        views[5].record_stream(down)   # a fresh tensor for a short last piece of B > 1 sequences
+        with torch.cuda.stream(down):
+            down.wait_event(done)
+            for b in range(B):
+                o[b, t0:t1].copy_(views[5][b], non_blocking=True)
+            out_free[bi].record(down)
+    hf = None
+    if want_h_final:
+        hf = h_final_out if h_final_out is not None else torch.empty(B, H, K, V, dtype=torch.float32)
+        with torch.cuda.stream(cs):
+            hf.copy_(h_prev, non_blocking=True)
+    cs.wait_stream(down)
+    cs.synchronize()
+    return o, hf
+
+
 def forward(q, k, v, g, beta, h0=None, *, chunk=64, scale=None, variant="auto", want_h_final=True,
-            workspace=None, stream=None, segments=0):
+            workspace=None, stream=None, segments=0, out=None, h_final_out=None, pieces=8):
     """o, h_final = forward(q, k, v, g, beta, h0).
 
-    Device tensors are used in place.  CPU tensors are copied to the current
-    CUDA device (non-blocking from pinned memory) and the results copied back.
+    Device tensors are used in place.  CPU tensors (pinned for asynchronous
+    copies) go to the current CUDA device and the results come back: into `out`
+    / `h_final_out` when given (host tensors of o's and h_final's shape and
+    dtype), else into new pinned host tensors.  Host inputs run in `pieces`
+    token ranges of whole chunks, so the copies overlap the kernels (pieces=1:
+    one copy in, one call, one copy out).  The results are complete on return.
     """
     on_host = q.device.type == "cpu"
+    if on_host and pieces > 1 and -(-q.shape[1] // chunk) >= 2:
+        return _forward_host_pipelined(q, k, v, g, beta, h0, chunk, scale, variant, want_h_final, stream, segments,
+                                       out, h_final_out, pieces, workspace)
     if on_host:
         dev = torch.device("cuda", torch.cuda.current_device())
         q, k, v, g, beta = (t.to(dev, non_blocking=True) for t in (q, k, v, g, beta))
@@ -270,8 +353,18 @@ def forward(q, k, v, g, beta, h0=None, *, chunk=64, scale=None, variant="auto", 
     have = 0 if workspace is None else workspace.numel() * workspace.element_size()
     gdr_forward(p, q, k, v, g, beta, h0, o, hf, workspace, have, stream)
     if on_host:
-        o = o.to("cpu", non_blocking=False)
-        hf = hf.to("cpu") if hf is not None else None
+        if out is not None:
+            out.copy_(o, non_blocking=True)
+            o = out
+        else:
+            o = o.to("cpu")
+        if hf is not None:
+            if h_final_out is not None:
+                h_final_out.copy_(hf, non_blocking=True)
+                hf = h_final_out
+            else:
+                hf = hf.to("cpu")
+        torch.cuda.current_stream().synchronize()   # the results are on the host when this returns
     return o, hf
 
 

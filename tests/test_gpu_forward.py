@@ -172,6 +172,35 @@ def test_convenience_forward_host_tensors():
     assert rel_frob(hf, ref["h_final"]) <= H_TOL["bf16"]
 
 
+def test_convenience_forward_into_pinned_outputs():
+    # host inputs, results written into the caller's pinned buffers and complete on return
+    x = make_inputs(1, 128, 2, 64, 64, io_dtype=torch.bfloat16, with_h0=True, seed=15)
+    hx = [t.pin_memory() for t in (x.q, x.k, x.v, x.g, x.beta, x.h0)]
+    o_out = torch.full((1, 128, 2, 64), float("nan"), dtype=torch.bfloat16).pin_memory()
+    hf_out = torch.full((1, 2, 64, 64), float("nan")).pin_memory()
+    o, hf = gdr.forward(*hx, chunk=64, out=o_out, h_final_out=hf_out)
+    assert o.data_ptr() == o_out.data_ptr() and hf.data_ptr() == hf_out.data_ptr()
+    ref = oracle.naive_forward(x.q, x.k, x.v, x.g, x.beta, x.h0, 64, 1 / 8.0, with_ckpt=False)
+    assert max_abs(o_out, ref["o"]) <= O_TOL["bf16"]
+    assert rel_frob(hf_out, ref["h_final"]) <= H_TOL["bf16"]
+
+
+@pytest.mark.parametrize("shape,per_k,variant", [((1, 1000, 2, 128, 128), False, "auto"),
+                                               ((2, 700, 3, 64, 64), False, "auto"),
+                                               ((2, 640, 2, 128, 64), True, "auto"),
+                                               ((1, 512, 2, 64, 64), False, "simt")])
+def test_pipelined_host_forward_equals_one_device_call(shape, per_k, variant):
+    # host inputs run in token pieces of whole chunks with the state carried between them: the same
+    # chunking and the same fp32 state as one call on device tensors, so the same bits
+    B, T, H, K, V = shape
+    dt = torch.float32 if variant == "simt" else torch.bfloat16
+    x = make_inputs(B, T, H, K, V, per_k_gate=per_k, io_dtype=dt, with_h0=True, seed=17)
+    hx = [t.pin_memory() for t in (x.q, x.k, x.v, x.g, x.beta, x.h0)]
+    o_p, hf_p = gdr.forward(*hx, chunk=64, variant=variant, pieces=4)
+    o_1, hf_1 = gdr.forward(*(t.cuda() for t in hx), chunk=64, variant=variant)
+    assert torch.equal(o_p, o_1.cpu()) and torch.equal(hf_p, hf_1.cpu())
+
+
 def test_fused_variant_refuses_per_key_gate():
     x = make_inputs(1, 64, 1, 64, 64, per_k_gate=True, io_dtype=torch.bfloat16, seed=12)
     with pytest.raises(gdr.GdrError) as e:

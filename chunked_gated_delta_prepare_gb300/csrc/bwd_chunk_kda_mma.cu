@@ -133,11 +133,29 @@ bwd_chunk_kda_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
     __syncthreads();
     {
         bool big = false;
-        for (int i = tid; i < C * K; i += kThreads) {
-            const int r = i / K, d = i % K;
-            const float dg = Grow(r)[d] - sGref[d];
-            big |= fabsf(dg) > kExpSafe;
-            Es[r * LK + d] = __float2bfloat16_rn(__expf(dg));
+        // eight elements per step, the 16-byte loads of all steps issued before any is used
+        constexpr int N8 = C * K / 8 / kThreads;
+        float4 g8[N8][2];
+#pragma unroll
+        for (int j = 0; j < N8; ++j) {
+            const int e = 8 * (tid + kThreads * j), r = e / K, d = e % K;
+            const float4* src = reinterpret_cast<const float4*>(Grow(r) + d);
+            g8[j][0] = src[0];
+            g8[j][1] = src[1];
+        }
+#pragma unroll
+        for (int j = 0; j < N8; ++j) {
+            const int e = 8 * (tid + kThreads * j), r = e / K, d = e % K;
+            const float gv[8] = {g8[j][0].x, g8[j][0].y, g8[j][0].z, g8[j][0].w,
+                                 g8[j][1].x, g8[j][1].y, g8[j][1].z, g8[j][1].w};
+            __nv_bfloat162 ev[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const float d0 = gv[2 * m] - sGref[d + 2 * m], d1 = gv[2 * m + 1] - sGref[d + 2 * m + 1];
+                big |= fabsf(d0) > kExpSafe || fabsf(d1) > kExpSafe;
+                ev[m] = __floats2bfloat162_rn(__expf(d0), __expf(d1));
+            }
+            *reinterpret_cast<uint4*>(Es + r * LK + d) = *reinterpret_cast<const uint4*>(ev);
         }
         if (__syncthreads_or(big)) {
             if (tid == 0) exact_flags[st_off] = 1;

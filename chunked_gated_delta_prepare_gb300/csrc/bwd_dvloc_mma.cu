@@ -72,8 +72,20 @@ bwd_dvloc_mma_kernel(const bf16* __restrict__ q, const bf16* __restrict__ k, con
     load_tile<V, kThreads>(DOs, d_o + tok0 * V, (int64_t)H * V, C, nv, tid);
     cp_async_commit();
     // G past T repeats its last value (q, k and do are zero there)
-    for (int i = tid; i < C * GW; i += kThreads)
-        Gs[i] = g_cum[(tok0 + (int64_t)min(i / GW, nv - 1) * H) * GW + i % GW];
+    if constexpr (PER_K) {
+        // 16-byte loads, all of a thread's issued before any is used
+        constexpr int NV4 = C * GW / 4 / kThreads;
+        float4 gv[NV4];
+#pragma unroll
+        for (int j = 0; j < NV4; ++j) {
+            const int e = 4 * (tid + kThreads * j);
+            gv[j] = *reinterpret_cast<const float4*>(g_cum + (tok0 + (int64_t)min(e / GW, nv - 1) * H) * GW + e % GW);
+        }
+#pragma unroll
+        for (int j = 0; j < NV4; ++j) *reinterpret_cast<float4*>(Gs + 4 * (tid + kThreads * j)) = gv[j];
+    } else {
+        for (int i = tid; i < C; i += kThreads) Gs[i] = g_cum[tok0 + (int64_t)min(i, nv - 1) * H];
+    }
     if (tid == 0) *sFlag = 0;
     cp_async_wait<0>();
     __syncthreads();

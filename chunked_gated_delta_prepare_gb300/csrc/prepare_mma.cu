@@ -182,11 +182,17 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
     }
     // beta; g (rows past T read as zero)
     for (int i = tid; i < kTile; i += 128) sB[i] = i < nvalid ? __bfloat162float(beta[row(i)]) : 0.f;
-    if (PER_K) {
-        for (int i = tid; i < kTile * GW; i += 128) {
-            const int t = i / GW;
-            sG[i] = t < nvalid ? g[row(t) * GW + i % GW] : 0.f;
+    if constexpr (PER_K) {
+        // 16-byte loads, all of a thread's issued before any is used (the tile is 32 KB at K = 128)
+        constexpr int NV4 = kTile * GW / 4 / 128;
+        float4 gv[NV4];
+#pragma unroll
+        for (int j = 0; j < NV4; ++j) {
+            const int e = 4 * (tid + 128 * j), t = e / GW;
+            gv[j] = t < nvalid ? *reinterpret_cast<const float4*>(g + row(t) * GW + e % GW) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
+#pragma unroll
+        for (int j = 0; j < NV4; ++j) *reinterpret_cast<float4*>(sG + 4 * (tid + 128 * j)) = gv[j];
     } else if (warp == 0) {
         // scalar gate: warp shuffle scan, lane l holds rows l and 32 + l
         float x0 = lane < nvalid ? g[row(lane)] : 0.f;

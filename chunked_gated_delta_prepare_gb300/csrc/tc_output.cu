@@ -71,11 +71,22 @@ tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
     auto krow = [&](int t) -> int64_t { return ((int64_t)b * T + t0 + t) * (H / G) + h / G; };   // q/k head h / G
     // per-key-dim gate: 8 consecutive G values of tile row t from global memory; past T the last
     // row's (q and k are zero there, and a bounded gap keeps the exp range check quiet)
-    auto g8 = [&](int t, int d0, float* out) {
-        const float4* src = reinterpret_cast<const float4*>(g_cum + row(min(t, nvalid - 1)) * K + d0);
-        const float4 a = src[0], c = src[1];
-        out[0] = a.x; out[1] = a.y; out[2] = a.z; out[3] = a.w;
-        out[4] = c.x; out[5] = c.y; out[6] = c.z; out[7] = c.w;
+    // per-key-dim gate: a thread's rows of G, eight key columns each, for every step of the loops over the
+    // tile's 16-byte groups (its column group lc = tid % (K / 8) is the same at every step), by 16-byte loads
+    // issued together before any is used
+    constexpr int NIT = kTile * (K / 8) / 128;
+    auto load_g_rows = [&](float4 (&ga)[NIT][2]) {
+#pragma unroll
+        for (int j = 0; j < NIT; ++j) {
+            const int i = tid + 128 * j, r = i / (K / 8), lc = i % (K / 8);
+            const float4* src = reinterpret_cast<const float4*>(g_cum + row(min(r, nvalid - 1)) * K + lc * 8);
+            ga[j][0] = src[0];
+            ga[j][1] = src[1];
+        }
+    };
+    auto unpack8 = [](const float4 (&a)[2], float* out) {
+        out[0] = a[0].x; out[1] = a[0].y; out[2] = a[0].z; out[3] = a[0].w;
+        out[4] = a[1].x; out[5] = a[1].y; out[6] = a[1].z; out[7] = a[1].w;
     };
     const uint32_t s_base = bw::smem_u32(sm);
 
@@ -120,18 +131,27 @@ tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
     __syncthreads();
     bool ok = bw::mbar_wait(&bar_tma, 0, err, kDeviceErrTimeout);
 
-    if (PER_K) {
-        for (int i = tid; i < kTile * (K / 8); i += 128) {
-            const int r = i / (K / 8), lc = i % (K / 8);
-            const int ref = (r / C) * C + C / 2;
+    if constexpr (PER_K) {
+        float4 ga[NIT][2], gref[L::NCH][2];   // this thread's rows of G; the middle row of each chunk
+        load_g_rows(ga);
+#pragma unroll
+        for (int ch = 0; ch < L::NCH; ++ch) {
+            const float4* src = reinterpret_cast<const float4*>(
+                g_cum + row(min(ch * C + C / 2, nvalid - 1)) * K + (tid % (K / 8)) * 8);
+            gref[ch][0] = src[0];
+            gref[ch][1] = src[1];
+        }
+#pragma unroll
+        for (int j = 0; j < NIT; ++j) {
+            const int i = tid + 128 * j, r = i / (K / 8), lc = i % (K / 8);
             const uint32_t off = (uint32_t)((lc >> 3) * 8192 + r * 128 + (((lc & 7) ^ (r & 7)) << 4));
             const uint4 rq = *reinterpret_cast<const uint4*>(sm + L::Q + off);
             const uint4 rk = *reinterpret_cast<const uint4*>(sm + L::Kt + off);
             const bf16* qv = reinterpret_cast<const bf16*>(&rq);
             const bf16* kv = reinterpret_cast<const bf16*>(&rk);
             float fa[8], fb[8], gr[8], gf[8];
-            g8(r, lc * 8, gr);
-            g8(ref, lc * 8, gf);
+            unpack8(ga[j], gr);
+            unpack8(L::NCH > 1 && r >= C ? gref[L::NCH - 1] : gref[0], gf);
             bool big = false;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
@@ -217,14 +237,17 @@ tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         __syncthreads();
     }
     // q exp(G) in place (and, for two chunks per tile, split by chunk into Q and Q1)
-    for (int i = tid; i < kTile * (K / 8); i += 128) {
-        const int r = i / (K / 8), lc = i % (K / 8);
+    float4 gq[PER_K ? NIT : 1][2];
+    if constexpr (PER_K) load_g_rows(gq);
+#pragma unroll
+    for (int j = 0; j < NIT; ++j) {
+        const int i = tid + 128 * j, r = i / (K / 8), lc = i % (K / 8);
         const uint32_t off = (uint32_t)((lc >> 3) * 8192 + r * 128 + (((lc & 7) ^ (r & 7)) << 4));
         const uint4 raw = *reinterpret_cast<const uint4*>(sm + L::Q + off);
         const bf16* qv = reinterpret_cast<const bf16*>(&raw);
         float f[8], gr[8];
         if constexpr (PER_K) {
-            g8(r, lc * 8, gr);
+            unpack8(gq[j], gr);
         } else {
 #pragma unroll
             for (int e = 0; e < 8; ++e) gr[e] = sG[r];

@@ -60,18 +60,6 @@ __device__ __forceinline__ void each(float (&acc)[NCW][2][4], int rb, int cb0, i
             for (int e = 0; e < 4; ++e) f(16 * rb + g4 + 8 * (e >> 1), 16 * (cb0 + j) + 8 * n + 2 * q4 + (e & 1), acc[j][n][e]);
 }
 
-// Calls f(j, n, e, row, col) for every element index of a warp's tiles, for epilogues over several
-// accumulators with the same tiling.
-template <int NCW, typename F>
-__device__ __forceinline__ void each_at(int rb, int cb0, int g4, int q4, F&& f) {
-#pragma unroll
-    for (int j = 0; j < NCW; ++j)
-#pragma unroll
-        for (int n = 0; n < 2; ++n)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) f(j, n, e, 16 * rb + g4 + 8 * (e >> 1), 16 * (cb0 + j) + 8 * n + 2 * q4 + (e & 1));
-}
-
 // Calls f(row, col, x0&, x1&) for every pair of adjacent columns (col, col + 1) of a warp's tiles: the
 // two accumulator elements a thread holds side by side, so a bf16x2 load or store serves both.
 template <int NCW, typename F>
@@ -129,32 +117,6 @@ __device__ __forceinline__ void load_tile(bf16* dst, const bf16* src, int64_t gs
                          : "memory");
         else
             *reinterpret_cast<uint4*>(d) = make_uint4(0, 0, 0, 0);
-    }
-}
-
-// One row of bytes (a multiple of 16, both addresses 16-byte aligned) by the bulk-copy engine, completing
-// on the mbarrier as transaction bytes.
-__device__ __forceinline__ void bulk_row(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     smem_addr(dst)),
-                 "l"(src), "r"(bytes), "r"(smem_addr(bar))
-                 : "memory");
-}
-
-// rows x D bf16 from global rows of stride gs elements into shared [rows][D + 8], one bulk copy per row
-// (thread (r + off) % NTHR takes row r), completing on bar with nrows * D * 2 bytes; rows >= nrows are
-// zeroed with plain stores (visible to other threads after the next CTA barrier).
-// off rotates the rows over the threads, so several tiles issued together spread over the CTA.
-template <int D, int NTHR>
-__device__ __forceinline__ void bulk_tile(bf16* dst, const bf16* src, int64_t gs, int rows, int nrows, int tid,
-                                          uint64_t* bar, int off = 0) {
-    for (int r = ((tid - off) % NTHR + NTHR) % NTHR; r < rows; r += NTHR) {
-        if (r < nrows) {
-            bulk_row(dst + r * (D + 8), src + r * gs, D * 2, bar);
-        } else {
-#pragma unroll
-            for (int c8 = 0; c8 < D / 8; ++c8) *reinterpret_cast<uint4*>(dst + r * (D + 8) + 8 * c8) = make_uint4(0, 0, 0, 0);
-        }
     }
 }
 

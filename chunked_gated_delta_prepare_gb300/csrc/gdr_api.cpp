@@ -754,6 +754,191 @@ gdr_status gdr_backward(const gdr_problem* p, const void* q, const void* k, cons
     return GDR_OK;
 }
 
+}  // extern "C"
+
+// ---- packed variable-length sequences: the batch rows are the sequences, padded with zero tokens
+namespace {
+
+// Bytes a token takes in each padded tensor, in order.  Forward: q k v g beta | o.  Backward:
+// q k v g beta do | dq dk dv dg dbeta.  The first kVarlenIn[backward] are packed in, the rest unpacked out.
+constexpr int kVarlenIn[2] = {5, 6};
+constexpr int kVarlenAll[2] = {6, 11};
+
+void varlen_rows(const gdr::Dims& d, bool backward, int64_t* rb) {
+    const int64_t es = (d.bf16 || d.f16) ? 2 : 4;
+    const int64_t qk = (int64_t)d.Hk * d.K * es, vv = (int64_t)d.H * d.V * es;
+    const int64_t gg = (int64_t)d.H * (d.per_k ? d.K : 1) * 4, bb = (int64_t)d.H * es;
+    const int64_t fw[6] = {qk, qk, vv, gg, bb, vv};
+    const int64_t bw[11] = {qk, qk, vv, gg, bb, vv, qk, qk, vv, gg, bb};
+    for (int i = 0; i < kVarlenAll[backward]; ++i) rb[i] = backward ? bw[i] : fw[i];
+}
+
+struct VarlenWorkspace {
+    size_t cu, pad[11], inner, inner_bytes, total;
+};
+
+VarlenWorkspace plan_varlen(const gdr::Dims& d, bool backward, size_t inner_bytes) {
+    VarlenWorkspace ws{};
+    int64_t rb[11];
+    varlen_rows(d, backward, rb);
+    size_t off = 0;
+    ws.cu = off;
+    off = round_up(off + (size_t)(d.B + 1) * sizeof(int32_t), 256);
+    for (int i = 0; i < kVarlenAll[backward]; ++i) {
+        ws.pad[i] = off;
+        off = round_up(off + (size_t)d.B * d.T * rb[i], 256);
+    }
+    ws.inner = off;
+    ws.inner_bytes = inner_bytes;
+    ws.total = off + inner_bytes;
+    return ws;
+}
+
+// cu_seqlens on the host: cu[0] = 0, cu[n] = total, every length in [0, T]
+gdr_status check_cu(const int32_t* cu, int64_t n, int64_t total, int64_t T) {
+    if (!cu) return GDR_ERR_NULL;
+    if (total < 0 || cu[0] != 0 || (int64_t)cu[n] != total) return GDR_ERR_ARG;
+    for (int64_t s = 0; s < n; ++s) {
+        const int64_t len = (int64_t)cu[s + 1] - cu[s];
+        if (len < 0 || len > T) return GDR_ERR_ARG;
+    }
+    return GDR_OK;
+}
+
+gdr_status varlen_inner_bytes(const gdr_problem* p, const gdr::Dims& d, bool backward, size_t* bytes) {
+    gdr_status st;
+    int S = 1;
+    if (backward) {
+        BwdPath path;
+        if ((st = pick_backward(p, d, &path)) != GDR_OK) return st;
+        if ((st = resolve_segments(p, d, path != BwdPath::Simt, &S)) != GDR_OK) return st;
+        *bytes = plan_backward(d, path, S).total;
+    } else {
+        Path path;
+        if ((st = pick_forward(p, d, &path)) != GDR_OK) return st;
+        if ((st = resolve_segments(p, d, path != Path::Simt, &S)) != GDR_OK) return st;
+        *bytes = plan_staged(d, path == Path::Fused, S).total;
+    }
+    return GDR_OK;
+}
+
+// Validates a varlen call up to the workspace and returns its plan and the device cu to use
+// (the caller's, or the host array copied into the workspace on `s`).
+gdr_status varlen_setup(const gdr_problem* p, gdr::Dims* d, bool backward, const int32_t* cu_host,
+                        const int32_t* cu_dev, int64_t total, void* workspace, size_t workspace_bytes,
+                        cudaStream_t s, VarlenWorkspace* ws, const int** cu) {
+    gdr_status st = check_problem(p, d);
+    if (st != GDR_OK) return st;
+    if ((st = check_cu(cu_host, p->B, total, p->T)) != GDR_OK) return st;
+    if (cu_dev && (reinterpret_cast<uintptr_t>(cu_dev) & 3u) != 0) return GDR_ERR_ALIGN;
+    size_t inner = 0;
+    if ((st = varlen_inner_bytes(p, *d, backward, &inner)) != GDR_OK) return st;
+    *ws = plan_varlen(*d, backward, inner);
+    if (!workspace || workspace_bytes < ws->total) return GDR_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GDR_ERR_ALIGN;
+    if (cu_dev) {
+        *cu = cu_dev;
+    } else {
+        int32_t* c = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + ws->cu);
+        if ((st = from_cuda(cudaMemcpyAsync(c, cu_host, (size_t)(d->B + 1) * sizeof(int32_t),
+                                            cudaMemcpyHostToDevice, s))) != GDR_OK)
+            return st;
+        *cu = c;
+    }
+    return GDR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t gdr_varlen_forward_workspace_bytes(const gdr_problem* p) {
+    gdr::Dims d;
+    size_t inner = 0;
+    if (check_problem(p, &d) != GDR_OK || varlen_inner_bytes(p, d, false, &inner) != GDR_OK) return 0;
+    return plan_varlen(d, false, inner).total;
+}
+
+size_t gdr_varlen_backward_workspace_bytes(const gdr_problem* p) {
+    gdr::Dims d;
+    size_t inner = 0;
+    if (check_problem(p, &d) != GDR_OK || varlen_inner_bytes(p, d, true, &inner) != GDR_OK) return 0;
+    return plan_varlen(d, true, inner).total;
+}
+
+gdr_status gdr_varlen_forward(const gdr_problem* p, const int32_t* cu_seqlens, const int32_t* cu_seqlens_device,
+                              int64_t total, const void* q, const void* k, const void* v, const float* g,
+                              const void* beta, const float* h0, void* o, float* h_final, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+    gdr::Dims d;
+    gdr_status st = check_problem(p, &d);
+    if (st != GDR_OK) return st;
+    if (total > 0 && (st = check_ptrs({q, k, v, g, beta, o}, {h0, h_final})) != GDR_OK) return st;
+    if (total <= 0 && (st = check_ptrs({}, {q, k, v, g, beta, o, h0, h_final})) != GDR_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    VarlenWorkspace ws;
+    const int* cu = nullptr;
+    if ((st = varlen_setup(p, &d, false, cu_seqlens, cu_seqlens_device, total, workspace, workspace_bytes, s, &ws,
+                           &cu)) != GDR_OK)
+        return st;
+    char* base = static_cast<char*>(workspace);
+    int64_t rb[11];
+    varlen_rows(d, false, rb);
+    const void* packed[5] = {q, k, v, g, beta};
+    gdr::RowCopy in[5];
+    for (int i = 0; i < 5; ++i) in[i] = {packed[i], base + ws.pad[i], rb[i]};
+    if ((st = from_cuda(gdr::varlen_pack(in, 5, cu, d.B, total, d.T, s))) != GDR_OK) return st;
+    if ((st = gdr_forward(p, base + ws.pad[0], base + ws.pad[1], base + ws.pad[2],
+                          reinterpret_cast<const float*>(base + ws.pad[3]), base + ws.pad[4], h0, base + ws.pad[5],
+                          h_final, base + ws.inner, ws.inner_bytes, stream)) != GDR_OK)
+        return st;
+    if (total > 0) {
+        const gdr::RowCopy out[1] = {{base + ws.pad[5], o, rb[5]}};
+        if ((st = from_cuda(gdr::varlen_unpack(out, 1, cu, d.B, total, d.T, s))) != GDR_OK) return st;
+    }
+    return GDR_OK;
+}
+
+gdr_status gdr_varlen_backward(const gdr_problem* p, const int32_t* cu_seqlens, const int32_t* cu_seqlens_device,
+                               int64_t total, const void* q, const void* k, const void* v, const float* g,
+                               const void* beta, const float* h0, const void* d_o, const float* dh_final, void* dq,
+                               void* dk, void* dv, float* dg, void* dbeta, float* dh0, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+    gdr::Dims d;
+    gdr_status st = check_problem(p, &d);
+    if (st != GDR_OK) return st;
+    if (total > 0 && (st = check_ptrs({q, k, v, g, beta, d_o, dq, dk, dv, dg, dbeta}, {h0, dh_final, dh0})) != GDR_OK)
+        return st;
+    if (total <= 0 &&
+        (st = check_ptrs({}, {q, k, v, g, beta, d_o, dq, dk, dv, dg, dbeta, h0, dh_final, dh0})) != GDR_OK)
+        return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    VarlenWorkspace ws;
+    const int* cu = nullptr;
+    if ((st = varlen_setup(p, &d, true, cu_seqlens, cu_seqlens_device, total, workspace, workspace_bytes, s, &ws,
+                           &cu)) != GDR_OK)
+        return st;
+    char* base = static_cast<char*>(workspace);
+    int64_t rb[11];
+    varlen_rows(d, true, rb);
+    const void* packed_in[6] = {q, k, v, g, beta, d_o};
+    gdr::RowCopy in[6];
+    for (int i = 0; i < 6; ++i) in[i] = {packed_in[i], base + ws.pad[i], rb[i]};
+    if ((st = from_cuda(gdr::varlen_pack(in, 6, cu, d.B, total, d.T, s))) != GDR_OK) return st;
+    auto pad = [&](int i) { return static_cast<void*>(base + ws.pad[i]); };
+    if ((st = gdr_backward(p, pad(0), pad(1), pad(2), static_cast<const float*>(pad(3)), pad(4), h0, pad(5), dh_final,
+                           pad(6), pad(7), pad(8), static_cast<float*>(pad(9)), pad(10), dh0, base + ws.inner,
+                           ws.inner_bytes, stream)) != GDR_OK)
+        return st;
+    if (total > 0) {
+        void* packed_out[5] = {dq, dk, dv, dg, dbeta};
+        gdr::RowCopy out[5];
+        for (int i = 0; i < 5; ++i) out[i] = {pad(6 + i), packed_out[i], rb[6 + i]};
+        if ((st = from_cuda(gdr::varlen_unpack(out, 5, cu, d.B, total, d.T, s))) != GDR_OK) return st;
+    }
+    return GDR_OK;
+}
+
 const char* gdr_status_string(gdr_status s) {
     switch (s) {
         case GDR_OK: return "ok";

@@ -109,6 +109,19 @@ cudaError_t mma_bwd_chunk_kda(const Dims& d, const void* q, const void* k, const
                               const void* h_ckpt, const void* d_o, const void* dv_new, const void* dh_ckpt, void* dq,
                               void* dk, void* dv, void* dbeta, float* dg, int* exact_flags, cudaStream_t s);
 
+// ---- packed variable-length sequences (varlen.cu)
+// One tensor of token rows: packed [total, row] <-> padded [n, T, row], row_bytes bytes a token.
+struct RowCopy {
+    const void* src;
+    void* dst;
+    int64_t row_bytes;
+};
+constexpr int kMaxCopies = 8;
+// pack: copies[i].src packed, .dst padded (rows past a sequence's length zeroed); unpack: .src padded,
+// .dst packed (rows past a sequence's length not read).  cu: device int32 [n + 1]; the grid is capped at 8 CTAs per SM.
+cudaError_t varlen_pack(const RowCopy* copies, int count, const int* cu, int n, int64_t total, int T, cudaStream_t s);
+cudaError_t varlen_unpack(const RowCopy* copies, int count, const int* cu, int n, int64_t total, int T, cudaStream_t s);
+
 // ---- device error word (device_status.cu)
 // Bounded waits in kernels write a nonzero code here instead of trapping.
 cudaError_t read_and_clear_device_error(unsigned int* code);

@@ -9,10 +9,13 @@ The functions mirror the C ABI names:
     gdr_chunk_output,
     gdr_scan_output, gdr_forward, gdr_forward_workspace_bytes, gdr_forward_segments, gdr_bwd_dv_local, gdr_bwd_scan_dh, gdr_bwd_dqkwg, gdr_bwd_wy,
     gdr_bwd_prepare, gdr_bwd_scan_dh_p, gdr_bwd_wy_dqkg, gdr_backward, gdr_backward_workspace_bytes,
+    gdr_varlen_forward, gdr_varlen_forward_workspace_bytes, gdr_varlen_backward,
+    gdr_varlen_backward_workspace_bytes,
     gdr_status_string, gdr_get_device_status,
     gdr_last_variant, gdr_version
 and `forward(...)` / `backward(...)` are the convenience calls that allocate outputs and
-the workspace (and, given CPU tensors, copy them to the GPU and the results back).
+the workspace (and, given CPU tensors, copy them to the GPU and the results back);
+`forward_varlen(...)` / `backward_varlen(...)` the same for packed variable-length sequences.
 """
 from __future__ import annotations
 
@@ -38,6 +41,8 @@ EXPORTS = ["gdr_prepare_wy", "gdr_scan_h", "gdr_chunk_output", "gdr_forward", "g
            "gdr_backward_workspace_bytes", "gdr_bwd_prepare", "gdr_bwd_scan_dh_p", "gdr_bwd_wy_dqkg",
            "gdr_bwd_group_sum", "gdr_bwd_dv_local_tc", "gdr_bwd_scan_dh_tc", "gdr_scan_transfer",
            "gdr_scan_combine", "gdr_scan_combine_reverse", "gdr_forward_segments",
+           "gdr_varlen_forward", "gdr_varlen_forward_workspace_bytes", "gdr_varlen_backward",
+           "gdr_varlen_backward_workspace_bytes",
            "gdr_status_string", "gdr_get_device_status", "gdr_last_variant", "gdr_version"]
 
 
@@ -95,6 +100,10 @@ def load(path: str | None = None):
             "gdr_scan_combine": [P, ctypes.c_int32, vp, vp, vp, vp, vp, vp],
             "gdr_scan_combine_reverse": [P, ctypes.c_int32, vp, vp, vp, vp, vp, vp],
             "gdr_forward_segments": [P],
+            "gdr_varlen_forward": [P, vp, vp, ctypes.c_int64] + [vp] * 8 + [vp, ctypes.c_size_t, vp],
+            "gdr_varlen_forward_workspace_bytes": [P],
+            "gdr_varlen_backward": [P, vp, vp, ctypes.c_int64] + [vp] * 14 + [vp, ctypes.c_size_t, vp],
+            "gdr_varlen_backward_workspace_bytes": [P],
             "gdr_status_string": [ctypes.c_int],
             "gdr_get_device_status": [vp],
             "gdr_last_variant": [],
@@ -106,6 +115,8 @@ def load(path: str | None = None):
             f.restype = ctypes.c_int
         lib.gdr_forward_workspace_bytes.restype = ctypes.c_size_t
         lib.gdr_backward_workspace_bytes.restype = ctypes.c_size_t
+        lib.gdr_varlen_forward_workspace_bytes.restype = ctypes.c_size_t
+        lib.gdr_varlen_backward_workspace_bytes.restype = ctypes.c_size_t
         lib.gdr_status_string.restype = ctypes.c_char_p
         lib.gdr_last_variant.restype = ctypes.c_char_p
         if path is None:
@@ -455,6 +466,98 @@ def backward(q, k, v, g, beta, h0, d_o, dh_final=None, *, chunk=64, scale=None, 
         workspace = torch.empty(max(nbytes, 1), device=q.device, dtype=torch.uint8)
     have = workspace.numel() * workspace.element_size()
     gdr_backward(p, q, k, v, g, beta, h0, d_o, dh_final, dq, dk, dv, dg, dbeta, dh0, workspace, have, stream)
+    return dq, dk, dv, dg, dbeta, dh0
+
+
+# ---------------------------------------------------------------- packed variable-length sequences
+
+def gdr_varlen_forward_workspace_bytes(p) -> int:
+    return int(load().gdr_varlen_forward_workspace_bytes(ctypes.byref(p)))
+
+
+def gdr_varlen_backward_workspace_bytes(p) -> int:
+    return int(load().gdr_varlen_backward_workspace_bytes(ctypes.byref(p)))
+
+
+def _host_cu(cu):
+    """cu_seqlens as a contiguous host int32 tensor (and its pointer for the C ABI)."""
+    if isinstance(cu, torch.Tensor):
+        h = cu.detach().to("cpu", torch.int32).contiguous()
+    else:
+        h = torch.tensor(list(cu), dtype=torch.int32)
+    return h
+
+
+def gdr_varlen_forward(p, cu_seqlens, cu_seqlens_device, total, q, k, v, g, beta, h0, o, h_final, workspace,
+                       workspace_bytes, stream=None):
+    """cu_seqlens: a host int32 tensor [n + 1]; cu_seqlens_device: a device int32 tensor or None."""
+    _check(load().gdr_varlen_forward(ctypes.byref(p), _ptr(cu_seqlens), _ptr(cu_seqlens_device), int(total), _ptr(q),
+                                     _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(o), _ptr(h_final),
+                                     _ptr(workspace), int(workspace_bytes), _stream(stream)), "gdr_varlen_forward")
+
+
+def gdr_varlen_backward(p, cu_seqlens, cu_seqlens_device, total, q, k, v, g, beta, h0, d_o, dh_final, dq, dk, dv, dg,
+                        dbeta, dh0, workspace, workspace_bytes, stream=None):
+    _check(load().gdr_varlen_backward(ctypes.byref(p), _ptr(cu_seqlens), _ptr(cu_seqlens_device), int(total),
+                                      _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(d_o),
+                                      _ptr(dh_final), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dbeta), _ptr(dh0),
+                                      _ptr(workspace), int(workspace_bytes), _stream(stream)), "gdr_varlen_backward")
+
+
+def _varlen_problem(q, v, g, cu_host, max_len, chunk, scale, variant, segments):
+    """The padded problem of packed q [total,H,K] (or [1,total,H,K]), v, g: B = n sequences, T = max_len."""
+    n = cu_host.numel() - 1
+    if n < 1:
+        raise ValueError("cu_seqlens needs at least two entries")
+    lens = (cu_host[1:] - cu_host[:-1]).tolist()
+    T = max(max(lens), 1) if max_len is None else int(max_len)
+    H, K = q.shape[-2], q.shape[-1]
+    HV, V = v.shape[-2], v.shape[-1]
+    per_k = g.dim() == q.dim()
+    return make_problem(n, T, H, K, V, chunk, q.dtype, per_k, scale, variant, HV=HV if HV != H else 0,
+                        segments=segments)
+
+
+def forward_varlen(q, k, v, g, beta, cu_seqlens, h0=None, *, chunk=64, scale=None, variant="auto", max_len=None,
+                   want_h_final=True, workspace=None, stream=None, segments=0):
+    """o, h_final = forward_varlen(q, k, v, g, beta, cu_seqlens, h0) on packed device tensors.
+
+    q, k [total,H,K] (or with a leading 1), v [total,HV,V], g [total,HV(,K)], beta [total,HV];
+    cu_seqlens: the n + 1 cumulative lengths (list, host or device int32 tensor); h0 [n,HV,K,V] or None.
+    Returns o packed like v and h_final [n,HV,K,V] fp32 (None if not wanted)."""
+    cu_host = _host_cu(cu_seqlens)
+    cu_dev = cu_seqlens if (isinstance(cu_seqlens, torch.Tensor) and cu_seqlens.is_cuda
+                            and cu_seqlens.dtype == torch.int32 and cu_seqlens.is_contiguous()) else None
+    p = _varlen_problem(q, v, g, cu_host, max_len, chunk, scale, variant, segments)
+    total = int(cu_host[-1])
+    n, K, HV, V = int(p.B), q.shape[-1], v.shape[-2], v.shape[-1]
+    o = torch.empty(v.shape, device=v.device, dtype=v.dtype)
+    hf = torch.empty(n, HV, K, V, device=v.device, dtype=torch.float32) if want_h_final else None
+    if workspace is None:
+        workspace = torch.empty(max(gdr_varlen_forward_workspace_bytes(p), 1), device=v.device, dtype=torch.uint8)
+    have = workspace.numel() * workspace.element_size()
+    gdr_varlen_forward(p, cu_host, cu_dev, total, q, k, v, g, beta, h0, o, hf, workspace, have, stream)
+    return o, hf
+
+
+def backward_varlen(q, k, v, g, beta, cu_seqlens, h0, d_o, dh_final=None, *, chunk=64, scale=None, variant="auto",
+                    max_len=None, workspace=None, stream=None, segments=0):
+    """dq, dk, dv, dg, dbeta, dh0 = backward_varlen(...): the gradient of forward_varlen's (o, h_final)
+    against do (packed like o) and dh_final [n,HV,K,V]; packed outputs like their inputs."""
+    cu_host = _host_cu(cu_seqlens)
+    cu_dev = cu_seqlens if (isinstance(cu_seqlens, torch.Tensor) and cu_seqlens.is_cuda
+                            and cu_seqlens.dtype == torch.int32 and cu_seqlens.is_contiguous()) else None
+    p = _varlen_problem(q, v, g, cu_host, max_len, chunk, scale, variant, segments)
+    total = int(cu_host[-1])
+    n, K, HV, V = int(p.B), q.shape[-1], v.shape[-2], v.shape[-1]
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dg, dbeta = torch.empty_like(g), torch.empty_like(beta)
+    dh0 = torch.empty(n, HV, K, V, device=v.device, dtype=torch.float32)
+    if workspace is None:
+        workspace = torch.empty(max(gdr_varlen_backward_workspace_bytes(p), 1), device=v.device, dtype=torch.uint8)
+    have = workspace.numel() * workspace.element_size()
+    gdr_varlen_backward(p, cu_host, cu_dev, total, q, k, v, g, beta, h0, d_o, dh_final, dq, dk, dv, dg, dbeta, dh0,
+                        workspace, have, stream)
     return dq, dk, dv, dg, dbeta, dh0
 
 

@@ -435,6 +435,46 @@ GDR_API gdr_status gdr_backward(const gdr_problem* p, const void* q, const void*
                                 void* dq, void* dk, void* dv, float* dg, void* dbeta, float* dh0,
                                 void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Packed variable-length sequences.  The pages take equal-length batches only
+ * (the scan's host wrapper in "kernel_fun/kda/_kernels/bwd_scan.py" asserts a
+ * whole number of chunks).  A packed batch is read here as n independent
+ * problems of the same recurrence, each sequence starting from its own initial
+ * state; the n sequences of one packed token axis are the batch rows of p:
+ *   p->B = n, p->T = a row length at least the longest sequence.
+ *   cu_seqlens:        host int32 [n + 1], cu[0] = 0, non-decreasing, cu[n] = total,
+ *                      every length cu[s+1] - cu[s] <= p->T; otherwise GDR_ERR_ARG.
+ *   cu_seqlens_device: the same numbers in device memory (4-byte aligned), or NULL:
+ *                      the call then copies cu_seqlens into the workspace on `stream`
+ *                      (cudaMemcpyAsync; from pinned memory the host array must stay
+ *                      unchanged until the stream has passed the call, and a stream
+ *                      being captured into a graph needs cu_seqlens_device).
+ *   total:             packed tokens; 0 allowed (the packed pointers may then be NULL).
+ * Packed tensors have the batched layouts with B = 1 and T = total: q, k
+ * [total,H,K] io; v [total,HV,V] io; g [total,HV] or [total,HV,K] fp32; beta
+ * [total,HV] io; o like v.  Per-sequence tensors keep the batched layouts:
+ * h0, h_final, dh_final, dh0 [n,HV,K,V] fp32 (sequence s starts from h0[s]).
+ * The call moves sequence s into row s of padded copies in the workspace,
+ * filling the row's tail with zero tokens (beta = 0, g = 0, q = k = v = 0: the
+ * state passes unchanged and their outputs are dropped), runs gdr_forward /
+ * gdr_backward on p, and moves the first len_s rows of each padded result back.
+ * Zero tokens cost the same as real ones: the padded work is n * p->T tokens.
+ * workspace: at least gdr_varlen_*_workspace_bytes(p), 256-byte aligned, owned by the caller.
+ */
+GDR_API size_t gdr_varlen_forward_workspace_bytes(const gdr_problem* p);
+GDR_API gdr_status gdr_varlen_forward(const gdr_problem* p, const int32_t* cu_seqlens, const int32_t* cu_seqlens_device,
+                                      int64_t total, const void* q, const void* k, const void* v, const float* g,
+                                      const void* beta, const float* h0, void* o, float* h_final, void* workspace,
+                                      size_t workspace_bytes, void* stream);
+/* The gradient of gdr_varlen_forward's (o, h_final): do packed like o, dh_final [n,HV,K,V]
+ * fp32 or NULL; dq, dk, dv, dg, dbeta packed like q, k, v, g, beta; dh0 [n,HV,K,V] or NULL. */
+GDR_API size_t gdr_varlen_backward_workspace_bytes(const gdr_problem* p);
+GDR_API gdr_status gdr_varlen_backward(const gdr_problem* p, const int32_t* cu_seqlens,
+                                       const int32_t* cu_seqlens_device, int64_t total, const void* q, const void* k,
+                                       const void* v, const float* g, const void* beta, const float* h0,
+                                       const void* d_o, const float* dh_final, void* dq, void* dk, void* dv, float* dg,
+                                       void* dbeta, float* dh0, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Static, human-readable text for a status code. */
 GDR_API const char* gdr_status_string(gdr_status s);
 

@@ -200,3 +200,64 @@ def test_stage_entry_points_validate(lib):
 def test_python_binding_raises_on_missing_library(tmp_path):
     with pytest.raises(RuntimeError):
         gdr.load(str(tmp_path / "libgdr_missing.so"))
+
+
+# ---------------------------------------------------------------- packed variable-length sequences
+
+def _cu(vals):
+    return None if vals is None else (ctypes.c_int32 * len(vals))(*vals)
+
+
+def _varlen_fwd(lib, p, cu, total, cu_dev=None, ws=None, ws_bytes=0, ptrs=None):
+    a = dict(q=16, k=16, v=16, g=16, beta=16, h0=None, o=16, hf=None)
+    a.update(ptrs or {})
+    return lib.gdr_varlen_forward(ctypes.byref(p), _cu(cu), cu_dev, total, a["q"], a["k"], a["v"], a["g"], a["beta"],
+                                  a["h0"], a["o"], a["hf"], ws, ws_bytes, None)
+
+
+def _varlen_bwd(lib, p, cu, total, ws=None, ws_bytes=0):
+    return lib.gdr_varlen_backward(ctypes.byref(p), _cu(cu), None, total, 16, 16, 16, 16, 16, None, 16, None, 16, 16,
+                                   16, 16, 16, None, ws, ws_bytes, None)
+
+
+def test_varlen_checks_cu_seqlens_on_the_host(lib):
+    p = gdr.make_problem(3, 100, 2, 64, 64, 64)           # three sequences, rows of 100 tokens
+    # a good cu reaches the workspace check (no workspace given: GDR_ERR_WORKSPACE) without launching
+    assert _varlen_fwd(lib, p, [0, 50, 50, 150], 150) == 5
+    assert _varlen_bwd(lib, p, [0, 50, 50, 150], 150) == 5
+    assert _varlen_fwd(lib, p, [0, 100, 200, 300], 300) == 5
+    for cu, total in (([1, 50, 50, 151], 151),            # does not start at 0
+                      ([0, 60, 50, 150], 150),            # decreases
+                      ([0, 101, 101, 150], 150),          # a sequence longer than the rows
+                      ([0, 50, 50, 150], 149)):           # total is not cu[n]
+        assert _varlen_fwd(lib, p, cu, total) == 9, cu
+        assert _varlen_bwd(lib, p, cu, total) == 9, cu
+    assert _varlen_fwd(lib, p, None, 150) == 1
+    assert _varlen_fwd(lib, p, [0, 50, 50, 150], 150, cu_dev=18) == 4   # device cu must be 4-byte aligned
+    assert _varlen_fwd(lib, p, [0, 50, 50, 150], 150, ptrs=dict(q=None)) == 1
+    assert _varlen_fwd(lib, p, [0, 50, 50, 150], 150, ptrs=dict(o=24)) == 4
+    # no tokens at all: the packed pointers may be NULL
+    empty = dict(q=None, k=None, v=None, g=None, beta=None, o=None)
+    assert _varlen_fwd(lib, p, [0, 0, 0, 0], 0, ptrs=empty) == 5
+    p.T = 0
+    assert _varlen_fwd(lib, p, [0, 0, 0, 0], 0, ptrs=empty) == 2
+
+
+def test_varlen_workspace_size_formula(lib):
+    # device cu, then every padded tensor [n, T, ...], each rounded up to 256 bytes, then the batched call's
+    r = lambda x: (x + 255) // 256 * 256
+    for (n, T, H, HV, K, V, C, dt, per_k, variant) in [(3, 100, 2, 2, 64, 64, 64, 1, False, "auto"),
+                                                        (5, 333, 1, 4, 128, 64, 32, 1, True, "auto"),
+                                                        (2, 64, 2, 2, 64, 128, 64, 0, True, "simt")]:
+        p = gdr.make_problem(n, T, H, K, V, C, dt, per_k, variant=variant, HV=HV if HV != H else 0)
+        e = 2 if dt else 4
+        qk, vv, gg, bb = H * K * e, HV * V * e, HV * (K if per_k else 1) * 4, HV * e
+        pad = lambda rows: sum(r(n * T * b) for b in rows)
+        fwd = r((n + 1) * 4) + pad([qk, qk, vv, gg, bb, vv]) + lib.gdr_forward_workspace_bytes(ctypes.byref(p))
+        bwd = r((n + 1) * 4) + pad([qk, qk, vv, gg, bb, vv, qk, qk, vv, gg, bb]) + \
+            lib.gdr_backward_workspace_bytes(ctypes.byref(p))
+        assert lib.gdr_varlen_forward_workspace_bytes(ctypes.byref(p)) == fwd
+        assert lib.gdr_varlen_backward_workspace_bytes(ctypes.byref(p)) == bwd
+    bad = gdr.make_problem(3, 100, 2, 96, 64, 64)
+    assert lib.gdr_varlen_forward_workspace_bytes(ctypes.byref(bad)) == 0
+    assert lib.gdr_varlen_backward_workspace_bytes(ctypes.byref(bad)) == 0

@@ -346,3 +346,61 @@ def test_segment_mutant_is_caught(what, old, new):
         src = f.read()
     assert src.count(old) == 1, f"mutation site not found: {old!r}"
     assert _segment_pins_fail(_load_segments(src.replace(old, new)))
+
+
+# ------------------------------------------------------------ packed variable-length sequences
+
+VARLEN_SRC = os.path.join(ROOT, "oracle", "varlen.py")
+
+VARLEN_MUTANTS = [
+    ("state carried into the next sequence", '        hf[s] = r["h_final"][0]\n    return o, hf',
+     '        hf[s] = r["h_final"][0]\n        if s + 1 < n:\n            h0[s + 1] = hf[s]\n    return o, hf'),
+    ("an empty sequence ends in the zero state", "            hf[s] = h0[s]\n", "            hf[s] = 0.0\n"),
+    ("a sequence reads the next one's first token",
+     "r = naive_forward(q[None, a:b], k[None, a:b],", "r = naive_forward(q[None, a + 1:b + 1], k[None, a:b],"),
+    ("outputs placed one row late", '        o[a:b] = r["o"][0]', '        o[a + 1:b + 1] = r["o"][0][:len(o[a + 1:b + 1])]'),
+    ("an empty sequence drops the final-state gradient", '            out["dh0"][s] = dhf[s]',
+     '            out["dh0"][s] = 0.0'),
+    ("the backward reads do from the packed start", "do[None, a:b], dhf[s:s + 1]", "do[None, 0:b - a], dhf[s:s + 1]"),
+]
+
+
+def _varlen_pins_fail(mod) -> bool:
+    import test_oracle_varlen_pins as pins
+    checks = [lambda: pins.test_one_token_sequences_closed_form()]
+    for per_k in (False, True):
+        checks.append(lambda per_k=per_k: pins.test_equal_lengths_are_the_batch(per_k))
+        checks.append(lambda per_k=per_k: pins.test_sequences_do_not_see_each_other(per_k))
+        checks.append(lambda per_k=per_k: pins.test_empty_sequence_passes_its_state(per_k))
+        checks.append(lambda per_k=per_k: pins.test_backward_matches_finite_differences(per_k))
+    saved = pins.varlen
+    pins.varlen = mod
+    try:
+        for check in checks:
+            try:
+                check()
+            except Exception:
+                return True
+        return False
+    finally:
+        pins.varlen = saved
+
+
+def _load_varlen(src: str):
+    mod = types.ModuleType("oracle.varlen_mutant")
+    mod.__package__ = "oracle"
+    exec(compile(src, "varlen_mutant.py", "exec"), mod.__dict__)
+    return mod
+
+
+def test_unmutated_varlen_passes_the_pins():
+    with open(VARLEN_SRC) as f:
+        assert not _varlen_pins_fail(_load_varlen(f.read()))
+
+
+@pytest.mark.parametrize("what,old,new", VARLEN_MUTANTS, ids=[m[0] for m in VARLEN_MUTANTS])
+def test_varlen_mutant_is_caught(what, old, new):
+    with open(VARLEN_SRC) as f:
+        src = f.read()
+    assert src.count(old) == 1, f"mutation site not found: {old!r}"
+    assert _varlen_pins_fail(_load_varlen(src.replace(old, new)))

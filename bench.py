@@ -10,6 +10,10 @@ timed step is bracketed by CUDA events on the launching stream; a 256 MiB
 buffer (about twice the L2) is overwritten before every timed step, outside the
 events.  Rank 0 prints one JSON line.
 
+The same line carries two more legs on the same workload: "backward" (the
+gradient of o and h_final, stage by stage) and "varlen" (the workload's tokens
+packed as eleven sequences of mixed length through gdr_varlen_forward).
+
 --impl reference times the float64 CPU oracle (the only other implementation
 of this computation) on the host cores, one bounded sample of the same workload
 per step.
@@ -35,7 +39,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from chunked_gated_delta_prepare_gb300 import gdr, workloads  # noqa: E402
-from chunked_gated_delta_prepare_gb300.inputs import make_workload_inputs  # noqa: E402
+from chunked_gated_delta_prepare_gb300.inputs import make_varlen_inputs, make_workload_inputs  # noqa: E402
 
 METRIC = "gated-delta-rule fwd tokens/s at 1 GB300; achieved HBM GB/s & % roofline"
 FLUSH_BYTES = 256 << 20
@@ -365,6 +369,65 @@ def time_backward(args, wl, x, dev, flush, stream, world):
             "upstream": "do ~ N(0,1) in the io dtype, dh_final ~ N(0,1) fp32, seed 7"}
 
 
+# packed variable-length leg: the workload's tokens as eleven sequences of mixed length (one empty,
+# one a single token, ragged tails), the mix given here for 32768 tokens and scaled to other totals
+VARLEN_MIX = [8192, 4096, 4133, 1, 6000, 0, 2048, 3000, 777, 2911, 1610]
+
+
+def varlen_lengths(total: int):
+    out = [n * total // sum(VARLEN_MIX) for n in VARLEN_MIX]
+    out[0] += total - sum(out)
+    return out
+
+
+def time_varlen(args, wl, dev, flush, stream, world):
+    """gdr_varlen_forward on the workload's B T tokens packed as VARLEN_MIX: one C-ABI call per step
+    (pack, the batched forward on rows as long as the longest sequence, unpack)."""
+    lengths = varlen_lengths(wl.B * wl.T)
+    x = make_varlen_inputs(lengths, wl.H, wl.K, wl.V, per_k_gate=wl.per_k_gate, io_dtype=wl.torch_dtype,
+                           with_h0=wl.with_h0, seed=0)
+    q, k, v, g, beta = (t.to(dev) for t in (x.q, x.k, x.v, x.g, x.beta))
+    h0 = x.h0.to(dev) if x.h0 is not None else None
+    cu_dev = x.cu.to(dev)
+    total = int(x.cu[-1])
+    p = gdr._varlen_problem(q, v, g, x.cu, None, wl.chunk, None, args.variant, args.segments)
+    o = torch.empty_like(v)
+    hf = torch.empty(int(p.B), wl.H, wl.K, wl.V, device=dev, dtype=torch.float32)
+    nbytes = gdr.gdr_varlen_forward_workspace_bytes(p)
+    ws = torch.empty(nbytes, device=dev, dtype=torch.uint8)
+
+    def call():
+        gdr.gdr_varlen_forward(p, x.cu, cu_dev, total, q, k, v, g, beta, h0, o, hf, ws, nbytes)
+
+    call()
+    variant = gdr.gdr_last_variant()
+    S = gdr.gdr_forward_segments(p)
+    launches = 2 + {"fused": 2}.get(variant, 3) + (2 if S > 1 else 0)
+    steps = max(3, min(args.steps, 10))
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        call()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for s in range(steps):
+        flush.fill_(s & 0xFF)
+        evs[s][0].record(stream)
+        call()
+        evs[s][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    if gdr.gdr_get_device_status() != 0:
+        raise RuntimeError("device status set after the packed forward's timed region")
+    total_s = max_over_ranks(sum(a.elapsed_time(b) for a, b in evs) / 1e3, world)
+    return {"ms_per_step": 1e3 * total_s / steps, "steps": steps,
+            "value": weak_scaling_throughput(world, total, steps, total_s), "unit": "tokens/s",
+            "sequences": len(lengths), "lengths": lengths, "row_tokens": int(p.T),
+            "padded_tokens": int(p.B * p.T), "variant": variant, "segments": S,
+            "gpu_launches": launches * steps}
+
+
 def run_ours(args, wl):
     world, rank, local = dist_setup()
     dev = torch.device("cuda", local)
@@ -510,6 +573,7 @@ def run_ours(args, wl):
     e2e_value = weak_scaling_throughput(world, B * T, e2e_steps, e2e_s)
 
     bwd = None if args.no_backward else time_backward(args, wl, x, dev, flush, stream, world)
+    vl = None if args.no_varlen else time_varlen(args, wl, dev, flush, stream, world)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -535,6 +599,8 @@ def run_ours(args, wl):
         }
         if bwd is not None:
             line["backward"] = bwd
+        if vl is not None:
+            line["varlen"] = vl
         if cpu is not None:
             line["cpu_baseline"] = {"value": cpu["tokens_per_s"], "unit": "tokens/s", "cores": cpu["cores"],
                                     "kind": "oracle", "sample": cpu["sample"]}
@@ -558,6 +624,7 @@ def main():
     ap.add_argument("--ref-heads", type=int, default=4, help="heads per step of --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-backward", action="store_true", help="skip timing the backward pass")
+    ap.add_argument("--no-varlen", action="store_true", help="skip timing the packed variable-length forward")
     ap.add_argument("--p-from", choices=["prepare", "scan"], default="prepare",
                     help="fused path: gated scores P written by the prepare, or formed inside the scan kernel")
     ap.add_argument("--seq-len", type=int, default=None,

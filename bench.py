@@ -381,8 +381,10 @@ def varlen_lengths(total: int):
 
 
 def time_varlen(args, wl, dev, flush, stream, world):
-    """gdr_varlen_forward on the workload's B T tokens packed as VARLEN_MIX: one C-ABI call per step
-    (pack, the batched forward on rows as long as the longest sequence, unpack)."""
+    """gdr_varlen_forward on the workload's B T tokens packed as VARLEN_MIX: one C-ABI call per step.
+    On the tensor cores it runs chunk-packed (the chunk map, the pack, the prepare, the scan and output
+    walking each sequence's chunks, the unpack); on the CUDA cores padded (the pack, gdr_forward on rows
+    as long as the longest sequence, the unpack)."""
     lengths = varlen_lengths(wl.B * wl.T)
     x = make_varlen_inputs(lengths, wl.H, wl.K, wl.V, per_k_gate=wl.per_k_gate, io_dtype=wl.torch_dtype,
                            with_h0=wl.with_h0, seed=0)
@@ -401,8 +403,15 @@ def time_varlen(args, wl, dev, flush, stream, world):
 
     call()
     variant = gdr.gdr_last_variant()
-    S = gdr.gdr_forward_segments(p)
-    launches = 2 + {"fused": 2}.get(variant, 3) + (2 if S > 1 else 0)
+    C = wl.chunk
+    chunked = variant != "simt" and total > 0
+    S = 1 if chunked else gdr.gdr_forward_segments(p)
+    if chunked:
+        layout, working = "chunk-packed", sum(-(-n // C) * C for n in lengths)
+        launches = 3 + (2 if variant == "fused" else 3)
+    else:
+        layout, working = "padded", int(p.B * p.T)
+        launches = 2 + (2 if variant == "fused" else 3) + (2 if S > 1 else 0)
     steps = max(3, min(args.steps, 10))
     for _ in range(args.warmup):
         flush.fill_(1)
@@ -423,8 +432,8 @@ def time_varlen(args, wl, dev, flush, stream, world):
     total_s = max_over_ranks(sum(a.elapsed_time(b) for a, b in evs) / 1e3, world)
     return {"ms_per_step": 1e3 * total_s / steps, "steps": steps,
             "value": weak_scaling_throughput(world, total, steps, total_s), "unit": "tokens/s",
-            "sequences": len(lengths), "lengths": lengths, "row_tokens": int(p.T),
-            "padded_tokens": int(p.B * p.T), "variant": variant, "segments": S,
+            "sequences": len(lengths), "lengths": lengths, "layout": layout, "working_tokens": working,
+            "variant": variant, "segments": S,
             "gpu_launches": launches * steps}
 
 

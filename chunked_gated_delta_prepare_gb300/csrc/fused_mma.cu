@@ -89,13 +89,15 @@ struct FLayout {
 // GENERAL: a partial last chunk or grouped value heads.  Whole chunks of ungrouped
 // heads take the variant without those guards: this kernel's schedule is sensitive
 // enough that the guards alone measured 4-7% slower where they are not needed.
+// co (packed variable-length sequences; NULL otherwise): one data row (B = 1) of whole-chunk runs,
+// sequence z = blockIdx.z on the chunks co[z] .. co[z+1]-1, from h0[z] to h_final[z].
 template <int K, int C, bool HAS_P, bool GENERAL>
 __global__ void __launch_bounds__(FLayout<K, C, HAS_P>::kThreads, 1)
 fused_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap mk,
                          const __grid_constant__ CUtensorMap mu, const __grid_constant__ CUtensorMap mq,
                          const __grid_constant__ CUtensorMap mpk, const float* __restrict__ g_cum,
-                         const float* __restrict__ h0, bf16* __restrict__ o, float* __restrict__ h_final, int T,
-                         int H, int V, int G, float scale, unsigned int* err) {
+                         const float* __restrict__ h0, bf16* __restrict__ o, float* __restrict__ h_final,
+                         const int* __restrict__ co, int T, int H, int V, int G, float scale, unsigned int* err) {
     using L = FLayout<K, C, HAS_P>;
     constexpr int NSA = L::NSA, NSB = L::NSB, NOW = L::NOW, NT8 = L::NT8, KH = L::KH;
     constexpr int NJH = KH / 8;
@@ -106,11 +108,15 @@ fused_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_co
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int v0 = blockIdx.x * kBV, h = blockIdx.y, b = blockIdx.z;
-    const int NT = GENERAL ? (T + C - 1) / C : T / C;   // a last, partial chunk runs as zero tokens past T
+    const int NTall = GENERAL ? (T + C - 1) / C : T / C;   // a last, partial chunk runs as zero tokens past T
+    // this CTA's chunks: c0 .. c0 + NT - 1 of data row bd (clamped, so any co stays inside the tensors)
+    const int c0 = co ? min(max(co[b], 0), NTall) : 0;
+    const int NT = co ? min(max(co[b + 1], c0), NTall) - c0 : NTall;
+    const int bd = co ? 0 : b;
     const int hk = GENERAL ? h / G : h;                  // q/k head of value head h
     const int g = lane >> 2, q4 = lane & 3, mi = lane >> 3, mr = lane & 7;
     auto row = [&](int t) -> int64_t {                   // G past T: its last value
-        return ((int64_t)b * T + (GENERAL ? min(t, T - 1) : t)) * H + h;
+        return ((int64_t)bd * T + (GENERAL ? min(t, T - 1) : t)) * H + h;
     };
 
     if (tid == 0) {
@@ -138,8 +144,8 @@ fused_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_co
         float gn[GPL], gln;
         auto load_g = [&](int c) {
 #pragma unroll
-            for (int i = 0; i < GPL; ++i) gn[i] = g_cum[row(c * C + lane + 32 * i)];
-            gln = g_cum[row(c * C + C - 1)];
+            for (int i = 0; i < GPL; ++i) gn[i] = g_cum[row((c0 + c) * C + lane + 32 * i)];
+            gln = g_cum[row((c0 + c) * C + C - 1)];
         };
         if (NT > 0) load_g(0);
         for (int c = 0; c < NT; ++c) {
@@ -149,15 +155,15 @@ fused_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_co
             for (int i = 0; i < GPL; ++i) gc[i] = gn[i];
             if (c + 1 < NT) load_g(c + 1);
             if (!bw::mbar_wait(&emptyA[s], ((c / NSA) & 1) ^ 1, err, kDeviceErrTimeout)) break;
-            const int t0 = c * C;
+            const int t0 = (c0 + c) * C;
             if (lane == 0) {
                 bw::mbar_arrive_expect_tx(&fullA[s], L::tx_a);
 #pragma unroll
                 for (int a = 0; a < K / 64; ++a) {
-                    bw::tma_load_4d(sm + L::W + s * L::kKC + a * C * 128, &mw, &fullA[s], a * 64, h, t0, b);
-                    bw::tma_load_4d(sm + L::KB + s * L::kKC + a * C * 128, &mk, &fullA[s], a * 64, hk, t0, b);
+                    bw::tma_load_4d(sm + L::W + s * L::kKC + a * C * 128, &mw, &fullA[s], a * 64, h, t0, bd);
+                    bw::tma_load_4d(sm + L::KB + s * L::kKC + a * C * 128, &mk, &fullA[s], a * 64, hk, t0, bd);
                 }
-                bw::tma_load_4d(sm + L::U + s * L::kU, &mu, &fullA[s], v0, h, t0, b);
+                bw::tma_load_4d(sm + L::U + s * L::kU, &mu, &fullA[s], v0, h, t0, bd);
                 sDec[s] = __expf(glc);
             }
 #pragma unroll
@@ -171,7 +177,7 @@ fused_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_co
         float* sG = reinterpret_cast<float*>(sm + L::GO);
         for (int c = 0; c < NT; ++c) {
             const int s = c % NSB;
-            const int t0 = c * C;
+            const int t0 = (c0 + c) * C;
             float gv[C / 32];
 #pragma unroll
             for (int i = 0; i < C / 32; ++i) gv[i] = g_cum[row(t0 + lane + 32 * i)];
@@ -180,11 +186,11 @@ fused_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_co
                 bw::mbar_arrive_expect_tx(&fullB[s], L::tx_b);
 #pragma unroll
                 for (int a = 0; a < K / 64; ++a) {
-                    bw::tma_load_4d(sm + L::Q + s * L::kKC + a * C * 128, &mq, &fullB[s], a * 64, hk, t0, b);
+                    bw::tma_load_4d(sm + L::Q + s * L::kKC + a * C * 128, &mq, &fullB[s], a * 64, hk, t0, bd);
                     if constexpr (!HAS_P)
-                        bw::tma_load_4d(sm + L::PK + s * L::kPK + a * C * 128, &mpk, &fullB[s], a * 64, hk, t0, b);
+                        bw::tma_load_4d(sm + L::PK + s * L::kPK + a * C * 128, &mpk, &fullB[s], a * 64, hk, t0, bd);
                 }
-                if constexpr (HAS_P) bw::tma_load_4d(sm + L::PK + s * L::kPK, &mpk, &fullB[s], 0, 0, h, b * NT + c);
+                if constexpr (HAS_P) bw::tma_load_4d(sm + L::PK + s * L::kPK, &mpk, &fullB[s], 0, 0, h, bd * NTall + c0 + c);
             }
 #pragma unroll
             for (int i = 0; i < C / 32; ++i) sG[s * C + lane + 32 * i] = gv[i];
@@ -350,7 +356,7 @@ fused_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_co
     bool ok = true;
     for (int c = 0; c < NT; ++c) {
         const int s = c % NSB, hb = c & 1;
-        const int t0 = c * C;
+        const int t0 = (c0 + c) * C;
         ok = ok && bw::mbar_wait(&fullB[s], (c / NSB) & 1, err, kDeviceErrTimeout);
         const uint32_t q_t = s_base + L::Q + s * L::kKC;
         const uint32_t pk_t = s_base + L::PK + s * L::kPK;
@@ -455,7 +461,7 @@ fused_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_co
                          : "memory");
         }
         __syncwarp();
-        bf16* dst = o + (((int64_t)b * T + t0 + r0) * H + h) * V + v0;
+        bf16* dst = o + (((int64_t)bd * T + t0 + r0) * H + h) * V + v0;
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
             const int rr = 8 * i + (lane >> 2), ch = lane & 3;
@@ -469,7 +475,8 @@ fused_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_co
 
 template <int K, int C, bool HAS_P, bool GENERAL>
 cudaError_t launch_v(const Dims& d, const void* q, const void* k, const void* w, const void* u, const float* g_cum,
-                     const void* P, const float* h0, void* o, float* h_final, cudaStream_t s, unsigned int* err) {
+                     const void* P, const float* h0, void* o, float* h_final, const int* co, int nseq, cudaStream_t s,
+                     unsigned int* err) {
     using L = FLayout<K, C, HAS_P>;
     CUtensorMap mw, mk, mu, mq, mpk;
     if (!make_tmap_tokens(&mw, w, d.B, d.T, d.H, K, C) || !make_tmap_tokens(&mk, k, d.B, d.T, d.Hk, K, C) ||
@@ -488,35 +495,36 @@ cudaError_t launch_v(const Dims& d, const void* q, const void* k, const void* w,
     const size_t smem = L::bytes + 1024;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const dim3 grid(d.V / kBV, d.H, d.B);
-    kern<<<grid, L::kThreads, smem, s>>>(mw, mk, mu, mq, mpk, g_cum, h0, (bf16*)o, h_final, d.T, d.H, d.V, d.G,
+    const dim3 grid(d.V / kBV, d.H, co ? nseq : d.B);
+    kern<<<grid, L::kThreads, smem, s>>>(mw, mk, mu, mq, mpk, g_cum, h0, (bf16*)o, h_final, co, d.T, d.H, d.V, d.G,
                                          d.scale, err);
     return cudaGetLastError();
 }
 
 template <int K, int C, bool HAS_P>
 cudaError_t launch(const Dims& d, const void* q, const void* k, const void* w, const void* u, const float* g_cum,
-                   const void* P, const float* h0, void* o, float* h_final, cudaStream_t s, unsigned int* err) {
+                   const void* P, const float* h0, void* o, float* h_final, const int* co, int nseq, cudaStream_t s,
+                   unsigned int* err) {
     if (d.T % C != 0 || d.G != 1)
-        return launch_v<K, C, HAS_P, true>(d, q, k, w, u, g_cum, P, h0, o, h_final, s, err);
-    return launch_v<K, C, HAS_P, false>(d, q, k, w, u, g_cum, P, h0, o, h_final, s, err);
+        return launch_v<K, C, HAS_P, true>(d, q, k, w, u, g_cum, P, h0, o, h_final, co, nseq, s, err);
+    return launch_v<K, C, HAS_P, false>(d, q, k, w, u, g_cum, P, h0, o, h_final, co, nseq, s, err);
 }
 
 }  // namespace
 
 cudaError_t mma_scan_output(const Dims& d, const void* q, const void* k, const void* w, const void* u,
                             const float* g_cum, const void* P, const float* h0, void* o, float* h_final,
-                            cudaStream_t s, unsigned int* err) {
-    if (!d.bf16 || d.per_k) return cudaErrorInvalidValue;
+                            cudaStream_t s, unsigned int* err, const int* co, int nseq) {
+    if (!d.bf16 || d.per_k || (co && (d.B != 1 || nseq < 1))) return cudaErrorInvalidValue;
     if (P) {
         if (d.C != 64) return cudaErrorInvalidValue;
-        return d.K == 64 ? launch<64, 64, true>(d, q, k, w, u, g_cum, P, h0, o, h_final, s, err)
-                         : launch<128, 64, true>(d, q, k, w, u, g_cum, P, h0, o, h_final, s, err);
+        return d.K == 64 ? launch<64, 64, true>(d, q, k, w, u, g_cum, P, h0, o, h_final, co, nseq, s, err)
+                         : launch<128, 64, true>(d, q, k, w, u, g_cum, P, h0, o, h_final, co, nseq, s, err);
     }
-    if (d.K == 64) return d.C == 32 ? launch<64, 32, false>(d, q, k, w, u, g_cum, P, h0, o, h_final, s, err)
-                                    : launch<64, 64, false>(d, q, k, w, u, g_cum, P, h0, o, h_final, s, err);
-    return d.C == 32 ? launch<128, 32, false>(d, q, k, w, u, g_cum, P, h0, o, h_final, s, err)
-                     : launch<128, 64, false>(d, q, k, w, u, g_cum, P, h0, o, h_final, s, err);
+    if (d.K == 64) return d.C == 32 ? launch<64, 32, false>(d, q, k, w, u, g_cum, P, h0, o, h_final, co, nseq, s, err)
+                                    : launch<64, 64, false>(d, q, k, w, u, g_cum, P, h0, o, h_final, co, nseq, s, err);
+    return d.C == 32 ? launch<128, 32, false>(d, q, k, w, u, g_cum, P, h0, o, h_final, co, nseq, s, err)
+                     : launch<128, 64, false>(d, q, k, w, u, g_cum, P, h0, o, h_final, co, nseq, s, err);
 }
 
 }  // namespace gdr

@@ -756,12 +756,14 @@ gdr_status gdr_backward(const gdr_problem* p, const void* q, const void* k, cons
 
 }  // extern "C"
 
-// ---- packed variable-length sequences: the batch rows are the sequences, padded with zero tokens
+// ---- packed variable-length sequences
+// The forward on the tensor cores runs them chunk-packed: every sequence a run of whole chunks of one
+// row (fewer than C zero tokens each), the scans walking each sequence's chunks.  The CUDA-core forward
+// and the backward run them padded: sequence s as row s of a batch of rows of p->T tokens.
 namespace {
 
-// Bytes a token takes in each padded tensor, in order.  Forward: q k v g beta | o.  Backward:
-// q k v g beta do | dq dk dv dg dbeta.  The first kVarlenIn[backward] are packed in, the rest unpacked out.
-constexpr int kVarlenIn[2] = {5, 6};
+// Bytes a token takes in each working tensor, in order.  Forward: q k v g beta (packed in) | o (unpacked
+// out).  Backward: q k v g beta do (in) | dq dk dv dg dbeta (out).
 constexpr int kVarlenAll[2] = {6, 11};
 
 void varlen_rows(const gdr::Dims& d, bool backward, int64_t* rb) {
@@ -773,20 +775,45 @@ void varlen_rows(const gdr::Dims& d, bool backward, int64_t* rb) {
     for (int i = 0; i < kVarlenAll[backward]; ++i) rb[i] = backward ? bw[i] : fw[i];
 }
 
+// The chunk-packed problem of at most `chunks` chunks: one row of whole chunks.
+gdr::Dims chunk_packed(const gdr::Dims& d, int64_t chunks) {
+    gdr::Dims v = d;
+    v.B = 1;
+    v.NT = (int)chunks;
+    v.T = (int)(chunks * d.C);
+    return v;
+}
+
+// chunks of the chunk-packed layout in the worst case for p: n sequences of p->T tokens
+int64_t max_chunks(const gdr::Dims& d) { return (int64_t)d.B * d.NT; }
+
+// the forward runs chunk-packed on the tensor cores, when the packed row's indices fit in int32
+bool forward_chunk_packed(const gdr::Dims& d, Path path) {
+    return path != Path::Simt && max_chunks(d) * d.C * d.H <= INT32_MAX;
+}
+
 struct VarlenWorkspace {
-    size_t cu, pad[11], inner, inner_bytes, total;
+    size_t cu, co, cs, pad[11], inner, inner_bytes, total;
+    int64_t rows;   // rows of every working tensor
 };
 
-VarlenWorkspace plan_varlen(const gdr::Dims& d, bool backward, size_t inner_bytes) {
+VarlenWorkspace plan_varlen(const gdr::Dims& d, bool backward, bool chunked, size_t inner_bytes) {
     VarlenWorkspace ws{};
     int64_t rb[11];
     varlen_rows(d, backward, rb);
+    ws.rows = chunked ? max_chunks(d) * d.C : (int64_t)d.B * d.T;
     size_t off = 0;
     ws.cu = off;
     off = round_up(off + (size_t)(d.B + 1) * sizeof(int32_t), 256);
+    ws.co = ws.cs = off;
+    if (chunked) {
+        off = round_up(off + (size_t)(d.B + 1) * sizeof(int32_t), 256);
+        ws.cs = off;
+        off = round_up(off + (size_t)max_chunks(d) * sizeof(int32_t), 256);
+    }
     for (int i = 0; i < kVarlenAll[backward]; ++i) {
         ws.pad[i] = off;
-        off = round_up(off + (size_t)d.B * d.T * rb[i], 256);
+        off = round_up(off + (size_t)ws.rows * rb[i], 256);
     }
     ws.inner = off;
     ws.inner_bytes = inner_bytes;
@@ -805,9 +832,13 @@ gdr_status check_cu(const int32_t* cu, int64_t n, int64_t total, int64_t T) {
     return GDR_OK;
 }
 
-gdr_status varlen_inner_bytes(const gdr_problem* p, const gdr::Dims& d, bool backward, size_t* bytes) {
+// workspace of the inner call(s): the padded problem's, and for a chunk-packed forward also the
+// largest chunk-packed problem's
+gdr_status varlen_inner_bytes(const gdr_problem* p, const gdr::Dims& d, bool backward, size_t* bytes,
+                              bool* chunked) {
     gdr_status st;
     int S = 1;
+    *chunked = false;
     if (backward) {
         BwdPath path;
         if ((st = pick_backward(p, d, &path)) != GDR_OK) return st;
@@ -818,6 +849,11 @@ gdr_status varlen_inner_bytes(const gdr_problem* p, const gdr::Dims& d, bool bac
         if ((st = pick_forward(p, d, &path)) != GDR_OK) return st;
         if ((st = resolve_segments(p, d, path != Path::Simt, &S)) != GDR_OK) return st;
         *bytes = plan_staged(d, path == Path::Fused, S).total;
+        if (forward_chunk_packed(d, path)) {
+            *chunked = true;
+            const size_t c = plan_staged(chunk_packed(d, max_chunks(d)), path == Path::Fused, 1).total;
+            if (c > *bytes) *bytes = c;
+        }
     }
     return GDR_OK;
 }
@@ -832,8 +868,9 @@ gdr_status varlen_setup(const gdr_problem* p, gdr::Dims* d, bool backward, const
     if ((st = check_cu(cu_host, p->B, total, p->T)) != GDR_OK) return st;
     if (cu_dev && (reinterpret_cast<uintptr_t>(cu_dev) & 3u) != 0) return GDR_ERR_ALIGN;
     size_t inner = 0;
-    if ((st = varlen_inner_bytes(p, *d, backward, &inner)) != GDR_OK) return st;
-    *ws = plan_varlen(*d, backward, inner);
+    bool chunked = false;
+    if ((st = varlen_inner_bytes(p, *d, backward, &inner, &chunked)) != GDR_OK) return st;
+    *ws = plan_varlen(*d, backward, chunked, inner);
     if (!workspace || workspace_bytes < ws->total) return GDR_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GDR_ERR_ALIGN;
     if (cu_dev) {
@@ -848,23 +885,21 @@ gdr_status varlen_setup(const gdr_problem* p, gdr::Dims* d, bool backward, const
     return GDR_OK;
 }
 
+size_t varlen_workspace_bytes(const gdr_problem* p, bool backward) {
+    gdr::Dims d;
+    size_t inner = 0;
+    bool chunked = false;
+    if (check_problem(p, &d) != GDR_OK || varlen_inner_bytes(p, d, backward, &inner, &chunked) != GDR_OK) return 0;
+    return plan_varlen(d, backward, chunked, inner).total;
+}
+
 }  // namespace
 
 extern "C" {
 
-size_t gdr_varlen_forward_workspace_bytes(const gdr_problem* p) {
-    gdr::Dims d;
-    size_t inner = 0;
-    if (check_problem(p, &d) != GDR_OK || varlen_inner_bytes(p, d, false, &inner) != GDR_OK) return 0;
-    return plan_varlen(d, false, inner).total;
-}
+size_t gdr_varlen_forward_workspace_bytes(const gdr_problem* p) { return varlen_workspace_bytes(p, false); }
 
-size_t gdr_varlen_backward_workspace_bytes(const gdr_problem* p) {
-    gdr::Dims d;
-    size_t inner = 0;
-    if (check_problem(p, &d) != GDR_OK || varlen_inner_bytes(p, d, true, &inner) != GDR_OK) return 0;
-    return plan_varlen(d, true, inner).total;
-}
+size_t gdr_varlen_backward_workspace_bytes(const gdr_problem* p) { return varlen_workspace_bytes(p, true); }
 
 gdr_status gdr_varlen_forward(const gdr_problem* p, const int32_t* cu_seqlens, const int32_t* cu_seqlens_device,
                               int64_t total, const void* q, const void* k, const void* v, const float* g,
@@ -881,21 +916,57 @@ gdr_status gdr_varlen_forward(const gdr_problem* p, const int32_t* cu_seqlens, c
     if ((st = varlen_setup(p, &d, false, cu_seqlens, cu_seqlens_device, total, workspace, workspace_bytes, s, &ws,
                            &cu)) != GDR_OK)
         return st;
+    Path path;
+    if ((st = pick_forward(p, d, &path)) != GDR_OK) return st;
     char* base = static_cast<char*>(workspace);
     int64_t rb[11];
     varlen_rows(d, false, rb);
     const void* packed[5] = {q, k, v, g, beta};
     gdr::RowCopy in[5];
     for (int i = 0; i < 5; ++i) in[i] = {packed[i], base + ws.pad[i], rb[i]};
-    if ((st = from_cuda(gdr::varlen_pack(in, 5, cu, d.B, total, d.T, s))) != GDR_OK) return st;
+    const gdr::RowCopy out[1] = {{base + ws.pad[5], o, rb[5]}};
+    int64_t chunks = 0;   // the chunk-packed row's chunks, from the host lengths
+    for (int64_t i = 0; i < d.B; ++i) chunks += ((int64_t)cu_seqlens[i + 1] - cu_seqlens[i] + d.C - 1) / d.C;
+    if (forward_chunk_packed(d, path) && chunks > 0) {
+        int* co = reinterpret_cast<int*>(base + ws.co);
+        int* cs = reinterpret_cast<int*>(base + ws.cs);
+        const gdr::VarlenMap m{cu, co, cs, d.B, total, 0, d.C, chunks * d.C};
+        const gdr::Dims d1 = chunk_packed(d, chunks);
+        const StagedWorkspace iw = plan_staged(d1, path == Path::Fused, 1);
+        char* ib = base + ws.inner;
+        float* g_cum = reinterpret_cast<float*>(ib + iw.g_cum);
+        void *w = ib + iw.w, *u = ib + iw.u, *v_new = ib + iw.v_new, *h_ckpt = ib + iw.h_ckpt;
+        void* P = (path == Path::Fused && d.C == 64) ? ib + iw.P : nullptr;
+        void* pad[6];
+        for (int i = 0; i < 6; ++i) pad[i] = base + ws.pad[i];
+        unsigned int* err = device_error_word();
+        if ((st = from_cuda(gdr::varlen_plan(cu, d.B, total, d.C, (int)chunks, co, cs, s))) != GDR_OK) return st;
+        if ((st = from_cuda(gdr::varlen_pack(in, 5, m, s))) != GDR_OK) return st;
+        if ((st = from_cuda(gdr::mma_prepare(d1, pad[1], pad[2], reinterpret_cast<const float*>(pad[3]), pad[4], w, u,
+                                             g_cum, s, err, pad[0], P))) != GDR_OK)
+            return st;
+        if (path == Path::Fused) {
+            if ((st = from_cuda(gdr::mma_scan_output(d1, pad[0], pad[1], w, u, g_cum, P, h0, pad[5], h_final, s, err,
+                                                     co, d.B))) != GDR_OK)
+                return st;
+        } else {
+            if ((st = from_cuda(gdr::mma_scan(d1, pad[1], w, u, g_cum, h0, h_ckpt, v_new, h_final, s, err, co,
+                                              d.B))) != GDR_OK)
+                return st;
+            if ((st = from_cuda(gdr::tc_output(d1, pad[0], pad[1], v_new, h_ckpt, g_cum, pad[5], s, err))) != GDR_OK)
+                return st;
+        }
+        if ((st = from_cuda(gdr::varlen_unpack(out, 1, m, s))) != GDR_OK) return st;
+        t_last_variant = path_name(path);
+        return GDR_OK;
+    }
+    const gdr::VarlenMap m{cu, nullptr, nullptr, d.B, total, d.T, d.C, (int64_t)d.B * d.T};
+    if ((st = from_cuda(gdr::varlen_pack(in, 5, m, s))) != GDR_OK) return st;
     if ((st = gdr_forward(p, base + ws.pad[0], base + ws.pad[1], base + ws.pad[2],
                           reinterpret_cast<const float*>(base + ws.pad[3]), base + ws.pad[4], h0, base + ws.pad[5],
                           h_final, base + ws.inner, ws.inner_bytes, stream)) != GDR_OK)
         return st;
-    if (total > 0) {
-        const gdr::RowCopy out[1] = {{base + ws.pad[5], o, rb[5]}};
-        if ((st = from_cuda(gdr::varlen_unpack(out, 1, cu, d.B, total, d.T, s))) != GDR_OK) return st;
-    }
+    if (total > 0 && (st = from_cuda(gdr::varlen_unpack(out, 1, m, s))) != GDR_OK) return st;
     return GDR_OK;
 }
 
@@ -921,10 +992,11 @@ gdr_status gdr_varlen_backward(const gdr_problem* p, const int32_t* cu_seqlens, 
     char* base = static_cast<char*>(workspace);
     int64_t rb[11];
     varlen_rows(d, true, rb);
+    const gdr::VarlenMap m{cu, nullptr, nullptr, d.B, total, d.T, d.C, (int64_t)d.B * d.T};
     const void* packed_in[6] = {q, k, v, g, beta, d_o};
     gdr::RowCopy in[6];
     for (int i = 0; i < 6; ++i) in[i] = {packed_in[i], base + ws.pad[i], rb[i]};
-    if ((st = from_cuda(gdr::varlen_pack(in, 6, cu, d.B, total, d.T, s))) != GDR_OK) return st;
+    if ((st = from_cuda(gdr::varlen_pack(in, 6, m, s))) != GDR_OK) return st;
     auto pad = [&](int i) { return static_cast<void*>(base + ws.pad[i]); };
     if ((st = gdr_backward(p, pad(0), pad(1), pad(2), static_cast<const float*>(pad(3)), pad(4), h0, pad(5), dh_final,
                            pad(6), pad(7), pad(8), static_cast<float*>(pad(9)), pad(10), dh0, base + ws.inner,
@@ -934,7 +1006,7 @@ gdr_status gdr_varlen_backward(const gdr_problem* p, const int32_t* cu_seqlens, 
         void* packed_out[5] = {dq, dk, dv, dg, dbeta};
         gdr::RowCopy out[5];
         for (int i = 0; i < 5; ++i) out[i] = {pad(6 + i), packed_out[i], rb[6 + i]};
-        if ((st = from_cuda(gdr::varlen_unpack(out, 5, cu, d.B, total, d.T, s))) != GDR_OK) return st;
+        if ((st = from_cuda(gdr::varlen_unpack(out, 5, m, s))) != GDR_OK) return st;
     }
     return GDR_OK;
 }

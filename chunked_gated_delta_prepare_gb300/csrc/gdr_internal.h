@@ -34,8 +34,11 @@ cudaError_t mma_prepare(const Dims& d, const void* k, const void* v, const float
                         void* u, float* g_cum, cudaStream_t s, unsigned int* err, const void* q = nullptr,
                         void* P = nullptr, void* tinv = nullptr);
 // the scan's recurrence runs on mma.sync (register-resident), see scan_mma.cu
+// co (packed variable-length sequences, else NULL): d has B = 1 and whole chunks; sequence z of nseq runs
+// the chunks co[z] .. co[z+1]-1 from h0[z] to h_final[z] (one CTA column per sequence)
 cudaError_t mma_scan(const Dims& d, const void* k, const void* w, const void* u, const float* g_cum, const float* h0,
-                     void* h_ckpt, void* v_new, float* h_final, cudaStream_t s, unsigned int* err);
+                     void* h_ckpt, void* v_new, float* h_final, cudaStream_t s, unsigned int* err,
+                     const int* co = nullptr, int nseq = 0);
 // the segment-parallel scan: on the segment view (B S sequences of T / S tokens), every segment's affine
 // map h_end = M h_start + Z (M [B S, H, K, K], Z [B S, H, K, V], fp32), then the serial stitch of the maps
 // into the segments' starting states h_start [B S, H, K, V] and h_final [B, H, K, V] (NULL: not written).
@@ -52,7 +55,7 @@ cudaError_t tc_output(const Dims& d, const void* q, const void* k, const void* v
 // P: the prepare's [B, NT, H, C, C] tiles (C = 64), or NULL to compute q k^T in the kernel
 cudaError_t mma_scan_output(const Dims& d, const void* q, const void* k, const void* w, const void* u,
                             const float* g_cum, const void* P, const float* h0, void* o, float* h_final,
-                            cudaStream_t s, unsigned int* err);
+                            cudaStream_t s, unsigned int* err, const int* co = nullptr, int nseq = 0);
 
 // ---- backward stages on the CUDA cores (simt_backward.cu): every shape and io dtype;
 // intermediates fp32, see include/gdr.h for each stage's definition
@@ -110,17 +113,33 @@ cudaError_t mma_bwd_chunk_kda(const Dims& d, const void* q, const void* k, const
                               void* dk, void* dv, void* dbeta, float* dg, int* exact_flags, cudaStream_t s);
 
 // ---- packed variable-length sequences (varlen.cu)
-// One tensor of token rows: packed [total, row] <-> padded [n, T, row], row_bytes bytes a token.
+// One tensor of token rows, row_bytes bytes a token: packed [total, row] <-> a working layout, either
+//   padded:       [n, T, row], sequence s on the rows s T .. s T + len_s - 1 (co == NULL), or
+//   chunk-packed: [NT C, row], sequence s on the rows C co[s] .. C co[s] + len_s - 1 (co, cs given);
+// rows of the working layout past a sequence's length are zero after a pack and not read by an unpack.
 struct RowCopy {
     const void* src;
     void* dst;
     int64_t row_bytes;
 };
 constexpr int kMaxCopies = 8;
-// pack: copies[i].src packed, .dst padded (rows past a sequence's length zeroed); unpack: .src padded,
-// .dst packed (rows past a sequence's length not read).  cu: device int32 [n + 1]; the grid is capped at 8 CTAs per SM.
-cudaError_t varlen_pack(const RowCopy* copies, int count, const int* cu, int n, int64_t total, int T, cudaStream_t s);
-cudaError_t varlen_unpack(const RowCopy* copies, int count, const int* cu, int n, int64_t total, int T, cudaStream_t s);
+struct VarlenMap {
+    const int* cu;     // device int32 [n + 1]
+    const int* co;     // chunk-packed: device int32 [n + 1] chunk offsets; NULL: padded
+    const int* cs;     // chunk-packed: device int32 [NT], the sequence owning each chunk
+    int n;
+    int64_t total;     // packed rows
+    int T;             // padded: tokens per row
+    int C;             // chunk-packed: tokens per chunk
+    int64_t rows;      // rows of the working layout: n T, or NT C
+};
+// pack: copies[i].src packed, .dst working layout; unpack: .src working layout, .dst packed.  The grid is
+// capped at 8 CTAs per SM.
+cudaError_t varlen_pack(const RowCopy* copies, int count, const VarlenMap& m, cudaStream_t s);
+cudaError_t varlen_unpack(const RowCopy* copies, int count, const VarlenMap& m, cudaStream_t s);
+// co[s] = sum over r < s of ceil(len_r / C), clamped to NT (co[n] too), and cs[c] = s for c in
+// [co[s], co[s+1]): the chunk-packed layout of the sequences in cu.  One CTA.
+cudaError_t varlen_plan(const int* cu, int n, int64_t total, int C, int NT, int* co, int* cs, cudaStream_t s);
 
 // ---- device error word (device_status.cu)
 // Bounded waits in kernels write a nonzero code here instead of trapping.

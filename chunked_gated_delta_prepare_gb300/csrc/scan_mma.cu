@@ -84,13 +84,16 @@ struct MScanLayout {
 // V/32 run u's columns from a zero state (their final state is Z, written to h_final), the others
 // run the columns of the identity with u = 0 (their final state is M, written to m_out [.., K, K]).
 // No checkpoint and no v' is written.
+// co (packed variable-length sequences; NULL otherwise): the tensors hold one row (B = 1) of whole-chunk
+// runs, sequence z on the chunks co[z] .. co[z+1]-1; blockIdx.z is the sequence, whose state starts from
+// h0[z] and ends in h_final[z].  Checkpoints and v' land at the chunks' places in the row.
 template <int K, int C, bool PER_K, bool GENERAL, bool TRANSFER>
 __global__ void __launch_bounds__(MScanLayout<K, C, PER_K, TRANSFER>::kThreads, TRANSFER && !PER_K ? 2 : 1)
 scan_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap mk,
                 const __grid_constant__ CUtensorMap mu, const bf16* __restrict__ k, const float* __restrict__ g_cum,
                 const float* __restrict__ h0, bf16* __restrict__ h_ckpt, bf16* __restrict__ v_new,
-                float* __restrict__ h_final, float* __restrict__ m_out, int T, int H, int V, int G,
-                unsigned int* err) {
+                float* __restrict__ h_final, float* __restrict__ m_out, const int* __restrict__ co, int T, int H,
+                int V, int G, unsigned int* err) {
     using L = MScanLayout<K, C, PER_K, TRANSFER>;
     constexpr int GW = L::GW, KH = L::KH, NT8 = L::NT8;
     constexpr int NJH = KH / 8;    // n-tiles of this warp's part of h^T
@@ -102,12 +105,16 @@ scan_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ 
     const bool mcols = TRANSFER && (int)blockIdx.x >= V / kBV;   // a slice of the identity's columns
     const int v0 = (mcols ? (int)blockIdx.x - V / kBV : (int)blockIdx.x) * kBV, h = blockIdx.y, b = blockIdx.z;
     const uint32_t tx = mcols ? L::tx - L::kU : L::tx;           // u = 0 there: no u tile
-    const int NT = GENERAL ? (T + C - 1) / C : T / C;   // a last, partial chunk runs as zero tokens past T
+    const int NTall = GENERAL ? (T + C - 1) / C : T / C;   // a last, partial chunk runs as zero tokens past T
+    // this CTA's chunks: c0 .. c0 + NT - 1 of data row bd (clamped, so any co stays inside the tensors)
+    const int c0 = co ? min(max(co[b], 0), NTall) : 0;
+    const int NT = co ? min(max(co[b + 1], c0), NTall) - c0 : NTall;
+    const int bd = co ? 0 : b;
     const uint32_t s_base = bw::smem_u32(sm);
-    auto row = [&](int t) -> int64_t { return ((int64_t)b * T + t) * H + h; };
+    auto row = [&](int t) -> int64_t { return ((int64_t)bd * T + t) * H + h; };
     auto rowc = [&](int t) -> int64_t { return row(GENERAL ? min(t, T - 1) : t); };   // G past T: its last value
     auto krow = [&](int t) -> int64_t {                                                 // k: q/k head h / G
-        return GENERAL ? ((int64_t)b * T + t) * (H / G) + h / G : row(t);
+        return GENERAL ? ((int64_t)bd * T + t) * (H / G) + h / G : row(t);
     };
     const int hk = GENERAL ? h / G : h;
 
@@ -131,8 +138,8 @@ scan_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ 
             float gn[GPL], gln;                        // next chunk's G, loaded a chunk ahead
             auto load_g = [&](int c) {
 #pragma unroll
-                for (int i = 0; i < GPL; ++i) gn[i] = g_cum[rowc(c * C + lane + 32 * i)];
-                gln = g_cum[rowc(c * C + C - 1)];
+                for (int i = 0; i < GPL; ++i) gn[i] = g_cum[rowc((c0 + c) * C + lane + 32 * i)];
+                gln = g_cum[rowc((c0 + c) * C + C - 1)];
             };
             if (NT > 0) load_g(0);
             for (int c = 0; c < NT; ++c) {
@@ -142,15 +149,15 @@ scan_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ 
                 for (int i = 0; i < GPL; ++i) gc[i] = gn[i];
                 if (c + 1 < NT) load_g(c + 1);
                 if (!bw::mbar_wait(&empty[s], ((c / L::NS) & 1) ^ 1, err, kDeviceErrTimeout)) break;
-                const int t0 = c * C;
+                const int t0 = (c0 + c) * C;
                 if (lane == 0) {
                     bw::mbar_arrive_expect_tx(&full[s], tx);
 #pragma unroll
                     for (int a = 0; a < K / 64; ++a) {
-                        bw::tma_load_4d(sm + L::W + s * L::kKC + a * C * 128, &mw, &full[s], a * 64, h, t0, b);
-                        bw::tma_load_4d(sm + L::KB + s * L::kKC + a * C * 128, &mk, &full[s], a * 64, hk, t0, b);
+                        bw::tma_load_4d(sm + L::W + s * L::kKC + a * C * 128, &mw, &full[s], a * 64, h, t0, bd);
+                        bw::tma_load_4d(sm + L::KB + s * L::kKC + a * C * 128, &mk, &full[s], a * 64, hk, t0, bd);
                     }
-                    if (!mcols) bw::tma_load_4d(sm + L::U + s * L::kU, &mu, &full[s], v0, h, t0, b);
+                    if (!mcols) bw::tma_load_4d(sm + L::U + s * L::kU, &mu, &full[s], v0, h, t0, bd);
                     sDec[s] = __expf(glc);
                 }
 #pragma unroll
@@ -170,7 +177,7 @@ scan_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ 
             };
             Staged sa, sb;
             auto load_chunk = [&](int c, Staged& st) {
-                const int t0 = c * C;
+                const int t0 = (c0 + c) * C;
 #pragma unroll
                 for (int j = 0; j < NI; ++j) {
                     const int t = r0 + j * RSTEP;
@@ -187,13 +194,13 @@ scan_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ 
             auto produce = [&](int c, const Staged& st) -> bool {
                 const int s = c % L::NS;
                 if (!bw::mbar_wait(&empty[s], ((c / L::NS) & 1) ^ 1, err, kDeviceErrTimeout)) return false;
-                const int t0 = c * C;
+                const int t0 = (c0 + c) * C;
                 if (pt == 0) {
                     bw::mbar_arrive_expect_tx(&full[s], tx);
 #pragma unroll
                     for (int a = 0; a < K / 64; ++a)
-                        bw::tma_load_4d(sm + L::W + s * L::kKC + a * C * 128, &mw, &full[s], a * 64, h, t0, b);
-                    if (!mcols) bw::tma_load_4d(sm + L::U + s * L::kU, &mu, &full[s], v0, h, t0, b);
+                        bw::tma_load_4d(sm + L::W + s * L::kKC + a * C * 128, &mw, &full[s], a * 64, h, t0, bd);
+                    if (!mcols) bw::tma_load_4d(sm + L::U + s * L::kU, &mu, &full[s], v0, h, t0, bd);
                 }
                 if (r0 == 0) {
 #pragma unroll
@@ -266,7 +273,7 @@ scan_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ 
     bool ready = NT > 0 && bw::mbar_test_wait(&full[0], 0);
     for (int c = 0; c < NT; ++c) {
         const int s = c % L::NS;
-        const int t0 = c * C;
+        const int t0 = (c0 + c) * C;
         if (!ready) ok = ok && bw::mbar_wait(&full[s], (c / L::NS) & 1, err, kDeviceErrTimeout);
         const uint32_t w_t = s_base + L::W + s * L::kKC;
         const uint32_t k_t = s_base + L::KB + s * L::kKC;
@@ -300,7 +307,7 @@ scan_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ 
                 wm::stsm_x4_t(st_h + stage_off(8 * j + 8 * (mi >> 1) + mr, mi & 1), r);
             }
             __syncwarp();
-            bf16* dst = h_ckpt + ((((int64_t)b * NT + c) * H + h) * K + d0) * V + v0 + vr0;
+            bf16* dst = h_ckpt + ((((int64_t)bd * NTall + c0 + c) * H + h) * K + d0) * V + v0 + vr0;
 #pragma unroll
             for (int i = 0; i < KH / 16; ++i) {
                 const int r = 16 * i + (lane >> 1), half = lane & 1;
@@ -398,7 +405,7 @@ scan_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ 
                 wm::stsm_x4_t(st_v + stage_off(8 * jq + 8 * (mi >> 1) + mr, mi & 1), r);
             }
             __syncwarp();
-            bf16* dst = v_new + (((int64_t)b * T + t0 + kh * (C / 2)) * H + h) * V + v0 + vr0;
+            bf16* dst = v_new + (((int64_t)bd * T + t0 + kh * (C / 2)) * H + h) * V + v0 + vr0;
 #pragma unroll
             for (int i = 0; i < C / 32; ++i) {
                 const int r = 16 * i + (lane >> 1), half = lane & 1;
@@ -427,7 +434,8 @@ scan_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ 
 
 template <int K, int C, bool PER_K, bool GENERAL, bool TRANSFER>
 cudaError_t launch_v(const Dims& d, const void* k, const void* w, const void* u, const float* g_cum, const float* h0,
-                     void* h_ckpt, void* v_new, float* h_final, float* m_out, cudaStream_t s, unsigned int* err) {
+                     void* h_ckpt, void* v_new, float* h_final, float* m_out, const int* co, int nseq, cudaStream_t s,
+                     unsigned int* err) {
     using L = MScanLayout<K, C, PER_K, TRANSFER>;
     CUtensorMap mw, mk, mu;
     if (!make_tmap_tokens(&mw, w, d.B, d.T, d.H, K, C) || !make_tmap_tokens(&mk, k, d.B, d.T, d.Hk, K, C) ||
@@ -437,24 +445,28 @@ cudaError_t launch_v(const Dims& d, const void* k, const void* w, const void* u,
     const size_t smem = L::bytes + 1024;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const dim3 grid(d.V / kBV + (TRANSFER ? K / kBV : 0), d.H, d.B);
+    const dim3 grid(d.V / kBV + (TRANSFER ? K / kBV : 0), d.H, co ? nseq : d.B);
     kern<<<grid, L::kThreads, smem, s>>>(mw, mk, mu, (const bf16*)k, g_cum, h0, (bf16*)h_ckpt, (bf16*)v_new,
-                                         h_final, m_out, d.T, d.H, d.V, d.G, err);
+                                         h_final, m_out, co, d.T, d.H, d.V, d.G, err);
     return cudaGetLastError();
 }
 
 template <int K, int C, bool PER_K, bool TRANSFER>
 cudaError_t launch(const Dims& d, const void* k, const void* w, const void* u, const float* g_cum, const float* h0,
-                   void* h_ckpt, void* v_new, float* h_final, float* m_out, cudaStream_t s, unsigned int* err) {
+                   void* h_ckpt, void* v_new, float* h_final, float* m_out, const int* co, int nseq, cudaStream_t s,
+                   unsigned int* err) {
     if (d.T % C != 0 || d.G != 1)
-        return launch_v<K, C, PER_K, true, TRANSFER>(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, m_out, s, err);
-    return launch_v<K, C, PER_K, false, TRANSFER>(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, m_out, s, err);
+        return launch_v<K, C, PER_K, true, TRANSFER>(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, m_out, co, nseq,
+                                                     s, err);
+    return launch_v<K, C, PER_K, false, TRANSFER>(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, m_out, co, nseq, s,
+                                                  err);
 }
 
 template <bool TRANSFER>
 cudaError_t dispatch(const Dims& d, const void* k, const void* w, const void* u, const float* g_cum, const float* h0,
-                     void* h_ckpt, void* v_new, float* h_final, float* m_out, cudaStream_t s, unsigned int* err) {
-#define GDR_SCAN_ARGS d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, m_out, s, err
+                     void* h_ckpt, void* v_new, float* h_final, float* m_out, const int* co, int nseq, cudaStream_t s,
+                     unsigned int* err) {
+#define GDR_SCAN_ARGS d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, m_out, co, nseq, s, err
     if (d.K == 64) {
         if (d.C == 32)
             return d.per_k ? launch<64, 32, true, TRANSFER>(GDR_SCAN_ARGS) : launch<64, 32, false, TRANSFER>(GDR_SCAN_ARGS);
@@ -469,15 +481,16 @@ cudaError_t dispatch(const Dims& d, const void* k, const void* w, const void* u,
 }  // namespace
 
 cudaError_t mma_scan(const Dims& d, const void* k, const void* w, const void* u, const float* g_cum, const float* h0,
-                     void* h_ckpt, void* v_new, float* h_final, cudaStream_t s, unsigned int* err) {
-    if (!d.bf16) return cudaErrorInvalidValue;
-    return dispatch<false>(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, nullptr, s, err);
+                     void* h_ckpt, void* v_new, float* h_final, cudaStream_t s, unsigned int* err, const int* co,
+                     int nseq) {
+    if (!d.bf16 || (co && (d.B != 1 || nseq < 1))) return cudaErrorInvalidValue;
+    return dispatch<false>(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, nullptr, co, nseq, s, err);
 }
 
 cudaError_t mma_scan_transfer(const Dims& d, const void* k, const void* w, const void* u, const float* g_cum,
                               float* m_out, float* z_out, cudaStream_t s, unsigned int* err) {
     if (!d.bf16 || !m_out || !z_out) return cudaErrorInvalidValue;
-    return dispatch<true>(d, k, w, u, g_cum, nullptr, nullptr, nullptr, z_out, m_out, s, err);
+    return dispatch<true>(d, k, w, u, g_cum, nullptr, nullptr, nullptr, z_out, m_out, nullptr, 0, s, err);
 }
 
 }  // namespace gdr

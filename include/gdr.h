@@ -454,11 +454,15 @@ GDR_API gdr_status gdr_backward(const gdr_problem* p, const void* q, const void*
  * [total,H,K] io; v [total,HV,V] io; g [total,HV] or [total,HV,K] fp32; beta
  * [total,HV] io; o like v.  Per-sequence tensors keep the batched layouts:
  * h0, h_final, dh_final, dh0 [n,HV,K,V] fp32 (sequence s starts from h0[s]).
- * The call moves sequence s into row s of padded copies in the workspace,
- * filling the row's tail with zero tokens (beta = 0, g = 0, q = k = v = 0: the
- * state passes unchanged and their outputs are dropped), runs gdr_forward /
- * gdr_backward on p, and moves the first len_s rows of each padded result back.
- * Zero tokens cost the same as real ones: the padded work is n * p->T tokens.
+ * The call copies the sequences into a working layout in the workspace, fills
+ * the rest with zero tokens (beta = 0, g = 0, q = k = v = 0: the state passes
+ * unchanged and their outputs are dropped), computes, and copies each
+ * sequence's results back.  The forward on the tensor cores (bf16 io) packs the
+ * sequences as runs of whole chunks of one row, sequence s taking ceil(len_s / C)
+ * chunks, and scans each run from h0[s]: the work is the real tokens plus fewer
+ * than C per sequence.  The CUDA-core forward and the backward use padded rows,
+ * sequence s as row s of p, and run gdr_forward / gdr_backward on p: the work
+ * is n * p->T tokens.
  * workspace: at least gdr_varlen_*_workspace_bytes(p), 256-byte aligned, owned by the caller.
  */
 GDR_API size_t gdr_varlen_forward_workspace_bytes(const gdr_problem* p);

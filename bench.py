@@ -430,8 +430,42 @@ def time_varlen(args, wl, dev, flush, stream, world):
     if gdr.gdr_get_device_status() != 0:
         raise RuntimeError("device status set after the packed forward's timed region")
     total_s = max_over_ranks(sum(a.elapsed_time(b) for a, b in evs) / 1e3, world)
+
+    # the backward of the same packed batch: gdr_varlen_backward, one call per step
+    gen = torch.Generator().manual_seed(7)
+    d_o = torch.randn(v.shape, generator=gen).to(v.dtype).to(dev)
+    dhf = torch.randn(hf.shape, generator=gen).to(dev)
+    grads = [torch.empty_like(t) for t in (q, k, v, g, beta)]
+    dh0 = torch.empty_like(hf)
+    bbytes = gdr.gdr_varlen_backward_workspace_bytes(p)
+    bws = torch.empty(bbytes, device=dev, dtype=torch.uint8)
+
+    def bcall():
+        gdr.gdr_varlen_backward(p, x.cu, cu_dev, total, q, k, v, g, beta, h0, d_o, dhf, *grads, dh0, bws, bbytes)
+
+    bcall()
+    bvariant = gdr.gdr_last_variant()
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        bcall()
+    torch.cuda.synchronize()
+    bevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for s in range(steps):
+        flush.fill_(s & 0xFF)
+        bevs[s][0].record(stream)
+        bcall()
+        bevs[s][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    if gdr.gdr_get_device_status() != 0:
+        raise RuntimeError("device status set after the packed backward's timed region")
+    bwd_s = max_over_ranks(sum(a.elapsed_time(b) for a, b in bevs) / 1e3, world)
     return {"ms_per_step": 1e3 * total_s / steps, "steps": steps,
             "value": weak_scaling_throughput(world, total, steps, total_s), "unit": "tokens/s",
+            "backward": {"ms_per_step": 1e3 * bwd_s / steps, "variant": bvariant,
+                         "value": weak_scaling_throughput(world, total, steps, bwd_s), "unit": "tokens/s"},
             "sequences": len(lengths), "lengths": lengths, "layout": layout, "working_tokens": working,
             "variant": variant, "segments": S,
             "gpu_launches": launches * steps}

@@ -85,6 +85,8 @@ struct RScanLayout {
     static_assert(!FROM_P || (C == 64 && !PER_K), "P tiles: scalar gate, 64 x 64");
 };
 
+// co (packed variable-length sequences; NULL otherwise): one data row (B = 1) of whole-chunk runs,
+// sequence z = blockIdx.z on the chunks co[z] .. co[z+1]-1, from dh_final[z] back to dh0[z].
 template <int K, int C, bool PER_K, bool FROM_P>
 __global__ void __launch_bounds__(RScanLayout<K, C, PER_K, FROM_P>::kThreads, 1)
 bwd_scan_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mw,
@@ -92,7 +94,8 @@ bwd_scan_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constan
                     const __grid_constant__ CUtensorMap mp, const __grid_constant__ CUtensorMap mdl,
                     const bf16* __restrict__ k_raw, const bf16* __restrict__ q_raw, const float* __restrict__ g_cum,
                     const float* __restrict__ dh_final, bf16* __restrict__ dh_ckpt, bf16* __restrict__ dv_new,
-                    float* __restrict__ dh0, int T, int H, int V, int G, float scale, unsigned int* err) {
+                    float* __restrict__ dh0, const int* __restrict__ co, int T, int H, int V, int G, float scale,
+                    unsigned int* err) {
     using L = RScanLayout<K, C, PER_K, FROM_P>;
     constexpr int KH = L::KH, NT8 = L::NT8;
     constexpr int NJH = KH / 8;
@@ -102,9 +105,13 @@ bwd_scan_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constan
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int v0 = blockIdx.x * kBV, h = blockIdx.y, b = blockIdx.z;
-    const int NT = (T + C - 1) / C;
+    const int NTall = (T + C - 1) / C;
+    // this CTA's chunks: c0 .. c0 + NT - 1 of data row bd (clamped, so any co stays inside the tensors)
+    const int c0 = co ? min(max(co[b], 0), NTall) : 0;
+    const int NT = co ? min(max(co[b + 1], c0), NTall) - c0 : NTall;
+    const int bd = co ? 0 : b;
     const uint32_t s_base = bw::smem_u32(sm);
-    auto rowc = [&](int t) -> int64_t { return ((int64_t)b * T + min(t, T - 1)) * H + h; };   // G past T: its last value
+    auto rowc = [&](int t) -> int64_t { return ((int64_t)bd * T + min(t, T - 1)) * H + h; };   // G past T: its last value
 
     if (tid == 0) {
         for (int s = 0; s < L::NS; ++s) {
@@ -123,7 +130,7 @@ bwd_scan_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constan
             float* sGam = reinterpret_cast<float*>(sm + L::GAM);
             float* sEG = reinterpret_cast<float*>(sm + L::EG);
             for (int i = 0; i < NT; ++i) {
-                const int c = NT - 1 - i, s = i % L::NS, t0 = c * C;
+                const int c = NT - 1 - i, s = i % L::NS, t0 = (c0 + c) * C;
                 float gv[GPL];
 #pragma unroll
                 for (int ii = 0; ii < GPL; ++ii) gv[ii] = g_cum[rowc(t0 + 32 * ii + lane)];
@@ -133,13 +140,13 @@ bwd_scan_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constan
                     bw::mbar_arrive_expect_tx(&full[s], L::tx);
 #pragma unroll
                     for (int a = 0; a < K / 64; ++a) {
-                        bw::tma_load_4d(sm + L::KB + s * L::kKC + a * C * 128, &mk, &full[s], a * 64, h / G, t0, b);
-                        bw::tma_load_4d(sm + L::WB + s * L::kKC + a * C * 128, &mw, &full[s], a * 64, h, t0, b);
-                        bw::tma_load_4d(sm + L::QB + s * L::kKC + a * C * 128, &mq, &full[s], a * 64, h / G, t0, b);
+                        bw::tma_load_4d(sm + L::KB + s * L::kKC + a * C * 128, &mk, &full[s], a * 64, h / G, t0, bd);
+                        bw::tma_load_4d(sm + L::WB + s * L::kKC + a * C * 128, &mw, &full[s], a * 64, h, t0, bd);
+                        bw::tma_load_4d(sm + L::QB + s * L::kKC + a * C * 128, &mq, &full[s], a * 64, h / G, t0, bd);
                     }
-                    bw::tma_load_4d(sm + L::DB + s * L::kD, &mdo, &full[s], v0, h, t0, b);
-                    if constexpr (FROM_P) bw::tma_load_4d(sm + L::PB + s * L::kP, &mp, &full[s], 0, 0, h, b * NT + c);
-                    else bw::tma_load_4d(sm + L::LB + s * L::kL, &mdl, &full[s], v0, h, t0, b);
+                    bw::tma_load_4d(sm + L::DB + s * L::kD, &mdo, &full[s], v0, h, t0, bd);
+                    if constexpr (FROM_P) bw::tma_load_4d(sm + L::PB + s * L::kP, &mp, &full[s], 0, 0, h, bd * NTall + c0 + c);
+                    else bw::tma_load_4d(sm + L::LB + s * L::kL, &mdl, &full[s], v0, h, t0, bd);
                     sDec[4 * s] = __expf(gl);
                 }
 #pragma unroll
@@ -160,11 +167,11 @@ bwd_scan_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constan
             uint4 kr[NI], qr[NI];
             float gr[NI][8], gl8[8];
             auto load = [&](int c) {
-                const int t0 = c * C;
+                const int t0 = (c0 + c) * C;
 #pragma unroll
                 for (int j = 0; j < NI; ++j) {
                     const int t = t0 + r0 + j * RSTEP;
-                    const int64_t krow = ((int64_t)b * T + t) * Hk + hk;
+                    const int64_t krow = ((int64_t)bd * T + t) * Hk + hk;
                     kr[j] = t < T ? *reinterpret_cast<const uint4*>(k_raw + krow * K + lc * 8) : make_uint4(0u, 0u, 0u, 0u);
                     qr[j] = t < T ? *reinterpret_cast<const uint4*>(q_raw + krow * K + lc * 8) : make_uint4(0u, 0u, 0u, 0u);
                     const float4* gt = reinterpret_cast<const float4*>(g_cum + rowc(t) * K + lc * 8);
@@ -180,15 +187,15 @@ bwd_scan_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constan
             };
             if (NT > 0) load(NT - 1);
             for (int i = 0; i < NT; ++i) {
-                const int c = NT - 1 - i, s = i % L::NS, t0 = c * C;
+                const int c = NT - 1 - i, s = i % L::NS, t0 = (c0 + c) * C;
                 if (!bw::mbar_wait(&empty[s], ((i / L::NS) & 1) ^ 1, err, kDeviceErrTimeout)) break;
                 if (pt == 0) {
                     bw::mbar_arrive_expect_tx(&full[s], L::tx);
 #pragma unroll
                     for (int a = 0; a < K / 64; ++a)
-                        bw::tma_load_4d(sm + L::WB + s * L::kKC + a * C * 128, &mw, &full[s], a * 64, h, t0, b);
-                    bw::tma_load_4d(sm + L::DB + s * L::kD, &mdo, &full[s], v0, h, t0, b);
-                    bw::tma_load_4d(sm + L::LB + s * L::kL, &mdl, &full[s], v0, h, t0, b);
+                        bw::tma_load_4d(sm + L::WB + s * L::kKC + a * C * 128, &mw, &full[s], a * 64, h, t0, bd);
+                    bw::tma_load_4d(sm + L::DB + s * L::kD, &mdo, &full[s], v0, h, t0, bd);
+                    bw::tma_load_4d(sm + L::LB + s * L::kL, &mdl, &full[s], v0, h, t0, bd);
                 }
                 if (r0 == 0) {
 #pragma unroll
@@ -255,7 +262,7 @@ bwd_scan_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constan
     bool ok = true;
     bool ready = NT > 0 && bw::mbar_test_wait(&full[0], 0);
     for (int i = 0; i < NT; ++i) {
-        const int c = NT - 1 - i, s = i % L::NS, t0 = c * C;
+        const int c = NT - 1 - i, s = i % L::NS, t0 = (c0 + c) * C;
         if (!ready) ok = ok && bw::mbar_wait(&full[s], (i / L::NS) & 1, err, kDeviceErrTimeout);
         const uint32_t k_t = s_base + L::KB + s * L::kKC;
         const uint32_t w_t = s_base + L::WB + s * L::kKC;
@@ -291,7 +298,7 @@ bwd_scan_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constan
         }
         __syncwarp();
         {
-            bf16* dst = dh_ckpt + ((((int64_t)b * NT + c) * H + h) * K + d0) * V + v0 + vr0;
+            bf16* dst = dh_ckpt + ((((int64_t)bd * NTall + c0 + c) * H + h) * K + d0) * V + v0 + vr0;
 #pragma unroll
             for (int r16 = 0; r16 < KH / 16; ++r16) {
                 const int r = 16 * r16 + (lane >> 1), half = lane & 1;
@@ -460,7 +467,7 @@ bwd_scan_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constan
                 wm::stsm_x4_t(st_v + stage_off(8 * jq + 8 * (mi >> 1) + mr, mi & 1), r);
             }
             __syncwarp();
-            bf16* dst = dv_new + (((int64_t)b * T + t0 + kh * (C / 2)) * H + h) * V + v0 + vr0;
+            bf16* dst = dv_new + (((int64_t)bd * T + t0 + kh * (C / 2)) * H + h) * V + v0 + vr0;
 #pragma unroll
             for (int r32 = 0; r32 < C / 32; ++r32) {
                 const int r = 16 * r32 + (lane >> 1), half = lane & 1;
@@ -488,7 +495,7 @@ bwd_scan_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constan
 template <int K, int C, bool PER_K, bool FROM_P>
 cudaError_t launch(const Dims& d, const void* q, const void* k, const void* w, const float* g_cum, const void* P,
                    const void* dv_loc, const void* d_o, const float* dh_final, void* dh_ckpt, void* dv_new,
-                   float* dh0, cudaStream_t s, unsigned int* err) {
+                   float* dh0, const int* co, int nseq, cudaStream_t s, unsigned int* err) {
     using L = RScanLayout<K, C, PER_K, FROM_P>;
     CUtensorMap mk, mw, mq, mdo, mp, mdl;
     if (!make_tmap_tokens(&mk, k, d.B, d.T, d.Hk, K, C) || !make_tmap_tokens(&mw, w, d.B, d.T, d.H, K, C) ||
@@ -508,43 +515,43 @@ cudaError_t launch(const Dims& d, const void* q, const void* k, const void* w, c
     const size_t smem = L::bytes + 1024;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const dim3 grid(d.V / kBV, d.H, d.B);
+    const dim3 grid(d.V / kBV, d.H, co ? nseq : d.B);
     kern<<<grid, L::kThreads, smem, s>>>(mk, mw, mq, mdo, mp, mdl, (const bf16*)k, (const bf16*)q, g_cum, dh_final,
-                                         (bf16*)dh_ckpt, (bf16*)dv_new, dh0, d.T, d.H, d.V, d.G, d.scale, err);
+                                         (bf16*)dh_ckpt, (bf16*)dv_new, dh0, co, d.T, d.H, d.V, d.G, d.scale, err);
     return cudaGetLastError();
 }
 
 template <int K, int C>
 cudaError_t from_dvloc(const Dims& d, const void* q, const void* k, const void* w, const float* g_cum,
                        const void* dv_loc, const void* d_o, const float* dh_final, void* dh_ckpt, void* dv_new,
-                       float* dh0, cudaStream_t s, unsigned int* err) {
+                       float* dh0, const int* co, int nseq, cudaStream_t s, unsigned int* err) {
     return d.per_k ? launch<K, C, true, false>(d, q, k, w, g_cum, nullptr, dv_loc, d_o, dh_final, dh_ckpt, dv_new,
-                                               dh0, s, err)
+                                               dh0, co, nseq, s, err)
                    : launch<K, C, false, false>(d, q, k, w, g_cum, nullptr, dv_loc, d_o, dh_final, dh_ckpt, dv_new,
-                                                dh0, s, err);
+                                                dh0, co, nseq, s, err);
 }
 
 }  // namespace
 
 cudaError_t mma_bwd_scan(const Dims& d, const void* q, const void* k, const void* w, const float* g_cum, const void* P,
                          const void* d_o, const float* dh_final, void* dh_ckpt, void* dv_new, float* dh0,
-                         cudaStream_t s, unsigned int* err) {
-    if (!d.bf16 || d.per_k || d.C != 64) return cudaErrorInvalidValue;
-    return d.K == 64
-               ? launch<64, 64, false, true>(d, q, k, w, g_cum, P, nullptr, d_o, dh_final, dh_ckpt, dv_new, dh0, s, err)
-               : launch<128, 64, false, true>(d, q, k, w, g_cum, P, nullptr, d_o, dh_final, dh_ckpt, dv_new, dh0, s,
-                                              err);
+                         cudaStream_t s, unsigned int* err, const int* co, int nseq) {
+    if (!d.bf16 || d.per_k || d.C != 64 || (co && (d.B != 1 || nseq < 1))) return cudaErrorInvalidValue;
+    return d.K == 64 ? launch<64, 64, false, true>(d, q, k, w, g_cum, P, nullptr, d_o, dh_final, dh_ckpt, dv_new, dh0,
+                                                   co, nseq, s, err)
+                     : launch<128, 64, false, true>(d, q, k, w, g_cum, P, nullptr, d_o, dh_final, dh_ckpt, dv_new, dh0,
+                                                    co, nseq, s, err);
 }
 
 cudaError_t mma_bwd_scan_dl(const Dims& d, const void* q, const void* k, const void* w, const float* g_cum,
                             const void* dv_loc, const void* d_o, const float* dh_final, void* dh_ckpt, void* dv_new,
-                            float* dh0, cudaStream_t s, unsigned int* err) {
-    if (!d.bf16) return cudaErrorInvalidValue;
+                            float* dh0, cudaStream_t s, unsigned int* err, const int* co, int nseq) {
+    if (!d.bf16 || (co && (d.B != 1 || nseq < 1))) return cudaErrorInvalidValue;
     if (d.K == 64)
-        return d.C == 32 ? from_dvloc<64, 32>(d, q, k, w, g_cum, dv_loc, d_o, dh_final, dh_ckpt, dv_new, dh0, s, err)
-                         : from_dvloc<64, 64>(d, q, k, w, g_cum, dv_loc, d_o, dh_final, dh_ckpt, dv_new, dh0, s, err);
-    return d.C == 32 ? from_dvloc<128, 32>(d, q, k, w, g_cum, dv_loc, d_o, dh_final, dh_ckpt, dv_new, dh0, s, err)
-                     : from_dvloc<128, 64>(d, q, k, w, g_cum, dv_loc, d_o, dh_final, dh_ckpt, dv_new, dh0, s, err);
+        return d.C == 32 ? from_dvloc<64, 32>(d, q, k, w, g_cum, dv_loc, d_o, dh_final, dh_ckpt, dv_new, dh0, co, nseq, s, err)
+                         : from_dvloc<64, 64>(d, q, k, w, g_cum, dv_loc, d_o, dh_final, dh_ckpt, dv_new, dh0, co, nseq, s, err);
+    return d.C == 32 ? from_dvloc<128, 32>(d, q, k, w, g_cum, dv_loc, d_o, dh_final, dh_ckpt, dv_new, dh0, co, nseq, s, err)
+                     : from_dvloc<128, 64>(d, q, k, w, g_cum, dv_loc, d_o, dh_final, dh_ckpt, dv_new, dh0, co, nseq, s, err);
 }
 
 }  // namespace gdr

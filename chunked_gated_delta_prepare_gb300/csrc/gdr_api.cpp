@@ -270,6 +270,141 @@ gdr_status pick_backward(const gdr_problem* p, const gdr::Dims& d, BwdPath* path
     }
 }
 
+// The backward's launches on validated dims d, path and S, with the workspace planned as ws at base.
+// co, nseq: packed variable-length sequences in the chunk-packed layout (d has B = 1; S = 1; the
+// tensor-core paths), else NULL and 0.
+gdr_status run_backward(const gdr::Dims& d, BwdPath path, int S, char* base, const BackwardWorkspace& ws,
+                        const void* q, const void* k, const void* v, const float* g, const void* beta,
+                        const float* h0, const void* d_o, const float* dh_final, void* dq, void* dk, void* dv,
+                        float* dg, void* dbeta, float* dh0, cudaStream_t s, const int* co, int nseq) {
+    gdr_status st;
+    const bool tensor = path != BwdPath::Simt;
+    if (co && (S != 1 || !tensor)) return GDR_ERR_ARG;
+    float* g_cum = reinterpret_cast<float*>(base + ws.g_cum);
+    void* w = base + ws.w;
+    void* u = base + ws.u;
+    void* v_new = base + ws.v_new;
+    void* h_ckpt = base + ws.h_ckpt;
+    float* dv_loc = reinterpret_cast<float*>(base + ws.dv_loc);
+    float* dv_new = reinterpret_cast<float*>(base + ws.dv_new);
+    float* dh_ckpt = reinterpret_cast<float*>(base + ws.dh_ckpt);
+    float* dk_part = reinterpret_cast<float*>(base + ws.dk_part);
+    float* dw = reinterpret_cast<float*>(base + ws.dw);
+    float* dG_part = reinterpret_cast<float*>(base + ws.dG_part);
+    // grouped value heads: the stages write per-value-head dq and dk, summed over each group at the end
+    void* const dq_out = dq;
+    void* const dk_out = dk;
+    if (d.G > 1) {
+        dq = base + ws.dq_v;
+        dk = base + ws.dk_v;
+    }
+    // The two serial scans, segment-parallel when S > 1.  The re-scan as the forward does it; the reverse
+    // scan once from a zero gradient at every segment end (its dh0 per segment are the offsets Zb), the
+    // reverse stitch with the forward maps transposed, then again from the stitched segment ends.
+    float* seg_m = reinterpret_cast<float*>(base + ws.seg_m);
+    float* seg_z = reinterpret_cast<float*>(base + ws.seg_z);
+    float* seg_h = reinterpret_cast<float*>(base + ws.seg_h);
+    float* seg_zb = reinterpret_cast<float*>(base + ws.seg_zb);
+    float* seg_e = reinterpret_cast<float*>(base + ws.seg_e);
+    auto rescan = [&](unsigned int* err) -> gdr_status {
+        if (S == 1) return from_cuda(gdr::mma_scan(d, k, w, u, g_cum, h0, h_ckpt, v_new, nullptr, s, err, co, nseq));
+        const gdr::Dims ds = segment_view(d, S);
+        gdr_status r = from_cuda(gdr::mma_scan_transfer(ds, k, w, u, g_cum, seg_m, seg_z, s, err));
+        if (r == GDR_OK) r = from_cuda(gdr::segment_combine(d, S, seg_m, seg_z, h0, seg_h, nullptr, s));
+        if (r == GDR_OK) r = from_cuda(gdr::mma_scan(ds, k, w, u, g_cum, seg_h, h_ckpt, v_new, nullptr, s, err));
+        return r;
+    };
+    auto reverse_scan = [&](auto run) -> gdr_status {   // run(dims, dh_final, dh0)
+        if (S == 1) return run(d, dh_final, dh0);
+        const gdr::Dims ds = segment_view(d, S);
+        gdr_status r = run(ds, nullptr, seg_zb);
+        if (r == GDR_OK) r = from_cuda(gdr::segment_combine(d, S, seg_m, seg_zb, dh_final, seg_e, dh0, s, true));
+        if (r == GDR_OK) r = run(ds, seg_e, nullptr);
+        return r;
+    };
+    if (path == BwdPath::Fast) {
+        // every step on the tensor cores: prepare (+ P and T), re-scan, reverse scan, per-chunk stage
+        unsigned int* err = device_error_word();
+        void* tinv = base + ws.tinv;
+        if (d.C == 64) {   // the prepare's gated scores P give the reverse scan its local term
+            void* P = base + ws.P;
+            if ((st = from_cuda(gdr::mma_prepare(d, k, v, g, beta, w, u, g_cum, s, err, q, P, tinv))) != GDR_OK)
+                return st;
+            if ((st = rescan(err)) != GDR_OK) return st;
+            st = reverse_scan([&](const gdr::Dims& dd, const float* dhf, float* dh0o) {
+                return from_cuda(gdr::mma_bwd_scan(dd, q, k, w, g_cum, P, d_o, dhf, dh_ckpt, dv_new, dh0o, s, err, co,
+                                                   nseq));
+            });
+            if (st != GDR_OK) return st;
+        } else {           // C = 32: the local term from its own kernel
+            if ((st = from_cuda(gdr::mma_prepare(d, k, v, g, beta, w, u, g_cum, s, err, nullptr, nullptr, tinv))) !=
+                GDR_OK)
+                return st;
+            if ((st = rescan(err)) != GDR_OK) return st;
+            if ((st = from_cuda(gdr::mma_bwd_dv_local(d, q, k, g_cum, d_o, dv_loc, s))) != GDR_OK) return st;
+            st = reverse_scan([&](const gdr::Dims& dd, const float* dhf, float* dh0o) {
+                return from_cuda(gdr::mma_bwd_scan_dl(dd, q, k, w, g_cum, dv_loc, d_o, dhf, dh_ckpt, dv_new, dh0o, s,
+                                                      err, co, nseq));
+            });
+            if (st != GDR_OK) return st;
+        }
+        st = from_cuda(d.C == 64 ? gdr::mma_bwd_chunk_tma(d, q, k, v, beta, g_cum, w, u, tinv, v_new, h_ckpt, d_o,
+                                                          dv_new, dh_ckpt, dq, dk, dv, dbeta, dg, s, err)
+                                 : gdr::mma_bwd_chunk(d, q, k, v, beta, g_cum, w, u, tinv, v_new, h_ckpt, d_o, dv_new,
+                                                      dh_ckpt, dq, dk, dv, dbeta, dg, s));
+        if (st != GDR_OK) return st;
+        if (d.G > 1 && (st = from_cuda(gdr::group_sum_heads(d, dq, dk, dq_out, dk_out, s))) != GDR_OK) return st;
+        t_last_variant = "tensor";
+        return GDR_OK;
+    }
+    // forward prepare and re-scan: G, w, u, the checkpoints and v'
+    if (tensor) {
+        // a per-key-dim gate: prepare (+ T), re-scan, local term, reverse scan and the per-chunk stage on the
+        // tensor cores; the CUDA-core per-chunk stages finish the chunks that stage flags
+        unsigned int* err = device_error_word();
+        void* tinv = base + ws.tinv;
+        int* flags = reinterpret_cast<int*>(base + ws.flags);
+        if ((st = from_cuda(gdr::mma_prepare(d, k, v, g, beta, w, u, g_cum, s, err, nullptr, nullptr, tinv))) !=
+            GDR_OK)
+            return st;
+        if ((st = rescan(err)) != GDR_OK) return st;
+        if ((st = from_cuda(gdr::mma_bwd_dv_local(d, q, k, g_cum, d_o, dv_loc, s))) != GDR_OK) return st;
+        st = reverse_scan([&](const gdr::Dims& dd, const float* dhf, float* dh0o) {
+            return from_cuda(gdr::mma_bwd_scan_dl(dd, q, k, w, g_cum, dv_loc, d_o, dhf, dh_ckpt, dv_new, dh0o, s, err,
+                                                  co, nseq));
+        });
+        if (st != GDR_OK) return st;
+        if ((st = from_cuda(gdr::mma_bwd_chunk_kda(d, q, k, v, beta, g_cum, w, u, tinv, v_new, h_ckpt, d_o, dv_new,
+                                                   dh_ckpt, dq, dk, dv, dbeta, dg, flags, s))) != GDR_OK)
+            return st;
+        if ((st = from_cuda(gdr::simt_bwd_dqkwg(d, q, k, v_new, g_cum, h_ckpt, dh_ckpt, d_o, dv_new, dq, dk_part, dw,
+                                                dG_part, s, true, flags))) != GDR_OK)
+            return st;
+        if ((st = from_cuda(gdr::simt_bwd_wy(d, k, v, beta, g_cum, dw, dv_new, dk_part, dG_part, dk, dv, dbeta, dg, s,
+                                             true, flags))) != GDR_OK)
+            return st;
+        if (d.G > 1 && (st = from_cuda(gdr::group_sum_heads(d, dq, dk, dq_out, dk_out, s))) != GDR_OK) return st;
+        t_last_variant = "tensor";
+        return GDR_OK;
+    } else {
+        if ((st = from_cuda(gdr::simt_prepare(d, k, v, g, beta, w, u, g_cum, s))) != GDR_OK) return st;
+        if ((st = from_cuda(gdr::simt_scan(d, k, w, u, g_cum, h0, h_ckpt, v_new, nullptr, s))) != GDR_OK) return st;
+    }
+    if ((st = from_cuda(gdr::simt_bwd_dv_local(d, q, k, g_cum, d_o, dv_loc, s))) != GDR_OK) return st;
+    if ((st = from_cuda(gdr::simt_bwd_scan_dh(d, q, k, w, g_cum, d_o, dv_loc, dh_final, dh_ckpt, dv_new, dh0, s))) !=
+        GDR_OK)
+        return st;
+    if ((st = from_cuda(gdr::simt_bwd_dqkwg(d, q, k, v_new, g_cum, h_ckpt, dh_ckpt, d_o, dv_new, dq, dk_part, dw,
+                                            dG_part, s))) != GDR_OK)
+        return st;
+    if ((st = from_cuda(gdr::simt_bwd_wy(d, k, v, beta, g_cum, dw, dv_new, dk_part, dG_part, dk, dv, dbeta, dg, s))) !=
+        GDR_OK)
+        return st;
+    if (d.G > 1 && (st = from_cuda(gdr::group_sum_heads(d, dq, dk, dq_out, dk_out, s))) != GDR_OK) return st;
+    t_last_variant = tensor ? "tensor" : "simt";
+    return GDR_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -629,137 +764,16 @@ gdr_status gdr_backward(const gdr_problem* p, const void* q, const void* k, cons
     const BackwardWorkspace ws = plan_backward(d, path, S);
     if (!workspace || workspace_bytes < ws.total) return GDR_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GDR_ERR_ALIGN;
-    char* base = static_cast<char*>(workspace);
-    float* g_cum = reinterpret_cast<float*>(base + ws.g_cum);
-    void* w = base + ws.w;
-    void* u = base + ws.u;
-    void* v_new = base + ws.v_new;
-    void* h_ckpt = base + ws.h_ckpt;
-    float* dv_loc = reinterpret_cast<float*>(base + ws.dv_loc);
-    float* dv_new = reinterpret_cast<float*>(base + ws.dv_new);
-    float* dh_ckpt = reinterpret_cast<float*>(base + ws.dh_ckpt);
-    float* dk_part = reinterpret_cast<float*>(base + ws.dk_part);
-    float* dw = reinterpret_cast<float*>(base + ws.dw);
-    float* dG_part = reinterpret_cast<float*>(base + ws.dG_part);
-    cudaStream_t s = (cudaStream_t)stream;
-    // grouped value heads: the stages write per-value-head dq and dk, summed over each group at the end
-    void* const dq_out = dq;
-    void* const dk_out = dk;
-    if (d.G > 1) {
-        dq = base + ws.dq_v;
-        dk = base + ws.dk_v;
-    }
-    // The two serial scans, segment-parallel when S > 1.  The re-scan as the forward does it; the reverse
-    // scan once from a zero gradient at every segment end (its dh0 per segment are the offsets Zb), the
-    // reverse stitch with the forward maps transposed, then again from the stitched segment ends.
-    float* seg_m = reinterpret_cast<float*>(base + ws.seg_m);
-    float* seg_z = reinterpret_cast<float*>(base + ws.seg_z);
-    float* seg_h = reinterpret_cast<float*>(base + ws.seg_h);
-    float* seg_zb = reinterpret_cast<float*>(base + ws.seg_zb);
-    float* seg_e = reinterpret_cast<float*>(base + ws.seg_e);
-    auto rescan = [&](unsigned int* err) -> gdr_status {
-        if (S == 1) return from_cuda(gdr::mma_scan(d, k, w, u, g_cum, h0, h_ckpt, v_new, nullptr, s, err));
-        const gdr::Dims ds = segment_view(d, S);
-        gdr_status r = from_cuda(gdr::mma_scan_transfer(ds, k, w, u, g_cum, seg_m, seg_z, s, err));
-        if (r == GDR_OK) r = from_cuda(gdr::segment_combine(d, S, seg_m, seg_z, h0, seg_h, nullptr, s));
-        if (r == GDR_OK) r = from_cuda(gdr::mma_scan(ds, k, w, u, g_cum, seg_h, h_ckpt, v_new, nullptr, s, err));
-        return r;
-    };
-    auto reverse_scan = [&](auto run) -> gdr_status {   // run(dims, dh_final, dh0)
-        if (S == 1) return run(d, dh_final, dh0);
-        const gdr::Dims ds = segment_view(d, S);
-        gdr_status r = run(ds, nullptr, seg_zb);
-        if (r == GDR_OK) r = from_cuda(gdr::segment_combine(d, S, seg_m, seg_zb, dh_final, seg_e, dh0, s, true));
-        if (r == GDR_OK) r = run(ds, seg_e, nullptr);
-        return r;
-    };
-    if (path == BwdPath::Fast) {
-        // every step on the tensor cores: prepare (+ P and T), re-scan, reverse scan, per-chunk stage
-        unsigned int* err = device_error_word();
-        void* tinv = base + ws.tinv;
-        if (d.C == 64) {   // the prepare's gated scores P give the reverse scan its local term
-            void* P = base + ws.P;
-            if ((st = from_cuda(gdr::mma_prepare(d, k, v, g, beta, w, u, g_cum, s, err, q, P, tinv))) != GDR_OK)
-                return st;
-            if ((st = rescan(err)) != GDR_OK) return st;
-            st = reverse_scan([&](const gdr::Dims& dd, const float* dhf, float* dh0o) {
-                return from_cuda(gdr::mma_bwd_scan(dd, q, k, w, g_cum, P, d_o, dhf, dh_ckpt, dv_new, dh0o, s, err));
-            });
-            if (st != GDR_OK) return st;
-        } else {           // C = 32: the local term from its own kernel
-            if ((st = from_cuda(gdr::mma_prepare(d, k, v, g, beta, w, u, g_cum, s, err, nullptr, nullptr, tinv))) !=
-                GDR_OK)
-                return st;
-            if ((st = rescan(err)) != GDR_OK) return st;
-            if ((st = from_cuda(gdr::mma_bwd_dv_local(d, q, k, g_cum, d_o, dv_loc, s))) != GDR_OK) return st;
-            st = reverse_scan([&](const gdr::Dims& dd, const float* dhf, float* dh0o) {
-                return from_cuda(gdr::mma_bwd_scan_dl(dd, q, k, w, g_cum, dv_loc, d_o, dhf, dh_ckpt, dv_new, dh0o, s,
-                                                      err));
-            });
-            if (st != GDR_OK) return st;
-        }
-        st = from_cuda(d.C == 64 ? gdr::mma_bwd_chunk_tma(d, q, k, v, beta, g_cum, w, u, tinv, v_new, h_ckpt, d_o,
-                                                          dv_new, dh_ckpt, dq, dk, dv, dbeta, dg, s, err)
-                                 : gdr::mma_bwd_chunk(d, q, k, v, beta, g_cum, w, u, tinv, v_new, h_ckpt, d_o, dv_new,
-                                                      dh_ckpt, dq, dk, dv, dbeta, dg, s));
-        if (st != GDR_OK) return st;
-        if (d.G > 1 && (st = from_cuda(gdr::group_sum_heads(d, dq, dk, dq_out, dk_out, s))) != GDR_OK) return st;
-        t_last_variant = "tensor";
-        return GDR_OK;
-    }
-    // forward prepare and re-scan: G, w, u, the checkpoints and v'
-    if (tensor) {
-        // a per-key-dim gate: prepare (+ T), re-scan, local term, reverse scan and the per-chunk stage on the
-        // tensor cores; the CUDA-core per-chunk stages finish the chunks that stage flags
-        unsigned int* err = device_error_word();
-        void* tinv = base + ws.tinv;
-        int* flags = reinterpret_cast<int*>(base + ws.flags);
-        if ((st = from_cuda(gdr::mma_prepare(d, k, v, g, beta, w, u, g_cum, s, err, nullptr, nullptr, tinv))) !=
-            GDR_OK)
-            return st;
-        if ((st = rescan(err)) != GDR_OK) return st;
-        if ((st = from_cuda(gdr::mma_bwd_dv_local(d, q, k, g_cum, d_o, dv_loc, s))) != GDR_OK) return st;
-        st = reverse_scan([&](const gdr::Dims& dd, const float* dhf, float* dh0o) {
-            return from_cuda(gdr::mma_bwd_scan_dl(dd, q, k, w, g_cum, dv_loc, d_o, dhf, dh_ckpt, dv_new, dh0o, s, err));
-        });
-        if (st != GDR_OK) return st;
-        if ((st = from_cuda(gdr::mma_bwd_chunk_kda(d, q, k, v, beta, g_cum, w, u, tinv, v_new, h_ckpt, d_o, dv_new,
-                                                   dh_ckpt, dq, dk, dv, dbeta, dg, flags, s))) != GDR_OK)
-            return st;
-        if ((st = from_cuda(gdr::simt_bwd_dqkwg(d, q, k, v_new, g_cum, h_ckpt, dh_ckpt, d_o, dv_new, dq, dk_part, dw,
-                                                dG_part, s, true, flags))) != GDR_OK)
-            return st;
-        if ((st = from_cuda(gdr::simt_bwd_wy(d, k, v, beta, g_cum, dw, dv_new, dk_part, dG_part, dk, dv, dbeta, dg, s,
-                                             true, flags))) != GDR_OK)
-            return st;
-        if (d.G > 1 && (st = from_cuda(gdr::group_sum_heads(d, dq, dk, dq_out, dk_out, s))) != GDR_OK) return st;
-        t_last_variant = "tensor";
-        return GDR_OK;
-    } else {
-        if ((st = from_cuda(gdr::simt_prepare(d, k, v, g, beta, w, u, g_cum, s))) != GDR_OK) return st;
-        if ((st = from_cuda(gdr::simt_scan(d, k, w, u, g_cum, h0, h_ckpt, v_new, nullptr, s))) != GDR_OK) return st;
-    }
-    if ((st = from_cuda(gdr::simt_bwd_dv_local(d, q, k, g_cum, d_o, dv_loc, s))) != GDR_OK) return st;
-    if ((st = from_cuda(gdr::simt_bwd_scan_dh(d, q, k, w, g_cum, d_o, dv_loc, dh_final, dh_ckpt, dv_new, dh0, s))) !=
-        GDR_OK)
-        return st;
-    if ((st = from_cuda(gdr::simt_bwd_dqkwg(d, q, k, v_new, g_cum, h_ckpt, dh_ckpt, d_o, dv_new, dq, dk_part, dw,
-                                            dG_part, s))) != GDR_OK)
-        return st;
-    if ((st = from_cuda(gdr::simt_bwd_wy(d, k, v, beta, g_cum, dw, dv_new, dk_part, dG_part, dk, dv, dbeta, dg, s))) !=
-        GDR_OK)
-        return st;
-    if (d.G > 1 && (st = from_cuda(gdr::group_sum_heads(d, dq, dk, dq_out, dk_out, s))) != GDR_OK) return st;
-    t_last_variant = tensor ? "tensor" : "simt";
-    return GDR_OK;
+    return run_backward(d, path, S, static_cast<char*>(workspace), ws, q, k, v, g, beta, h0, d_o, dh_final, dq, dk, dv,
+                        dg, dbeta, dh0, (cudaStream_t)stream, nullptr, 0);
 }
 
 }  // extern "C"
 
 // ---- packed variable-length sequences
-// The forward on the tensor cores runs them chunk-packed: every sequence a run of whole chunks of one
-// row (fewer than C zero tokens each), the scans walking each sequence's chunks.  The CUDA-core forward
-// and the backward run them padded: sequence s as row s of a batch of rows of p->T tokens.
+// On the tensor cores they run chunk-packed: every sequence a run of whole chunks of one row (fewer
+// than C zero tokens each), the scans walking each sequence's chunks.  On the CUDA cores they run
+// padded: sequence s as row s of a batch of rows of p->T tokens.
 namespace {
 
 // Bytes a token takes in each working tensor, in order.  Forward: q k v g beta (packed in) | o (unpacked
@@ -787,10 +801,8 @@ gdr::Dims chunk_packed(const gdr::Dims& d, int64_t chunks) {
 // chunks of the chunk-packed layout in the worst case for p: n sequences of p->T tokens
 int64_t max_chunks(const gdr::Dims& d) { return (int64_t)d.B * d.NT; }
 
-// the forward runs chunk-packed on the tensor cores, when the packed row's indices fit in int32
-bool forward_chunk_packed(const gdr::Dims& d, Path path) {
-    return path != Path::Simt && max_chunks(d) * d.C * d.H <= INT32_MAX;
-}
+// the chunk-packed row's indices fit in int32
+bool chunk_packed_fits(const gdr::Dims& d) { return max_chunks(d) * d.C * d.H <= INT32_MAX; }
 
 struct VarlenWorkspace {
     size_t cu, co, cs, pad[11], inner, inner_bytes, total;
@@ -832,8 +844,8 @@ gdr_status check_cu(const int32_t* cu, int64_t n, int64_t total, int64_t T) {
     return GDR_OK;
 }
 
-// workspace of the inner call(s): the padded problem's, and for a chunk-packed forward also the
-// largest chunk-packed problem's
+// workspace of the inner call(s): the padded problem's, and on the tensor cores also the largest
+// chunk-packed problem's
 gdr_status varlen_inner_bytes(const gdr_problem* p, const gdr::Dims& d, bool backward, size_t* bytes,
                               bool* chunked) {
     gdr_status st;
@@ -844,12 +856,17 @@ gdr_status varlen_inner_bytes(const gdr_problem* p, const gdr::Dims& d, bool bac
         if ((st = pick_backward(p, d, &path)) != GDR_OK) return st;
         if ((st = resolve_segments(p, d, path != BwdPath::Simt, &S)) != GDR_OK) return st;
         *bytes = plan_backward(d, path, S).total;
+        if (path != BwdPath::Simt && chunk_packed_fits(d)) {
+            *chunked = true;
+            const size_t c = plan_backward(chunk_packed(d, max_chunks(d)), path, 1).total;
+            if (c > *bytes) *bytes = c;
+        }
     } else {
         Path path;
         if ((st = pick_forward(p, d, &path)) != GDR_OK) return st;
         if ((st = resolve_segments(p, d, path != Path::Simt, &S)) != GDR_OK) return st;
         *bytes = plan_staged(d, path == Path::Fused, S).total;
-        if (forward_chunk_packed(d, path)) {
+        if (path != Path::Simt && chunk_packed_fits(d)) {
             *chunked = true;
             const size_t c = plan_staged(chunk_packed(d, max_chunks(d)), path == Path::Fused, 1).total;
             if (c > *bytes) *bytes = c;
@@ -927,7 +944,7 @@ gdr_status gdr_varlen_forward(const gdr_problem* p, const int32_t* cu_seqlens, c
     const gdr::RowCopy out[1] = {{base + ws.pad[5], o, rb[5]}};
     int64_t chunks = 0;   // the chunk-packed row's chunks, from the host lengths
     for (int64_t i = 0; i < d.B; ++i) chunks += ((int64_t)cu_seqlens[i + 1] - cu_seqlens[i] + d.C - 1) / d.C;
-    if (forward_chunk_packed(d, path) && chunks > 0) {
+    if (path != Path::Simt && chunk_packed_fits(d) && chunks > 0) {
         int* co = reinterpret_cast<int*>(base + ws.co);
         int* cs = reinterpret_cast<int*>(base + ws.cs);
         const gdr::VarlenMap m{cu, co, cs, d.B, total, 0, d.C, chunks * d.C};
@@ -989,25 +1006,39 @@ gdr_status gdr_varlen_backward(const gdr_problem* p, const int32_t* cu_seqlens, 
     if ((st = varlen_setup(p, &d, true, cu_seqlens, cu_seqlens_device, total, workspace, workspace_bytes, s, &ws,
                            &cu)) != GDR_OK)
         return st;
+    BwdPath path;
+    if ((st = pick_backward(p, d, &path)) != GDR_OK) return st;
     char* base = static_cast<char*>(workspace);
     int64_t rb[11];
     varlen_rows(d, true, rb);
-    const gdr::VarlenMap m{cu, nullptr, nullptr, d.B, total, d.T, d.C, (int64_t)d.B * d.T};
     const void* packed_in[6] = {q, k, v, g, beta, d_o};
-    gdr::RowCopy in[6];
-    for (int i = 0; i < 6; ++i) in[i] = {packed_in[i], base + ws.pad[i], rb[i]};
-    if ((st = from_cuda(gdr::varlen_pack(in, 6, m, s))) != GDR_OK) return st;
+    void* packed_out[5] = {dq, dk, dv, dg, dbeta};
     auto pad = [&](int i) { return static_cast<void*>(base + ws.pad[i]); };
+    gdr::RowCopy in[6], out[5];
+    for (int i = 0; i < 6; ++i) in[i] = {packed_in[i], pad(i), rb[i]};
+    for (int i = 0; i < 5; ++i) out[i] = {pad(6 + i), packed_out[i], rb[6 + i]};
+    int64_t chunks = 0;   // the chunk-packed row's chunks, from the host lengths
+    for (int64_t i = 0; i < d.B; ++i) chunks += ((int64_t)cu_seqlens[i + 1] - cu_seqlens[i] + d.C - 1) / d.C;
+    if (path != BwdPath::Simt && chunk_packed_fits(d) && chunks > 0) {
+        int* co = reinterpret_cast<int*>(base + ws.co);
+        int* cs = reinterpret_cast<int*>(base + ws.cs);
+        const gdr::VarlenMap m{cu, co, cs, d.B, total, 0, d.C, chunks * d.C};
+        const gdr::Dims d1 = chunk_packed(d, chunks);
+        if ((st = from_cuda(gdr::varlen_plan(cu, d.B, total, d.C, (int)chunks, co, cs, s))) != GDR_OK) return st;
+        if ((st = from_cuda(gdr::varlen_pack(in, 6, m, s))) != GDR_OK) return st;
+        if ((st = run_backward(d1, path, 1, base + ws.inner, plan_backward(d1, path, 1), pad(0), pad(1), pad(2),
+                               static_cast<const float*>(pad(3)), pad(4), h0, pad(5), dh_final, pad(6), pad(7),
+                               pad(8), static_cast<float*>(pad(9)), pad(10), dh0, s, co, d.B)) != GDR_OK)
+            return st;
+        return from_cuda(gdr::varlen_unpack(out, 5, m, s));
+    }
+    const gdr::VarlenMap m{cu, nullptr, nullptr, d.B, total, d.T, d.C, (int64_t)d.B * d.T};
+    if ((st = from_cuda(gdr::varlen_pack(in, 6, m, s))) != GDR_OK) return st;
     if ((st = gdr_backward(p, pad(0), pad(1), pad(2), static_cast<const float*>(pad(3)), pad(4), h0, pad(5), dh_final,
                            pad(6), pad(7), pad(8), static_cast<float*>(pad(9)), pad(10), dh0, base + ws.inner,
                            ws.inner_bytes, stream)) != GDR_OK)
         return st;
-    if (total > 0) {
-        void* packed_out[5] = {dq, dk, dv, dg, dbeta};
-        gdr::RowCopy out[5];
-        for (int i = 0; i < 5; ++i) out[i] = {pad(6 + i), packed_out[i], rb[6 + i]};
-        if ((st = from_cuda(gdr::varlen_unpack(out, 5, m, s))) != GDR_OK) return st;
-    }
+    if (total > 0 && (st = from_cuda(gdr::varlen_unpack(out, 5, m, s))) != GDR_OK) return st;
     return GDR_OK;
 }
 

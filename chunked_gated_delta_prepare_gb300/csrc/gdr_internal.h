@@ -81,15 +81,16 @@ cudaError_t group_sum_heads(const Dims& d, const void* dq_v, const void* dk_v, v
 
 // ---- backward on the tensor cores (bf16 io, scalar gate, C = 64)
 // reverse scan: dv' = scale P^T do + (k gamma) dh, dh = e^(G_L) dh + scale (q e^G)^T do - w^T dv';
+// co, nseq: packed variable-length sequences as for mma_scan (dh_final[z] back to dh0[z])
 // dh_ckpt [B,NT,H,K,V] and dv_new [B,T,H,V] bf16 (bwd_scan_mma.cu)
 cudaError_t mma_bwd_scan(const Dims& d, const void* q, const void* k, const void* w, const float* g_cum, const void* P,
                          const void* d_o, const float* dh_final, void* dh_ckpt, void* dv_new, float* dh0,
-                         cudaStream_t s, unsigned int* err);
+                         cudaStream_t s, unsigned int* err, const int* co = nullptr, int nseq = 0);
 // the reverse scan with the local term precomputed: dv' = dv_loc + kg dh; dv_loc [B,T,H,V] bf16;
 // either gate, C = 32 or 64 (bwd_scan_mma.cu)
 cudaError_t mma_bwd_scan_dl(const Dims& d, const void* q, const void* k, const void* w, const float* g_cum,
                             const void* dv_loc, const void* d_o, const float* dh_final, void* dh_ckpt, void* dv_new,
-                            float* dh0, cudaStream_t s, unsigned int* err);
+                            float* dh0, cudaStream_t s, unsigned int* err, const int* co = nullptr, int nseq = 0);
 // dv_loc = scale tril_0(Q~)^T do per chunk, bf16 (bwd_dvloc_mma.cu)
 cudaError_t mma_bwd_dv_local(const Dims& d, const void* q, const void* k, const float* g_cum, const void* d_o,
                              void* dv_loc, cudaStream_t s);

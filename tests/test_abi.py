@@ -246,30 +246,31 @@ def test_varlen_checks_cu_seqlens_on_the_host(lib):
 def test_varlen_workspace_size_formula(lib):
     # device cu; on the tensor cores also the chunk offsets co [n + 1] and the chunk -> sequence map [NTmax],
     # NTmax = n ceil(T / C); then every working tensor (rows: NTmax C chunk-packed, n T padded), each
-    # rounded up to 256 bytes; then the inner calls' workspace (forward on the tensor cores: the larger of
-    # the padded problem's and the largest chunk-packed problem's)
+    # rounded up to 256 bytes; then the inner call's workspace (on the tensor cores the larger of the padded
+    # problem's and that of the largest chunk-packed problem, one row of NTmax chunks without segments)
     r = lambda x: (x + 255) // 256 * 256
-    for (n, T, H, HV, K, V, C, dt, per_k, variant, fused) in [(3, 100, 2, 2, 64, 64, 64, 1, False, "auto", True),
-                                                               (5, 333, 1, 4, 128, 64, 32, 1, True, "auto", False),
-                                                               (2, 64, 2, 2, 64, 128, 64, 0, True, "simt", None)]:
-        p = gdr.make_problem(n, T, H, K, V, C, dt, per_k, variant=variant, HV=HV if HV != H else 0)
+    for (n, T, H, HV, K, V, C, dt, per_k, variant) in [(3, 100, 2, 2, 64, 64, 64, 1, False, "auto"),
+                                                       (5, 333, 1, 4, 128, 64, 32, 1, True, "auto"),
+                                                       (4, 4096, 2, 2, 128, 128, 64, 1, False, "tensor"),
+                                                       (2, 64, 2, 2, 64, 128, 64, 0, True, "simt")]:
+        mk = lambda B, T_, segments=0: gdr.make_problem(B, T_, H, K, V, C, dt, per_k, variant=variant,
+                                                        HV=HV if HV != H else 0, segments=segments)
+        p = mk(n, T)
         e = 2 if dt else 4
         qk, vv, gg, bb = H * K * e, HV * V * e, HV * (K if per_k else 1) * 4, HV * e
-        chunked = fused is not None
+        chunked = variant != "simt"
         ntmax = n * -(-T // C)
         rows = ntmax * C if chunked else n * T
         head = r((n + 1) * 4) + (r((n + 1) * 4) + r(ntmax * 4) if chunked else 0)
         pad = lambda sizes: sum(r(rows * b) for b in sizes)
-        inner = lib.gdr_forward_workspace_bytes(ctypes.byref(p))
-        if chunked:   # g_cum, w, u, then P (fused, C = 64) or v_new and the checkpoints
-            tok = ntmax * C * HV
-            c = r(tok * gg // HV) + r(tok * K * e) + r(tok * V * e)
-            c += (r(ntmax * HV * C * C * e) if C == 64 else 0) if fused else \
-                r(tok * V * e) + r(ntmax * HV * K * V * e)
-            inner = max(inner, c)
-        fwd = head + pad([qk, qk, vv, gg, bb, vv]) + inner
-        bwd = r((n + 1) * 4) + sum(r(n * T * b) for b in [qk, qk, vv, gg, bb, vv, qk, qk, vv, gg, bb]) + \
-            lib.gdr_backward_workspace_bytes(ctypes.byref(p))
+        big = mk(1, ntmax * C, segments=1)
+        fin = lib.gdr_forward_workspace_bytes(ctypes.byref(p))
+        bin_ = lib.gdr_backward_workspace_bytes(ctypes.byref(p))
+        if chunked:
+            fin = max(fin, lib.gdr_forward_workspace_bytes(ctypes.byref(big)))
+            bin_ = max(bin_, lib.gdr_backward_workspace_bytes(ctypes.byref(big)))
+        fwd = head + pad([qk, qk, vv, gg, bb, vv]) + fin
+        bwd = head + pad([qk, qk, vv, gg, bb, vv, qk, qk, vv, gg, bb]) + bin_
         assert lib.gdr_varlen_forward_workspace_bytes(ctypes.byref(p)) == fwd
         assert lib.gdr_varlen_backward_workspace_bytes(ctypes.byref(p)) == bwd
     bad = gdr.make_problem(3, 100, 2, 96, 64, 64)

@@ -157,3 +157,22 @@ def test_varlen_long_mixed_batch_sampled_heads():
     o_ref, hf_ref = reference(sub, C)
     assert max_abs(o[:, heads], o_ref) <= O_TOL["bf16"]
     assert rel_frob(hf[:, heads], hf_ref) <= H_TOL["bf16"]
+
+
+def test_varlen_backward_long_mixed_batch_sampled_heads():
+    # 32 heads of 128 x 128 over 8k packed tokens in six sequences; the oracle recomputes two heads
+    lengths = [2048, 1, 0, 3000, 777, 2366]
+    H, K, V, C = 32, 128, 128, 64
+    x = inputs(lengths, False, torch.bfloat16, H=H, K=K, V=V, seed=12)
+    do, dhf = upstream(x, 4)
+    q, k, v, g, beta, h0 = (dev(t) for t in (x.q, x.k, x.v, x.g, x.beta, x.h0))
+    got = gdr.backward_varlen(q, k, v, g, beta, x.cu, h0, dev(do), dev(dhf), chunk=C, scale=SCALE)
+    torch.cuda.synchronize()
+    assert gdr.gdr_get_device_status() == 0
+    assert gdr.gdr_last_variant() == "tensor"
+    heads = [5, 27]
+    d = {n_: t[:, heads].double().numpy() for n_, t in x.tensors().items()}
+    ref = varlen.backward(d["q"], d["k"], d["v"], d["g"], d["beta"], x.cu.numpy(), d["h0"],
+                          do[:, heads].double().numpy(), dhf[:, heads].double().numpy(), C, SCALE)
+    for name, t in zip(("dq", "dk", "dv", "dg", "dbeta", "dh0"), got):
+        assert scaled_err(t[:, heads], ref[name]) <= BWD_TOL["bf16"], (name, scaled_err(t[:, heads], ref[name]))

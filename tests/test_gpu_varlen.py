@@ -176,3 +176,24 @@ def test_varlen_backward_long_mixed_batch_sampled_heads():
                           do[:, heads].double().numpy(), dhf[:, heads].double().numpy(), C, SCALE)
     for name, t in zip(("dq", "dk", "dv", "dg", "dbeta", "dh0"), got):
         assert scaled_err(t[:, heads], ref[name]) <= BWD_TOL["bf16"], (name, scaled_err(t[:, heads], ref[name]))
+
+
+@pytest.mark.parametrize("per_k", [False, True])
+def test_varlen_many_short_sequences(per_k):
+    # 2500 sequences of 0 to 70 tokens: the chunk map's prefix sum runs over several 1024-sequence tiles
+    lengths = np.random.default_rng(13).integers(0, 71, size=2500).tolist()
+    x = inputs(lengths, per_k, torch.bfloat16, H=2, K=64, V=64, seed=13)
+    o, hf, var = gpu_forward(x, 64, "auto")
+    assert var == ("tensor" if per_k else "fused")
+    o_ref, hf_ref = reference(x, 64)
+    assert max_abs(o, o_ref) <= O_TOL["bf16"] and rel_frob(hf, hf_ref) <= H_TOL["bf16"]
+    do, dhf = upstream(x, 5)
+    q, k, v, g, beta, h0 = (dev(t) for t in (x.q, x.k, x.v, x.g, x.beta, x.h0))
+    got = gdr.backward_varlen(q, k, v, g, beta, x.cu, h0, dev(do), dev(dhf), chunk=64, scale=SCALE)
+    torch.cuda.synchronize()
+    assert gdr.gdr_get_device_status() == 0
+    d = {n_: t.double().numpy() for n_, t in x.tensors().items()}
+    ref = varlen.backward(d["q"], d["k"], d["v"], d["g"], d["beta"], x.cu.numpy(), d["h0"], do.double().numpy(),
+                          dhf.double().numpy(), 64, SCALE)
+    for name, t in zip(("dq", "dk", "dv", "dg", "dbeta", "dh0"), got):
+        assert scaled_err(t, ref[name]) <= BWD_TOL["bf16"], (name, scaled_err(t, ref[name]))

@@ -153,7 +153,7 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
     float* sB = reinterpret_cast<float*>(F + L::fB);
     float* sE = reinterpret_cast<float*>(F + L::fE);
     int* sFlag = reinterpret_cast<int*>(F + L::fFlag);
-    __shared__ uint64_t bar_tma;
+    __shared__ uint64_t bar_k, bar_q, bar_v;   // one per tile, each waited on just before its first use
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int t0 = blockIdx.x * kTile, h = blockIdx.y, b = blockIdx.z;
@@ -163,22 +163,27 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
     const uint32_t s_base = bw::smem_u32(sm);
 
     if (tid == 0) {
-        bw::mbar_init(&bar_tma, 1);
+        bw::mbar_init(&bar_k, 1);
+        bw::mbar_init(&bar_q, 1);
+        bw::mbar_init(&bar_v, 1);
         bw::fence_mbar_init();
         *sFlag = 0;
     }
     __syncthreads();
 
     if (tid == 0) {
-        bw::mbar_arrive_expect_tx(&bar_tma, (K + V + (WITH_P ? K : 0)) * 128);
+        // k first (S = k k^T needs it at once), then q (P), then v (u, the last product)
+        bw::mbar_arrive_expect_tx(&bar_k, K * 128);
 #pragma unroll
-        for (int a = 0; a < K / 64; ++a) bw::tma_load_4d(sm + L::kK + a * 8192, &mk, &bar_tma, a * 64, hk, t0, b);
-#pragma unroll
-        for (int a = 0; a < V / 64; ++a) bw::tma_load_4d(sm + L::kV + a * 8192, &mv, &bar_tma, a * 64, h, t0, b);
+        for (int a = 0; a < K / 64; ++a) bw::tma_load_4d(sm + L::kK + a * 8192, &mk, &bar_k, a * 64, hk, t0, b);
         if constexpr (WITH_P) {
+            bw::mbar_arrive_expect_tx(&bar_q, K * 128);
 #pragma unroll
-            for (int a = 0; a < K / 64; ++a) bw::tma_load_4d(sm + L::kQ + a * 8192, &mq, &bar_tma, a * 64, hk, t0, b);
+            for (int a = 0; a < K / 64; ++a) bw::tma_load_4d(sm + L::kQ + a * 8192, &mq, &bar_q, a * 64, hk, t0, b);
         }
+        bw::mbar_arrive_expect_tx(&bar_v, V * 128);
+#pragma unroll
+        for (int a = 0; a < V / 64; ++a) bw::tma_load_4d(sm + L::kV + a * 8192, &mv, &bar_v, a * 64, h, t0, b);
     }
     // beta; g (rows past T read as zero)
     for (int i = tid; i < kTile; i += 128) sB[i] = i < nvalid ? __bfloat162float(beta[row(i)]) : 0.f;
@@ -225,7 +230,7 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
         __syncthreads();
     }
 
-    bool ok = bw::mbar_wait(&bar_tma, 0, err, kDeviceErrTimeout);
+    bool ok = bw::mbar_wait(&bar_k, 0, err, kDeviceErrTimeout);
 
     if (PER_K) {
         // gated copies for S: Ka = k exp(G - G_ref), Kb = k exp(G_ref - G), G_ref = middle row of the chunk
@@ -299,6 +304,7 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
         }
     }
     if constexpr (WITH_P) {
+        ok = bw::mbar_wait(&bar_q, 0, err, kDeviceErrTimeout) && ok;
         // P = tril_0(q k^T * exp(G_i - G_j)) for this warp's rows (key blocks past the diagonal are
         // zero and skipped) -> bf16 into the q tile's place (each warp overwrites only its own rows of
         // q, after reading them), as a [64][64] tile in the 128-byte swizzle; stored with w and u below
@@ -563,6 +569,7 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
     // w over the tile it reads (k, or its scaled copy Ka), then u over v
     const uint32_t w_tile = PER_K ? L::kKa : L::kK;
     product_in_place(tw, s_base + w_tile, std::integral_constant<int, K>{});
+    ok = bw::mbar_wait(&bar_v, 0, err, kDeviceErrTimeout) && ok;
     product_in_place(tu, s_base + L::kV, std::integral_constant<int, V>{});
     bw::fence_async_shared();
     __syncthreads();

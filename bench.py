@@ -392,7 +392,7 @@ def time_varlen(args, wl, dev, flush, stream, world):
     h0 = x.h0.to(dev) if x.h0 is not None else None
     cu_dev = x.cu.to(dev)
     total = int(x.cu[-1])
-    p = gdr._varlen_problem(q, v, g, x.cu, None, wl.chunk, None, args.variant, args.segments)
+    p = gdr.varlen_problem(q, v, g, x.cu, None, wl.chunk, None, args.variant, args.segments)
     o = torch.empty_like(v)
     hf = torch.empty(int(p.B), wl.H, wl.K, wl.V, device=dev, dtype=torch.float32)
     nbytes = gdr.gdr_varlen_forward_workspace_bytes(p)

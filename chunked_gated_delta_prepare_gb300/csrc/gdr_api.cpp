@@ -880,6 +880,7 @@ gdr_status varlen_inner_bytes(const gdr_problem* p, const gdr::Dims& d, bool bac
 gdr_status varlen_setup(const gdr_problem* p, gdr::Dims* d, bool backward, const int32_t* cu_host,
                         const int32_t* cu_dev, int64_t total, void* workspace, size_t workspace_bytes,
                         cudaStream_t s, VarlenWorkspace* ws, const int** cu) {
+    // p is the caller's problem with segments = 1 (see varlen_problem)
     gdr_status st = check_problem(p, d);
     if (st != GDR_OK) return st;
     if ((st = check_cu(cu_host, p->B, total, p->T)) != GDR_OK) return st;
@@ -902,10 +903,21 @@ gdr_status varlen_setup(const gdr_problem* p, gdr::Dims* d, bool backward, const
     return GDR_OK;
 }
 
-size_t varlen_workspace_bytes(const gdr_problem* p, bool backward) {
+// The varlen calls scan each sequence whole: the segment-parallel scan does not apply, so the caller's
+// p->segments is replaced by 1 before anything else looks at the problem.
+gdr_problem varlen_problem(const gdr_problem* p) {
+    gdr_problem q = *p;
+    q.segments = 1;
+    return q;
+}
+
+size_t varlen_workspace_bytes(const gdr_problem* p_in, bool backward) {
     gdr::Dims d;
     size_t inner = 0;
     bool chunked = false;
+    if (!p_in) return 0;
+    const gdr_problem p1 = varlen_problem(p_in);
+    const gdr_problem* p = &p1;
     if (check_problem(p, &d) != GDR_OK || varlen_inner_bytes(p, d, backward, &inner, &chunked) != GDR_OK) return 0;
     return plan_varlen(d, backward, chunked, inner).total;
 }
@@ -918,10 +930,13 @@ size_t gdr_varlen_forward_workspace_bytes(const gdr_problem* p) { return varlen_
 
 size_t gdr_varlen_backward_workspace_bytes(const gdr_problem* p) { return varlen_workspace_bytes(p, true); }
 
-gdr_status gdr_varlen_forward(const gdr_problem* p, const int32_t* cu_seqlens, const int32_t* cu_seqlens_device,
+gdr_status gdr_varlen_forward(const gdr_problem* p_in, const int32_t* cu_seqlens, const int32_t* cu_seqlens_device,
                               int64_t total, const void* q, const void* k, const void* v, const float* g,
                               const void* beta, const float* h0, void* o, float* h_final, void* workspace,
                               size_t workspace_bytes, void* stream) {
+    if (!p_in) return GDR_ERR_NULL;
+    const gdr_problem p1 = varlen_problem(p_in);
+    const gdr_problem* p = &p1;
     gdr::Dims d;
     gdr_status st = check_problem(p, &d);
     if (st != GDR_OK) return st;
@@ -987,11 +1002,14 @@ gdr_status gdr_varlen_forward(const gdr_problem* p, const int32_t* cu_seqlens, c
     return GDR_OK;
 }
 
-gdr_status gdr_varlen_backward(const gdr_problem* p, const int32_t* cu_seqlens, const int32_t* cu_seqlens_device,
+gdr_status gdr_varlen_backward(const gdr_problem* p_in, const int32_t* cu_seqlens, const int32_t* cu_seqlens_device,
                                int64_t total, const void* q, const void* k, const void* v, const float* g,
                                const void* beta, const float* h0, const void* d_o, const float* dh_final, void* dq,
                                void* dk, void* dv, float* dg, void* dbeta, float* dh0, void* workspace,
                                size_t workspace_bytes, void* stream) {
+    if (!p_in) return GDR_ERR_NULL;
+    const gdr_problem p1 = varlen_problem(p_in);
+    const gdr_problem* p = &p1;
     gdr::Dims d;
     gdr_status st = check_problem(p, &d);
     if (st != GDR_OK) return st;

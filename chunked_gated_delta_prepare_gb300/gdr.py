@@ -504,7 +504,7 @@ def gdr_varlen_backward(p, cu_seqlens, cu_seqlens_device, total, q, k, v, g, bet
                                       _ptr(workspace), int(workspace_bytes), _stream(stream)), "gdr_varlen_backward")
 
 
-def _varlen_problem(q, v, g, cu_host, max_len, chunk, scale, variant, segments):
+def varlen_problem(q, v, g, cu_host, max_len, chunk, scale, variant, segments):
     """The padded problem of packed q [total,H,K] (or [1,total,H,K]), v, g: B = n sequences, T = max_len."""
     n = cu_host.numel() - 1
     if n < 1:
@@ -528,7 +528,7 @@ def forward_varlen(q, k, v, g, beta, cu_seqlens, h0=None, *, chunk=64, scale=Non
     cu_host = _host_cu(cu_seqlens)
     cu_dev = cu_seqlens if (isinstance(cu_seqlens, torch.Tensor) and cu_seqlens.is_cuda
                             and cu_seqlens.dtype == torch.int32 and cu_seqlens.is_contiguous()) else None
-    p = _varlen_problem(q, v, g, cu_host, max_len, chunk, scale, variant, segments)
+    p = varlen_problem(q, v, g, cu_host, max_len, chunk, scale, variant, segments)
     total = int(cu_host[-1])
     n, K, HV, V = int(p.B), q.shape[-1], v.shape[-2], v.shape[-1]
     o = torch.empty(v.shape, device=v.device, dtype=v.dtype)
@@ -547,7 +547,7 @@ def backward_varlen(q, k, v, g, beta, cu_seqlens, h0, d_o, dh_final=None, *, chu
     cu_host = _host_cu(cu_seqlens)
     cu_dev = cu_seqlens if (isinstance(cu_seqlens, torch.Tensor) and cu_seqlens.is_cuda
                             and cu_seqlens.dtype == torch.int32 and cu_seqlens.is_contiguous()) else None
-    p = _varlen_problem(q, v, g, cu_host, max_len, chunk, scale, variant, segments)
+    p = varlen_problem(q, v, g, cu_host, max_len, chunk, scale, variant, segments)
     total = int(cu_host[-1])
     n, K, HV, V = int(p.B), q.shape[-1], v.shape[-2], v.shape[-1]
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)

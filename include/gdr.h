@@ -463,6 +463,7 @@ GDR_API gdr_status gdr_backward(const gdr_problem* p, const void* q, const void*
  * than C per sequence.  The CUDA-core forward and the backward use padded rows,
  * sequence s as row s of p, and run gdr_forward / gdr_backward on p: the work
  * is n * p->T tokens.
+ * p->segments is not used: every sequence is scanned whole.
  * workspace: at least gdr_varlen_*_workspace_bytes(p), 256-byte aligned, owned by the caller.
  */
 GDR_API size_t gdr_varlen_forward_workspace_bytes(const gdr_problem* p);

@@ -276,3 +276,16 @@ def test_varlen_workspace_size_formula(lib):
     bad = gdr.make_problem(3, 100, 2, 96, 64, 64)
     assert lib.gdr_varlen_forward_workspace_bytes(ctypes.byref(bad)) == 0
     assert lib.gdr_varlen_backward_workspace_bytes(ctypes.byref(bad)) == 0
+
+
+def test_varlen_ignores_segments(lib):
+    # every sequence is scanned whole: the problem's segment count changes nothing, not even when it would
+    # be invalid for the padded batch
+    base = gdr.make_problem(4, 4096, 2, 128, 128, 64, 1, False, segments=1)
+    for seg in (0, 3, 8):
+        p = gdr.make_problem(4, 4096, 2, 128, 128, 64, 1, False, segments=seg)
+        for fn in (lib.gdr_varlen_forward_workspace_bytes, lib.gdr_varlen_backward_workspace_bytes):
+            assert fn(ctypes.byref(p)) == fn(ctypes.byref(base)) > 0
+    assert lib.gdr_varlen_forward_workspace_bytes(None) == 0
+    assert lib.gdr_varlen_forward(None, None, None, 0, None, None, None, None, None, None, None, None, None, 0,
+                                  None) == 1

@@ -92,7 +92,7 @@ def test_varlen_forward_replays_in_a_graph():
     xs = [make_varlen_inputs(lengths, 2, 128, 128, io_dtype=torch.bfloat16, with_h0=True, seed=s) for s in (5, 6)]
     q, k, v, g, beta, h0 = (dev(t) for t in xs[0].tensors().values())
     cu_host, cu_dev = xs[0].cu, xs[0].cu.to("cuda")
-    p = gdr._varlen_problem(q, v, g, cu_host, None, 64, None, "auto", 0)
+    p = gdr.varlen_problem(q, v, g, cu_host, None, 64, None, "auto", 0)
     total = int(cu_host[-1])
     o = torch.empty_like(v)
     hf = torch.empty(len(lengths), 2, 128, 128, device="cuda")

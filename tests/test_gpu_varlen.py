@@ -35,7 +35,7 @@ def inputs(lengths, per_k, dtype, *, H=2, HV=None, K=64, V=64, seed=0):
 def gpu_forward(x, C, variant, *, device_cu=False, max_len=None):
     q, k, v, g, beta, h0 = (dev(t) for t in (x.q, x.k, x.v, x.g, x.beta, x.h0))
     cu = x.cu.to("cuda") if device_cu else x.cu
-    p = gdr._varlen_problem(q, v, g, x.cu, max_len, C, SCALE, variant, 0)
+    p = gdr.varlen_problem(q, v, g, x.cu, max_len, C, SCALE, variant, 0)
     n, K, HV, V = int(p.B), q.shape[-1], v.shape[-2], v.shape[-1]
     o = torch.full(v.shape, float("nan"), device="cuda", dtype=v.dtype)
     hf = torch.full((n, HV, K, V), float("nan"), device="cuda")

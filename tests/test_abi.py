@@ -247,7 +247,7 @@ def test_varlen_workspace_size_formula(lib):
     # device cu; on the tensor cores also the chunk offsets co [n + 1] and the chunk -> sequence map [NTmax],
     # NTmax = n ceil(T / C); then every working tensor (rows: NTmax C chunk-packed, n T padded), each
     # rounded up to 256 bytes; then the inner call's workspace (on the tensor cores the larger of the padded
-    # problem's and that of the largest chunk-packed problem, one row of NTmax chunks without segments)
+    # problem's and that of the largest chunk-packed problem, one row of NTmax chunks; neither segmented)
     r = lambda x: (x + 255) // 256 * 256
     for (n, T, H, HV, K, V, C, dt, per_k, variant) in [(3, 100, 2, 2, 64, 64, 64, 1, False, "auto"),
                                                        (5, 333, 1, 4, 128, 64, 32, 1, True, "auto"),
@@ -256,6 +256,7 @@ def test_varlen_workspace_size_formula(lib):
         mk = lambda B, T_, segments=0: gdr.make_problem(B, T_, H, K, V, C, dt, per_k, variant=variant,
                                                         HV=HV if HV != H else 0, segments=segments)
         p = mk(n, T)
+        p1 = mk(n, T, segments=1)      # the padded inner call: each sequence scanned whole
         e = 2 if dt else 4
         qk, vv, gg, bb = H * K * e, HV * V * e, HV * (K if per_k else 1) * 4, HV * e
         chunked = variant != "simt"
@@ -264,8 +265,8 @@ def test_varlen_workspace_size_formula(lib):
         head = r((n + 1) * 4) + (r((n + 1) * 4) + r(ntmax * 4) if chunked else 0)
         pad = lambda sizes: sum(r(rows * b) for b in sizes)
         big = mk(1, ntmax * C, segments=1)
-        fin = lib.gdr_forward_workspace_bytes(ctypes.byref(p))
-        bin_ = lib.gdr_backward_workspace_bytes(ctypes.byref(p))
+        fin = lib.gdr_forward_workspace_bytes(ctypes.byref(p1))
+        bin_ = lib.gdr_backward_workspace_bytes(ctypes.byref(p1))
         if chunked:
             fin = max(fin, lib.gdr_forward_workspace_bytes(ctypes.byref(big)))
             bin_ = max(bin_, lib.gdr_backward_workspace_bytes(ctypes.byref(big)))

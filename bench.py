@@ -382,9 +382,11 @@ def varlen_lengths(total: int):
 
 def time_varlen(args, wl, dev, flush, stream, world):
     """gdr_varlen_forward on the workload's B T tokens packed as VARLEN_MIX: one C-ABI call per step.
-    On the tensor cores it runs chunk-packed (the chunk map, the pack, the prepare, the scan and output
-    walking each sequence's chunks, the unpack); on the CUDA cores padded (the pack, gdr_forward on rows
-    as long as the longest sequence, the unpack)."""
+    On the fused path at 64-token chunks it runs chunk-packed with the packed tensors read and o written in
+    place (the chunk map, the prepare, the fused scan and output walking each sequence's chunks); on the
+    other tensor-core paths chunk-packed through copies (the pack, the prepare, the scan and output, the
+    unpack); on the CUDA cores padded (the pack, gdr_forward on rows as long as the longest sequence, the
+    unpack)."""
     lengths = varlen_lengths(wl.B * wl.T)
     x = make_varlen_inputs(lengths, wl.H, wl.K, wl.V, per_k_gate=wl.per_k_gate, io_dtype=wl.torch_dtype,
                            with_h0=wl.with_h0, seed=0)
@@ -406,7 +408,10 @@ def time_varlen(args, wl, dev, flush, stream, world):
     C = wl.chunk
     chunked = variant != "simt" and total > 0
     S = 1 if chunked else gdr.gdr_forward_segments(p)
-    if chunked:
+    if chunked and variant == "fused" and C == 64:   # q, k, v, g, beta read and o written in place
+        layout, working = "chunk-packed, read in place", sum(-(-n // C) * C for n in lengths)
+        launches = 3
+    elif chunked:
         layout, working = "chunk-packed", sum(-(-n // C) * C for n in lengths)
         launches = 3 + (2 if variant == "fused" else 3)
     else:

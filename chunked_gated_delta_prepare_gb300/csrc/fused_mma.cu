@@ -91,13 +91,18 @@ struct FLayout {
 // enough that the guards alone measured 4-7% slower where they are not needed.
 // co (packed variable-length sequences; NULL otherwise): one data row (B = 1) of whole-chunk runs,
 // sequence z = blockIdx.z on the chunks co[z] .. co[z+1]-1, from h0[z] to h_final[z].
+// pcu (with co and P; NULL otherwise): q, k and o are the caller's packed tensors [Tin, ...] rather than
+// the chunk-packed row; chunk c of sequence z reads q and k from packed row pcu[z] + c C, the rows past
+// the sequence's end in k are zeroed once they land (they hold the next sequence's tokens; their v' is
+// zero, but 0 * inf is not), and only o's rows inside the sequence are stored.
 template <int K, int C, bool HAS_P, bool GENERAL>
 __global__ void __launch_bounds__(FLayout<K, C, HAS_P>::kThreads, 1)
 fused_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap mk,
                          const __grid_constant__ CUtensorMap mu, const __grid_constant__ CUtensorMap mq,
                          const __grid_constant__ CUtensorMap mpk, const float* __restrict__ g_cum,
                          const float* __restrict__ h0, bf16* __restrict__ o, float* __restrict__ h_final,
-                         const int* __restrict__ co, int T, int H, int V, int G, float scale, unsigned int* err) {
+                         const int* __restrict__ co, const int* __restrict__ pcu, int Tin, int T, int H, int V, int G,
+                         float scale, unsigned int* err) {
     using L = FLayout<K, C, HAS_P>;
     constexpr int NSA = L::NSA, NSB = L::NSB, NOW = L::NOW, NT8 = L::NT8, KH = L::KH;
     constexpr int NJH = KH / 8;
@@ -113,6 +118,11 @@ fused_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_co
     const int c0 = co ? min(max(co[b], 0), NTall) : 0;
     const int NT = co ? min(max(co[b + 1], c0), NTall) - c0 : NTall;
     const int bd = co ? 0 : b;
+    // packed q, k, o: the sequence's first packed row and its length (clamped to the tensor and its chunks)
+    const bool packed = co && pcu;
+    const int in0 = packed ? min(max(pcu[b], 0), Tin) : 0;
+    const int len = packed ? min(min(max(pcu[b + 1] - in0, 0), Tin - in0), NT * C) : 0;
+    auto qk_row = [&](int c) -> int { return packed ? in0 + c * C : (c0 + c) * C; };
     const int hk = GENERAL ? h / G : h;                  // q/k head of value head h
     const int g = lane >> 2, q4 = lane & 3, mi = lane >> 3, mr = lane & 7;
     auto row = [&](int t) -> int64_t {                   // G past T: its last value
@@ -161,7 +171,7 @@ fused_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_co
 #pragma unroll
                 for (int a = 0; a < K / 64; ++a) {
                     bw::tma_load_4d(sm + L::W + s * L::kKC + a * C * 128, &mw, &fullA[s], a * 64, h, t0, bd);
-                    bw::tma_load_4d(sm + L::KB + s * L::kKC + a * C * 128, &mk, &fullA[s], a * 64, hk, t0, bd);
+                    bw::tma_load_4d(sm + L::KB + s * L::kKC + a * C * 128, &mk, &fullA[s], a * 64, hk, qk_row(c), bd);
                 }
                 bw::tma_load_4d(sm + L::U + s * L::kU, &mu, &fullA[s], v0, h, t0, bd);
                 sDec[s] = __expf(glc);
@@ -186,7 +196,7 @@ fused_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_co
                 bw::mbar_arrive_expect_tx(&fullB[s], L::tx_b);
 #pragma unroll
                 for (int a = 0; a < K / 64; ++a) {
-                    bw::tma_load_4d(sm + L::Q + s * L::kKC + a * C * 128, &mq, &fullB[s], a * 64, hk, t0, bd);
+                    bw::tma_load_4d(sm + L::Q + s * L::kKC + a * C * 128, &mq, &fullB[s], a * 64, hk, qk_row(c), bd);
                     if constexpr (!HAS_P)
                         bw::tma_load_4d(sm + L::PK + s * L::kPK + a * C * 128, &mpk, &fullB[s], a * 64, hk, t0, bd);
                 }
@@ -229,6 +239,19 @@ fused_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_co
             const uint32_t w_t = s_base + L::W + s * L::kKC;
             const uint32_t k_t = s_base + L::KB + s * L::kKC;
             const uint32_t u_t = s_base + L::U + s * L::kU;
+            if (packed && (c + 1) * C > len) {
+                // the sequence's last, partial chunk: every warp zeroes the k rows past its end itself
+                // (the same zeros), so each reads only zeros there; fenced before the slot goes back to TMA
+                const int first = max(len - c * C, 0);
+                unsigned char* kt = sm + L::KB + s * L::kKC;
+                for (int i = lane; i < (C - first) * (K / 8); i += 32) {
+                    const int r = first + i / (K / 8), u16 = i % (K / 8);
+                    *reinterpret_cast<uint4*>(kt + (u16 >> 3) * C * 128 + r * 128 + (u16 & 7) * 16) =
+                        make_uint4(0, 0, 0, 0);
+                }
+                bw::fence_async_shared();
+                __syncwarp();
+            }
 
             // partial D = h^T[:, my keys] w[:, my keys]^T  [16 x C]
             float D[NT8][4];
@@ -461,12 +484,13 @@ fused_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_co
                          : "memory");
         }
         __syncwarp();
-        bf16* dst = o + (((int64_t)bd * T + t0 + r0) * H + h) * V + v0;
+        bf16* dst = o + (((int64_t)bd * T + (packed ? in0 + c * C : t0) + r0) * H + h) * V + v0;
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
             const int rr = 8 * i + (lane >> 2), ch = lane & 3;
             const uint4 x = wm::lds128(os + sw64(rr, ch));
-            if (!GENERAL || t0 + r0 + rr < T) *reinterpret_cast<uint4*>(dst + (int64_t)rr * H * V + 8 * ch) = x;
+            const bool in = packed ? c * C + r0 + rr < len : (!GENERAL || t0 + r0 + rr < T);
+            if (in) *reinterpret_cast<uint4*>(dst + (int64_t)rr * H * V + 8 * ch) = x;
         }
         __syncwarp();
     }
@@ -475,12 +499,13 @@ fused_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_co
 
 template <int K, int C, bool HAS_P, bool GENERAL>
 cudaError_t launch_v(const Dims& d, const void* q, const void* k, const void* w, const void* u, const float* g_cum,
-                     const void* P, const float* h0, void* o, float* h_final, const int* co, int nseq, cudaStream_t s,
-                     unsigned int* err) {
+                     const void* P, const float* h0, void* o, float* h_final, const int* co, int nseq,
+                     const int* pcu, int Tin, cudaStream_t s, unsigned int* err) {
     using L = FLayout<K, C, HAS_P>;
     CUtensorMap mw, mk, mu, mq, mpk;
-    if (!make_tmap_tokens(&mw, w, d.B, d.T, d.H, K, C) || !make_tmap_tokens(&mk, k, d.B, d.T, d.Hk, K, C) ||
-        !make_tmap_tokens_sw64(&mu, u, d.B, d.T, d.H, d.V, C) || !make_tmap_tokens(&mq, q, d.B, d.T, d.Hk, K, C))
+    const int tq = pcu ? Tin : d.T;   // rows of q and k: the caller's packed tokens, or the data row
+    if (!make_tmap_tokens(&mw, w, d.B, d.T, d.H, K, C) || !make_tmap_tokens(&mk, k, d.B, tq, d.Hk, K, C) ||
+        !make_tmap_tokens_sw64(&mu, u, d.B, d.T, d.H, d.V, C) || !make_tmap_tokens(&mq, q, d.B, tq, d.Hk, K, C))
         return cudaErrorInvalidValue;
     if constexpr (HAS_P) {
         // P [B, NT, H, C, C] seen as (C, C, H, B*NT); one 64 x 64 box per chunk
@@ -496,35 +521,36 @@ cudaError_t launch_v(const Dims& d, const void* q, const void* k, const void* w,
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const dim3 grid(d.V / kBV, d.H, co ? nseq : d.B);
-    kern<<<grid, L::kThreads, smem, s>>>(mw, mk, mu, mq, mpk, g_cum, h0, (bf16*)o, h_final, co, d.T, d.H, d.V, d.G,
-                                         d.scale, err);
+    kern<<<grid, L::kThreads, smem, s>>>(mw, mk, mu, mq, mpk, g_cum, h0, (bf16*)o, h_final, co, pcu, Tin, d.T, d.H,
+                                         d.V, d.G, d.scale, err);
     return cudaGetLastError();
 }
 
 template <int K, int C, bool HAS_P>
 cudaError_t launch(const Dims& d, const void* q, const void* k, const void* w, const void* u, const float* g_cum,
-                   const void* P, const float* h0, void* o, float* h_final, const int* co, int nseq, cudaStream_t s,
-                   unsigned int* err) {
+                   const void* P, const float* h0, void* o, float* h_final, const int* co, int nseq,
+                   const int* pcu, int Tin, cudaStream_t s, unsigned int* err) {
     if (d.T % C != 0 || d.G != 1)
-        return launch_v<K, C, HAS_P, true>(d, q, k, w, u, g_cum, P, h0, o, h_final, co, nseq, s, err);
-    return launch_v<K, C, HAS_P, false>(d, q, k, w, u, g_cum, P, h0, o, h_final, co, nseq, s, err);
+        return launch_v<K, C, HAS_P, true>(d, q, k, w, u, g_cum, P, h0, o, h_final, co, nseq, pcu, Tin, s, err);
+    return launch_v<K, C, HAS_P, false>(d, q, k, w, u, g_cum, P, h0, o, h_final, co, nseq, pcu, Tin, s, err);
 }
 
 }  // namespace
 
 cudaError_t mma_scan_output(const Dims& d, const void* q, const void* k, const void* w, const void* u,
                             const float* g_cum, const void* P, const float* h0, void* o, float* h_final,
-                            cudaStream_t s, unsigned int* err, const int* co, int nseq) {
+                            cudaStream_t s, unsigned int* err, const int* co, int nseq, const int* pcu, int Tin) {
     if (!d.bf16 || d.per_k || (co && (d.B != 1 || nseq < 1))) return cudaErrorInvalidValue;
+    if (pcu && (!co || !P || Tin < 1)) return cudaErrorInvalidValue;
     if (P) {
         if (d.C != 64) return cudaErrorInvalidValue;
-        return d.K == 64 ? launch<64, 64, true>(d, q, k, w, u, g_cum, P, h0, o, h_final, co, nseq, s, err)
-                         : launch<128, 64, true>(d, q, k, w, u, g_cum, P, h0, o, h_final, co, nseq, s, err);
+        return d.K == 64 ? launch<64, 64, true>(d, q, k, w, u, g_cum, P, h0, o, h_final, co, nseq, pcu, Tin, s, err)
+                         : launch<128, 64, true>(d, q, k, w, u, g_cum, P, h0, o, h_final, co, nseq, pcu, Tin, s, err);
     }
-    if (d.K == 64) return d.C == 32 ? launch<64, 32, false>(d, q, k, w, u, g_cum, P, h0, o, h_final, co, nseq, s, err)
-                                    : launch<64, 64, false>(d, q, k, w, u, g_cum, P, h0, o, h_final, co, nseq, s, err);
-    return d.C == 32 ? launch<128, 32, false>(d, q, k, w, u, g_cum, P, h0, o, h_final, co, nseq, s, err)
-                     : launch<128, 64, false>(d, q, k, w, u, g_cum, P, h0, o, h_final, co, nseq, s, err);
+    if (d.K == 64) return d.C == 32 ? launch<64, 32, false>(d, q, k, w, u, g_cum, P, h0, o, h_final, co, nseq, pcu, Tin, s, err)
+                                    : launch<64, 64, false>(d, q, k, w, u, g_cum, P, h0, o, h_final, co, nseq, pcu, Tin, s, err);
+    return d.C == 32 ? launch<128, 32, false>(d, q, k, w, u, g_cum, P, h0, o, h_final, co, nseq, pcu, Tin, s, err)
+                     : launch<128, 64, false>(d, q, k, w, u, g_cum, P, h0, o, h_final, co, nseq, pcu, Tin, s, err);
 }
 
 }  // namespace gdr

@@ -959,6 +959,26 @@ gdr_status gdr_varlen_forward(const gdr_problem* p_in, const int32_t* cu_seqlens
     const gdr::RowCopy out[1] = {{base + ws.pad[5], o, rb[5]}};
     int64_t chunks = 0;   // the chunk-packed row's chunks, from the host lengths
     for (int64_t i = 0; i < d.B; ++i) chunks += ((int64_t)cu_seqlens[i + 1] - cu_seqlens[i] + d.C - 1) / d.C;
+    if (path == Path::Fused && d.C == 64 && chunk_packed_fits(d) && chunks > 0) {
+        // the fused path reads q, k, v, g, beta in place and writes o in place: no copies
+        int* co = reinterpret_cast<int*>(base + ws.co);
+        int* cs = reinterpret_cast<int*>(base + ws.cs);
+        const gdr::Dims d1 = chunk_packed(d, chunks);
+        const StagedWorkspace iw = plan_staged(d1, true, 1);
+        char* ib = base + ws.inner;
+        float* g_cum = reinterpret_cast<float*>(ib + iw.g_cum);
+        void *w = ib + iw.w, *u = ib + iw.u, *P = ib + iw.P;
+        unsigned int* err = device_error_word();
+        if ((st = from_cuda(gdr::varlen_plan(cu, d.B, total, d.C, (int)chunks, co, cs, s))) != GDR_OK) return st;
+        if ((st = from_cuda(gdr::mma_prepare_packed(d1, q, k, v, g, beta, w, u, g_cum, P, cu, co, cs, d.B, (int)total,
+                                                    s, err))) != GDR_OK)
+            return st;
+        if ((st = from_cuda(gdr::mma_scan_output(d1, q, k, w, u, g_cum, P, h0, o, h_final, s, err, co, d.B, cu,
+                                                 (int)total))) != GDR_OK)
+            return st;
+        t_last_variant = path_name(path);
+        return GDR_OK;
+    }
     if (path != Path::Simt && chunk_packed_fits(d) && chunks > 0) {
         int* co = reinterpret_cast<int*>(base + ws.co);
         int* cs = reinterpret_cast<int*>(base + ws.cs);

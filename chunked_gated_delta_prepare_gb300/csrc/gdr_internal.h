@@ -33,6 +33,13 @@ cudaError_t simt_output(const Dims& d, const void* q, const void* k, const void*
 cudaError_t mma_prepare(const Dims& d, const void* k, const void* v, const float* g, const void* beta, void* w,
                         void* u, float* g_cum, cudaStream_t s, unsigned int* err, const void* q = nullptr,
                         void* P = nullptr, void* tinv = nullptr);
+// The prepare with P (scalar gate, C = 64) on the chunk-packed row d (B = 1) of packed variable-length
+// sequences, reading q, k, v, g, beta in place from the caller's packed tensors of `total` tokens: chunk c of
+// the row is chunk c - co[s] of sequence s = cs[c] (cu, co, cs as varlen_plan makes them).  w, u, g_cum and
+// P fill the row as mma_prepare's would for the chunk-packed copy of the inputs.
+cudaError_t mma_prepare_packed(const Dims& d, const void* q, const void* k, const void* v, const float* g,
+                               const void* beta, void* w, void* u, float* g_cum, void* P, const int* cu,
+                               const int* co, const int* cs, int nseq, int total, cudaStream_t s, unsigned int* err);
 // the scan's recurrence runs on mma.sync (register-resident), see scan_mma.cu
 // co (packed variable-length sequences, else NULL): d has B = 1 and whole chunks; sequence z of nseq runs
 // the chunks co[z] .. co[z+1]-1 from h0[z] to h_final[z] (one CTA column per sequence)
@@ -55,7 +62,10 @@ cudaError_t tc_output(const Dims& d, const void* q, const void* k, const void* v
 // P: the prepare's [B, NT, H, C, C] tiles (C = 64), or NULL to compute q k^T in the kernel
 cudaError_t mma_scan_output(const Dims& d, const void* q, const void* k, const void* w, const void* u,
                             const float* g_cum, const void* P, const float* h0, void* o, float* h_final,
-                            cudaStream_t s, unsigned int* err, const int* co = nullptr, int nseq = 0);
+                            cudaStream_t s, unsigned int* err, const int* co = nullptr, int nseq = 0,
+                            const int* pcu = nullptr, int Tin = 0);
+// pcu, Tin (with co and P): q, k and o are the caller's packed tensors of Tin tokens, sequence z starting at
+// packed row pcu[z]; w, u, g_cum and P are the chunk-packed row's (see fused_mma.cu)
 
 // ---- backward stages on the CUDA cores (simt_backward.cu): every shape and io dtype;
 // intermediates fp32, see include/gdr.h for each stage's definition

@@ -137,13 +137,27 @@ constexpr float kExpSafe = 40.f;
 
 // EXTRA: grouped value heads (q/k head h / G) or the backward's T output.  The plain forward takes
 // the variant without either (its schedule measured slower with them compiled in).
-template <int K, int V, int C, bool PER_K, bool WITH_P, bool EXTRA>
+// PACKED (C = 64, packed variable-length sequences read in place): the outputs fill one row of whole
+// chunks (B = 1, T = NT C) as the chunk-packed layout places them, while q, k, v, g, beta are read from
+// the caller's packed tensors [total, ...]: chunk c of the row is chunk c - co[s] of sequence s = cs[c],
+// whose tokens start at cu[s].  Rows past the sequence's end are zero tokens: beta and g read as zero,
+// the k, q and v rows zeroed after they land (they hold the next sequence's tokens).
+struct PackedIn {
+    const int* cu;   // device int32 [n + 1]
+    const int* co;   // device int32 [n + 1]
+    const int* cs;   // device int32 [NT]
+    int n;
+    int total;
+};
+
+template <int K, int V, int C, bool PER_K, bool WITH_P, bool EXTRA, bool PACKED>
 __global__ void __launch_bounds__(128, 3)
 prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
                    const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap mu,
                    const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mp,
                    const float* __restrict__ g, const bf16* __restrict__ beta, float* __restrict__ g_cum,
-                   bf16* __restrict__ tinv, int T, int H, int G, unsigned int* err) {
+                   bf16* __restrict__ tinv, int T, int H, int G, PackedIn pin, unsigned int* err) {
+    static_assert(!PACKED || (C == kTile && !PER_K), "packed inputs: whole 64-token chunks, scalar gate");
     using L = PrepLayout<K, V, C, PER_K, WITH_P>;
     constexpr int GW = L::GW;
     extern __shared__ unsigned char smem_raw[];
@@ -158,8 +172,32 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int t0 = blockIdx.x * kTile, h = blockIdx.y, b = blockIdx.z;
     const int hk = EXTRA ? h / G : h;                 // q/k head of value head h
-    const int nvalid = min(kTile, T - t0);
+    const int nout = min(kTile, T - t0);             // rows of the outputs (g_cum) this tile writes
+    int nvalid = nout, t_in = t0, b_in = b, T_in = T; // input rows: how many are real tokens, and where
+    if constexpr (PACKED) {
+        const int c = t0 / C, sq = pin.cs[c];
+        nvalid = 0;
+        t_in = 0;
+        b_in = 0;
+        T_in = pin.total;
+        if (sq >= 0 && sq < pin.n && pin.co[sq] <= c && c < pin.co[sq + 1]) {
+            const int a = min(max(pin.cu[sq], 0), pin.total);
+            const int len = min(max(pin.cu[sq + 1] - a, 0), pin.total - a);
+            const int j = c - pin.co[sq];
+            t_in = a + j * C;
+            nvalid = min(max(len - j * C, 0), kTile);
+        }
+    }
     auto row = [&](int t) -> int64_t { return ((int64_t)b * T + t0 + t) * H + h; };
+    auto row_in = [&](int t) -> int64_t { return ((int64_t)b_in * T_in + t_in + t) * H + h; };
+    // rows nvalid.. of a [64][D] tile in the 128-byte swizzle (whole 128-byte rows of every atom) to zero
+    auto zero_rows = [&](uint32_t tile, int D, int first, int last, int id, int nthr) {
+        const int per = (last - first) * (D / 8);
+        for (int i = id; i < per; i += nthr) {
+            const int r = first + i / (D / 8), u16 = i % (D / 8);
+            *reinterpret_cast<uint4*>(sm + tile + (u16 >> 3) * 8192 + r * 128 + (u16 & 7) * 16) = make_uint4(0, 0, 0, 0);
+        }
+    };
     const uint32_t s_base = bw::smem_u32(sm);
 
     if (tid == 0) {
@@ -175,18 +213,18 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
         // k first (S = k k^T needs it at once), then q (P), then v (u, the last product)
         bw::mbar_arrive_expect_tx(&bar_k, K * 128);
 #pragma unroll
-        for (int a = 0; a < K / 64; ++a) bw::tma_load_4d(sm + L::kK + a * 8192, &mk, &bar_k, a * 64, hk, t0, b);
+        for (int a = 0; a < K / 64; ++a) bw::tma_load_4d(sm + L::kK + a * 8192, &mk, &bar_k, a * 64, hk, t_in, b_in);
         if constexpr (WITH_P) {
             bw::mbar_arrive_expect_tx(&bar_q, K * 128);
 #pragma unroll
-            for (int a = 0; a < K / 64; ++a) bw::tma_load_4d(sm + L::kQ + a * 8192, &mq, &bar_q, a * 64, hk, t0, b);
+            for (int a = 0; a < K / 64; ++a) bw::tma_load_4d(sm + L::kQ + a * 8192, &mq, &bar_q, a * 64, hk, t_in, b_in);
         }
         bw::mbar_arrive_expect_tx(&bar_v, V * 128);
 #pragma unroll
-        for (int a = 0; a < V / 64; ++a) bw::tma_load_4d(sm + L::kV + a * 8192, &mv, &bar_v, a * 64, h, t0, b);
+        for (int a = 0; a < V / 64; ++a) bw::tma_load_4d(sm + L::kV + a * 8192, &mv, &bar_v, a * 64, h, t_in, b_in);
     }
     // beta; g (rows past T read as zero)
-    for (int i = tid; i < kTile; i += 128) sB[i] = i < nvalid ? __bfloat162float(beta[row(i)]) : 0.f;
+    for (int i = tid; i < kTile; i += 128) sB[i] = i < nvalid ? __bfloat162float(beta[row_in(i)]) : 0.f;
     if constexpr (PER_K) {
         // 16-byte loads, all of a thread's issued before any is used (the tile is 32 KB at K = 128)
         constexpr int NV4 = kTile * GW / 4 / 128;
@@ -194,14 +232,14 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
 #pragma unroll
         for (int j = 0; j < NV4; ++j) {
             const int e = 4 * (tid + 128 * j), t = e / GW;
-            gv[j] = t < nvalid ? *reinterpret_cast<const float4*>(g + row(t) * GW + e % GW) : make_float4(0.f, 0.f, 0.f, 0.f);
+            gv[j] = t < nvalid ? *reinterpret_cast<const float4*>(g + row_in(t) * GW + e % GW) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
         for (int j = 0; j < NV4; ++j) *reinterpret_cast<float4*>(sG + 4 * (tid + 128 * j)) = gv[j];
     } else if (warp == 0) {
         // scalar gate: warp shuffle scan, lane l holds rows l and 32 + l
-        float x0 = lane < nvalid ? g[row(lane)] : 0.f;
-        float x1 = 32 + lane < nvalid ? g[row(32 + lane)] : 0.f;
+        float x0 = lane < nvalid ? g[row_in(lane)] : 0.f;
+        float x1 = 32 + lane < nvalid ? g[row_in(32 + lane)] : 0.f;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const float y0 = __shfl_up_sync(0xffffffffu, x0, o), y1 = __shfl_up_sync(0xffffffffu, x1, o);
@@ -212,8 +250,8 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
         sG[32 + lane] = x1;
         sE[lane] = __expf(x0);
         sE[32 + lane] = __expf(x1);
-        if (lane < nvalid) g_cum[row(lane)] = x0;
-        if (32 + lane < nvalid) g_cum[row(32 + lane)] = x1;
+        if (lane < nout) g_cum[row(lane)] = x0;
+        if (32 + lane < nout) g_cum[row(32 + lane)] = x1;
     }
     __syncthreads();
     // chunk-local inclusive cumsum (per-key-dim gate: one thread per key column)
@@ -224,13 +262,14 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
             for (int t = ch * C; t < ch * C + C; ++t) {
                 run += sG[t * K + d];
                 sG[t * K + d] = run;
-                if (t < nvalid) g_cum[row(t) * K + d] = run;
+                if (t < nout) g_cum[row(t) * K + d] = run;
             }
         }
         __syncthreads();
     }
 
     bool ok = bw::mbar_wait(&bar_k, 0, err, kDeviceErrTimeout);
+    if (PACKED && nvalid < kTile) zero_rows(L::kK, K, nvalid, kTile, tid, 128);   // a barrier follows
 
     if (PER_K) {
         // gated copies for S: Ka = k exp(G - G_ref), Kb = k exp(G_ref - G), G_ref = middle row of the chunk
@@ -305,6 +344,10 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
     }
     if constexpr (WITH_P) {
         ok = bw::mbar_wait(&bar_q, 0, err, kDeviceErrTimeout) && ok;
+        if (PACKED && nvalid < warp * 16 + 16) {   // this warp's own rows of q, which only it reads
+            zero_rows(L::kQ, K, max(nvalid, warp * 16), warp * 16 + 16, lane, 32);
+            __syncwarp();
+        }
         // P = tril_0(q k^T * exp(G_i - G_j)) for this warp's rows (key blocks past the diagonal are
         // zero and skipped) -> bf16 into the q tile's place (each warp overwrites only its own rows of
         // q, after reading them), as a [64][64] tile in the 128-byte swizzle; stored with w and u below
@@ -570,6 +613,10 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
     const uint32_t w_tile = PER_K ? L::kKa : L::kK;
     product_in_place(tw, s_base + w_tile, std::integral_constant<int, K>{});
     ok = bw::mbar_wait(&bar_v, 0, err, kDeviceErrTimeout) && ok;
+    if (PACKED && nvalid < kTile) {   // CTA-uniform
+        zero_rows(L::kV, V, nvalid, kTile, tid, 128);
+        __syncthreads();
+    }
     product_in_place(tu, s_base + L::kV, std::integral_constant<int, V>{});
     bw::fence_async_shared();
     __syncthreads();
@@ -585,14 +632,16 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
     }
 }
 
-template <int K, int V, int C, bool PER_K, bool WITH_P, bool EXTRA>
+template <int K, int V, int C, bool PER_K, bool WITH_P, bool EXTRA, bool PACKED = false>
 cudaError_t launch_prepare_v(const Dims& d, const void* q, const void* k, const void* v, const float* g,
                              const void* beta, void* w, void* u, float* g_cum, void* P, void* tinv, cudaStream_t s,
-                             unsigned int* err) {
+                             unsigned int* err, PackedIn pin = PackedIn{}) {
     using L = PrepLayout<K, V, C, PER_K, WITH_P>;
     CUtensorMap mk, mv, mw, mu, mq, mp;
-    // q and k have the Hk q/k heads; every other token tensor the H value heads
-    if (!make_tmap_tokens(&mk, k, d.B, d.T, d.Hk, K, kTile) || !make_tmap_tokens(&mv, v, d.B, d.T, d.H, V, kTile) ||
+    // q and k have the Hk q/k heads; every other token tensor the H value heads.  Packed inputs: one
+    // row of the caller's total tokens.
+    const int bi = PACKED ? 1 : d.B, ti = PACKED ? pin.total : d.T;
+    if (!make_tmap_tokens(&mk, k, bi, ti, d.Hk, K, kTile) || !make_tmap_tokens(&mv, v, bi, ti, d.H, V, kTile) ||
         !make_tmap_tokens(&mw, w, d.B, d.T, d.H, K, kTile) || !make_tmap_tokens(&mu, u, d.B, d.T, d.H, V, kTile))
         return cudaErrorInvalidValue;
     mq = mk;
@@ -602,16 +651,16 @@ cudaError_t launch_prepare_v(const Dims& d, const void* q, const void* k, const 
         const uint64_t dims[4] = {(uint64_t)C, (uint64_t)C, (uint64_t)d.H, (uint64_t)d.B * d.NT};
         const uint64_t st[3] = {(uint64_t)C * 2, (uint64_t)C * C * 2, (uint64_t)d.H * C * C * 2};
         const uint32_t box[4] = {64, 64, 1, 1};
-        if (!make_tmap_tokens(&mq, q, d.B, d.T, d.Hk, K, kTile) || !make_tmap_bf16_4d(&mp, P, dims, st, box))
+        if (!make_tmap_tokens(&mq, q, bi, ti, d.Hk, K, kTile) || !make_tmap_bf16_4d(&mp, P, dims, st, box))
             return cudaErrorInvalidValue;
     }
-    auto kern = prepare_mma_kernel<K, V, C, PER_K, WITH_P, EXTRA>;
+    auto kern = prepare_mma_kernel<K, V, C, PER_K, WITH_P, EXTRA, PACKED>;
     const size_t smem = L::bytes + 1024;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const dim3 grid((d.T + kTile - 1) / kTile, d.H, d.B);
     kern<<<grid, 128, smem, s>>>(mk, mv, mw, mu, mq, mp, g, (const bf16*)beta, g_cum, (bf16*)tinv, d.T, d.H, d.G,
-                                 err);
+                                 pin, err);
     return cudaGetLastError();
 }
 
@@ -641,7 +690,30 @@ cudaError_t pick_chunk(const Dims& d, const void* q, const void* k, const void* 
                      : pick_gate<K, V, 64>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err);
 }
 
+template <int K, int V>
+cudaError_t packed_prepare(const Dims& d, const void* q, const void* k, const void* v, const float* g,
+                           const void* beta, void* w, void* u, float* g_cum, void* P, cudaStream_t s,
+                           unsigned int* err, PackedIn pin) {
+    if (d.G != 1)
+        return launch_prepare_v<K, V, 64, false, true, true, true>(d, q, k, v, g, beta, w, u, g_cum, P, nullptr, s,
+                                                                   err, pin);
+    return launch_prepare_v<K, V, 64, false, true, false, true>(d, q, k, v, g, beta, w, u, g_cum, P, nullptr, s, err,
+                                                                pin);
+}
+
 }  // namespace
+
+cudaError_t mma_prepare_packed(const Dims& d, const void* q, const void* k, const void* v, const float* g,
+                               const void* beta, void* w, void* u, float* g_cum, void* P, const int* cu,
+                               const int* co, const int* cs, int nseq, int total, cudaStream_t s, unsigned int* err) {
+    if (!d.bf16 || d.per_k || d.C != 64 || d.B != 1 || !q || !P || !cu || !co || !cs || nseq < 1 || total < 1)
+        return cudaErrorInvalidValue;
+    const PackedIn pin{cu, co, cs, nseq, total};
+    if (d.K == 64 && d.V == 64) return packed_prepare<64, 64>(d, q, k, v, g, beta, w, u, g_cum, P, s, err, pin);
+    if (d.K == 64 && d.V == 128) return packed_prepare<64, 128>(d, q, k, v, g, beta, w, u, g_cum, P, s, err, pin);
+    if (d.K == 128 && d.V == 64) return packed_prepare<128, 64>(d, q, k, v, g, beta, w, u, g_cum, P, s, err, pin);
+    return packed_prepare<128, 128>(d, q, k, v, g, beta, w, u, g_cum, P, s, err, pin);
+}
 
 cudaError_t mma_prepare(const Dims& d, const void* k, const void* v, const float* g, const void* beta, void* w,
                         void* u, float* g_cum, cudaStream_t s, unsigned int* err, const void* q, void* P,

@@ -197,3 +197,19 @@ def test_varlen_many_short_sequences(per_k):
                           dhf.double().numpy(), 64, SCALE)
     for name, t in zip(("dq", "dk", "dv", "dg", "dbeta", "dh0"), got):
         assert scaled_err(t, ref[name]) <= BWD_TOL["bf16"], (name, scaled_err(t, ref[name]))
+
+
+@pytest.mark.parametrize("variant,C", [("fused", 64), ("fused", 32), ("tensor", 64)])
+def test_varlen_sequences_are_isolated_from_nonfinite_neighbours(variant, C):
+    # the fused path at C = 64 reads the packed tensors in place, so a sequence's last chunk sees the next
+    # sequence's tokens in its tail rows until they are zeroed: an inf or a NaN there must not leak
+    lengths = [100, 37, 70]
+    x = inputs(lengths, False, torch.bfloat16, H=2, K=128, V=128, seed=14)
+    o, hf, _ = gpu_forward(x, C, variant)
+    a, b = int(x.cu[1]), int(x.cu[2])
+    x.k[a:b] = float("nan")
+    x.q[a:b] = float("inf")
+    x.v[a:b] = float("nan")
+    o2, hf2, _ = gpu_forward(x, C, variant)
+    assert torch.equal(o2[:a], o[:a]) and torch.equal(o2[b:], o[b:])
+    assert torch.equal(hf2[0], hf[0]) and torch.equal(hf2[2], hf[2])

@@ -454,15 +454,16 @@ GDR_API gdr_status gdr_backward(const gdr_problem* p, const void* q, const void*
  * [total,H,K] io; v [total,HV,V] io; g [total,HV] or [total,HV,K] fp32; beta
  * [total,HV] io; o like v.  Per-sequence tensors keep the batched layouts:
  * h0, h_final, dh_final, dh0 [n,HV,K,V] fp32 (sequence s starts from h0[s]).
- * The call copies the sequences into a working layout in the workspace, fills
- * the rest with zero tokens (beta = 0, g = 0, q = k = v = 0: the state passes
- * unchanged and their outputs are dropped), computes, and copies each
- * sequence's results back.  The forward on the tensor cores (bf16 io) packs the
- * sequences as runs of whole chunks of one row, sequence s taking ceil(len_s / C)
- * chunks, and scans each run from h0[s]: the work is the real tokens plus fewer
- * than C per sequence.  The CUDA-core forward and the backward use padded rows,
- * sequence s as row s of p, and run gdr_forward / gdr_backward on p: the work
- * is n * p->T tokens.
+ * The sequences are computed in a working layout in the workspace, the rest of
+ * it zero tokens (beta = 0, g = 0, q = k = v = 0: the state passes unchanged and
+ * their outputs are dropped).  On the tensor cores (bf16 io) it is chunk-packed:
+ * one row of whole chunks, sequence s taking ceil(len_s / C) of them, each run
+ * scanned from h0[s]; the work is the real tokens plus fewer than C per
+ * sequence.  The fused forward at C = 64 reads q, k, v, g, beta and writes o in
+ * place; the other tensor-core paths copy the inputs into the row and the
+ * results back.  The CUDA-core paths use padded rows, sequence s as row s of p,
+ * through gdr_forward / gdr_backward on p: the work is n * p->T tokens.  A
+ * sequence's results never depend on another sequence's tokens, finite or not.
  * p->segments is not used: every sequence is scanned whole.
  * workspace: at least gdr_varlen_*_workspace_bytes(p), 256-byte aligned, owned by the caller.
  */

@@ -95,7 +95,7 @@ struct FLayout {
 // the chunk-packed row; chunk c of sequence z reads q and k from packed row pcu[z] + c C, the rows past
 // the sequence's end in k are zeroed once they land (they hold the next sequence's tokens; their v' is
 // zero, but 0 * inf is not), and only o's rows inside the sequence are stored.
-template <int K, int C, bool HAS_P, bool GENERAL>
+template <int K, int C, bool HAS_P, bool GENERAL, bool PACKED>
 __global__ void __launch_bounds__(FLayout<K, C, HAS_P>::kThreads, 1)
 fused_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap mk,
                          const __grid_constant__ CUtensorMap mu, const __grid_constant__ CUtensorMap mq,
@@ -119,7 +119,7 @@ fused_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_co
     const int NT = co ? min(max(co[b + 1], c0), NTall) - c0 : NTall;
     const int bd = co ? 0 : b;
     // packed q, k, o: the sequence's first packed row and its length (clamped to the tensor and its chunks)
-    const bool packed = co && pcu;
+    const bool packed = PACKED && co && pcu;   // compiled out of the batched variant
     const int in0 = packed ? min(max(pcu[b], 0), Tin) : 0;
     const int len = packed ? min(min(max(pcu[b + 1] - in0, 0), Tin - in0), NT * C) : 0;
     auto qk_row = [&](int c) -> int { return packed ? in0 + c * C : (c0 + c) * C; };
@@ -497,7 +497,7 @@ fused_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_co
     (void)ok;
 }
 
-template <int K, int C, bool HAS_P, bool GENERAL>
+template <int K, int C, bool HAS_P, bool GENERAL, bool PACKED>
 cudaError_t launch_v(const Dims& d, const void* q, const void* k, const void* w, const void* u, const float* g_cum,
                      const void* P, const float* h0, void* o, float* h_final, const int* co, int nseq,
                      const int* pcu, int Tin, cudaStream_t s, unsigned int* err) {
@@ -516,7 +516,7 @@ cudaError_t launch_v(const Dims& d, const void* q, const void* k, const void* w,
     } else {
         mpk = mk;
     }
-    auto kern = fused_scan_output_kernel<K, C, HAS_P, GENERAL>;
+    auto kern = fused_scan_output_kernel<K, C, HAS_P, GENERAL, PACKED>;
     const size_t smem = L::bytes + 1024;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -530,9 +530,19 @@ template <int K, int C, bool HAS_P>
 cudaError_t launch(const Dims& d, const void* q, const void* k, const void* w, const void* u, const float* g_cum,
                    const void* P, const float* h0, void* o, float* h_final, const int* co, int nseq,
                    const int* pcu, int Tin, cudaStream_t s, unsigned int* err) {
+    if constexpr (HAS_P) {   // packed q, k, o (pcu) only with P
+        if (pcu) {
+            if (d.T % C != 0 || d.G != 1)
+                return launch_v<K, C, true, true, true>(d, q, k, w, u, g_cum, P, h0, o, h_final, co, nseq, pcu, Tin, s,
+                                                        err);
+            return launch_v<K, C, true, false, true>(d, q, k, w, u, g_cum, P, h0, o, h_final, co, nseq, pcu, Tin, s,
+                                                     err);
+        }
+    }
     if (d.T % C != 0 || d.G != 1)
-        return launch_v<K, C, HAS_P, true>(d, q, k, w, u, g_cum, P, h0, o, h_final, co, nseq, pcu, Tin, s, err);
-    return launch_v<K, C, HAS_P, false>(d, q, k, w, u, g_cum, P, h0, o, h_final, co, nseq, pcu, Tin, s, err);
+        return launch_v<K, C, HAS_P, true, false>(d, q, k, w, u, g_cum, P, h0, o, h_final, co, nseq, nullptr, 0, s,
+                                                  err);
+    return launch_v<K, C, HAS_P, false, false>(d, q, k, w, u, g_cum, P, h0, o, h_final, co, nseq, nullptr, 0, s, err);
 }
 
 }  // namespace

@@ -109,3 +109,29 @@ def test_seq_len_override_keeps_the_problem_shape():
     assert (wl.T, wl.NT) == (100, 2)
     with pytest.raises(ValueError):
         workloads.THROUGHPUT.with_tokens(0)
+
+
+def test_varlen_mix_covers_every_token():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.varlen_lengths(32768) == bench.VARLEN_MIX
+    for total in (1, 100, 4096, 16384, 65536, 100003):
+        lengths = bench.varlen_lengths(total)
+        assert sum(lengths) == total and min(lengths) >= 0 and len(lengths) == len(bench.VARLEN_MIX)
+
+
+def test_varlen_problem_from_packed_tensors():
+    # the padded problem of a packed batch: B = sequences, T = the longest one (or the caller's row length)
+    import torch
+    from chunked_gated_delta_prepare_gb300 import gdr
+    from chunked_gated_delta_prepare_gb300.inputs import make_varlen_inputs
+    x = make_varlen_inputs([5, 0, 70, 12], 1, 64, 128, HV=2, per_k_gate=True, io_dtype=torch.bfloat16)
+    assert x.cu.tolist() == [0, 5, 5, 75, 87]
+    p = gdr.varlen_problem(x.q, x.v, x.g, x.cu, None, 64, None, "auto", 0)
+    assert (p.B, p.T, p.H, p.K, p.V, p.chunk, p.HV, p.gate, p.io_dtype) == (4, 70, 1, 64, 128, 64, 2, 1, 1)
+    p = gdr.varlen_problem(x.q, x.v, x.g, x.cu, 128, 64, None, "auto", 0)
+    assert p.T == 128
+    e = make_varlen_inputs([0, 0], 2, 64, 64)
+    assert gdr.varlen_problem(e.q, e.v, e.g, e.cu, None, 64, None, "auto", 0).T == 1   # no tokens: rows of one
+    with pytest.raises(ValueError):
+        gdr.varlen_problem(e.q, e.v, e.g, torch.tensor([0], dtype=torch.int32), None, 64, None, "auto", 0)

@@ -273,3 +273,20 @@ def test_fp16_io_refused_by_the_tensor_core_variants(variant):
     with pytest.raises(gdr.GdrError) as e:
         gpu_forward(x, 64, variant)
     assert e.value.status == 8
+
+
+@pytest.mark.parametrize("shape", [(2, 256, 2, 128, 128, 64), (1, 200, 3, 64, 64, 32)],
+                         ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("variant,dtype", [("tensor", torch.bfloat16), ("simt", torch.float32)])
+def test_constant_per_key_gate_is_the_scalar_gate(shape, variant, dtype):
+    # a per-key-dim gate equal over K is the scalar gate (the recurrence's decay is the same diagonal), so
+    # the KDA kernels on g broadcast over K match the GDN kernels on g, within the io dtype's bars
+    B, T, H, K, V, C = shape
+    x = make_inputs(B, T, H, K, V, io_dtype=dtype, with_h0=True, seed=31)
+    xk = GdrInputs(q=x.q, k=x.k, v=x.v, g=x.g[..., None].expand(B, T, H, K).contiguous(), beta=x.beta, h0=x.h0)
+    o, hf, ran = gpu_forward(x, C, variant)
+    ok_, hfk, ran_k = gpu_forward(xk, C, variant)
+    assert ran == ran_k == variant
+    io = io_name(dtype)
+    assert max_abs(ok_, o.double().cpu().numpy()) <= O_TOL[io]
+    assert rel_frob(hfk, hf.double().cpu().numpy()) <= H_TOL[io]

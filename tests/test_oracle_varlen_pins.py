@@ -133,3 +133,22 @@ def test_cu_must_start_at_zero_and_not_decrease():
     for bad in ([1, 4, 8], [0, 5, 4]):
         with pytest.raises(ValueError):
             run(d, np.array(bad), 16, 0.5)
+
+
+@pytest.mark.parametrize("per_k", [False, True])
+def test_backward_equal_lengths_are_the_chunked_batch(per_k):
+    # the packed reverse mode (the C adjoint per sequence) against the chunked numpy backward on the
+    # reshaped batch, a formulation it shares nothing with
+    from oracle import chunked_backward
+    L, n = 40, 3
+    d, cu = packed([L] * n, per_k, K=6, V=5, seed=10)
+    rng = np.random.default_rng(11)
+    do = rng.standard_normal(d["v"].shape)
+    dhf = rng.standard_normal(d["h0"].shape)
+    got = varlen.backward(d["q"], d["k"], d["v"], d["g"], d["beta"], cu, d["h0"], do, dhf, 16, 0.4)
+    batch = {nm: d[nm].reshape((n, L) + d[nm].shape[1:]) for nm in ("q", "k", "v", "g", "beta")}
+    ref = chunked_backward.backward_chunked(batch["q"], batch["k"], batch["v"], batch["g"], batch["beta"], d["h0"],
+                                            do.reshape((n, L) + do.shape[1:]), dhf, 16, 0.4)
+    for name in ("dq", "dk", "dv", "dg", "dbeta"):
+        np.testing.assert_allclose(got[name], ref[name].reshape(got[name].shape), atol=1e-9, err_msg=name)
+    np.testing.assert_allclose(got["dh0"], ref["dh0"], atol=1e-9)

@@ -135,3 +135,12 @@ def test_varlen_problem_from_packed_tensors():
     assert gdr.varlen_problem(e.q, e.v, e.g, e.cu, None, 64, None, "auto", 0).T == 1   # no tokens: rows of one
     with pytest.raises(ValueError):
         gdr.varlen_problem(e.q, e.v, e.g, torch.tensor([0], dtype=torch.int32), None, 64, None, "auto", 0)
+
+
+def test_host_cu_accepts_lists_and_tensors():
+    import torch
+    from chunked_gated_delta_prepare_gb300 import gdr
+    for cu in ([0, 3, 3, 10], torch.tensor([0, 3, 3, 10]), torch.tensor([0, 3, 3, 10], dtype=torch.int32)):
+        h = gdr._host_cu(cu)
+        assert h.dtype == torch.int32 and h.device.type == "cpu" and h.is_contiguous()
+        assert h.tolist() == [0, 3, 3, 10]

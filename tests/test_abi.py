@@ -290,3 +290,39 @@ def test_varlen_ignores_segments(lib):
     assert lib.gdr_varlen_forward_workspace_bytes(None) == 0
     assert lib.gdr_varlen_forward(None, None, None, 0, None, None, None, None, None, None, None, None, None, 0,
                                   None) == 1
+
+
+def test_header_is_plain_c_and_a_c_program_links(lib, tmp_path):
+    # the boundary is a C ABI: a C99 program includes gdr.h, links libgdr and calls the host-only entry
+    # points (no device is touched: version, status text, workspace sizes, a validation error)
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use_gdr.c"
+    src.write_text(r"""
+#include <stdio.h>
+#include <string.h>
+#include "gdr.h"
+int main(void) {
+    gdr_problem p;
+    memset(&p, 0, sizeof p);
+    p.B = 2; p.T = 256; p.H = 4; p.K = 128; p.V = 128; p.chunk = 64;
+    p.io_dtype = GDR_BF16; p.gate = GDR_GATE_SCALAR; p.scale = -1.f; p.variant = GDR_VARIANT_AUTO;
+    if (gdr_version() <= 0) return 1;
+    if (gdr_forward_workspace_bytes(&p) == 0 || gdr_backward_workspace_bytes(&p) == 0) return 2;
+    if (gdr_varlen_forward_workspace_bytes(&p) == 0) return 3;
+    if (gdr_forward(&p, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, 0, NULL) != GDR_ERR_NULL) return 4;
+    p.K = 96;
+    if (gdr_forward_workspace_bytes(&p) != 0) return 5;
+    printf("%s\n", gdr_status_string(GDR_ERR_SHAPE));
+    return 0;
+}
+""")
+    libdir = os.path.dirname(gdr.LIB_PATH)
+    exe = tmp_path / "use_gdr"
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), str(src), "-L", libdir,
+                    "-lgdr", "-Wl,-rpath," + libdir, "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert out.returncode == 0, (out.returncode, out.stderr)
+    assert out.stdout.strip() == gdr.gdr_status_string(2)

@@ -326,3 +326,17 @@ int main(void) {
     out = subprocess.run([str(exe)], capture_output=True, text=True)
     assert out.returncode == 0, (out.returncode, out.stderr)
     assert out.stdout.strip() == gdr.gdr_status_string(2)
+
+
+def test_library_exports_only_the_c_abi(lib):
+    # every exported function of libgdr is a gdr_* entry point the header declares; the rest of the library
+    # (kernels, launchers, the CUDA runtime) stays hidden.  C++ runtime template statics (mangled _ZZ...) are
+    # emitted weak by the compiler and are not part of the interface.
+    import shutil
+    import subprocess
+    if shutil.which("nm") is None:
+        pytest.skip("no nm")
+    out = subprocess.run(["nm", "-D", "--defined-only", gdr.LIB_PATH], capture_output=True, text=True, check=True)
+    names = [ln.split()[-1] for ln in out.stdout.splitlines() if ln.strip()]
+    exported = {n for n in names if not n.startswith("_ZZ")}
+    assert exported == set(declared_functions())

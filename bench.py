@@ -6,9 +6,11 @@
 One step = one whole forward (gate cumsum, WY prepare, state scan, chunk output)
 over one batch of the 32k-token GDN workload (B=1, T=32768, H=32, K=V=128, C=64,
 bf16 io, fp32 state, h0 ~ N(0, 0.02)), inputs already resident in HBM.  Each
-timed step is bracketed by CUDA events on the launching stream; a 256 MiB
-buffer (about twice the L2) is overwritten before every timed step, outside the
-events.  Rank 0 prints one JSON line.
+timed step is one gdr_forward call bracketed by CUDA events on the launching
+stream; a 256 MiB buffer (about twice the L2) is overwritten before every timed
+step, outside the events.  A separate pass calls the same kernels one by one
+through their stage entry points to split the step by kernel.  Rank 0 prints
+one JSON line.
 
 The same line carries two more legs on the same workload: "backward" (the
 gradient of o and h_final, stage by stage) and "varlen" (the workload's tokens
@@ -87,6 +89,17 @@ def algorithmic_bytes(wl, kernel: str, with_p: bool = False, segs: int = 1) -> i
         per = 2 * K * e + 2 * V * e + gw + e
         return th * per + bh * state
     raise ValueError(kernel)
+
+
+def overlap_pieces(wl, variant: str, segments: int) -> int:
+    """Pieces gdr_forward cuts one sequence into on the tcgen05 fused path (the library's rule: B = 1, no
+    segments, pieces of at least 64 chunks and at most 16 of them); 1 when it does not."""
+    if variant != "fused_tc" or segments != 1 or wl.B != 1:
+        return 1
+    NT = wl.NT
+    per = max(64, -(-NT // 16))
+    n = -(-NT // per)
+    return n if n >= 2 else 1
 
 
 class ClockSampler:
@@ -496,7 +509,8 @@ def run_ours(args, wl):
     gdr.gdr_forward(p, q, k, v, g, beta, h0, o, hf, ws if nbytes else None, nbytes)
     torch.cuda.synchronize()
     variant = gdr.gdr_last_variant()
-    staged = variant != "fused"
+    fused = variant in ("fused", "fused_tc")
+    staged = not fused
     P = None
     # the segment-parallel scan (S > 1): every segment's map, the stitch, then the scan of all
     # segments at once on the view of B S sequences of T / S tokens
@@ -512,7 +526,7 @@ def run_ours(args, wl):
         seg_calls = [lambda: gdr.gdr_scan_transfer(sp, k, w, u, g_cum, S, M, Z),
                      lambda: gdr.gdr_scan_combine(sp, S, M, Z, h0, starts, hf)]
         del Hk
-    if variant == "fused":
+    if fused:
         # the two kernels gdr_forward runs on this path, called one by one so each can be timed
         g_cum = torch.empty_like(g)
         w = torch.empty_like(k)
@@ -548,6 +562,35 @@ def run_ours(args, wl):
                 [scan, lambda: gdr.gdr_chunk_output(sp, q, k, v_new, h_ckpt, g_cum, o)]
         del e
 
+    # The headline: one gdr_forward call per step, events on the launching stream around it.
+    def forward_call():
+        gdr.gdr_forward(p, q, k, v, g, beta, h0, o, hf, ws if nbytes else None, nbytes)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        forward_call()
+    torch.cuda.synchronize()
+    assert gdr.gdr_get_device_status() == 0
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for s in range(args.steps):
+            flush.fill_(s & 0xFF)
+            evs[s][0].record(stream)
+            forward_call()
+            evs[s][1].record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    status = gdr.gdr_get_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed region")
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    total_s = max_over_ranks(sum(step_ms) / 1e3, world)
+    value = weak_scaling_throughput(world, B * T, args.steps, total_s)
+
+    # The split: the same kernels gdr_forward launches, called one by one through their stage entry
+    # points in a separate timed pass, so each kernel's share of the step can be read.
     calls = launches()
     stage_variant = []
     for f in calls:
@@ -559,42 +602,38 @@ def run_ours(args, wl):
             f()
     torch.cuda.synchronize()
     assert gdr.gdr_get_device_status() == 0
-
     n = len(calls)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)] for _ in range(args.steps)]
-    barrier(world)
+    split_steps = max(3, min(args.steps, 10))
+    sevs = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)] for _ in range(split_steps)]
     torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        for s in range(args.steps):
-            flush.fill_(s & 0xFF)
-            evs[s][0].record(stream)
-            for i, f in enumerate(calls):
-                f()
-                evs[s][i + 1].record(stream)
-        torch.cuda.synchronize()
-    barrier(world)
-    status = gdr.gdr_get_device_status()
-    if status != 0:
-        raise RuntimeError(f"device status {status} after the timed region")
-    per_kernel_ms = [0.0] * n
-    step_ms = []
-    for s in range(args.steps):
-        step_ms.append(evs[s][0].elapsed_time(evs[s][n]))
-        for i in range(n):
-            per_kernel_ms[i] += evs[s][i].elapsed_time(evs[s][i + 1])
-    total_s = max_over_ranks(sum(step_ms) / 1e3, world)
-    value = weak_scaling_throughput(world, B * T, args.steps, total_s)
+    for s in range(split_steps):
+        flush.fill_(s & 0xFF)
+        sevs[s][0].record(stream)
+        for i, f in enumerate(calls):
+            f()
+            sevs[s][i + 1].record(stream)
+    torch.cuda.synchronize()
+    if gdr.gdr_get_device_status() != 0:
+        raise RuntimeError("device status set after the split pass")
+    avg_ms = [sum(sevs[s][i].elapsed_time(sevs[s][i + 1]) for s in range(split_steps)) / split_steps
+              for i in range(n)]
+    split_step_ms = sum(sevs[s][0].elapsed_time(sevs[s][n]) for s in range(split_steps)) / split_steps
 
-    # roofline of the dominant kernel
+    pieces = overlap_pieces(wl, variant, S)
+
+    # Roofline of the dominant kernel.  "achieved" counts the forward's algorithmic bytes (the I/O
+    # floor: q, k, v, g, beta read once, o written once, the state in and out) over that kernel's
+    # average launch time; "frac_own_io" counts instead the bytes that kernel itself must move in this
+    # kernel split (its inputs and outputs, intermediates included).
     hbm_gbs, _, peak_kind = peaks()
-    avg_ms = [t / args.steps for t in per_kernel_ms]
     dom = max(range(n), key=lambda i: avg_ms[i])
     dom_name = kernels[dom]
-    dom_bytes = algorithmic_bytes(wl, dom_name, with_p=variant == "fused" and P is not None, segs=S)
-    achieved = dom_bytes / (avg_ms[dom] / 1e3) / 1e9
+    floor_bytes = algorithmic_bytes(wl, "forward")
+    own_bytes = algorithmic_bytes(wl, dom_name, with_p=fused and P is not None, segs=S)
+    achieved = floor_bytes / (avg_ms[dom] / 1e3) / 1e9
     kname = {"prepare": "prepare_mma_kernel", "scan": "scan_mma_kernel", "output": "tc_output_kernel",
-             "scan_output": "fused_scan_output_kernel", "transfer": "scan_mma_kernel<transfer>",
-             "combine": "segment_combine_kernel"}[dom_name]
+             "scan_output": "tc_scan_output_kernel" if variant == "fused_tc" else "fused_scan_output_kernel",
+             "transfer": "scan_mma_kernel<transfer>", "combine": "segment_combine_kernel"}[dom_name]
     if stage_variant[dom] == "simt":
         kname = f"simt_{dom_name}_kernel"
     traffic = traffic_for(kname, wl.name)
@@ -634,15 +673,20 @@ def run_ours(args, wl):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.io == "bf16" else "f32",
             "data": "synthetic (seeded; q,k unit-norm, v N(0,1), beta sigmoid, g logsigmoid/16)",
             "config": dict(wl.describe(), variant=variant, l2="256 MiB buffer overwritten before every timed step",
-                           kernels_per_step=n, segments=S),
+                           kernels_per_step=2 * pieces if pieces > 1 else n, segments=S, pieces=pieces),
             "roofline": {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
                          "frac": achieved / hbm_gbs, "peak_source": f"{peak_kind} HBM copy bandwidth",
-                         "traffic": traffic, "algorithmic_bytes_per_launch": dom_bytes,
-                         "avg_launch_ms": avg_ms[dom]},
+                         "traffic": traffic, "algorithmic_bytes_per_launch": floor_bytes,
+                         "algorithmic_bytes": "the forward's I/O floor (q, k, v, g, beta, h0 in; o, h_final out)",
+                         "avg_launch_ms": avg_ms[dom],
+                         "frac_own_io": own_bytes / (avg_ms[dom] / 1e3) / 1e9 / hbm_gbs,
+                         "own_io_bytes_per_launch": own_bytes},
             "kernel_ms": {f"{kernels[i]}[{stage_variant[i]}]": avg_ms[i] for i in range(n)},
-            "floor_roofline_frac": (algorithmic_bytes(wl, "forward") / (hbm_gbs * 1e9)) / (total_s / args.steps),
+            "split_ms_per_step": split_step_ms,
+            "floor_roofline_frac": (floor_bytes / (hbm_gbs * 1e9)) / (total_s / args.steps),
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": n * args.steps,
+            "gpu_launches": (2 * pieces if pieces > 1 else n) * args.steps,
+            "timed": "events around one gdr_forward call per step; kernel_ms from a separate pass of its stage calls",
             "clocks": clk.summary(),
         }
         if bwd is not None:

@@ -21,6 +21,13 @@
 //  * The first call on each device looks up the array's device address (with
 //    that device current) and caches it.  Make that first call before any
 //    stream capture begins on the calling thread.
+//  * The cached address lives as long as the device's primary context.  After a
+//    cudaDeviceReset (or any other teardown of that context) the array is a new
+//    allocation and the cached address is stale: a process that resets a device
+//    must not call this entry point on that device again.
+//  * Variant AUTO runs what gdr_forward's AUTO runs when the fused path is left
+//    out: the tensor-core stages for bf16 io, the CUDA-core stages for fp32 and
+//    fp16 io.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -56,9 +63,11 @@ extern "C" gdr_status gdr_forward_static_scratch(const gdr_problem* p, const voi
                                                  const float* g, const void* beta, const float* h0, void* o,
                                                  float* h_final, void* stream) {
     if (!p) return GDR_ERR_NULL;
-    if (p->variant == GDR_VARIANT_FUSED) return GDR_ERR_UNSUPPORTED;  // only the staged variants are offered here
+    if (p->variant == GDR_VARIANT_FUSED || p->variant == GDR_VARIANT_FUSED_TC)
+        return GDR_ERR_UNSUPPORTED;   // only the staged variants are offered here
     gdr_problem staged = *p;
-    if (staged.variant == GDR_VARIANT_AUTO) staged.variant = GDR_VARIANT_SIMT;
+    if (staged.variant == GDR_VARIANT_AUTO)
+        staged.variant = staged.io_dtype == GDR_BF16 ? GDR_VARIANT_TENSOR : GDR_VARIANT_SIMT;
     const size_t need = gdr_forward_workspace_bytes(&staged);
     if (need == 0) {
         // the problem itself is invalid: let gdr_forward report why, launching nothing

@@ -68,12 +68,13 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Waits for the phase with the given parity to complete.  On giving up, sets
-// *err (if not already set) and returns false.
+// Waits for the phase with the given parity to complete, polling at most `limit`
+// times.  On giving up, sets *err (if not already set) and returns false.
 // Every 4096 failed polls it also looks at *err: once any wait of the launch has
 // given up, the others stop waiting too instead of each running out its own limit.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* err, unsigned int code) {
-    for (uint32_t i = 0; i < kMaxPolls; ++i) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* err, unsigned int code,
+                                          uint32_t limit = kMaxPolls) {
+    for (uint32_t i = 0; i < limit; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 4095u) == 4095u && err && *reinterpret_cast<volatile unsigned int*>(err) != 0u) return false;
     }

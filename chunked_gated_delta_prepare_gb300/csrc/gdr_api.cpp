@@ -3,6 +3,7 @@
 // every step runs in the kernels.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -34,7 +35,7 @@ gdr_status check_problem(const gdr_problem* p, gdr::Dims* d) {
     if (p->T > INT32_MAX || HV > kMaxGridYZ || p->B * (p->V / 32) > kMaxGridYZ) return GDR_ERR_SHAPE;
     if (p->B > INT32_MAX / p->T || p->B * p->T > INT32_MAX / HV) return GDR_ERR_SHAPE;
     if (std::isnan(p->scale) || std::isinf(p->scale)) return GDR_ERR_ARG;
-    if (p->variant < GDR_VARIANT_AUTO || p->variant > GDR_VARIANT_FUSED) return GDR_ERR_ARG;
+    if (p->variant < GDR_VARIANT_AUTO || p->variant > GDR_VARIANT_FUSED_TC) return GDR_ERR_ARG;
     if (p->segments < 0) return GDR_ERR_ARG;
     d->B = (int)p->B;
     d->T = (int)p->T;
@@ -70,6 +71,7 @@ gdr_status pick_stage(const gdr_problem* p, const gdr::Dims& d, bool* tensor) {
         case GDR_VARIANT_SIMT: *tensor = false; return GDR_OK;
         case GDR_VARIANT_TENSOR:
         case GDR_VARIANT_FUSED:
+        case GDR_VARIANT_FUSED_TC:
             if (!d.bf16) return GDR_ERR_UNSUPPORTED;
             *tensor = true;
             return GDR_OK;
@@ -78,7 +80,11 @@ gdr_status pick_stage(const gdr_problem* p, const gdr::Dims& d, bool* tensor) {
     }
 }
 
-enum class Path { Simt, Tensor, Fused };
+enum class Path { Simt, Tensor, Fused, FusedTc };
+
+constexpr int kSmCount = 152;   // GB300
+constexpr int kPieceChunks = 64;   // the overlapped forward's chunks per piece, at least
+bool segments_apply(const gdr_problem* p, const gdr::Dims& d);
 
 // The path a whole forward takes: SIMT (fp32 CUDA-core kernels for every stage),
 // TENSOR (the three bf16 tensor-core stage kernels) or FUSED (the bf16 prepare,
@@ -94,19 +100,38 @@ gdr_status pick_forward(const gdr_problem* p, const gdr::Dims& d, Path* path) {
             if (!d.bf16 || d.per_k) return GDR_ERR_UNSUPPORTED;
             *path = Path::Fused;
             return GDR_OK;
+        case GDR_VARIANT_FUSED_TC:
+            if (!gdr::tc_scan_output_supported(d)) return GDR_ERR_UNSUPPORTED;
+            *path = Path::FusedTc;
+            return GDR_OK;
         case GDR_VARIANT_AUTO:
             // bf16 with a scalar gate and 64-token chunks: FUSED (its prepare also writes the gated
             // scores, so scan and output run as one kernel) measures fastest; other bf16 problems
             // take the staged tensor-core kernels; fp32 the exact CUDA-core path
+            // The tcgen05 form of the fused kernel (see fused_tc.cu) when the warp-level one would need
+            // more than one wave of the GPU, or for one long sequence scanned whole, which it runs in
+            // pieces overlapped with the prepare (see forward_tc_overlapped).
             if (!d.bf16) *path = Path::Simt;
-            else if (!d.per_k && d.C == 64) *path = Path::Fused;
+            else if (!d.per_k && d.C == 64)
+                *path = gdr::tc_scan_output_supported(d) &&
+                                ((int64_t)d.B * d.H * (d.V / 32) > kSmCount || (d.B == 1 && d.NT >= 2 * kPieceChunks &&
+                                                                                 !segments_apply(p, d)))
+                            ? Path::FusedTc
+                            : Path::Fused;
             else *path = Path::Tensor;
             return GDR_OK;
         default: return GDR_ERR_UNSUPPORTED;
     }
 }
 
-const char* path_name(Path p) { return p == Path::Simt ? "simt" : (p == Path::Tensor ? "tensor" : "fused"); }
+const char* path_name(Path p) {
+    switch (p) {
+        case Path::Simt: return "simt";
+        case Path::Tensor: return "tensor";
+        case Path::Fused: return "fused";
+        default: return "fused_tc";
+    }
+}
 
 unsigned int* device_error_word() {
     unsigned int* p = nullptr;
@@ -130,7 +155,6 @@ gdr::Dims segment_view(const gdr::Dims& d, int S) {
 // (0): when the serial scan's grid, B HV V/32 CTAs, fills less than half the GPU, the largest
 // divisor of NT that keeps the segmented grid within one wave of 152 SMs and every segment at least
 // kSegMinChunks chunks long.  The CUDA-core path is never segmented.
-constexpr int kSmCount = 152;
 constexpr int kSegMinChunks = 16;
 
 gdr_status resolve_segments(const gdr_problem* p, const gdr::Dims& d, bool tensor, int* S) {
@@ -152,13 +176,19 @@ gdr_status resolve_segments(const gdr_problem* p, const gdr::Dims& d, bool tenso
     return GDR_OK;
 }
 
+// Whether the tensor-core paths would scan this problem in segments (resolve_segments with S > 1).
+bool segments_apply(const gdr_problem* p, const gdr::Dims& d) {
+    int S = 1;
+    return resolve_segments(p, d, true, &S) == GDR_OK && S > 1;
+}
+
 // gdr_forward scratch: g_cum, w, u and (staged paths) v_new, h_ckpt, (S > 1) the segment maps and
 // starts, each 256-byte aligned.
 struct StagedWorkspace {
-    size_t g_cum, w, u, v_new, h_ckpt, P, seg_m, seg_z, seg_h, total;
+    size_t g_cum, w, u, v_new, h_ckpt, P, seg_m, seg_z, seg_h, carry, total;
 };
 
-StagedWorkspace plan_staged(const gdr::Dims& d, bool fused, int S) {
+StagedWorkspace plan_staged(const gdr::Dims& d, bool fused, int S, int pieces = 1) {
     const size_t e = (d.bf16 || d.f16) ? 2 : 4;
     const size_t rows = (size_t)d.B * d.T * d.H;
     StagedWorkspace ws;
@@ -183,8 +213,59 @@ StagedWorkspace plan_staged(const gdr::Dims& d, bool fused, int S) {
         ws.seg_h = round_up(ws.seg_z + maps * d.V * 4, 256);
         off = round_up(ws.seg_h + maps * d.V * 4, 256);
     }
+    ws.carry = off;
+    if (pieces > 1)   // the state between pieces of the overlapped forward, [pieces - 1][B, H, K, V] fp32
+        off = round_up(off + (size_t)(pieces - 1) * d.B * d.H * d.K * d.V * 4, 256);
     ws.total = off;
     return ws;
+}
+
+// ---------------------------------------------------------------- the overlapped tcgen05 forward
+// One long sequence on the tcgen05 fused path (B = 1, no segments) runs in pieces of whole chunks on
+// the caller's stream: prepare(0), scan(0), prepare(1), scan(1), ...  Each prepare after the first is
+// launched as the programmatic dependent of the scan before it: once every scan CTA holds its SM (one
+// per head) the next piece's prepare starts on the SMs left free and overlaps the scan.  Each scan is
+// an ordinary launch, so it starts after its own piece's prepare and the previous scan; the state
+// passes between pieces in fp32 through the workspace.
+constexpr int kMaxPieces = 16;
+
+int overlap_pieces(const gdr::Dims& d, Path path, int S) {
+    if (path != Path::FusedTc || S != 1 || d.B != 1) return 1;
+    const int per = std::max(kPieceChunks, (d.NT + kMaxPieces - 1) / kMaxPieces);
+    const int n = (d.NT + per - 1) / per;
+    return n >= 2 ? n : 1;
+}
+
+gdr_status forward_tc_overlapped(const gdr::Dims& d, int pieces, const StagedWorkspace& ws, char* base, const void* q,
+                                 const void* k, const void* v, const float* g, const void* beta, const float* h0,
+                                 void* o, float* h_final, cudaStream_t s, unsigned int* err) {
+    const int per = (d.NT + pieces - 1) / pieces;
+    const size_t e = 2;                                 // bf16
+    float* carry = reinterpret_cast<float*>(base + ws.carry);
+    const size_t state = (size_t)d.H * d.K * d.V;
+    for (int i = 0; i < pieces; ++i) {
+        const int c0 = i * per, c1 = std::min(d.NT, c0 + per);
+        const int64_t t0 = (int64_t)c0 * d.C, t1 = std::min<int64_t>(d.T, (int64_t)c1 * d.C);
+        gdr::Dims dp = d;
+        dp.T = (int)(t1 - t0);
+        dp.NT = c1 - c0;
+        const char* qp = static_cast<const char*>(q) + (size_t)t0 * d.Hk * d.K * e;
+        const char* kp = static_cast<const char*>(k) + (size_t)t0 * d.Hk * d.K * e;
+        const char* vp = static_cast<const char*>(v) + (size_t)t0 * d.H * d.V * e;
+        const char* bp = static_cast<const char*>(beta) + (size_t)t0 * d.H * e;
+        const float* gp = g + t0 * d.H;
+        float* g_cum = reinterpret_cast<float*>(base + ws.g_cum) + t0 * d.H;
+        char* w = base + ws.w + (size_t)t0 * d.H * d.K * e;
+        char* u = base + ws.u + (size_t)t0 * d.H * d.V * e;
+        char* P = base + ws.P + (size_t)c0 * d.H * d.C * d.C * e;
+        char* op = static_cast<char*>(o) + (size_t)t0 * d.H * d.V * e;
+        const float* hin = i == 0 ? h0 : carry + (size_t)(i - 1) * state;
+        float* hout = i == pieces - 1 ? h_final : carry + (size_t)i * state;
+        cudaError_t ce = gdr::mma_prepare(dp, kp, vp, gp, bp, w, u, g_cum, s, err, qp, P, nullptr, i > 0);
+        if (ce == cudaSuccess) ce = gdr::tc_scan_output(dp, qp, kp, w, u, g_cum, P, hin, op, hout, s, err);
+        if (ce != cudaSuccess) return GDR_ERR_CUDA;
+    }
+    return GDR_OK;
 }
 
 // gdr_backward scratch: the forward's g_cum, w, u, v_new, h_ckpt (io dtype), then the
@@ -498,7 +579,7 @@ size_t gdr_forward_workspace_bytes(const gdr_problem* p) {
     Path path;
     int S = 1;
     if (pick_forward(p, d, &path) != GDR_OK || resolve_segments(p, d, path != Path::Simt, &S) != GDR_OK) return 0;
-    return plan_staged(d, path == Path::Fused, S).total;
+    return plan_staged(d, path == Path::Fused || path == Path::FusedTc, S, overlap_pieces(d, path, S)).total;
 }
 
 int gdr_forward_segments(const gdr_problem* p) {
@@ -521,7 +602,8 @@ gdr_status gdr_forward(const gdr_problem* p, const void* q, const void* k, const
     if ((st = pick_forward(p, d, &path)) != GDR_OK) return st;
     int S = 1;
     if ((st = resolve_segments(p, d, path != Path::Simt, &S)) != GDR_OK) return st;
-    const StagedWorkspace ws = plan_staged(d, path == Path::Fused, S);
+    const int pieces = overlap_pieces(d, path, S);
+    const StagedWorkspace ws = plan_staged(d, path == Path::Fused || path == Path::FusedTc, S, pieces);
     if (!workspace || workspace_bytes < ws.total) return GDR_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GDR_ERR_ALIGN;
     char* base = static_cast<char*>(workspace);
@@ -532,12 +614,16 @@ gdr_status gdr_forward(const gdr_problem* p, const void* q, const void* k, const
     void* h_ckpt = base + ws.h_ckpt;
     cudaStream_t s = (cudaStream_t)stream;
     unsigned int* err = path == Path::Simt ? nullptr : device_error_word();
-    if (path == Path::Simt) {
+    if (pieces > 1) {
+        if ((st = forward_tc_overlapped(d, pieces, ws, base, q, k, v, g, beta, h0, o, h_final, s, err)) != GDR_OK)
+            return st;
+    } else if (path == Path::Simt) {
         if ((st = from_cuda(gdr::simt_prepare(d, k, v, g, beta, w, u, g_cum, s))) != GDR_OK) return st;
         if ((st = from_cuda(gdr::simt_scan(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, s))) != GDR_OK) return st;
         if ((st = from_cuda(gdr::simt_output(d, q, k, v_new, h_ckpt, g_cum, o, s))) != GDR_OK) return st;
     } else {
-        void* P = (path == Path::Fused && d.C == 64) ? base + ws.P : nullptr;
+        const bool fused = path == Path::Fused || path == Path::FusedTc;
+        void* P = (fused && d.C == 64) ? base + ws.P : nullptr;
         if ((st = from_cuda(gdr::mma_prepare(d, k, v, g, beta, w, u, g_cum, s, err, q, P))) != GDR_OK) return st;
         // segments: every segment's map from a zero state, the starts stitched serially, then the
         // scan (and output) of all segments at once from their starts
@@ -554,9 +640,11 @@ gdr_status gdr_forward(const gdr_problem* p, const void* q, const void* k, const
             hs = starts;
             hf = nullptr;
         }
-        if (path == Path::Fused) {
-            if ((st = from_cuda(gdr::mma_scan_output(ds, q, k, w, u, g_cum, P, hs, o, hf, s, err))) != GDR_OK)
-                return st;
+        if (fused) {
+            const cudaError_t e = path == Path::FusedTc
+                                      ? gdr::tc_scan_output(ds, q, k, w, u, g_cum, P, hs, o, hf, s, err)
+                                      : gdr::mma_scan_output(ds, q, k, w, u, g_cum, P, hs, o, hf, s, err);
+            if ((st = from_cuda(e)) != GDR_OK) return st;
         } else {
             if ((st = from_cuda(gdr::mma_scan(ds, k, w, u, g_cum, hs, h_ckpt, v_new, hf, s, err))) != GDR_OK)
                 return st;
@@ -575,9 +663,19 @@ gdr_status gdr_scan_output(const gdr_problem* p, const void* q, const void* k, c
     if (st != GDR_OK) return st;
     if ((st = check_ptrs({q, k, w, u, g_cum, o}, {P, h0, h_final})) != GDR_OK) return st;
     if (p->variant == GDR_VARIANT_SIMT || !d.bf16 || d.per_k || (P && d.C != 64)) return GDR_ERR_UNSUPPORTED;
-    st = from_cuda(gdr::mma_scan_output(d, q, k, w, u, g_cum, P, h0, o, h_final, (cudaStream_t)stream,
-                                        device_error_word()));
-    if (st == GDR_OK) t_last_variant = "fused";
+    // the tcgen05 kernel for variant FUSED_TC, and for AUTO where gdr_forward would take it
+    Path path;
+    if ((st = pick_forward(p, d, &path)) != GDR_OK) return st;
+    bool tc = path == Path::FusedTc;
+    if (tc && !P) {   // the tcgen05 kernel takes P from the prepare
+        if (p->variant == GDR_VARIANT_FUSED_TC) return GDR_ERR_UNSUPPORTED;
+        tc = false;
+    }
+    st = from_cuda(tc ? gdr::tc_scan_output(d, q, k, w, u, g_cum, P, h0, o, h_final, (cudaStream_t)stream,
+                                            device_error_word())
+                      : gdr::mma_scan_output(d, q, k, w, u, g_cum, P, h0, o, h_final, (cudaStream_t)stream,
+                                             device_error_word()));
+    if (st == GDR_OK) t_last_variant = tc ? "fused_tc" : "fused";
     return st;
 }
 
@@ -864,6 +962,7 @@ gdr_status varlen_inner_bytes(const gdr_problem* p, const gdr::Dims& d, bool bac
     } else {
         Path path;
         if ((st = pick_forward(p, d, &path)) != GDR_OK) return st;
+        if (path == Path::FusedTc) path = Path::Fused;   // packed sequences: the warp-level fused kernel
         if ((st = resolve_segments(p, d, path != Path::Simt, &S)) != GDR_OK) return st;
         *bytes = plan_staged(d, path == Path::Fused, S).total;
         if (path != Path::Simt && chunk_packed_fits(d)) {
@@ -950,6 +1049,7 @@ gdr_status gdr_varlen_forward(const gdr_problem* p_in, const int32_t* cu_seqlens
         return st;
     Path path;
     if ((st = pick_forward(p, d, &path)) != GDR_OK) return st;
+    if (path == Path::FusedTc) path = Path::Fused;   // packed sequences: the warp-level fused kernel
     char* base = static_cast<char*>(workspace);
     int64_t rb[11];
     varlen_rows(d, false, rb);

@@ -30,9 +30,11 @@ cudaError_t simt_output(const Dims& d, const void* q, const void* k, const void*
 // ---- tensor-core kernels (bf16 io only)
 // with q and P non-NULL (scalar gate, C = 64) it also writes P = tril_0(q k^T * exp(G_i - G_j))
 // per chunk as [B, NT, H, C, C] bf16; with tinv non-NULL, (I + A)^{-1} per chunk, [B, NT, H, C, C] bf16
+// pdl: launch as the programmatic dependent of the stream's previous kernel (see gdr_api.cpp's overlapped
+// forward): it may start once every CTA of that kernel has signalled, and must read nothing it writes.
 cudaError_t mma_prepare(const Dims& d, const void* k, const void* v, const float* g, const void* beta, void* w,
                         void* u, float* g_cum, cudaStream_t s, unsigned int* err, const void* q = nullptr,
-                        void* P = nullptr, void* tinv = nullptr);
+                        void* P = nullptr, void* tinv = nullptr, bool pdl = false);
 // The prepare with P (scalar gate, C = 64) on the chunk-packed row d (B = 1) of packed variable-length
 // sequences, reading q, k, v, g, beta in place from the caller's packed tensors of `total` tokens: chunk c of
 // the row is chunk c - co[s] of sequence s = cs[c] (cu, co, cs as varlen_plan makes them).  w, u, g_cum and
@@ -66,6 +68,13 @@ cudaError_t mma_scan_output(const Dims& d, const void* q, const void* k, const v
                             const int* pcu = nullptr, int Tin = 0);
 // pcu, Tin (with co and P): q, k and o are the caller's packed tensors of Tin tokens, sequence z starting at
 // packed row pcu[z]; w, u, g_cum and P are the chunk-packed row's (see fused_mma.cu)
+
+// The same scan and output on the tcgen05 tensor cores, one CTA per (batch, head) (fused_tc.cu): bf16 io,
+// scalar gate, K = V = 128, C = 64 (any T, grouped value heads), and P from the prepare.
+bool tc_scan_output_supported(const Dims& d);
+cudaError_t tc_scan_output(const Dims& d, const void* q, const void* k, const void* w, const void* u,
+                           const float* g_cum, const void* P, const float* h0, void* o, float* h_final,
+                           cudaStream_t s, unsigned int* err);
 
 // ---- backward stages on the CUDA cores (simt_backward.cu): every shape and io dtype;
 // intermediates fp32, see include/gdr.h for each stage's definition

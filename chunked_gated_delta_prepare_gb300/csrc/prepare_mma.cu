@@ -632,10 +632,12 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
     }
 }
 
+// pdl: launched as the programmatic dependent of the kernel before it in the stream (it may start as
+// soon as every CTA of that kernel has signalled, and reads nothing that kernel writes).
 template <int K, int V, int C, bool PER_K, bool WITH_P, bool EXTRA, bool PACKED = false>
 cudaError_t launch_prepare_v(const Dims& d, const void* q, const void* k, const void* v, const float* g,
                              const void* beta, void* w, void* u, float* g_cum, void* P, void* tinv, cudaStream_t s,
-                             unsigned int* err, PackedIn pin = PackedIn{}) {
+                             unsigned int* err, PackedIn pin = PackedIn{}, bool pdl = false) {
     using L = PrepLayout<K, V, C, PER_K, WITH_P>;
     CUtensorMap mk, mv, mw, mu, mq, mp;
     // q and k have the Hk q/k heads; every other token tensor the H value heads.  Packed inputs: one
@@ -659,6 +661,20 @@ cudaError_t launch_prepare_v(const Dims& d, const void* q, const void* k, const 
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const dim3 grid((d.T + kTile - 1) / kTile, d.H, d.B);
+    if (pdl) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = grid;
+        cfg.blockDim = dim3(128);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, kern, mk, mv, mw, mu, mq, mp, g, (const bf16*)beta, g_cum, (bf16*)tinv, d.T,
+                                  d.H, d.G, pin, err);
+    }
     kern<<<grid, 128, smem, s>>>(mk, mv, mw, mu, mq, mp, g, (const bf16*)beta, g_cum, (bf16*)tinv, d.T, d.H, d.G,
                                  pin, err);
     return cudaGetLastError();
@@ -667,27 +683,31 @@ cudaError_t launch_prepare_v(const Dims& d, const void* q, const void* k, const 
 template <int K, int V, int C, bool PER_K, bool WITH_P>
 cudaError_t launch_prepare(const Dims& d, const void* q, const void* k, const void* v, const float* g,
                            const void* beta, void* w, void* u, float* g_cum, void* P, void* tinv, cudaStream_t s,
-                           unsigned int* err) {
+                           unsigned int* err, bool pdl) {
     if (d.G != 1 || tinv)
-        return launch_prepare_v<K, V, C, PER_K, WITH_P, true>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err);
-    return launch_prepare_v<K, V, C, PER_K, WITH_P, false>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err);
+        return launch_prepare_v<K, V, C, PER_K, WITH_P, true>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err,
+                                                              PackedIn{}, pdl);
+    return launch_prepare_v<K, V, C, PER_K, WITH_P, false>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err,
+                                                           PackedIn{}, pdl);
 }
 
 template <int K, int V, int C>
 cudaError_t pick_gate(const Dims& d, const void* q, const void* k, const void* v, const float* g, const void* beta,
-                      void* w, void* u, float* g_cum, void* P, void* tinv, cudaStream_t s, unsigned int* err) {
-    if (d.per_k) return launch_prepare<K, V, C, true, false>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err);
+                      void* w, void* u, float* g_cum, void* P, void* tinv, cudaStream_t s, unsigned int* err,
+                      bool pdl) {
+    if (d.per_k) return launch_prepare<K, V, C, true, false>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err, pdl);
     if constexpr (C == 64) {
-        if (P) return launch_prepare<K, V, C, false, true>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err);
+        if (P) return launch_prepare<K, V, C, false, true>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err, pdl);
     }
-    return launch_prepare<K, V, C, false, false>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err);
+    return launch_prepare<K, V, C, false, false>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err, pdl);
 }
 
 template <int K, int V>
 cudaError_t pick_chunk(const Dims& d, const void* q, const void* k, const void* v, const float* g, const void* beta,
-                       void* w, void* u, float* g_cum, void* P, void* tinv, cudaStream_t s, unsigned int* err) {
-    return d.C == 32 ? pick_gate<K, V, 32>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err)
-                     : pick_gate<K, V, 64>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err);
+                       void* w, void* u, float* g_cum, void* P, void* tinv, cudaStream_t s, unsigned int* err,
+                       bool pdl) {
+    return d.C == 32 ? pick_gate<K, V, 32>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err, pdl)
+                     : pick_gate<K, V, 64>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err, pdl);
 }
 
 template <int K, int V>
@@ -717,13 +737,13 @@ cudaError_t mma_prepare_packed(const Dims& d, const void* q, const void* k, cons
 
 cudaError_t mma_prepare(const Dims& d, const void* k, const void* v, const float* g, const void* beta, void* w,
                         void* u, float* g_cum, cudaStream_t s, unsigned int* err, const void* q, void* P,
-                        void* tinv) {
+                        void* tinv, bool pdl) {
     if (!d.bf16) return cudaErrorInvalidValue;
     if (P && (d.per_k || d.C != 64 || !q)) return cudaErrorInvalidValue;
-    if (d.K == 64 && d.V == 64) return pick_chunk<64, 64>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err);
-    if (d.K == 64 && d.V == 128) return pick_chunk<64, 128>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err);
-    if (d.K == 128 && d.V == 64) return pick_chunk<128, 64>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err);
-    return pick_chunk<128, 128>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err);
+    if (d.K == 64 && d.V == 64) return pick_chunk<64, 64>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err, pdl);
+    if (d.K == 64 && d.V == 128) return pick_chunk<64, 128>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err, pdl);
+    if (d.K == 128 && d.V == 64) return pick_chunk<128, 64>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err, pdl);
+    return pick_chunk<128, 128>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err, pdl);
 }
 
 }  // namespace gdr

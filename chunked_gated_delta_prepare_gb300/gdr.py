@@ -11,7 +11,7 @@ The functions mirror the C ABI names:
     gdr_bwd_prepare, gdr_bwd_scan_dh_p, gdr_bwd_wy_dqkg, gdr_backward, gdr_backward_workspace_bytes,
     gdr_varlen_forward, gdr_varlen_forward_workspace_bytes, gdr_varlen_backward,
     gdr_varlen_backward_workspace_bytes,
-    gdr_status_string, gdr_get_device_status,
+    gdr_status_string, gdr_get_device_status, gdr_selftest_bounded_wait,
     gdr_last_variant, gdr_version
 and `forward(...)` / `backward(...)` are the convenience calls that allocate outputs and
 the workspace (and, given CPU tensors, copy them to the GPU and the results back);
@@ -34,7 +34,7 @@ STATUS_NAMES = {0: "GDR_OK", 1: "GDR_ERR_NULL", 2: "GDR_ERR_SHAPE", 3: "GDR_ERR_
                 5: "GDR_ERR_WORKSPACE", 6: "GDR_ERR_CUDA", 7: "GDR_ERR_DEVICE_TIMEOUT",
                 8: "GDR_ERR_UNSUPPORTED", 9: "GDR_ERR_ARG"}
 DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
-VARIANTS = {"auto": 0, "simt": 1, "tensor": 2, "fused": 3}
+VARIANTS = {"auto": 0, "simt": 1, "tensor": 2, "fused": 3, "fused_tc": 4}
 EXPORTS = ["gdr_prepare_wy", "gdr_scan_h", "gdr_chunk_output", "gdr_forward", "gdr_forward_workspace_bytes",
            "gdr_forward_static_scratch", "gdr_scan_output", "gdr_prepare_wyp",
            "gdr_bwd_dv_local", "gdr_bwd_scan_dh", "gdr_bwd_dqkwg", "gdr_bwd_wy", "gdr_backward",
@@ -43,7 +43,8 @@ EXPORTS = ["gdr_prepare_wy", "gdr_scan_h", "gdr_chunk_output", "gdr_forward", "g
            "gdr_scan_combine", "gdr_scan_combine_reverse", "gdr_forward_segments",
            "gdr_varlen_forward", "gdr_varlen_forward_workspace_bytes", "gdr_varlen_backward",
            "gdr_varlen_backward_workspace_bytes",
-           "gdr_status_string", "gdr_get_device_status", "gdr_last_variant", "gdr_version"]
+           "gdr_status_string", "gdr_get_device_status", "gdr_selftest_bounded_wait", "gdr_last_variant",
+           "gdr_version"]
 
 
 class GdrError(RuntimeError):
@@ -106,6 +107,7 @@ def load(path: str | None = None):
             "gdr_varlen_backward_workspace_bytes": [P],
             "gdr_status_string": [ctypes.c_int],
             "gdr_get_device_status": [vp],
+            "gdr_selftest_bounded_wait": [ctypes.c_int32, ctypes.c_int32, vp],
             "gdr_last_variant": [],
             "gdr_version": [],
         }
@@ -244,6 +246,13 @@ def gdr_status_string(status: int) -> str:
 
 def gdr_get_device_status(stream=None) -> int:
     return int(load().gdr_get_device_status(_stream(stream)))
+
+
+def gdr_selftest_bounded_wait(polls: int, arrive: bool, stream=None):
+    """Run the bounded-wait check: a kernel waits on an mbarrier with a limit of `polls` polls;
+    with arrive=False nothing arrives and the wait gives up (see include/gdr.h)."""
+    _check(load().gdr_selftest_bounded_wait(int(polls), 1 if arrive else 0, _stream(stream)),
+           "gdr_selftest_bounded_wait")
 
 
 def gdr_last_variant() -> str:

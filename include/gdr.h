@@ -94,14 +94,22 @@ typedef enum gdr_gate {
 } gdr_gate;
 
 /* Which kernels to run.  AUTO picks the fastest measured variant that supports
- * the problem: FUSED for bf16 io with a scalar gate and 64-token chunks, TENSOR
- * for other bf16 problems, SIMT for fp32 io.  The single-stage entry points run
- * their tensor-core kernel for AUTO, TENSOR and FUSED on bf16 io. */
+ * the problem: for bf16 io with a scalar gate and 64-token chunks FUSED_TC when
+ * K = V = 128 and either B * HV * V / 32 > 152 (the warp-level fused kernel's grid
+ * would need more than one wave of the GPU's 152 SMs) or B = 1 with at least 128
+ * chunks and no segmented scan (one long sequence, which FUSED_TC runs in pieces
+ * whose scans overlap the next piece's prepare), else FUSED; TENSOR for other
+ * bf16 problems; SIMT for fp32 io.  The single-stage entry points run their
+ * tensor-core kernel for AUTO, TENSOR, FUSED and FUSED_TC on bf16 io. */
 typedef enum gdr_variant {
     GDR_VARIANT_AUTO = 0,
     GDR_VARIANT_SIMT = 1,     /* fp32 CUDA-core arithmetic throughout (exact-fp32 path) */
     GDR_VARIANT_TENSOR = 2,   /* staged kernels on the tensor cores (bf16 io only) */
-    GDR_VARIANT_FUSED = 3     /* WY prepare, then scan and output fused (bf16 io, scalar gate) */
+    GDR_VARIANT_FUSED = 3,    /* WY prepare, then scan and output fused, warp-level MMA, one CTA per
+                                 (batch, head, 32 value columns) (bf16 io, scalar gate) */
+    GDR_VARIANT_FUSED_TC = 4  /* the same with scan and output on the tcgen05 tensor cores, one CTA per
+                                 (batch, head) (bf16 io, scalar gate, K = V = 128, chunk 64); packed
+                                 sequences (gdr_varlen_*) run FUSED for it */
 } gdr_variant;
 
 typedef struct gdr_problem {
@@ -212,7 +220,9 @@ GDR_API gdr_status gdr_chunk_output(const gdr_problem* p, const void* q, const v
  *          as gdr_prepare_wyp writes it, or NULL to form it here (C = 64 for a
  *          non-NULL P); h0 [B,H,K,V] fp32 or NULL.
  * Outputs: o [B,T,H,V] bf16; h_final [B,H,K,V] fp32 or NULL (not written).
- * Returns GDR_ERR_UNSUPPORTED for fp32 io or a per-key-dim gate.
+ * Returns GDR_ERR_UNSUPPORTED for fp32 io or a per-key-dim gate.  The kernel is the
+ * tcgen05 one for variant FUSED_TC (K = V = 128, C = 64, P required) and for AUTO
+ * where gdr_forward's AUTO would take it; the warp-level one otherwise.
  */
 GDR_API gdr_status gdr_scan_output(const gdr_problem* p, const void* q, const void* k, const void* w, const void* u,
                                    const float* g_cum, const void* P, const float* h0, void* o, float* h_final,
@@ -255,11 +265,13 @@ GDR_API gdr_status gdr_forward(const gdr_problem* p, const void* q, const void* 
  * device memory, or a latency-critical loop that must not call cudaMalloc).
  * The method pages have no counterpart to this call; it is a deployment aid.
  *
- * It runs the staged forward (variant AUTO runs the fp32 CUDA-core stages;
- * SIMT and TENSOR are honoured; FUSED is not offered here and returns
- * GDR_ERR_UNSUPPORTED -- call gdr_forward for it) and takes the scratch from
- * an array of GDR_STATIC_SCRATCH_BYTES compiled into the library.  Arguments and
- * outputs are those of gdr_forward.
+ * It runs the staged forward (variant AUTO runs the tensor-core stages for
+ * bf16 io and the CUDA-core stages for fp32 and fp16 io, as gdr_forward's AUTO
+ * does with the fused path left out; SIMT and TENSOR are honoured; FUSED and
+ * FUSED_TC are not offered here and return GDR_ERR_UNSUPPORTED -- call gdr_forward
+ * for them) and
+ * takes the scratch from an array of GDR_STATIC_SCRATCH_BYTES compiled into the
+ * library.  Arguments and outputs are those of gdr_forward.
  * - A problem whose gdr_forward_workspace_bytes exceeds GDR_STATIC_SCRATCH_BYTES
  *   is rejected with GDR_ERR_WORKSPACE; nothing is launched.
  * - Every GPU that loads this part of the library holds that array until the
@@ -269,7 +281,9 @@ GDR_API gdr_status gdr_forward(const gdr_problem* p, const void* q, const void* 
  * - The array keeps the previous call's contents; nothing needs clearing,
  *   because the stages write every scratch byte before reading it.
  * - The first call on each device looks up the array's device address with
- *   that device current; make it before any stream capture starts.
+ *   that device current; make it before any stream capture starts.  The address
+ *   is kept for the life of the device's context: after a cudaDeviceReset of a
+ *   device, do not call this entry point on that device again.
  */
 #define GDR_STATIC_SCRATCH_BYTES (64ull << 20)
 GDR_API gdr_status gdr_forward_static_scratch(const gdr_problem* p, const void* q, const void* k, const void* v,
@@ -490,6 +504,19 @@ GDR_API const char* gdr_status_string(gdr_status s);
  * the synchronisation itself failed.
  */
 GDR_API gdr_status gdr_get_device_status(void* stream);
+
+/*
+ * A check of the failure detection above, on the GPU, with nothing else in flight.
+ * One CTA initialises an mbarrier that expects one arrival and waits on it with a
+ * limit of `polls` polls (1 .. 4194304; GDR_ERR_ARG otherwise).  With arrive == 0
+ * nothing arrives: the wait runs out, the kernel records GDR_ERR_DEVICE_TIMEOUT in
+ * the device error word and exits normally, so the next gdr_get_device_status
+ * reports it (and clears it).  With arrive != 0 the thread arrives first and the
+ * wait succeeds.  No tensor-core work or TMA copy is issued, so nothing is left
+ * running when the wait gives up.  The method pages have no counterpart to this
+ * call; it exists to exercise the library's bounded waits.
+ */
+GDR_API gdr_status gdr_selftest_bounded_wait(int32_t polls, int32_t arrive, void* stream);
 
 /*
  * Name of the kernel variant the last successful call on this host thread

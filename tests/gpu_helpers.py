@@ -49,6 +49,15 @@ def rel_frob(x, ref):
     return float(np.linalg.norm((x - ref).ravel()) / max(np.linalg.norm(np.asarray(ref).ravel()), 1e-30))
 
 
+def variant_supports(variant, K, V, C, per_k=False):
+    """Whether a forward variant takes these sizes (the tcgen05 fused form: K = V = 128, C = 64, scalar gate)."""
+    if variant == "fused_tc":
+        return K == 128 and V == 128 and C == 64 and not per_k
+    if variant == "fused":
+        return not per_k
+    return True
+
+
 def problem(x, C, variant="auto", scale=None):
     return gdr.problem_for(x.q, x.v, x.g, C, scale, variant)
 

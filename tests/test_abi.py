@@ -156,9 +156,51 @@ def test_fused_workspace_size_formula(lib):
     for (B, T, H, K, V, C) in [(1, 256, 2, 64, 64, 64), (2, 4096, 8, 64, 64, 32), (1, 32768, 32, 128, 128, 64)]:
         rows = B * T * H
         want = r(rows * 4) + r(rows * K * 2) + r(rows * V * 2) + (r(rows * C * 2) if C == 64 else 0)
-        for variant in ("fused", "auto" if C == 64 else "fused"):
+        variants = ["fused", "auto" if C == 64 else "fused"]
+        if K == V == 128 and C == 64 and B > 1:
+            variants.append("fused_tc")      # the tcgen05 form keeps the same intermediates (batched: no pieces)
+        for variant in variants:
             p = gdr.make_problem(B, T, H, K, V, C, 1, False, variant=variant, segments=1)
-            assert lib.gdr_forward_workspace_bytes(ctypes.byref(p)) == want
+            extra = 0
+            if variant == "auto" and B == 1 and K == V == 128 and -(-T // C) >= 128:
+                # AUTO runs one long sequence on the overlapped tcgen05 path: 8 pieces of 64 chunks here, the
+                # state carried between them in fp32
+                extra = r(7 * H * K * V * 4)
+            assert lib.gdr_forward_workspace_bytes(ctypes.byref(p)) == want + extra
+
+
+def test_overlapped_fused_tc_workspace(lib):
+    # one sequence on the tcgen05 fused path runs in pieces of at least 64 chunks (at most 16 pieces); the
+    # workspace adds the fp32 state carried between pieces, [pieces - 1][H, K, V]
+    r = lambda x: (x + 255) // 256 * 256
+    for (T, H, pieces) in [(64 * 64, 2, 1), (64 * 64 + 1, 2, 2), (32768, 32, 8), (64 * 64 * 40, 1, 16)]:
+        rows = T * H
+        NT = -(-T // 64)
+        base = r(rows * 4) + r(rows * 128 * 2) + r(rows * 128 * 2) + r(NT * H * 64 * 64 * 2)
+        want = base + (r((pieces - 1) * H * 128 * 128 * 4) if pieces > 1 else 0)
+        p = gdr.make_problem(1, T, H, 128, 128, 64, 1, False, variant="fused_tc", segments=1)
+        assert lib.gdr_forward_workspace_bytes(ctypes.byref(p)) == want, (T, H)
+        # two sequences run batched, not in pieces: no carried state
+        rows2 = 2 * rows
+        base2 = r(rows2 * 4) + r(rows2 * 128 * 2) + r(rows2 * 128 * 2) + r(2 * NT * H * 64 * 64 * 2)
+        p2 = gdr.make_problem(2, T, H, 128, 128, 64, 1, False, variant="fused_tc", segments=1)
+        assert lib.gdr_forward_workspace_bytes(ctypes.byref(p2)) == base2
+
+
+def test_fused_tc_variant_takes_its_sizes_only(lib):
+    # K = V = 128, C = 64, bf16, scalar gate; anything else is GDR_ERR_UNSUPPORTED before a launch
+    for (K, V, C, dt, per_k, code) in [(128, 128, 64, 1, False, None), (64, 64, 64, 1, False, 8),
+                                       (128, 64, 64, 1, False, 8), (128, 128, 32, 1, False, 8),
+                                       (128, 128, 64, 1, True, 8), (128, 128, 64, 0, False, 8)]:
+        p = gdr.make_problem(1, 256, 2, K, V, C, dt, per_k, variant="fused_tc")
+        if code is None:
+            assert lib.gdr_forward_workspace_bytes(ctypes.byref(p)) > 0
+        else:
+            assert lib.gdr_forward_workspace_bytes(ctypes.byref(p)) == 0
+            assert _fwd(lib, p) == code
+    p = gdr.make_problem(1, 256, 2, 128, 128, 64, 1, False)
+    p.variant = 5
+    assert _fwd(lib, p) == 9
 
 
 def test_segment_choice_and_workspace(lib):

@@ -10,25 +10,27 @@ import oracle
 from chunked_gated_delta_prepare_gb300 import gdr, workloads
 from chunked_gated_delta_prepare_gb300.inputs import GdrInputs, make_inputs, make_workload_inputs
 from gpu_helpers import (H_TOL, O_TOL, all_pairs, check_forward, gpu_forward, grouped_inputs, io_name, max_abs,
-                         rel_frob)
+                         rel_frob, variant_supports)
 
 pytestmark = pytest.mark.gpu
 
 # every variant gdr_forward offers, with the io dtypes it takes
 FORWARD_VARIANTS = {"simt": (torch.float32, torch.bfloat16), "tensor": (torch.bfloat16,),
-                    "fused": (torch.bfloat16,)}
-# the fused path takes a scalar gate only
-GATES = {"simt": (False, True), "tensor": (False, True), "fused": (False,)}
+                    "fused": (torch.bfloat16,), "fused_tc": (torch.bfloat16,)}
+# the fused paths take a scalar gate only
+GATES = {"simt": (False, True), "tensor": (False, True), "fused": (False,), "fused_tc": (False,)}
 SHAPES = [(2, 256, 3, 64, 64, 64), (1, 192, 2, 128, 128, 64), (2, 128, 3, 64, 128, 32),
           (1, 160, 1, 128, 64, 32), (1, 64, 2, 128, 128, 64), (1, 32, 1, 64, 64, 32),
           # a last, partial chunk: 36 of 64 tokens; 13 of 32 (the second half of a 64-token
           # tile past T); a lone 20-token chunk; 22 of 32 with two batches
-          (2, 100, 3, 64, 64, 64), (1, 77, 2, 128, 128, 32), (1, 20, 1, 128, 64, 64), (2, 150, 1, 64, 128, 32)]
+          (2, 100, 3, 64, 64, 64), (1, 77, 2, 128, 128, 32), (1, 20, 1, 128, 64, 64), (2, 150, 1, 64, 128, 32),
+          # the tcgen05 fused form's sizes: several chunks and heads; a partial chunk (36 of 64); one token
+          (2, 320, 3, 128, 128, 64), (1, 100, 2, 128, 128, 64), (1, 1, 2, 128, 128, 64)]
 
 
 def small_cases():
     for shape, per_k, (variant, dts) in itertools.product(SHAPES, (False, True), FORWARD_VARIANTS.items()):
-        if per_k not in GATES[variant]:
+        if per_k not in GATES[variant] or not variant_supports(variant, shape[3], shape[4], shape[5], per_k):
             continue
         for dt in dts:
             yield pytest.param(shape, per_k, variant, dt,
@@ -96,15 +98,16 @@ def test_state_carry(variant, dtype):
 
 @pytest.mark.parametrize("variant,dtype", [(v, d) for v, ds in FORWARD_VARIANTS.items() for d in ds])
 def test_null_h0_is_zero_state_and_h_final_optional(variant, dtype):
-    x = make_inputs(1, 128, 2, 64, 64, io_dtype=dtype, with_h0=False, seed=8)
+    D = 128 if variant == "fused_tc" else 64
+    x = make_inputs(1, 128, 2, D, D, io_dtype=dtype, with_h0=False, seed=8)
     o1, h1, _ = gpu_forward(x, 64, variant, h0=None)
-    o2, h2, _ = gpu_forward(x, 64, variant, h0=torch.zeros(1, 2, 64, 64))
+    o2, h2, _ = gpu_forward(x, 64, variant, h0=torch.zeros(1, 2, D, D))
     o3, _, _ = gpu_forward(x, 64, variant, h0=None, want_h_final=False)
     assert torch.equal(o1, o2) and torch.equal(h1, h2) and torch.equal(o1, o3)
 
 
-def _edge_inputs(kind, per_k, dtype):
-    x = make_inputs(1, 128, 2, 64, 64, per_k_gate=per_k, io_dtype=dtype, with_h0=True, seed=9)
+def _edge_inputs(kind, per_k, dtype, D=64):
+    x = make_inputs(1, 128, 2, D, D, per_k_gate=per_k, io_dtype=dtype, with_h0=True, seed=9)
     g, beta = x.g.clone(), x.beta.clone()
     if kind == "beta_zero":
         beta.zero_()
@@ -137,6 +140,10 @@ def test_partial_chunk_touches_nothing_past_T(T, C, variant, dtype, per_k):
     """Inputs and output sit in buffers with room for whole chunks, NaN past T: a read
     past T would turn the results NaN and a write past T would overwrite the NaN tail."""
     H, K, V = 2, 64, 128
+    if variant == "fused_tc":
+        if C != 64:
+            pytest.skip("the tcgen05 fused form takes 64-token chunks")
+        K = 128
     Tb = -(-T // C) * C + C
     x = make_inputs(1, T, H, K, V, per_k_gate=per_k, io_dtype=dtype, with_h0=True, seed=21 + T)
     q, k, v, g, beta = (_padded(t, T, Tb) for t in (x.q, x.k, x.v, x.g, x.beta))
@@ -157,10 +164,12 @@ def test_partial_chunk_touches_nothing_past_T(T, C, variant, dtype, per_k):
 @pytest.mark.parametrize("variant,dtype,per_k", [(v, d, pk) for v, ds in FORWARD_VARIANTS.items() for d in ds
                                                   for pk in GATES[v]])
 def test_edge_cases(kind, per_k, variant, dtype):
-    x = _edge_inputs(kind, per_k, dtype)
-    C = 32
-    o, hf, _ = gpu_forward(x, C, variant)
-    check_forward(x, o, hf, all_pairs(1, 2), C, 1.0 / 8.0, io_name(dtype))
+    # the tcgen05 fused form takes K = V = 128 and 64-token chunks only
+    D, C = (128, 64) if variant == "fused_tc" else (64, 32)
+    x = _edge_inputs(kind, per_k, dtype, D)
+    o, hf, ran = gpu_forward(x, C, variant)
+    assert ran == variant
+    check_forward(x, o, hf, all_pairs(1, 2), C, 1.0 / np.sqrt(D), io_name(dtype))
 
 
 def test_convenience_forward_host_tensors():
@@ -201,10 +210,19 @@ def test_pipelined_host_forward_equals_one_device_call(shape, per_k, variant):
     assert torch.equal(o_p, o_1.cpu()) and torch.equal(hf_p, hf_1.cpu())
 
 
-def test_fused_variant_refuses_per_key_gate():
-    x = make_inputs(1, 64, 1, 64, 64, per_k_gate=True, io_dtype=torch.bfloat16, seed=12)
+@pytest.mark.parametrize("variant", ["fused", "fused_tc"])
+def test_fused_variant_refuses_per_key_gate(variant):
+    x = make_inputs(1, 64, 1, 128, 128, per_k_gate=True, io_dtype=torch.bfloat16, seed=12)
     with pytest.raises(gdr.GdrError) as e:
-        gpu_forward(x, 64, "fused")
+        gpu_forward(x, 64, variant)
+    assert e.value.status == 8
+
+
+@pytest.mark.parametrize("K,V,C", [(64, 64, 64), (128, 64, 64), (128, 128, 32)])
+def test_fused_tc_refuses_other_sizes(K, V, C):
+    x = make_inputs(1, 64, 1, K, V, io_dtype=torch.bfloat16, seed=12)
+    with pytest.raises(gdr.GdrError) as e:
+        gpu_forward(x, C, "fused_tc")
     assert e.value.status == 8
 
 
@@ -216,6 +234,13 @@ def test_auto_variant_choice():
     assert gpu_forward(xk, 64, "auto")[2] == "tensor"
     xf = make_inputs(1, 128, 2, 64, 64, io_dtype=torch.float32, with_h0=True, seed=13)
     assert gpu_forward(xf, 64, "auto")[2] == "simt"
+    # K = V = 128 with more (batch, head) pairs than 152 SMs take warp-level fused CTAs (4 each): tcgen05
+    xt = make_inputs(1, 128, 38, 128, 128, io_dtype=torch.bfloat16, with_h0=True, seed=13)
+    assert gpu_forward(xt, 64, "auto")[2] == "fused"          # 38 x 4 = 152 CTAs: one wave
+    xt = make_inputs(1, 128, 39, 128, 128, io_dtype=torch.bfloat16, with_h0=True, seed=13)
+    o, hf, ran = gpu_forward(xt, 64, "auto")
+    assert ran == "fused_tc"
+    check_forward(xt, o, hf, all_pairs(1, 39), 64, 1.0 / np.sqrt(128), "bf16")
 
 
 def test_convenience_forward_refuses_a_small_workspace():
@@ -247,6 +272,8 @@ GROUPED = [(2, 128, 2, 2, 64, 64, 64), (1, 100, 1, 4, 128, 128, 64), (1, 96, 2, 
 def test_grouped_value_heads_forward(shape, variant, dtype, per_k):
     # H q/k heads shared by H * G value heads: every value head against the oracle
     B, T, H, G, K, V, C = shape
+    if not variant_supports(variant, K, V, C, per_k):
+        pytest.skip("sizes the variant does not take")
     x = grouped_inputs(B, T, H, G, K, V, per_k_gate=per_k, io_dtype=dtype, seed=82)
     o, hf, ran = gpu_forward(x, C, variant)
     assert ran == variant and o.shape == (B, T, H * G, V)
@@ -267,7 +294,7 @@ def test_fp16_io_forward(shape, per_k, variant):
     check_forward(x, o, hf, all_pairs(B, H), C, 1.0 / np.sqrt(K), "f16")
 
 
-@pytest.mark.parametrize("variant", ["tensor", "fused"])
+@pytest.mark.parametrize("variant", ["tensor", "fused", "fused_tc"])
 def test_fp16_io_refused_by_the_tensor_core_variants(variant):
     x = make_inputs(1, 64, 1, 64, 64, io_dtype=torch.float16, seed=91)
     with pytest.raises(gdr.GdrError) as e:
@@ -290,3 +317,22 @@ def test_constant_per_key_gate_is_the_scalar_gate(shape, variant, dtype):
     io = io_name(dtype)
     assert max_abs(ok_, o.double().cpu().numpy()) <= O_TOL[io]
     assert rel_frob(hfk, hf.double().cpu().numpy()) <= H_TOL[io]
+
+
+# ---------------------------------------------------------------- the overlapped tcgen05 forward
+
+@pytest.mark.parametrize("T,H", [(64 * 64 * 3 + 100, 2), (64 * 128, 3), (64 * 64 + 64, 1)])
+def test_overlapped_fused_tc_single_sequence(T, H):
+    # one sequence on the tcgen05 fused path runs in pieces of 64 chunks, each piece's scan overlapping the
+    # next piece's prepare on an internal stream, the state carried between pieces: every head against the
+    # token oracle (a partial last chunk in the first case, a single-chunk last piece in the last)
+    x = make_inputs(1, T, H, 128, 128, io_dtype=torch.bfloat16, with_h0=True, seed=41)
+    o, hf, ran = gpu_forward(x, 64, "fused_tc")
+    assert ran == "fused_tc"
+    check_forward(x, o, hf, all_pairs(1, H), 64, 1.0 / np.sqrt(128), "bf16")
+    # the same problem as two batch rows (one piece each, no overlap) gives the same o and h_final
+    x2 = GdrInputs(q=x.q.repeat(2, 1, 1, 1), k=x.k.repeat(2, 1, 1, 1), v=x.v.repeat(2, 1, 1, 1),
+                   g=x.g.repeat(2, 1, 1), beta=x.beta.repeat(2, 1, 1), h0=x.h0.repeat(2, 1, 1, 1))
+    o2, hf2, _ = gpu_forward(x2, 64, "fused_tc")
+    assert max_abs(o, o2[:1].double().cpu().numpy()) <= 2e-3
+    assert rel_frob(hf, hf2[:1].double().cpu().numpy()) <= 2e-3

@@ -35,10 +35,16 @@ def _capture(fn):
     return graph
 
 
-@pytest.mark.parametrize("variant,dtype,per_k", [("fused", torch.bfloat16, False), ("tensor", torch.bfloat16, True),
-                                                 ("simt", torch.float32, False)])
-def test_forward_replays_in_a_graph(variant, dtype, per_k):
-    B, T, H, K, V, C = 2, 320, 3, 128, 64, 64
+@pytest.mark.parametrize("variant,dtype,per_k,B,T", [("fused", torch.bfloat16, False, 2, 320),
+                                                     ("fused_tc", torch.bfloat16, False, 2, 320),
+                                                     ("fused_tc", torch.bfloat16, False, 1, 64 * 64 * 2 + 50),
+                                                     ("tensor", torch.bfloat16, True, 2, 320),
+                                                     ("simt", torch.float32, False, 2, 320)])
+def test_forward_replays_in_a_graph(variant, dtype, per_k, B, T):
+    # (the single long sequence on fused_tc runs overlapped: its internal stream forks from and joins the
+    # captured stream)
+    H, C = 3, 64
+    K, V = 128, 128 if variant == "fused_tc" else 64
     xs = [make_inputs(B, T, H, K, V, per_k_gate=per_k, io_dtype=dtype, with_h0=True, seed=s) for s in (0, 1)]
     q, k, v, g, beta, h0 = (dev(t) for t in xs[0].tensors().values())
     p = gdr.problem_for(q, v, g, C, None, variant)

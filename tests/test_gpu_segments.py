@@ -86,6 +86,7 @@ def test_stitch(K, V, with_h0):
 
 # whole forwards with explicit segments: (B, T, H, K, V, C, S, per_k, variant)
 FORWARD_CASES = [(1, 2048, 2, 128, 128, 64, 4, False, "fused"), (1, 2048, 2, 128, 128, 64, 8, False, "fused"),
+                 (1, 2048, 2, 128, 128, 64, 4, False, "fused_tc"),
                  (2, 1024, 1, 64, 64, 64, 2, False, "fused"), (1, 2048, 2, 128, 128, 64, 4, True, "tensor"),
                  (1, 1024, 2, 64, 128, 32, 4, False, "tensor"), (2, 1024, 1, 128, 64, 32, 8, True, "tensor")]
 

@@ -163,6 +163,40 @@ def test_scan_output_stage(shape, with_h0):
     assert rel_frob(hf, scan["h_final"]) <= STAGE_TOL["bf16"]
 
 
+@pytest.mark.parametrize("shape", [(2, 256, 3, 128, 128, 64), (1, 100, 2, 128, 128, 64), (1, 64, 1, 128, 128, 64)],
+                         ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("with_h0", [False, True])
+def test_scan_output_stage_tcgen05(shape, with_h0):
+    """The tcgen05 form of the fused scan and output (variant FUSED_TC), fed the oracle's rounded w, u, G
+    and gated scores P, against the chunked oracle's scan and output stages."""
+    B, T, H, K, V, C = shape
+    dtype = torch.bfloat16
+    x = make_inputs(B, T, H, K, V, io_dtype=dtype, with_h0=with_h0, seed=15)
+    pre = chunked.prepare_wy(x.k, x.v, x.g, x.beta, C)
+    w_r, u_r, G_r = rounded(pre["w"], dtype), rounded(pre["u"], dtype), rounded(pre["G"], torch.float32)
+    P_r = rounded(chunked.gated_causal_scores(x.q, x.k, G_r, C), dtype)
+    h0 = None if x.h0 is None else x.h0 * 20
+    scan = chunked.scan_h(x.k, w_r, u_r, G_r, h0, C)
+    o_ref = chunked.chunk_output(x.q, x.k, scan["v_new"], scan["ckpt"], G_r, C, 0.125)
+    p = gdr.problem_for(x.q, x.v, x.g, C, scale=0.125, variant="fused_tc")
+    o = torch.full((B, T, H, V), float("nan"), device="cuda", dtype=dtype)
+    hf = torch.full((B, H, K, V), float("nan"), device="cuda", dtype=torch.float32)
+    gdr.gdr_scan_output(p, dev(x.q), dev(x.k), dev(w_r), dev(u_r), dev(G_r), dev(P_r), dev(h0), o, hf)
+    torch.cuda.synchronize()
+    assert gdr.gdr_get_device_status() == 0
+    assert gdr.gdr_last_variant() == "fused_tc"
+    assert scaled_err(o, o_ref) <= STAGE_TOL["bf16"]
+    assert rel_frob(hf, scan["h_final"]) <= STAGE_TOL["bf16"]
+
+
+def test_scan_output_tcgen05_needs_the_scores():
+    x = make_inputs(1, 64, 1, 128, 128, io_dtype=torch.bfloat16)
+    t = torch.zeros(64, 1, 128, device="cuda", dtype=torch.bfloat16)
+    with pytest.raises(gdr.GdrError) as e:
+        gdr.gdr_scan_output(gdr.problem_for(x.q, x.v, x.g, 64, variant="fused_tc"), t, t, t, t, t, None, None, t, None)
+    assert e.value.status == 8
+
+
 def test_scan_output_refuses_per_key_gate_and_fp32():
     x = make_inputs(1, 64, 1, 64, 64, per_k_gate=True, io_dtype=torch.bfloat16)
     t = torch.zeros(64, 1, 64, device="cuda", dtype=torch.bfloat16)

@@ -93,13 +93,19 @@ def algorithmic_bytes(wl, kernel: str, with_p: bool = False, segs: int = 1) -> i
 
 def overlap_pieces(wl, variant: str, segments: int) -> int:
     """Pieces gdr_forward cuts one sequence into on the tcgen05 fused path (the library's rule: B = 1, no
-    segments, pieces of at least 64 chunks and at most 16 of them); 1 when it does not."""
-    if variant != "fused_tc" or segments != 1 or wl.B != 1:
-        return 1
+    segments, at least 128 chunks; sizes from 16 chunks growing by 3/2, never below an equal share of what
+    is left among at most 32 pieces); 1 when it does not."""
     NT = wl.NT
-    per = max(64, -(-NT // 16))
-    n = -(-NT // per)
-    return n if n >= 2 else 1
+    if variant != "fused_tc" or segments != 1 or wl.B != 1 or NT < 128:
+        return 1
+    n = c = 0
+    ln = 16
+    while c < NT:
+        ln = max(ln, -(-(NT - c) // (32 - n)))
+        c = min(NT, c + ln)
+        n += 1
+        ln += ln // 2
+    return n
 
 
 class ClockSampler:

@@ -227,24 +227,47 @@ StagedWorkspace plan_staged(const gdr::Dims& d, bool fused, int S, int pieces = 
 // per head) the next piece's prepare starts on the SMs left free and overlaps the scan.  Each scan is
 // an ordinary launch, so it starts after its own piece's prepare and the previous scan; the state
 // passes between pieces in fp32 through the workspace.
-constexpr int kMaxPieces = 16;
+//
+// Piece sizes grow geometrically from kFirstPiece chunks by 3/2: only the first prepare runs alone, and
+// each later prepare, on the SMs the scan leaves, is shorter than the scan it overlaps (a scan chunk
+// costs about 1.5 us on one SM per head, a prepare chunk about 1.3 us of the whole GPU per 32 heads).
+// A piece is never shorter than an equal share of what is left among the pieces still allowed, so
+// there are at most kMaxPieces.
+constexpr int kFirstPiece = 16;
+constexpr int kMaxPieces = 32;
 
-int overlap_pieces(const gdr::Dims& d, Path path, int S) {
-    if (path != Path::FusedTc || S != 1 || d.B != 1) return 1;
-    const int per = std::max(kPieceChunks, (d.NT + kMaxPieces - 1) / kMaxPieces);
-    const int n = (d.NT + per - 1) / per;
-    return n >= 2 ? n : 1;
+// Chunk offsets of the pieces: bounds[0] = 0 < bounds[1] < ... < bounds[n] = NT; returns n (1: no pieces).
+int overlap_bounds(const gdr::Dims& d, Path path, int S, int* bounds) {
+    bounds[0] = 0;
+    if (path != Path::FusedTc || S != 1 || d.B != 1 || d.NT < 2 * kPieceChunks) {
+        bounds[1] = d.NT;
+        return 1;
+    }
+    int n = 0, c = 0, len = kFirstPiece;
+    while (c < d.NT) {
+        const int share = (d.NT - c + (kMaxPieces - n) - 1) / (kMaxPieces - n);
+        len = std::max(len, share);
+        c = std::min(d.NT, c + len);
+        bounds[++n] = c;
+        len += len / 2;
+    }
+    return n;
 }
 
-gdr_status forward_tc_overlapped(const gdr::Dims& d, int pieces, const StagedWorkspace& ws, char* base, const void* q,
-                                 const void* k, const void* v, const float* g, const void* beta, const float* h0,
-                                 void* o, float* h_final, cudaStream_t s, unsigned int* err) {
-    const int per = (d.NT + pieces - 1) / pieces;
+int overlap_pieces(const gdr::Dims& d, Path path, int S) {
+    int bounds[kMaxPieces + 1];
+    return overlap_bounds(d, path, S, bounds);
+}
+
+gdr_status forward_tc_overlapped(const gdr::Dims& d, const int* bounds, int pieces, const StagedWorkspace& ws,
+                                 char* base, const void* q, const void* k, const void* v, const float* g,
+                                 const void* beta, const float* h0, void* o, float* h_final, cudaStream_t s,
+                                 unsigned int* err) {
     const size_t e = 2;                                 // bf16
     float* carry = reinterpret_cast<float*>(base + ws.carry);
     const size_t state = (size_t)d.H * d.K * d.V;
     for (int i = 0; i < pieces; ++i) {
-        const int c0 = i * per, c1 = std::min(d.NT, c0 + per);
+        const int c0 = bounds[i], c1 = bounds[i + 1];
         const int64_t t0 = (int64_t)c0 * d.C, t1 = std::min<int64_t>(d.T, (int64_t)c1 * d.C);
         gdr::Dims dp = d;
         dp.T = (int)(t1 - t0);
@@ -602,7 +625,8 @@ gdr_status gdr_forward(const gdr_problem* p, const void* q, const void* k, const
     if ((st = pick_forward(p, d, &path)) != GDR_OK) return st;
     int S = 1;
     if ((st = resolve_segments(p, d, path != Path::Simt, &S)) != GDR_OK) return st;
-    const int pieces = overlap_pieces(d, path, S);
+    int bounds[kMaxPieces + 1];
+    const int pieces = overlap_bounds(d, path, S, bounds);
     const StagedWorkspace ws = plan_staged(d, path == Path::Fused || path == Path::FusedTc, S, pieces);
     if (!workspace || workspace_bytes < ws.total) return GDR_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GDR_ERR_ALIGN;
@@ -615,7 +639,8 @@ gdr_status gdr_forward(const gdr_problem* p, const void* q, const void* k, const
     cudaStream_t s = (cudaStream_t)stream;
     unsigned int* err = path == Path::Simt ? nullptr : device_error_word();
     if (pieces > 1) {
-        if ((st = forward_tc_overlapped(d, pieces, ws, base, q, k, v, g, beta, h0, o, h_final, s, err)) != GDR_OK)
+        if ((st = forward_tc_overlapped(d, bounds, pieces, ws, base, q, k, v, g, beta, h0, o, h_final, s, err)) !=
+            GDR_OK)
             return st;
     } else if (path == Path::Simt) {
         if ((st = from_cuda(gdr::simt_prepare(d, k, v, g, beta, w, u, g_cum, s))) != GDR_OK) return st;

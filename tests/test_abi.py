@@ -163,19 +163,39 @@ def test_fused_workspace_size_formula(lib):
             p = gdr.make_problem(B, T, H, K, V, C, 1, False, variant=variant, segments=1)
             extra = 0
             if variant == "auto" and B == 1 and K == V == 128 and -(-T // C) >= 128:
-                # AUTO runs one long sequence on the overlapped tcgen05 path: 8 pieces of 64 chunks here, the
-                # state carried between them in fp32
-                extra = r(7 * H * K * V * 4)
+                # AUTO runs one long sequence on the overlapped tcgen05 path: 7 pieces here, the state carried
+                # between them in fp32
+                extra = r((overlap_pieces(-(-T // C)) - 1) * H * K * V * 4)
             assert lib.gdr_forward_workspace_bytes(ctypes.byref(p)) == want + extra
 
 
+def overlap_pieces(NT, first=16, most=32):
+    """The overlapped forward's piece count for NT chunks: sizes grow from 16 chunks by 3/2, never below an
+    equal share of what is left among the pieces still allowed (at most 32); none below 128 chunks."""
+    if NT < 128:
+        return 1
+    n = c = 0
+    ln = first
+    while c < NT:
+        ln = max(ln, -(-(NT - c) // (most - n)))
+        c = min(NT, c + ln)
+        n += 1
+        ln += ln // 2
+    return n
+
+
+def test_overlap_piece_rule():
+    assert [overlap_pieces(n) for n in (64, 127, 128, 131, 193, 512, 2560, 100000)] == [1, 1, 4, 5, 5, 7, 7, 7]
+
+
 def test_overlapped_fused_tc_workspace(lib):
-    # one sequence on the tcgen05 fused path runs in pieces of at least 64 chunks (at most 16 pieces); the
-    # workspace adds the fp32 state carried between pieces, [pieces - 1][H, K, V]
+    # one sequence on the tcgen05 fused path runs in pieces; the workspace adds the fp32 state carried
+    # between pieces, [pieces - 1][H, K, V]
     r = lambda x: (x + 255) // 256 * 256
-    for (T, H, pieces) in [(64 * 64, 2, 1), (64 * 64 + 1, 2, 2), (32768, 32, 8), (64 * 64 * 40, 1, 16)]:
+    for (T, H) in [(64 * 64, 2), (64 * 128, 2), (64 * 131 - 10, 3), (32768, 32), (64 * 2560, 1)]:
         rows = T * H
         NT = -(-T // 64)
+        pieces = overlap_pieces(NT)
         base = r(rows * 4) + r(rows * 128 * 2) + r(rows * 128 * 2) + r(NT * H * 64 * 64 * 2)
         want = base + (r((pieces - 1) * H * 128 * 128 * 4) if pieces > 1 else 0)
         p = gdr.make_problem(1, T, H, 128, 128, 64, 1, False, variant="fused_tc", segments=1)

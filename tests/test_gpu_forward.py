@@ -321,11 +321,11 @@ def test_constant_per_key_gate_is_the_scalar_gate(shape, variant, dtype):
 
 # ---------------------------------------------------------------- the overlapped tcgen05 forward
 
-@pytest.mark.parametrize("T,H", [(64 * 64 * 3 + 100, 2), (64 * 128, 3), (64 * 64 + 64, 1)])
+@pytest.mark.parametrize("T,H", [(64 * 64 * 3 + 100, 2), (64 * 128, 3), (64 * 131, 1)])
 def test_overlapped_fused_tc_single_sequence(T, H):
-    # one sequence on the tcgen05 fused path runs in pieces of 64 chunks, each piece's scan overlapping the
-    # next piece's prepare on an internal stream, the state carried between pieces: every head against the
-    # token oracle (a partial last chunk in the first case, a single-chunk last piece in the last)
+    # one sequence on the tcgen05 fused path runs in pieces (16, 24, 36, 54, ... chunks), each piece's
+    # prepare overlapping the previous piece's scan, the state carried between pieces: every head against
+    # the token oracle (a partial last chunk in the first case, a single-chunk last piece in the last)
     x = make_inputs(1, T, H, 128, 128, io_dtype=torch.bfloat16, with_h0=True, seed=41)
     o, hf, ran = gpu_forward(x, 64, "fused_tc")
     assert ran == "fused_tc"

@@ -21,8 +21,12 @@
 //   h^T  = exp(G_last) h^T + dh^T   CUDA cores; h stays fp32 in registers for the whole sequence
 //   o    = scale (exp(G_t) O1^T + O2^T), stored by the same threads (thread = value column)
 //
-// The chain's two products (D, dh) are issued first; the output's two trail them on the tensor
-// pipe and run while the CUDA cores update h, so h_c^T is double-buffered by chunk parity.
+// Issue order per chunk c: D(c); then O2(c-1), which runs while the CUDA cores form v'(c); dh(c);
+// then O1(c), which runs while they update h.  The o epilogue of chunk c-1 runs in the chain warps
+// while the tensor cores form dh(c), so neither output product nor the o stores sit between the two
+// chain products.  h_c^T and v'^T are double-buffered by chunk parity for the trailing output products.
+// The fp32 element work uses the packed two-lane forms (__ffma2_rn, __fmul2_rn), which round each lane
+// exactly like the scalar operations.
 //
 // Warp roles: warp 0 loads each chunk's w, q, k, u, P by TMA into a 3-stage ring and forms
 // gamma, exp(G), exp(G_last), reading the next chunk's gate while this one's tiles land; warp 1
@@ -33,12 +37,13 @@
 // through its normal exit.
 //
 // Where it pays: one CTA carries a whole head, so a problem needs B*H CTAs here against
-// B*H*V/32 for the warp-level kernel of fused_mma.cu, but each chunk step costs about 3,200 SM
+// B*H*V/32 for the warp-level kernel of fused_mma.cu, but each chunk step costs about 2,800 SM
 // cycles here against about 2,400 there (the per-element work of v', h and o on one SM's four
-// schedulers, between two dependent MMA round trips).  Measured on the 2048-token, 64-head
-// workload (256 warp-level CTAs, two waves): 0.060 ms here, 0.085 ms there; on the 32k-token,
-// 32-head one (128 CTAs, one wave): 0.795 ms here, 0.601 ms there.  Variant AUTO therefore
-// takes this kernel when the warp-level grid would not fit one wave of the GPU.
+// schedulers, between two dependent MMA round trips; the 256 two-byte-per-lane o stores of a chunk
+// alone cost about 400).  Measured on the 2048-token, 64-head workload (256 warp-level CTAs, two
+// waves): 0.058 ms here, 0.085 ms there; on the 32k-token, 32-head one (128 CTAs, one wave): 0.689 ms
+// here, 0.601 ms there.  Variant AUTO therefore takes this kernel when the warp-level grid would not
+// fit one wave of the GPU, and for one long sequence, whose pieces overlap their prepares with it.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -72,11 +77,11 @@ struct TcLayout {
 
 // tensor-memory columns (512 allocated)
 constexpr uint32_t cHB = 0;      // h_c^T bf16 [128 v][128 key]: two buffers of 64 columns (chunk parity)
-constexpr uint32_t cVP = 128;    // v'^T bf16 [128 v][64 t]: 32 columns
-constexpr uint32_t cVG = 160;    // (v' diag gamma)^T bf16: 32 columns
-constexpr uint32_t cD = 192;     // D^T fp32 (64 columns), then dh^T fp32 (128 columns)
-constexpr uint32_t cO1 = 320;    // O1^T fp32, 64 columns
-constexpr uint32_t cO2 = 384;    // O2^T fp32, 64 columns
+constexpr uint32_t cVP = 128;    // v'^T bf16 [128 v][64 t]: two buffers of 32 columns (chunk parity)
+constexpr uint32_t cVG = 192;    // (v' diag gamma)^T bf16: 32 columns
+constexpr uint32_t cD = 256;     // D^T fp32 (64 columns), then dh^T fp32 (128 columns)
+constexpr uint32_t cO1 = 384;    // O1^T fp32, 64 columns
+constexpr uint32_t cO2 = 448;    // O2^T fp32, 64 columns
 
 __device__ __forceinline__ void mma_ta(uint32_t d, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc, uint32_t acc) {
     asm volatile(
@@ -196,31 +201,40 @@ tc_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_const
         constexpr uint64_t kQoff = (L::Q - L::W) >> 4;   // the q tile's descriptors: w's plus this start offset
         constexpr uint32_t idT = bw::idesc_bf16(128, 64, 0, 0);     // N = 64 tokens, B K-major
         constexpr uint32_t idK = bw::idesc_bf16(128, 128, 0, 1);    // N = 128 keys, B MN-major
+        // O2 of a chunk: v'^T P^T, then its output and its stage are complete
+        auto issue_o2 = [&](int cc) {
+            const uint64_t so = (uint64_t)((cc % kNS) * L::kStage) >> 4;
+            const uint32_t vp = cVP + 32 * (cc & 1);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) mma_ta(tmem + cO2, tmem + vp + 8 * kk, pd[kk] + so, idT, kk > 0);
+            bw::mma_commit_warp(&barO);
+            bw::mma_commit_warp(&empty[cc % kNS]);
+        };
+        bool ok = true;
         for (int c = 0; c < NT; ++c) {
             const int s = c % kNS;
             const uint32_t hb = cHB + 64 * (c & 1);                 // h_c^T
             const uint64_t so = (uint64_t)(s * L::kStage) >> 4;     // the stage's start-address offset
-            if (!bw::mbar_wait(&full[s], (c / kNS) & 1, err, kDeviceErrTimeout)) break;
-            if (!bw::mbar_wait(&hbReady, c & 1, err, kDeviceErrTimeout)) break;
+            if (!bw::mbar_wait(&full[s], (c / kNS) & 1, err, kDeviceErrTimeout)) { ok = false; break; }
+            if (!bw::mbar_wait(&hbReady, c & 1, err, kDeviceErrTimeout)) { ok = false; break; }
             bw::tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) mma_ta(tmem + cD, tmem + hb + 8 * kk, wd[kk] + so, idT, kk > 0);
             bw::mma_commit_warp(&barD);
-            if (!bw::mbar_wait(&vpReady, c & 1, err, kDeviceErrTimeout)) break;
+            // the previous chunk's O2 runs while the CUDA cores form this chunk's v'
+            if (c >= 1) issue_o2(c - 1);
+            if (!bw::mbar_wait(&vpReady, c & 1, err, kDeviceErrTimeout)) { ok = false; break; }
             bw::tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) mma_ta(tmem + cD, tmem + cVG + 8 * kk, kd[kk] + so, idK, kk > 0);
             bw::mma_commit_warp(&barE);
-            // the output products trail the chain's: they run while the CUDA cores update h
-            if (c >= 1 && !bw::mbar_wait(&oFree, (c - 1) & 1, err, kDeviceErrTimeout)) break;
+            // O1 runs while the CUDA cores update h; the previous chunk's output must have been read
+            if (c >= 1 && !bw::mbar_wait(&oFree, (c - 1) & 1, err, kDeviceErrTimeout)) { ok = false; break; }
             bw::tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) mma_ta(tmem + cO1, tmem + hb + 8 * kk, wd[kk] + so + kQoff, idT, kk > 0);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) mma_ta(tmem + cO2, tmem + cVP + 8 * kk, pd[kk] + so, idT, kk > 0);
-            bw::mma_commit_warp(&barO);
-            bw::mma_commit_warp(&empty[s]);
         }
+        if (ok && NT > 0) issue_o2(NT - 1);
         // nothing of this CTA's may still be running on the tensor cores when it frees the TMEM
         bw::mma_commit_warp(&drain);
         bw::mbar_wait(&drain, 0, err, kDeviceErrTimeout);
@@ -244,10 +258,44 @@ tc_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_const
             __syncwarp();
             if (lane == 0) bw::mbar_arrive(&hbReady);
         };
+        // o = scale (exp(G_t) O1^T + O2^T) of chunk cc, tokens tok0 .. tok0 + 15; then its stage is released
+        auto epilogue = [&](int cc) -> bool {
+            if (!bw::mbar_wait(&barO, cc & 1, err, kDeviceErrTimeout)) return false;
+            bw::tc_fence_after();
+            float a[16], e[16];
+            bw::tmem_ld16(lb + cO1 + tok0, a);
+            bw::tmem_ld16(lb + cO2 + tok0, e);
+            bw::tmem_ld_wait();
+            bw::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) bw::mbar_arrive(&oFree);
+            const float* F = reinterpret_cast<const float*>(sm + L::F + (cc % kNS) * L::kF);
+            const int tt = cc * kC + tok0;
+            bf16* dst = o + (((int64_t)b * T + tt) * H + h) * kV + v;
+            const float4* e4 = reinterpret_cast<const float4*>(F + kC + tok0);
+#pragma unroll
+            for (int j4 = 0; j4 < 4; ++j4) {
+                const float4 eg = e4[j4];
+                const float2 r0 = __fmul2_rn(make_float2(scale, scale),
+                                             __ffma2_rn(make_float2(eg.x, eg.y), make_float2(a[4 * j4], a[4 * j4 + 1]),
+                                                        make_float2(e[4 * j4], e[4 * j4 + 1])));
+                const float2 r1 = __fmul2_rn(make_float2(scale, scale),
+                                             __ffma2_rn(make_float2(eg.z, eg.w), make_float2(a[4 * j4 + 2], a[4 * j4 + 3]),
+                                                        make_float2(e[4 * j4 + 2], e[4 * j4 + 3])));
+                const float r[4] = {r0.x, r0.y, r1.x, r1.y};
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (!GENERAL || tt + 4 * j4 + i < T) dst[(int64_t)(4 * j4 + i) * H * kV] = __float2bfloat16_rn(r[i]);
+            }
+            __syncwarp();
+            if (lane == 0) bw::mbar_arrive(&empty[cc % kNS]);
+            return true;
+        };
         store_h(0);
+        bool ok = true;
         for (int c = 0; c < NT; ++c) {
             const int s = c % kNS;
-            if (!bw::mbar_wait(&full[s], (c / kNS) & 1, err, kDeviceErrTimeout)) break;
+            if (!bw::mbar_wait(&full[s], (c / kNS) & 1, err, kDeviceErrTimeout)) { ok = false; break; }
             const unsigned char* us = sm + s * L::kStage + L::U;
             const float* F = reinterpret_cast<const float*>(sm + L::F + s * L::kF);
             float uu[16];
@@ -255,28 +303,39 @@ tc_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_const
             for (int j = 0; j < 16; ++j)
                 uu[j] = __bfloat162float(*reinterpret_cast<const bf16*>(us + (tok0 + j) * (kV * 2) + v * 2));
             // v'^T = u^T - D^T for tokens tok0 .. tok0 + 15
-            if (!bw::mbar_wait(&barD, c & 1, err, kDeviceErrTimeout)) break;
+            if (!bw::mbar_wait(&barD, c & 1, err, kDeviceErrTimeout)) { ok = false; break; }
             bw::tc_fence_after();
             {
                 float d[16];
                 bw::tmem_ld16(lb + cD + tok0, d);
                 bw::tmem_ld_wait();
                 uint32_t pv[8], pg[8];
+                const float4* g4 = reinterpret_cast<const float4*>(F + tok0);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const float x0 = uu[2 * j] - d[2 * j], x1 = uu[2 * j + 1] - d[2 * j + 1];
-                    pv[j] = bw::pack_bf16(x0, x1);
-                    pg[j] = bw::pack_bf16(x0 * F[tok0 + 2 * j], x1 * F[tok0 + 2 * j + 1]);
+                for (int j = 0; j < 4; ++j) {
+                    const float4 gm = g4[j];
+                    const float2 x0 = __ffma2_rn(make_float2(d[4 * j], d[4 * j + 1]), make_float2(-1.f, -1.f),
+                                                 make_float2(uu[4 * j], uu[4 * j + 1]));
+                    const float2 x1 = __ffma2_rn(make_float2(d[4 * j + 2], d[4 * j + 3]), make_float2(-1.f, -1.f),
+                                                 make_float2(uu[4 * j + 2], uu[4 * j + 3]));
+                    pv[2 * j] = bw::pack_bf16(x0.x, x0.y);
+                    pv[2 * j + 1] = bw::pack_bf16(x1.x, x1.y);
+                    const float2 y0 = __fmul2_rn(x0, make_float2(gm.x, gm.y));
+                    const float2 y1 = __fmul2_rn(x1, make_float2(gm.z, gm.w));
+                    pg[2 * j] = bw::pack_bf16(y0.x, y0.y);
+                    pg[2 * j + 1] = bw::pack_bf16(y1.x, y1.y);
                 }
-                tmem_st8(lb + cVP + tok0 / 2, pv);
+                tmem_st8(lb + cVP + 32 * (c & 1) + tok0 / 2, pv);
                 tmem_st8(lb + cVG + tok0 / 2, pg);
                 tmem_st_wait();
             }
             bw::tc_fence_before();
             __syncwarp();
             if (lane == 0) bw::mbar_arrive(&vpReady);
+            // the previous chunk's output, while the tensor cores form dh
+            if (c >= 1 && !epilogue(c - 1)) { ok = false; break; }
             // h^T = exp(G_last) h^T + dh^T for keys key0 .. key0 + 31
-            if (!bw::mbar_wait(&barE, c & 1, err, kDeviceErrTimeout)) break;
+            if (!bw::mbar_wait(&barE, c & 1, err, kDeviceErrTimeout)) { ok = false; break; }
             bw::tc_fence_after();
             {
                 float d[32];
@@ -284,31 +343,16 @@ tc_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_const
                 bw::tmem_ld_wait();
                 const float dec = F[2 * kC];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) hs[j] = fmaf(dec, hs[j], d[j]);
+                for (int j = 0; j < 16; ++j) {
+                    const float2 r = __ffma2_rn(make_float2(dec, dec), make_float2(hs[2 * j], hs[2 * j + 1]),
+                                                make_float2(d[2 * j], d[2 * j + 1]));
+                    hs[2 * j] = r.x;
+                    hs[2 * j + 1] = r.y;
+                }
             }
             store_h((c + 1) & 1);
-            // o = scale (exp(G_t) O1^T + O2^T) for tokens tok0 .. tok0 + 15
-            if (!bw::mbar_wait(&barO, c & 1, err, kDeviceErrTimeout)) break;
-            bw::tc_fence_after();
-            {
-                float a[16], e[16];
-                bw::tmem_ld16(lb + cO1 + tok0, a);
-                bw::tmem_ld16(lb + cO2 + tok0, e);
-                bw::tmem_ld_wait();
-                const int tt = c * kC + tok0;
-                bf16* dst = o + (((int64_t)b * T + tt) * H + h) * kV + v;
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    if (!GENERAL || tt + j < T)
-                        dst[(int64_t)j * H * kV] = __float2bfloat16_rn(scale * fmaf(F[kC + tok0 + j], a[j], e[j]));
-            }
-            bw::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                bw::mbar_arrive(&oFree);
-                bw::mbar_arrive(&empty[s]);
-            }
         }
+        if (ok && NT > 0) epilogue(NT - 1);
         if (h_final) {
 #pragma unroll
             for (int j = 0; j < 32; ++j) h_final[(state + key0 + j) * kV + v] = hs[j];

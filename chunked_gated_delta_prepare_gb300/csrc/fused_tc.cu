@@ -37,13 +37,14 @@
 // through its normal exit.
 //
 // Where it pays: one CTA carries a whole head, so a problem needs B*H CTAs here against
-// B*H*V/32 for the warp-level kernel of fused_mma.cu, but each chunk step costs about 2,800 SM
+// B*H*V/32 for the warp-level kernel of fused_mma.cu, but each chunk step costs about 2,700 SM
 // cycles here against about 2,400 there (the per-element work of v', h and o on one SM's four
-// schedulers, between two dependent MMA round trips; the 256 two-byte-per-lane o stores of a chunk
-// alone cost about 400).  Measured on the 2048-token, 64-head workload (256 warp-level CTAs, two
-// waves): 0.058 ms here, 0.085 ms there; on the 32k-token, 32-head one (128 CTAs, one wave): 0.689 ms
-// here, 0.601 ms there.  Variant AUTO therefore takes this kernel when the warp-level grid would not
-// fit one wave of the GPU, and for one long sequence, whose pieces overlap their prepares with it.
+// schedulers, between two dependent MMA round trips; the o stores of a chunk alone cost about 300,
+// with lanes v, v^1 trading halves of their token pairs so that each store writes two adjacent
+// columns).  Measured on the 2048-token, 64-head workload (256 warp-level CTAs, two waves): 0.056 ms
+// here, 0.085 ms there; on the 32k-token, 32-head one (128 CTAs, one wave): 0.670 ms here, 0.601 ms
+// there.  Variant AUTO therefore takes this kernel when the warp-level grid would not fit one wave
+// of the GPU, and for one long sequence, whose pieces overlap their prepares with it.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -271,8 +272,8 @@ tc_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_const
             if (lane == 0) bw::mbar_arrive(&oFree);
             const float* F = reinterpret_cast<const float*>(sm + L::F + (cc % kNS) * L::kF);
             const int tt = cc * kC + tok0;
-            bf16* dst = o + (((int64_t)b * T + tt) * H + h) * kV + v;
             const float4* e4 = reinterpret_cast<const float4*>(F + kC + tok0);
+            float r[16];
 #pragma unroll
             for (int j4 = 0; j4 < 4; ++j4) {
                 const float4 eg = e4[j4];
@@ -282,10 +283,19 @@ tc_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_const
                 const float2 r1 = __fmul2_rn(make_float2(scale, scale),
                                              __ffma2_rn(make_float2(eg.z, eg.w), make_float2(a[4 * j4 + 2], a[4 * j4 + 3]),
                                                         make_float2(e[4 * j4 + 2], e[4 * j4 + 3])));
-                const float r[4] = {r0.x, r0.y, r1.x, r1.y};
+                r[4 * j4] = r0.x; r[4 * j4 + 1] = r0.y; r[4 * j4 + 2] = r1.x; r[4 * j4 + 3] = r1.y;
+            }
+            // lanes v, v^1 swap halves of their token pairs: the even lane stores columns v, v+1 of token
+            // 2m, the odd lane columns v-1, v of token 2m+1 (one 4-byte store per pair of tokens)
+            const int odd = lane & 1;
+            bf16* dst = o + (((int64_t)b * T + tt + odd) * H + h) * kV + (v & ~1);
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    if (!GENERAL || tt + 4 * j4 + i < T) dst[(int64_t)(4 * j4 + i) * H * kV] = __float2bfloat16_rn(r[i]);
+            for (int m = 0; m < 8; ++m) {
+                const uint32_t pk = bw::pack_bf16(r[2 * m], r[2 * m + 1]);
+                const uint32_t ot = __shfl_xor_sync(0xffffffffu, pk, 1);
+                const uint32_t word = odd ? __byte_perm(ot, pk, 0x7632) : __byte_perm(pk, ot, 0x5410);
+                if (!GENERAL || tt + 2 * m + odd < T)
+                    *reinterpret_cast<uint32_t*>(dst + (int64_t)(2 * m) * H * kV) = word;
             }
             __syncwarp();
             if (lane == 0) bw::mbar_arrive(&empty[cc % kNS]);

@@ -680,6 +680,167 @@ gdr_status gdr_forward(const gdr_problem* p, const void* q, const void* k, const
     return GDR_OK;
 }
 
+// ---------------------------------------------------------------- the forward over host tensors
+namespace {
+
+constexpr int kHostPiecesDefault = 8;
+constexpr int kHostPiecesMax = 64;
+
+// Per token, the bytes of each host tensor the forward reads (q, k, v, g, beta) and writes (o).
+struct HostRows {
+    size_t q, k, v, g, beta, o;
+};
+HostRows host_rows(const gdr::Dims& d) {
+    const size_t e = d.bf16 || d.f16 ? 2 : 4;
+    return {(size_t)d.Hk * d.K * e, (size_t)d.Hk * d.K * e, (size_t)d.H * d.V * e,
+            (size_t)d.H * (d.per_k ? d.K : 1) * 4, (size_t)d.H * e, (size_t)d.H * d.V * e};
+}
+
+// Device scratch of the host forward: two slots of one piece's inputs and output, the two states the
+// pieces alternate between, h0, and one piece's gdr_forward workspace.
+struct HostScratch {
+    int pieces, chunks_per_piece;
+    size_t slot[2][6];   // q, k, v, g, beta, o
+    size_t state[2], h0, ws, ws_bytes, total;
+};
+
+bool plan_host(const gdr_problem* p, const gdr::Dims& d, int pieces_req, HostScratch* hs) {
+    int pieces = pieces_req > 0 ? pieces_req : kHostPiecesDefault;
+    pieces = std::min(std::min(pieces, kHostPiecesMax), d.NT);
+    const int cpp = (d.NT + pieces - 1) / pieces;   // chunks per piece; the last piece may be shorter
+    hs->pieces = (d.NT + cpp - 1) / cpp;
+    hs->chunks_per_piece = cpp;
+    const int64_t Tp = std::min<int64_t>((int64_t)cpp * d.C, d.T);
+    const HostRows r = host_rows(d);
+    const size_t rows[6] = {r.q, r.k, r.v, r.g, r.beta, r.o};
+    size_t off = 0;
+    for (int sl = 0; sl < 2; ++sl)
+        for (int i = 0; i < 6; ++i) {
+            hs->slot[sl][i] = off;
+            off = round_up(off + (size_t)d.B * Tp * rows[i], 256);
+        }
+    const size_t state = (size_t)d.B * d.H * d.K * d.V * 4;
+    hs->state[0] = off; off = round_up(off + state, 256);
+    hs->state[1] = off; off = round_up(off + state, 256);
+    hs->h0 = off;       off = round_up(off + state, 256);
+    // the workspace of the longest piece and of the last one (a different T may plan differently)
+    gdr_problem pp = *p;
+    pp.T = Tp;
+    size_t ws = gdr_forward_workspace_bytes(&pp);
+    const int64_t last = d.T - (int64_t)(hs->pieces - 1) * cpp * d.C;
+    pp.T = last;
+    ws = std::max(ws, gdr_forward_workspace_bytes(&pp));
+    hs->ws = off;
+    hs->ws_bytes = ws;
+    hs->total = round_up(off + ws, 256);
+    return true;
+}
+
+// One tensor's token range [t0, t0 + n) of every sequence: host [B, T, row] <-> device [B, n, row].
+cudaError_t copy_rows(void* dst, const void* src, size_t row, int B, int64_t T, int64_t t0, int64_t n, bool to_device,
+                      cudaStream_t s) {
+    if (to_device)
+        return cudaMemcpy2DAsync(dst, (size_t)n * row, static_cast<const char*>(src) + (size_t)t0 * row, (size_t)T * row,
+                                 (size_t)n * row, (size_t)B, cudaMemcpyHostToDevice, s);
+    return cudaMemcpy2DAsync(static_cast<char*>(dst) + (size_t)t0 * row, (size_t)T * row, src, (size_t)n * row,
+                             (size_t)n * row, (size_t)B, cudaMemcpyDeviceToHost, s);
+}
+
+}  // namespace
+
+size_t gdr_forward_host_scratch_bytes(const gdr_problem* p, int32_t pieces) {
+    gdr::Dims d;
+    if (check_problem(p, &d) != GDR_OK || pieces < 0) return 0;
+    HostScratch hs;
+    plan_host(p, d, pieces, &hs);
+    return hs.total;
+}
+
+gdr_status gdr_forward_host(const gdr_problem* p, const void* q, const void* k, const void* v, const float* g,
+                            const void* beta, const float* h0, void* o, float* h_final, int32_t pieces, void* scratch,
+                            size_t scratch_bytes, void* stream) {
+    gdr::Dims d;
+    gdr_status st = check_problem(p, &d);
+    if (st != GDR_OK) return st;
+    if (pieces < 0) return GDR_ERR_ARG;
+    if (!q || !k || !v || !g || !beta || !o) return GDR_ERR_NULL;
+    HostScratch hs;
+    plan_host(p, d, pieces, &hs);
+    if (!scratch || scratch_bytes < hs.total) return GDR_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(scratch) & 255u) != 0) return GDR_ERR_ALIGN;
+    char* base = static_cast<char*>(scratch);
+    cudaStream_t s = (cudaStream_t)stream;
+    const HostRows r = host_rows(d);
+    const size_t rows[6] = {r.q, r.k, r.v, r.g, r.beta, r.o};
+    const void* src[5] = {q, k, v, g, beta};
+    const size_t state = (size_t)d.B * d.H * d.K * d.V * 4;
+
+    // the copies run on two streams of this call's own; everything they do is ordered after the work
+    // already queued on `stream` (which may still be using the scratch) and before what follows there
+    cudaStream_t up = nullptr, down = nullptr;
+    cudaEvent_t start = nullptr, ready[2] = {}, done[2] = {}, out_free[2] = {}, fin = nullptr;
+    auto cleanup = [&]() {
+        for (cudaEvent_t e : {start, ready[0], ready[1], done[0], done[1], out_free[0], out_free[1], fin})
+            if (e) cudaEventDestroy(e);
+        if (up) cudaStreamDestroy(up);
+        if (down) cudaStreamDestroy(down);
+    };
+    auto fail = [&](cudaError_t e) {
+        cleanup();
+        return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+    };
+    cudaError_t e = cudaStreamCreateWithFlags(&up, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&down, cudaStreamNonBlocking);
+    for (cudaEvent_t* ev : {&start, &ready[0], &ready[1], &done[0], &done[1], &out_free[0], &out_free[1], &fin})
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventRecord(start, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(up, start, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(down, start, 0);
+    const float* h_prev = nullptr;
+    if (h0 && e == cudaSuccess) {
+        e = cudaMemcpyAsync(base + hs.h0, h0, state, cudaMemcpyHostToDevice, s);
+        h_prev = reinterpret_cast<const float*>(base + hs.h0);
+    }
+    if (e != cudaSuccess) return fail(e);
+
+    const int64_t per = (int64_t)hs.chunks_per_piece * d.C;
+    for (int i = 0; i < hs.pieces; ++i) {
+        const int sl = i & 1;
+        const int64_t t0 = (int64_t)i * per, n = std::min<int64_t>(per, d.T - t0);
+        char* buf[6];
+        for (int j = 0; j < 6; ++j) buf[j] = base + hs.slot[sl][j];
+        // inputs of piece i, once piece i - 2 has finished reading this slot
+        if (i >= 2) e = cudaStreamWaitEvent(up, done[sl], 0);
+        for (int j = 0; j < 5 && e == cudaSuccess; ++j) e = copy_rows(buf[j], src[j], rows[j], d.B, d.T, t0, n, true, up);
+        if (e == cudaSuccess) e = cudaEventRecord(ready[sl], up);
+        // piece i on the caller's stream, from the state piece i - 1 left, once its output slot is free
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ready[sl], 0);
+        if (e == cudaSuccess && i >= 2) e = cudaStreamWaitEvent(s, out_free[sl], 0);
+        if (e != cudaSuccess) return fail(e);
+        gdr_problem pp = *p;
+        pp.T = n;
+        float* hout = reinterpret_cast<float*>(base + hs.state[sl]);
+        st = gdr_forward(&pp, buf[0], buf[1], buf[2], reinterpret_cast<const float*>(buf[3]), buf[4], h_prev, buf[5],
+                         hout, base + hs.ws, hs.ws_bytes, s);
+        if (st != GDR_OK) {
+            fail(cudaSuccess);
+            return st;
+        }
+        h_prev = hout;
+        e = cudaEventRecord(done[sl], s);
+        // its output back to the host
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(down, done[sl], 0);
+        if (e == cudaSuccess) e = copy_rows(o, buf[5], rows[5], d.B, d.T, t0, n, false, down);
+        if (e == cudaSuccess) e = cudaEventRecord(out_free[sl], down);
+        if (e != cudaSuccess) return fail(e);
+    }
+    if (h_final) e = cudaMemcpyAsync(h_final, h_prev, state, cudaMemcpyDeviceToHost, s);
+    // `stream` completes only after the last output copy
+    if (e == cudaSuccess) e = cudaEventRecord(fin, down);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, fin, 0);
+    return fail(e);
+}
+
 gdr_status gdr_scan_output(const gdr_problem* p, const void* q, const void* k, const void* w, const void* u,
                            const float* g_cum, const void* P, const float* h0, void* o, float* h_final,
                            void* stream) {

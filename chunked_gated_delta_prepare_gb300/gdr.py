@@ -36,6 +36,7 @@ STATUS_NAMES = {0: "GDR_OK", 1: "GDR_ERR_NULL", 2: "GDR_ERR_SHAPE", 3: "GDR_ERR_
 DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
 VARIANTS = {"auto": 0, "simt": 1, "tensor": 2, "fused": 3, "fused_tc": 4}
 EXPORTS = ["gdr_prepare_wy", "gdr_scan_h", "gdr_chunk_output", "gdr_forward", "gdr_forward_workspace_bytes",
+           "gdr_forward_host", "gdr_forward_host_scratch_bytes",
            "gdr_forward_static_scratch", "gdr_scan_output", "gdr_prepare_wyp",
            "gdr_bwd_dv_local", "gdr_bwd_scan_dh", "gdr_bwd_dqkwg", "gdr_bwd_wy", "gdr_backward",
            "gdr_backward_workspace_bytes", "gdr_bwd_prepare", "gdr_bwd_scan_dh_p", "gdr_bwd_wy_dqkg",
@@ -85,6 +86,8 @@ def load(path: str | None = None):
             "gdr_scan_output": [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp],
             "gdr_prepare_wyp": [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp],
             "gdr_forward_workspace_bytes": [P],
+            "gdr_forward_host": [P, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int32, vp, ctypes.c_size_t, vp],
+            "gdr_forward_host_scratch_bytes": [P, ctypes.c_int32],
             "gdr_bwd_dv_local": [P, vp, vp, vp, vp, vp, vp],
             "gdr_bwd_scan_dh": [P] + [vp] * 11,
             "gdr_bwd_dqkwg": [P] + [vp] * 14,
@@ -116,6 +119,7 @@ def load(path: str | None = None):
             f.argtypes = args
             f.restype = ctypes.c_int
         lib.gdr_forward_workspace_bytes.restype = ctypes.c_size_t
+        lib.gdr_forward_host_scratch_bytes.restype = ctypes.c_size_t
         lib.gdr_backward_workspace_bytes.restype = ctypes.c_size_t
         lib.gdr_varlen_forward_workspace_bytes.restype = ctypes.c_size_t
         lib.gdr_varlen_backward_workspace_bytes.restype = ctypes.c_size_t
@@ -229,6 +233,18 @@ def gdr_forward(p, q, k, v, g, beta, h0, o, h_final, workspace, workspace_bytes,
            "gdr_forward")
 
 
+def gdr_forward_host_scratch_bytes(p, pieces=0) -> int:
+    return int(load().gdr_forward_host_scratch_bytes(ctypes.byref(p), int(pieces)))
+
+
+def gdr_forward_host(p, q, k, v, g, beta, h0, o, h_final, pieces, scratch, scratch_bytes, stream=None):
+    """gdr_forward over host tensors (q .. beta, h0 in, o and h_final out, all host memory), pipelined
+    against the host link inside the library (see include/gdr.h)."""
+    _check(load().gdr_forward_host(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
+                                   _ptr(o), _ptr(h_final), int(pieces), _ptr(scratch), int(scratch_bytes),
+                                   _stream(stream)), "gdr_forward_host")
+
+
 def gdr_forward_static_scratch(p, q, k, v, g, beta, h0, o, h_final, stream=None):
     """gdr_forward with the scratch taken from the library's fixed device array
     (for callers that cannot allocate device memory; see include/gdr.h)."""
@@ -265,79 +281,27 @@ def gdr_version() -> int:
 
 # ---------------------------------------------------------------- convenience
 
-def _host_pieces(T: int, chunk: int, pieces: int):
-    """Token ranges of whole chunks (the last one may end in a partial chunk) for a pipelined forward."""
-    nt = -(-T // chunk)
-    n = max(1, min(pieces, nt))
-    per = -(-nt // n) * chunk
-    return [(t0, min(T, t0 + per)) for t0 in range(0, T, per)]
-
-
-def _forward_host_pipelined(q, k, v, g, beta, h0, chunk, scale, variant, want_h_final, stream, segments, out,
-                            h_final_out, pieces, workspace):
-    """forward() for host tensors, in token pieces of whole chunks: piece i's inputs go to the device on one
-    stream while piece i - 1 computes on the current stream (from the state piece i - 2 left) and piece
-    i - 2's output returns on a third.  The chunking and the fp32 state carried between pieces are those of
-    one call over the whole sequence, so the results are the same."""
+def _forward_host(q, k, v, g, beta, h0, chunk, scale, variant, want_h_final, stream, segments, out, h_final_out,
+                  pieces, workspace):
+    """forward() for host tensors through gdr_forward_host: the library runs the sequence in token pieces
+    of whole chunks and overlaps each piece's copies with the computation of its neighbours, carrying the
+    fp32 state between pieces, so the results are those of one call over the whole sequence."""
     dev = torch.device("cuda", torch.cuda.current_device())
-    B, T, Hq, K = q.shape
+    B, T, _, K = q.shape
     H, V = v.shape[2], v.shape[-1]
-    cs = torch.cuda.current_stream() if stream is None else stream
-    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    srcs = [t.contiguous() for t in (q, k, v, g, beta)]
+    h0 = h0.contiguous() if h0 is not None else None
+    p = problem_for(q, v, g, chunk, scale, variant, segments)
     o = out if out is not None else torch.empty(B, T, H, V, dtype=q.dtype, pin_memory=True)
-    ranges = _host_pieces(T, chunk, pieces)
-    Tp = ranges[0][1] - ranges[0][0]
-    srcs = (q, k, v, g, beta)
-
-    def piece_buffers():
-        return [torch.empty((B, Tp) + tuple(t.shape[2:]), dtype=t.dtype, device=dev) for t in srcs] + \
-               [torch.empty(B, Tp, H, V, dtype=q.dtype, device=dev)]
-    bufs = [piece_buffers(), piece_buffers()]
-    states = [torch.empty(B, H, K, V, dtype=torch.float32, device=dev) for _ in range(2)]
-    h_prev = h0.to(dev, non_blocking=True) if h0 is not None else None
-    in_free = [torch.cuda.Event(), torch.cuda.Event()]     # piece buffers free for the next upload
-    out_free = [torch.cuda.Event(), torch.cuda.Event()]    # output buffers read by the download
-    ws = workspace
-    for i, (t0, t1) in enumerate(ranges):
-        bi, n = i % 2, t1 - t0
-        buf = bufs[bi]
-        with torch.cuda.stream(up):
-            if i >= 2:
-                up.wait_event(in_free[bi])
-            for d, src in zip(buf[:5], srcs):
-                for b in range(B):
-                    d[b, :n].copy_(src[b, t0:t1], non_blocking=True)
-            ready = torch.cuda.Event()
-            ready.record(up)
-        cs.wait_event(ready)
-        if i >= 2:
-            cs.wait_event(out_free[bi])
-        with torch.cuda.stream(cs):
-            views = [t[:, :n] if n == Tp else t[:, :n].contiguous() for t in buf]
-            p = problem_for(views[0], views[2], views[3], chunk, scale, variant, segments)
-            nbytes = gdr_forward_workspace_bytes(p)
-            if nbytes and (ws is None or ws.numel() * ws.element_size() < nbytes):
-                ws = torch.empty(nbytes, device=dev, dtype=torch.uint8)
-            hs = states[bi]
-            gdr_forward(p, *views[:5], h_prev, views[5], hs, ws, 0 if ws is None else ws.numel() * ws.element_size(),
-                        cs)
-            h_prev = hs
-            in_free[bi].record(cs)
-            done = torch.cuda.Event()
-            done.record(cs)
-        views[5].record_stream(down)   # a fresh tensor for a short last piece of B > 1 sequences
-        with torch.cuda.stream(down):
-            down.wait_event(done)
-            for b in range(B):
-                o[b, t0:t1].copy_(views[5][b], non_blocking=True)
-            out_free[bi].record(down)
     hf = None
     if want_h_final:
-        hf = h_final_out if h_final_out is not None else torch.empty(B, H, K, V, dtype=torch.float32)
-        with torch.cuda.stream(cs):
-            hf.copy_(h_prev, non_blocking=True)
-    cs.wait_stream(down)
-    cs.synchronize()
+        hf = h_final_out if h_final_out is not None else torch.empty(B, H, K, V, dtype=torch.float32, pin_memory=True)
+    nbytes = gdr_forward_host_scratch_bytes(p, pieces)
+    ws = workspace
+    if ws is None or not ws.is_cuda or ws.numel() * ws.element_size() < nbytes:
+        ws = torch.empty(nbytes, device=dev, dtype=torch.uint8)
+    gdr_forward_host(p, *srcs, h0, o, hf, pieces, ws, ws.numel() * ws.element_size(), stream)
+    (torch.cuda.current_stream() if stream is None else stream).synchronize()
     return o, hf
 
 
@@ -348,14 +312,15 @@ def forward(q, k, v, g, beta, h0=None, *, chunk=64, scale=None, variant="auto", 
     Device tensors are used in place.  CPU tensors (pinned for asynchronous
     copies) go to the current CUDA device and the results come back: into `out`
     / `h_final_out` when given (host tensors of o's and h_final's shape and
-    dtype), else into new pinned host tensors.  Host inputs run in `pieces`
-    token ranges of whole chunks, so the copies overlap the kernels (pieces=1:
-    one copy in, one call, one copy out).  The results are complete on return.
+    dtype), else into new pinned host tensors.  Host inputs go through
+    gdr_forward_host in `pieces` token ranges of whole chunks, so the copies
+    overlap the kernels (pieces=1: one copy in, one call, one copy out).  The
+    results are complete on return.
     """
     on_host = q.device.type == "cpu"
     if on_host and pieces > 1 and -(-q.shape[1] // chunk) >= 2:
-        return _forward_host_pipelined(q, k, v, g, beta, h0, chunk, scale, variant, want_h_final, stream, segments,
-                                       out, h_final_out, pieces, workspace)
+        return _forward_host(q, k, v, g, beta, h0, chunk, scale, variant, want_h_final, stream, segments, out,
+                             h_final_out, pieces, workspace)
     if on_host:
         dev = torch.device("cuda", torch.cuda.current_device())
         q, k, v, g, beta = (t.to(dev, non_blocking=True) for t in (q, k, v, g, beta))

@@ -260,6 +260,38 @@ GDR_API gdr_status gdr_forward(const gdr_problem* p, const void* q, const void* 
                        float* h_final, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * The whole forward over HOST tensors, for callers whose inputs and outputs live in
+ * host memory.  The method pages have no counterpart to this call; it is a
+ * deployment aid that hides the host link behind the computation.
+ *
+ * The sequence runs in `pieces` token ranges of whole chunks (every sequence of the
+ * batch alike).  While piece i computes on `stream` (gdr_forward on the piece, from
+ * the fp32 state piece i-1 left), the inputs of piece i+1 travel to the device and
+ * the output of piece i-1 back to the host, each on a stream the call creates and
+ * releases itself.  The chunking and the state carried between pieces are those of
+ * one gdr_forward over the whole sequence, so the results equal gdr_forward's for
+ * the variant the pieces run (each piece is its own problem of T_piece tokens, on
+ * which AUTO may choose another variant than on the whole).
+ * Inputs:  q, k, v, g, beta, h0 as gdr_forward's, in host memory.  Page-locked
+ *          memory (cudaHostAlloc, cudaHostRegister) lets the copies overlap the
+ *          computation; pageable memory works, with the copies serialised.
+ * Outputs: o, h_final as gdr_forward's, in host memory (h_final NULL: not written).
+ * pieces:  0 selects 8; at most 64 and at most the chunk count are used.
+ * scratch: device memory of at least gdr_forward_host_scratch_bytes(p, pieces)
+ *          bytes, 256-byte aligned, owned by the caller: two pieces' inputs and
+ *          outputs, the states and one piece's gdr_forward workspace.
+ * Asynchronous like every call: everything it queues is ordered after the work
+ * already on `stream`, and the results are in host memory once `stream` has
+ * completed (cudaStreamSynchronize).  The host buffers must stay valid until then.
+ * Returns GDR_ERR_WORKSPACE for a missing or short scratch, GDR_ERR_ARG for
+ * pieces < 0, and gdr_forward's codes for the problem.
+ */
+GDR_API size_t gdr_forward_host_scratch_bytes(const gdr_problem* p, int32_t pieces);
+GDR_API gdr_status gdr_forward_host(const gdr_problem* p, const void* q, const void* k, const void* v,
+                                   const float* g, const void* beta, const float* h0, void* o, float* h_final,
+                                   int32_t pieces, void* scratch, size_t scratch_bytes, void* stream);
+
+/*
  * gdr_forward without a workspace argument, for callers that cannot allocate
  * device memory themselves (for example a plugin whose host framework owns all
  * device memory, or a latency-critical loop that must not call cudaMalloc).

@@ -402,3 +402,42 @@ def test_library_exports_only_the_c_abi(lib):
     names = [ln.split()[-1] for ln in out.stdout.splitlines() if ln.strip()]
     exported = {n for n in names if not n.startswith("_ZZ")}
     assert exported == set(declared_functions())
+
+
+def test_host_forward_scratch_formula(lib):
+    # two slots of one piece's q, k, v, g, beta and o ([B, T_piece, ...], each rounded up to 256 bytes),
+    # three fp32 states [B, HV, K, V] (two alternating, h0), then gdr_forward's workspace for the longest
+    # piece and for the last one, whichever is larger
+    r = lambda x: (x + 255) // 256 * 256
+    for (B, T, H, HV, K, V, C, bf16, per_k, pieces) in [(1, 32768, 32, 32, 128, 128, 64, 1, False, 8),
+                                                        (2, 1000, 2, 4, 128, 128, 64, 1, False, 5),
+                                                        (2, 700, 3, 3, 64, 64, 32, 0, True, 0),
+                                                        (1, 100, 1, 1, 64, 64, 64, 1, False, 64)]:
+        p = gdr.make_problem(B, T, H, K, V, C, 1 if bf16 else 0, per_k, HV=HV if HV != H else 0)
+        e = 2 if bf16 else 4
+        nt = -(-T // C)
+        n = min(pieces or 8, 64, nt)
+        cpp = -(-nt // n)
+        Tp = min(cpp * C, T)
+        last = T - (-(-nt // cpp) - 1) * cpp * C
+        rows = [H * K * e, H * K * e, HV * V * e, HV * (K if per_k else 1) * 4, HV * e, HV * V * e]
+        want = 2 * sum(r(B * Tp * x) for x in rows) + 3 * r(B * HV * K * V * 4)
+        ws = 0
+        for t in (Tp, last):
+            pp = gdr.make_problem(B, t, H, K, V, C, 1 if bf16 else 0, per_k, HV=HV if HV != H else 0)
+            ws = max(ws, lib.gdr_forward_workspace_bytes(ctypes.byref(pp)))
+        want = r(want + ws)
+        assert lib.gdr_forward_host_scratch_bytes(ctypes.byref(p), pieces) == want
+    p = gdr.make_problem(1, 256, 2, 64, 64, 64, 1, False)
+    assert lib.gdr_forward_host_scratch_bytes(ctypes.byref(p), -1) == 0
+
+
+def test_host_forward_rejects_bad_arguments_before_launching(lib):
+    p = gdr.make_problem(1, 256, 2, 64, 64, 64, 1, False)
+    a = ctypes.c_void_p(16)
+    args = [a] * 5
+    assert lib.gdr_forward_host(ctypes.byref(p), *args, None, a, None, 0, None, 0, None) == 5   # no scratch
+    assert lib.gdr_forward_host(ctypes.byref(p), *args, None, a, None, -2, a, 1 << 40, None) == 9
+    assert lib.gdr_forward_host(ctypes.byref(p), None, *args[1:], None, a, None, 0, a, 1 << 40, None) == 1
+    bad = gdr.make_problem(1, 256, 2, 96, 64, 64, 1, False)
+    assert lib.gdr_forward_host(ctypes.byref(bad), *args, None, a, None, 0, a, 1 << 40, None) == 2

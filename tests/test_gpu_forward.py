@@ -1,3 +1,4 @@
+import ctypes
 """Whole-forward parity on the GPU (gdr_forward through the C ABI) against the
 float64 token-recurrence oracle, plus invariants and edge cases."""
 import itertools
@@ -208,6 +209,63 @@ def test_pipelined_host_forward_equals_one_device_call(shape, per_k, variant):
     o_p, hf_p = gdr.forward(*hx, chunk=64, variant=variant, pieces=4)
     o_1, hf_1 = gdr.forward(*(t.cuda() for t in hx), chunk=64, variant=variant)
     assert torch.equal(o_p, o_1.cpu()) and torch.equal(hf_p, hf_1.cpu())
+
+
+def _host_problem(x, chunk, variant):
+    p = gdr.problem_for(x.q, x.v, x.g, chunk, None, variant)
+    return p
+
+
+@pytest.mark.parametrize("pinned", [True, False])
+def test_host_forward_pageable_and_grouped_heads(pinned):
+    # grouped value heads (HV = 2 H), a ragged last piece and h_final omitted; pageable host memory
+    # serialises the copies but gives the same bits
+    x = grouped_inputs(2, 1000, 2, 2, 128, 128, io_dtype=torch.bfloat16, with_h0=True, seed=23)
+    hx = [t.pin_memory() if pinned else t.contiguous() for t in (x.q, x.k, x.v, x.g, x.beta, x.h0)]
+    o_p, hf_p = gdr.forward(*hx, chunk=64, pieces=5, want_h_final=False)
+    assert hf_p is None
+    o_1, _ = gdr.forward(*(t.cuda() for t in hx), chunk=64)
+    assert torch.equal(o_p, o_1.cpu())
+
+
+def test_host_forward_calls_queue_behind_each_other():
+    # two calls on one stream and one scratch, no synchronisation between them: the second call's
+    # uploads wait for the first call's work on the stream
+    x1 = make_inputs(1, 2048, 4, 128, 128, io_dtype=torch.bfloat16, with_h0=True, seed=24)
+    x2 = make_inputs(1, 2048, 4, 128, 128, io_dtype=torch.bfloat16, with_h0=True, seed=25)
+    p = _host_problem(x1, 64, "auto")
+    nb = gdr.gdr_forward_host_scratch_bytes(p, 8)
+    ws = torch.empty(nb, device="cuda", dtype=torch.uint8)
+    outs = []
+    for x in (x1, x2):
+        hx = [t.pin_memory() for t in (x.q, x.k, x.v, x.g, x.beta, x.h0)]
+        o = torch.empty(x.v.shape, dtype=torch.bfloat16, pin_memory=True)
+        hf = torch.empty(x.h0.shape, dtype=torch.float32, pin_memory=True)
+        gdr.gdr_forward_host(p, *hx, o, hf, 8, ws, nb)
+        outs.append((hx, o, hf))
+    torch.cuda.synchronize()
+    for hx, o, hf in outs:
+        o_1, hf_1 = gdr.forward(*(t.cuda() for t in hx), chunk=64)
+        assert torch.equal(o, o_1.cpu()) and torch.equal(hf, hf_1.cpu())
+
+
+def test_host_forward_argument_errors():
+    lib = gdr.load()
+    x = make_inputs(1, 256, 2, 64, 64, io_dtype=torch.bfloat16, seed=26)
+    p = _host_problem(x, 64, "auto")
+    hx = [t.pin_memory() for t in (x.q, x.k, x.v, x.g, x.beta)]
+    o = torch.empty(x.v.shape, dtype=torch.bfloat16, pin_memory=True)
+    nb = gdr.gdr_forward_host_scratch_bytes(p, 0)
+    ws = torch.empty(nb + 512, device="cuda", dtype=torch.uint8)
+    ptrs = [t.data_ptr() for t in hx]
+    call = lambda pieces, scr, n: lib.gdr_forward_host(ctypes.byref(p), *ptrs, None, o.data_ptr(), None, pieces, scr,
+                                                      n, None)
+    assert call(0, ws.data_ptr(), nb - 1) == 5             # GDR_ERR_WORKSPACE
+    assert call(0, None, nb) == 5
+    assert call(-1, ws.data_ptr(), nb) == 9                # GDR_ERR_ARG
+    assert call(0, ws.data_ptr() + 16, nb) == 4            # GDR_ERR_ALIGN
+    assert call(0, ws.data_ptr(), nb) == 0
+    torch.cuda.synchronize()
 
 
 @pytest.mark.parametrize("variant", ["fused", "fused_tc"])

@@ -170,7 +170,11 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
     __shared__ uint64_t bar_k, bar_q, bar_v;   // one per tile, each waited on just before its first use
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int t0 = blockIdx.x * kTile, h = blockIdx.y, b = blockIdx.z;
+    // CTAs run chunk-major, the sequence's last tile first, so the first chunks are the last written and
+    // still in L2 when the scan that follows reads them first (one grid dimension: tiles x heads)
+    const int ntiles = (T + kTile - 1) / kTile;
+    const int h = (int)(blockIdx.x % (unsigned)H), t0 = (ntiles - 1 - (int)(blockIdx.x / (unsigned)H)) * kTile;
+    const int b = blockIdx.z;
     const int hk = EXTRA ? h / G : h;                 // q/k head of value head h
     const int nout = min(kTile, T - t0);             // rows of the outputs (g_cum) this tile writes
     int nvalid = nout, t_in = t0, b_in = b, T_in = T; // input rows: how many are real tokens, and where
@@ -677,7 +681,7 @@ cudaError_t launch_prepare_v(const Dims& d, const void* q, const void* k, const 
     const size_t smem = L::bytes + 1024;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const dim3 grid((d.T + kTile - 1) / kTile, d.H, d.B);
+    const dim3 grid((unsigned)((d.T + kTile - 1) / kTile) * (unsigned)d.H, 1, d.B);
     if (pdl) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = grid;

@@ -154,6 +154,9 @@ tc_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_const
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
+        // launched as the programmatic dependent of the prepare, the only warp that reads what it wrote
+        // waits here for it to complete (a no-op after an ordinary launch)
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         const float* gr = g_cum + (int64_t)b * T * H + h;
         auto gat = [&](int t) { return gr[(int64_t)(GENERAL ? min(t, T - 1) : t) * H]; };   // past T: its last value
         float g0 = 0.f, g1 = 0.f, gl = 0.f;
@@ -381,7 +384,7 @@ bool tc_scan_output_supported(const Dims& d) {
 
 cudaError_t tc_scan_output(const Dims& d, const void* q, const void* k, const void* w, const void* u,
                            const float* g_cum, const void* P, const float* h0, void* o, float* h_final,
-                           cudaStream_t s, unsigned int* err) {
+                           cudaStream_t s, unsigned int* err, bool pdl) {
     if (!tc_scan_output_supported(d) || !P) return cudaErrorInvalidValue;
     CUtensorMap mw, mq, mk, mu, mp;
     if (!make_tmap_tokens(&mw, w, d.B, d.T, d.H, kK, kC) || !make_tmap_tokens(&mq, q, d.B, d.T, d.Hk, kK, kC) ||
@@ -396,6 +399,20 @@ cudaError_t tc_scan_output(const Dims& d, const void* q, const void* k, const vo
     auto kern = (d.T % kC != 0 || d.G != 1) ? tc_scan_output_kernel<true> : tc_scan_output_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
+    if (pdl) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(d.B * d.H);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, kern, mw, mq, mk, mu, mp, g_cum, h0, (bf16*)o, h_final, d.T, d.H, d.NT, d.G,
+                                  d.scale, err);
+    }
     kern<<<d.B * d.H, kThreads, smem, s>>>(mw, mq, mk, mu, mp, g_cum, h0, (bf16*)o, h_final, d.T, d.H, d.NT, d.G,
                                           d.scale, err);
     return cudaGetLastError();

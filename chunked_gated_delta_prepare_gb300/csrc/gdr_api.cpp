@@ -667,7 +667,7 @@ gdr_status gdr_forward(const gdr_problem* p, const void* q, const void* k, const
         }
         if (fused) {
             const cudaError_t e = path == Path::FusedTc
-                                      ? gdr::tc_scan_output(ds, q, k, w, u, g_cum, P, hs, o, hf, s, err)
+                                      ? gdr::tc_scan_output(ds, q, k, w, u, g_cum, P, hs, o, hf, s, err, S == 1)
                                       : gdr::mma_scan_output(ds, q, k, w, u, g_cum, P, hs, o, hf, s, err);
             if ((st = from_cuda(e)) != GDR_OK) return st;
         } else {

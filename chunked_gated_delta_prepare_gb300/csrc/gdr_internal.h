@@ -72,9 +72,11 @@ cudaError_t mma_scan_output(const Dims& d, const void* q, const void* k, const v
 // The same scan and output on the tcgen05 tensor cores, one CTA per (batch, head) (fused_tc.cu): bf16 io,
 // scalar gate, K = V = 128, C = 64 (any T, grouped value heads), and P from the prepare.
 bool tc_scan_output_supported(const Dims& d);
+// pdl: launch as the programmatic dependent of the stream's previous kernel (the prepare), which must
+// trigger early (griddepcontrol.launch_dependents); the scan's setup then runs under its tail.
 cudaError_t tc_scan_output(const Dims& d, const void* q, const void* k, const void* w, const void* u,
                            const float* g_cum, const void* P, const float* h0, void* o, float* h_final,
-                           cudaStream_t s, unsigned int* err);
+                           cudaStream_t s, unsigned int* err, bool pdl = false);
 
 // ---- backward stages on the CUDA cores (simt_backward.cu): every shape and io dtype;
 // intermediates fp32, see include/gdr.h for each stage's definition

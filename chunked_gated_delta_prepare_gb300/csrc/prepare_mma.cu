@@ -203,6 +203,10 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
         }
     };
     const uint32_t s_base = bw::smem_u32(sm);
+    // a kernel launched as this one's programmatic dependent (the tcgen05 scan after a prepare with P)
+    // may start its setup once every CTA of this grid has begun; it waits for this grid's completion
+    // before it reads anything written here
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // beta and (scalar gate) g of the tile, loaded first: their latency runs under the barrier setup and
     // the TMA issue (rows past T read as zero)
     float b_pre = 0.f, g_pre0 = 0.f, g_pre1 = 0.f;

@@ -80,6 +80,8 @@ def algorithmic_bytes(wl, kernel: str, with_p: bool = False, segs: int = 1) -> i
     if kernel == "scan_output":  # read q, k, w, u, g_cum (+ P); write o; state in and out
         per = 3 * K * e + 2 * V * e + gw + p_bytes
         return th * per + bh * state
+    if kernel == "gated_operands":   # per-key-dim gate: read q, k, g_cum; write P, qg, kg
+        return th * (2 * K * e + gw + C * e + 2 * K * e)
     if kernel == "transfer":     # read k, w, u, g_cum; write each segment's M [K,K] and Z [K,V] (fp32)
         per = 2 * K * e + V * e + gw
         return th * per + segs * bh * 4 * (K * K + K * V)
@@ -532,7 +534,26 @@ def run_ours(args, wl):
         seg_calls = [lambda: gdr.gdr_scan_transfer(sp, k, w, u, g_cum, S, M, Z),
                      lambda: gdr.gdr_scan_combine(sp, S, M, Z, h0, starts, hf)]
         del Hk
-    if fused:
+    if fused and wl.per_k_gate:
+        # the per-key-dim gate on the tcgen05 path: the prepare, the gated operands P, qg, kg, then the scan
+        # and output on them
+        g_cum = torch.empty_like(g)
+        w = torch.empty_like(k)
+        u = torch.empty_like(v)
+        P = torch.empty(B, -(-T // C), H, C, C, device=dev, dtype=q.dtype)
+        qg = torch.empty(B, T, H, K, device=dev, dtype=q.dtype)
+        kg = torch.empty(B, T, H, K, device=dev, dtype=q.dtype)
+        sp = gdr.problem_for(q, v, g, C, None, "fused_tc", 1)   # the stage call takes the gated operands there
+        if vp is not None:
+            vp.variant = gdr.VARIANTS["fused_tc"]
+        kernels = ["prepare", "gated_operands"] + seg_names + ["scan_output"]
+
+        def launches():
+            scan = (lambda: gdr.gdr_scan_output(vp, qg, kg, w, u, g_cum, P, starts, o, None)) if vp is not None else \
+                (lambda: gdr.gdr_scan_output(sp, qg, kg, w, u, g_cum, P, h0, o, hf))
+            return [lambda: gdr.gdr_prepare_wy(sp, k, v, g, beta, w, u, g_cum),
+                    lambda: gdr.gdr_gated_operands(sp, q, k, g_cum, P, kg, qg)] + seg_calls + [scan]
+    elif fused:
         # the two kernels gdr_forward runs on this path, called one by one so each can be timed
         g_cum = torch.empty_like(g)
         w = torch.empty_like(k)
@@ -639,7 +660,8 @@ def run_ours(args, wl):
     achieved = floor_bytes / (avg_ms[dom] / 1e3) / 1e9
     kname = {"prepare": "prepare_mma_kernel", "scan": "scan_mma_kernel", "output": "tc_output_kernel",
              "scan_output": "tc_scan_output_kernel" if variant == "fused_tc" else "fused_scan_output_kernel",
-             "transfer": "scan_mma_kernel<transfer>", "combine": "segment_combine_kernel"}[dom_name]
+             "transfer": "scan_mma_kernel<transfer>", "combine": "segment_combine_kernel",
+             "gated_operands": "tc_output_kernel<gated operands>"}[dom_name]
     if stage_variant[dom] == "simt":
         kname = f"simt_{dom_name}_kernel"
     traffic = traffic_for(kname, wl.name)

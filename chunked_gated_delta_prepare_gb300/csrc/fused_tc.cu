@@ -110,7 +110,10 @@ __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.
 // reads q and k of head h / G).  The partial chunk runs as zero tokens past T: the TMA boxes read zeros
 // there, the gate repeats its last value (so those tokens neither decay nor move the state) and no o row
 // past T is stored.  Whole chunks of ungrouped heads take the variant without those guards.
-template <bool GENERAL>
+// GATED (a per-key-dim gate): q and k are the gated operands qg = q exp(G) and kg = k exp(G_last - G)
+// (per element, one per value head; see tc_gated_operands), so dh^T = v'^T kg, o = scale (O1^T + O2^T)
+// with O2 accumulated onto O1, and the decay exp(G_last) is a vector over the keys.
+template <bool GENERAL, bool GATED>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap mq,
                       const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mu,
@@ -124,7 +127,7 @@ tc_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_const
     __shared__ uint32_t tslot;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int bh = blockIdx.x, b = bh / H, h = bh % H;
-    const int hk = GENERAL ? h / G : h;                   // q/k head of value head h
+    const int hk = GENERAL && !GATED ? h / G : h;         // q/k head of value head h (gated: per value head)
 
     if (tid == 0) {
         for (int s = 0; s < kNS; ++s) {
@@ -157,10 +160,22 @@ tc_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_const
         // launched as the programmatic dependent of the prepare, the only warp that reads what it wrote
         // waits here for it to complete (a no-op after an ordinary launch)
         asm volatile("griddepcontrol.wait;" ::: "memory");
-        const float* gr = g_cum + (int64_t)b * T * H + h;
-        auto gat = [&](int t) { return gr[(int64_t)(GENERAL ? min(t, T - 1) : t) * H]; };   // past T: its last value
-        float g0 = 0.f, g1 = 0.f, gl = 0.f;
-        if (NT > 0) { g0 = gat(lane); g1 = gat(lane + 32); gl = gat(kC - 1); }
+        constexpr int GW = GATED ? kK : 1;
+        const float* gr = g_cum + ((int64_t)b * T * H + h) * GW;
+        // G at token t (key d); past T: its last value
+        auto gat = [&](int t, int d) { return gr[(int64_t)(GENERAL ? min(t, T - 1) : t) * H * GW + d]; };
+        float g0 = 0.f, g1 = 0.f, gl = 0.f, gk[4] = {0.f, 0.f, 0.f, 0.f};
+        auto read_gate = [&](int t0) {
+            if constexpr (GATED) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) gk[i] = gat(t0 + kC - 1, lane + 32 * i);
+            } else {
+                g0 = gat(t0 + lane, 0);
+                g1 = gat(t0 + lane + 32, 0);
+                gl = gat(t0 + kC - 1, 0);
+            }
+        };
+        if (NT > 0) read_gate(0);
         int issued = 0;
         for (int c = 0; c < NT; ++c) {
             const int s = c % kNS;
@@ -179,15 +194,21 @@ tc_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_const
                 bw::tma_load_4d(st + L::P, &mp, &full[s], 0, 0, h, b * NT + c);
             }
             issued = c + 1;
-            // gamma_t = exp(G_last - G_t), exp(G_t), exp(G_last) of the chunk; then the next chunk's gate
+            // gamma_t = exp(G_last - G_t), exp(G_t), exp(G_last) of the chunk (GATED: exp(G_last) per key);
+            // then the next chunk's gate
             float* F = reinterpret_cast<float*>(sm + L::F + s * L::kF);
-            F[lane] = __expf(gl - g0);
-            F[lane + 32] = __expf(gl - g1);
-            F[kC + lane] = __expf(g0);
-            F[kC + lane + 32] = __expf(g1);
-            if (lane == 0) F[2 * kC] = __expf(gl);
+            if constexpr (GATED) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) F[lane + 32 * i] = __expf(gk[i]);
+            } else {
+                F[lane] = __expf(gl - g0);
+                F[lane + 32] = __expf(gl - g1);
+                F[kC + lane] = __expf(g0);
+                F[kC + lane + 32] = __expf(g1);
+                if (lane == 0) F[2 * kC] = __expf(gl);
+            }
             bw::mbar_arrive(&full[s]);
-            if (c + 1 < NT) { g0 = gat(t0 + kC + lane); g1 = gat(t0 + kC + lane + 32); gl = gat(t0 + 2 * kC - 1); }
+            if (c + 1 < NT) read_gate(t0 + kC);
         }
         // no load of this CTA may still be landing when it exits
         for (int c = max(issued - kNS, 0); c < issued; ++c)
@@ -210,7 +231,8 @@ tc_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_const
             const uint64_t so = (uint64_t)((cc % kNS) * L::kStage) >> 4;
             const uint32_t vp = cVP + 32 * (cc & 1);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) mma_ta(tmem + cO2, tmem + vp + 8 * kk, pd[kk] + so, idT, kk > 0);
+            for (int kk = 0; kk < 4; ++kk)
+                mma_ta(tmem + (GATED ? cO1 : cO2), tmem + vp + 8 * kk, pd[kk] + so, idT, GATED ? 1u : (uint32_t)(kk > 0));
             bw::mma_commit_warp(&barO);
             bw::mma_commit_warp(&empty[cc % kNS]);
         };
@@ -229,8 +251,9 @@ tc_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_const
             if (c >= 1) issue_o2(c - 1);
             if (!bw::mbar_wait(&vpReady, c & 1, err, kDeviceErrTimeout)) { ok = false; break; }
             bw::tc_fence_after();
+            const uint32_t va = GATED ? cVP + 32 * (c & 1) : cVG;    // v' (against kg) or (v' diag gamma)
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) mma_ta(tmem + cD, tmem + cVG + 8 * kk, kd[kk] + so, idK, kk > 0);
+            for (int kk = 0; kk < 4; ++kk) mma_ta(tmem + cD, tmem + va + 8 * kk, kd[kk] + so, idK, kk > 0);
             bw::mma_commit_warp(&barE);
             // O1 runs while the CUDA cores update h; the previous chunk's output must have been read
             if (c >= 1 && !bw::mbar_wait(&oFree, (c - 1) & 1, err, kDeviceErrTimeout)) { ok = false; break; }
@@ -268,7 +291,7 @@ tc_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_const
             bw::tc_fence_after();
             float a[16], e[16];
             bw::tmem_ld16(lb + cO1 + tok0, a);
-            bw::tmem_ld16(lb + cO2 + tok0, e);
+            if constexpr (!GATED) bw::tmem_ld16(lb + cO2 + tok0, e);
             bw::tmem_ld_wait();
             bw::tc_fence_before();
             __syncwarp();
@@ -277,8 +300,16 @@ tc_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_const
             const int tt = cc * kC + tok0;
             const float4* e4 = reinterpret_cast<const float4*>(F + kC + tok0);
             float r[16];
+            if constexpr (GATED) {   // o = scale (O1^T + O2^T), one accumulator
 #pragma unroll
-            for (int j4 = 0; j4 < 4; ++j4) {
+                for (int j = 0; j < 8; ++j) {
+                    const float2 x = __fmul2_rn(make_float2(scale, scale), make_float2(a[2 * j], a[2 * j + 1]));
+                    r[2 * j] = x.x;
+                    r[2 * j + 1] = x.y;
+                }
+            }
+#pragma unroll
+            for (int j4 = 0; j4 < (GATED ? 0 : 4); ++j4) {
                 const float4 eg = e4[j4];
                 const float2 r0 = __fmul2_rn(make_float2(scale, scale),
                                              __ffma2_rn(make_float2(eg.x, eg.y), make_float2(a[4 * j4], a[4 * j4 + 1]),
@@ -326,20 +357,22 @@ tc_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_const
                 const float4* g4 = reinterpret_cast<const float4*>(F + tok0);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const float4 gm = g4[j];
                     const float2 x0 = __ffma2_rn(make_float2(d[4 * j], d[4 * j + 1]), make_float2(-1.f, -1.f),
                                                  make_float2(uu[4 * j], uu[4 * j + 1]));
                     const float2 x1 = __ffma2_rn(make_float2(d[4 * j + 2], d[4 * j + 3]), make_float2(-1.f, -1.f),
                                                  make_float2(uu[4 * j + 2], uu[4 * j + 3]));
                     pv[2 * j] = bw::pack_bf16(x0.x, x0.y);
                     pv[2 * j + 1] = bw::pack_bf16(x1.x, x1.y);
-                    const float2 y0 = __fmul2_rn(x0, make_float2(gm.x, gm.y));
-                    const float2 y1 = __fmul2_rn(x1, make_float2(gm.z, gm.w));
-                    pg[2 * j] = bw::pack_bf16(y0.x, y0.y);
-                    pg[2 * j + 1] = bw::pack_bf16(y1.x, y1.y);
+                    if constexpr (!GATED) {
+                        const float4 gm = g4[j];
+                        const float2 y0 = __fmul2_rn(x0, make_float2(gm.x, gm.y));
+                        const float2 y1 = __fmul2_rn(x1, make_float2(gm.z, gm.w));
+                        pg[2 * j] = bw::pack_bf16(y0.x, y0.y);
+                        pg[2 * j + 1] = bw::pack_bf16(y1.x, y1.y);
+                    }
                 }
                 tmem_st8(lb + cVP + 32 * (c & 1) + tok0 / 2, pv);
-                tmem_st8(lb + cVG + tok0 / 2, pg);
+                if constexpr (!GATED) tmem_st8(lb + cVG + tok0 / 2, pg);
                 tmem_st_wait();
             }
             bw::tc_fence_before();
@@ -354,13 +387,24 @@ tc_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_const
                 float d[32];
                 bw::tmem_ld32(lb + cD + key0, d);
                 bw::tmem_ld_wait();
-                const float dec = F[2 * kC];
+                if constexpr (GATED) {   // exp(G_last) per key
+                    const float2* dk = reinterpret_cast<const float2*>(F + key0);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const float2 r = __ffma2_rn(make_float2(dec, dec), make_float2(hs[2 * j], hs[2 * j + 1]),
-                                                make_float2(d[2 * j], d[2 * j + 1]));
-                    hs[2 * j] = r.x;
-                    hs[2 * j + 1] = r.y;
+                    for (int j = 0; j < 16; ++j) {
+                        const float2 r = __ffma2_rn(dk[j], make_float2(hs[2 * j], hs[2 * j + 1]),
+                                                    make_float2(d[2 * j], d[2 * j + 1]));
+                        hs[2 * j] = r.x;
+                        hs[2 * j + 1] = r.y;
+                    }
+                } else {
+                    const float dec = F[2 * kC];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float2 r = __ffma2_rn(make_float2(dec, dec), make_float2(hs[2 * j], hs[2 * j + 1]),
+                                                    make_float2(d[2 * j], d[2 * j + 1]));
+                        hs[2 * j] = r.x;
+                        hs[2 * j + 1] = r.y;
+                    }
                 }
             }
             store_h((c + 1) & 1);
@@ -379,16 +423,18 @@ tc_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_const
 }  // namespace
 
 bool tc_scan_output_supported(const Dims& d) {
-    return d.bf16 && !d.per_k && d.K == kK && d.V == kV && d.C == kC && (int64_t)d.B * d.H <= 0x7fffffff;
+    return d.bf16 && d.K == kK && d.V == kV && d.C == kC && (int64_t)d.B * d.H <= 0x7fffffff;
 }
 
 cudaError_t tc_scan_output(const Dims& d, const void* q, const void* k, const void* w, const void* u,
                            const float* g_cum, const void* P, const float* h0, void* o, float* h_final,
                            cudaStream_t s, unsigned int* err, bool pdl) {
     if (!tc_scan_output_supported(d) || !P) return cudaErrorInvalidValue;
+    // a per-key-dim gate takes the gated operands qg, kg in place of q, k: one per value head
+    const int hq = d.per_k ? d.H : d.Hk;
     CUtensorMap mw, mq, mk, mu, mp;
-    if (!make_tmap_tokens(&mw, w, d.B, d.T, d.H, kK, kC) || !make_tmap_tokens(&mq, q, d.B, d.T, d.Hk, kK, kC) ||
-        !make_tmap_tokens(&mk, k, d.B, d.T, d.Hk, kK, kC) || !make_tmap_tokens_plain(&mu, u, d.B, d.T, d.H, kV, kV, kC))
+    if (!make_tmap_tokens(&mw, w, d.B, d.T, d.H, kK, kC) || !make_tmap_tokens(&mq, q, d.B, d.T, hq, kK, kC) ||
+        !make_tmap_tokens(&mk, k, d.B, d.T, hq, kK, kC) || !make_tmap_tokens_plain(&mu, u, d.B, d.T, d.H, kV, kV, kC))
         return cudaErrorInvalidValue;
     // P [B, NT, H, C, C] seen as (C, C, H, B*NT); one 64 x 64 box per chunk
     const uint64_t dims[4] = {(uint64_t)kC, (uint64_t)kC, (uint64_t)d.H, (uint64_t)d.B * d.NT};
@@ -396,7 +442,9 @@ cudaError_t tc_scan_output(const Dims& d, const void* q, const void* k, const vo
     const uint32_t box[4] = {64, 64, 1, 1};
     if (!make_tmap_bf16_4d(&mp, P, dims, st, box)) return cudaErrorInvalidValue;
     const size_t smem = TcLayout::bytes + 1024;
-    auto kern = (d.T % kC != 0 || d.G != 1) ? tc_scan_output_kernel<true> : tc_scan_output_kernel<false>;
+    const bool general = d.T % kC != 0 || (!d.per_k && d.G != 1);
+    auto kern = d.per_k ? (general ? tc_scan_output_kernel<true, true> : tc_scan_output_kernel<false, true>)
+                        : (general ? tc_scan_output_kernel<true, false> : tc_scan_output_kernel<false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if (pdl) {

@@ -111,6 +111,8 @@ gdr_status pick_forward(const gdr_problem* p, const gdr::Dims& d, Path* path) {
             // The tcgen05 form of the fused kernel (see fused_tc.cu) when the warp-level one would need
             // more than one wave of the GPU, or for one long sequence scanned whole, which it runs in
             // pieces overlapped with the prepare (see forward_tc_overlapped).
+            // A per-key-dim gate at K = V = 128, C = 64 takes the tcgen05 form too (its gated operands from
+            // their own kernel) unless the segment-parallel scan applies.
             if (!d.bf16) *path = Path::Simt;
             else if (!d.per_k && d.C == 64)
                 *path = gdr::tc_scan_output_supported(d) &&
@@ -118,6 +120,7 @@ gdr_status pick_forward(const gdr_problem* p, const gdr::Dims& d, Path* path) {
                                                                                  !segments_apply(p, d)))
                             ? Path::FusedTc
                             : Path::Fused;
+            else if (d.per_k && gdr::tc_scan_output_supported(d) && !segments_apply(p, d)) *path = Path::FusedTc;
             else *path = Path::Tensor;
             return GDR_OK;
         default: return GDR_ERR_UNSUPPORTED;
@@ -185,10 +188,11 @@ bool segments_apply(const gdr_problem* p, const gdr::Dims& d) {
 // gdr_forward scratch: g_cum, w, u and (staged paths) v_new, h_ckpt, (S > 1) the segment maps and
 // starts, each 256-byte aligned.
 struct StagedWorkspace {
-    size_t g_cum, w, u, v_new, h_ckpt, P, seg_m, seg_z, seg_h, carry, total;
+    size_t g_cum, w, u, v_new, h_ckpt, P, kg, qg, seg_m, seg_z, seg_h, carry, total;
 };
 
-StagedWorkspace plan_staged(const gdr::Dims& d, bool fused, int S, int pieces = 1) {
+// gated: the tcgen05 path with a per-key-dim gate, which also keeps kg and qg [B, T, H, K] (io dtype)
+StagedWorkspace plan_staged(const gdr::Dims& d, bool fused, int S, int pieces = 1, bool gated = false) {
     const size_t e = (d.bf16 || d.f16) ? 2 : 4;
     const size_t rows = (size_t)d.B * d.T * d.H;
     StagedWorkspace ws;
@@ -205,6 +209,11 @@ StagedWorkspace plan_staged(const gdr::Dims& d, bool fused, int S, int pieces = 
         off = round_up(off + (size_t)d.B * d.NT * d.H * d.K * d.V * e, 256);
     } else if (d.C == 64) {   // ... and reads the prepare's gated causal scores [B, NT, H, C, C]
         off = round_up(off + (size_t)d.B * d.NT * d.H * d.C * d.C * e, 256);
+    }
+    ws.kg = ws.qg = off;
+    if (gated) {
+        ws.qg = round_up(off + rows * d.K * e, 256);
+        off = round_up(ws.qg + rows * d.K * e, 256);
     }
     ws.seg_m = ws.seg_z = ws.seg_h = off;
     if (S > 1) {   // M [B S, H, K, K], Z and the segment starts [B S, H, K, V], fp32
@@ -239,7 +248,7 @@ constexpr int kMaxPieces = 32;
 // Chunk offsets of the pieces: bounds[0] = 0 < bounds[1] < ... < bounds[n] = NT; returns n (1: no pieces).
 int overlap_bounds(const gdr::Dims& d, Path path, int S, int* bounds) {
     bounds[0] = 0;
-    if (path != Path::FusedTc || S != 1 || d.B != 1 || d.NT < 2 * kPieceChunks) {
+    if (path != Path::FusedTc || d.per_k || S != 1 || d.B != 1 || d.NT < 2 * kPieceChunks) {
         bounds[1] = d.NT;
         return 1;
     }
@@ -602,7 +611,9 @@ size_t gdr_forward_workspace_bytes(const gdr_problem* p) {
     Path path;
     int S = 1;
     if (pick_forward(p, d, &path) != GDR_OK || resolve_segments(p, d, path != Path::Simt, &S) != GDR_OK) return 0;
-    return plan_staged(d, path == Path::Fused || path == Path::FusedTc, S, overlap_pieces(d, path, S)).total;
+    return plan_staged(d, path == Path::Fused || path == Path::FusedTc, S, overlap_pieces(d, path, S),
+                       path == Path::FusedTc && d.per_k)
+        .total;
 }
 
 int gdr_forward_segments(const gdr_problem* p) {
@@ -627,7 +638,8 @@ gdr_status gdr_forward(const gdr_problem* p, const void* q, const void* k, const
     if ((st = resolve_segments(p, d, path != Path::Simt, &S)) != GDR_OK) return st;
     int bounds[kMaxPieces + 1];
     const int pieces = overlap_bounds(d, path, S, bounds);
-    const StagedWorkspace ws = plan_staged(d, path == Path::Fused || path == Path::FusedTc, S, pieces);
+    const bool gated = path == Path::FusedTc && d.per_k;
+    const StagedWorkspace ws = plan_staged(d, path == Path::Fused || path == Path::FusedTc, S, pieces, gated);
     if (!workspace || workspace_bytes < ws.total) return GDR_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GDR_ERR_ALIGN;
     char* base = static_cast<char*>(workspace);
@@ -649,7 +661,14 @@ gdr_status gdr_forward(const gdr_problem* p, const void* q, const void* k, const
     } else {
         const bool fused = path == Path::Fused || path == Path::FusedTc;
         void* P = (fused && d.C == 64) ? base + ws.P : nullptr;
-        if ((st = from_cuda(gdr::mma_prepare(d, k, v, g, beta, w, u, g_cum, s, err, q, P))) != GDR_OK) return st;
+        void* kg = base + ws.kg;
+        void* qg = base + ws.qg;
+        if (gated) {   // per-key-dim gate: the prepare, then P, kg and qg from q, k and G
+            if ((st = from_cuda(gdr::mma_prepare(d, k, v, g, beta, w, u, g_cum, s, err))) != GDR_OK) return st;
+            if ((st = from_cuda(gdr::tc_gated_operands(d, q, k, g_cum, P, kg, qg, s, err))) != GDR_OK) return st;
+        } else if ((st = from_cuda(gdr::mma_prepare(d, k, v, g, beta, w, u, g_cum, s, err, q, P))) != GDR_OK) {
+            return st;
+        }
         // segments: every segment's map from a zero state, the starts stitched serially, then the
         // scan (and output) of all segments at once from their starts
         gdr::Dims ds = d;
@@ -666,9 +685,10 @@ gdr_status gdr_forward(const gdr_problem* p, const void* q, const void* k, const
             hf = nullptr;
         }
         if (fused) {
-            const cudaError_t e = path == Path::FusedTc
-                                      ? gdr::tc_scan_output(ds, q, k, w, u, g_cum, P, hs, o, hf, s, err, S == 1)
-                                      : gdr::mma_scan_output(ds, q, k, w, u, g_cum, P, hs, o, hf, s, err);
+            const cudaError_t e =
+                path != Path::FusedTc ? gdr::mma_scan_output(ds, q, k, w, u, g_cum, P, hs, o, hf, s, err)
+                : gated               ? gdr::tc_scan_output(ds, qg, kg, w, u, g_cum, P, hs, o, hf, s, err)
+                                      : gdr::tc_scan_output(ds, q, k, w, u, g_cum, P, hs, o, hf, s, err, S == 1);
             if ((st = from_cuda(e)) != GDR_OK) return st;
         } else {
             if ((st = from_cuda(gdr::mma_scan(ds, k, w, u, g_cum, hs, h_ckpt, v_new, hf, s, err))) != GDR_OK)
@@ -848,7 +868,9 @@ gdr_status gdr_scan_output(const gdr_problem* p, const void* q, const void* k, c
     gdr_status st = check_problem(p, &d);
     if (st != GDR_OK) return st;
     if ((st = check_ptrs({q, k, w, u, g_cum, o}, {P, h0, h_final})) != GDR_OK) return st;
-    if (p->variant == GDR_VARIANT_SIMT || !d.bf16 || d.per_k || (P && d.C != 64)) return GDR_ERR_UNSUPPORTED;
+    if (p->variant == GDR_VARIANT_SIMT || !d.bf16 || (P && d.C != 64)) return GDR_ERR_UNSUPPORTED;
+    // a per-key-dim gate: the tcgen05 kernel only, on gdr_gated_operands' P, qg and kg
+    if (d.per_k && (p->variant != GDR_VARIANT_FUSED_TC || !P)) return GDR_ERR_UNSUPPORTED;
     // the tcgen05 kernel for variant FUSED_TC, and for AUTO where gdr_forward would take it
     Path path;
     if ((st = pick_forward(p, d, &path)) != GDR_OK) return st;
@@ -862,6 +884,19 @@ gdr_status gdr_scan_output(const gdr_problem* p, const void* q, const void* k, c
                       : gdr::mma_scan_output(d, q, k, w, u, g_cum, P, h0, o, h_final, (cudaStream_t)stream,
                                              device_error_word()));
     if (st == GDR_OK) t_last_variant = tc ? "fused_tc" : "fused";
+    return st;
+}
+
+gdr_status gdr_gated_operands(const gdr_problem* p, const void* q, const void* k, const float* g_cum, void* P, void* kg,
+                              void* qg, void* stream) {
+    gdr::Dims d;
+    gdr_status st = check_problem(p, &d);
+    if (st != GDR_OK) return st;
+    if ((st = check_ptrs({q, k, g_cum, P, kg, qg}, {})) != GDR_OK) return st;
+    if (p->variant == GDR_VARIANT_SIMT || !d.bf16 || !d.per_k || d.K != 128 || d.V != 128 || d.C != 64)
+        return GDR_ERR_UNSUPPORTED;
+    st = from_cuda(gdr::tc_gated_operands(d, q, k, g_cum, P, kg, qg, (cudaStream_t)stream, device_error_word()));
+    if (st == GDR_OK) t_last_variant = "fused_tc";
     return st;
 }
 
@@ -1148,7 +1183,8 @@ gdr_status varlen_inner_bytes(const gdr_problem* p, const gdr::Dims& d, bool bac
     } else {
         Path path;
         if ((st = pick_forward(p, d, &path)) != GDR_OK) return st;
-        if (path == Path::FusedTc) path = Path::Fused;   // packed sequences: the warp-level fused kernel
+        if (path == Path::FusedTc)   // packed sequences: the warp-level fused kernel, or the staged one (KDA)
+            path = d.per_k ? Path::Tensor : Path::Fused;
         if ((st = resolve_segments(p, d, path != Path::Simt, &S)) != GDR_OK) return st;
         *bytes = plan_staged(d, path == Path::Fused, S).total;
         if (path != Path::Simt && chunk_packed_fits(d)) {
@@ -1235,7 +1271,8 @@ gdr_status gdr_varlen_forward(const gdr_problem* p_in, const int32_t* cu_seqlens
         return st;
     Path path;
     if ((st = pick_forward(p, d, &path)) != GDR_OK) return st;
-    if (path == Path::FusedTc) path = Path::Fused;   // packed sequences: the warp-level fused kernel
+    if (path == Path::FusedTc)   // packed sequences: the warp-level fused kernel, or the staged one (KDA)
+        path = d.per_k ? Path::Tensor : Path::Fused;
     char* base = static_cast<char*>(workspace);
     int64_t rb[11];
     varlen_rows(d, false, rb);

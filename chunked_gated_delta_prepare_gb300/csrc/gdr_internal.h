@@ -70,8 +70,14 @@ cudaError_t mma_scan_output(const Dims& d, const void* q, const void* k, const v
 // packed row pcu[z]; w, u, g_cum and P are the chunk-packed row's (see fused_mma.cu)
 
 // The same scan and output on the tcgen05 tensor cores, one CTA per (batch, head) (fused_tc.cu): bf16 io,
-// scalar gate, K = V = 128, C = 64 (any T, grouped value heads), and P from the prepare.
+// K = V = 128, C = 64 (any T, grouped value heads), and P from the prepare.  With a per-key-dim gate q and k
+// are the gated operands qg and kg and P comes from tc_gated_operands.
 bool tc_scan_output_supported(const Dims& d);
+// Per (batch, value head, chunk) with a per-key-dim gate (bf16, K = V = 128, C = 64): P = tril_0(Q~) as the
+// prepare with P writes it for a scalar gate, qg = q exp(G) and kg = k exp(G_last - G) [B, T, H, K] bf16
+// (tc_output.cu, the output kernel's first half).
+cudaError_t tc_gated_operands(const Dims& d, const void* q, const void* k, const float* g_cum, void* P, void* kg,
+                              void* qg, cudaStream_t s, unsigned int* err);
 // pdl: launch as the programmatic dependent of the stream's previous kernel (the prepare), which must
 // trigger early (griddepcontrol.launch_dependents); the scan's setup then runs under its tail.
 cudaError_t tc_scan_output(const Dims& d, const void* q, const void* k, const void* w, const void* u,

@@ -11,6 +11,10 @@
 //                                            tile holds two chunks, each with its own h_c)
 //   MMA 3    D += P v'                      (B = v', MN-major)
 //   SIMT     o = scale * D -> bf16 -> global
+//
+// OPS (per-key-dim gate, K = V = 128, C = 64): the gated operands of the tcgen05 scan and output kernel
+// instead of o.  The CTA forms P and q exp(G) as above, and kg = k exp(G_last - G) beside the gated copy of
+// k (G_last the chunk's last row), and stores the three by TMA: no v', no checkpoints, no MMA 2 or 3.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -29,33 +33,36 @@ using namespace tc;
 constexpr float kExpClamp = 60.f;
 constexpr float kExpSafe = 40.f;
 
-template <int K, int V, int C, bool PER_K>
+template <int K, int V, int C, bool PER_K, bool OPS = false>
 struct OutLayout {
     static constexpr int NCH = kTile / C;                          // chunks per tile
     static constexpr int GW = PER_K ? K : 1;
     // With a per-key-dim gate the gate is read from global memory (L2) where needed instead of
     // being staged (32 KB), k's gated copy is written over k, and P over that once S is formed:
-    // two CTAs per SM.
+    // two CTAs per SM.  OPS keeps no checkpoints (qg goes over q, kg into the v' region): three per SM.
     static constexpr uint32_t Q = 0;                               // q, then q exp(G) for chunk 0
     static constexpr uint32_t Kt = Q + K * 128;                    // k (per-key-dim gate: then k exp(Gref - G))
     static constexpr uint32_t VP = Kt + K * 128;                   // v' [64][V]
-    static constexpr uint32_t Hc = VP + V * 128;                   // checkpoints [NCH][K][V]
+    static constexpr uint32_t Hc = VP + V * 128;                   // checkpoints [NCH][K][V] (none with OPS)
     static constexpr uint32_t P = PER_K ? Kt : Hc + NCH * K * V * 2;   // P [64][64]
-    static constexpr uint32_t Q1 = PER_K ? Hc + NCH * K * V * 2 : P + 8192;   // C = 32: q exp(G) for chunk 1
+    static constexpr uint32_t Q1 = PER_K ? Hc + (OPS ? 0 : NCH * K * V * 2) : P + 8192;   // C = 32: q exp(G), chunk 1
     static constexpr uint32_t Qa = Q1 + (NCH > 1 ? K * 128 : 0);   // per-key-dim gate: q exp(G - Gref)
     static constexpr uint32_t F = Qa + (PER_K ? K * 128 : 0);      // fp32: G [64] (scalar gate), flag
     static constexpr uint32_t bytes = F + 4 * ((PER_K ? 0 : kTile) + 4);
     static constexpr uint32_t tx = 2 * K * 128 + V * 128 + NCH * K * V * 2;
-    static constexpr uint32_t tmem_cols = 256;                     // S at 0 (64 cols), D at 64 (V cols)
+    static constexpr uint32_t tmem_cols = OPS ? 64 : 256;          // S at 0 (64 cols), D at 64 (V cols)
 };
 
-template <int K, int V, int C, bool PER_K>
+// OPS: mvp and mh are the kg and qg store maps and mp the P store map (otherwise mp is unused).
+template <int K, int V, int C, bool PER_K, bool OPS = false>
 __global__ void __launch_bounds__(128, 1)
 tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                  const __grid_constant__ CUtensorMap mvp, const __grid_constant__ CUtensorMap mh,
-                 const float* __restrict__ g_cum, const bf16* __restrict__ k_raw, bf16* __restrict__ o, int T,
-                 int H, int NT, int G, float scale, unsigned int* err) {
-    using L = OutLayout<K, V, C, PER_K>;
+                 const __grid_constant__ CUtensorMap mp, const float* __restrict__ g_cum,
+                 const bf16* __restrict__ q_raw, const bf16* __restrict__ k_raw, bf16* __restrict__ o, int T, int H,
+                 int NT, int G, float scale, unsigned int* err) {
+    static_assert(!OPS || (PER_K && C == 64 && K == V), "gated operands: per-key-dim gate, one chunk per tile");
+    using L = OutLayout<K, V, C, PER_K, OPS>;
     constexpr int GW = L::GW;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -105,15 +112,17 @@ tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
     const uint32_t tmem = tslot;
 
     if (tid == 0) {
-        const int nch = (nvalid + C - 1) / C;   // checkpoints that exist for this tile
-        bw::mbar_arrive_expect_tx(&bar_tma, 2 * K * 128 + V * 128 + nch * K * V * 2);
+        const int nch = OPS ? 0 : (nvalid + C - 1) / C;   // checkpoints that exist for this tile
+        bw::mbar_arrive_expect_tx(&bar_tma, 2 * K * 128 + (OPS ? 0 : V * 128) + nch * K * V * 2);
 #pragma unroll
         for (int a = 0; a < K / 64; ++a) {
             bw::tma_load_4d(sm + L::Q + a * 8192, &mq, &bar_tma, a * 64, h / G, t0, b);
             bw::tma_load_4d(sm + L::Kt + a * 8192, &mk, &bar_tma, a * 64, h / G, t0, b);
         }
+        if constexpr (!OPS) {
 #pragma unroll
-        for (int a = 0; a < V / 64; ++a) bw::tma_load_4d(sm + L::VP + a * 8192, &mvp, &bar_tma, a * 64, h, t0, b);
+            for (int a = 0; a < V / 64; ++a) bw::tma_load_4d(sm + L::VP + a * 8192, &mvp, &bar_tma, a * 64, h, t0, b);
+        }
         for (int ch = 0; ch < nch; ++ch) {
             const int c = t0 / C + ch;
 #pragma unroll
@@ -133,13 +142,33 @@ tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
 
     if constexpr (PER_K) {
         float4 ga[NIT][2], gref[L::NCH][2];   // this thread's rows of G; the middle row of each chunk
+        float4 glast[2];                      // OPS: the chunk's last row of G
         load_g_rows(ga);
+        if constexpr (OPS) {
+            const float4* src = reinterpret_cast<const float4*>(g_cum + row(nvalid - 1) * K + (tid % (K / 8)) * 8);
+            glast[0] = src[0];
+            glast[1] = src[1];
+        }
 #pragma unroll
         for (int ch = 0; ch < L::NCH; ++ch) {
             const float4* src = reinterpret_cast<const float4*>(
                 g_cum + row(min(ch * C + C / 2, nvalid - 1)) * K + (tid % (K / 8)) * 8);
             gref[ch][0] = src[0];
             gref[ch][1] = src[1];
+        }
+        // OPS: exp(G_ref) and exp(G_last - G_ref) of this thread's eight key columns (the same at every step),
+        // so that qg = (q exp(G - G_ref)) exp(G_ref) and kg = (k exp(G_ref - G)) exp(G_last - G_ref) reuse the
+        // gated copies' exponentials where |G - G_ref| <= kExpSafe
+        float eref[8], elref[8];
+        if constexpr (OPS) {
+            float gf0[8], gl0[8];
+            unpack8(gref[0], gf0);
+            unpack8(glast, gl0);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                eref[e] = __expf(gf0[e]);
+                elref[e] = __expf(gl0[e] - gf0[e]);
+            }
         }
 #pragma unroll
         for (int j = 0; j < NIT; ++j) {
@@ -153,14 +182,37 @@ tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
             unpack8(ga[j], gr);
             unpack8(L::NCH > 1 && r >= C ? gref[L::NCH - 1] : gref[0], gf);
             bool big = false;
+            float fq[8], fk[8];   // OPS: qg and kg
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const float dg = gr[e] - gf[e];
-                big |= fabsf(dg) > kExpSafe;
-                fa[e] = __bfloat162float(qv[e]) * __expf(fminf(fmaxf(dg, -kExpClamp), kExpClamp));
-                fb[e] = __bfloat162float(kv[e]) * __expf(fminf(fmaxf(-dg, -kExpClamp), kExpClamp));
+                const bool far = fabsf(dg) > kExpSafe;
+                big |= far;
+                const float xq = __bfloat162float(qv[e]), xk = __bfloat162float(kv[e]);
+                fa[e] = xq * __expf(fminf(fmaxf(dg, -kExpClamp), kExpClamp));
+                fb[e] = xk * __expf(fminf(fmaxf(-dg, -kExpClamp), kExpClamp));
+                if constexpr (OPS) {
+                    if (!far) {
+                        fq[e] = fa[e] * eref[e];
+                        fk[e] = fb[e] * elref[e];
+                    } else {
+                        float gl[8];
+                        unpack8(glast, gl);
+                        fq[e] = xq * __expf(gr[e]);
+                        fk[e] = xk * __expf(gl[e] - gr[e]);
+                    }
+                }
             }
             if (big) *sFlag = 1;
+            if constexpr (OPS) {   // qg into the unused checkpoint region, kg into the unused v' region
+                uint4 pq, pk;
+                pq.x = bw::pack_bf16(fq[0], fq[1]); pq.y = bw::pack_bf16(fq[2], fq[3]);
+                pq.z = bw::pack_bf16(fq[4], fq[5]); pq.w = bw::pack_bf16(fq[6], fq[7]);
+                pk.x = bw::pack_bf16(fk[0], fk[1]); pk.y = bw::pack_bf16(fk[2], fk[3]);
+                pk.z = bw::pack_bf16(fk[4], fk[5]); pk.w = bw::pack_bf16(fk[6], fk[7]);
+                *reinterpret_cast<uint4*>(sm + L::Q + off) = pq;   // over q: each thread rewrites what it read
+                *reinterpret_cast<uint4*>(sm + L::VP + off) = pk;
+            }
             uint4 pa, pb;
             pa.x = bw::pack_bf16(fa[0], fa[1]); pa.y = bw::pack_bf16(fa[2], fa[3]);
             pa.z = bw::pack_bf16(fa[4], fa[5]); pa.w = bw::pack_bf16(fa[6], fa[7]);
@@ -224,7 +276,9 @@ tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
             if (j >= (i / C) * C && j <= i) {
                 float acc = 0.f;
                 for (int d = 0; d < K; ++d) {
-                    const float qi = __bfloat162float(*reinterpret_cast<const bf16*>(sm + L::Q + tile_off(i, d)));
+                    // OPS: q's tile now holds qg, so raw q comes from global memory too
+                    const float qi = OPS ? (i < nvalid ? __bfloat162float(q_raw[krow(i) * K + d]) : 0.f)
+                                         : __bfloat162float(*reinterpret_cast<const bf16*>(sm + L::Q + tile_off(i, d)));
                     // k's tile now holds its gated copy: raw k and G come from global memory (rare path)
                     const float kj = j < nvalid ? __bfloat162float(k_raw[krow(j) * K + d]) : 0.f;
                     const float gi = i < nvalid ? g_cum[row(i) * K + d] : 0.f;
@@ -236,6 +290,28 @@ tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         }
         __syncthreads();
     }
+    if constexpr (OPS) {
+        // P, kg and qg leave by TMA (rows past T clipped); nothing of the output's second half runs
+        bw::fence_async_shared();
+        __syncthreads();
+        if (tid == 0) {
+            if (ok) {
+                bw::tma_store_4d(&mp, sm + L::P, 0, 0, h, b * NT + t0 / C);
+#pragma unroll
+                for (int a = 0; a < K / 64; ++a) {
+                    bw::tma_store_4d(&mvp, sm + L::VP + a * 8192, a * 64, h, t0, b);
+                    bw::tma_store_4d(&mh, sm + L::Q + a * 8192, a * 64, h, t0, b);
+                }
+                bw::bulk_commit();
+            }
+            bw::bulk_wait_read<0>();
+        }
+        bw::tc_fence_before();
+        __syncthreads();
+        if (warp == 0) bw::tmem_dealloc(tmem, L::tmem_cols);
+        return;
+    }
+
     // q exp(G) in place (and, for two chunks per tile, split by chunk into Q and Q1)
     float4 gq[PER_K ? NIT : 1][2];
     if constexpr (PER_K) load_g_rows(gq);
@@ -321,8 +397,8 @@ cudaError_t launch_output(const Dims& d, const void* q, const void* k, const voi
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const dim3 grid((d.T + kTile - 1) / kTile, d.H, d.B);
-    kern<<<grid, 128, smem, s>>>(mq, mk, mvp, mh, g_cum, (const bf16*)k, (bf16*)o, d.T, d.H, d.NT, d.G, d.scale,
-                                 err);
+    kern<<<grid, 128, smem, s>>>(mq, mk, mvp, mh, mh, g_cum, (const bf16*)q, (const bf16*)k, (bf16*)o, d.T, d.H, d.NT,
+                                 d.G, d.scale, err);
     return cudaGetLastError();
 }
 
@@ -341,6 +417,29 @@ cudaError_t out_chunk(const Dims& d, const void* q, const void* k, const void* v
 }
 
 }  // namespace
+
+cudaError_t tc_gated_operands(const Dims& d, const void* q, const void* k, const float* g_cum, void* P, void* kg,
+                              void* qg, cudaStream_t s, unsigned int* err) {
+    constexpr int K = 128, V = 128, C = 64;
+    if (!d.bf16 || !d.per_k || d.K != K || d.V != V || d.C != C) return cudaErrorInvalidValue;
+    using L = OutLayout<K, V, C, true, true>;
+    CUtensorMap mq, mk, mkg, mqg, mp;
+    const uint64_t dims[4] = {(uint64_t)C, (uint64_t)C, (uint64_t)d.H, (uint64_t)d.B * d.NT};
+    const uint64_t st[3] = {(uint64_t)C * 2, (uint64_t)C * C * 2, (uint64_t)d.H * C * C * 2};
+    const uint32_t box[4] = {64, 64, 1, 1};
+    if (!make_tmap_tokens(&mq, q, d.B, d.T, d.Hk, K, kTile) || !make_tmap_tokens(&mk, k, d.B, d.T, d.Hk, K, kTile) ||
+        !make_tmap_tokens(&mkg, kg, d.B, d.T, d.H, K, kTile) || !make_tmap_tokens(&mqg, qg, d.B, d.T, d.H, K, kTile) ||
+        !make_tmap_bf16_4d(&mp, P, dims, st, box))
+        return cudaErrorInvalidValue;
+    auto kern = tc_output_kernel<K, V, C, true, true>;
+    const size_t smem = L::bytes + 1024;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const dim3 grid((d.T + kTile - 1) / kTile, d.H, d.B);
+    kern<<<grid, 128, smem, s>>>(mq, mk, mkg, mqg, mp, g_cum, (const bf16*)q, (const bf16*)k, nullptr, d.T, d.H, d.NT,
+                                 d.G, d.scale, err);
+    return cudaGetLastError();
+}
 
 cudaError_t tc_output(const Dims& d, const void* q, const void* k, const void* v_new, const void* h_ckpt,
                       const float* g_cum, void* o, cudaStream_t s, unsigned int* err) {

@@ -37,7 +37,7 @@ DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
 VARIANTS = {"auto": 0, "simt": 1, "tensor": 2, "fused": 3, "fused_tc": 4}
 EXPORTS = ["gdr_prepare_wy", "gdr_scan_h", "gdr_chunk_output", "gdr_forward", "gdr_forward_workspace_bytes",
            "gdr_forward_host", "gdr_forward_host_scratch_bytes",
-           "gdr_forward_static_scratch", "gdr_scan_output", "gdr_prepare_wyp",
+           "gdr_forward_static_scratch", "gdr_scan_output", "gdr_prepare_wyp", "gdr_gated_operands",
            "gdr_bwd_dv_local", "gdr_bwd_scan_dh", "gdr_bwd_dqkwg", "gdr_bwd_wy", "gdr_backward",
            "gdr_backward_workspace_bytes", "gdr_bwd_prepare", "gdr_bwd_scan_dh_p", "gdr_bwd_wy_dqkg",
            "gdr_bwd_group_sum", "gdr_bwd_dv_local_tc", "gdr_bwd_scan_dh_tc", "gdr_scan_transfer",
@@ -85,6 +85,7 @@ def load(path: str | None = None):
             "gdr_forward_static_scratch": [P, vp, vp, vp, vp, vp, vp, vp, vp, vp],
             "gdr_scan_output": [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp],
             "gdr_prepare_wyp": [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp],
+            "gdr_gated_operands": [P, vp, vp, vp, vp, vp, vp, vp],
             "gdr_forward_workspace_bytes": [P],
             "gdr_forward_host": [P, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int32, vp, ctypes.c_size_t, vp],
             "gdr_forward_host_scratch_bytes": [P, ctypes.c_int32],
@@ -231,6 +232,11 @@ def gdr_forward(p, q, k, v, g, beta, h0, o, h_final, workspace, workspace_bytes,
     _check(load().gdr_forward(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(o),
                               _ptr(h_final), _ptr(workspace), int(workspace_bytes), _stream(stream)),
            "gdr_forward")
+
+
+def gdr_gated_operands(p, q, k, g_cum, P, kg, qg, stream=None):
+    _check(load().gdr_gated_operands(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(g_cum), _ptr(P), _ptr(kg), _ptr(qg),
+                                     _stream(stream)), "gdr_gated_operands")
 
 
 def gdr_forward_host_scratch_bytes(p, pieces=0) -> int:

@@ -220,9 +220,11 @@ GDR_API gdr_status gdr_chunk_output(const gdr_problem* p, const void* q, const v
  *          as gdr_prepare_wyp writes it, or NULL to form it here (C = 64 for a
  *          non-NULL P); h0 [B,H,K,V] fp32 or NULL.
  * Outputs: o [B,T,H,V] bf16; h_final [B,H,K,V] fp32 or NULL (not written).
- * Returns GDR_ERR_UNSUPPORTED for fp32 io or a per-key-dim gate.  The kernel is the
- * tcgen05 one for variant FUSED_TC (K = V = 128, C = 64, P required) and for AUTO
- * where gdr_forward's AUTO would take it; the warp-level one otherwise.
+ * Returns GDR_ERR_UNSUPPORTED for fp32 io.  The kernel is the tcgen05 one for
+ * variant FUSED_TC (K = V = 128, C = 64, P required) and for AUTO where
+ * gdr_forward's AUTO would take it; the warp-level one otherwise.
+ * Per-key-dim gate: variant FUSED_TC only, with q, k, P replaced by the qg, kg
+ * and P that gdr_gated_operands writes (GDR_ERR_UNSUPPORTED otherwise).
  */
 GDR_API gdr_status gdr_scan_output(const gdr_problem* p, const void* q, const void* k, const void* w, const void* u,
                                    const float* g_cum, const void* P, const float* h0, void* o, float* h_final,
@@ -238,6 +240,24 @@ GDR_API gdr_status gdr_scan_output(const gdr_problem* p, const void* q, const vo
  */
 GDR_API gdr_status gdr_prepare_wyp(const gdr_problem* p, const void* q, const void* k, const void* v, const float* g,
                                    const void* beta, void* w, void* u, float* g_cum, void* P, void* stream);
+
+/*
+ * For a per-key-dim gate, the operands the tcgen05 scan+output kernel takes in
+ * place of q, k (gdr_scan_output, variant FUSED_TC), per (b, value head, chunk)
+ * with G = g_cum of the chunk (a K-vector per token) and G_last its last row:
+ *     P  = tril_0(Q~),  Q~_ij = sum_d q_id k_jd exp(G_id - G_jd)   [C,C] (no scale)
+ *     qg = q * exp(G),  kg = k * exp(G_last - G)                    [C,K]
+ * so that o_c = scale [qg h_c + P v'_c] and h <- exp(G_last) * h + kg^T v'_c are
+ * the chunk output and the scan of gdr_chunk_output and gdr_scan_h.  P follows
+ * the output page's form ("kernel_fun/kda/_kernels/bwd_scan.py", module
+ * docstring: the o assembly); a chunk whose gate spreads by more than 40 within
+ * it is formed in fp32 instead of from gated bf16 copies.
+ * Inputs:  q, k [B,T,H,K] bf16; g_cum [B,T,HV,K] fp32 (gdr_prepare_wy's).
+ * Outputs: P [B,NT,HV,C,C] bf16; qg, kg [B,T,HV,K] bf16 (value heads).
+ * bf16, per-key-dim gate, K = V = 128, C = 64 only (GDR_ERR_UNSUPPORTED otherwise).
+ */
+GDR_API gdr_status gdr_gated_operands(const gdr_problem* p, const void* q, const void* k, const float* g_cum, void* P,
+                                      void* kg, void* qg, void* stream);
 
 /*
  * Bytes of device workspace gdr_forward needs for this problem (0 when the

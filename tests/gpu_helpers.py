@@ -50,9 +50,10 @@ def rel_frob(x, ref):
 
 
 def variant_supports(variant, K, V, C, per_k=False):
-    """Whether a forward variant takes these sizes (the tcgen05 fused form: K = V = 128, C = 64, scalar gate)."""
+    """Whether a forward variant takes these sizes (the tcgen05 fused form: K = V = 128, C = 64, either gate;
+    the warp-level fused form: a scalar gate)."""
     if variant == "fused_tc":
-        return K == 128 and V == 128 and C == 64 and not per_k
+        return K == 128 and V == 128 and C == 64
     if variant == "fused":
         return not per_k
     return True

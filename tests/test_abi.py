@@ -208,10 +208,11 @@ def test_overlapped_fused_tc_workspace(lib):
 
 
 def test_fused_tc_variant_takes_its_sizes_only(lib):
-    # K = V = 128, C = 64, bf16, scalar gate; anything else is GDR_ERR_UNSUPPORTED before a launch
+    # K = V = 128, C = 64, bf16, either gate; anything else is GDR_ERR_UNSUPPORTED before a launch
     for (K, V, C, dt, per_k, code) in [(128, 128, 64, 1, False, None), (64, 64, 64, 1, False, 8),
                                        (128, 64, 64, 1, False, 8), (128, 128, 32, 1, False, 8),
-                                       (128, 128, 64, 1, True, 8), (128, 128, 64, 0, False, 8)]:
+                                       (128, 128, 64, 1, True, None), (128, 128, 32, 1, True, 8),
+                                       (128, 128, 64, 0, False, 8)]:
         p = gdr.make_problem(1, 256, 2, K, V, C, dt, per_k, variant="fused_tc")
         if code is None:
             assert lib.gdr_forward_workspace_bytes(ctypes.byref(p)) > 0
@@ -441,3 +442,25 @@ def test_host_forward_rejects_bad_arguments_before_launching(lib):
     assert lib.gdr_forward_host(ctypes.byref(p), None, *args[1:], None, a, None, 0, a, 1 << 40, None) == 1
     bad = gdr.make_problem(1, 256, 2, 96, 64, 64, 1, False)
     assert lib.gdr_forward_host(ctypes.byref(bad), *args, None, a, None, 0, a, 1 << 40, None) == 2
+
+
+def test_fused_tc_per_key_gate_workspace(lib):
+    # per-key-dim gate on the tcgen05 path: g_cum [B,T,HV,K] fp32, w, u, P [B,NT,HV,C,C], then the gated
+    # operands kg and qg [B,T,HV,K] (bf16), each rounded up to 256 bytes; no pieces (one call), no segments
+    r = lambda x: (x + 255) // 256 * 256
+    for (B, T, H, HV) in [(2, 8192, 16, 16), (1, 100, 2, 4), (1, 32768, 4, 4)]:
+        p = gdr.make_problem(B, T, H, 128, 128, 64, 1, True, variant="fused_tc", HV=HV if HV != H else 0,
+                             segments=1)
+        rows, nt = B * T * HV, -(-T // 64)
+        want = r(rows * 128 * 4) + 2 * r(rows * 128 * 2) + r(B * nt * HV * 64 * 64 * 2) + 2 * r(rows * 128 * 2)
+        assert lib.gdr_forward_workspace_bytes(ctypes.byref(p)) == want
+
+
+def test_gated_operands_sizes_and_gate(lib):
+    # bf16, per-key-dim gate, K = V = 128, C = 64 only
+    a = ctypes.c_void_p(16)
+    for (K, V, C, per_k, code) in [(128, 128, 64, False, 8), (64, 64, 64, True, 8), (128, 128, 32, True, 8)]:
+        p = gdr.make_problem(1, 256, 2, K, V, C, 1, per_k)
+        assert lib.gdr_gated_operands(ctypes.byref(p), a, a, a, a, a, a, None) == code
+    p = gdr.make_problem(1, 256, 2, 128, 128, 64, 1, True)
+    assert lib.gdr_gated_operands(ctypes.byref(p), a, None, a, a, a, a, None) == 1

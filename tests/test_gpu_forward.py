@@ -18,8 +18,8 @@ pytestmark = pytest.mark.gpu
 # every variant gdr_forward offers, with the io dtypes it takes
 FORWARD_VARIANTS = {"simt": (torch.float32, torch.bfloat16), "tensor": (torch.bfloat16,),
                     "fused": (torch.bfloat16,), "fused_tc": (torch.bfloat16,)}
-# the fused paths take a scalar gate only
-GATES = {"simt": (False, True), "tensor": (False, True), "fused": (False,), "fused_tc": (False,)}
+# the warp-level fused path takes a scalar gate only
+GATES = {"simt": (False, True), "tensor": (False, True), "fused": (False,), "fused_tc": (False, True)}
 SHAPES = [(2, 256, 3, 64, 64, 64), (1, 192, 2, 128, 128, 64), (2, 128, 3, 64, 128, 32),
           (1, 160, 1, 128, 64, 32), (1, 64, 2, 128, 128, 64), (1, 32, 1, 64, 64, 32),
           # a last, partial chunk: 36 of 64 tokens; 13 of 32 (the second half of a 64-token
@@ -268,7 +268,7 @@ def test_host_forward_argument_errors():
     torch.cuda.synchronize()
 
 
-@pytest.mark.parametrize("variant", ["fused", "fused_tc"])
+@pytest.mark.parametrize("variant", ["fused"])
 def test_fused_variant_refuses_per_key_gate(variant):
     x = make_inputs(1, 64, 1, 128, 128, per_k_gate=True, io_dtype=torch.bfloat16, seed=12)
     with pytest.raises(gdr.GdrError) as e:

@@ -189,6 +189,70 @@ def test_scan_output_stage_tcgen05(shape, with_h0):
     assert rel_frob(hf, scan["h_final"]) <= STAGE_TOL["bf16"]
 
 
+def _gated_ref(x, G, C):
+    """qg = q exp(G) and kg = k exp(G_last - G) per chunk (G_last the chunk's last token, or the last
+    one before T), from their definitions on the oracle's G."""
+    q, k, G = (t.double().numpy() for t in (x.q, x.k, G))
+    T = q.shape[1]
+    qg, kg = q * np.exp(G), np.empty_like(k)
+    for t0 in range(0, T, C):
+        t1 = min(T, t0 + C)
+        kg[:, t0:t1] = k[:, t0:t1] * np.exp(G[:, t1 - 1:t1] - G[:, t0:t1])
+    return qg, kg
+
+
+@pytest.mark.parametrize("shape", [(1, 256, 2, 128, 128, 64), (2, 100, 1, 128, 128, 64)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_gated_operands_stage(shape):
+    """gdr_gated_operands (per-key-dim gate) on the oracle's rounded G: P against the chunked oracle's
+    gated scores, qg and kg against their definitions."""
+    B, T, H, K, V, C = shape
+    x = make_inputs(B, T, H, K, V, per_k_gate=True, io_dtype=torch.bfloat16, seed=16)
+    G_r = rounded(chunked.prepare_wy(x.k, x.v, x.g, x.beta, C)["G"], torch.float32)
+    NT = -(-T // C)
+    P = torch.full((B, NT, H, C, C), float("nan"), device="cuda", dtype=torch.bfloat16)
+    kg = torch.full((B, T, H, K), float("nan"), device="cuda", dtype=torch.bfloat16)
+    qg = torch.full((B, T, H, K), float("nan"), device="cuda", dtype=torch.bfloat16)
+    p = gdr.problem_for(x.q, x.v, x.g, C)
+    gdr.gdr_gated_operands(p, dev(x.q), dev(x.k), dev(G_r), P, kg, qg)
+    torch.cuda.synchronize()
+    assert gdr.gdr_get_device_status() == 0
+    qg_ref, kg_ref = _gated_ref(x, G_r, C)
+    assert scaled_err(P, chunked.gated_causal_scores(x.q, x.k, G_r, C)) <= STAGE_TOL["bf16"]
+    assert scaled_err(qg, qg_ref) <= STAGE_TOL["bf16"] and scaled_err(kg, kg_ref) <= STAGE_TOL["bf16"]
+
+
+@pytest.mark.parametrize("shape", [(1, 256, 2, 128, 128, 64), (2, 100, 1, 128, 128, 64)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_scan_output_stage_tcgen05_per_key_gate(shape):
+    """The tcgen05 scan and output with a per-key-dim gate, fed the oracle's rounded w, u, G, P, qg and kg,
+    against the chunked oracle's scan and output stages."""
+    B, T, H, K, V, C = shape
+    dtype = torch.bfloat16
+    x = make_inputs(B, T, H, K, V, per_k_gate=True, io_dtype=dtype, with_h0=True, seed=17)
+    pre = chunked.prepare_wy(x.k, x.v, x.g, x.beta, C)
+    w_r, u_r, G_r = rounded(pre["w"], dtype), rounded(pre["u"], dtype), rounded(pre["G"], torch.float32)
+    P_r = rounded(chunked.gated_causal_scores(x.q, x.k, G_r, C), dtype)
+    qg_ref, kg_ref = _gated_ref(x, G_r, C)
+    qg_r, kg_r = rounded(qg_ref, dtype), rounded(kg_ref, dtype)
+    h0 = x.h0 * 20
+    scan = chunked.scan_h(x.k, w_r, u_r, G_r, h0, C)
+    o_ref = chunked.chunk_output(x.q, x.k, scan["v_new"], scan["ckpt"], G_r, C, 0.125)
+    p = gdr.problem_for(x.q, x.v, x.g, C, scale=0.125, variant="fused_tc")
+    o = torch.full((B, T, H, V), float("nan"), device="cuda", dtype=dtype)
+    hf = torch.full((B, H, K, V), float("nan"), device="cuda", dtype=torch.float32)
+    gdr.gdr_scan_output(p, dev(qg_r), dev(kg_r), dev(w_r), dev(u_r), dev(G_r), dev(P_r), dev(h0), o, hf)
+    torch.cuda.synchronize()
+    assert gdr.gdr_get_device_status() == 0 and gdr.gdr_last_variant() == "fused_tc"
+    assert scaled_err(o, o_ref) <= STAGE_TOL["bf16"]
+    assert rel_frob(hf, scan["h_final"]) <= STAGE_TOL["bf16"]
+    # the per-key-dim gate runs only on the tcgen05 kernel, with P
+    p.variant = gdr.VARIANTS["auto"]
+    with pytest.raises(gdr.GdrError) as e:
+        gdr.gdr_scan_output(p, dev(qg_r), dev(kg_r), dev(w_r), dev(u_r), dev(G_r), dev(P_r), dev(h0), o, hf)
+    assert e.value.status == 8
+
+
 def test_scan_output_tcgen05_needs_the_scores():
     x = make_inputs(1, 64, 1, 128, 128, io_dtype=torch.bfloat16)
     t = torch.zeros(64, 1, 128, device="cuda", dtype=torch.bfloat16)

@@ -28,6 +28,10 @@
 // The fp32 element work uses the packed two-lane forms (__ffma2_rn, __fmul2_rn), which round each lane
 // exactly like the scalar operations.
 //
+// A per-key-dim gate (GATED) runs the same kernel on the gated operands qg = q exp(G) and
+// kg = k exp(G_last - G) that tc_gated_operands writes with P: dh^T = v'^T kg (no gamma, no second copy
+// of v'), O2 accumulates onto O1 (o = scale (O1^T + O2^T)), and h decays by exp(G_last) per key.
+//
 // Warp roles: warp 0 loads each chunk's w, q, k, u, P by TMA into a 3-stage ring and forms
 // gamma, exp(G), exp(G_last), reading the next chunk's gate while this one's tiles land; warp 1
 // issues the MMAs (one elected lane, fully unrolled, descriptors precomputed); warps 2..17 are

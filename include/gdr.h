@@ -98,8 +98,9 @@ typedef enum gdr_gate {
  * K = V = 128 and either B * HV * V / 32 > 152 (the warp-level fused kernel's grid
  * would need more than one wave of the GPU's 152 SMs) or B = 1 with at least 128
  * chunks and no segmented scan (one long sequence, which FUSED_TC runs in pieces
- * whose scans overlap the next piece's prepare), else FUSED; TENSOR for other
- * bf16 problems; SIMT for fp32 io.  The single-stage entry points run their
+ * whose scans overlap the next piece's prepare), else FUSED; with a per-key-dim
+ * gate FUSED_TC when K = V = 128, C = 64 and no segmented scan applies; TENSOR for
+ * other bf16 problems; SIMT for fp32 io.  The single-stage entry points run their
  * tensor-core kernel for AUTO, TENSOR, FUSED and FUSED_TC on bf16 io. */
 typedef enum gdr_variant {
     GDR_VARIANT_AUTO = 0,
@@ -108,8 +109,9 @@ typedef enum gdr_variant {
     GDR_VARIANT_FUSED = 3,    /* WY prepare, then scan and output fused, warp-level MMA, one CTA per
                                  (batch, head, 32 value columns) (bf16 io, scalar gate) */
     GDR_VARIANT_FUSED_TC = 4  /* the same with scan and output on the tcgen05 tensor cores, one CTA per
-                                 (batch, head) (bf16 io, scalar gate, K = V = 128, chunk 64); packed
-                                 sequences (gdr_varlen_*) run FUSED for it */
+                                 (batch, head) (bf16 io, K = V = 128, chunk 64; a per-key-dim gate
+                                 adds the gdr_gated_operands kernel); packed sequences (gdr_varlen_*)
+                                 run FUSED for it, or TENSOR with a per-key-dim gate */
 } gdr_variant;
 
 typedef struct gdr_problem {

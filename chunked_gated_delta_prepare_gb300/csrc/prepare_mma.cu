@@ -586,50 +586,82 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
             tw[J][3] = wm::pack2(Xr[J][1][2] * bb.x * eb.x, Xr[J][1][3] * bb.y * eb.y);
         }
     }
-    // out[16 x D] = T [16 x 64] * B [64 x D], B = k (or k exp(G)) or v read token-major by ldmatrix.trans;
-    // k-steps outside J0 .. I multiply zeros and are skipped
-    auto product = [&](const uint32_t (&ta)[4][4], uint32_t b_t, int n0, float (&acc)[8][4]) {
+    // The products out[64 x D] = T [64 x 64] * B [64 x D], B = k (or k exp(G)) or v read token-major by
+    // ldmatrix.trans, balanced over the warps: each warp takes a quarter of the output columns over every
+    // row block (row block I needs the k-steps J0(I) .. I, so row-block ownership would leave warp 3 four
+    // times warp 0's work).  The T fragments therefore go through shared memory, over the solve's scratch.
+    __syncthreads();   // every warp is past the solve's scratch
+    const uint32_t tw_t = s_base + L::kF + 1024, tu_t = tw_t + 8192;   // T's [64][64] bf16 tiles
+    static_assert(L::scratch >= 1024 + 2 * 8192, "the T tiles fit the solve's scratch");
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+    for (int J = 0; J < 4; ++J) {
+        const uint32_t off = tile_off(warp * 16 + 8 * (mi & 1) + mr, 16 * J + 8 * (mi >> 1));
+        asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(tw_t + off), "r"(tw[J][0]),
+                     "r"(tw[J][1]), "r"(tw[J][2]), "r"(tw[J][3])
+                     : "memory");
+        asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(tu_t + off), "r"(tu[J][0]),
+                     "r"(tu[J][1]), "r"(tu[J][2]), "r"(tu[J][3])
+                     : "memory");
+    }
+    __syncthreads();
+    // this warp's D / 4 output columns of all four row blocks; k-steps outside J0(I) .. I multiply zeros
+    auto product = [&](uint32_t a_t, uint32_t b_t, auto dcols, float (&acc)[4][decltype(dcols)::value / 32][4]) {
+        constexpr int D = decltype(dcols)::value, NW = D / 32;
+        const int n0 = warp * (D / 4);
+#pragma unroll
+        for (int I = 0; I < 4; ++I)
+#pragma unroll
+            for (int j = 0; j < NW; ++j) acc[I][j][0] = acc[I][j][1] = acc[I][j][2] = acc[I][j][3] = 0.f;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-            if (kk < J0 || kk > I) continue;
+            uint32_t bfr[NW / 2][4];
 #pragma unroll
-            for (int jp = 0; jp < 8; jp += 2) {
-                uint32_t bfr[4];
-                wm::ldsm_x4_t(b_t + tile_off(16 * kk + 8 * (mi & 1) + mr, n0 + 8 * jp + 8 * (mi >> 1)), bfr);
-                wm::mma16816(acc[jp], ta[kk], bfr[0], bfr[1]);
-                wm::mma16816(acc[jp + 1], ta[kk], bfr[2], bfr[3]);
+            for (int jp = 0; jp < NW / 2; ++jp)
+                wm::ldsm_x4_t(b_t + tile_off(16 * kk + 8 * (mi & 1) + mr, n0 + 16 * jp + 8 * (mi >> 1)), bfr[jp]);
+#pragma unroll
+            for (int I = 0; I < 4; ++I) {
+                if (kk > I || kk < (I / NB) * NB) continue;
+                uint32_t a[4];
+                wm::ldsm_x4(a_t + tile_off(16 * I + 8 * (mi & 1) + mr, 16 * kk + 8 * (mi >> 1)), a);
+#pragma unroll
+                for (int jp = 0; jp < NW / 2; ++jp) {
+                    wm::mma16816(acc[I][2 * jp], a, bfr[jp][0], bfr[jp][1]);
+                    wm::mma16816(acc[I][2 * jp + 1], a, bfr[jp][2], bfr[jp][3]);
+                }
             }
         }
     };
     // bf16 results into a tile of the same layout (128-byte swizzle, 64-column atoms) by stmatrix
-    auto stage_out = [&](uint32_t st, int n0, const float (&acc)[8][4]) {
+    auto stage_out = [&](uint32_t st, auto dcols, const float (&acc)[4][decltype(dcols)::value / 32][4]) {
+        constexpr int D = decltype(dcols)::value, NW = D / 32;
+        const int n0 = warp * (D / 4);
 #pragma unroll
-        for (int jp = 0; jp < 8; jp += 2) {
-            const uint32_t r[4] = {wm::pack2(acc[jp][0], acc[jp][1]), wm::pack2(acc[jp][2], acc[jp][3]),
-                                   wm::pack2(acc[jp + 1][0], acc[jp + 1][1]), wm::pack2(acc[jp + 1][2], acc[jp + 1][3])};
-            asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(
-                             st + tile_off(warp * 16 + 8 * (mi & 1) + mr, n0 + 8 * jp + 8 * (mi >> 1))),
-                         "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
-                         : "memory");
-        }
+        for (int I = 0; I < 4; ++I)
+#pragma unroll
+            for (int jp = 0; jp < NW / 2; ++jp) {
+                const uint32_t r[4] = {wm::pack2(acc[I][2 * jp][0], acc[I][2 * jp][1]),
+                                       wm::pack2(acc[I][2 * jp][2], acc[I][2 * jp][3]),
+                                       wm::pack2(acc[I][2 * jp + 1][0], acc[I][2 * jp + 1][1]),
+                                       wm::pack2(acc[I][2 * jp + 1][2], acc[I][2 * jp + 1][3])};
+                asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(
+                                 st + tile_off(16 * I + 8 * (mi & 1) + mr, n0 + 16 * jp + 8 * (mi >> 1))),
+                             "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
+                             : "memory");
+            }
     };
-    // One tile at a time, the result replacing the tile it was computed from: products of all its
-    // 64-column atoms into registers, a barrier (every warp is done reading it), then the results over it.
-    // This keeps the CTA at three per SM (no separate staging region).
-    auto product_in_place = [&](const uint32_t (&ta)[4][4], uint32_t tile, auto dcols) {
+    // One tile at a time, the result replacing the tile it was computed from: this warp's products into
+    // registers, a barrier (every warp is done reading the tile), then the results over it.  This keeps
+    // the CTA at three per SM (no separate staging region).
+    auto product_in_place = [&](uint32_t a_t, uint32_t tile, auto dcols) {
         constexpr int D = decltype(dcols)::value;
-        float acc[D / 64][8][4];
-#pragma unroll
-        for (int a = 0; a < D / 64; ++a) product(ta, tile, 64 * a, acc[a]);
+        float acc[4][D / 32][4];
+        product(a_t, tile, dcols, acc);
         __syncthreads();
-#pragma unroll
-        for (int a = 0; a < D / 64; ++a) stage_out(tile, 64 * a, acc[a]);
+        stage_out(tile, dcols, acc);
     };
     // w over the tile it reads (k, or its scaled copy Ka), then u over v
     const uint32_t w_tile = PER_K ? L::kKa : L::kK;
-    product_in_place(tw, s_base + w_tile, std::integral_constant<int, K>{});
+    product_in_place(tw_t, s_base + w_tile, std::integral_constant<int, K>{});
     // w and P leave while u is formed (rows past T are clipped by the tensor maps)
     bw::fence_async_shared();
     __syncthreads();
@@ -644,7 +676,7 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
         zero_rows(L::kV, V, nvalid, kTile, tid, 128);
         __syncthreads();
     }
-    product_in_place(tu, s_base + L::kV, std::integral_constant<int, V>{});
+    product_in_place(tu_t, s_base + L::kV, std::integral_constant<int, V>{});
     bw::fence_async_shared();
     __syncthreads();
     if (tid == 0) {

@@ -293,7 +293,7 @@ gdr_status forward_tc_overlapped(const gdr::Dims& d, const int* bounds, int piec
         char* op = static_cast<char*>(o) + (size_t)t0 * d.H * d.V * e;
         const float* hin = i == 0 ? h0 : carry + (size_t)(i - 1) * state;
         float* hout = i == pieces - 1 ? h_final : carry + (size_t)i * state;
-        cudaError_t ce = gdr::mma_prepare(dp, kp, vp, gp, bp, w, u, g_cum, s, err, qp, P, nullptr, i > 0);
+        cudaError_t ce = gdr::mma_prepare(dp, kp, vp, gp, bp, w, u, g_cum, s, err, qp, P, nullptr, i > 0, true);
         if (ce == cudaSuccess) ce = gdr::tc_scan_output(dp, qp, kp, w, u, g_cum, P, hin, op, hout, s, err);
         if (ce != cudaSuccess) return GDR_ERR_CUDA;
     }

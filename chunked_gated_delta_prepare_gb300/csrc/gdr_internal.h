@@ -32,9 +32,12 @@ cudaError_t simt_output(const Dims& d, const void* q, const void* k, const void*
 // per chunk as [B, NT, H, C, C] bf16; with tinv non-NULL, (I + A)^{-1} per chunk, [B, NT, H, C, C] bf16
 // pdl: launch as the programmatic dependent of the stream's previous kernel (see gdr_api.cpp's overlapped
 // forward): it may start once every CTA of that kernel has signalled, and must read nothing it writes.
+// tc_scores: S = k k^T and P = q k^T on tcgen05 (K = V = 128 with P, one q/k head per value head, no
+// inverse; other calls ignore it).  The overlapped forward asks for it: beside the scan the forward
+// measured faster with it, while a prepare on its own is faster on mma.sync.
 cudaError_t mma_prepare(const Dims& d, const void* k, const void* v, const float* g, const void* beta, void* w,
                         void* u, float* g_cum, cudaStream_t s, unsigned int* err, const void* q = nullptr,
-                        void* P = nullptr, void* tinv = nullptr, bool pdl = false);
+                        void* P = nullptr, void* tinv = nullptr, bool pdl = false, bool tc_scores = false);
 // The prepare with P (scalar gate, C = 64) on the chunk-packed row d (B = 1) of packed variable-length
 // sequences, reading q, k, v, g, beta in place from the caller's packed tensors of `total` tokens: chunk c of
 // the row is chunk c - co[s] of sequence s = cs[c] (cu, co, cs as varlen_plan makes them).  w, u, g_cum and

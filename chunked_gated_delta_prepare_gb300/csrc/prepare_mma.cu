@@ -22,9 +22,14 @@
 //            each warp skipping the k-steps where its row of X is zero
 //
 // The products are warp-level mma.sync m16n8k16 (bf16 in, fp32 accumulate) fed
-// by ldmatrix from the swizzled tiles: at these sizes (64 x 64 x 128 and
-// 64 x 128 x 64 per tile) a tcgen05 MMA's fixed ~240-cycle cost per K=16 step
-// makes it slower than mma.sync, and without tensor memory more CTAs fit an SM.
+// by ldmatrix from the swizzled tiles, or, for S and P, tcgen05 with the
+// accumulators in tensor memory (UMMA below).  Measured on the 32k-token,
+// 32-head workload (the prepare alone over the whole GPU / the overlapped
+// forward): every product on mma.sync 0.386 / 0.799 ms; S and P on tcgen05
+// 0.392 / 0.786 ms; S, P, w and u on tcgen05 0.409 / 0.797 ms.  At three CTAs
+// per SM a tile is latency-bound: tcgen05 shortens S and P (the warps wait for
+// one product instead of issuing up to 64 mma each), but w and u each add a
+// round trip and a second pass through the same 128 TMEM columns.
 // beta (and, for a scalar gate, exp(G)) is folded into the columns of X, so k
 // and v feed the MMA as TMA left them.
 #include <cuda.h>
@@ -150,7 +155,13 @@ struct PackedIn {
     int total;
 };
 
-template <int K, int V, int C, bool PER_K, bool WITH_P, bool EXTRA, bool PACKED>
+// UMMA (K = V = 128, C = 64, scalar gate, with P, tokens read in place): S = k k^T and P = q k^T on
+// tcgen05 instead of mma.sync.  Warp 1 issues both (M = N = 64, K = 128) from one elected lane as soon as
+// the k and q tiles land; the accumulators take 128 columns of tensor memory (S, then P), which the warps
+// read back with 16x256b loads in the mma.sync accumulator layout, so the gating, the solve and the
+// products that follow are shared with the mma.sync form.  An M = 64 accumulator keeps rows 16q .. 16q+15
+// in lanes 0 .. 15 of sub-partition q: warp q's own block row.
+template <int K, int V, int C, bool PER_K, bool WITH_P, bool EXTRA, bool PACKED, bool UMMA>
 __global__ void __launch_bounds__(128, 3)
 prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
                    const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap mu,
@@ -158,6 +169,7 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
                    const float* __restrict__ g, const bf16* __restrict__ beta, float* __restrict__ g_cum,
                    bf16* __restrict__ tinv, int T, int H, int G, PackedIn pin, unsigned int* err) {
     static_assert(!PACKED || (C == kTile && !PER_K), "packed inputs: whole 64-token chunks, scalar gate");
+    static_assert(!UMMA || (K == 128 && V == 128 && C == 64 && !PER_K && WITH_P && !PACKED), "tcgen05 S, P: one shape");
     using L = PrepLayout<K, V, C, PER_K, WITH_P>;
     constexpr int GW = L::GW;
     extern __shared__ unsigned char smem_raw[];
@@ -168,6 +180,8 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
     float* sE = reinterpret_cast<float*>(F + L::fE);
     int* sFlag = reinterpret_cast<int*>(F + L::fFlag);
     __shared__ uint64_t bar_k, bar_q, bar_v;   // one per tile, each waited on just before its first use
+    __shared__ uint64_t bar_s, bar_p;   // UMMA: one per product, each completed once
+    __shared__ uint32_t tslot;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // CTAs run chunk-major, the sequence's last tile first, so the first chunks are the last written and
@@ -220,6 +234,10 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
         bw::mbar_init(&bar_k, 1);
         bw::mbar_init(&bar_q, 1);
         bw::mbar_init(&bar_v, 1);
+        if constexpr (UMMA) {
+            bw::mbar_init(&bar_s, 1);
+            bw::mbar_init(&bar_p, 1);
+        }
         bw::fence_mbar_init();
         *sFlag = 0;
     }
@@ -241,6 +259,32 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
     }
     static_assert(kTile <= 128, "one beta row per thread");
     if (tid < kTile) sB[tid] = b_pre;
+    // UMMA: warp 1 (idle while warp 0 scans the gate) takes 128 tensor-memory columns (three CTAs per SM
+    // take 384 of the 512) and issues S = k k^T (columns 0..63) and P = q k^T (64..127) as k and q land
+    if (UMMA && warp == 1) {
+        __syncwarp();
+        bw::tmem_alloc(&tslot, 128);
+        bw::tmem_relinquish();
+        bw::tc_fence_before();
+        __syncwarp();
+        bw::tc_fence_after();
+        const uint32_t t = tslot;
+        constexpr uint32_t idS = bw::idesc_bf16(64, 64, 0, 0);
+        bw::mbar_wait(&bar_k, 0, err, kDeviceErrTimeout);   // a timeout is recorded; the stores follow thread 0's waits
+        __syncwarp();
+        bw::tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < K / 16; ++kk)
+            bw::mma_bf16_warp(t, desc_kmajor(s_base + L::kK, kk), desc_kmajor(s_base + L::kK, kk), idS, kk > 0);
+        bw::mma_commit_warp(&bar_s);
+        bw::mbar_wait(&bar_q, 0, err, kDeviceErrTimeout);
+        __syncwarp();
+        bw::tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < K / 16; ++kk)
+            bw::mma_bf16_warp(t + 64, desc_kmajor(s_base + L::kQ, kk), desc_kmajor(s_base + L::kK, kk), idS, kk > 0);
+        bw::mma_commit_warp(&bar_p);
+    }
     if constexpr (PER_K) {
         // 16-byte loads, all of a thread's issued before any is used (the tile is 32 KB at K = 128)
         constexpr int NV4 = kTile * GW / 4 / 128;
@@ -318,6 +362,14 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
     }
     __syncthreads();
 
+    // UMMA: the tensor-memory columns warp 1 took (S at 0..63, P at 64..127) in this warp's sub-partition
+    uint32_t tmem = 0, tq = 0;
+    if constexpr (UMMA) {
+        bw::tc_fence_after();
+        tmem = tslot;
+        tq = tmem + ((uint32_t)(warp * 32) << 16);
+    }
+
     const int g4 = lane >> 2, q4 = lane & 3, mi = lane >> 3, mr = lane & 7;
     const int i0 = warp * 16 + g4, i1 = i0 + 8;       // the two tile rows of this thread's fragments
     float Af[8][4];                                   // A block row of this warp as C fragments
@@ -326,6 +378,13 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
         const uint32_t a_t = s_base + (PER_K ? L::kKa : L::kK);
         const uint32_t b_t = s_base + (PER_K ? L::kKb : L::kK);
         float S[8][4];
+        if constexpr (UMMA) {
+            ok = bw::mbar_wait(&bar_s, 0, err, kDeviceErrTimeout) && ok;
+            __syncwarp();   // the loads below are warp-wide
+            bw::tc_fence_after();
+            bw::tmem_ld16x256b_x8(tq, &S[0][0]);
+            bw::tmem_ld_wait();
+        } else {
 #pragma unroll
         for (int j = 0; j < 8; ++j) S[j][0] = S[j][1] = S[j][2] = S[j][3] = 0.f;
 #pragma unroll
@@ -342,6 +401,7 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
                 wm::mma16816(S[jp], a, bfr[0], bfr[1]);
                 wm::mma16816(S[jp + 1], a, bfr[2], bfr[3]);
             }
+        }
         }
         // A from S, in place: element (i, j) of this thread's fragments
         const int c0 = (i0 / C) * C;                 // i0 and i1 share a chunk (16-row blocks never straddle one)
@@ -370,6 +430,13 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
         // zero and skipped) -> bf16 into the q tile's place (each warp overwrites only its own rows of
         // q, after reading them), as a [64][64] tile in the 128-byte swizzle; stored with w and u below
         float Pq[8][4];
+        if constexpr (UMMA) {   // the product has read every row of q once its barrier completes
+            ok = bw::mbar_wait(&bar_p, 0, err, kDeviceErrTimeout) && ok;
+            __syncwarp();
+            bw::tc_fence_after();
+            bw::tmem_ld16x256b_x8(tq + 64, &Pq[0][0]);
+            bw::tmem_ld_wait();
+        } else {
 #pragma unroll
         for (int j = 0; j < 8; ++j) Pq[j][0] = Pq[j][1] = Pq[j][2] = Pq[j][3] = 0.f;
 #pragma unroll
@@ -384,6 +451,7 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
                 wm::mma16816(Pq[jp], aq, bfr[0], bfr[1]);
                 wm::mma16816(Pq[jp + 1], aq, bfr[2], bfr[3]);
             }
+        }
         }
 #pragma unroll
         for (int jp = 0; jp < 8; jp += 2) {
@@ -590,7 +658,12 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
     // ldmatrix.trans, balanced over the warps: each warp takes a quarter of the output columns over every
     // row block (row block I needs the k-steps J0(I) .. I, so row-block ownership would leave warp 3 four
     // times warp 0's work).  The T fragments therefore go through shared memory, over the solve's scratch.
+    if constexpr (UMMA) bw::tc_fence_before();   // the S and P loads are complete
     __syncthreads();   // every warp is past the solve's scratch
+    if (UMMA && warp == 1) {
+        bw::tc_fence_after();
+        bw::tmem_dealloc(tmem, 128);
+    }
     const uint32_t tw_t = s_base + L::kF + 1024, tu_t = tw_t + 8192;   // T's [64][64] bf16 tiles
     static_assert(L::scratch >= 1024 + 2 * 8192, "the T tiles fit the solve's scratch");
 #pragma unroll
@@ -691,7 +764,7 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
 
 // pdl: launched as the programmatic dependent of the kernel before it in the stream (it may start as
 // soon as every CTA of that kernel has signalled, and reads nothing that kernel writes).
-template <int K, int V, int C, bool PER_K, bool WITH_P, bool EXTRA, bool PACKED = false>
+template <int K, int V, int C, bool PER_K, bool WITH_P, bool EXTRA, bool PACKED = false, bool UMMA = false>
 cudaError_t launch_prepare_v(const Dims& d, const void* q, const void* k, const void* v, const float* g,
                              const void* beta, void* w, void* u, float* g_cum, void* P, void* tinv, cudaStream_t s,
                              unsigned int* err, PackedIn pin = PackedIn{}, bool pdl = false) {
@@ -713,7 +786,7 @@ cudaError_t launch_prepare_v(const Dims& d, const void* q, const void* k, const 
         if (!make_tmap_tokens(&mq, q, bi, ti, d.Hk, K, kTile) || !make_tmap_bf16_4d(&mp, P, dims, st, box))
             return cudaErrorInvalidValue;
     }
-    auto kern = prepare_mma_kernel<K, V, C, PER_K, WITH_P, EXTRA, PACKED>;
+    auto kern = prepare_mma_kernel<K, V, C, PER_K, WITH_P, EXTRA, PACKED, UMMA>;
     const size_t smem = L::bytes + 1024;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -740,7 +813,12 @@ cudaError_t launch_prepare_v(const Dims& d, const void* q, const void* k, const 
 template <int K, int V, int C, bool PER_K, bool WITH_P>
 cudaError_t launch_prepare(const Dims& d, const void* q, const void* k, const void* v, const float* g,
                            const void* beta, void* w, void* u, float* g_cum, void* P, void* tinv, cudaStream_t s,
-                           unsigned int* err, bool pdl) {
+                           unsigned int* err, bool pdl, bool tc_scores) {
+    if constexpr (K == 128 && V == 128 && C == 64 && !PER_K && WITH_P) {
+        if (tc_scores && d.G == 1 && !tinv)
+            return launch_prepare_v<K, V, C, PER_K, WITH_P, false, false, true>(d, q, k, v, g, beta, w, u, g_cum, P,
+                                                                                tinv, s, err, PackedIn{}, pdl);
+    }
     if (d.G != 1 || tinv)
         return launch_prepare_v<K, V, C, PER_K, WITH_P, true>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err,
                                                               PackedIn{}, pdl);
@@ -751,20 +829,21 @@ cudaError_t launch_prepare(const Dims& d, const void* q, const void* k, const vo
 template <int K, int V, int C>
 cudaError_t pick_gate(const Dims& d, const void* q, const void* k, const void* v, const float* g, const void* beta,
                       void* w, void* u, float* g_cum, void* P, void* tinv, cudaStream_t s, unsigned int* err,
-                      bool pdl) {
-    if (d.per_k) return launch_prepare<K, V, C, true, false>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err, pdl);
+                      bool pdl, bool tc) {
+    if (d.per_k)
+        return launch_prepare<K, V, C, true, false>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err, pdl, tc);
     if constexpr (C == 64) {
-        if (P) return launch_prepare<K, V, C, false, true>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err, pdl);
+        if (P) return launch_prepare<K, V, C, false, true>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err, pdl, tc);
     }
-    return launch_prepare<K, V, C, false, false>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err, pdl);
+    return launch_prepare<K, V, C, false, false>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err, pdl, tc);
 }
 
 template <int K, int V>
 cudaError_t pick_chunk(const Dims& d, const void* q, const void* k, const void* v, const float* g, const void* beta,
                        void* w, void* u, float* g_cum, void* P, void* tinv, cudaStream_t s, unsigned int* err,
-                       bool pdl) {
-    return d.C == 32 ? pick_gate<K, V, 32>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err, pdl)
-                     : pick_gate<K, V, 64>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err, pdl);
+                       bool pdl, bool tc) {
+    return d.C == 32 ? pick_gate<K, V, 32>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err, pdl, tc)
+                     : pick_gate<K, V, 64>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err, pdl, tc);
 }
 
 template <int K, int V>
@@ -794,13 +873,14 @@ cudaError_t mma_prepare_packed(const Dims& d, const void* q, const void* k, cons
 
 cudaError_t mma_prepare(const Dims& d, const void* k, const void* v, const float* g, const void* beta, void* w,
                         void* u, float* g_cum, cudaStream_t s, unsigned int* err, const void* q, void* P,
-                        void* tinv, bool pdl) {
+                        void* tinv, bool pdl, bool tc_scores) {
     if (!d.bf16) return cudaErrorInvalidValue;
     if (P && (d.per_k || d.C != 64 || !q)) return cudaErrorInvalidValue;
-    if (d.K == 64 && d.V == 64) return pick_chunk<64, 64>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err, pdl);
-    if (d.K == 64 && d.V == 128) return pick_chunk<64, 128>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err, pdl);
-    if (d.K == 128 && d.V == 64) return pick_chunk<128, 64>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err, pdl);
-    return pick_chunk<128, 128>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err, pdl);
+    const bool tc = tc_scores;
+    if (d.K == 64 && d.V == 64) return pick_chunk<64, 64>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err, pdl, tc);
+    if (d.K == 64 && d.V == 128) return pick_chunk<64, 128>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err, pdl, tc);
+    if (d.K == 128 && d.V == 64) return pick_chunk<128, 64>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err, pdl, tc);
+    return pick_chunk<128, 128>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err, pdl, tc);
 }
 
 }  // namespace gdr

@@ -10,6 +10,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace gdr {
@@ -200,6 +201,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_
            | ((uint32_t)(M >> 4) << 24);   // M / 16
 }
 
+// The same descriptor for A and B of the io type: bf16, or fp16 (format 0 in both fields) when f16.
+__host__ __device__ constexpr uint32_t idesc_io(int M, int N, int a_mn, int b_mn, bool f16) {
+    return idesc_bf16(M, N, a_mn, b_mn) & ~(f16 ? ((7u << 7) | (7u << 10)) : 0u);
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle.
 //   start: byte address of the operand's first element (smem)
 //   lbo, sbo: leading / stride byte offsets (multiples of 16)
@@ -266,6 +272,21 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int col) {   // byte o
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+// The io type's pair (bf16, or fp16 when F16) and its scalar read.
+template <bool F16>
+__device__ __forceinline__ uint32_t pack_io(float lo, float hi) {
+    if constexpr (F16) return pack_f16(lo, hi);
+    else return pack_bf16(lo, hi);
+}
+template <bool F16>
+__device__ __forceinline__ float load_io(const void* p) {
+    if constexpr (F16) return __half2float(*reinterpret_cast<const __half*>(p));
+    else return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(p));
 }
 
 }  // namespace bw

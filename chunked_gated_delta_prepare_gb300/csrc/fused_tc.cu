@@ -1,6 +1,6 @@
 // State scan + chunk output of one (batch, head) per CTA on the tcgen05 tensor
-// cores, for bf16 io, a scalar gate, K = V = 128 and 64-token chunks (any T,
-// grouped value heads):
+// cores, for bf16 io (or fp16, scalar gate), K = V = 128 and 64-token chunks
+// (any T, grouped value heads):
 //
 //   scan   ("kernel_fun/kda/_kernels/bwd_scan.py", module docstring):
 //          v'_c = u_c - w_c h_c;  h_{c+1} = exp(G_last) h_c + (k exp(G_last - G))^T v'_c
@@ -117,7 +117,9 @@ __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.
 // GATED (a per-key-dim gate): q and k are the gated operands qg = q exp(G) and kg = k exp(G_last - G)
 // (per element, one per value head; see tc_gated_operands), so dh^T = v'^T kg, o = scale (O1^T + O2^T)
 // with O2 accumulated onto O1, and the decay exp(G_last) is a vector over the keys.
-template <bool GENERAL, bool GATED>
+// F16 (scalar gate): fp16 io.  q, k and the prepare's w, u, P are fp16, and so are the tensor-memory
+// operands written here (h_c^T, v'^T), since both operands of one MMA share a type; o is stored as fp16.
+template <bool GENERAL, bool GATED, bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap mq,
                       const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mu,
@@ -228,8 +230,8 @@ tc_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_const
             pd[kk] = tc::desc_kmajor(s_base + L::P, kk);
         }
         constexpr uint64_t kQoff = (L::Q - L::W) >> 4;   // the q tile's descriptors: w's plus this start offset
-        constexpr uint32_t idT = bw::idesc_bf16(128, 64, 0, 0);     // N = 64 tokens, B K-major
-        constexpr uint32_t idK = bw::idesc_bf16(128, 128, 0, 1);    // N = 128 keys, B MN-major
+        constexpr uint32_t idT = bw::idesc_io(128, 64, 0, 0, F16);     // N = 64 tokens, B K-major
+        constexpr uint32_t idK = bw::idesc_io(128, 128, 0, 1, F16);    // N = 128 keys, B MN-major
         // O2 of a chunk: v'^T P^T, then its output and its stage are complete
         auto issue_o2 = [&](int cc) {
             const uint64_t so = (uint64_t)((cc % kNS) * L::kStage) >> 4;
@@ -282,7 +284,7 @@ tc_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_const
         auto store_h = [&](int buf) {
             uint32_t pk[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) pk[j] = bw::pack_bf16(hs[2 * j], hs[2 * j + 1]);
+            for (int j = 0; j < 16; ++j) pk[j] = bw::pack_io<F16>(hs[2 * j], hs[2 * j + 1]);
             tmem_st16(lb + cHB + 64 * buf + part * 16, pk);
             tmem_st_wait();
             bw::tc_fence_before();
@@ -329,7 +331,7 @@ tc_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_const
             bf16* dst = o + (((int64_t)b * T + tt + odd) * H + h) * kV + (v & ~1);
 #pragma unroll
             for (int m = 0; m < 8; ++m) {
-                const uint32_t pk = bw::pack_bf16(r[2 * m], r[2 * m + 1]);
+                const uint32_t pk = bw::pack_io<F16>(r[2 * m], r[2 * m + 1]);
                 const uint32_t ot = __shfl_xor_sync(0xffffffffu, pk, 1);
                 const uint32_t word = odd ? __byte_perm(ot, pk, 0x7632) : __byte_perm(pk, ot, 0x5410);
                 if (!GENERAL || tt + 2 * m + odd < T)
@@ -349,7 +351,7 @@ tc_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_const
             float uu[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j)
-                uu[j] = __bfloat162float(*reinterpret_cast<const bf16*>(us + (tok0 + j) * (kV * 2) + v * 2));
+                uu[j] = bw::load_io<F16>(us + (tok0 + j) * (kV * 2) + v * 2);
             // v'^T = u^T - D^T for tokens tok0 .. tok0 + 15
             if (!bw::mbar_wait(&barD, c & 1, err, kDeviceErrTimeout)) { ok = false; break; }
             bw::tc_fence_after();
@@ -365,14 +367,14 @@ tc_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_const
                                                  make_float2(uu[4 * j], uu[4 * j + 1]));
                     const float2 x1 = __ffma2_rn(make_float2(d[4 * j + 2], d[4 * j + 3]), make_float2(-1.f, -1.f),
                                                  make_float2(uu[4 * j + 2], uu[4 * j + 3]));
-                    pv[2 * j] = bw::pack_bf16(x0.x, x0.y);
-                    pv[2 * j + 1] = bw::pack_bf16(x1.x, x1.y);
+                    pv[2 * j] = bw::pack_io<F16>(x0.x, x0.y);
+                    pv[2 * j + 1] = bw::pack_io<F16>(x1.x, x1.y);
                     if constexpr (!GATED) {
                         const float4 gm = g4[j];
                         const float2 y0 = __fmul2_rn(x0, make_float2(gm.x, gm.y));
                         const float2 y1 = __fmul2_rn(x1, make_float2(gm.z, gm.w));
-                        pg[2 * j] = bw::pack_bf16(y0.x, y0.y);
-                        pg[2 * j + 1] = bw::pack_bf16(y1.x, y1.y);
+                        pg[2 * j] = bw::pack_io<F16>(y0.x, y0.y);
+                        pg[2 * j + 1] = bw::pack_io<F16>(y1.x, y1.y);
                     }
                 }
                 tmem_st8(lb + cVP + 32 * (c & 1) + tok0 / 2, pv);
@@ -427,7 +429,9 @@ tc_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_const
 }  // namespace
 
 bool tc_scan_output_supported(const Dims& d) {
-    return d.bf16 && d.K == kK && d.V == kV && d.C == kC && (int64_t)d.B * d.H <= 0x7fffffff;
+    // fp16 io: scalar gate (the prepare's fp16 form)
+    const bool io = d.bf16 || (d.f16 && !d.per_k);
+    return io && d.K == kK && d.V == kV && d.C == kC && (int64_t)d.B * d.H <= 0x7fffffff;
 }
 
 cudaError_t tc_scan_output(const Dims& d, const void* q, const void* k, const void* w, const void* u,
@@ -447,8 +451,10 @@ cudaError_t tc_scan_output(const Dims& d, const void* q, const void* k, const vo
     if (!make_tmap_bf16_4d(&mp, P, dims, st, box)) return cudaErrorInvalidValue;
     const size_t smem = TcLayout::bytes + 1024;
     const bool general = d.T % kC != 0 || (!d.per_k && d.G != 1);
-    auto kern = d.per_k ? (general ? tc_scan_output_kernel<true, true> : tc_scan_output_kernel<false, true>)
-                        : (general ? tc_scan_output_kernel<true, false> : tc_scan_output_kernel<false, false>);
+    auto kern = d.f16 ? (general ? tc_scan_output_kernel<true, false, true> : tc_scan_output_kernel<false, false, true>)
+                : d.per_k ? (general ? tc_scan_output_kernel<true, true, false> : tc_scan_output_kernel<false, true, false>)
+                          : (general ? tc_scan_output_kernel<true, false, false>
+                                     : tc_scan_output_kernel<false, false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if (pdl) {

@@ -113,7 +113,10 @@ gdr_status pick_forward(const gdr_problem* p, const gdr::Dims& d, Path* path) {
             // pieces overlapped with the prepare (see forward_tc_overlapped).
             // A per-key-dim gate at K = V = 128, C = 64 takes the tcgen05 form too (its gated operands from
             // their own kernel) unless the segment-parallel scan applies.
-            if (!d.bf16) *path = Path::Simt;
+            // fp16 io: the tcgen05 form where it is built (scalar gate, K = V = 128, C = 64), else the
+            // CUDA-core path.
+            if (d.f16) *path = gdr::tc_scan_output_supported(d) ? Path::FusedTc : Path::Simt;
+            else if (!d.bf16) *path = Path::Simt;
             else if (!d.per_k && d.C == 64)
                 *path = gdr::tc_scan_output_supported(d) &&
                                 ((int64_t)d.B * d.H * (d.V / 32) > kSmCount || (d.B == 1 && d.NT >= 2 * kPieceChunks &&
@@ -163,6 +166,7 @@ constexpr int kSegMinChunks = 16;
 gdr_status resolve_segments(const gdr_problem* p, const gdr::Dims& d, bool tensor, int* S) {
     *S = 1;
     if (p->segments == 1 || !tensor) return GDR_OK;
+    if (d.f16) return p->segments > 1 ? GDR_ERR_UNSUPPORTED : GDR_OK;   // the segment maps are bf16 kernels
     if (p->segments > 1) {
         if (d.T % d.C != 0 || d.NT % p->segments != 0 || p->segments > kMaxGridYZ / d.B) return GDR_ERR_ARG;
         *S = (int)p->segments;
@@ -1271,8 +1275,8 @@ gdr_status gdr_varlen_forward(const gdr_problem* p_in, const int32_t* cu_seqlens
         return st;
     Path path;
     if ((st = pick_forward(p, d, &path)) != GDR_OK) return st;
-    if (path == Path::FusedTc)   // packed sequences: the warp-level fused kernel, or the staged one (KDA)
-        path = d.per_k ? Path::Tensor : Path::Fused;
+    if (path == Path::FusedTc)   // packed sequences: the warp-level fused kernel, or the staged one (KDA);
+        path = d.f16 ? Path::Simt : d.per_k ? Path::Tensor : Path::Fused;   // fp16: the CUDA-core path
     char* base = static_cast<char*>(workspace);
     int64_t rb[11];
     varlen_rows(d, false, rb);

@@ -1,5 +1,6 @@
-// WY prepare for bf16 io ("Reuse P as beta tiles in gated deltanet fused
-// prepare": the gated A, its inverse, w and u per chunk).
+// WY prepare for bf16 io, and fp16 io at K = V = 128, C = 64 ("Reuse P as beta
+// tiles in gated deltanet fused prepare": the gated A, its inverse, w and u per
+// chunk).
 //
 // One CTA of 128 threads per 64-token tile of one (batch, head): one chunk when
 // C = 64, two when C = 32 (kept apart by the block-diagonal structure).  Warp I
@@ -161,7 +162,10 @@ struct PackedIn {
 // read back with 16x256b loads in the mma.sync accumulator layout, so the gating, the solve and the
 // products that follow are shared with the mma.sync form.  An M = 64 accumulator keeps rows 16q .. 16q+15
 // in lanes 0 .. 15 of sub-partition q: warp q's own block row.
-template <int K, int V, int C, bool PER_K, bool WITH_P, bool EXTRA, bool PACKED, bool UMMA>
+// F16 (the same shape, with P): q, k, v, beta and the outputs w, u, P are fp16 instead of bf16, so the
+// tcgen05 scan that reads them multiplies operands of one type; the solve's hi/lo split stays bf16.
+// beta arrives through the bf16 pointer either way (two bytes per element).
+template <int K, int V, int C, bool PER_K, bool WITH_P, bool EXTRA, bool PACKED, bool UMMA, bool F16>
 __global__ void __launch_bounds__(128, 3)
 prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
                    const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap mu,
@@ -170,6 +174,8 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
                    bf16* __restrict__ tinv, int T, int H, int G, PackedIn pin, unsigned int* err) {
     static_assert(!PACKED || (C == kTile && !PER_K), "packed inputs: whole 64-token chunks, scalar gate");
     static_assert(!UMMA || (K == 128 && V == 128 && C == 64 && !PER_K && WITH_P && !PACKED), "tcgen05 S, P: one shape");
+    static_assert(!F16 || (K == 128 && V == 128 && C == 64 && !PER_K && WITH_P && !PACKED),
+                  "fp16 io: the shape of the tcgen05 scan");
     using L = PrepLayout<K, V, C, PER_K, WITH_P>;
     constexpr int GW = L::GW;
     extern __shared__ unsigned char smem_raw[];
@@ -224,7 +230,7 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
     // beta and (scalar gate) g of the tile, loaded first: their latency runs under the barrier setup and
     // the TMA issue (rows past T read as zero)
     float b_pre = 0.f, g_pre0 = 0.f, g_pre1 = 0.f;
-    if (tid < kTile && tid < nvalid) b_pre = __bfloat162float(beta[row_in(tid)]);
+    if (tid < kTile && tid < nvalid) b_pre = bw::load_io<F16>(beta + row_in(tid));
     if (!PER_K && warp == 0) {
         if (lane < nvalid) g_pre0 = g[row_in(lane)];
         if (32 + lane < nvalid) g_pre1 = g[row_in(32 + lane)];
@@ -269,7 +275,7 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
         __syncwarp();
         bw::tc_fence_after();
         const uint32_t t = tslot;
-        constexpr uint32_t idS = bw::idesc_bf16(64, 64, 0, 0);
+        constexpr uint32_t idS = bw::idesc_io(64, 64, 0, 0, F16);
         bw::mbar_wait(&bar_k, 0, err, kDeviceErrTimeout);   // a timeout is recorded; the stores follow thread 0's waits
         __syncwarp();
         bw::tc_fence_after();
@@ -398,8 +404,8 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
                 if (!PER_K && jp / 2 > warp) continue;
                 uint32_t bfr[4];
                 wm::ldsm_x4(b_t + tile_off(8 * jp + 8 * (mi >> 1) + mr, 16 * kk + 8 * (mi & 1)), bfr);
-                wm::mma16816(S[jp], a, bfr[0], bfr[1]);
-                wm::mma16816(S[jp + 1], a, bfr[2], bfr[3]);
+                wm::mma16816_io<F16>(S[jp], a, bfr[0], bfr[1]);
+                wm::mma16816_io<F16>(S[jp + 1], a, bfr[2], bfr[3]);
             }
         }
         }
@@ -448,8 +454,8 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
                 if (jp / 2 > warp) continue;
                 uint32_t bfr[4];
                 wm::ldsm_x4(s_base + L::kK + tile_off(8 * jp + 8 * (mi >> 1) + mr, 16 * kk + 8 * (mi & 1)), bfr);
-                wm::mma16816(Pq[jp], aq, bfr[0], bfr[1]);
-                wm::mma16816(Pq[jp + 1], aq, bfr[2], bfr[3]);
+                wm::mma16816_io<F16>(Pq[jp], aq, bfr[0], bfr[1]);
+                wm::mma16816_io<F16>(Pq[jp + 1], aq, bfr[2], bfr[3]);
             }
         }
         }
@@ -464,8 +470,8 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
                 pv[hh][2] = j0 <= i1 ? Pq[jn][2] * __expf(sG[i1] - sG[j0]) : 0.f;
                 pv[hh][3] = j0 + 1 <= i1 ? Pq[jn][3] * __expf(sG[i1] - sG[j0 + 1]) : 0.f;
             }
-            const uint32_t r[4] = {wm::pack2(pv[0][0], pv[0][1]), wm::pack2(pv[0][2], pv[0][3]),
-                                   wm::pack2(pv[1][0], pv[1][1]), wm::pack2(pv[1][2], pv[1][3])};
+            const uint32_t r[4] = {wm::pack2_io<F16>(pv[0][0], pv[0][1]), wm::pack2_io<F16>(pv[0][2], pv[0][3]),
+                                   wm::pack2_io<F16>(pv[1][0], pv[1][1]), wm::pack2_io<F16>(pv[1][2], pv[1][3])};
             __syncwarp();
             asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(
                              s_base + L::kQ + tile_off(warp * 16 + 8 * (mi & 1) + mr, 8 * jp + 8 * (mi >> 1))),
@@ -639,19 +645,19 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
     for (int J = 0; J < 4; ++J) {
         const int j0 = 16 * J + 2 * q4, j1 = j0 + 8;
         const float2 ba = *reinterpret_cast<const float2*>(sB + j0), bb = *reinterpret_cast<const float2*>(sB + j1);
-        tu[J][0] = wm::pack2(Xr[J][0][0] * ba.x, Xr[J][0][1] * ba.y);
-        tu[J][1] = wm::pack2(Xr[J][0][2] * ba.x, Xr[J][0][3] * ba.y);
-        tu[J][2] = wm::pack2(Xr[J][1][0] * bb.x, Xr[J][1][1] * bb.y);
-        tu[J][3] = wm::pack2(Xr[J][1][2] * bb.x, Xr[J][1][3] * bb.y);
+        tu[J][0] = wm::pack2_io<F16>(Xr[J][0][0] * ba.x, Xr[J][0][1] * ba.y);
+        tu[J][1] = wm::pack2_io<F16>(Xr[J][0][2] * ba.x, Xr[J][0][3] * ba.y);
+        tu[J][2] = wm::pack2_io<F16>(Xr[J][1][0] * bb.x, Xr[J][1][1] * bb.y);
+        tu[J][3] = wm::pack2_io<F16>(Xr[J][1][2] * bb.x, Xr[J][1][3] * bb.y);
         if constexpr (PER_K) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) tw[J][e] = tu[J][e];
         } else {
             const float2 ea = *reinterpret_cast<const float2*>(sE + j0), eb = *reinterpret_cast<const float2*>(sE + j1);
-            tw[J][0] = wm::pack2(Xr[J][0][0] * ba.x * ea.x, Xr[J][0][1] * ba.y * ea.y);
-            tw[J][1] = wm::pack2(Xr[J][0][2] * ba.x * ea.x, Xr[J][0][3] * ba.y * ea.y);
-            tw[J][2] = wm::pack2(Xr[J][1][0] * bb.x * eb.x, Xr[J][1][1] * bb.y * eb.y);
-            tw[J][3] = wm::pack2(Xr[J][1][2] * bb.x * eb.x, Xr[J][1][3] * bb.y * eb.y);
+            tw[J][0] = wm::pack2_io<F16>(Xr[J][0][0] * ba.x * ea.x, Xr[J][0][1] * ba.y * ea.y);
+            tw[J][1] = wm::pack2_io<F16>(Xr[J][0][2] * ba.x * ea.x, Xr[J][0][3] * ba.y * ea.y);
+            tw[J][2] = wm::pack2_io<F16>(Xr[J][1][0] * bb.x * eb.x, Xr[J][1][1] * bb.y * eb.y);
+            tw[J][3] = wm::pack2_io<F16>(Xr[J][1][2] * bb.x * eb.x, Xr[J][1][3] * bb.y * eb.y);
         }
     }
     // The products out[64 x D] = T [64 x 64] * B [64 x D], B = k (or k exp(G)) or v read token-major by
@@ -698,8 +704,8 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
                 wm::ldsm_x4(a_t + tile_off(16 * I + 8 * (mi & 1) + mr, 16 * kk + 8 * (mi >> 1)), a);
 #pragma unroll
                 for (int jp = 0; jp < NW / 2; ++jp) {
-                    wm::mma16816(acc[I][2 * jp], a, bfr[jp][0], bfr[jp][1]);
-                    wm::mma16816(acc[I][2 * jp + 1], a, bfr[jp][2], bfr[jp][3]);
+                    wm::mma16816_io<F16>(acc[I][2 * jp], a, bfr[jp][0], bfr[jp][1]);
+                    wm::mma16816_io<F16>(acc[I][2 * jp + 1], a, bfr[jp][2], bfr[jp][3]);
                 }
             }
         }
@@ -712,10 +718,10 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
         for (int I = 0; I < 4; ++I)
 #pragma unroll
             for (int jp = 0; jp < NW / 2; ++jp) {
-                const uint32_t r[4] = {wm::pack2(acc[I][2 * jp][0], acc[I][2 * jp][1]),
-                                       wm::pack2(acc[I][2 * jp][2], acc[I][2 * jp][3]),
-                                       wm::pack2(acc[I][2 * jp + 1][0], acc[I][2 * jp + 1][1]),
-                                       wm::pack2(acc[I][2 * jp + 1][2], acc[I][2 * jp + 1][3])};
+                const uint32_t r[4] = {wm::pack2_io<F16>(acc[I][2 * jp][0], acc[I][2 * jp][1]),
+                                       wm::pack2_io<F16>(acc[I][2 * jp][2], acc[I][2 * jp][3]),
+                                       wm::pack2_io<F16>(acc[I][2 * jp + 1][0], acc[I][2 * jp + 1][1]),
+                                       wm::pack2_io<F16>(acc[I][2 * jp + 1][2], acc[I][2 * jp + 1][3])};
                 asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(
                                  st + tile_off(16 * I + 8 * (mi & 1) + mr, n0 + 16 * jp + 8 * (mi >> 1))),
                              "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
@@ -764,7 +770,8 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
 
 // pdl: launched as the programmatic dependent of the kernel before it in the stream (it may start as
 // soon as every CTA of that kernel has signalled, and reads nothing that kernel writes).
-template <int K, int V, int C, bool PER_K, bool WITH_P, bool EXTRA, bool PACKED = false, bool UMMA = false>
+template <int K, int V, int C, bool PER_K, bool WITH_P, bool EXTRA, bool PACKED = false, bool UMMA = false,
+          bool F16 = false>
 cudaError_t launch_prepare_v(const Dims& d, const void* q, const void* k, const void* v, const float* g,
                              const void* beta, void* w, void* u, float* g_cum, void* P, void* tinv, cudaStream_t s,
                              unsigned int* err, PackedIn pin = PackedIn{}, bool pdl = false) {
@@ -786,7 +793,7 @@ cudaError_t launch_prepare_v(const Dims& d, const void* q, const void* k, const 
         if (!make_tmap_tokens(&mq, q, bi, ti, d.Hk, K, kTile) || !make_tmap_bf16_4d(&mp, P, dims, st, box))
             return cudaErrorInvalidValue;
     }
-    auto kern = prepare_mma_kernel<K, V, C, PER_K, WITH_P, EXTRA, PACKED, UMMA>;
+    auto kern = prepare_mma_kernel<K, V, C, PER_K, WITH_P, EXTRA, PACKED, UMMA, F16>;
     const size_t smem = L::bytes + 1024;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -815,10 +822,25 @@ cudaError_t launch_prepare(const Dims& d, const void* q, const void* k, const vo
                            const void* beta, void* w, void* u, float* g_cum, void* P, void* tinv, cudaStream_t s,
                            unsigned int* err, bool pdl, bool tc_scores) {
     if constexpr (K == 128 && V == 128 && C == 64 && !PER_K && WITH_P) {
+        if (d.f16) {   // fp16 io: the tcgen05 scan's shape, no inverse
+            if (tinv) return cudaErrorInvalidValue;
+            if (d.G != 1)
+                return launch_prepare_v<K, V, C, PER_K, WITH_P, true, false, false, true>(d, q, k, v, g, beta, w, u,
+                                                                                          g_cum, P, tinv, s, err,
+                                                                                          PackedIn{}, pdl);
+            if (tc_scores)
+                return launch_prepare_v<K, V, C, PER_K, WITH_P, false, false, true, true>(d, q, k, v, g, beta, w, u,
+                                                                                          g_cum, P, tinv, s, err,
+                                                                                          PackedIn{}, pdl);
+            return launch_prepare_v<K, V, C, PER_K, WITH_P, false, false, false, true>(d, q, k, v, g, beta, w, u,
+                                                                                       g_cum, P, tinv, s, err,
+                                                                                       PackedIn{}, pdl);
+        }
         if (tc_scores && d.G == 1 && !tinv)
             return launch_prepare_v<K, V, C, PER_K, WITH_P, false, false, true>(d, q, k, v, g, beta, w, u, g_cum, P,
                                                                                 tinv, s, err, PackedIn{}, pdl);
     }
+    if (d.f16) return cudaErrorInvalidValue;
     if (d.G != 1 || tinv)
         return launch_prepare_v<K, V, C, PER_K, WITH_P, true>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err,
                                                               PackedIn{}, pdl);
@@ -874,7 +896,7 @@ cudaError_t mma_prepare_packed(const Dims& d, const void* q, const void* k, cons
 cudaError_t mma_prepare(const Dims& d, const void* k, const void* v, const float* g, const void* beta, void* w,
                         void* u, float* g_cum, cudaStream_t s, unsigned int* err, const void* q, void* P,
                         void* tinv, bool pdl, bool tc_scores) {
-    if (!d.bf16) return cudaErrorInvalidValue;
+    if (!d.bf16 && !d.f16) return cudaErrorInvalidValue;   // fp16: one shape, checked where it is launched
     if (P && (d.per_k || d.C != 64 || !q)) return cudaErrorInvalidValue;
     const bool tc = tc_scores;
     if (d.K == 64 && d.V == 64) return pick_chunk<64, 64>(d, q, k, v, g, beta, w, u, g_cum, P, tinv, s, err, pdl, tc);

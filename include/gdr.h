@@ -85,7 +85,9 @@ typedef enum gdr_status {
     GDR_ERR_ARG = 9              /* another invalid argument (e.g. a NaN scale) */
 } gdr_status;
 
-/* fp16 io runs the CUDA-core kernels (variant AUTO or SIMT); the tensor-core kernels take bf16. */
+/* fp16 io runs FUSED_TC where it is built for fp16 (scalar gate, K = V = 128, chunk 64, no segmented
+ * scan: q, k, v, beta, o and every intermediate fp16) and the CUDA-core kernels otherwise (variant
+ * AUTO or SIMT); the other tensor-core kernels take bf16. */
 typedef enum gdr_dtype { GDR_F32 = 0, GDR_BF16 = 1, GDR_F16 = 2 } gdr_dtype;
 
 typedef enum gdr_gate {
@@ -100,7 +102,8 @@ typedef enum gdr_gate {
  * chunks and no segmented scan (one long sequence, which FUSED_TC runs in pieces
  * whose scans overlap the next piece's prepare), else FUSED; with a per-key-dim
  * gate FUSED_TC when K = V = 128, C = 64 and no segmented scan applies; TENSOR for
- * other bf16 problems; SIMT for fp32 io.  The single-stage entry points run their
+ * other bf16 problems; SIMT for fp32 io; for fp16 io FUSED_TC where it takes fp16
+ * (see gdr_dtype), else SIMT.  The single-stage entry points run their
  * tensor-core kernel for AUTO, TENSOR, FUSED and FUSED_TC on bf16 io. */
 typedef enum gdr_variant {
     GDR_VARIANT_AUTO = 0,
@@ -110,8 +113,9 @@ typedef enum gdr_variant {
                                  (batch, head, 32 value columns) (bf16 io, scalar gate) */
     GDR_VARIANT_FUSED_TC = 4  /* the same with scan and output on the tcgen05 tensor cores, one CTA per
                                  (batch, head) (bf16 io, K = V = 128, chunk 64; a per-key-dim gate
-                                 adds the gdr_gated_operands kernel); packed sequences (gdr_varlen_*)
-                                 run FUSED for it, or TENSOR with a per-key-dim gate */
+                                 adds the gdr_gated_operands kernel; fp16 io with a scalar gate);
+                                 packed sequences (gdr_varlen_*) run FUSED for it, TENSOR with a
+                                 per-key-dim gate, SIMT for fp16 */
 } gdr_variant;
 
 typedef struct gdr_problem {
@@ -123,7 +127,8 @@ typedef struct gdr_problem {
     int32_t variant;    /* gdr_variant */
     int64_t HV;         /* value heads, a multiple of H; 0 means HV = H (see below) */
     int32_t segments;   /* gdr_forward on the tensor cores: scan each sequence as this many segments
-                           in parallel (see gdr_scan_transfer); 0 = chosen from the problem, 1 = off */
+                           in parallel (see gdr_scan_transfer); 0 = chosen from the problem, 1 = off;
+                           fp16 io scans whole (0 means 1; > 1 is GDR_ERR_UNSUPPORTED) */
 } gdr_problem;
 
 /*

@@ -208,11 +208,14 @@ def test_overlapped_fused_tc_workspace(lib):
 
 
 def test_fused_tc_variant_takes_its_sizes_only(lib):
-    # K = V = 128, C = 64, bf16, either gate; anything else is GDR_ERR_UNSUPPORTED before a launch
+    # K = V = 128, C = 64: bf16 with either gate, fp16 with a scalar gate; anything else is
+    # GDR_ERR_UNSUPPORTED before a launch
     for (K, V, C, dt, per_k, code) in [(128, 128, 64, 1, False, None), (64, 64, 64, 1, False, 8),
                                        (128, 64, 64, 1, False, 8), (128, 128, 32, 1, False, 8),
                                        (128, 128, 64, 1, True, None), (128, 128, 32, 1, True, 8),
-                                       (128, 128, 64, 0, False, 8)]:
+                                       (128, 128, 64, 0, False, 8), (128, 128, 64, 2, False, None),
+                                       (128, 128, 64, 2, True, 8), (64, 64, 64, 2, False, 8),
+                                       (128, 128, 32, 2, False, 8)]:
         p = gdr.make_problem(1, 256, 2, K, V, C, dt, per_k, variant="fused_tc")
         if code is None:
             assert lib.gdr_forward_workspace_bytes(ctypes.byref(p)) > 0
@@ -222,6 +225,26 @@ def test_fused_tc_variant_takes_its_sizes_only(lib):
     p = gdr.make_problem(1, 256, 2, 128, 128, 64, 1, False)
     p.variant = 5
     assert _fwd(lib, p) == 9
+
+
+def test_fp16_fused_tc_rules(lib):
+    # fp16 on the tcgen05 fused path: no segmented scan; AUTO takes it at K = V = 128, C = 64 with a
+    # scalar gate, grouped value heads included (the same workspace as the variant asked by name), and
+    # otherwise the CUDA-core path
+    p = gdr.make_problem(1, 256, 2, 128, 128, 64, 2, False, variant="fused_tc", HV=4)
+    assert lib.gdr_forward_workspace_bytes(ctypes.byref(p)) == lib.gdr_forward_workspace_bytes(
+        ctypes.byref(gdr.make_problem(1, 256, 2, 128, 128, 64, 2, False, HV=4))) > 0
+    p = gdr.make_problem(1, 4096, 2, 128, 128, 64, 2, False, variant="fused_tc", segments=4)
+    assert lib.gdr_forward_workspace_bytes(ctypes.byref(p)) == 0 and _fwd(lib, p) == 8
+    assert lib.gdr_forward_segments(ctypes.byref(gdr.make_problem(1, 4096, 1, 128, 128, 64, 2, False))) == 1
+    for B, T in [(2, 320), (1, 64 * 200)]:
+        named = gdr.make_problem(B, T, 2, 128, 128, 64, 2, False, variant="fused_tc")
+        auto = gdr.make_problem(B, T, 2, 128, 128, 64, 2, False)
+        assert lib.gdr_forward_workspace_bytes(ctypes.byref(auto)) == lib.gdr_forward_workspace_bytes(
+            ctypes.byref(named)) > 0
+    auto = gdr.make_problem(2, 320, 2, 128, 128, 64, 2, True)
+    simt = gdr.make_problem(2, 320, 2, 128, 128, 64, 2, True, variant="simt")
+    assert lib.gdr_forward_workspace_bytes(ctypes.byref(auto)) == lib.gdr_forward_workspace_bytes(ctypes.byref(simt))
 
 
 def test_segment_choice_and_workspace(lib):

@@ -17,9 +17,14 @@ pytestmark = pytest.mark.gpu
 
 # every variant gdr_forward offers, with the io dtypes it takes
 FORWARD_VARIANTS = {"simt": (torch.float32, torch.bfloat16), "tensor": (torch.bfloat16,),
-                    "fused": (torch.bfloat16,), "fused_tc": (torch.bfloat16,)}
+                    "fused": (torch.bfloat16,), "fused_tc": (torch.bfloat16, torch.float16)}
 # the warp-level fused path takes a scalar gate only
 GATES = {"simt": (False, True), "tensor": (False, True), "fused": (False,), "fused_tc": (False, True)}
+
+
+def gates(variant, dtype):
+    # fp16 on the tcgen05 fused path: scalar gate only
+    return (False,) if dtype == torch.float16 else GATES[variant]
 SHAPES = [(2, 256, 3, 64, 64, 64), (1, 192, 2, 128, 128, 64), (2, 128, 3, 64, 128, 32),
           (1, 160, 1, 128, 64, 32), (1, 64, 2, 128, 128, 64), (1, 32, 1, 64, 64, 32),
           # a last, partial chunk: 36 of 64 tokens; 13 of 32 (the second half of a 64-token
@@ -34,6 +39,8 @@ def small_cases():
         if per_k not in GATES[variant] or not variant_supports(variant, shape[3], shape[4], shape[5], per_k):
             continue
         for dt in dts:
+            if per_k not in gates(variant, dt):
+                continue
             yield pytest.param(shape, per_k, variant, dt,
                                id=f"{'x'.join(map(str, shape))}-{'kda' if per_k else 'gdn'}-{variant}-{io_name(dt)}")
 
@@ -71,7 +78,7 @@ def test_forward_workload_full_size(wl):
 
 
 @pytest.mark.parametrize("variant,dtype,per_k", [(v, d, pk) for v, ds in FORWARD_VARIANTS.items() for d in ds
-                                                  for pk in GATES[v]])
+                                                  for pk in gates(v, d)])
 def test_deterministic_and_exact_scaling(variant, dtype, per_k):
     """Two runs are bitwise equal; scaling (v, h0) by 2 scales (o, h_final) by exactly 2."""
     x = make_inputs(2, 256, 2, 128, 128, per_k_gate=per_k, io_dtype=dtype, with_h0=True, seed=6)
@@ -80,7 +87,12 @@ def test_deterministic_and_exact_scaling(variant, dtype, per_k):
     assert torch.equal(o1, o2) and torch.equal(h1, h2)
     x2 = GdrInputs(q=x.q, k=x.k, v=x.v * 2, g=x.g, beta=x.beta, h0=x.h0 * 2)
     o3, h3, _ = gpu_forward(x2, 64, variant)
-    assert torch.equal(o3, o1 * 2) and torch.equal(h3, h1 * 2)
+    if dtype == torch.float16:
+        # fp16 has subnormals below 2^-14: stored intermediates there (v', w, P, o) round on a fixed grid
+        # of 2^-24, not relative to the value, so doubling is exact only up to that grid's errors
+        assert (o3.float() - 2 * o1.float()).abs().max() <= 1e-4 and (h3 - 2 * h1).abs().max() <= 1e-4
+    else:
+        assert torch.equal(o3, o1 * 2) and torch.equal(h3, h1 * 2)
 
 
 @pytest.mark.parametrize("variant,dtype", [(v, d) for v, ds in FORWARD_VARIANTS.items() for d in ds])
@@ -136,7 +148,7 @@ def _padded(t, T, Tb):
 
 @pytest.mark.parametrize("T,C", [(100, 64), (77, 32), (1, 64), (33, 32)])
 @pytest.mark.parametrize("variant,dtype,per_k", [(v, d, pk) for v, ds in FORWARD_VARIANTS.items() for d in ds
-                                                  for pk in GATES[v]])
+                                                  for pk in gates(v, d)])
 def test_partial_chunk_touches_nothing_past_T(T, C, variant, dtype, per_k):
     """Inputs and output sit in buffers with room for whole chunks, NaN past T: a read
     past T would turn the results NaN and a write past T would overwrite the NaN tail."""
@@ -163,7 +175,7 @@ def test_partial_chunk_touches_nothing_past_T(T, C, variant, dtype, per_k):
 @pytest.mark.parametrize("kind", ["beta_zero", "no_decay", "strong_decay", "single_chunk", "single_token",
                                   "ragged_strong_decay"])
 @pytest.mark.parametrize("variant,dtype,per_k", [(v, d, pk) for v, ds in FORWARD_VARIANTS.items() for d in ds
-                                                  for pk in GATES[v]])
+                                                  for pk in gates(v, d)])
 def test_edge_cases(kind, per_k, variant, dtype):
     # the tcgen05 fused form takes K = V = 128 and 64-token chunks only
     D, C = (128, 64) if variant == "fused_tc" else (64, 32)
@@ -326,7 +338,7 @@ GROUPED = [(2, 128, 2, 2, 64, 64, 64), (1, 100, 1, 4, 128, 128, 64), (1, 96, 2, 
 
 @pytest.mark.parametrize("shape", GROUPED, ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("variant,dtype,per_k", [(v, d, pk) for v, ds in FORWARD_VARIANTS.items() for d in ds
-                                                  for pk in GATES[v]])
+                                                  for pk in gates(v, d)])
 def test_grouped_value_heads_forward(shape, variant, dtype, per_k):
     # H q/k heads shared by H * G value heads: every value head against the oracle
     B, T, H, G, K, V, C = shape
@@ -344,20 +356,63 @@ def test_grouped_value_heads_forward(shape, variant, dtype, per_k):
 @pytest.mark.parametrize("per_k", [False, True])
 @pytest.mark.parametrize("variant", ["auto", "simt"])
 def test_fp16_io_forward(shape, per_k, variant):
-    # fp16 runs the CUDA-core kernels (the AUTO choice for it)
+    # AUTO runs fp16 on the tcgen05 fused path where it takes it (scalar gate, K = V = 128, C = 64), on
+    # the CUDA-core kernels otherwise
     B, T, H, K, V, C = shape
     x = make_inputs(B, T, H, K, V, per_k_gate=per_k, io_dtype=torch.float16, with_h0=True, seed=90)
     o, hf, ran = gpu_forward(x, C, variant)
-    assert ran == "simt" and o.dtype == torch.float16
+    tc = variant == "auto" and not per_k and K == V == 128 and C == 64
+    assert ran == ("fused_tc" if tc else "simt") and o.dtype == torch.float16
     check_forward(x, o, hf, all_pairs(B, H), C, 1.0 / np.sqrt(K), "f16")
+
+
+@pytest.mark.parametrize("T,H", [(64 * 131, 1), (64 * 128 + 30, 2)])
+def test_fp16_io_overlapped_single_sequence(T, H):
+    # one long fp16 sequence: the overlapped pieces, their prepares with S and P on tcgen05, against the
+    # token oracle on every head; the same tokens as two batch rows (no pieces) agree with it
+    x = make_inputs(1, T, H, 128, 128, io_dtype=torch.float16, with_h0=True, seed=92)
+    o, hf, ran = gpu_forward(x, 64, "auto")
+    assert ran == "fused_tc" and o.dtype == torch.float16
+    check_forward(x, o, hf, all_pairs(1, H), 64, 1.0 / np.sqrt(128), "f16")
+    x2 = GdrInputs(q=x.q.repeat(2, 1, 1, 1), k=x.k.repeat(2, 1, 1, 1), v=x.v.repeat(2, 1, 1, 1),
+                   g=x.g.repeat(2, 1, 1), beta=x.beta.repeat(2, 1, 1), h0=x.h0.repeat(2, 1, 1, 1))
+    o2, hf2, _ = gpu_forward(x2, 64, "fused_tc")
+    assert max_abs(o, o2[:1].double().cpu().numpy()) <= 2e-3
+    assert rel_frob(hf, hf2[:1].double().cpu().numpy()) <= 2e-3
+
+
+def test_fp16_io_tensor_core_forward_is_closer_to_the_oracle_than_bf16():
+    # the same draw rounded to fp16 and to bf16: the fp16 run keeps three more mantissa bits in every
+    # stored operand (w, u, P, h, v'), so its error against the oracle of its own inputs is smaller
+    errs = {}
+    for dt in (torch.float16, torch.bfloat16):
+        x = make_inputs(2, 320, 2, 128, 128, io_dtype=dt, with_h0=True, seed=93)
+        o, hf, ran = gpu_forward(x, 64, "fused_tc")
+        assert ran == "fused_tc"
+        errs[dt] = check_forward(x, o, hf, all_pairs(2, 2), 64, 1.0 / np.sqrt(128), io_name(dt))
+    assert errs[torch.float16][0] < errs[torch.bfloat16][0] and errs[torch.float16][1] < errs[torch.bfloat16][1]
 
 
 @pytest.mark.parametrize("variant", ["tensor", "fused", "fused_tc"])
 def test_fp16_io_refused_by_the_tensor_core_variants(variant):
+    # K = V = 64 everywhere; the staged and warp-level tensor-core variants take no fp16 at all
     x = make_inputs(1, 64, 1, 64, 64, io_dtype=torch.float16, seed=91)
     with pytest.raises(gdr.GdrError) as e:
         gpu_forward(x, 64, variant)
     assert e.value.status == 8
+
+
+@pytest.mark.parametrize("case", ["per_key_gate", "segments"])
+def test_fp16_io_fused_tc_refuses_what_it_does_not_build(case):
+    if case == "per_key_gate":
+        x, seg = make_inputs(1, 128, 1, 128, 128, per_k_gate=True, io_dtype=torch.float16, seed=94), 0
+    else:
+        x, seg = make_inputs(1, 4096, 1, 128, 128, io_dtype=torch.float16, seed=94), 4
+    with pytest.raises(gdr.GdrError) as e:
+        gpu_forward(x, 64, "fused_tc", segments=seg)
+    assert e.value.status == 8
+    o, hf, ran = gpu_forward(x, 64, "auto", segments=1 if case == "segments" else 0)   # AUTO still runs it
+    assert ran == ("fused_tc" if case == "segments" else "simt")
 
 
 @pytest.mark.parametrize("shape", [(2, 256, 2, 128, 128, 64), (1, 200, 3, 64, 64, 32)],

@@ -102,16 +102,7 @@ tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         bw::mbar_init(&bar_mma, 1);
         bw::fence_mbar_init();
         *sFlag = 0;
-    }
-    if (warp == 0) {
-        bw::tmem_alloc(&tslot, L::tmem_cols);
-        bw::tmem_relinquish();
-    }
-    __syncthreads();
-    bw::tc_fence_after();
-    const uint32_t tmem = tslot;
-
-    if (tid == 0) {
+        // the tiles first: their latency runs under the tensor-memory allocation and the gate loads
         const int nch = OPS ? 0 : (nvalid + C - 1) / C;   // checkpoints that exist for this tile
         bw::mbar_arrive_expect_tx(&bar_tma, 2 * K * 128 + (OPS ? 0 : V * 128) + nch * K * V * 2);
 #pragma unroll
@@ -130,19 +121,10 @@ tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
                 bw::tma_load_4d(sm + L::Hc + ch * K * V * 2 + a * K * 128, &mh, &bar_tma, a * 64, 0, h, b * NT + c);
         }
     }
-    if constexpr (!PER_K)
-        for (int i = tid; i < kTile; i += 128) sG[i] = i < nvalid ? g_cum[row(i)] : 0.f;
-    if (L::NCH > 1 && nvalid <= C) {
-        // a half tile: the second chunk's checkpoint is absent; give its rows a zero state
-        for (int i = tid; i < K * V / 8; i += 128)
-            *reinterpret_cast<uint4*>(sm + L::Hc + K * V * 2 + i * 16) = make_uint4(0, 0, 0, 0);
-    }
-    __syncthreads();
-    bool ok = bw::mbar_wait(&bar_tma, 0, err, kDeviceErrTimeout);
-
+    // per-key-dim gate: this thread's rows of G, the middle row of each chunk and (OPS) the chunk's last
+    // row, all in flight together with the tiles
+    float4 ga[PER_K ? NIT : 1][2], gref[L::NCH][2], glast[2];
     if constexpr (PER_K) {
-        float4 ga[NIT][2], gref[L::NCH][2];   // this thread's rows of G; the middle row of each chunk
-        float4 glast[2];                      // OPS: the chunk's last row of G
         load_g_rows(ga);
         if constexpr (OPS) {
             const float4* src = reinterpret_cast<const float4*>(g_cum + row(nvalid - 1) * K + (tid % (K / 8)) * 8);
@@ -156,6 +138,24 @@ tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
             gref[ch][0] = src[0];
             gref[ch][1] = src[1];
         }
+    }
+    if (warp == 0) {
+        bw::tmem_alloc(&tslot, L::tmem_cols);
+        bw::tmem_relinquish();
+    }
+    if constexpr (!PER_K)
+        for (int i = tid; i < kTile; i += 128) sG[i] = i < nvalid ? g_cum[row(i)] : 0.f;
+    if (L::NCH > 1 && nvalid <= C) {
+        // a half tile: the second chunk's checkpoint is absent; give its rows a zero state
+        for (int i = tid; i < K * V / 8; i += 128)
+            *reinterpret_cast<uint4*>(sm + L::Hc + K * V * 2 + i * 16) = make_uint4(0, 0, 0, 0);
+    }
+    __syncthreads();
+    bw::tc_fence_after();
+    const uint32_t tmem = tslot;
+    bool ok = bw::mbar_wait(&bar_tma, 0, err, kDeviceErrTimeout);
+
+    if constexpr (PER_K) {
         // OPS: exp(G_ref) and exp(G_last - G_ref) of this thread's eight key columns (the same at every step),
         // so that qg = (q exp(G - G_ref)) exp(G_ref) and kg = (k exp(G_ref - G)) exp(G_last - G_ref) reuse the
         // gated copies' exponentials where |G - G_ref| <= kExpSafe

@@ -240,6 +240,18 @@ def test_host_forward_pageable_and_grouped_heads(pinned):
     assert torch.equal(o_p, o_1.cpu())
 
 
+def test_host_forward_fp16_on_the_tcgen05_path():
+    # fp16 host tensors through the pipelined host forward: each piece runs the tcgen05 fused path in fp16,
+    # and the pieces carry the state exactly as one device call does
+    x = make_inputs(1, 64 * 40 + 17, 3, 128, 128, io_dtype=torch.float16, with_h0=True, seed=95)
+    hx = [t.pin_memory() for t in (x.q, x.k, x.v, x.g, x.beta, x.h0)]
+    o, hf = gdr.forward(*hx, chunk=64, pieces=4)
+    assert o.dtype == torch.float16 and gdr.gdr_last_variant() == "fused_tc"
+    o_1, hf_1 = gdr.forward(*(t.cuda() for t in hx), chunk=64)
+    assert torch.equal(o, o_1.cpu()) and torch.equal(hf, hf_1.cpu())
+    check_forward(x, o, hf, all_pairs(1, 3), 64, 1.0 / np.sqrt(128), "f16")
+
+
 def test_host_forward_calls_queue_behind_each_other():
     # two calls on one stream and one scratch, no synchronisation between them: the second call's
     # uploads wait for the first call's work on the stream

@@ -23,6 +23,7 @@ namespace gdr {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kMaxChunk = 64;   // C is 32 or 64
 
 __device__ __forceinline__ float ld(const float* p, int64_t i) { return p[i]; }
 __device__ __forceinline__ float ld(const __nv_bfloat16* p, int64_t i) { return __bfloat162float(p[i]); }
@@ -40,7 +41,7 @@ __device__ __forceinline__ void st(__half* p, int64_t i, float x) { p[i] = __flo
 //   Xs [C][C+1]        (I + A)^{-1}
 //   ys [C][max(K,V)+1] k*beta*exp(G), then reused for v*beta (its lifetimes do not overlap)
 template <typename IO, bool PER_K>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 1)   // the column solve keeps a 64-entry column in registers
 simt_prepare_kernel(Dims d, const IO* __restrict__ k, const IO* __restrict__ v, const float* __restrict__ g,
                     const IO* __restrict__ beta, IO* __restrict__ w, IO* __restrict__ u,
                     float* __restrict__ g_cum) {
@@ -62,9 +63,9 @@ simt_prepare_kernel(Dims d, const IO* __restrict__ k, const IO* __restrict__ v, 
     auto krow = [&](int t) { return (tok0 + t) * d.Hk + h / d.G; };   // q, k: q/k head h / G
 
     // tokens past T (a last, partial chunk) read as g = 0, beta = 0, k = v = 0
-    for (int i = tid; i < C * GW; i += kThreads) Gs[i] = i / GW < nv ? g[row(i / GW) * GW + i % GW] : 0.f;
+        for (int i = tid; i < C * GW; i += kThreads) Gs[i] = i / GW < nv ? g[row(i / GW) * GW + i % GW] : 0.f;
     for (int i = tid; i < C; i += kThreads) bs[i] = i < nv ? ld(beta, row(i)) : 0.f;
-    for (int i = tid; i < C * K; i += kThreads) ks[(i / K) * KP + i % K] = i / K < nv ? ld(k, krow(i / K) * K + i % K) : 0.f;
+        for (int i = tid; i < C * K; i += kThreads) ks[(i / K) * KP + i % K] = i / K < nv ? ld(k, krow(i / K) * K + i % K) : 0.f;
     __syncthreads();
     // chunk-local inclusive cumsum, one thread per gate column
     for (int col = tid; col < GW; col += kThreads) {
@@ -76,34 +77,50 @@ simt_prepare_kernel(Dims d, const IO* __restrict__ k, const IO* __restrict__ v, 
         }
     }
     __syncthreads();
-    // A_ij = beta_i sum_d k_id k_jd exp(G_id - G_jd), i > j
-    for (int idx = tid; idx < C * C; idx += kThreads) {
-        const int i = idx / C, j = idx % C;
-        float a = 0.f;
-        if (i > j) {
-            float s = 0.f;
-            if (PER_K) {
-                for (int e = 0; e < K; ++e)
-                    s += ks[i * KP + e] * ks[j * KP + e] * expf(Gs[i * K + e] - Gs[j * K + e]);
-                a = bs[i] * s;
-            } else {
-                for (int e = 0; e < K; ++e) s += ks[i * KP + e] * ks[j * KP + e];
-                a = bs[i] * expf(Gs[i] - Gs[j]) * s;
+    // A_ij = beta_i sum_d k_id k_jd exp(G_id - G_jd), i > j: rows i0 .. i0+3 per thread share each load of
+    // k_j (four independent sums, each in the same order as one entry alone)
+    for (int idx = tid; idx < (C / 4) * C; idx += kThreads) {
+        const int i0 = (idx / C) * 4, j = idx % C;
+        float s[4] = {0.f, 0.f, 0.f, 0.f};
+        if (i0 + 3 > j) {
+            for (int e = 0; e < K; ++e) {
+                const float kj = ks[j * KP + e];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    if (PER_K) s[r] += ks[(i0 + r) * KP + e] * kj * expf(Gs[(i0 + r) * K + e] - Gs[j * K + e]);
+                    else s[r] += ks[(i0 + r) * KP + e] * kj;
+                }
             }
         }
-        As[i * CP + j] = a;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int i = i0 + r;
+            float a = 0.f;
+            if (i > j) a = PER_K ? bs[i] * s[r] : bs[i] * expf(Gs[i] - Gs[j]) * s[r];
+            As[i * CP + j] = a;
+        }
     }
     __syncthreads();
-    // X = (I + A)^{-1} by forward substitution, one thread per column col:
-    // X[col][col] = 1, X[i][col] = -sum_{j=col}^{i-1} A[i][j] X[j][col] for i > col.
-    for (int col = tid; col < C; col += kThreads) {
-        for (int i = 0; i < col; ++i) Xs[i * CP + col] = 0.f;
-        Xs[col * CP + col] = 1.f;
-        for (int i = col + 1; i < C; ++i) {
-            float s = 0.f;
-            for (int j = col; j < i; ++j) s += As[i * CP + j] * Xs[j * CP + col];
-            Xs[i * CP + col] = -s;
+    // X = (I + A)^{-1} by forward substitution, one thread per column col, the column in registers:
+    // X[col][col] = 1, X[i][col] = -sum_{j=col}^{i-1} A[i][j] X[j][col] for i > col.  The sum runs from
+    // j = 0 over the column's zeros above the diagonal, which adds exact zeros: the same sum.
+    static_assert(kMaxChunk <= kThreads, "one thread per column");
+    if (tid < C) {
+        const int col = tid;
+        float x[kMaxChunk];
+#pragma unroll
+        for (int i = 0; i < kMaxChunk; ++i) {
+            x[i] = 0.f;
+            if (i < C) {
+                float s = 0.f;
+#pragma unroll
+                for (int j = 0; j < i; ++j) s += As[i * CP + j] * x[j];
+                x[i] = i < col ? 0.f : (i == col ? 1.f : -s);
+            }
         }
+#pragma unroll
+        for (int i = 0; i < kMaxChunk; ++i)
+            if (i < C) Xs[i * CP + col] = x[i];
     }
     for (int i = tid; i < C * K; i += kThreads) {
         const int t = i / K, e = i % K;
@@ -111,25 +128,40 @@ simt_prepare_kernel(Dims d, const IO* __restrict__ k, const IO* __restrict__ v, 
         ys[t * YP + e] = ks[t * KP + e] * bs[t] * gate;
     }
     __syncthreads();
-    // w = X (k * beta * exp(G))
-    for (int idx = tid; idx < C * K; idx += kThreads) {
-        const int i = idx / K, e = idx % K;
-        float s = 0.f;
-        for (int j = 0; j <= i; ++j) s += Xs[i * CP + j] * ys[j * YP + e];
-        if (i < nv) st(w, row(i) * K + e, s);
+    // w = X (k * beta * exp(G)): rows i0 .. i0+3 per thread share each load of the right factor (each
+    // row's sum over j <= i in the same order as alone)
+    for (int idx = tid; idx < (C / 4) * K; idx += kThreads) {
+        const int i0 = (idx / K) * 4, e = idx % K;
+        float s[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int j = 0; j <= i0 + 3; ++j) {
+            const float yj = ys[j * YP + e];
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+                if (j <= i0 + r) s[r] += Xs[(i0 + r) * CP + j] * yj;
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+            if (i0 + r < nv) st(w, row(i0 + r) * K + e, s[r]);
     }
     __syncthreads();
-    for (int i = tid; i < C * V; i += kThreads) {
+        for (int i = tid; i < C * V; i += kThreads) {
         const int t = i / V, e = i % V;
         ys[t * YP + e] = t < nv ? ld(v, row(t) * V + e) * bs[t] : 0.f;
     }
     __syncthreads();
-    // u = X (v * beta)
-    for (int idx = tid; idx < C * V; idx += kThreads) {
-        const int i = idx / V, e = idx % V;
-        float s = 0.f;
-        for (int j = 0; j <= i; ++j) s += Xs[i * CP + j] * ys[j * YP + e];
-        if (i < nv) st(u, row(i) * V + e, s);
+    // u = X (v * beta), blocked as w
+    for (int idx = tid; idx < (C / 4) * V; idx += kThreads) {
+        const int i0 = (idx / V) * 4, e = idx % V;
+        float s[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int j = 0; j <= i0 + 3; ++j) {
+            const float yj = ys[j * YP + e];
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+                if (j <= i0 + r) s[r] += Xs[(i0 + r) * CP + j] * yj;
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+            if (i0 + r < nv) st(u, row(i0 + r) * V + e, s[r]);
     }
 }
 
@@ -159,7 +191,7 @@ simt_scan_kernel(Dims d, const IO* __restrict__ k, const IO* __restrict__ w, con
     const int tid = threadIdx.x;
     const int64_t state_off = ((int64_t)b * H + h) * K * V;
 
-    for (int i = tid; i < K * BV; i += kThreads) {
+        for (int i = tid; i < K * BV; i += kThreads) {
         const int e = i / BV, j = i % BV;
         hs[i] = h0 ? h0[state_off + (int64_t)e * V + v0 + j] : 0.f;
     }
@@ -175,31 +207,48 @@ simt_scan_kernel(Dims d, const IO* __restrict__ k, const IO* __restrict__ w, con
             for (int i = tid; i < K * BV; i += kThreads)
                 st(h_ckpt, ck + (int64_t)(i / BV) * V + v0 + i % BV, hs[i]);
         }
-        for (int i = tid; i < C * K; i += kThreads) {
+                for (int i = tid; i < C * K; i += kThreads) {
             const int t = i / K, e = i % K;
             const int gi = PER_K ? e : 0;
             ws[t * KP + e] = t < nv ? ld(w, row(t) * K + e) : 0.f;
             kgs[t * KP + e] = t < nv ? ld(k, krow(t) * K + e) * expf(Gl[gi] - g_cum[row(t) * GW + gi]) : 0.f;
         }
-        for (int i = tid; i < C * BV; i += kThreads)
+                for (int i = tid; i < C * BV; i += kThreads)
             us[(i / BV) * BVP + i % BV] = i / BV < nv ? ld(u, row(i / BV) * V + v0 + i % BV) : 0.f;
         __syncthreads();
-        // v' = u - w h
-        for (int idx = tid; idx < C * BV; idx += kThreads) {
-            const int t = idx / BV, j = idx % BV;
-            float s = 0.f;
-            for (int e = 0; e < K; ++e) s += ws[t * KP + e] * hs[e * BV + j];
-            const float vp = us[t * BVP + j] - s;
-            vps[t * BVP + j] = vp;
-            if (t < nv) st(v_new, row(t) * V + v0 + j, vp);
+        // v' = u - w h: four rows t0 .. t0+3 per thread share each load of h (four independent sums,
+        // each in the same order as one row alone)
+        for (int idx = tid; idx < (C / 4) * BV; idx += kThreads) {
+            const int t0 = (idx / BV) * 4, j = idx % BV;
+            float s[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int e = 0; e < K; ++e) {
+                const float he = hs[e * BV + j];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) s[r] += ws[(t0 + r) * KP + e] * he;
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int t = t0 + r;
+                const float vp = us[t * BVP + j] - s[r];
+                vps[t * BVP + j] = vp;
+                if (t < nv) st(v_new, row(t) * V + v0 + j, vp);
+            }
         }
         __syncthreads();
-        // h = exp(G_last) * h + kg^T v'
-        for (int idx = tid; idx < K * BV; idx += kThreads) {
-            const int e = idx / BV, j = idx % BV;
-            float s = 0.f;
-            for (int t = 0; t < C; ++t) s += kgs[t * KP + e] * vps[t * BVP + j];
-            hs[idx] = expf(Gl[PER_K ? e : 0]) * hs[idx] + s;
+        // h = exp(G_last) * h + kg^T v': four key rows per thread share each load of v'
+        for (int idx = tid; idx < (K / 4) * BV; idx += kThreads) {
+            const int e0 = (idx / BV) * 4, j = idx % BV;
+            float s[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int t = 0; t < C; ++t) {
+                const float vt = vps[t * BVP + j];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) s[r] += kgs[t * KP + e0 + r] * vt;
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int e = e0 + r;
+                hs[e * BV + j] = expf(Gl[PER_K ? e : 0]) * hs[e * BV + j] + s[r];
+            }
         }
         __syncthreads();
     }
@@ -237,15 +286,15 @@ simt_output_kernel(Dims d, const IO* __restrict__ q, const IO* __restrict__ k, c
     const int64_t ck = (((int64_t)b * d.NT + c) * H + h) * K * V;
     const int nv = min(C, d.T - c * C);   // a last, partial chunk: zero q, k, v' past T, G held at its last value
 
-    for (int i = tid; i < C * K; i += kThreads) {
+        for (int i = tid; i < C * K; i += kThreads) {
         const bool in = i / K < nv;
         qs[(i / K) * KP + i % K] = in ? ld(q, krow(i / K) * K + i % K) : 0.f;
         ks[(i / K) * KP + i % K] = in ? ld(k, krow(i / K) * K + i % K) : 0.f;
     }
-    for (int i = tid; i < C * GW; i += kThreads) Gs[i] = g_cum[row(min(i / GW, nv - 1)) * GW + i % GW];
-    for (int i = tid; i < C * VT; i += kThreads)
+        for (int i = tid; i < C * GW; i += kThreads) Gs[i] = g_cum[row(min(i / GW, nv - 1)) * GW + i % GW];
+        for (int i = tid; i < C * VT; i += kThreads)
         vps[(i / VT) * VTP + i % VT] = i / VT < nv ? ld(v_new, row(i / VT) * V + v0 + i % VT) : 0.f;
-    for (int i = tid; i < K * VT; i += kThreads) hs[i] = ld(h_ckpt, ck + (int64_t)(i / VT) * V + v0 + i % VT);
+        for (int i = tid; i < K * VT; i += kThreads) hs[i] = ld(h_ckpt, ck + (int64_t)(i / VT) * V + v0 + i % VT);
     __syncthreads();
     // Q~_ij = sum_d q_id k_jd exp(G_id - G_jd), j <= i
     for (int idx = tid; idx < C * C; idx += kThreads) {
@@ -270,12 +319,25 @@ simt_output_kernel(Dims d, const IO* __restrict__ q, const IO* __restrict__ k, c
         qs[t * KP + e] *= expf(Gs[t * GW + (PER_K ? e : 0)]);
     }
     __syncthreads();
-    for (int idx = tid; idx < C * VT; idx += kThreads) {
-        const int i = idx / VT, j = idx % VT;
-        float s = 0.f;
-        for (int e = 0; e < K; ++e) s += qs[i * KP + e] * hs[e * VT + j];
-        for (int t = 0; t <= i; ++t) s += Qt[i * CP + t] * vps[t * VTP + j];
-        if (i < nv) st(o, row(i) * V + v0 + j, d.scale * s);
+    // four rows i0 .. i0+3 per thread share each load of h and of v' (four independent sums, each in the
+    // same order as one row alone: the q h terms, then the causal P v' terms)
+    for (int idx = tid; idx < (C / 4) * VT; idx += kThreads) {
+        const int i0 = (idx / VT) * 4, j = idx % VT;
+        float s[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int e = 0; e < K; ++e) {
+            const float he = hs[e * VT + j];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) s[r] += qs[(i0 + r) * KP + e] * he;
+        }
+        for (int t = 0; t <= i0 + 3; ++t) {
+            const float vt = vps[t * VTP + j];
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+                if (t <= i0 + r) s[r] += Qt[(i0 + r) * CP + t] * vt;
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+            if (i0 + r < nv) st(o, row(i0 + r) * V + v0 + j, d.scale * s[r]);
     }
 }
 

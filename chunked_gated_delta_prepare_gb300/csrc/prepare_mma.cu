@@ -22,8 +22,8 @@
 //            w = (X diag(beta)) (k * exp(G)), u as above       (per-key-dim gate)
 //            each warp skipping the k-steps where its row of X is zero
 //
-// The products are warp-level mma.sync m16n8k16 (bf16 in, fp32 accumulate) fed
-// by ldmatrix from the swizzled tiles, or, for S and P, tcgen05 with the
+// The products are warp-level mma.sync m16n8k16 (bf16 or fp16 in, fp32 accumulate)
+// fed by ldmatrix from the swizzled tiles, or, for S and P, tcgen05 with the
 // accumulators in tensor memory (UMMA below).  Measured on the 32k-token,
 // 32-head workload (the prepare alone over the whole GPU / the overlapped
 // forward): every product on mma.sync 0.386 / 0.799 ms; S and P on tcgen05

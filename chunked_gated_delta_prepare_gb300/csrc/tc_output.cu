@@ -140,6 +140,7 @@ tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         }
     }
     if (warp == 0) {
+        __syncwarp();   // thread 0 issued the loads alone; the allocation is warp-wide
         bw::tmem_alloc(&tslot, L::tmem_cols);
         bw::tmem_relinquish();
     }

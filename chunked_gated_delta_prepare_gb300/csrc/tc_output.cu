@@ -39,28 +39,31 @@ struct OutLayout {
     static constexpr int GW = PER_K ? K : 1;
     // With a per-key-dim gate the gate is read from global memory (L2) where needed instead of
     // being staged (32 KB), k's gated copy is written over k, and P over that once S is formed:
-    // two CTAs per SM.  OPS keeps no checkpoints (qg goes over q, kg into the v' region): three per SM.
+    // two CTAs per SM.  OPS keeps no v' and no checkpoints, writes q's gated copy over q and sends qg
+    // and kg straight to global memory: two tiles, four CTAs per SM.
     static constexpr uint32_t Q = 0;                               // q, then q exp(G) for chunk 0
     static constexpr uint32_t Kt = Q + K * 128;                    // k (per-key-dim gate: then k exp(Gref - G))
-    static constexpr uint32_t VP = Kt + K * 128;                   // v' [64][V]
-    static constexpr uint32_t Hc = VP + V * 128;                   // checkpoints [NCH][K][V] (none with OPS)
+    static constexpr uint32_t VP = Kt + K * 128;                   // v' [64][V] (none with OPS)
+    static constexpr uint32_t Hc = VP + (OPS ? 0 : V * 128);       // checkpoints [NCH][K][V] (none with OPS)
     static constexpr uint32_t P = PER_K ? Kt : Hc + NCH * K * V * 2;   // P [64][64]
     static constexpr uint32_t Q1 = PER_K ? Hc + (OPS ? 0 : NCH * K * V * 2) : P + 8192;   // C = 32: q exp(G), chunk 1
-    static constexpr uint32_t Qa = Q1 + (NCH > 1 ? K * 128 : 0);   // per-key-dim gate: q exp(G - Gref)
-    static constexpr uint32_t F = Qa + (PER_K ? K * 128 : 0);      // fp32: G [64] (scalar gate), flag
+    static constexpr uint32_t Qa = OPS ? Q : Q1 + (NCH > 1 ? K * 128 : 0);   // per-key-dim gate: q exp(G - Gref)
+    static constexpr uint32_t F = OPS ? Q1 : Qa + (PER_K ? K * 128 : 0);     // fp32: G [64] (scalar gate), flag
     static constexpr uint32_t bytes = F + 4 * ((PER_K ? 0 : kTile) + 4);
     static constexpr uint32_t tx = 2 * K * 128 + V * 128 + NCH * K * V * 2;
     static constexpr uint32_t tmem_cols = OPS ? 64 : 256;          // S at 0 (64 cols), D at 64 (V cols)
 };
 
-// OPS: mvp and mh are the kg and qg store maps and mp the P store map (otherwise mp is unused).
+// OPS: mp is the P store map (otherwise unused), kg_out and qg_out [B, T, H, K] the gated operands'
+// outputs (otherwise null).
 template <int K, int V, int C, bool PER_K, bool OPS = false>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(128, OPS ? 4 : 1)
 tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                  const __grid_constant__ CUtensorMap mvp, const __grid_constant__ CUtensorMap mh,
                  const __grid_constant__ CUtensorMap mp, const float* __restrict__ g_cum,
                  const bf16* __restrict__ q_raw, const bf16* __restrict__ k_raw, bf16* __restrict__ o, int T, int H,
-                 int NT, int G, float scale, unsigned int* err) {
+                 int NT, int G, float scale, unsigned int* err, bf16* __restrict__ kg_out = nullptr,
+                 bf16* __restrict__ qg_out = nullptr) {
     static_assert(!OPS || (PER_K && C == 64 && K == V), "gated operands: per-key-dim gate, one chunk per tile");
     using L = OutLayout<K, V, C, PER_K, OPS>;
     constexpr int GW = L::GW;
@@ -122,9 +125,10 @@ tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         }
     }
     // per-key-dim gate: this thread's rows of G, the middle row of each chunk and (OPS) the chunk's last
-    // row, all in flight together with the tiles
-    float4 ga[PER_K ? NIT : 1][2], gref[L::NCH][2], glast[2];
-    if constexpr (PER_K) {
+    // row.  Without OPS (two CTAs per SM) they are loaded here, in flight together with the tiles; OPS
+    // loads them after the tiles' wait, in fewer registers, for four CTAs per SM
+    float4 ga[NIT][2], gref[L::NCH][2], glast[2];
+    auto load_gates = [&]() {
         load_g_rows(ga);
         if constexpr (OPS) {
             const float4* src = reinterpret_cast<const float4*>(g_cum + row(nvalid - 1) * K + (tid % (K / 8)) * 8);
@@ -138,7 +142,8 @@ tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
             gref[ch][0] = src[0];
             gref[ch][1] = src[1];
         }
-    }
+    };
+    if constexpr (PER_K && !OPS) load_gates();
     if (warp == 0) {
         __syncwarp();   // thread 0 issued the loads alone; the allocation is warp-wide
         bw::tmem_alloc(&tslot, L::tmem_cols);
@@ -157,6 +162,7 @@ tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
     bool ok = bw::mbar_wait(&bar_tma, 0, err, kDeviceErrTimeout);
 
     if constexpr (PER_K) {
+        if constexpr (OPS) load_gates();
         // OPS: exp(G_ref) and exp(G_last - G_ref) of this thread's eight key columns (the same at every step),
         // so that qg = (q exp(G - G_ref)) exp(G_ref) and kg = (k exp(G_ref - G)) exp(G_last - G_ref) reuse the
         // gated copies' exponentials where |G - G_ref| <= kExpSafe
@@ -205,21 +211,23 @@ tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
                 }
             }
             if (big) *sFlag = 1;
-            if constexpr (OPS) {   // qg into the unused checkpoint region, kg into the unused v' region
+            if constexpr (OPS) {   // qg and kg straight to global memory: 16 threads write a row's 256 bytes
                 uint4 pq, pk;
                 pq.x = bw::pack_bf16(fq[0], fq[1]); pq.y = bw::pack_bf16(fq[2], fq[3]);
                 pq.z = bw::pack_bf16(fq[4], fq[5]); pq.w = bw::pack_bf16(fq[6], fq[7]);
                 pk.x = bw::pack_bf16(fk[0], fk[1]); pk.y = bw::pack_bf16(fk[2], fk[3]);
                 pk.z = bw::pack_bf16(fk[4], fk[5]); pk.w = bw::pack_bf16(fk[6], fk[7]);
-                *reinterpret_cast<uint4*>(sm + L::Q + off) = pq;   // over q: each thread rewrites what it read
-                *reinterpret_cast<uint4*>(sm + L::VP + off) = pk;
+                if (r < nvalid) {
+                    *reinterpret_cast<uint4*>(qg_out + row(r) * K + lc * 8) = pq;
+                    *reinterpret_cast<uint4*>(kg_out + row(r) * K + lc * 8) = pk;
+                }
             }
             uint4 pa, pb;
             pa.x = bw::pack_bf16(fa[0], fa[1]); pa.y = bw::pack_bf16(fa[2], fa[3]);
             pa.z = bw::pack_bf16(fa[4], fa[5]); pa.w = bw::pack_bf16(fa[6], fa[7]);
             pb.x = bw::pack_bf16(fb[0], fb[1]); pb.y = bw::pack_bf16(fb[2], fb[3]);
             pb.z = bw::pack_bf16(fb[4], fb[5]); pb.w = bw::pack_bf16(fb[6], fb[7]);
-            *reinterpret_cast<uint4*>(sm + L::Qa + off) = pa;
+            *reinterpret_cast<uint4*>(sm + L::Qa + off) = pa;   // OPS: over q, each thread rewriting what it read
             *reinterpret_cast<uint4*>(sm + L::Kt + off) = pb;   // over k: each thread rewrites what it read
         }
         bw::fence_async_shared();
@@ -277,7 +285,7 @@ tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
             if (j >= (i / C) * C && j <= i) {
                 float acc = 0.f;
                 for (int d = 0; d < K; ++d) {
-                    // OPS: q's tile now holds qg, so raw q comes from global memory too
+                    // OPS: q's tile now holds q's gated copy, so raw q comes from global memory too
                     const float qi = OPS ? (i < nvalid ? __bfloat162float(q_raw[krow(i) * K + d]) : 0.f)
                                          : __bfloat162float(*reinterpret_cast<const bf16*>(sm + L::Q + tile_off(i, d)));
                     // k's tile now holds its gated copy: raw k and G come from global memory (rare path)
@@ -292,17 +300,12 @@ tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         __syncthreads();
     }
     if constexpr (OPS) {
-        // P, kg and qg leave by TMA (rows past T clipped); nothing of the output's second half runs
+        // P leaves by TMA (rows past T clipped); nothing of the output's second half runs
         bw::fence_async_shared();
         __syncthreads();
         if (tid == 0) {
             if (ok) {
                 bw::tma_store_4d(&mp, sm + L::P, 0, 0, h, b * NT + t0 / C);
-#pragma unroll
-                for (int a = 0; a < K / 64; ++a) {
-                    bw::tma_store_4d(&mvp, sm + L::VP + a * 8192, a * 64, h, t0, b);
-                    bw::tma_store_4d(&mh, sm + L::Q + a * 8192, a * 64, h, t0, b);
-                }
                 bw::bulk_commit();
             }
             bw::bulk_wait_read<0>();
@@ -399,7 +402,7 @@ cudaError_t launch_output(const Dims& d, const void* q, const void* k, const voi
     if (e != cudaSuccess) return e;
     const dim3 grid((d.T + kTile - 1) / kTile, d.H, d.B);
     kern<<<grid, 128, smem, s>>>(mq, mk, mvp, mh, mh, g_cum, (const bf16*)q, (const bf16*)k, (bf16*)o, d.T, d.H, d.NT,
-                                 d.G, d.scale, err);
+                                 d.G, d.scale, err, nullptr, nullptr);
     return cudaGetLastError();
 }
 
@@ -429,16 +432,17 @@ cudaError_t tc_gated_operands(const Dims& d, const void* q, const void* k, const
     const uint64_t st[3] = {(uint64_t)C * 2, (uint64_t)C * C * 2, (uint64_t)d.H * C * C * 2};
     const uint32_t box[4] = {64, 64, 1, 1};
     if (!make_tmap_tokens(&mq, q, d.B, d.T, d.Hk, K, kTile) || !make_tmap_tokens(&mk, k, d.B, d.T, d.Hk, K, kTile) ||
-        !make_tmap_tokens(&mkg, kg, d.B, d.T, d.H, K, kTile) || !make_tmap_tokens(&mqg, qg, d.B, d.T, d.H, K, kTile) ||
         !make_tmap_bf16_4d(&mp, P, dims, st, box))
         return cudaErrorInvalidValue;
+    mkg = mq;   // unused by the operands form (qg and kg are plain stores)
+    mqg = mq;
     auto kern = tc_output_kernel<K, V, C, true, true>;
     const size_t smem = L::bytes + 1024;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const dim3 grid((d.T + kTile - 1) / kTile, d.H, d.B);
     kern<<<grid, 128, smem, s>>>(mq, mk, mkg, mqg, mp, g_cum, (const bf16*)q, (const bf16*)k, nullptr, d.T, d.H, d.NT,
-                                 d.G, d.scale, err);
+                                 d.G, d.scale, err, (bf16*)kg, (bf16*)qg);
     return cudaGetLastError();
 }
 

@@ -319,16 +319,36 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
         if (32 + lane < nout) g_cum[row(32 + lane)] = x1;
     }
     __syncthreads();
-    // chunk-local inclusive cumsum (per-key-dim gate: one thread per key column)
-    if (PER_K) {
-        for (int col = tid; col < (kTile / C) * K; col += 128) {
-            const int ch = col / K, d = col % K;
-            float run = 0.f;
-            for (int t = ch * C; t < ch * C + C; ++t) {
-                run += sG[t * K + d];
-                sG[t * K + d] = run;
-                if (t < nout) g_cum[row(t) * K + d] = run;
-            }
+    // chunk-local inclusive cumsum (per-key-dim gate) in two levels: thread (column quad cq, row block rb)
+    // forms the prefix of its RPB rows of four columns, the block totals pass through the still unused Kb
+    // tile, and each block adds the totals of the blocks before it in its chunk
+    if constexpr (PER_K) {
+        constexpr int NQ = K / 4, NRB = 128 / NQ, RPB = kTile / NRB;   // K = 128: 32 quads x 4 blocks of 16 rows
+        static_assert(NQ * NRB == 128 && C % RPB == 0, "blocks tile the threads and the chunks");
+        float4* sG4 = reinterpret_cast<float4*>(sG);
+        float4* tot = reinterpret_cast<float4*>(sm + L::kKb);        // [NRB][NQ]
+        const int cq = tid % NQ, rb = tid / NQ, r0 = rb * RPB;
+        float4 pre[RPB];
+        float4 run = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < RPB; ++i) {
+            const float4 x = sG4[(r0 + i) * NQ + cq];
+            run.x += x.x; run.y += x.y; run.z += x.z; run.w += x.w;
+            pre[i] = run;
+        }
+        tot[rb * NQ + cq] = run;
+        __syncthreads();
+        float4 off = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int b2 = (r0 / C) * C / RPB; b2 < rb; ++b2) {   // the blocks before this one in its chunk
+            const float4 y = tot[b2 * NQ + cq];
+            off.x += y.x; off.y += y.y; off.z += y.z; off.w += y.w;
+        }
+#pragma unroll
+        for (int i = 0; i < RPB; ++i) {
+            const int t = r0 + i;
+            const float4 v4 = make_float4(off.x + pre[i].x, off.y + pre[i].y, off.z + pre[i].z, off.w + pre[i].w);
+            sG4[t * NQ + cq] = v4;
+            if (t < nout) *reinterpret_cast<float4*>(g_cum + row(t) * K + 4 * cq) = v4;
         }
         __syncthreads();
     }

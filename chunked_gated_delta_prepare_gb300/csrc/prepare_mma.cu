@@ -54,32 +54,42 @@ using namespace tc;
 template <int K, int V, int C, bool PER_K, bool WITH_P>
 struct PrepLayout {
     static constexpr int GW = PER_K ? K : 1;
-    static constexpr uint32_t kK = 0;                               // k tile [64][K]
-    static constexpr uint32_t kV = kK + K * 128;                    // v tile [64][V]
-    static constexpr uint32_t kQ = kV + V * 128;                    // q tile [64][K] (with P)
+    // SPLITG (per-key-dim gate, K = V = 128): G passes through a [64][64] half tile, one half of the keys
+    // at a time; k e^G is written over k as the gated copies are made; v lands in Kb's place once S is
+    // formed; the solve's scratch takes the dead Ka and G-half tiles.  67 KB: three CTAs per SM.
+    static constexpr bool SPLITG = PER_K && K == 128 && V == 128;
+    static constexpr uint32_t kK = 0;                               // k tile [64][K] (SPLITG: then k exp(G))
+    static constexpr uint32_t kKb0 = kK + K * 128;                  // SPLITG: Kb, then v
+    static constexpr uint32_t kV = SPLITG ? kKb0 : kK + K * 128;   // v tile [64][V]
+    static constexpr uint32_t kQ = kV + (SPLITG ? K * 128 : V * 128);   // q tile [64][K] (with P)
     static constexpr uint32_t kKa = kQ + (WITH_P ? K * 128 : 0);    // KDA: gated k copies
-    static constexpr uint32_t kKb = kKa + (PER_K ? K * 128 : 0);
-    static constexpr uint32_t kF = kKb + (PER_K ? K * 128 : 0);     // fp32 / block scratch
+    static constexpr uint32_t kKb = SPLITG ? kKb0 : kKa + (PER_K ? K * 128 : 0);
+    static constexpr uint32_t kGh = kKa + (PER_K ? K * 128 : 0);    // SPLITG: G half [64][64] fp32
+    static constexpr uint32_t kF = SPLITG ? kGh + 64 * 64 * 4 : kKb + (PER_K ? K * 128 : 0);   // fp32 / block scratch
     // byte offsets from kF
-    static constexpr uint32_t fG = 0;                                // G [64][GW] fp32
-    static constexpr uint32_t fB = fG + 64 * GW * 4;                 // beta [64] fp32
+    static constexpr uint32_t fG = 0;                                // G [64][GW] fp32 (SPLITG: in the half tile)
+    static constexpr uint32_t fB = fG + (SPLITG ? 0 : 64 * GW * 4);  // beta [64] fp32
     static constexpr uint32_t fE = fB + 64 * 4;                      // exp(G) [64] fp32 (scalar gate)
     static constexpr uint32_t fFlag = fE + 64 * 4;                   // KDA: exact-path flag
+    static constexpr uint32_t fTot = fFlag + 16;                     // SPLITG: the cumsum's block totals
     // The solve's scratch.  With a per-key-dim gate and K = 128 it reuses the 32 KB of G, dead by then
-    // (the last reader is the k exp(G) rescale, a barrier before the solve): two CTAs per SM.
+    // (the last reader is the k exp(G) rescale, a barrier before the solve): two CTAs per SM.  SPLITG puts it
+    // over the Ka and G-half tiles.
     static constexpr uint32_t kDw = 2 * 16 * 17 * 4;
     static constexpr uint32_t kSolveBytes = ((4 * kDw + 1023) & ~1023u) + 14 * 2 * 512;
-    static constexpr bool kAliasG = PER_K && 64 * GW * 4 >= kSolveBytes;
-    static constexpr uint32_t fD = kAliasG ? 0 : fFlag + 16;         // per warp: A_II, X_II fp32 [16][17] each
+    static constexpr bool kAliasG = PER_K && !SPLITG && 64 * GW * 4 >= kSolveBytes;
+    static constexpr uint32_t kScr = SPLITG ? kKa : kF;              // the scratch's base
+    static constexpr uint32_t fD = (kAliasG || SPLITG) ? 0 : fFlag + 16;   // per warp: A_II, X_II fp32 [16][17] each
     static constexpr uint32_t fXs = (fD + 4 * kDw + 1023) & ~1023u;  // X blocks (M, J), J <= M: hi, lo bf16 [16][16]
     static constexpr uint32_t kXb = 2 * 512;
     static constexpr uint32_t fSs = fXs + 10 * kXb;                  // per warp: S_IJ hi, lo bf16 [16][16]
     static constexpr uint32_t solve_end = fSs + 4 * kXb;
-    static constexpr uint32_t scratch = kAliasG ? fFlag + 16 : solve_end;
-    static constexpr uint32_t bytes = kF + scratch;
+    static constexpr uint32_t scratch = SPLITG ? 2 * K * 128 : (kAliasG ? fFlag + 16 : solve_end);   // from kScr
+    static constexpr uint32_t bytes = SPLITG ? kF + fTot + 2048 : kF + scratch;
     static_assert(!kAliasG || solve_end <= 64 * GW * 4, "the solve's scratch fits in G's space");
-    // KDA exact path: A fp32 [64][64] over the Ka and Kb tiles (dead once S = Ka Kb^T is formed)
-    static_assert(!PER_K || 64 * 64 * 4 <= 2 * K * 128, "the exact A fits over Ka and Kb");
+    static_assert(!SPLITG || solve_end <= scratch, "the solve's scratch fits over Ka and the G half");
+    // KDA exact path: A fp32 [64][64] over the Ka and Kb tiles (dead once S = Ka Kb^T is formed; SPLITG: Ka)
+    static_assert(!PER_K || 64 * 64 * 4 <= (SPLITG ? 1 : 2) * K * 128, "the exact A fits");
     static_assert(!WITH_P || (C == 64 && !PER_K), "P is produced for 64-token chunks and a scalar gate");
 };
 
@@ -171,7 +181,8 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
                    const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap mu,
                    const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mp,
                    const float* __restrict__ g, const bf16* __restrict__ beta, float* __restrict__ g_cum,
-                   bf16* __restrict__ tinv, int T, int H, int G, PackedIn pin, unsigned int* err) {
+                   bf16* __restrict__ tinv, int T, int H, int G, PackedIn pin, unsigned int* err,
+                   const bf16* __restrict__ k_raw) {
     static_assert(!PACKED || (C == kTile && !PER_K), "packed inputs: whole 64-token chunks, scalar gate");
     static_assert(!UMMA || (K == 128 && V == 128 && C == 64 && !PER_K && WITH_P && !PACKED), "tcgen05 S, P: one shape");
     static_assert(!F16 || (K == 128 && V == 128 && C == 64 && !PER_K && WITH_P && !PACKED),
@@ -180,8 +191,9 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
     constexpr int GW = L::GW;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    constexpr bool SPLITG = L::SPLITG;
     unsigned char* F = sm + L::kF;
-    float* sG = reinterpret_cast<float*>(F + L::fG);
+    float* sG = reinterpret_cast<float*>(SPLITG ? sm + L::kGh : F + L::fG);   // SPLITG: the half tile
     float* sB = reinterpret_cast<float*>(F + L::fB);
     float* sE = reinterpret_cast<float*>(F + L::fE);
     int* sFlag = reinterpret_cast<int*>(F + L::fFlag);
@@ -259,9 +271,11 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
 #pragma unroll
             for (int a = 0; a < K / 64; ++a) bw::tma_load_4d(sm + L::kQ + a * 8192, &mq, &bar_q, a * 64, hk, t_in, b_in);
         }
-        bw::mbar_arrive_expect_tx(&bar_v, V * 128);
+        if constexpr (!SPLITG) {   // SPLITG: v lands in Kb's place once S is formed
+            bw::mbar_arrive_expect_tx(&bar_v, V * 128);
 #pragma unroll
-        for (int a = 0; a < V / 64; ++a) bw::tma_load_4d(sm + L::kV + a * 8192, &mv, &bar_v, a * 64, h, t_in, b_in);
+            for (int a = 0; a < V / 64; ++a) bw::tma_load_4d(sm + L::kV + a * 8192, &mv, &bar_v, a * 64, h, t_in, b_in);
+        }
     }
     static_assert(kTile <= 128, "one beta row per thread");
     if (tid < kTile) sB[tid] = b_pre;
@@ -292,16 +306,19 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
         bw::mma_commit_warp(&bar_p);
     }
     if constexpr (PER_K) {
-        // 16-byte loads, all of a thread's issued before any is used (the tile is 32 KB at K = 128)
-        constexpr int NV4 = kTile * GW / 4 / 128;
-        float4 gv[NV4];
+        if constexpr (!SPLITG) {   // SPLITG loads G by halves of the keys, below
+            // 16-byte loads, all of a thread's issued before any is used (the tile is 32 KB at K = 128)
+            constexpr int NV4 = kTile * GW / 4 / 128;
+            float4 gv[NV4];
 #pragma unroll
-        for (int j = 0; j < NV4; ++j) {
-            const int e = 4 * (tid + 128 * j), t = e / GW;
-            gv[j] = t < nvalid ? *reinterpret_cast<const float4*>(g + row_in(t) * GW + e % GW) : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int j = 0; j < NV4; ++j) {
+                const int e = 4 * (tid + 128 * j), t = e / GW;
+                gv[j] = t < nvalid ? *reinterpret_cast<const float4*>(g + row_in(t) * GW + e % GW)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int j = 0; j < NV4; ++j) *reinterpret_cast<float4*>(sG + 4 * (tid + 128 * j)) = gv[j];
         }
-#pragma unroll
-        for (int j = 0; j < NV4; ++j) *reinterpret_cast<float4*>(sG + 4 * (tid + 128 * j)) = gv[j];
     } else if (warp == 0) {
         // scalar gate: warp shuffle scan, lane l holds rows l and 32 + l
         float x0 = g_pre0, x1 = g_pre1;
@@ -322,7 +339,7 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
     // chunk-local inclusive cumsum (per-key-dim gate) in two levels: thread (column quad cq, row block rb)
     // forms the prefix of its RPB rows of four columns, the block totals pass through the still unused Kb
     // tile, and each block adds the totals of the blocks before it in its chunk
-    if constexpr (PER_K) {
+    if constexpr (PER_K && !SPLITG) {
         constexpr int NQ = K / 4, NRB = 128 / NQ, RPB = kTile / NRB;   // K = 128: 32 quads x 4 blocks of 16 rows
         static_assert(NQ * NRB == 128 && C % RPB == 0, "blocks tile the threads and the chunks");
         float4* sG4 = reinterpret_cast<float4*>(sG);
@@ -356,7 +373,86 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
     bool ok = bw::mbar_wait(&bar_k, 0, err, kDeviceErrTimeout);
     if (PACKED && nvalid < kTile) zero_rows(L::kK, K, nvalid, kTile, tid, 128);   // a barrier follows
 
-    if (PER_K) {
+    if constexpr (SPLITG) {
+        // per-key-dim gate at K = 128, G by halves of the keys through the [64][64] half tile: load, the
+        // chunk-local cumsum in two levels (as below), g_cum, then the gated copies Ka, Kb of those keys
+        // and k exp(G) over k
+        constexpr int HK = 64, NQ = HK / 4, NRB = 128 / NQ, RPB = kTile / NRB;   // 16 quads x 8 blocks of 8 rows
+        static_assert(C % RPB == 0, "row blocks tile the chunks");
+        float4* sG4 = reinterpret_cast<float4*>(sG);
+        float4* tot = reinterpret_cast<float4*>(F + L::fTot);   // [NRB][NQ]
+        const int cq = tid % NQ, rb = tid / NQ, r0 = rb * RPB;
+        bool big = false;
+        for (int hf = 0; hf < K / HK; ++hf) {
+            float4 gv[kTile * HK / 4 / 128];
+#pragma unroll
+            for (int j = 0; j < kTile * HK / 4 / 128; ++j) {
+                const int e = 4 * (tid + 128 * j), t = e / HK;
+                gv[j] = t < nvalid ? *reinterpret_cast<const float4*>(g + row_in(t) * GW + hf * HK + e % HK)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int j = 0; j < kTile * HK / 4 / 128; ++j) sG4[tid + 128 * j] = gv[j];
+            __syncthreads();
+            float4 pre[RPB];
+            float4 run = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int i = 0; i < RPB; ++i) {
+                const float4 x = sG4[(r0 + i) * NQ + cq];
+                run.x += x.x; run.y += x.y; run.z += x.z; run.w += x.w;
+                pre[i] = run;
+            }
+            tot[rb * NQ + cq] = run;
+            __syncthreads();
+            float4 off = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int b2 = (r0 / C) * C / RPB; b2 < rb; ++b2) {
+                const float4 y = tot[b2 * NQ + cq];
+                off.x += y.x; off.y += y.y; off.z += y.z; off.w += y.w;
+            }
+#pragma unroll
+            for (int i = 0; i < RPB; ++i) {
+                const int t = r0 + i;
+                const float4 v4 = make_float4(off.x + pre[i].x, off.y + pre[i].y, off.z + pre[i].z, off.w + pre[i].w);
+                sG4[t * NQ + cq] = v4;
+                if (t < nout) *reinterpret_cast<float4*>(g_cum + row(t) * K + hf * HK + 4 * cq) = v4;
+            }
+            __syncthreads();
+            // this half's 64 x 64 keys as 512 chunks of eight: Ka, Kb, and k exp(G) over k (each thread
+            // rewrites the chunk of k it read)
+#pragma unroll
+            for (int j = 0; j < kTile * (HK / 8) / 128; ++j) {
+                const int i = tid + 128 * j, r = i / (HK / 8), lc = i % (HK / 8);
+                const int ref = (r / C) * C + C / 2;
+                const uint32_t off = (uint32_t)(hf * 8192 + r * 128 + ((lc ^ (r & 7)) << 4));
+                const uint4 raw = *reinterpret_cast<const uint4*>(sm + L::kK + off);
+                const bf16* kv = reinterpret_cast<const bf16*>(&raw);
+                float fa[8], fb[8], fw[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float gr = sG[r * HK + lc * 8 + e];
+                    const float dg = gr - sG[ref * HK + lc * 8 + e];
+                    big |= fabsf(dg) > kExpSafe;
+                    const float x = __bfloat162float(kv[e]);
+                    fa[e] = x * __expf(fminf(fmaxf(dg, -kExpClamp), kExpClamp));
+                    fb[e] = x * __expf(fminf(fmaxf(-dg, -kExpClamp), kExpClamp));
+                    fw[e] = x * __expf(gr);
+                }
+                uint4 pa, pb, pw;
+                pa.x = bw::pack_bf16(fa[0], fa[1]); pa.y = bw::pack_bf16(fa[2], fa[3]);
+                pa.z = bw::pack_bf16(fa[4], fa[5]); pa.w = bw::pack_bf16(fa[6], fa[7]);
+                pb.x = bw::pack_bf16(fb[0], fb[1]); pb.y = bw::pack_bf16(fb[2], fb[3]);
+                pb.z = bw::pack_bf16(fb[4], fb[5]); pb.w = bw::pack_bf16(fb[6], fb[7]);
+                pw.x = bw::pack_bf16(fw[0], fw[1]); pw.y = bw::pack_bf16(fw[2], fw[3]);
+                pw.z = bw::pack_bf16(fw[4], fw[5]); pw.w = bw::pack_bf16(fw[6], fw[7]);
+                *reinterpret_cast<uint4*>(sm + L::kKa + off) = pa;
+                *reinterpret_cast<uint4*>(sm + L::kKb + off) = pb;
+                *reinterpret_cast<uint4*>(sm + L::kK + off) = pw;
+            }
+            __syncthreads();   // the half tile is rewritten next (or dead)
+        }
+        if (big) *sFlag = 1;
+        bw::fence_async_shared();
+    } else if (PER_K) {
         // gated copies for S: Ka = k exp(G - G_ref), Kb = k exp(G_ref - G), G_ref = middle row of the chunk
         for (int i = tid; i < kTile * (K / 8); i += 128) {
             const int r = i / (K / 8), lc = i % (K / 8);
@@ -501,19 +597,33 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
     }
     if (PER_K) {
         __syncthreads();
+        if (SPLITG && tid == 0) {   // S is formed: v lands in Kb's place under the solve
+            bw::mbar_arrive_expect_tx(&bar_v, V * 128);
+#pragma unroll
+            for (int a = 0; a < V / 64; ++a) bw::tma_load_4d(sm + L::kV + a * 8192, &mv, &bar_v, a * 64, h, t_in, b_in);
+        }
         if (*sFlag) {
             // exact fp32 A for chunks with extreme gates: A_ij = beta_i sum_d k_id k_jd exp(G_id - G_jd)
-            float* sA = reinterpret_cast<float*>(sm + L::kKa);   // over the dead Ka and Kb tiles
+            // (SPLITG: raw k and G come from global memory, k's tile holding k exp(G) and G only its last half)
+            float* sA = reinterpret_cast<float*>(sm + L::kKa);   // over the dead Ka (and Kb) tiles
+            const int Hk = EXTRA ? H / G : H;
+            auto kval = [&](int i, int d) -> float {
+                if constexpr (SPLITG)
+                    return i < nvalid ? __bfloat162float(k_raw[(((int64_t)b_in * T_in + t_in + i) * Hk + hk) * K + d])
+                                      : 0.f;
+                else
+                    return __bfloat162float(*reinterpret_cast<const bf16*>(sm + L::kK + tile_off(i, d)));
+            };
+            auto gval = [&](int i, int d) -> float {
+                if constexpr (SPLITG) return i < nvalid ? g_cum[row(i) * K + d] : 0.f;
+                else return sG[i * K + d];
+            };
             for (int idx = tid; idx < kTile * kTile; idx += 128) {
                 const int i = idx / kTile, j = idx % kTile;
                 float a = 0.f;
-                if (j >= (i / C) * C && j < i) {
+                if (j >= (i / C) * C && j < i && i < nvalid) {   // rows past T have k = 0: A is 0 there
                     float acc = 0.f;
-                    for (int d = 0; d < K; ++d) {
-                        const float ki = __bfloat162float(*reinterpret_cast<const bf16*>(sm + L::kK + tile_off(i, d)));
-                        const float kj = __bfloat162float(*reinterpret_cast<const bf16*>(sm + L::kK + tile_off(j, d)));
-                        acc += ki * kj * __expf(sG[i * K + d] - sG[j * K + d]);
-                    }
+                    for (int d = 0; d < K; ++d) acc += kval(i, d) * kval(j, d) * __expf(gval(i, d) - gval(j, d));
                     a = sB[i] * acc;
                 }
                 sA[i * 64 + j] = a;
@@ -530,8 +640,9 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
             }
             __syncthreads();   // every warp has its A before Ka is rewritten below
         }
-        // B operand of w: k * exp(G) per element, into Ka (its gated copy is no longer needed)
-        for (int i = tid; i < kTile * (K / 8); i += 128) {
+        // B operand of w: k * exp(G) per element, into Ka (its gated copy is no longer needed); SPLITG made it
+        // over k with the gated copies
+        for (int i = tid; i < (SPLITG ? 0 : kTile * (K / 8)); i += 128) {
             const int r = i / (K / 8), lc = i % (K / 8);
             const uint32_t off = (uint32_t)((lc >> 3) * 8192 + r * 128 + (((lc & 7) ^ (r & 7)) << 4));
             const uint4 raw = *reinterpret_cast<const uint4*>(sm + L::kK + off);
@@ -555,10 +666,10 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
     for (int J = 0; J < 4; ++J)
 #pragma unroll
         for (int n = 0; n < 2; ++n) Xr[J][n][0] = Xr[J][n][1] = Xr[J][n][2] = Xr[J][n][3] = 0.f;
-    const uint32_t xs_base = s_base + L::kF + L::fXs;            // block (M, J) at xslot(M, J) * kXb: hi, then lo
+    const uint32_t xs_base = s_base + L::kScr + L::fXs;            // block (M, J) at xslot(M, J) * kXb: hi, then lo
     {
         // diagonal block: A_II to shared memory, 16 lanes invert it column by column in fp32
-        float* dA = reinterpret_cast<float*>(F + L::fD + warp * L::kDw);
+        float* dA = reinterpret_cast<float*>(sm + L::kScr + L::fD + warp * L::kDw);
         float* dX = dA + 16 * 17;
 #pragma unroll
         for (int J = 0; J < 4; ++J) {
@@ -623,7 +734,7 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
                 mma_block_split(Sb, ah, al, xb, xb + 512, mi, mr);
             }
             // X_IJ = -X_II S_IJ  (S_IJ back through this warp's block scratch as the B operand)
-            const uint32_t sb = s_base + L::kF + L::fSs + warp * L::kXb;
+            const uint32_t sb = s_base + L::kScr + L::fSs + warp * L::kXb;
             store_block_split(sb, sb + 512, Sb[0], Sb[1], mi, mr);
             __syncwarp();
             float Xb[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -690,7 +801,7 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
         bw::tc_fence_after();
         bw::tmem_dealloc(tmem, 128);
     }
-    const uint32_t tw_t = s_base + L::kF + 1024, tu_t = tw_t + 8192;   // T's [64][64] bf16 tiles
+    const uint32_t tw_t = s_base + L::kScr + 1024, tu_t = tw_t + 8192;   // T's [64][64] bf16 tiles
     static_assert(L::scratch >= 1024 + 2 * 8192, "the T tiles fit the solve's scratch");
 #pragma unroll
     for (int J = 0; J < 4; ++J) {
@@ -759,7 +870,7 @@ prepare_mma_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
         stage_out(tile, dcols, acc);
     };
     // w over the tile it reads (k, or its scaled copy Ka), then u over v
-    const uint32_t w_tile = PER_K ? L::kKa : L::kK;
+    const uint32_t w_tile = (PER_K && !SPLITG) ? L::kKa : L::kK;
     product_in_place(tw_t, s_base + w_tile, std::integral_constant<int, K>{});
     // w and P leave while u is formed (rows past T are clipped by the tensor maps)
     bw::fence_async_shared();
@@ -830,10 +941,10 @@ cudaError_t launch_prepare_v(const Dims& d, const void* q, const void* k, const 
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         return cudaLaunchKernelEx(&cfg, kern, mk, mv, mw, mu, mq, mp, g, (const bf16*)beta, g_cum, (bf16*)tinv, d.T,
-                                  d.H, d.G, pin, err);
+                                  d.H, d.G, pin, err, (const bf16*)k);
     }
     kern<<<grid, 128, smem, s>>>(mk, mv, mw, mu, mq, mp, g, (const bf16*)beta, g_cum, (bf16*)tinv, d.T, d.H, d.G,
-                                 pin, err);
+                                 pin, err, (const bf16*)k);
     return cudaGetLastError();
 }
 

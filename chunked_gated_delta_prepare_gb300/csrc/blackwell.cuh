@@ -288,6 +288,33 @@ __device__ __forceinline__ float load_io(const void* p) {
     if constexpr (F16) return __half2float(*reinterpret_cast<const __half*>(p));
     else return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(p));
 }
+template <bool F16>
+__device__ __forceinline__ void store_io(void* p, float x) {
+    if constexpr (F16) *reinterpret_cast<__half*>(p) = __float2half_rn(x);
+    else *reinterpret_cast<__nv_bfloat16*>(p) = __float2bfloat16_rn(x);
+}
+// A packed pair of the io type as fp32.
+template <bool F16>
+__device__ __forceinline__ float2 unpack2_io(uint32_t w) {
+    if constexpr (F16) return __half22float2(*reinterpret_cast<const __half2*>(&w));
+    else return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
+}
+// The eight io-type values of a 16-byte group as fp32, and eight fp32 values packed back.
+template <bool F16>
+__device__ __forceinline__ void unpack8_io(const uint4& raw, float* f) {
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float2 x = unpack2_io<F16>(w[e]);
+        f[2 * e] = x.x;
+        f[2 * e + 1] = x.y;
+    }
+}
+template <bool F16>
+__device__ __forceinline__ uint4 pack8_io(const float* f) {
+    return make_uint4(pack_io<F16>(f[0], f[1]), pack_io<F16>(f[2], f[3]), pack_io<F16>(f[4], f[5]),
+                      pack_io<F16>(f[6], f[7]));
+}
 
 }  // namespace bw
 }  // namespace gdr

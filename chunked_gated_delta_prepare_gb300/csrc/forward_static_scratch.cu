@@ -26,8 +26,8 @@
 //    allocation and the cached address is stale: a process that resets a device
 //    must not call this entry point on that device again.
 //  * Variant AUTO runs what gdr_forward's AUTO runs when the fused path is left
-//    out: the tensor-core stages for bf16 io, the CUDA-core stages for fp32 and
-//    fp16 io.
+//    out: the tensor-core stages for bf16 and fp16 io, the CUDA-core stages for
+//    fp32 io.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -67,7 +67,7 @@ extern "C" gdr_status gdr_forward_static_scratch(const gdr_problem* p, const voi
         return GDR_ERR_UNSUPPORTED;   // only the staged variants are offered here
     gdr_problem staged = *p;
     if (staged.variant == GDR_VARIANT_AUTO)
-        staged.variant = staged.io_dtype == GDR_BF16 ? GDR_VARIANT_TENSOR : GDR_VARIANT_SIMT;
+        staged.variant = staged.io_dtype == GDR_F32 ? GDR_VARIANT_SIMT : GDR_VARIANT_TENSOR;
     const size_t need = gdr_forward_workspace_bytes(&staged);
     if (need == 0) {
         // the problem itself is invalid: let gdr_forward report why, launching nothing

@@ -1,4 +1,4 @@
-// Fused state scan + chunk output for bf16 io and a scalar (per-head) gate:
+// Fused state scan + chunk output for bf16 or fp16 io and a scalar (per-head) gate:
 // given w, u and the chunk-local cumulative gate G (from the WY prepare),
 //
 //   scan   ("kernel_fun/kda/_kernels/bwd_scan.py", module docstring):
@@ -26,6 +26,8 @@
 // The two rings are separate so the output warps, which trail the recurrence,
 // never hold it back.  Tiles read by ldmatrix use 128-byte (w, k, q, P) or
 // 64-byte (u, h_c, v', o) XOR swizzles, so every access is conflict-free.
+// With fp16 io (F16) every operand and staged tile is fp16 in the same places; the state
+// and the accumulators stay fp32.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -95,7 +97,7 @@ struct FLayout {
 // the chunk-packed row; chunk c of sequence z reads q and k from packed row pcu[z] + c C, the rows past
 // the sequence's end in k are zeroed once they land (they hold the next sequence's tokens; their v' is
 // zero, but 0 * inf is not), and only o's rows inside the sequence are stored.
-template <int K, int C, bool HAS_P, bool GENERAL, bool PACKED>
+template <int K, int C, bool HAS_P, bool GENERAL, bool PACKED, bool F16>
 __global__ void __launch_bounds__(FLayout<K, C, HAS_P>::kThreads, 1)
 fused_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap mk,
                          const __grid_constant__ CUtensorMap mu, const __grid_constant__ CUtensorMap mq,
@@ -259,15 +261,15 @@ fused_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_co
             for (int j = 0; j < NT8; ++j) D[j][0] = D[j][1] = D[j][2] = D[j][3] = 0.f;
 #pragma unroll
             for (int kk = 0; kk < KH / 16; ++kk) {
-                const uint32_t a[4] = {wm::pack2(hT[2 * kk][0], hT[2 * kk][1]), wm::pack2(hT[2 * kk][2], hT[2 * kk][3]),
-                                       wm::pack2(hT[2 * kk + 1][0], hT[2 * kk + 1][1]),
-                                       wm::pack2(hT[2 * kk + 1][2], hT[2 * kk + 1][3])};
+                const uint32_t a[4] = {wm::pack2_io<F16>(hT[2 * kk][0], hT[2 * kk][1]), wm::pack2_io<F16>(hT[2 * kk][2], hT[2 * kk][3]),
+                                       wm::pack2_io<F16>(hT[2 * kk + 1][0], hT[2 * kk + 1][1]),
+                                       wm::pack2_io<F16>(hT[2 * kk + 1][2], hT[2 * kk + 1][3])};
 #pragma unroll
                 for (int jp = 0; jp < NT8; jp += 2) {
                     uint32_t bfr[4];
                     wm::ldsm_x4(w_t + sw128(8 * jp + 8 * (mi >> 1) + mr, d0 + 16 * kk + 8 * (mi & 1), C), bfr);
-                    wm::mma16816(D[jp], a, bfr[0], bfr[1]);
-                    wm::mma16816(D[jp + 1], a, bfr[2], bfr[3]);
+                    wm::mma16816_io<F16>(D[jp], a, bfr[0], bfr[1]);
+                    wm::mma16816_io<F16>(D[jp + 1], a, bfr[2], bfr[3]);
                 }
             }
 
@@ -277,8 +279,8 @@ fused_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_co
                 const uint32_t st = s_base + L::HC + hb * (K * kBV * 2);
 #pragma unroll
                 for (int j = 0; j < NJH; j += 2) {
-                    const uint32_t r[4] = {wm::pack2(hT[j][0], hT[j][1]), wm::pack2(hT[j][2], hT[j][3]),
-                                           wm::pack2(hT[j + 1][0], hT[j + 1][1]), wm::pack2(hT[j + 1][2], hT[j + 1][3])};
+                    const uint32_t r[4] = {wm::pack2_io<F16>(hT[j][0], hT[j][1]), wm::pack2_io<F16>(hT[j][2], hT[j][3]),
+                                           wm::pack2_io<F16>(hT[j + 1][0], hT[j + 1][1]), wm::pack2_io<F16>(hT[j + 1][2], hT[j + 1][3])};
                     wm::stsm_x4_t(st + sw64(d0 + 8 * j + 8 * (mi >> 1) + mr, 2 * vh + (mi & 1)), r);
                 }
             }
@@ -312,10 +314,10 @@ fused_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_co
             for (int jp = 0; jp < NT8; jp += 2) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const __nv_bfloat162 uv = *reinterpret_cast<const __nv_bfloat162*>(&ur[jp / 2][e]);
+                    const float2 uv = bw::unpack2_io<F16>(ur[jp / 2][e]);
                     float* dd = D[jp + (e >> 1)] + 2 * (e & 1);
-                    dd[0] = __bfloat162float(uv.x) - dd[0];
-                    dd[1] = __bfloat162float(uv.y) - dd[1];
+                    dd[0] = uv.x - dd[0];
+                    dd[1] = uv.y - dd[1];
                 }
             }
             // h^T[:, my keys] = exp(G_last) h^T + (v'^T diag(gamma)) k[:, my keys]
@@ -328,16 +330,16 @@ fused_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_co
             for (int kk = 0; kk < C / 16; ++kk) {
                 const float2 ga = *reinterpret_cast<const float2*>(sGam + s * C + 16 * kk + 2 * q4);
                 const float2 gb = *reinterpret_cast<const float2*>(sGam + s * C + 16 * kk + 8 + 2 * q4);
-                const uint32_t a[4] = {wm::pack2(D[2 * kk][0] * ga.x, D[2 * kk][1] * ga.y),
-                                       wm::pack2(D[2 * kk][2] * ga.x, D[2 * kk][3] * ga.y),
-                                       wm::pack2(D[2 * kk + 1][0] * gb.x, D[2 * kk + 1][1] * gb.y),
-                                       wm::pack2(D[2 * kk + 1][2] * gb.x, D[2 * kk + 1][3] * gb.y)};
+                const uint32_t a[4] = {wm::pack2_io<F16>(D[2 * kk][0] * ga.x, D[2 * kk][1] * ga.y),
+                                       wm::pack2_io<F16>(D[2 * kk][2] * ga.x, D[2 * kk][3] * ga.y),
+                                       wm::pack2_io<F16>(D[2 * kk + 1][0] * gb.x, D[2 * kk + 1][1] * gb.y),
+                                       wm::pack2_io<F16>(D[2 * kk + 1][2] * gb.x, D[2 * kk + 1][3] * gb.y)};
 #pragma unroll
                 for (int jp = 0; jp < NJH; jp += 2) {
                     uint32_t bfr[4];
                     wm::ldsm_x4_t(k_t + sw128(16 * kk + 8 * (mi & 1) + mr, d0 + 8 * jp + 8 * (mi >> 1), C), bfr);
-                    wm::mma16816(hT[jp], a, bfr[0], bfr[1]);
-                    wm::mma16816(hT[jp + 1], a, bfr[2], bfr[3]);
+                    wm::mma16816_io<F16>(hT[jp], a, bfr[0], bfr[1]);
+                    wm::mma16816_io<F16>(hT[jp + 1], a, bfr[2], bfr[3]);
                 }
             }
             __syncwarp();
@@ -348,8 +350,8 @@ fused_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_co
 #pragma unroll
                 for (int jp = 0; jp < NT8; jp += 2) {
                     if ((jp >= NT8 / 2) != (kh == 1)) continue;   // static register indices, runtime half
-                    const uint32_t r[4] = {wm::pack2(D[jp][0], D[jp][1]), wm::pack2(D[jp][2], D[jp][3]),
-                                           wm::pack2(D[jp + 1][0], D[jp + 1][1]), wm::pack2(D[jp + 1][2], D[jp + 1][3])};
+                    const uint32_t r[4] = {wm::pack2_io<F16>(D[jp][0], D[jp][1]), wm::pack2_io<F16>(D[jp][2], D[jp][3]),
+                                           wm::pack2_io<F16>(D[jp + 1][0], D[jp + 1][1]), wm::pack2_io<F16>(D[jp + 1][2], D[jp + 1][3])};
                     wm::stsm_x4_t(st + sw64(8 * jp + 8 * (mi >> 1) + mr, 2 * vh + (mi & 1)), r);
                 }
             }
@@ -410,8 +412,8 @@ fused_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_co
                     if (jp / 2 > ow) continue;           // key blocks above the diagonal are masked anyway
                     uint32_t bfr[4];
                     wm::ldsm_x4(pk_t + sw128(8 * jp + 8 * (mi >> 1) + mr, 16 * kk + 8 * (mi & 1), C), bfr);
-                    wm::mma16816(S[jp], qa[kk], bfr[0], bfr[1]);
-                    wm::mma16816(S[jp + 1], qa[kk], bfr[2], bfr[3]);
+                    wm::mma16816_io<F16>(S[jp], qa[kk], bfr[0], bfr[1]);
+                    wm::mma16816_io<F16>(S[jp + 1], qa[kk], bfr[2], bfr[3]);
                 }
             }
 #pragma unroll
@@ -427,10 +429,10 @@ fused_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_co
                     pv[hh][2] = j0 <= i1 ? S[jn][2] * __expf(Gi1 - Gj0) : 0.f;
                     pv[hh][3] = j0 + 1 <= i1 ? S[jn][3] * __expf(Gi1 - Gj1) : 0.f;
                 }
-                pa[kk][0] = wm::pack2(pv[0][0], pv[0][1]);
-                pa[kk][1] = wm::pack2(pv[0][2], pv[0][3]);
-                pa[kk][2] = wm::pack2(pv[1][0], pv[1][1]);
-                pa[kk][3] = wm::pack2(pv[1][2], pv[1][3]);
+                pa[kk][0] = wm::pack2_io<F16>(pv[0][0], pv[0][1]);
+                pa[kk][1] = wm::pack2_io<F16>(pv[0][2], pv[0][3]);
+                pa[kk][2] = wm::pack2_io<F16>(pv[1][0], pv[1][1]);
+                pa[kk][3] = wm::pack2_io<F16>(pv[1][2], pv[1][3]);
             }
         }
         // o = exp(G_i) (q h_c) + P v'   [16 x 32]
@@ -446,8 +448,8 @@ fused_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_co
             for (int jp = 0; jp < 4; jp += 2) {
                 uint32_t bfr[4];
                 wm::ldsm_x4_t(hc_t + sw64(16 * kk + 8 * (mi & 1) + mr, jp + (mi >> 1)), bfr);
-                wm::mma16816(acc[jp], qa[kk], bfr[0], bfr[1]);
-                wm::mma16816(acc[jp + 1], qa[kk], bfr[2], bfr[3]);
+                wm::mma16816_io<F16>(acc[jp], qa[kk], bfr[0], bfr[1]);
+                wm::mma16816_io<F16>(acc[jp + 1], qa[kk], bfr[2], bfr[3]);
             }
         }
         {
@@ -462,8 +464,8 @@ fused_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_co
             for (int jp = 0; jp < 4; jp += 2) {
                 uint32_t bfr[4];
                 wm::ldsm_x4_t(vp_t + sw64(16 * kk + 8 * (mi & 1) + mr, jp + (mi >> 1)), bfr);
-                wm::mma16816(acc[jp], pa[kk], bfr[0], bfr[1]);
-                wm::mma16816(acc[jp + 1], pa[kk], bfr[2], bfr[3]);
+                wm::mma16816_io<F16>(acc[jp], pa[kk], bfr[0], bfr[1]);
+                wm::mma16816_io<F16>(acc[jp + 1], pa[kk], bfr[2], bfr[3]);
             }
         }
         __syncwarp();
@@ -474,10 +476,10 @@ fused_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_co
         // o * scale -> bf16 staging [16][32] -> 16-byte global stores
 #pragma unroll
         for (int jp = 0; jp < 4; jp += 2) {
-            const uint32_t r[4] = {wm::pack2(acc[jp][0] * scale, acc[jp][1] * scale),
-                                   wm::pack2(acc[jp][2] * scale, acc[jp][3] * scale),
-                                   wm::pack2(acc[jp + 1][0] * scale, acc[jp + 1][1] * scale),
-                                   wm::pack2(acc[jp + 1][2] * scale, acc[jp + 1][3] * scale)};
+            const uint32_t r[4] = {wm::pack2_io<F16>(acc[jp][0] * scale, acc[jp][1] * scale),
+                                   wm::pack2_io<F16>(acc[jp][2] * scale, acc[jp][3] * scale),
+                                   wm::pack2_io<F16>(acc[jp + 1][0] * scale, acc[jp + 1][1] * scale),
+                                   wm::pack2_io<F16>(acc[jp + 1][2] * scale, acc[jp + 1][3] * scale)};
             asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(
                              os + sw64(8 * (mi & 1) + mr, jp + (mi >> 1))),
                          "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
@@ -497,7 +499,7 @@ fused_scan_output_kernel(const __grid_constant__ CUtensorMap mw, const __grid_co
     (void)ok;
 }
 
-template <int K, int C, bool HAS_P, bool GENERAL, bool PACKED>
+template <int K, int C, bool HAS_P, bool GENERAL, bool PACKED, bool F16>
 cudaError_t launch_v(const Dims& d, const void* q, const void* k, const void* w, const void* u, const float* g_cum,
                      const void* P, const float* h0, void* o, float* h_final, const int* co, int nseq,
                      const int* pcu, int Tin, cudaStream_t s, unsigned int* err) {
@@ -516,7 +518,7 @@ cudaError_t launch_v(const Dims& d, const void* q, const void* k, const void* w,
     } else {
         mpk = mk;
     }
-    auto kern = fused_scan_output_kernel<K, C, HAS_P, GENERAL, PACKED>;
+    auto kern = fused_scan_output_kernel<K, C, HAS_P, GENERAL, PACKED, F16>;
     const size_t smem = L::bytes + 1024;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -530,19 +532,28 @@ template <int K, int C, bool HAS_P>
 cudaError_t launch(const Dims& d, const void* q, const void* k, const void* w, const void* u, const float* g_cum,
                    const void* P, const float* h0, void* o, float* h_final, const int* co, int nseq,
                    const int* pcu, int Tin, cudaStream_t s, unsigned int* err) {
+    if (d.f16) {   // fp16 io: one unpacked form per shape (the guarded one serves whole chunks too)
+        if (pcu) return cudaErrorInvalidValue;
+        if (d.T % C != 0 || d.G != 1)
+            return launch_v<K, C, HAS_P, true, false, true>(d, q, k, w, u, g_cum, P, h0, o, h_final, co, nseq, nullptr,
+                                                            0, s, err);
+        return launch_v<K, C, HAS_P, false, false, true>(d, q, k, w, u, g_cum, P, h0, o, h_final, co, nseq, nullptr, 0,
+                                                         s, err);
+    }
     if constexpr (HAS_P) {   // packed q, k, o (pcu) only with P
         if (pcu) {
             if (d.T % C != 0 || d.G != 1)
-                return launch_v<K, C, true, true, true>(d, q, k, w, u, g_cum, P, h0, o, h_final, co, nseq, pcu, Tin, s,
-                                                        err);
-            return launch_v<K, C, true, false, true>(d, q, k, w, u, g_cum, P, h0, o, h_final, co, nseq, pcu, Tin, s,
-                                                     err);
+                return launch_v<K, C, true, true, true, false>(d, q, k, w, u, g_cum, P, h0, o, h_final, co, nseq, pcu,
+                                                               Tin, s, err);
+            return launch_v<K, C, true, false, true, false>(d, q, k, w, u, g_cum, P, h0, o, h_final, co, nseq, pcu,
+                                                            Tin, s, err);
         }
     }
     if (d.T % C != 0 || d.G != 1)
-        return launch_v<K, C, HAS_P, true, false>(d, q, k, w, u, g_cum, P, h0, o, h_final, co, nseq, nullptr, 0, s,
-                                                  err);
-    return launch_v<K, C, HAS_P, false, false>(d, q, k, w, u, g_cum, P, h0, o, h_final, co, nseq, nullptr, 0, s, err);
+        return launch_v<K, C, HAS_P, true, false, false>(d, q, k, w, u, g_cum, P, h0, o, h_final, co, nseq, nullptr, 0,
+                                                         s, err);
+    return launch_v<K, C, HAS_P, false, false, false>(d, q, k, w, u, g_cum, P, h0, o, h_final, co, nseq, nullptr, 0,
+                                                      s, err);
 }
 
 }  // namespace
@@ -550,7 +561,7 @@ cudaError_t launch(const Dims& d, const void* q, const void* k, const void* w, c
 cudaError_t mma_scan_output(const Dims& d, const void* q, const void* k, const void* w, const void* u,
                             const float* g_cum, const void* P, const float* h0, void* o, float* h_final,
                             cudaStream_t s, unsigned int* err, const int* co, int nseq, const int* pcu, int Tin) {
-    if (!d.bf16 || d.per_k || (co && (d.B != 1 || nseq < 1))) return cudaErrorInvalidValue;
+    if (!(d.bf16 || d.f16) || d.per_k || (co && (d.B != 1 || nseq < 1))) return cudaErrorInvalidValue;
     if (pcu && (!co || !P || Tin < 1)) return cudaErrorInvalidValue;
     if (P) {
         if (d.C != 64) return cudaErrorInvalidValue;

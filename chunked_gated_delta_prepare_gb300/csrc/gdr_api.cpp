@@ -48,7 +48,7 @@ gdr_status check_problem(const gdr_problem* p, gdr::Dims* d) {
     d->NT = (d->T + d->C - 1) / d->C;   // a last, partial chunk counts
     d->per_k = p->gate == GDR_GATE_PER_K;
     d->bf16 = p->io_dtype == GDR_BF16;
-    d->f16 = p->io_dtype == GDR_F16;   // runs the CUDA-core kernels only
+    d->f16 = p->io_dtype == GDR_F16;
     d->scale = p->scale > 0.f ? p->scale : 1.0f / std::sqrt((float)p->K);
     return GDR_OK;
 }
@@ -65,17 +65,17 @@ gdr_status check_ptrs(std::initializer_list<const void*> required, std::initiali
 
 gdr_status from_cuda(cudaError_t e) { return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA; }
 
-// A single stage runs its bf16 tensor-core kernel unless SIMT is asked for.
+// A single stage runs its tensor-core kernel (bf16 or fp16 io) unless SIMT is asked for.
 gdr_status pick_stage(const gdr_problem* p, const gdr::Dims& d, bool* tensor) {
     switch (p->variant) {
         case GDR_VARIANT_SIMT: *tensor = false; return GDR_OK;
         case GDR_VARIANT_TENSOR:
         case GDR_VARIANT_FUSED:
         case GDR_VARIANT_FUSED_TC:
-            if (!d.bf16) return GDR_ERR_UNSUPPORTED;
+            if (!d.bf16 && !d.f16) return GDR_ERR_UNSUPPORTED;
             *tensor = true;
             return GDR_OK;
-        case GDR_VARIANT_AUTO: *tensor = d.bf16 != 0; return GDR_OK;
+        case GDR_VARIANT_AUTO: *tensor = d.bf16 || d.f16; return GDR_OK;
         default: return GDR_ERR_UNSUPPORTED;
     }
 }
@@ -87,17 +87,18 @@ constexpr int kPieceChunks = 64;   // the overlapped forward's chunks per piece,
 bool segments_apply(const gdr_problem* p, const gdr::Dims& d);
 
 // The path a whole forward takes: SIMT (fp32 CUDA-core kernels for every stage),
-// TENSOR (the three bf16 tensor-core stage kernels) or FUSED (the bf16 prepare,
-// then scan and output in one kernel; scalar gate only).
+// TENSOR (the three tensor-core stage kernels, bf16 or fp16 io) or FUSED (the
+// prepare, then scan and output in one kernel; scalar gate only).
 gdr_status pick_forward(const gdr_problem* p, const gdr::Dims& d, Path* path) {
+    const bool io16 = d.bf16 || d.f16;
     switch (p->variant) {
         case GDR_VARIANT_SIMT: *path = Path::Simt; return GDR_OK;
         case GDR_VARIANT_TENSOR:
-            if (!d.bf16) return GDR_ERR_UNSUPPORTED;
+            if (!io16) return GDR_ERR_UNSUPPORTED;
             *path = Path::Tensor;
             return GDR_OK;
         case GDR_VARIANT_FUSED:
-            if (!d.bf16 || d.per_k) return GDR_ERR_UNSUPPORTED;
+            if (!io16 || d.per_k) return GDR_ERR_UNSUPPORTED;
             *path = Path::Fused;
             return GDR_OK;
         case GDR_VARIANT_FUSED_TC:
@@ -113,10 +114,9 @@ gdr_status pick_forward(const gdr_problem* p, const gdr::Dims& d, Path* path) {
             // pieces overlapped with the prepare (see forward_tc_overlapped).
             // A per-key-dim gate at K = V = 128, C = 64 takes the tcgen05 form too (its gated operands from
             // their own kernel) unless the segment-parallel scan applies.
-            // fp16 io: the tcgen05 form where it is built (scalar gate, K = V = 128, C = 64), else the
-            // CUDA-core path.
-            if (d.f16) *path = gdr::tc_scan_output_supported(d) ? Path::FusedTc : Path::Simt;
-            else if (!d.bf16) *path = Path::Simt;
+            // fp16 io follows the same rules; its tcgen05 form takes a scalar gate only (see
+            // tc_scan_output_supported), so a per-key-dim gate runs the staged kernels.
+            if (!io16) *path = Path::Simt;
             else if (!d.per_k && d.C == 64)
                 *path = gdr::tc_scan_output_supported(d) &&
                                 ((int64_t)d.B * d.H * (d.V / 32) > kSmCount || (d.B == 1 && d.NT >= 2 * kPieceChunks &&
@@ -872,7 +872,7 @@ gdr_status gdr_scan_output(const gdr_problem* p, const void* q, const void* k, c
     gdr_status st = check_problem(p, &d);
     if (st != GDR_OK) return st;
     if ((st = check_ptrs({q, k, w, u, g_cum, o}, {P, h0, h_final})) != GDR_OK) return st;
-    if (p->variant == GDR_VARIANT_SIMT || !d.bf16 || (P && d.C != 64)) return GDR_ERR_UNSUPPORTED;
+    if (p->variant == GDR_VARIANT_SIMT || !(d.bf16 || d.f16) || (P && d.C != 64)) return GDR_ERR_UNSUPPORTED;
     // a per-key-dim gate: the tcgen05 kernel only, on gdr_gated_operands' P, qg and kg
     if (d.per_k && (p->variant != GDR_VARIANT_FUSED_TC || !P)) return GDR_ERR_UNSUPPORTED;
     // the tcgen05 kernel for variant FUSED_TC, and for AUTO where gdr_forward would take it
@@ -910,7 +910,7 @@ gdr_status gdr_prepare_wyp(const gdr_problem* p, const void* q, const void* k, c
     gdr_status st = check_problem(p, &d);
     if (st != GDR_OK) return st;
     if ((st = check_ptrs({q, k, v, g, beta, w, u, g_cum, P}, {})) != GDR_OK) return st;
-    if (p->variant == GDR_VARIANT_SIMT || !d.bf16 || d.per_k || d.C != 64) return GDR_ERR_UNSUPPORTED;
+    if (p->variant == GDR_VARIANT_SIMT || !(d.bf16 || d.f16) || d.per_k || d.C != 64) return GDR_ERR_UNSUPPORTED;
     st = from_cuda(gdr::mma_prepare(d, k, v, g, beta, w, u, g_cum, (cudaStream_t)stream, device_error_word(), q, P));
     if (st == GDR_OK) t_last_variant = "tensor";
     return st;
@@ -1275,8 +1275,8 @@ gdr_status gdr_varlen_forward(const gdr_problem* p_in, const int32_t* cu_seqlens
         return st;
     Path path;
     if ((st = pick_forward(p, d, &path)) != GDR_OK) return st;
-    if (path == Path::FusedTc)   // packed sequences: the warp-level fused kernel, or the staged one (KDA);
-        path = d.f16 ? Path::Simt : d.per_k ? Path::Tensor : Path::Fused;   // fp16: the CUDA-core path
+    if (path == Path::FusedTc)   // packed sequences: the warp-level fused kernel, or the staged one (KDA)
+        path = d.per_k ? Path::Tensor : Path::Fused;
     char* base = static_cast<char*>(workspace);
     int64_t rb[11];
     varlen_rows(d, false, rb);
@@ -1286,8 +1286,9 @@ gdr_status gdr_varlen_forward(const gdr_problem* p_in, const int32_t* cu_seqlens
     const gdr::RowCopy out[1] = {{base + ws.pad[5], o, rb[5]}};
     int64_t chunks = 0;   // the chunk-packed row's chunks, from the host lengths
     for (int64_t i = 0; i < d.B; ++i) chunks += ((int64_t)cu_seqlens[i + 1] - cu_seqlens[i] + d.C - 1) / d.C;
-    if (path == Path::Fused && d.C == 64 && chunk_packed_fits(d) && chunks > 0) {
-        // the fused path reads q, k, v, g, beta in place and writes o in place: no copies
+    if (path == Path::Fused && d.bf16 && d.C == 64 && chunk_packed_fits(d) && chunks > 0) {
+        // the fused path reads q, k, v, g, beta in place and writes o in place: no copies (bf16; fp16
+        // takes the chunk-packed copies below)
         int* co = reinterpret_cast<int*>(base + ws.co);
         int* cs = reinterpret_cast<int*>(base + ws.cs);
         const gdr::Dims d1 = chunk_packed(d, chunks);

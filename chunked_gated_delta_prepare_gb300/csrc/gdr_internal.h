@@ -27,7 +27,7 @@ cudaError_t simt_scan(const Dims& d, const void* k, const void* w, const void* u
 cudaError_t simt_output(const Dims& d, const void* q, const void* k, const void* v_new, const void* h_ckpt,
                         const float* g_cum, void* o, cudaStream_t s);
 
-// ---- tensor-core kernels (bf16 io only)
+// ---- tensor-core kernels (bf16 io; the forward's also fp16 io, with d.f16)
 // with q and P non-NULL (scalar gate, C = 64) it also writes P = tril_0(q k^T * exp(G_i - G_j))
 // per chunk as [B, NT, H, C, C] bf16; with tinv non-NULL, (I + A)^{-1} per chunk, [B, NT, H, C, C] bf16
 // pdl: launch as the programmatic dependent of the stream's previous kernel (see gdr_api.cpp's overlapped
@@ -38,6 +38,10 @@ cudaError_t simt_output(const Dims& d, const void* q, const void* k, const void*
 cudaError_t mma_prepare(const Dims& d, const void* k, const void* v, const float* g, const void* beta, void* w,
                         void* u, float* g_cum, cudaStream_t s, unsigned int* err, const void* q = nullptr,
                         void* P = nullptr, void* tinv = nullptr, bool pdl = false, bool tc_scores = false);
+// mma_prepare for fp16 io (d.f16): every shape and gate of the bf16 forms, no inverse.
+cudaError_t mma_prepare_f16(const Dims& d, const void* k, const void* v, const float* g, const void* beta, void* w,
+                            void* u, float* g_cum, cudaStream_t s, unsigned int* err, const void* q, void* P,
+                            void* tinv, bool pdl, bool tc_scores);
 // The prepare with P (scalar gate, C = 64) on the chunk-packed row d (B = 1) of packed variable-length
 // sequences, reading q, k, v, g, beta in place from the caller's packed tensors of `total` tokens: chunk c of
 // the row is chunk c - co[s] of sequence s = cs[c] (cu, co, cs as varlen_plan makes them).  w, u, g_cum and

@@ -1,4 +1,4 @@
-// State scan for bf16 io with the recurrence in registers (the re-scan of
+// State scan for bf16 and fp16 io with the recurrence in registers (the re-scan of
 // "kernel_fun/kda/_kernels/bwd_scan.py", module docstring: hck[c] = h before the
 // update, v' = u - w h, h = exp(decay) h + kg^T v').
 //
@@ -26,6 +26,8 @@
 // and k 128-byte swizzled, the staging XOR-swizzled, so every ldmatrix and
 // stmatrix is free of bank conflicts.  The ring's full barrier for chunk c+1 is
 // tested (non-blocking) in the middle of chunk c, so its latency stays off the chain.
+// With fp16 io (F16) every operand, checkpoint and v' is fp16 in the same places; the
+// state stays fp32.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -87,7 +89,7 @@ struct MScanLayout {
 // co (packed variable-length sequences; NULL otherwise): the tensors hold one row (B = 1) of whole-chunk
 // runs, sequence z on the chunks co[z] .. co[z+1]-1; blockIdx.z is the sequence, whose state starts from
 // h0[z] and ends in h_final[z].  Checkpoints and v' land at the chunks' places in the row.
-template <int K, int C, bool PER_K, bool GENERAL, bool TRANSFER>
+template <int K, int C, bool PER_K, bool GENERAL, bool TRANSFER, bool F16>
 __global__ void __launch_bounds__(MScanLayout<K, C, PER_K, TRANSFER>::kThreads, TRANSFER && !PER_K ? 2 : 1)
 scan_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap mk,
                 const __grid_constant__ CUtensorMap mu, const bf16* __restrict__ k, const float* __restrict__ g_cum,
@@ -210,14 +212,12 @@ scan_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ 
 #pragma unroll
                 for (int j = 0; j < NI; ++j) {
                     const int t = r0 + j * RSTEP;
-                    const bf16* kv = reinterpret_cast<const bf16*>(&st.kr[j]);
                     float f[8];
+                    bw::unpack8_io<F16>(st.kr[j], f);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) f[e] = __bfloat162float(kv[e]) * __expf(st.gl8[e] - st.gr[j][e]);
-                    uint4 p;
-                    p.x = bw::pack_bf16(f[0], f[1]); p.y = bw::pack_bf16(f[2], f[3]);
-                    p.z = bw::pack_bf16(f[4], f[5]); p.w = bw::pack_bf16(f[6], f[7]);
-                    *reinterpret_cast<uint4*>(kg_t + (lc >> 3) * C * 128 + t * 128 + (((lc & 7) ^ (t & 7)) << 4)) = p;
+                    for (int e = 0; e < 8; ++e) f[e] *= __expf(st.gl8[e] - st.gr[j][e]);
+                    *reinterpret_cast<uint4*>(kg_t + (lc >> 3) * C * 128 + t * 128 + (((lc & 7) ^ (t & 7)) << 4)) =
+                        bw::pack8_io<F16>(f);
                 }
                 bw::fence_async_shared();
                 bw::mbar_arrive(&full[s]);
@@ -285,16 +285,17 @@ scan_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ 
         for (int j = 0; j < NT8; ++j) D[j][0] = D[j][1] = D[j][2] = D[j][3] = 0.f;
 #pragma unroll
         for (int kk = 0; kk < KH / 16; ++kk) {
-            const uint32_t a[4] = {wm::pack2(hT[2 * kk][0], hT[2 * kk][1]), wm::pack2(hT[2 * kk][2], hT[2 * kk][3]),
-                                   wm::pack2(hT[2 * kk + 1][0], hT[2 * kk + 1][1]),
-                                   wm::pack2(hT[2 * kk + 1][2], hT[2 * kk + 1][3])};
+            const uint32_t a[4] = {wm::pack2_io<F16>(hT[2 * kk][0], hT[2 * kk][1]),
+                                   wm::pack2_io<F16>(hT[2 * kk][2], hT[2 * kk][3]),
+                                   wm::pack2_io<F16>(hT[2 * kk + 1][0], hT[2 * kk + 1][1]),
+                                   wm::pack2_io<F16>(hT[2 * kk + 1][2], hT[2 * kk + 1][3])};
 #pragma unroll
             for (int jp = 0; jp < NT8; jp += 2) {
                 const int t = 8 * jp + 8 * (mi >> 1) + mr, d = d0 + 16 * kk + 8 * (mi & 1);
                 uint32_t bfr[4];
                 wm::ldsm_x4(w_t + (d >> 6) * C * 128 + t * 128 + ((((d & 63) >> 3) ^ (t & 7)) << 4), bfr);
-                wm::mma16816(D[jp], a, bfr[0], bfr[1]);
-                wm::mma16816(D[jp + 1], a, bfr[2], bfr[3]);
+                wm::mma16816_io<F16>(D[jp], a, bfr[0], bfr[1]);
+                wm::mma16816_io<F16>(D[jp + 1], a, bfr[2], bfr[3]);
             }
         }
 
@@ -302,8 +303,9 @@ scan_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ 
         if (h_ckpt) {
 #pragma unroll
             for (int j = 0; j < NJH; j += 2) {
-                const uint32_t r[4] = {wm::pack2(hT[j][0], hT[j][1]), wm::pack2(hT[j][2], hT[j][3]),
-                                       wm::pack2(hT[j + 1][0], hT[j + 1][1]), wm::pack2(hT[j + 1][2], hT[j + 1][3])};
+                const uint32_t r[4] = {wm::pack2_io<F16>(hT[j][0], hT[j][1]), wm::pack2_io<F16>(hT[j][2], hT[j][3]),
+                                       wm::pack2_io<F16>(hT[j + 1][0], hT[j + 1][1]),
+                                       wm::pack2_io<F16>(hT[j + 1][2], hT[j + 1][3])};
                 wm::stsm_x4_t(st_h + stage_off(8 * j + 8 * (mi >> 1) + mr, mi & 1), r);
             }
             __syncwarp();
@@ -350,10 +352,10 @@ scan_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ 
         for (int jp = 0; jp < NT8; jp += 2) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const __nv_bfloat162 uv = *reinterpret_cast<const __nv_bfloat162*>(&ur[jp / 2][e]);
+                const float2 uv = bw::unpack2_io<F16>(ur[jp / 2][e]);
                 float* dd = D[jp + (e >> 1)] + 2 * (e & 1);
-                dd[0] = __bfloat162float(uv.x) - dd[0];
-                dd[1] = __bfloat162float(uv.y) - dd[1];
+                dd[0] = uv.x - dd[0];
+                dd[1] = uv.y - dd[1];
             }
         }
 
@@ -378,17 +380,17 @@ scan_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ 
                 const float2 gb = *reinterpret_cast<const float2*>(sGam + s * C + 16 * kk + 8 + 2 * q4);
                 x0 = ga.x; x1 = ga.y; y0 = gb.x; y1 = gb.y;
             }
-            const uint32_t a[4] = {wm::pack2(D[2 * kk][0] * x0, D[2 * kk][1] * x1),
-                                   wm::pack2(D[2 * kk][2] * x0, D[2 * kk][3] * x1),
-                                   wm::pack2(D[2 * kk + 1][0] * y0, D[2 * kk + 1][1] * y1),
-                                   wm::pack2(D[2 * kk + 1][2] * y0, D[2 * kk + 1][3] * y1)};
+            const uint32_t a[4] = {wm::pack2_io<F16>(D[2 * kk][0] * x0, D[2 * kk][1] * x1),
+                                   wm::pack2_io<F16>(D[2 * kk][2] * x0, D[2 * kk][3] * x1),
+                                   wm::pack2_io<F16>(D[2 * kk + 1][0] * y0, D[2 * kk + 1][1] * y1),
+                                   wm::pack2_io<F16>(D[2 * kk + 1][2] * y0, D[2 * kk + 1][3] * y1)};
 #pragma unroll
             for (int jp = 0; jp < NJH; jp += 2) {
                 const int t = 16 * kk + 8 * (mi & 1) + mr, d = d0 + 8 * jp + 8 * (mi >> 1);
                 uint32_t bfr[4];
                 wm::ldsm_x4_t(k_t + (d >> 6) * C * 128 + t * 128 + ((((d & 63) >> 3) ^ (t & 7)) << 4), bfr);
-                wm::mma16816(hT[jp], a, bfr[0], bfr[1]);
-                wm::mma16816(hT[jp + 1], a, bfr[2], bfr[3]);
+                wm::mma16816_io<F16>(hT[jp], a, bfr[0], bfr[1]);
+                wm::mma16816_io<F16>(hT[jp + 1], a, bfr[2], bfr[3]);
             }
         }
         __syncwarp();
@@ -400,8 +402,9 @@ scan_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ 
             for (int jp = 0; jp < NT8; jp += 2) {
                 if ((jp >= NT8 / 2) != (kh == 1)) continue;   // static register indices, runtime half
                 const int jq = jp - kh * (NT8 / 2);
-                const uint32_t r[4] = {wm::pack2(D[jp][0], D[jp][1]), wm::pack2(D[jp][2], D[jp][3]),
-                                       wm::pack2(D[jp + 1][0], D[jp + 1][1]), wm::pack2(D[jp + 1][2], D[jp + 1][3])};
+                const uint32_t r[4] = {wm::pack2_io<F16>(D[jp][0], D[jp][1]), wm::pack2_io<F16>(D[jp][2], D[jp][3]),
+                                       wm::pack2_io<F16>(D[jp + 1][0], D[jp + 1][1]),
+                                       wm::pack2_io<F16>(D[jp + 1][2], D[jp + 1][3])};
                 wm::stsm_x4_t(st_v + stage_off(8 * jq + 8 * (mi >> 1) + mr, mi & 1), r);
             }
             __syncwarp();
@@ -432,7 +435,7 @@ scan_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ 
     (void)ok;
 }
 
-template <int K, int C, bool PER_K, bool GENERAL, bool TRANSFER>
+template <int K, int C, bool PER_K, bool GENERAL, bool TRANSFER, bool F16>
 cudaError_t launch_v(const Dims& d, const void* k, const void* w, const void* u, const float* g_cum, const float* h0,
                      void* h_ckpt, void* v_new, float* h_final, float* m_out, const int* co, int nseq, cudaStream_t s,
                      unsigned int* err) {
@@ -441,7 +444,7 @@ cudaError_t launch_v(const Dims& d, const void* k, const void* w, const void* u,
     if (!make_tmap_tokens(&mw, w, d.B, d.T, d.H, K, C) || !make_tmap_tokens(&mk, k, d.B, d.T, d.Hk, K, C) ||
         !make_tmap_tokens_sw64(&mu, u, d.B, d.T, d.H, d.V, C))
         return cudaErrorInvalidValue;
-    auto kern = scan_mma_kernel<K, C, PER_K, GENERAL, TRANSFER>;
+    auto kern = scan_mma_kernel<K, C, PER_K, GENERAL, TRANSFER, F16>;
     const size_t smem = L::bytes + 1024;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -455,11 +458,20 @@ template <int K, int C, bool PER_K, bool TRANSFER>
 cudaError_t launch(const Dims& d, const void* k, const void* w, const void* u, const float* g_cum, const float* h0,
                    void* h_ckpt, void* v_new, float* h_final, float* m_out, const int* co, int nseq, cudaStream_t s,
                    unsigned int* err) {
+    if constexpr (!TRANSFER) {   // fp16 io: the scan proper (the segment maps are bf16 only)
+        if (d.f16) {
+            if (d.T % C != 0 || d.G != 1)
+                return launch_v<K, C, PER_K, true, false, true>(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, m_out,
+                                                                co, nseq, s, err);
+            return launch_v<K, C, PER_K, false, false, true>(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, m_out, co,
+                                                             nseq, s, err);
+        }
+    }
     if (d.T % C != 0 || d.G != 1)
-        return launch_v<K, C, PER_K, true, TRANSFER>(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, m_out, co, nseq,
-                                                     s, err);
-    return launch_v<K, C, PER_K, false, TRANSFER>(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, m_out, co, nseq, s,
-                                                  err);
+        return launch_v<K, C, PER_K, true, TRANSFER, false>(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, m_out, co,
+                                                            nseq, s, err);
+    return launch_v<K, C, PER_K, false, TRANSFER, false>(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, m_out, co,
+                                                         nseq, s, err);
 }
 
 template <bool TRANSFER>
@@ -483,7 +495,7 @@ cudaError_t dispatch(const Dims& d, const void* k, const void* w, const void* u,
 cudaError_t mma_scan(const Dims& d, const void* k, const void* w, const void* u, const float* g_cum, const float* h0,
                      void* h_ckpt, void* v_new, float* h_final, cudaStream_t s, unsigned int* err, const int* co,
                      int nseq) {
-    if (!d.bf16 || (co && (d.B != 1 || nseq < 1))) return cudaErrorInvalidValue;
+    if (!(d.bf16 || d.f16) || (co && (d.B != 1 || nseq < 1))) return cudaErrorInvalidValue;
     return dispatch<false>(d, k, w, u, g_cum, h0, h_ckpt, v_new, h_final, nullptr, co, nseq, s, err);
 }
 

@@ -1,4 +1,4 @@
-// Tensor-core chunk output for bf16 io:
+// Tensor-core chunk output for bf16 and fp16 io:
 //     o = scale * [ (q * exp(G)) h_c + tril_0(Q~) v' ],   Q~_ij = sum_d q_id k_jd exp(G_id - G_jd)
 // (the output assembly that the re-scan page, "kernel_fun/kda/_kernels/bwd_scan.py",
 // says the forward's epilogue warps performed).
@@ -15,6 +15,10 @@
 // OPS (per-key-dim gate, K = V = 128, C = 64): the gated operands of the tcgen05 scan and output kernel
 // instead of o.  The CTA forms P and q exp(G) as above, and kg = k exp(G_last - G) beside the gated copy of
 // k (G_last the chunk's last row), and stores the three by TMA: no v', no checkpoints, no MMA 2 or 3.
+//
+// F16 (fp16 io; not with OPS): q, k, v', the checkpoints, P, q exp(G) and o are fp16, MMA 2 and 3 take
+// fp16 operands.  A per-key-dim gate's gated copies for S stay bf16 (their factors reach e^40, past
+// fp16's range), so MMA 1 is bf16 there and fp16 for a scalar gate.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -56,7 +60,7 @@ struct OutLayout {
 
 // OPS: mp is the P store map (otherwise unused), kg_out and qg_out [B, T, H, K] the gated operands'
 // outputs (otherwise null).
-template <int K, int V, int C, bool PER_K, bool OPS = false>
+template <int K, int V, int C, bool PER_K, bool OPS = false, bool F16 = false>
 __global__ void __launch_bounds__(128, OPS ? 4 : 1)
 tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                  const __grid_constant__ CUtensorMap mvp, const __grid_constant__ CUtensorMap mh,
@@ -65,6 +69,7 @@ tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
                  int NT, int G, float scale, unsigned int* err, bf16* __restrict__ kg_out = nullptr,
                  bf16* __restrict__ qg_out = nullptr) {
     static_assert(!OPS || (PER_K && C == 64 && K == V), "gated operands: per-key-dim gate, one chunk per tile");
+    static_assert(!(OPS && F16), "gated operands: bf16 io");
     using L = OutLayout<K, V, C, PER_K, OPS>;
     constexpr int GW = L::GW;
     extern __shared__ unsigned char smem_raw[];
@@ -183,9 +188,9 @@ tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
             const uint32_t off = (uint32_t)((lc >> 3) * 8192 + r * 128 + (((lc & 7) ^ (r & 7)) << 4));
             const uint4 rq = *reinterpret_cast<const uint4*>(sm + L::Q + off);
             const uint4 rk = *reinterpret_cast<const uint4*>(sm + L::Kt + off);
-            const bf16* qv = reinterpret_cast<const bf16*>(&rq);
-            const bf16* kv = reinterpret_cast<const bf16*>(&rk);
-            float fa[8], fb[8], gr[8], gf[8];
+            float qv[8], kv[8], fa[8], fb[8], gr[8], gf[8];
+            bw::unpack8_io<F16>(rq, qv);
+            bw::unpack8_io<F16>(rk, kv);
             unpack8(ga[j], gr);
             unpack8(L::NCH > 1 && r >= C ? gref[L::NCH - 1] : gref[0], gf);
             bool big = false;
@@ -195,7 +200,7 @@ tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
                 const float dg = gr[e] - gf[e];
                 const bool far = fabsf(dg) > kExpSafe;
                 big |= far;
-                const float xq = __bfloat162float(qv[e]), xk = __bfloat162float(kv[e]);
+                const float xq = qv[e], xk = kv[e];
                 fa[e] = xq * __expf(fminf(fmaxf(dg, -kExpClamp), kExpClamp));
                 fb[e] = xk * __expf(fminf(fmaxf(-dg, -kExpClamp), kExpClamp));
                 if constexpr (OPS) {
@@ -237,7 +242,7 @@ tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
     // MMA 1: S = q k^T
     if (tid == 0 && ok) {
         bw::tc_fence_after();
-        constexpr uint32_t idesc = bw::idesc_bf16(64, 64, 0, 0);
+        constexpr uint32_t idesc = bw::idesc_io(64, 64, 0, 0, F16 && !PER_K);   // gated copies: bf16
         const uint32_t a_t = s_base + (PER_K ? L::Qa : L::Q);
         const uint32_t b_t = s_base + L::Kt;
 #pragma unroll
@@ -247,7 +252,7 @@ tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
     ok = ok && bw::mbar_wait(&bar_mma, 0, err, kDeviceErrTimeout);
     bw::tc_fence_after();
 
-    // P = tril_0(S * gate) -> bf16 K-major [64][64]
+    // P = tril_0(S * gate) -> io type, K-major [64][64]
     {
         const int r = m64_row(warp, lane);
         float s[64];
@@ -269,10 +274,7 @@ tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
                     }
                     pv[e] = x;
                 }
-                uint4 p;
-                p.x = bw::pack_bf16(pv[0], pv[1]); p.y = bw::pack_bf16(pv[2], pv[3]);
-                p.z = bw::pack_bf16(pv[4], pv[5]); p.w = bw::pack_bf16(pv[6], pv[7]);
-                *reinterpret_cast<uint4*>(sm + L::P + bw::sw128_offset(r, j)) = p;
+                *reinterpret_cast<uint4*>(sm + L::P + bw::sw128_offset(r, j)) = bw::pack8_io<F16>(pv);
             }
         }
     }
@@ -286,15 +288,15 @@ tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
                 float acc = 0.f;
                 for (int d = 0; d < K; ++d) {
                     // OPS: q's tile now holds q's gated copy, so raw q comes from global memory too
-                    const float qi = OPS ? (i < nvalid ? __bfloat162float(q_raw[krow(i) * K + d]) : 0.f)
-                                         : __bfloat162float(*reinterpret_cast<const bf16*>(sm + L::Q + tile_off(i, d)));
+                    const float qi = OPS ? (i < nvalid ? bw::load_io<F16>(q_raw + krow(i) * K + d) : 0.f)
+                                         : bw::load_io<F16>(sm + L::Q + tile_off(i, d));
                     // k's tile now holds its gated copy: raw k and G come from global memory (rare path)
-                    const float kj = j < nvalid ? __bfloat162float(k_raw[krow(j) * K + d]) : 0.f;
+                    const float kj = j < nvalid ? bw::load_io<F16>(k_raw + krow(j) * K + d) : 0.f;
                     const float gi = i < nvalid ? g_cum[row(i) * K + d] : 0.f;
                     const float gj = j < nvalid ? g_cum[row(j) * K + d] : 0.f;
                     acc += qi * kj * __expf(gi - gj);
                 }
-                *reinterpret_cast<bf16*>(sm + L::P + bw::sw128_offset(i, j)) = __float2bfloat16_rn(acc);
+                bw::store_io<F16>(sm + L::P + bw::sw128_offset(i, j), acc);
             }
         }
         __syncthreads();
@@ -324,8 +326,8 @@ tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         const int i = tid + 128 * j, r = i / (K / 8), lc = i % (K / 8);
         const uint32_t off = (uint32_t)((lc >> 3) * 8192 + r * 128 + (((lc & 7) ^ (r & 7)) << 4));
         const uint4 raw = *reinterpret_cast<const uint4*>(sm + L::Q + off);
-        const bf16* qv = reinterpret_cast<const bf16*>(&raw);
         float f[8], gr[8];
+        bw::unpack8_io<F16>(raw, f);
         if constexpr (PER_K) {
             unpack8(gq[j], gr);
         } else {
@@ -333,10 +335,8 @@ tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
             for (int e = 0; e < 8; ++e) gr[e] = sG[r];
         }
 #pragma unroll
-        for (int e = 0; e < 8; ++e) f[e] = __bfloat162float(qv[e]) * __expf(gr[e]);
-        uint4 p;
-        p.x = bw::pack_bf16(f[0], f[1]); p.y = bw::pack_bf16(f[2], f[3]);
-        p.z = bw::pack_bf16(f[4], f[5]); p.w = bw::pack_bf16(f[6], f[7]);
+        for (int e = 0; e < 8; ++e) f[e] *= __expf(gr[e]);
+        const uint4 p = bw::pack8_io<F16>(f);
         const uint4 zero = make_uint4(0, 0, 0, 0);
         if (L::NCH > 1) {
             const bool first = r < C;
@@ -352,7 +352,7 @@ tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
     // MMA 2, 3: D = (q exp(G)) h_c + P v'
     if (tid == 0 && ok) {
         bw::tc_fence_after();
-        constexpr uint32_t idesc = bw::idesc_bf16(64, V, 0, 1);
+        constexpr uint32_t idesc = bw::idesc_io(64, V, 0, 1, F16);
         const uint32_t d_t = tmem + 64;
 #pragma unroll
         for (int ch = 0; ch < L::NCH; ++ch) {
@@ -380,7 +380,10 @@ tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
             bw::tmem_ld_wait();
 #pragma unroll
             for (int e = 0; e < 16; ++e) v16[e] *= scale;
-            if (store) store_bf16x16(orow + c0, v16);
+            if (store) {
+                reinterpret_cast<uint4*>(orow + c0)[0] = bw::pack8_io<F16>(v16);
+                reinterpret_cast<uint4*>(orow + c0)[1] = bw::pack8_io<F16>(v16 + 8);
+            }
         }
     }
     bw::tc_fence_before();
@@ -388,7 +391,7 @@ tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
     if (warp == 0) bw::tmem_dealloc(tmem, L::tmem_cols);
 }
 
-template <int K, int V, int C, bool PER_K>
+template <int K, int V, int C, bool PER_K, bool F16>
 cudaError_t launch_output(const Dims& d, const void* q, const void* k, const void* v_new, const void* h_ckpt,
                           const float* g_cum, void* o, cudaStream_t s, unsigned int* err) {
     using L = OutLayout<K, V, C, PER_K>;
@@ -396,7 +399,7 @@ cudaError_t launch_output(const Dims& d, const void* q, const void* k, const voi
     if (!make_tmap_tokens(&mq, q, d.B, d.T, d.Hk, K, kTile) || !make_tmap_tokens(&mk, k, d.B, d.T, d.Hk, K, kTile) ||
         !make_tmap_tokens(&mvp, v_new, d.B, d.T, d.H, V, kTile) || !make_tmap_ckpt(&mh, h_ckpt, d.B, d.NT, d.H, K, V))
         return cudaErrorInvalidValue;
-    auto kern = tc_output_kernel<K, V, C, PER_K>;
+    auto kern = tc_output_kernel<K, V, C, PER_K, false, F16>;
     const size_t smem = L::bytes + 1024;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -409,8 +412,11 @@ cudaError_t launch_output(const Dims& d, const void* q, const void* k, const voi
 template <int K, int V, int C>
 cudaError_t out_gate(const Dims& d, const void* q, const void* k, const void* v_new, const void* h_ckpt,
                      const float* g_cum, void* o, cudaStream_t s, unsigned int* err) {
-    return d.per_k ? launch_output<K, V, C, true>(d, q, k, v_new, h_ckpt, g_cum, o, s, err)
-                   : launch_output<K, V, C, false>(d, q, k, v_new, h_ckpt, g_cum, o, s, err);
+    if (d.f16)
+        return d.per_k ? launch_output<K, V, C, true, true>(d, q, k, v_new, h_ckpt, g_cum, o, s, err)
+                       : launch_output<K, V, C, false, true>(d, q, k, v_new, h_ckpt, g_cum, o, s, err);
+    return d.per_k ? launch_output<K, V, C, true, false>(d, q, k, v_new, h_ckpt, g_cum, o, s, err)
+                   : launch_output<K, V, C, false, false>(d, q, k, v_new, h_ckpt, g_cum, o, s, err);
 }
 
 template <int K, int V>
@@ -448,7 +454,7 @@ cudaError_t tc_gated_operands(const Dims& d, const void* q, const void* k, const
 
 cudaError_t tc_output(const Dims& d, const void* q, const void* k, const void* v_new, const void* h_ckpt,
                       const float* g_cum, void* o, cudaStream_t s, unsigned int* err) {
-    if (!d.bf16) return cudaErrorInvalidValue;
+    if (!d.bf16 && !d.f16) return cudaErrorInvalidValue;
     if (d.K == 64 && d.V == 64) return out_chunk<64, 64>(d, q, k, v_new, h_ckpt, g_cum, o, s, err);
     if (d.K == 64) return out_chunk<64, 128>(d, q, k, v_new, h_ckpt, g_cum, o, s, err);
     if (d.V == 64) return out_chunk<128, 64>(d, q, k, v_new, h_ckpt, g_cum, o, s, err);

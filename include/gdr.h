@@ -85,9 +85,11 @@ typedef enum gdr_status {
     GDR_ERR_ARG = 9              /* another invalid argument (e.g. a NaN scale) */
 } gdr_status;
 
-/* fp16 io runs FUSED_TC where it is built for fp16 (scalar gate, K = V = 128, chunk 64, no segmented
- * scan: q, k, v, beta, o and every intermediate fp16) and the CUDA-core kernels otherwise (variant
- * AUTO or SIMT); the other tensor-core kernels take bf16. */
+/* fp16 io runs the forward's tensor-core kernels as bf16 does (q, k, v, beta, o and every
+ * intermediate fp16, the state fp32), with three exceptions: FUSED_TC takes a scalar gate only, no
+ * segmented scan runs (segments > 1 is GDR_ERR_UNSUPPORTED), and the backward runs the CUDA-core
+ * kernels.  A per-key-dim gate keeps its gated copies of k and q for the scores in bf16 inside the
+ * kernels, because their factors exceed fp16's range. */
 typedef enum gdr_dtype { GDR_F32 = 0, GDR_BF16 = 1, GDR_F16 = 2 } gdr_dtype;
 
 typedef enum gdr_gate {
@@ -102,20 +104,21 @@ typedef enum gdr_gate {
  * chunks and no segmented scan (one long sequence, which FUSED_TC runs in pieces
  * whose scans overlap the next piece's prepare), else FUSED; with a per-key-dim
  * gate FUSED_TC when K = V = 128, C = 64 and no segmented scan applies; TENSOR for
- * other bf16 problems; SIMT for fp32 io; for fp16 io FUSED_TC where it takes fp16
- * (see gdr_dtype), else SIMT.  The single-stage entry points run their
- * tensor-core kernel for AUTO, TENSOR, FUSED and FUSED_TC on bf16 io. */
+ * other bf16 problems; SIMT for fp32 io.  fp16 io follows the bf16 rules (its
+ * FUSED_TC taking a scalar gate only, see gdr_dtype).  The single-stage entry
+ * points run their tensor-core kernel for AUTO, TENSOR, FUSED and FUSED_TC on
+ * bf16 and fp16 io. */
 typedef enum gdr_variant {
     GDR_VARIANT_AUTO = 0,
     GDR_VARIANT_SIMT = 1,     /* fp32 CUDA-core arithmetic throughout (exact-fp32 path) */
-    GDR_VARIANT_TENSOR = 2,   /* staged kernels on the tensor cores (bf16 io only) */
+    GDR_VARIANT_TENSOR = 2,   /* staged kernels on the tensor cores (bf16 or fp16 io) */
     GDR_VARIANT_FUSED = 3,    /* WY prepare, then scan and output fused, warp-level MMA, one CTA per
-                                 (batch, head, 32 value columns) (bf16 io, scalar gate) */
+                                 (batch, head, 32 value columns) (bf16 or fp16 io, scalar gate) */
     GDR_VARIANT_FUSED_TC = 4  /* the same with scan and output on the tcgen05 tensor cores, one CTA per
                                  (batch, head) (bf16 io, K = V = 128, chunk 64; a per-key-dim gate
                                  adds the gdr_gated_operands kernel; fp16 io with a scalar gate);
                                  packed sequences (gdr_varlen_*) run FUSED for it, TENSOR with a
-                                 per-key-dim gate, SIMT for fp16 */
+                                 per-key-dim gate */
 } gdr_variant;
 
 typedef struct gdr_problem {
@@ -217,16 +220,16 @@ GDR_API gdr_status gdr_chunk_output(const gdr_problem* p, const void* q, const v
                             const void* h_ckpt, const float* g_cum, void* o, void* stream);
 
 /*
- * Stages 2 and 3 fused, for a scalar gate and bf16 io: the state scan of
+ * Stages 2 and 3 fused, for a scalar gate and bf16 or fp16 io: the state scan of
  * gdr_scan_h and the chunk output of gdr_chunk_output in one pass, so v' and the
  * checkpoints never reach device memory.  Per (b, h): h = h0 (zero if NULL); for
  * each chunk c, v'_c = u_c - w_c h, o_c = scale [ (q exp(G)) h + tril_0(Q~) v'_c ],
  * h = exp(G_last) h + (k exp(G_last - G))^T v'_c.
- * Inputs:  q, k, w [B,T,H,K] bf16; u [B,T,H,V] bf16; g_cum [B,T,H] fp32 (the
- *          chunk-local cumsum, as gdr_prepare_wy writes it); P [B,NT,H,C,C] bf16
+ * Inputs:  q, k, w [B,T,H,K] io; u [B,T,H,V] io; g_cum [B,T,H] fp32 (the
+ *          chunk-local cumsum, as gdr_prepare_wy writes it); P [B,NT,H,C,C] io
  *          as gdr_prepare_wyp writes it, or NULL to form it here (C = 64 for a
  *          non-NULL P); h0 [B,H,K,V] fp32 or NULL.
- * Outputs: o [B,T,H,V] bf16; h_final [B,H,K,V] fp32 or NULL (not written).
+ * Outputs: o [B,T,H,V] io; h_final [B,H,K,V] fp32 or NULL (not written).
  * Returns GDR_ERR_UNSUPPORTED for fp32 io.  The kernel is the tcgen05 one for
  * variant FUSED_TC (K = V = 128, C = 64, P required) and for AUTO where
  * gdr_forward's AUTO would take it; the warp-level one otherwise.
@@ -241,8 +244,8 @@ GDR_API gdr_status gdr_scan_output(const gdr_problem* p, const void* q, const vo
  * gdr_prepare_wy plus, per chunk, the gated causal score matrix of the chunk
  * output, P = tril_0(Q~) with Q~_ij = sum_d q_id k_jd exp(G_i - G_j) (no scale),
  * so that gdr_scan_output need not form q k^T once per value slice.
- * Scalar gate, bf16 io and chunk C = 64 only (GDR_ERR_UNSUPPORTED otherwise).
- * Extra input: q [B,T,H,K] bf16.  Extra output: P [B,NT,H,C,C] bf16, row i of
+ * Scalar gate, bf16 or fp16 io and chunk C = 64 only (GDR_ERR_UNSUPPORTED otherwise).
+ * Extra input: q [B,T,H,K] io.  Extra output: P [B,NT,H,C,C] io, row i of
  * chunk c holding the scores of query token c*C+i against key tokens c*C+j.
  */
 GDR_API gdr_status gdr_prepare_wyp(const gdr_problem* p, const void* q, const void* k, const void* v, const float* g,
@@ -325,7 +328,7 @@ GDR_API gdr_status gdr_forward_host(const gdr_problem* p, const void* q, const v
  * The method pages have no counterpart to this call; it is a deployment aid.
  *
  * It runs the staged forward (variant AUTO runs the tensor-core stages for
- * bf16 io and the CUDA-core stages for fp32 and fp16 io, as gdr_forward's AUTO
+ * bf16 and fp16 io and the CUDA-core stages for fp32 io, as gdr_forward's AUTO
  * does with the fused path left out; SIMT and TENSOR are honoured; FUSED and
  * FUSED_TC are not offered here and return GDR_ERR_UNSUPPORTED -- call gdr_forward
  * for them) and
@@ -529,11 +532,11 @@ GDR_API gdr_status gdr_backward(const gdr_problem* p, const void* q, const void*
  * h0, h_final, dh_final, dh0 [n,HV,K,V] fp32 (sequence s starts from h0[s]).
  * The sequences are computed in a working layout in the workspace, the rest of
  * it zero tokens (beta = 0, g = 0, q = k = v = 0: the state passes unchanged and
- * their outputs are dropped).  On the tensor cores (bf16 io) it is chunk-packed:
+ * their outputs are dropped).  On the tensor cores (bf16 or fp16 io) it is chunk-packed:
  * one row of whole chunks, sequence s taking ceil(len_s / C) of them, each run
  * scanned from h0[s]; the work is the real tokens plus fewer than C per
- * sequence.  The fused forward at C = 64 reads q, k, v, g, beta and writes o in
- * place; the other tensor-core paths copy the inputs into the row and the
+ * sequence.  The fused forward at C = 64 with bf16 io reads q, k, v, g, beta and writes o
+ * in place; the other tensor-core paths copy the inputs into the row and the
  * results back.  The CUDA-core paths use padded rows, sequence s as row s of p,
  * through gdr_forward / gdr_backward on p: the work is n * p->T tokens.  A
  * sequence's results never depend on another sequence's tokens, finite or not.

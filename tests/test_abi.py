@@ -228,9 +228,9 @@ def test_fused_tc_variant_takes_its_sizes_only(lib):
 
 
 def test_fp16_fused_tc_rules(lib):
-    # fp16 on the tcgen05 fused path: no segmented scan; AUTO takes it at K = V = 128, C = 64 with a
-    # scalar gate, grouped value heads included (the same workspace as the variant asked by name), and
-    # otherwise the CUDA-core path
+    # fp16 on the tensor-core paths: no segmented scan; AUTO takes the fused forms at K = V = 128, C = 64
+    # with a scalar gate, grouped value heads included (the same workspace as the variant asked by name),
+    # and the staged kernels for a per-key-dim gate
     p = gdr.make_problem(1, 256, 2, 128, 128, 64, 2, False, variant="fused_tc", HV=4)
     assert lib.gdr_forward_workspace_bytes(ctypes.byref(p)) == lib.gdr_forward_workspace_bytes(
         ctypes.byref(gdr.make_problem(1, 256, 2, 128, 128, 64, 2, False, HV=4))) > 0
@@ -243,8 +243,18 @@ def test_fp16_fused_tc_rules(lib):
         assert lib.gdr_forward_workspace_bytes(ctypes.byref(auto)) == lib.gdr_forward_workspace_bytes(
             ctypes.byref(named)) > 0
     auto = gdr.make_problem(2, 320, 2, 128, 128, 64, 2, True)
-    simt = gdr.make_problem(2, 320, 2, 128, 128, 64, 2, True, variant="simt")
-    assert lib.gdr_forward_workspace_bytes(ctypes.byref(auto)) == lib.gdr_forward_workspace_bytes(ctypes.byref(simt))
+    staged = gdr.make_problem(2, 320, 2, 128, 128, 64, 2, True, variant="tensor")
+    assert lib.gdr_forward_workspace_bytes(ctypes.byref(auto)) == lib.gdr_forward_workspace_bytes(
+        ctypes.byref(staged)) > 0
+    # the staged and warp-level variants take fp16 at every shape; the warp-level one a scalar gate only
+    for (K, V, C, per_k, variant, ok) in [(64, 64, 32, False, "tensor", True), (64, 128, 64, True, "tensor", True),
+                                          (128, 64, 64, False, "fused", True), (64, 64, 32, False, "fused", True),
+                                          (64, 64, 64, True, "fused", False)]:
+        p = gdr.make_problem(1, 256, 2, K, V, C, 2, per_k, variant=variant)
+        if ok:
+            assert lib.gdr_forward_workspace_bytes(ctypes.byref(p)) > 0
+        else:
+            assert lib.gdr_forward_workspace_bytes(ctypes.byref(p)) == 0 and _fwd(lib, p) == 8
 
 
 def test_segment_choice_and_workspace(lib):

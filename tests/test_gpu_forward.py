@@ -16,15 +16,15 @@ from gpu_helpers import (H_TOL, O_TOL, all_pairs, check_forward, gather_heads, g
 pytestmark = pytest.mark.gpu
 
 # every variant gdr_forward offers, with the io dtypes it takes
-FORWARD_VARIANTS = {"simt": (torch.float32, torch.bfloat16), "tensor": (torch.bfloat16,),
-                    "fused": (torch.bfloat16,), "fused_tc": (torch.bfloat16, torch.float16)}
+FORWARD_VARIANTS = {"simt": (torch.float32, torch.bfloat16), "tensor": (torch.bfloat16, torch.float16),
+                    "fused": (torch.bfloat16, torch.float16), "fused_tc": (torch.bfloat16, torch.float16)}
 # the warp-level fused path takes a scalar gate only
 GATES = {"simt": (False, True), "tensor": (False, True), "fused": (False,), "fused_tc": (False, True)}
 
 
 def gates(variant, dtype):
     # fp16 on the tcgen05 fused path: scalar gate only
-    return (False,) if dtype == torch.float16 else GATES[variant]
+    return (False,) if dtype == torch.float16 and variant == "fused_tc" else GATES[variant]
 SHAPES = [(2, 256, 3, 64, 64, 64), (1, 192, 2, 128, 128, 64), (2, 128, 3, 64, 128, 32),
           (1, 160, 1, 128, 64, 32), (1, 64, 2, 128, 128, 64), (1, 32, 1, 64, 64, 32),
           # a last, partial chunk: 36 of 64 tokens; 13 of 32 (the second half of a 64-token
@@ -245,9 +245,9 @@ def test_host_forward_fp16_on_the_tcgen05_path():
     # and the pieces carry the state exactly as one device call does
     x = make_inputs(1, 64 * 40 + 17, 3, 128, 128, io_dtype=torch.float16, with_h0=True, seed=95)
     hx = [t.pin_memory() for t in (x.q, x.k, x.v, x.g, x.beta, x.h0)]
-    o, hf = gdr.forward(*hx, chunk=64, pieces=4)
+    o, hf = gdr.forward(*hx, chunk=64, variant="fused_tc", pieces=4)
     assert o.dtype == torch.float16 and gdr.gdr_last_variant() == "fused_tc"
-    o_1, hf_1 = gdr.forward(*(t.cuda() for t in hx), chunk=64)
+    o_1, hf_1 = gdr.forward(*(t.cuda() for t in hx), chunk=64, variant="fused_tc")
     assert torch.equal(o, o_1.cpu()) and torch.equal(hf, hf_1.cpu())
     check_forward(x, o, hf, all_pairs(1, 3), 64, 1.0 / np.sqrt(128), "f16")
 
@@ -368,13 +368,14 @@ def test_grouped_value_heads_forward(shape, variant, dtype, per_k):
 @pytest.mark.parametrize("per_k", [False, True])
 @pytest.mark.parametrize("variant", ["auto", "simt"])
 def test_fp16_io_forward(shape, per_k, variant):
-    # AUTO runs fp16 on the tcgen05 fused path where it takes it (scalar gate, K = V = 128, C = 64), on
-    # the CUDA-core kernels otherwise
+    # AUTO picks for fp16 as for bf16: at these sizes the warp-level fused kernel for a scalar gate and
+    # 64-token chunks, the staged tensor-core kernels otherwise (the tcgen05 form takes no per-key-dim
+    # gate in fp16)
     B, T, H, K, V, C = shape
     x = make_inputs(B, T, H, K, V, per_k_gate=per_k, io_dtype=torch.float16, with_h0=True, seed=90)
     o, hf, ran = gpu_forward(x, C, variant)
-    tc = variant == "auto" and not per_k and K == V == 128 and C == 64
-    assert ran == ("fused_tc" if tc else "simt") and o.dtype == torch.float16
+    want = "simt" if variant == "simt" else ("fused" if not per_k and C == 64 else "tensor")
+    assert ran == want and o.dtype == torch.float16
     check_forward(x, o, hf, all_pairs(B, H), C, 1.0 / np.sqrt(K), "f16")
 
 
@@ -393,22 +394,24 @@ def test_fp16_io_overlapped_single_sequence(T, H):
     assert rel_frob(hf, hf2[:1].double().cpu().numpy()) <= 2e-3
 
 
-def test_fp16_io_tensor_core_forward_is_closer_to_the_oracle_than_bf16():
+@pytest.mark.parametrize("variant", ["fused_tc", "fused", "tensor"])
+def test_fp16_io_tensor_core_forward_is_closer_to_the_oracle_than_bf16(variant):
     # the same draw rounded to fp16 and to bf16: the fp16 run keeps three more mantissa bits in every
     # stored operand (w, u, P, h, v'), so its error against the oracle of its own inputs is smaller
     errs = {}
     for dt in (torch.float16, torch.bfloat16):
         x = make_inputs(2, 320, 2, 128, 128, io_dtype=dt, with_h0=True, seed=93)
-        o, hf, ran = gpu_forward(x, 64, "fused_tc")
-        assert ran == "fused_tc"
+        o, hf, ran = gpu_forward(x, 64, variant)
+        assert ran == variant
         errs[dt] = check_forward(x, o, hf, all_pairs(2, 2), 64, 1.0 / np.sqrt(128), io_name(dt))
     assert errs[torch.float16][0] < errs[torch.bfloat16][0] and errs[torch.float16][1] < errs[torch.bfloat16][1]
 
 
-@pytest.mark.parametrize("variant", ["tensor", "fused", "fused_tc"])
-def test_fp16_io_refused_by_the_tensor_core_variants(variant):
-    # K = V = 64 everywhere; the staged and warp-level tensor-core variants take no fp16 at all
-    x = make_inputs(1, 64, 1, 64, 64, io_dtype=torch.float16, seed=91)
+@pytest.mark.parametrize("variant,per_k", [("fused_tc", False), ("fused", True)])
+def test_fp16_io_refused_where_no_kernel_takes_it(variant, per_k):
+    # the tcgen05 fused form at K = V = 64, the warp-level one with a per-key-dim gate: refused before a
+    # launch, in fp16 as in bf16
+    x = make_inputs(1, 64, 1, 64, 64, per_k_gate=per_k, io_dtype=torch.float16, seed=91)
     with pytest.raises(gdr.GdrError) as e:
         gpu_forward(x, 64, variant)
     assert e.value.status == 8
@@ -423,8 +426,10 @@ def test_fp16_io_fused_tc_refuses_what_it_does_not_build(case):
     with pytest.raises(gdr.GdrError) as e:
         gpu_forward(x, 64, "fused_tc", segments=seg)
     assert e.value.status == 8
-    o, hf, ran = gpu_forward(x, 64, "auto", segments=1 if case == "segments" else 0)   # AUTO still runs it
-    assert ran == ("fused_tc" if case == "segments" else "simt")
+    # AUTO runs the problem on the tensor cores all the same: the warp-level fused kernel for the short
+    # single sequence (as for bf16), the staged kernels for the per-key-dim gate
+    o, hf, ran = gpu_forward(x, 64, "auto", segments=1 if case == "segments" else 0)
+    assert ran == ("fused" if case == "segments" else "tensor")
 
 
 @pytest.mark.parametrize("shape", [(2, 256, 2, 128, 128, 64), (1, 200, 3, 64, 64, 32)],

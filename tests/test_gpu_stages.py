@@ -20,10 +20,11 @@ SHAPES = [(2, 256, 3, 64, 64, 64), (1, 192, 2, 128, 128, 64), (2, 128, 3, 64, 12
           (2, 100, 3, 64, 64, 64), (1, 77, 2, 128, 128, 32), (1, 20, 1, 128, 64, 64)]
 # per stage: the variants that run it, with the io dtypes each one takes
 BOTH = (torch.float32, torch.bfloat16)
+IO16 = (torch.bfloat16, torch.float16)
 STAGE_VARIANTS = {
-    "prepare": {"simt": BOTH, "tensor": (torch.bfloat16,)},
-    "scan": {"simt": BOTH, "tensor": (torch.bfloat16,)},
-    "output": {"simt": BOTH, "tensor": (torch.bfloat16,)},
+    "prepare": {"simt": BOTH, "tensor": IO16},
+    "scan": {"simt": BOTH, "tensor": IO16},
+    "output": {"simt": BOTH, "tensor": IO16},
 }
 
 
@@ -142,11 +143,11 @@ SCAN_OUTPUT_SHAPES = [(2, 256, 3, 64, 64, 64), (1, 192, 2, 128, 128, 64), (2, 12
 
 @pytest.mark.parametrize("shape", SCAN_OUTPUT_SHAPES, ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("with_h0", [False, True])
-def test_scan_output_stage(shape, with_h0):
+@pytest.mark.parametrize("dtype", IO16, ids=io_name)
+def test_scan_output_stage(shape, with_h0, dtype):
     """Scan and output fused: o and h_final against the chunked oracle's scan and
     output stages fed the same rounded w, u, G."""
     B, T, H, K, V, C = shape
-    dtype = torch.bfloat16
     x = make_inputs(B, T, H, K, V, io_dtype=dtype, with_h0=with_h0, seed=14)
     pre = chunked.prepare_wy(x.k, x.v, x.g, x.beta, C)
     w_r, u_r, G_r = rounded(pre["w"], dtype), rounded(pre["u"], dtype), rounded(pre["G"], torch.float32)
@@ -158,9 +159,9 @@ def test_scan_output_stage(shape, with_h0):
     hf = torch.full((B, H, K, V), float("nan"), device="cuda", dtype=torch.float32)
     gdr.gdr_scan_output(p, dev(x.q), dev(x.k), dev(w_r), dev(u_r), dev(G_r), None, dev(h0), o, hf)
     torch.cuda.synchronize()
-    assert gdr.gdr_last_variant() == "fused"
-    assert scaled_err(o, o_ref) <= STAGE_TOL["bf16"]
-    assert rel_frob(hf, scan["h_final"]) <= STAGE_TOL["bf16"]
+    assert gdr.gdr_last_variant() == "fused" and o.dtype == dtype
+    assert scaled_err(o, o_ref) <= STAGE_TOL[io_name(dtype)]
+    assert rel_frob(hf, scan["h_final"]) <= STAGE_TOL[io_name(dtype)]
 
 
 @pytest.mark.parametrize("shape", [(2, 256, 3, 128, 128, 64), (1, 100, 2, 128, 128, 64), (1, 64, 1, 128, 128, 64)],
@@ -277,11 +278,11 @@ def test_scan_output_refuses_per_key_gate_and_fp32():
 @pytest.mark.parametrize("shape", [(2, 256, 3, 64, 64, 64), (1, 192, 2, 128, 128, 64), (1, 320, 1, 128, 64, 64),
                                    (2, 100, 2, 128, 128, 64), (2, 20, 1, 64, 64, 64)],
                          ids=lambda s: "x".join(map(str, s)))
-def test_prepare_with_scores_then_scan_output(shape):
+@pytest.mark.parametrize("dtype", IO16, ids=io_name)
+def test_prepare_with_scores_then_scan_output(shape, dtype):
     """gdr_prepare_wyp's P against the oracle's gated causal scores, then
     gdr_scan_output reading that P against the oracle's scan and output."""
     B, T, H, K, V, C = shape
-    dtype = torch.bfloat16
     x = make_inputs(B, T, H, K, V, io_dtype=dtype, with_h0=True, seed=15)
     p = gdr.problem_for(x.q, x.v, x.g, C, scale=0.125)
     q, k, v, g, beta = (dev(t) for t in (x.q, x.k, x.v, x.g, x.beta))
@@ -293,10 +294,10 @@ def test_prepare_with_scores_then_scan_output(shape):
     gdr.gdr_prepare_wyp(p, q, k, v, g, beta, w, u, g_cum, P)
     torch.cuda.synchronize()
     pre = chunked.prepare_wy(x.k, x.v, x.g, x.beta, C)
-    assert scaled_err(w, pre["w"]) <= STAGE_TOL["bf16"]
-    assert scaled_err(u, pre["u"]) <= STAGE_TOL["bf16"]
+    assert scaled_err(w, pre["w"]) <= STAGE_TOL[io_name(dtype)]
+    assert scaled_err(u, pre["u"]) <= STAGE_TOL[io_name(dtype)]
     assert scaled_err(g_cum, pre["G"]) <= 1e-6
-    assert scaled_err(P, chunked.gated_causal_scores(x.q, x.k, pre["G"], C)) <= STAGE_TOL["bf16"]
+    assert scaled_err(P, chunked.gated_causal_scores(x.q, x.k, pre["G"], C)) <= STAGE_TOL[io_name(dtype)]
     o = torch.full((B, T, H, V), float("nan"), device="cuda", dtype=dtype)
     hf = torch.full((B, H, K, V), float("nan"), device="cuda", dtype=torch.float32)
     gdr.gdr_scan_output(p, q, k, w, u, g_cum, P, dev(x.h0), o, hf)
@@ -309,5 +310,5 @@ def test_prepare_with_scores_then_scan_output(shape):
     vc = chunked._to_chunks(chunked._pad_tokens(scan["v_new"], C), C)
     Gc = chunked._gate_vec(chunked._pad_tokens(chunked._f64(G_r), C, edge=True), C)
     o_ref = chunked._from_chunks(0.125 * ((qc * np.exp(Gc)) @ scan["ckpt"] + chunked._f64(P_r) @ vc))[:, :T]
-    assert scaled_err(o, o_ref) <= STAGE_TOL["bf16"]
-    assert rel_frob(hf, scan["h_final"]) <= STAGE_TOL["bf16"]
+    assert scaled_err(o, o_ref) <= STAGE_TOL[io_name(dtype)]
+    assert rel_frob(hf, scan["h_final"]) <= STAGE_TOL[io_name(dtype)]

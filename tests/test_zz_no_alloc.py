@@ -12,8 +12,8 @@ The checks, per case:
   kernels are deterministic, so any difference is a stale-scratch read), and
   each meets the workloads' bars against the float64 oracle;
 - the cases cover both staged variants AUTO resolves to (the tensor-core stages
-  for bf16, the CUDA-core stages for fp32), both gates, C = 32 and 64, and the
-  segment-parallel scan, whose maps and starts also live in the array.
+  for bf16 and fp16, the CUDA-core stages for fp32), both gates, C = 32 and 64,
+  and the segment-parallel scan, whose maps and starts also live in the array.
 A problem too large for the array is refused before anything runs.  This file
 is named to be collected last.
 """
@@ -34,6 +34,8 @@ CASES = [  # (B, T, H, K, V, C, per-key-dim gate, io dtype, segments, variant AU
     (1, 192, 2, 128, 64, 32, False, torch.bfloat16, 0, "tensor"),
     (1, 192, 2, 128, 128, 64, True, torch.bfloat16, 0, "tensor"),
     (1, 2048, 2, 64, 64, 64, False, torch.bfloat16, 4, "tensor"),
+    (1, 192, 2, 64, 128, 32, True, torch.float16, 0, "tensor"),
+    (2, 256, 2, 128, 128, 64, False, torch.float16, 0, "tensor"),
 ]
 
 # run through the shared array before each case, so the case reads over another problem's leftovers

@@ -40,7 +40,6 @@ constexpr float kExpSafe = 40.f;
 template <int K, int V, int C, bool PER_K, bool OPS = false>
 struct OutLayout {
     static constexpr int NCH = kTile / C;                          // chunks per tile
-    static constexpr int GW = PER_K ? K : 1;
     // With a per-key-dim gate the gate is read from global memory (L2) where needed instead of
     // being staged (32 KB), k's gated copy is written over k, and P over that once S is formed:
     // two CTAs per SM.  OPS keeps no v' and no checkpoints, writes q's gated copy over q and sends qg
@@ -54,7 +53,6 @@ struct OutLayout {
     static constexpr uint32_t Qa = OPS ? Q : Q1 + (NCH > 1 ? K * 128 : 0);   // per-key-dim gate: q exp(G - Gref)
     static constexpr uint32_t F = OPS ? Q1 : Qa + (PER_K ? K * 128 : 0);     // fp32: G [64] (scalar gate), flag
     static constexpr uint32_t bytes = F + 4 * ((PER_K ? 0 : kTile) + 4);
-    static constexpr uint32_t tx = 2 * K * 128 + V * 128 + NCH * K * V * 2;
     static constexpr uint32_t tmem_cols = OPS ? 64 : 256;          // S at 0 (64 cols), D at 64 (V cols)
 };
 
@@ -71,7 +69,6 @@ tc_output_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
     static_assert(!OPS || (PER_K && C == 64 && K == V), "gated operands: per-key-dim gate, one chunk per tile");
     static_assert(!(OPS && F16), "gated operands: bf16 io");
     using L = OutLayout<K, V, C, PER_K, OPS>;
-    constexpr int GW = L::GW;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float* sG = reinterpret_cast<float*>(sm + L::F);

@@ -257,6 +257,36 @@ def test_fp16_fused_tc_rules(lib):
             assert lib.gdr_forward_workspace_bytes(ctypes.byref(p)) == 0 and _fwd(lib, p) == 8
 
 
+def test_fp16_plans_like_bf16(lib):
+    # fp16 runs the forward kernels bf16 runs, so every variant plans the same scratch for both, batched
+    # and packed, wherever no segmented scan applies; the exceptions are the tcgen05 form with a
+    # per-key-dim gate (fp16 refused; AUTO runs the staged kernels there instead, as TENSOR does for
+    # bf16) and the segments AUTO picks for bf16 only
+    fwd = lambda p: lib.gdr_forward_workspace_bytes(ctypes.byref(p))
+    packed = lambda p: lib.gdr_varlen_forward_workspace_bytes(ctypes.byref(p))
+    for (B, T, H, K, V, C) in [(4, 320, 16, 128, 128, 64), (4, 300, 16, 64, 64, 32), (4, 200, 16, 128, 64, 64),
+                               (4, 256, 16, 64, 128, 32), (1, 64 * 140, 40, 128, 128, 64)]:
+        for per_k in (False, True):
+            for variant in ("auto", "simt", "tensor", "fused", "fused_tc"):
+                b = gdr.make_problem(B, T, H, K, V, C, 1, per_k, variant=variant)
+                f = gdr.make_problem(B, T, H, K, V, C, 2, per_k, variant=variant)
+                if variant == "fused_tc" and per_k:
+                    assert fwd(f) == 0 and (fwd(b) > 0) == (K == V == 128 and C == 64)
+                    continue
+                if fwd(b) == 0:   # a variant that takes neither (the shape, or a per-key-dim gate)
+                    assert fwd(f) == 0 and packed(f) == packed(b) == 0
+                    continue
+                assert lib.gdr_forward_segments(ctypes.byref(b)) == 1   # no segments: the plans compare
+                assert packed(f) == packed(b), (B, T, H, K, V, C, per_k, variant)
+                if variant == "auto" and per_k and K == V == 128 and C == 64:
+                    b = gdr.make_problem(B, T, H, K, V, C, 1, per_k, variant="tensor")
+                assert fwd(f) == fwd(b), (B, T, H, K, V, C, per_k, variant)
+    # where AUTO segments a bf16 scan, fp16 scans whole
+    b = gdr.make_problem(1, 32768, 4, 128, 128, 64, 1, False)
+    f = gdr.make_problem(1, 32768, 4, 128, 128, 64, 2, False)
+    assert lib.gdr_forward_segments(ctypes.byref(b)) == 8 and lib.gdr_forward_segments(ctypes.byref(f)) == 1
+
+
 def test_segment_choice_and_workspace(lib):
     # automatic segments: only when the serial scan's B H V/32 CTAs fill at most half of 152 SMs; the
     # largest divisor S of NT with S B H V/32 <= 152 and NT / S >= 16

@@ -48,20 +48,5 @@ __device__ __forceinline__ uint64_t desc_mnmajor_r(uint32_t tile, int kk, int ro
     return bw::sdesc_sw128(tile + (uint32_t)(kk * 2048), (uint32_t)(rows * 128), 1024);
 }
 
-// Stores n (multiple of 16) fp32 values as bf16 to 16-byte aligned global memory.
-__device__ __forceinline__ void store_bf16x16(__nv_bfloat16* dst, const float* v) {
-    uint4 a, b;
-    a.x = bw::pack_bf16(v[0], v[1]);
-    a.y = bw::pack_bf16(v[2], v[3]);
-    a.z = bw::pack_bf16(v[4], v[5]);
-    a.w = bw::pack_bf16(v[6], v[7]);
-    b.x = bw::pack_bf16(v[8], v[9]);
-    b.y = bw::pack_bf16(v[10], v[11]);
-    b.z = bw::pack_bf16(v[12], v[13]);
-    b.w = bw::pack_bf16(v[14], v[15]);
-    reinterpret_cast<uint4*>(dst)[0] = a;
-    reinterpret_cast<uint4*>(dst)[1] = b;
-}
-
 }  // namespace tc
 }  // namespace gdr
